@@ -1,0 +1,122 @@
+"""Pins for the allocator model (the oracle of the host block allocator).
+
+SplitMix64 is pinned to its published reference outputs; the rest is pinned by
+invariants that any correct ref-counted block pool satisfies, checked after
+every step of long random operation sequences.
+"""
+import random
+
+import pytest
+
+from oracle.alloc_model import BlockAllocatorModel, OutOfBlocks, SplitMix64
+
+
+def test_splitmix64_reference_outputs():
+    # reference sequence for seed 1234567 (as published with the algorithm's
+    # public-domain C reference and Java's SplittableRandom tests)
+    r = SplitMix64(1234567)
+    assert [r.next() for _ in range(3)] == [6457827717110365317, 3203168211198807973,
+                                            9817491932198370423]
+    r0 = SplitMix64(0)
+    assert r0.next() == 0xE220A8397B1DCDAF
+
+
+def test_initial_free_list_is_a_seeded_permutation():
+    a = BlockAllocatorModel(1000, 16, seed=3)
+    b = BlockAllocatorModel(1000, 16, seed=3)
+    c = BlockAllocatorModel(1000, 16, seed=4)
+    assert sorted(a.free) == list(range(1000))
+    assert a.free == b.free and a.free != c.free
+    assert a.free != list(range(1000))
+
+
+def check_invariants(m: BlockAllocatorModel):
+    counts = [0] * m.num_blocks
+    for s in m.seqs.values():
+        assert len(s["blocks"]) == -(-s["len"] // m.block_size)
+        for blk in s["blocks"]:
+            counts[blk] += 1
+    # every reference held by a live sequence is counted exactly once
+    assert counts == m.ref
+    live = {i for i in range(m.num_blocks) if m.ref[i] > 0}
+    free, pend = set(m.free), set(m.pending)
+    assert len(free) == len(m.free) and len(pend) == len(m.pending)
+    # free, pending and live blocks partition the pool
+    assert not (free & pend) and not (free & live) and not (pend & live)
+    assert free | pend | live == set(range(m.num_blocks))
+
+
+def test_random_operation_sequences_keep_invariants():
+    rnd = random.Random(42)
+    for trial in range(20):
+        bs = rnd.choice([1, 4, 16, 32])
+        m = BlockAllocatorModel(rnd.randint(0, 120), bs, seed=trial)
+        for _ in range(400):
+            op = rnd.random()
+            sids = list(m.seqs)
+            snapshot = (list(m.free), list(m.pending), list(m.ref),
+                        {k: (list(v["blocks"]), v["len"]) for k, v in m.seqs.items()})
+            try:
+                if op < 0.3 or not sids:
+                    n = rnd.randint(0, 5 * bs)
+                    before = m.num_free()
+                    sid = m.add(n)
+                    assert m.num_free() == before - (-(-n // bs))
+                    assert all(m.refcount(b) == 1 for b in m.table(sid))
+                elif op < 0.45:
+                    src = rnd.choice(sids)
+                    sid = m.fork(src)
+                    assert m.table(sid) == m.table(src)
+                elif op < 0.75:
+                    sid = rnd.choice(sids)
+                    old_tab, old_len = m.table(sid), m.seq_len(sid)
+                    shared_last = bool(old_tab) and m.refcount(old_tab[-1]) > 1
+                    n = rnd.randint(0, 3 * bs)
+                    src, dst = m.append(sid, n)
+                    new_tab = m.table(sid)
+                    if n > 0 and old_len % bs != 0 and shared_last:
+                        assert src == old_tab[-1] and dst == new_tab[len(old_tab) - 1]
+                        assert new_tab[:len(old_tab) - 1] == old_tab[:-1]
+                    else:
+                        assert (src, dst) == (-1, -1)
+                        assert new_tab[:len(old_tab)] == old_tab
+                elif op < 0.95:
+                    m.free_seq(rnd.choice(sids))
+                else:
+                    m.reclaim()
+                    assert m.num_pending() == 0
+            except OutOfBlocks:
+                # rejected operations leave the state unchanged
+                assert snapshot == (list(m.free), list(m.pending), list(m.ref),
+                                    {k: (list(v["blocks"]), v["len"])
+                                     for k, v in m.seqs.items()})
+            check_invariants(m)
+
+
+def test_exhaustion_rejects_and_deferred_reclaim():
+    m = BlockAllocatorModel(4, 16, seed=1)
+    a = m.add(64)
+    with pytest.raises(OutOfBlocks):
+        m.add(1)
+    m.free_seq(a)
+    assert m.num_free() == 0 and m.num_pending() == 4
+    with pytest.raises(OutOfBlocks):
+        m.add(1)       # freed blocks are not reusable before reclaim
+    assert m.reclaim() == 4
+    b = m.add(17)
+    assert len(m.table(b)) == 2
+
+
+def test_shared_prefix_fork_and_copy_on_write():
+    m = BlockAllocatorModel(64, 16, seed=2)
+    p = m.add(40)                    # 3 blocks, last one partial
+    forks = [m.fork(p) for _ in range(5)]
+    assert all(m.refcount(b) == 6 for b in m.table(p))
+    src, dst = m.append(forks[0], 1)
+    assert src == m.table(p)[-1] and m.refcount(src) == 5 and m.refcount(dst) == 1
+    assert m.table(forks[0])[:2] == m.table(p)[:2]
+    # a full last block needs no copy
+    q = m.add(32)
+    f = m.fork(q)
+    assert m.append(f, 5) == (-1, -1)
+    assert m.table(f)[:2] == m.table(q)

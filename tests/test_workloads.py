@@ -1,0 +1,98 @@
+"""Structure of the seeded workloads: layouts, sharing, poisoning, determinism."""
+import numpy as np
+import torch
+
+from workloads import CONFIGS, generate
+from workloads.configs import Spec
+from workloads.gen import draw_seq_lens
+
+
+def _small_prefix_window_spec(**kw):
+    base = dict(name="pw_small", batch=6, num_q_heads=4, num_kv_heads=2, head_dim=16,
+                block_size=16, dtype="bf16", window=40, shared_prefix=32,
+                len_dist=("uniform", 1, 90), seed=77)
+    base.update(kw)
+    return Spec(**base)
+
+
+def test_named_configs_match_their_descriptions():
+    c = CONFIGS
+    assert (c["tiny"].batch, c["tiny"].num_q_heads, c["tiny"].num_kv_heads, c["tiny"].head_dim,
+            c["tiny"].block_size, c["tiny"].dtype, c["tiny"].pool_blocks) == \
+        (4, 8, 2, 64, 16, "f16", 64)
+    assert c["tiny"].softmax_scale == 1 / 8
+    assert (c["llama8b"].batch, c["llama8b"].group, c["llama8b"].head_dim) == (64, 4, 128)
+    assert (c["long_skew"].batch, c["long_skew"].group, c["long_skew"].block_size) == (8, 8, 32)
+    assert c["prefix_window"].window == 4096 and c["prefix_window"].shared_prefix == 2048
+    assert c["fp8"].kv_fp8 and c["fp8"].batch == 256
+    seeds = [s.seed for s in c.values()]
+    assert seeds == [267001, 267002, 267003, 267004, 267005]
+
+
+def test_length_distributions():
+    rng = np.random.default_rng(0)
+    L = draw_seq_lens(CONFIGS["long_skew"], rng)
+    assert L[0] == 131072 and ((L[1:] >= 256) & (L[1:] <= 2048)).all()
+    L = draw_seq_lens(CONFIGS["fp8"], np.random.default_rng(1))
+    assert ((L >= 1024) & (L <= 8192)).all() and 2500 < L.mean() < 4500
+    L = draw_seq_lens(CONFIGS["prefix_window"], np.random.default_rng(2))
+    assert ((L >= 2048 + 128) & (L <= 2048 + 30000)).all()
+
+
+def test_tiny_layout_and_poison():
+    w = generate(CONFIGS["tiny"])
+    assert w.num_blocks == 64 and w.max_blocks == 13
+    used = w.block_tables[w.block_tables >= 0]
+    assert len(np.unique(used)) == len(used)                # private blocks only
+    for b, L in enumerate(w.seq_lens):
+        n = -(-int(L) // 16)
+        assert (w.block_tables[b, :n] >= 0).all() and (w.block_tables[b, n:] == -1).all()
+    kc = w.key_cache
+    for b, L in enumerate(w.seq_lens):
+        L = int(L)
+        for p in range(L):
+            row = kc[w.block_tables[b, p // 16], :, p % 16, :]
+            assert torch.isnan(row).all() == (p == L - 1)    # new token not written yet
+        last = w.block_tables[b, (L - 1) // 16]
+        assert torch.isnan(kc[last, :, (L - 1) % 16 + 1:, :]).all()  # tail of the last block
+    unused = np.setdiff1d(np.arange(64), used)
+    assert torch.isnan(kc[torch.as_tensor(unused)]).all()
+
+
+def test_shared_prefix_and_window_poison():
+    s = _small_prefix_window_spec()
+    w = generate(s)
+    t = w.block_tables
+    assert (t[:, :2] == t[0, :2]).all()                      # prefix blocks shared by all
+    priv = t[:, 2:][t[:, 2:] >= 0]
+    assert len(np.unique(priv)) == len(priv)
+    kc = w.key_cache
+    starts = np.maximum(0, w.seq_lens.astype(np.int64) - 40)
+    for b, L in enumerate(w.seq_lens):
+        for p in range(int(L)):
+            row = kc[t[b, p // 16], :, p % 16, :]
+            read_by_someone = any(
+                starts[c] <= p < w.seq_lens[c] and (p < 32 or c == b) for c in range(s.batch))
+            want_nan = (not read_by_someone) or p == L - 1
+            assert bool(torch.isnan(row).all()) == want_nan, (b, p)
+
+
+def test_generation_is_deterministic_and_seeded():
+    s = _small_prefix_window_spec()
+    a, b = generate(s), generate(s)
+    c = generate(s.with_(seed=78))
+    assert np.array_equal(a.block_tables, b.block_tables)
+    assert torch.equal(a.q, b.q) and torch.equal(a.k_new, b.k_new)
+    assert not np.array_equal(a.block_tables, c.block_tables) or not torch.equal(a.q, c.q)
+
+
+def test_fp8_workload_scales_and_history():
+    s = _small_prefix_window_spec(kv_fp8=True, window=0)
+    w = generate(s)
+    assert w.key_cache is None and w.k_hist is not None
+    assert w.k_hist.shape[0] == w.slot_hist.shape[0]
+    assert len(torch.unique(w.slot_hist)) == w.slot_hist.shape[0]
+    allk = torch.cat([w.k_hist, w.k_new]).float()
+    assert w.k_scale == float(allk.abs().amax() / 448.0)
+    kc, vc = w.empty_fp8_cache()
+    assert kc.dtype == torch.uint8 and (kc == 0x7F).all()
