@@ -1,0 +1,486 @@
+"""Benchmark of one paged decode step on GB300 (driver contract: one JSON line).
+
+A step is the whole hot path over one batch: pa_reshape_and_cache of the new
+token of every sequence, then pa_decode (decode kernel + merge kernel), on
+the Llama-3-8B-shaped workload (batch 64, 32 q / 8 kv heads, head_dim 128,
+block_size 16, bf16, seq_lens uniform [512, 4096], shuffled blocks).
+
+value  : algorithmic HBM GB/s of the step (bytes the step must move / device
+         time per step), whole job (all ranks' bytes / slowest rank's time).
+e2e    : the same metric through the public API with host buffers: per step
+         the H2D copy of q, k/v of the new tokens, slots, block tables and
+         seq_lens from pinned memory, the step, and the D2H copy of the output.
+roofline: the decode kernel alone (CUDA events around it on its stream).
+cpu_baseline: the fp64 C oracle on this host's cores.
+
+--impl reference times the oracle (the CPU reference of this build) on a
+bounded sample of the same workload with the same metric.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from workloads import generate, get_config  # noqa: E402
+
+METRIC = "paged decode attention: μs/step, achieved HBM GB/s and % of GB300 peak"
+UNIT = "GB/s"
+
+
+# ----------------------------------------------------------- byte models
+
+def decode_bytes(w) -> dict:
+    """Algorithmic bytes of one pa_decode: every attended K/V row once, q,
+    out, the block-table entries of the touched blocks and seq_lens."""
+    s = w.spec
+    L = w.seq_lens.astype(np.int64)
+    st = w.starts.astype(np.int64)
+    n = L - st
+    elt = 1 if s.kv_fp8 else 2
+    kv = int(n.sum()) * s.num_kv_heads * 2 * s.head_dim * elt
+    blocks = np.where(L > 0, -(-L // s.block_size) - st // s.block_size, 0)
+    q = s.batch * s.num_q_heads * s.head_dim * 2
+    tables = 4 * int(blocks.sum()) + 4 * s.batch
+    return {"kv": kv, "q": q, "out": q, "tables": tables,
+            "kernel": kv + q + tables, "total": kv + 2 * q + tables,
+            "tokens": int(n.sum())}
+
+
+def reshape_bytes(w) -> int:
+    s = w.spec
+    T = int((w.slot_new >= 0).sum().item())
+    elt = 1 if s.kv_fp8 else 2
+    per_row = s.num_kv_heads * s.head_dim
+    return T * per_row * 2 * 2 + T * per_row * elt * 2 + 8 * w.slot_new.numel()
+
+
+# ----------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.lines: list[str] = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, ValueError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------- helpers
+
+def measured_peak() -> tuple[float, str]:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in ("decode.cuh", "ptx.cuh"):
+        with open(os.path.join(ROOT, "paged_kv_cache_267_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(config: str, decode_launch_bytes: float):
+    """dram bytes per launch of the decode kernel from the committed ncu
+    summary, if it was taken on the current kernel source."""
+    p = os.path.join(ROOT, "profiles", f"decode_{config}_traffic.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if d.get("kernel_hash") != kernel_source_hash():
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+def dist_setup(n_gpus: int):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64,
+                     device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64,
+                     device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def rank_spec(config: str, rank: int):
+    """Each rank decodes its own batch (weak scaling): same shape, own seed."""
+    s = get_config(config)
+    return s.with_(seed=s.seed + 1000 * rank) if rank else s
+
+
+# ----------------------------------------------------------- oracle timing
+
+def oracle_baseline(w, kc_host, vc_host, budget_s: float, seq_subset=None) -> dict:
+    import oracle
+    s = w.spec
+    B = s.batch
+    seqs = list(range(B)) if seq_subset is None else list(seq_subset)
+    pairs = np.array([(b, h) for b in seqs for h in range(s.num_q_heads)], np.int32)
+    sel = np.zeros(B, bool)
+    sel[seqs] = True
+    L = w.seq_lens.astype(np.int64)
+    n = (L - w.starts)[sel]
+    elt = 1 if s.kv_fp8 else 2
+    bytes_ = int(n.sum()) * s.num_kv_heads * 2 * s.head_dim * elt + 2 * len(pairs) * s.head_dim * 2
+    threads = oracle.default_threads()
+    qh = w.q.cpu()
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        oracle.decode(qh, kc_host, vc_host, w.block_tables, w.seq_lens,
+                      num_kv_heads=s.num_kv_heads, scale=s.softmax_scale,
+                      block_size=s.block_size, window=s.window, q_dtype=s.dtype,
+                      cache_dtype="fp8" if s.kv_fp8 else s.dtype, k_scale=w.k_scale,
+                      v_scale=w.v_scale, pairs=pairs, threads=threads)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    per = el / reps
+    return {"value": bytes_ / per / 1e9, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "seconds_per_sample": per,
+            "sample": f"fp64 C oracle decode of {len(seqs)} of {B} sequences x "
+                      f"{s.num_q_heads} heads ({int(n.sum())} attended tokens), {reps} run(s)"}
+
+
+def host_caches(w, kc, vc):
+    def h(t):
+        t = t.cpu().contiguous()
+        if t.dtype in (torch.float16, torch.bfloat16):
+            return t.view(torch.int16).numpy().view(np.uint16)
+        return t.numpy()
+    return h(kc), h(vc)
+
+
+# ----------------------------------------------------------- reference arm
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    from oracle.build import build_oracle
+    import oracle
+    build_oracle()
+    w = generate(rank_spec(args.config, 0), device="cpu")
+    s = w.spec
+    if s.kv_fp8:
+        from workloads.gen import E4M3_NAN
+        shape = (w.num_blocks, s.num_kv_heads, s.block_size, s.head_dim)
+        kc = np.full(shape, E4M3_NAN, np.uint8)
+        vc = np.full(shape, E4M3_NAN, np.uint8)
+        oracle.reshape_and_cache(w.k_hist, w.v_hist, kc, vc, w.slot_hist.numpy(), s.dtype, "fp8",
+                                 w.k_scale, w.v_scale)
+    else:
+        kc, vc = host_caches(w, w.key_cache, w.value_cache)
+    oracle.reshape_and_cache(w.k_new, w.v_new, kc, vc, w.slot_new.numpy(), s.dtype,
+                             "fp8" if s.kv_fp8 else s.dtype, w.k_scale, w.v_scale)
+    # bounded sample per step: a few sequences, sized so the whole run stays short
+    total_budget = 120.0
+    per_step = max(0.01, total_budget / max(1, args.steps + args.warmup))
+    probe = oracle_baseline(w, kc, vc, budget_s=0.0, seq_subset=[0])
+    per_seq = probe["seconds_per_sample"]
+    nseq = int(max(1, min(s.batch, per_step / max(per_seq, 1e-6))))
+    subset = list(range(nseq))
+    for _ in range(args.warmup):
+        oracle_baseline(w, kc, vc, 0.0, subset)
+    times, vals = [], []
+    for _ in range(args.steps):
+        r = oracle_baseline(w, kc, vc, 0.0, subset)
+        times.append(r["seconds_per_sample"])
+        vals.append(r["value"])
+    ms = 1e3 * statistics.mean(times)
+    value = statistics.mean(vals)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": f"{args.config}: {workload_desc(s)}",
+                       "sample_per_step": f"{nseq} of {s.batch} sequences, all heads"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": r["cores"],
+                             "kind": "oracle", "sample": r["sample"]},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def workload_desc(s) -> str:
+    d = (f"batch {s.batch}, {s.num_q_heads} q / {s.num_kv_heads} kv heads, head_dim "
+         f"{s.head_dim}, block_size {s.block_size}, {s.dtype}")
+    if s.kv_fp8:
+        d += ", e4m3 KV"
+    if s.window:
+        d += f", window {s.window}"
+    if s.shared_prefix:
+        d += f", shared prefix {s.shared_prefix}"
+    return d
+
+
+# ----------------------------------------------------------- our arm
+
+def run_ours(args, world, rank, local):
+    import paged_kv_cache_267_gb300 as pa
+    from paged_kv_cache_267_gb300.build import build_library
+    build_library()
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    w = generate(rank_spec(args.config, rank), device=dev)
+    s = w.spec
+    kv = "fp8" if s.kv_fp8 else "auto"
+    if s.kv_fp8:
+        kc, vc = w.empty_fp8_cache()
+        pa.reshape_and_cache(w.k_hist, w.v_hist, kc, vc, w.slot_hist, kv, w.k_scale, w.v_scale)
+        w.k_hist = w.v_hist = w.slot_hist = None
+    else:
+        kc, vc = w.key_cache, w.value_cache
+    bt = torch.from_numpy(w.block_tables).to(dev)
+    sl = torch.from_numpy(w.seq_lens).to(dev)
+    out = torch.empty_like(w.q)
+    stream = torch.cuda.current_stream()
+    kw = dict(num_kv_heads=s.num_kv_heads, scale=s.softmax_scale, block_size=s.block_size,
+              window=s.window, kv_dtype=kv, k_scale=w.k_scale, v_scale=w.v_scale, out=out)
+
+    def step():
+        pa.reshape_and_cache(w.k_new, w.v_new, kc, vc, w.slot_new, kv, w.k_scale, w.v_scale)
+        pa.decode(w.q, kc, vc, bt, sl, **kw)
+
+    dbytes = decode_bytes(w)
+    rbytes = reshape_bytes(w)
+    step_bytes = dbytes["total"] + rbytes
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.15)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    n0 = pa.launch_count()
+    barrier(world)
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter()
+    for i in range(args.steps):
+        flush.zero_()
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    wall = time.perf_counter() - t_wall
+    launches = pa.launch_count() - n0
+    step_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+    # keep the clock window open for at least ~1 s of identical work
+    extra = 0
+    while time.perf_counter() - t_wall < 1.0 and extra < 20000:
+        flush.zero_()
+        step()
+        extra += 1
+        if extra % 50 == 0:
+            torch.cuda.synchronize()
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    ms_rank = statistics.mean(step_ms)
+    ms = max_over_ranks(ms_rank, world)
+    total_bytes = sum_over_ranks(float(step_bytes), world)
+    value = total_bytes / (ms * 1e-3) / 1e9
+
+    # ---- roofline: decode kernel alone, events around it on the launch stream
+    ev_a = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ev_b = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    for i in range(args.steps):
+        flush.zero_()
+        pa.profile_events(ev_a[i], ev_b[i])
+        pa.decode(w.q, kc, vc, bt, sl, **kw)
+    pa.profile_events(None, None)
+    torch.cuda.synchronize()
+    k_ms = statistics.mean(a.elapsed_time(b) for a, b in zip(ev_a, ev_b))
+    peak, peak_kind = measured_peak()
+    achieved = dbytes["kernel"] / (k_ms * 1e-3) / 1e9
+    traffic = profiled_traffic(args.config, dbytes["kernel"])
+
+    # ---- end to end through the public API with host buffers
+    host_in = {n: t.detach().cpu().pin_memory() for n, t in
+               (("q", w.q), ("k", w.k_new), ("v", w.v_new), ("slot", w.slot_new),
+                ("bt", bt), ("sl", sl))}
+    dev_in = {n: torch.empty_like(t, device=dev) for n, t in host_in.items()}
+    host_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = host_out.numel() * host_out.element_size()
+
+    def e2e_step():
+        for n, t in host_in.items():
+            dev_in[n].copy_(t, non_blocking=True)
+        pa.reshape_and_cache(dev_in["k"], dev_in["v"], kc, vc, dev_in["slot"], kv, w.k_scale,
+                             w.v_scale)
+        pa.decode(dev_in["q"], kc, vc, dev_in["bt"], dev_in["sl"], **kw)
+        host_out.copy_(out, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    e_s = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    e_e = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    for i in range(args.steps):
+        flush.zero_()
+        e_s[i].record(stream)
+        e2e_step()
+        e_e[i].record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in zip(e_s, e_e)), world)
+    e2e_value = total_bytes / (e2e_ms * 1e-3) / 1e9
+
+    bad = pa.check_device_error()
+    if bad:
+        raise RuntimeError(f"device error flag {bad} during the benchmark")
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        kch, vch = host_caches(w, kc, vc)
+        cpu = oracle_baseline(w, kch, vch, budget_s=args.cpu_budget)
+
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "us_per_step": ms * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16" if s.dtype == "bf16" else "f16",
+        "data": "synthetic",
+        "config": {"workload": f"{args.config}: {workload_desc(s)}",
+                   "global_batch": s.batch * world, "parallelism": f"replicas{world}",
+                   "step": "pa_reshape_and_cache (1 new token per sequence) + pa_decode",
+                   "attended_tokens_per_rank": dbytes["tokens"],
+                   "bytes_per_step_per_rank": step_bytes,
+                   "l2": "flushed (2x L2 write between timed steps, outside the events)"},
+        "pct_of_peak": 100.0 * value / world / peak,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "kernel": "paged_decode_kernel", "kernel_us": k_ms * 1e3,
+                     "bytes_per_launch": dbytes["kernel"], "peak_kind": peak_kind},
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": launches,
+        "clocks": clk,
+        "wall_s_timed": wall,
+    }
+    if cpu is not None:
+        line["cpu_baseline"] = cpu
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", default="llama8b")
+    ap.add_argument("--cpu-budget", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    world, rank, local = dist_setup(args.gpus)
+    try:
+        if args.impl == "reference":
+            run_reference(args, world, rank)
+        else:
+            run_ours(args, world, rank, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

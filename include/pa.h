@@ -1,0 +1,228 @@
+/*
+ * pa.h — C ABI of the GB300 paged-attention decode library (libpa.so).
+ *
+ * One decode step of PagedAttention: every sequence contributes one query
+ * token per q head, which attends over that sequence's K/V rows stored in
+ * fixed-size physical blocks of a shared pool and reached through a per-
+ * sequence block table. Sources (page title and section):
+ *   - "vLLM 0.5 深度解析" §2.1: blocks of block_size tokens, a block table per
+ *     request mapping logical to physical blocks, ceil(n / block_size) blocks
+ *     for n tokens; §2.2: scale = head_dim ** -0.5, the forward signature
+ *     (query, key_cache, value_cache, block_table, seq_lens); §2.3: per
+ *     physical block, K loaded, scaled dot product, softmax max/sum state,
+ *     V-weighted sum.
+ *   - "vLLM 0.7.2深度解析" §2.1: physical blocks shared by several sequences,
+ *     ref-counted deferred reclamation; §2.2: GQA head groups and the FP8 e4m3
+ *     KV cache; §2.3: masking of positions outside a sliding window and never
+ *     loading blocks that lie wholly outside it; §5.3: a hard cap on pool
+ *     blocks, requests beyond it rejected.
+ *
+ * Conventions for every entry point:
+ *   - Returns PA_OK (0) or a negative pa_status; a message for the calling
+ *     thread is available from pa_last_error(). No C++ exception crosses the
+ *     ABI. Host-detectable errors are reported before anything is launched.
+ *   - Tensors are described by pa_tensor: data pointer, dtype, rank, shape and
+ *     strides in elements. Device tensors must live in memory of the current
+ *     CUDA device. The caller owns every tensor; the library keeps no pointer
+ *     to them after the call returns.
+ *   - Launches are asynchronous on the given stream (a cudaStream_t; NULL is
+ *     the legacy default stream). No entry point synchronises the stream
+ *     except pa_check_device_error().
+ *   - Device-side data errors (a block id outside the pool, a seq_len beyond
+ *     max_blocks_per_seq * block_size, a slot beyond the pool) never cause an
+ *     out-of-bounds access: the kernel substitutes a safe value, and records
+ *     a bit in a device error word that pa_check_device_error() returns.
+ */
+#ifndef PA_H
+#define PA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int32_t pa_status;
+
+enum {
+  PA_OK = 0,
+  PA_ERR_INVALID_ARG = -1,   /* null pointer, bad value, aliasing, mismatched shapes */
+  PA_ERR_UNSUPPORTED = -2,   /* a shape or dtype this build has no kernel for */
+  PA_ERR_LAYOUT = -3,        /* a tensor is not contiguous or not aligned as required */
+  PA_ERR_CUDA = -4,          /* a CUDA runtime call or launch failed */
+  PA_ERR_OUT_OF_BLOCKS = -5, /* allocator: the pool cannot cover the request */
+  PA_ERR_WORKSPACE = -6,     /* decode workspace missing or too small */
+  PA_ERR_NOT_FOUND = -7      /* allocator: unknown sequence or block id */
+};
+
+/* Element types. */
+enum { PA_F16 = 0, PA_BF16 = 1, PA_FP8_E4M3 = 2, PA_I32 = 3, PA_I64 = 4 };
+
+/* kv_dtype argument: cache elements have the dtype of k/q (PA_KV_AUTO), or are
+ * OCP e4m3 codes (uint8) with per-tensor scales (PA_KV_FP8_E4M3). */
+enum { PA_KV_AUTO = 0, PA_KV_FP8_E4M3 = 2 };
+
+/* Bits of the device error word. */
+enum {
+  PA_DEVERR_BLOCK_ID = 1,  /* a block table entry outside [0, num_blocks) */
+  PA_DEVERR_SEQ_LEN = 2,   /* seq_len < 0 or > max_blocks_per_seq * block_size */
+  PA_DEVERR_SLOT = 4,      /* a slot_mapping entry >= num_blocks * block_size */
+  PA_DEVERR_TIMEOUT = 8    /* a pipeline wait gave up (should never happen) */
+};
+
+#define PA_MAX_DIMS 6
+
+typedef struct pa_tensor {
+  void* data;
+  int32_t dtype;                  /* PA_F16 ... PA_I64 */
+  int32_t ndim;                   /* 1 .. PA_MAX_DIMS */
+  int64_t shape[PA_MAX_DIMS];
+  int64_t strides[PA_MAX_DIMS];   /* in elements */
+} pa_tensor;
+
+typedef void* pa_stream; /* cudaStream_t */
+
+/* ------------------------------------------------------------ write path */
+
+/*
+ * pa_reshape_and_cache — scatter new K/V rows into their cache slots.
+ * For every t < T with slot = slot_mapping[t] >= 0 and every head h:
+ *   key_cache[slot / bs, h, slot % bs, :]   = enc(k[t, h, :])
+ *   value_cache[slot / bs, h, slot % bs, :] = enc(v[t, h, :])
+ * enc is the identity (bit copy) for PA_KV_AUTO; for PA_KV_FP8_E4M3 it is
+ * e4m3(round-to-nearest-even, saturating)(float(x) / scale) with the division
+ * in IEEE fp32, k_scale for K and v_scale for V. Slots < 0 are skipped; slots
+ * beyond the pool are skipped and flagged (PA_DEVERR_SLOT). Duplicate
+ * non-negative slots are a caller error (the surviving row is unspecified).
+ *
+ *   k, v          [T, Hkv, D] f16/bf16; dims 1 and 2 contiguous, dim 0 any
+ *                 stride; rows 16-byte aligned.
+ *   key_cache,    [NB, Hkv, bs, D] contiguous; dtype of k (PA_KV_AUTO) or
+ *   value_cache   PA_FP8_E4M3 (uint8 codes).
+ *   slot_mapping  [T] int64, slot = physical_block * bs + offset.
+ *   k_scale, v_scale  used only for FP8 (finite, > 0).
+ * D must be a multiple of 8 (16 for FP8).
+ */
+pa_status pa_reshape_and_cache(const pa_tensor* k, const pa_tensor* v,
+                               const pa_tensor* key_cache, const pa_tensor* value_cache,
+                               const pa_tensor* slot_mapping, int32_t kv_dtype,
+                               float k_scale, float v_scale, pa_stream stream);
+
+/* ---------------------------------------------------------------- decode */
+
+/*
+ * pa_decode — one decode step of paged attention.
+ * For every sequence b and q head h, with G = Hq / Hkv, kvh = h / G,
+ * L = seq_lens[b], start = (window > 0 && L > window) ? L - window : 0:
+ *   out[b, h, :] = sum_{j in [start, L)} softmax_j(scale * q[b,h,:] . K_j) V_j
+ * where K_j, V_j are the rows at block_tables[b][j / bs], offset j % bs, KV
+ * head kvh (for FP8: decode(code) * k_scale, resp. * v_scale). An empty range
+ * (L == 0) gives a row of zeros. Blocks wholly outside [start, L) are never
+ * read; table entries past ceil(L / bs) are never read.
+ *
+ *   out           [B, Hq, D] contiguous, dtype of q; must not overlap inputs.
+ *   q             [B, Hq, D] contiguous, f16 or bf16.
+ *   key_cache,    [NB, Hkv, bs, D] contiguous, base 16-byte aligned; dtype of
+ *   value_cache   q (PA_KV_AUTO) or PA_FP8_E4M3.
+ *   block_tables  [B, MB] int32 contiguous.
+ *   seq_lens      [B] int32.
+ *   num_kv_heads  Hkv (== key_cache.shape[1]); Hq % Hkv == 0, G <= 16.
+ *   block_size    bs (== key_cache.shape[2]), a multiple of 16, <= 1024.
+ *   window        <= 0: no window.
+ * Supported D: 64, 128, 256 for 16-bit caches; 128, 256 for FP8. B <= 4096.
+ *
+ * Workspace: the step writes per-worker partial results (running max, sum and
+ * unnormalised output) and a small control block to a device workspace of
+ * pa_decode_workspace_size() bytes. It is the buffer given to
+ * pa_set_workspace() for the current device, or else a buffer the library
+ * allocates once per (device, stream) outside stream capture and keeps. Calls
+ * that overlap on the GPU must not share a workspace.
+ */
+pa_status pa_decode(const pa_tensor* out, const pa_tensor* q, const pa_tensor* key_cache,
+                    const pa_tensor* value_cache, const pa_tensor* block_tables,
+                    const pa_tensor* seq_lens, int32_t num_kv_heads, float scale,
+                    int32_t block_size, int32_t window, int32_t kv_dtype, float k_scale,
+                    float v_scale, pa_stream stream);
+
+/* Workspace bytes pa_decode needs on the current device for a batch of
+ * `batch` sequences with these head counts and head_dim. */
+pa_status pa_decode_workspace_size(int64_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+                                   int32_t head_dim, size_t* bytes);
+
+/* Use caller-owned device memory [ptr, ptr + bytes) as the decode workspace on
+ * the current device (ptr 256-byte aligned). ptr == NULL returns to the
+ * library-managed workspace. The caller keeps the memory alive while decode
+ * steps that use it are in flight. */
+pa_status pa_set_workspace(void* ptr, size_t bytes);
+
+/* Test and tuning knob: max_ctas > 0 caps the persistent decode grid;
+ * min_tiles > 0 is the least number of 16-token tiles per worker warp.
+ * Both 0 restore the defaults. Affects later pa_decode calls process-wide. */
+pa_status pa_set_decode_tuning(int32_t max_ctas, int32_t min_tiles);
+
+/* Profiling hook: when both are non-NULL, the next pa_decode calls on this
+ * thread record the CUDA events (cudaEvent_t) immediately before and after the
+ * main decode kernel on the call's stream. NULL, NULL turns it off. */
+pa_status pa_profile_events(void* ev_before, void* ev_after);
+
+/* Reads and clears the device error word of the current device (PA_DEVERR_*
+ * bits); synchronises `stream`. */
+pa_status pa_check_device_error(int32_t* bits, pa_stream stream);
+
+/* Number of kernels this library has launched in this process. */
+uint64_t pa_launch_count(void);
+
+/* Message for the last error on the calling thread ("" if none). */
+const char* pa_last_error(void);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int32_t pa_version(void);
+
+/* --------------------------------------------------- host block allocator */
+
+/*
+ * A fixed pool of num_blocks physical blocks of block_size tokens, used to
+ * build block tables ("vLLM 0.5 深度解析" §2.1; "vLLM 0.7.2深度解析" §2.1, §5.3).
+ *   - The free list starts as 0..NB-1 shuffled by Fisher-Yates driven by
+ *     SplitMix64(seed); allocation pops from its end.
+ *   - A sequence of n tokens holds ceil(n / block_size) blocks.
+ *   - fork() shares every block of a sequence (reference count + 1 each).
+ *   - append() grows a sequence; if its last block is partial and shared it is
+ *     first copied (copy-on-write): *cow_src / *cow_dst name the blocks whose
+ *     cached rows the caller must copy (-1 / -1 when no copy is needed).
+ *   - free() drops one reference per block; blocks reaching zero wait in a
+ *     pending list until reclaim() returns them to the free list (deferred
+ *     reclamation: call it once the GPU work reading them has finished).
+ *   - Every call is all-or-nothing: PA_ERR_OUT_OF_BLOCKS leaves the pool as it
+ *     was (a hard cap: requests beyond it are rejected, not queued).
+ * Handles are not thread-safe; use one per thread or lock around calls.
+ */
+typedef struct pa_alloc pa_alloc;
+
+pa_status pa_alloc_create(int32_t num_blocks, int32_t block_size, uint64_t seed, pa_alloc** out);
+void pa_alloc_destroy(pa_alloc* a);
+pa_status pa_alloc_add(pa_alloc* a, int64_t n_tokens, int32_t* seq_out);
+pa_status pa_alloc_fork(pa_alloc* a, int32_t src_seq, int32_t* seq_out);
+pa_status pa_alloc_append(pa_alloc* a, int32_t seq, int64_t n_tokens, int32_t* cow_src,
+                          int32_t* cow_dst);
+pa_status pa_alloc_free(pa_alloc* a, int32_t seq);
+/* Returns the number of blocks moved from pending to free. */
+int32_t pa_alloc_reclaim(pa_alloc* a);
+/* Copies the sequence's block ids (logical order) into out[0 .. capacity);
+ * *n_out receives the count; PA_ERR_INVALID_ARG if capacity is too small. */
+pa_status pa_alloc_block_table(const pa_alloc* a, int32_t seq, int32_t* out, int32_t capacity,
+                               int32_t* n_out);
+pa_status pa_alloc_seq_len(const pa_alloc* a, int32_t seq, int64_t* len_out);
+/* Writes a [n, max_blocks] int32 table matrix (-1 padded) and int32 lengths
+ * for the listed sequences, the layout pa_decode reads. */
+pa_status pa_alloc_fill_tables(const pa_alloc* a, const int32_t* seqs, int32_t n,
+                               int32_t* tables, int32_t max_blocks, int32_t* lens_out);
+int32_t pa_alloc_refcount(const pa_alloc* a, int32_t block); /* -1 for a bad id */
+int32_t pa_alloc_num_free(const pa_alloc* a);
+int32_t pa_alloc_num_pending(const pa_alloc* a);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* PA_H */

@@ -1,0 +1,582 @@
+// Persistent paged-decode kernel for sm_103a.
+//
+// Work decomposition (balanced split-KV). Every (sequence b, KV head) pair owns
+// the 16-token tiles that cover its attended positions [start, L) — tiles never
+// straddle a physical block because block_size is a multiple of 16. All tiles
+// of all pairs form one flat index space (pair-major). Each worker warp takes
+// a contiguous range of `wt` tiles of it, so every warp moves the same number
+// of K/V bytes however skewed the sequence lengths are. A worker's range cut
+// at pair boundaries gives "segments"; each segment produces one partial
+// result (running max m, running sum l, unnormalised output) in partial slot
+// (pair index + worker index), which is unique because the walk through the
+// (pair, worker) grid is a monotone staircase. A small merge kernel combines
+// the partials of each pair by their log-sum-exp weights.
+//
+// Data movement. Each warp owns a ring of STAGES shared-memory stages; one
+// stage holds the K tile and the V tile [16 rows x D] of one (block, KV head),
+// loaded by TMA boxes of [16 rows x 128 bytes] with the 128-byte swizzle, and
+// signalled on an mbarrier. Block ids are read 32 at a time per warp and
+// broadcast with shuffles. Each K/V byte of the step is loaded once and used
+// by all G query heads of its group. Blocks wholly outside the window are
+// never loaded ("vLLM 0.7.2深度解析" §2.3).
+//
+// Math (per tile, per warp), on the tensor cores with fp32 accumulation:
+//   S^T[16 tok x 8 heads] = K[16 x D] . Q^T[D x 8]     (mma m16n8k16, M = tokens)
+//   online softmax on S in the log2 domain (scale * log2 e folded in)
+//   O^T[D x 8 heads] += V^T[D x 16 tok] . P^T[16 x 8]  (P^T via movmatrix)
+// i.e. the block-wise scaled dot product, max/sum state and V-weighted sum of
+// "vLLM 0.5 深度解析" §2.3, done in one pass. Positions outside [start, L) in
+// the first and last tile of a pair get score -inf and their V rows are
+// zeroed in the fragment, so poisoned slots never reach the result.
+//
+// FP8 e4m3 caches: codes are converted to f16 in registers (exact), Q is
+// converted once per segment to f16 after a power-of-two rescale so its
+// largest magnitude lies in [2^14, 2^15), and k_scale, v_scale and the rescale
+// are folded into the score scale and the partial outputs.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "pa_internal.h"
+#include "ptx.cuh"
+
+namespace pa {
+
+constexpr uint64_t kWaitLimitNs = 2000000000ull;   // pipeline wait bound (2 s)
+constexpr uint64_t kDrainLimitNs = 200000000ull;   // bound while draining after an error
+constexpr int kErrBlockId = 1, kErrSeqLen = 2, kErrTimeout = 8;
+
+template <int CT, int D, int STAGES>
+struct Geometry {
+  static constexpr int ELT = (CT == kE4M3) ? 1 : 2;
+  static constexpr int ROW_BYTES = D * ELT;
+  static constexpr int BOXES = ROW_BYTES / 128;   // 128-byte column boxes per row
+  static constexpr int BOX_ELEMS = 128 / ELT;
+  static constexpr int TILE_BYTES = kTile * ROW_BYTES;
+  static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
+  static constexpr int RING_BYTES = STAGES * STAGE_BYTES;
+  static constexpr int MT = D / 16;
+  static_assert(ROW_BYTES % 128 == 0, "rows must be whole 128-byte boxes");
+};
+
+// Shared-memory byte offset of 16-byte chunk c (counted along the full row) of
+// tile row r. A tile is stored as [box][16 rows][128 B]; within a box the TMA
+// 128-byte swizzle places chunk j of row r at position j ^ (r & 7).
+__device__ __forceinline__ uint32_t tile_off(int r, int c) {
+  return (static_cast<uint32_t>(c >> 3) << 11) + (static_cast<uint32_t>(r) << 7) +
+         (static_cast<uint32_t>((c & 7) ^ (r & 7)) << 4);
+}
+
+__device__ __forceinline__ int win_start(int L, int W) { return (W > 0 && L > W) ? L - W : 0; }
+__device__ __forceinline__ int tiles_of(int L, int W) {
+  return L > 0 ? (L + kTile - 1) / kTile - win_start(L, W) / kTile : 0;
+}
+
+struct Cursor {
+  int b, kvh, t, nt;
+};
+
+// Places the cursor on flat tile f (f < total): pair (b, kvh), tile t of nt.
+__device__ __forceinline__ void cursor_locate(Cursor& c, int f, const int* pref, int B,
+                                              int Hkv) {
+  int lo = 0, hi = B;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (Hkv * pref[mid] <= f) lo = mid; else hi = mid;
+  }
+  c.b = lo;
+  c.nt = pref[lo + 1] - pref[lo];
+  const int rem = f - Hkv * pref[lo];
+  c.kvh = rem / c.nt;
+  c.t = rem - c.kvh * c.nt;
+}
+
+__device__ __forceinline__ void cursor_next(Cursor& c, const int* pref, int B, int Hkv) {
+  if (++c.t < c.nt) return;
+  c.t = 0;
+  if (++c.kvh < Hkv) return;
+  c.kvh = 0;
+  do {
+    ++c.b;
+  } while (c.b < B && pref[c.b + 1] == pref[c.b]);
+  if (c.b < B) c.nt = pref[c.b + 1] - pref[c.b];
+}
+
+template <bool BF16>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  if constexpr (BF16) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+  } else {
+    __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+  }
+}
+
+template <int QT>
+__device__ __forceinline__ float to_float(uint16_t x) {
+  if constexpr (QT == kBF16) {
+    return __uint_as_float(static_cast<uint32_t>(x) << 16);
+  } else {
+    return __half2float(__ushort_as_half(x));
+  }
+}
+
+// Head-dim index held by accumulator row (m-tile mt, fragment row g + 8 * hi).
+template <bool FP8>
+__device__ __forceinline__ int acc_dim(int mt, int g, int hi) {
+  if constexpr (FP8) {
+    return 32 * (mt >> 1) + 4 * g + 2 * (mt & 1) + hi;
+  } else {
+    return 16 * mt + g + 8 * hi;
+  }
+}
+
+template <int CT, int QT, int D, int NT, int WARPS, int STAGES>
+__global__ void __launch_bounds__(WARPS * 32)
+    paged_decode_kernel(const __grid_constant__ CUtensorMap tmK,
+                        const __grid_constant__ CUtensorMap tmV, const DecodeArgs a) {
+  using Gm = Geometry<CT, D, STAGES>;
+  constexpr bool kFp8 = (CT == kE4M3);
+  constexpr bool kBf16Mma = (CT == kBF16);
+  constexpr int MT = Gm::MT;
+  constexpr unsigned FULL = 0xffffffffu;
+
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_addr(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (base - raw);
+  const uint32_t bars = base + WARPS * Gm::RING_BYTES;
+  int* s_len = reinterpret_cast<int*>(gbase + WARPS * Gm::RING_BYTES + WARPS * STAGES * 8);
+  int* s_pref = s_len + a.B;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g = lane >> 2, t4 = lane & 3;
+
+  griddep_wait();
+  griddep_launch_dependents();
+
+  if (tid == 0) {
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+    for (int i = 0; i < WARPS * STAGES; ++i) mbar_init(bars + 8 * i, 1);
+    fence_mbar_init();
+    fence_proxy_async();
+  }
+  // sequence lengths, clamped to the block-table capacity
+  const int cap = a.MB * a.bs;
+  for (int b = tid; b < a.B; b += blockDim.x) {
+    int L = a.seq_lens[b];
+    if (L < 0 || L > cap) {
+      atomicOr(a.err, kErrSeqLen);
+      L = L < 0 ? 0 : cap;
+    }
+    s_len[b] = L;
+  }
+  __syncthreads();
+  // exclusive prefix of tiles per pair over the sequences (one warp)
+  if (warp == 0) {
+    int run = 0;
+    for (int b0 = 0; b0 < a.B; b0 += 32) {
+      const int b = b0 + lane;
+      int x = (b < a.B) ? tiles_of(s_len[b], a.window) : 0;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(FULL, x, o);
+        if (lane >= o) x += y;
+      }
+      if (b < a.B) s_pref[b + 1] = run + x;
+      run += __shfl_sync(FULL, x, 31);
+    }
+    if (lane == 0) s_pref[0] = 0;
+  }
+  __syncthreads();
+
+  const int total = a.Hkv * s_pref[a.B];
+  const int nw = gridDim.x * WARPS;
+  int wt = (total + nw - 1) / nw;
+  if (wt < a.min_tiles) wt = a.min_tiles;
+  if (blockIdx.x == 0) {
+    if (tid == 0) {
+      a.ctrl[0] = wt;
+      a.ctrl[1] = total;
+    }
+    for (int b = tid; b <= a.B; b += blockDim.x) a.ctrl[2 + b] = s_pref[b];
+  }
+  const int w = blockIdx.x * WARPS + warp;
+  const long long f0ll = static_cast<long long>(w) * wt;
+  if (f0ll >= total) return;
+  const int f0 = static_cast<int>(f0ll);
+  const int f1 = min(f0 + wt, total);
+
+  const uint32_t ring = base + warp * Gm::RING_BYTES;
+  const uint32_t wbars = bars + warp * STAGES * 8;
+
+  // ---------------------------------------------------------------- producer
+  Cursor pc, cc;
+  cursor_locate(pc, f0, s_pref, a.B, a.Hkv);
+  cc = pc;
+  int id_b = -1, id_lb0 = 0, id_val = 0;
+  auto produce = [&](int slot) {
+    const int L = s_len[pc.b];
+    const int pt = win_start(L, a.window) / kTile + pc.t;  // tile index in position space
+    const int lb = (pt * kTile) / a.bs;
+    if (pc.b != id_b || lb < id_lb0 || lb >= id_lb0 + 32) {
+      id_b = pc.b;
+      id_lb0 = lb;
+      const int e = lb + lane;
+      id_val = (e < a.MB) ? __ldg(a.block_tables + static_cast<size_t>(pc.b) * a.MB + e) : 0;
+    }
+    int phys = __shfl_sync(FULL, id_val, lb - id_lb0);
+    if (static_cast<unsigned>(phys) >= static_cast<unsigned>(a.NB)) {
+      if (lane == 0) atomicOr(a.err, kErrBlockId);
+      phys = 0;
+    }
+    const int row = (phys * a.Hkv + pc.kvh) * a.bs + (pt * kTile) % a.bs;
+    if (lane == 0) {
+      const uint32_t bar = wbars + 8 * slot;
+      const uint32_t kd = ring + slot * Gm::STAGE_BYTES;
+      mbar_arrive_expect_tx(bar, Gm::STAGE_BYTES);
+#pragma unroll
+      for (int j = 0; j < Gm::BOXES; ++j) {
+        tma_load_2d(kd + j * 2048, &tmK, j * Gm::BOX_ELEMS, row, bar);
+        tma_load_2d(kd + Gm::TILE_BYTES + j * 2048, &tmV, j * Gm::BOX_ELEMS, row, bar);
+      }
+    }
+    cursor_next(pc, s_pref, a.B, a.Hkv);
+  };
+
+  int produced = 0, consumed = 0;
+  for (int f = f0; f < f1 && produced < STAGES; ++f) {
+    produce(produced % STAGES);
+    ++produced;
+  }
+
+  // ---------------------------------------------------------------- consumer
+  uint32_t qf[MT][NT][2];
+  float m_run[NT][2], l_run[NT][2];
+  float acc[MT][NT][4];
+  float sc = a.score_scale;
+  bool ok = true;
+
+  for (int f = f0; f < f1; ++f) {
+    const int slot = consumed % STAGES;
+    const uint32_t parity = (consumed / STAGES) & 1;
+    const bool seg_start = (f == f0) || (cc.t == 0);
+    if (seg_start) {
+      // query fragments of this pair's G heads (B operand, k = head dim)
+      const uint16_t* qg = reinterpret_cast<const uint16_t*>(a.q) +
+                           (static_cast<size_t>(cc.b) * a.Hq + cc.kvh * a.G) * D;
+      sc = a.score_scale;
+      if constexpr (!kFp8) {
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          const int h = 8 * nt + g;
+          const uint32_t* qh = reinterpret_cast<const uint32_t*>(qg + h * D);
+#pragma unroll
+          for (int ks = 0; ks < MT; ++ks) {
+            qf[ks][nt][0] = (h < a.G) ? qh[(16 * ks + 2 * t4) >> 1] : 0u;
+            qf[ks][nt][1] = (h < a.G) ? qh[(16 * ks + 8 + 2 * t4) >> 1] : 0u;
+          }
+        }
+      } else {
+        // k-step ks = 4 * qd + j covers head dims 64 qd + 16 t4 + 4 j + {0..3}
+        float qv[MT][NT][4];
+        float amax = 0.f;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          const int h = 8 * nt + g;
+#pragma unroll
+          for (int ks = 0; ks < MT; ++ks) {
+            const int d = 64 * (ks >> 2) + 16 * t4 + 4 * (ks & 3);
+            uint2 raw2 = make_uint2(0u, 0u);
+            if (h < a.G) raw2 = *reinterpret_cast<const uint2*>(qg + h * D + d);
+            qv[ks][nt][0] = to_float<QT>(static_cast<uint16_t>(raw2.x & 0xffffu));
+            qv[ks][nt][1] = to_float<QT>(static_cast<uint16_t>(raw2.x >> 16));
+            qv[ks][nt][2] = to_float<QT>(static_cast<uint16_t>(raw2.y & 0xffffu));
+            qv[ks][nt][3] = to_float<QT>(static_cast<uint16_t>(raw2.y >> 16));
+#pragma unroll
+            for (int i = 0; i < 4; ++i) amax = fmaxf(amax, fabsf(qv[ks][nt][i]));
+          }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(FULL, amax, o));
+        int sh = 0;
+        if (amax > 0.f && amax < INFINITY) {
+          int e;
+          frexpf(amax, &e);  // amax = m * 2^e, m in [0.5, 1)
+          sh = (e - 1) - 14;
+        }
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int ks = 0; ks < MT; ++ks) {
+            qf[ks][nt][0] = pack2<false>(ldexpf(qv[ks][nt][0], -sh), ldexpf(qv[ks][nt][1], -sh));
+            qf[ks][nt][1] = pack2<false>(ldexpf(qv[ks][nt][2], -sh), ldexpf(qv[ks][nt][3], -sh));
+          }
+        sc = ldexpf(a.score_scale, sh);
+      }
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        m_run[nt][0] = m_run[nt][1] = -INFINITY;
+        l_run[nt][0] = l_run[nt][1] = 0.f;
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) acc[mt][nt][i] = 0.f;
+      }
+    }
+
+    const bool got = mbar_wait_bounded(wbars + 8 * slot, parity, kWaitLimitNs);
+    if (!__all_sync(FULL, got)) {
+      ok = false;
+      break;
+    }
+    const uint32_t kt = ring + slot * Gm::STAGE_BYTES;
+    const uint32_t vt = kt + Gm::TILE_BYTES;
+
+    // tile position and edge masks
+    const int L = s_len[cc.b];
+    const int st = win_start(L, a.window);
+    const int p0 = (st / kTile + cc.t) * kTile;
+    const bool edge = (p0 < st) || (p0 + kTile > L);
+    auto valid = [&](int r) { return !edge || (p0 + r >= st && p0 + r < L); };
+
+    // ---- S^T = K . Q^T
+    float sacc[NT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) sacc[nt][i] = 0.f;
+    if constexpr (!kFp8) {
+#pragma unroll
+      for (int ks = 0; ks < MT; ++ks) {
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4(kt + tile_off(lane & 15, 2 * ks + (lane >> 4)), a0, a1, a2, a3);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+          mma_16816<kBf16Mma>(sacc[nt], a0, a1, a2, a3, qf[ks][nt][0], qf[ks][nt][1]);
+      }
+    } else {
+#pragma unroll
+      for (int qd = 0; qd < D / 64; ++qd) {
+        uint32_t wlo[4], whi[4];
+        const int c = (64 * qd + 16 * t4) >> 4;
+        lds_v4(kt + tile_off(g, c), wlo[0], wlo[1], wlo[2], wlo[3]);
+        lds_v4(kt + tile_off(g + 8, c), whi[0], whi[1], whi[2], whi[3]);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint32_t a0 = e4m3x2_to_f16x2(static_cast<uint16_t>(wlo[j] & 0xffffu));
+          const uint32_t a2 = e4m3x2_to_f16x2(static_cast<uint16_t>(wlo[j] >> 16));
+          const uint32_t a1 = e4m3x2_to_f16x2(static_cast<uint16_t>(whi[j] & 0xffffu));
+          const uint32_t a3 = e4m3x2_to_f16x2(static_cast<uint16_t>(whi[j] >> 16));
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt)
+            mma_16816<false>(sacc[nt], a0, a1, a2, a3, qf[4 * qd + j][nt][0],
+                             qf[4 * qd + j][nt][1]);
+        }
+      }
+    }
+
+    // ---- online softmax (log2 domain), P^T fragments
+    const bool vlo = valid(g), vhi = valid(g + 8);
+    uint32_t pb[NT][2];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const float s0 = vlo ? sacc[nt][0] * sc : -INFINITY;
+      const float s1 = vlo ? sacc[nt][1] * sc : -INFINITY;
+      const float s2 = vhi ? sacc[nt][2] * sc : -INFINITY;
+      const float s3 = vhi ? sacc[nt][3] * sc : -INFINITY;
+      float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1) {
+        mx0 = fmaxf(mx0, __shfl_xor_sync(FULL, mx0, o));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(FULL, mx1, o));
+      }
+      const float mn0 = fmaxf(m_run[nt][0], mx0), mn1 = fmaxf(m_run[nt][1], mx1);
+      const float al0 = fast_exp2(m_run[nt][0] - mn0), al1 = fast_exp2(m_run[nt][1] - mn1);
+      m_run[nt][0] = mn0;
+      m_run[nt][1] = mn1;
+      const float p0v = fast_exp2(s0 - mn0), p1v = fast_exp2(s1 - mn1);
+      const float p2v = fast_exp2(s2 - mn0), p3v = fast_exp2(s3 - mn1);
+      l_run[nt][0] = l_run[nt][0] * al0 + (p0v + p2v);
+      l_run[nt][1] = l_run[nt][1] * al1 + (p1v + p3v);
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) {
+        acc[mt][nt][0] *= al0;
+        acc[mt][nt][1] *= al1;
+        acc[mt][nt][2] *= al0;
+        acc[mt][nt][3] *= al1;
+      }
+      pb[nt][0] = movmatrix_trans(pack2<kBf16Mma>(p0v, p1v));
+      pb[nt][1] = movmatrix_trans(pack2<kBf16Mma>(p2v, p3v));
+    }
+
+    // ---- O^T += V^T . P^T
+    uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;
+    if (edge) {
+      mlo = (valid(2 * t4) ? 0x0000ffffu : 0u) | (valid(2 * t4 + 1) ? 0xffff0000u : 0u);
+      mhi = (valid(2 * t4 + 8) ? 0x0000ffffu : 0u) | (valid(2 * t4 + 9) ? 0xffff0000u : 0u);
+    }
+    if constexpr (!kFp8) {
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) {
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4_trans(vt + tile_off((lane & 7) + ((lane >> 4) << 3), 2 * mt + ((lane >> 3) & 1)),
+                      a0, a1, a2, a3);
+        a0 &= mlo;
+        a1 &= mlo;
+        a2 &= mhi;
+        a3 &= mhi;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+          mma_16816<kBf16Mma>(acc[mt][nt], a0, a1, a2, a3, pb[nt][0], pb[nt][1]);
+      }
+    } else {
+#pragma unroll
+      for (int u = 0; u < D / 32; ++u) {
+        const int dby = 32 * u + 4 * g;  // byte (= element) offset in the row
+        const uint32_t co = (dby & 15);
+        const int c = dby >> 4;
+        const uint32_t w0 = lds_b32(vt + tile_off(2 * t4, c) + co);
+        const uint32_t w1 = lds_b32(vt + tile_off(2 * t4 + 1, c) + co);
+        const uint32_t w8 = lds_b32(vt + tile_off(2 * t4 + 8, c) + co);
+        const uint32_t w9 = lds_b32(vt + tile_off(2 * t4 + 9, c) + co);
+        const uint32_t x01a = __byte_perm(w0, w1, 0x5140), x01b = __byte_perm(w0, w1, 0x7362);
+        const uint32_t x89a = __byte_perm(w8, w9, 0x5140), x89b = __byte_perm(w8, w9, 0x7362);
+        // m-tile 2u: rows g, g+8 hold dims dby, dby+1; m-tile 2u+1: dby+2, dby+3
+        const uint32_t e0 = e4m3x2_to_f16x2(static_cast<uint16_t>(x01a & 0xffffu)) & mlo;
+        const uint32_t e1 = e4m3x2_to_f16x2(static_cast<uint16_t>(x01a >> 16)) & mlo;
+        const uint32_t e2 = e4m3x2_to_f16x2(static_cast<uint16_t>(x89a & 0xffffu)) & mhi;
+        const uint32_t e3 = e4m3x2_to_f16x2(static_cast<uint16_t>(x89a >> 16)) & mhi;
+        const uint32_t f0v = e4m3x2_to_f16x2(static_cast<uint16_t>(x01b & 0xffffu)) & mlo;
+        const uint32_t f1v = e4m3x2_to_f16x2(static_cast<uint16_t>(x01b >> 16)) & mlo;
+        const uint32_t f2v = e4m3x2_to_f16x2(static_cast<uint16_t>(x89b & 0xffffu)) & mhi;
+        const uint32_t f3v = e4m3x2_to_f16x2(static_cast<uint16_t>(x89b >> 16)) & mhi;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          mma_16816<false>(acc[2 * u][nt], e0, e1, e2, e3, pb[nt][0], pb[nt][1]);
+          mma_16816<false>(acc[2 * u + 1][nt], f0v, f1v, f2v, f3v, pb[nt][0], pb[nt][1]);
+        }
+      }
+    }
+    __syncwarp();
+    ++consumed;
+    if (produced < f1 - f0) {  // refill the stage just consumed
+      produce(produced % STAGES);
+      ++produced;
+    }
+
+    // ---- segment end: write the partial (m, l, unnormalised output)
+    const bool seg_end = (f == f1 - 1) || (cc.t == cc.nt - 1);
+    if (seg_end) {
+      const int pair = cc.b * a.Hkv + cc.kvh;
+      float* P = a.part + static_cast<size_t>(pair + w) * (a.G * (D + 2));
+      const float vs = kFp8 ? a.v_scale : 1.f;
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          float l = l_run[nt][e];
+          l += __shfl_xor_sync(FULL, l, 4);
+          l += __shfl_xor_sync(FULL, l, 8);
+          l += __shfl_xor_sync(FULL, l, 16);
+          const int h = 8 * nt + 2 * t4 + e;
+          if (h < a.G) {
+            float* Ph = P + h * D;
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt) {
+              Ph[acc_dim<kFp8>(mt, g, 0)] = acc[mt][nt][e] * vs;
+              Ph[acc_dim<kFp8>(mt, g, 1)] = acc[mt][nt][2 + e] * vs;
+            }
+            if (g == 0) {
+              P[a.G * D + h] = m_run[nt][e];
+              P[a.G * D + a.G + h] = l;
+            }
+          }
+        }
+      }
+    }
+    cursor_next(cc, s_pref, a.B, a.Hkv);
+  }
+
+  if (!ok) {
+    // Record the failure, then give the copies still in flight a bounded
+    // chance to land before the warp leaves.
+    if (lane == 0) atomicOr(a.err, kErrTimeout);
+    for (int k = consumed; k < produced; ++k)
+      (void)mbar_wait_bounded(wbars + 8 * (k % STAGES), (k / STAGES) & 1, kDrainLimitNs);
+  }
+}
+
+// ---------------------------------------------------------------- host side
+
+template <int CT, int QT, int D, int NT, int WARPS, int STAGES>
+struct DecodeKernel {
+  using Gm = Geometry<CT, D, STAGES>;
+  static void* fn() {
+    return reinterpret_cast<void*>(&paged_decode_kernel<CT, QT, D, NT, WARPS, STAGES>);
+  }
+  static DecodeVariant variant() { return DecodeVariant{WARPS, STAGES, WARPS * Gm::RING_BYTES}; }
+  static cudaError_t prepare(int smem, int* ctas_per_sm) {
+    cudaError_t e =
+        cudaFuncSetAttribute(fn(), cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, fn(), WARPS * 32, smem);
+  }
+  static cudaError_t launch(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArgs& a,
+                            int grid, int smem, cudaStream_t s, bool pdl) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(WARPS * 32);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, paged_decode_kernel<CT, QT, D, NT, WARPS, STAGES>, tk, tv, a);
+  }
+};
+
+// Stage count per variant: about 24 KB of ring per warp (two stages at least).
+template <int CT, int D>
+constexpr int stages_for() {
+  constexpr int pair = 2 * kTile * D * ((CT == kE4M3) ? 1 : 2);
+  constexpr int s = (24 * 1024) / pair;
+  return s < 2 ? 2 : s;
+}
+
+constexpr int kWarps = 4;
+
+// Expands `BODY` with the kernel type K for a runtime (D, NT) pair.
+#define PA_DECODE_DISPATCH(CT, QT, D_, NT_, BODY)                                \
+  do {                                                                            \
+    if ((D_) == 64 && (NT_) == 1 && (CT) != kE4M3) {                              \
+      using K = DecodeKernel<CT, QT, ((CT) != kE4M3 ? 64 : 128), 1, kWarps,       \
+                             stages_for<CT, ((CT) != kE4M3 ? 64 : 128)>()>;       \
+      BODY;                                                                       \
+    } else if ((D_) == 64 && (NT_) == 2 && (CT) != kE4M3) {                       \
+      using K = DecodeKernel<CT, QT, ((CT) != kE4M3 ? 64 : 128), 2, kWarps,       \
+                             stages_for<CT, ((CT) != kE4M3 ? 64 : 128)>()>;       \
+      BODY;                                                                       \
+    } else if ((D_) == 128 && (NT_) == 1) {                                       \
+      using K = DecodeKernel<CT, QT, 128, 1, kWarps, stages_for<CT, 128>()>;      \
+      BODY;                                                                       \
+    } else if ((D_) == 128 && (NT_) == 2) {                                       \
+      using K = DecodeKernel<CT, QT, 128, 2, kWarps, stages_for<CT, 128>()>;      \
+      BODY;                                                                       \
+    } else if ((D_) == 256 && (NT_) == 1) {                                       \
+      using K = DecodeKernel<CT, QT, 256, 1, kWarps, stages_for<CT, 256>()>;      \
+      BODY;                                                                       \
+    } else if ((D_) == 256 && (NT_) == 2) {                                       \
+      using K = DecodeKernel<CT, QT, 256, 2, kWarps, stages_for<CT, 256>()>;      \
+      BODY;                                                                       \
+    } else {                                                                      \
+      return cudaErrorInvalidValue;                                               \
+    }                                                                             \
+  } while (0)
+
+}  // namespace pa

@@ -1,0 +1,561 @@
+// C-ABI layer of libpa: argument validation, workspace management, TMA
+// descriptor encoding, variant dispatch and launch on the caller's stream.
+// All validation happens on the host before any CUDA call, so argument
+// errors are reported without touching the device.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <string>
+#include <tuple>
+
+#include "../../include/pa.h"
+#include "pa_internal.h"
+
+namespace {
+
+thread_local std::string g_last_error;
+std::atomic<uint64_t> g_launches{0};
+std::atomic<int32_t> g_tune_max_ctas{0};
+std::atomic<int32_t> g_tune_min_tiles{0};
+thread_local void* g_prof_before = nullptr;
+thread_local void* g_prof_after = nullptr;
+
+constexpr int kDefaultMinTiles = 4;
+constexpr int kMaxCtasPerSm = 2;
+constexpr int kWarpsPerCta = 4;
+constexpr int64_t kMaxBatch = 4096;
+
+pa_status fail(pa_status code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return code;
+}
+
+pa_status ok() {
+  g_last_error.clear();
+  return PA_OK;
+}
+
+pa_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(PA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+int elem_size(int32_t dt) {
+  switch (dt) {
+    case PA_F16:
+    case PA_BF16: return 2;
+    case PA_FP8_E4M3: return 1;
+    case PA_I32: return 4;
+    case PA_I64: return 8;
+    default: return 0;
+  }
+}
+
+bool is_contiguous(const pa_tensor* t) {
+  int64_t expect = 1;
+  for (int i = t->ndim - 1; i >= 0; --i) {
+    if (t->shape[i] != 1 && t->strides[i] != expect) return false;
+    expect *= t->shape[i];
+  }
+  return true;
+}
+
+int64_t numel(const pa_tensor* t) {
+  int64_t n = 1;
+  for (int i = 0; i < t->ndim; ++i) n *= t->shape[i];
+  return n;
+}
+
+// Byte span [lo, hi) covered by a tensor (assumes non-negative strides).
+void span(const pa_tensor* t, uintptr_t* lo, uintptr_t* hi) {
+  int64_t last = 0;
+  for (int i = 0; i < t->ndim; ++i) last += (t->shape[i] - 1) * t->strides[i];
+  *lo = reinterpret_cast<uintptr_t>(t->data);
+  *hi = *lo + static_cast<uintptr_t>((last + 1) * elem_size(t->dtype));
+}
+
+bool overlaps(const pa_tensor* a, const pa_tensor* b) {
+  if (numel(a) == 0 || numel(b) == 0) return false;
+  uintptr_t alo, ahi, blo, bhi;
+  span(a, &alo, &ahi);
+  span(b, &blo, &bhi);
+  return alo < bhi && blo < ahi;
+}
+
+pa_status check_tensor(const pa_tensor* t, const char* name, int ndim) {
+  if (!t) return fail(PA_ERR_INVALID_ARG, "%s: null tensor", name);
+  if (t->ndim != ndim) return fail(PA_ERR_INVALID_ARG, "%s: expected %d dims, got %d", name, ndim, t->ndim);
+  if (elem_size(t->dtype) == 0) return fail(PA_ERR_INVALID_ARG, "%s: bad dtype %d", name, t->dtype);
+  for (int i = 0; i < ndim; ++i) {
+    if (t->shape[i] < 0) return fail(PA_ERR_INVALID_ARG, "%s: negative extent", name);
+    if (t->strides[i] < 0) return fail(PA_ERR_LAYOUT, "%s: negative stride", name);
+  }
+  if (!t->data && numel(t) > 0) return fail(PA_ERR_INVALID_ARG, "%s: null data", name);
+  return PA_OK;
+}
+
+// ------------------------------------------------------------ device state
+
+struct DeviceState {
+  bool init = false;
+  int num_sms = 0;
+  int32_t* err_word = nullptr;
+  void* user_ws = nullptr;
+  size_t user_ws_bytes = 0;
+  std::map<uintptr_t, std::pair<void*, size_t>> lib_ws;  // per stream
+  std::map<std::tuple<int, int, int, int, int>, int> occupancy;
+};
+
+std::mutex g_mu;
+std::map<int, DeviceState> g_dev;
+
+pa_status device_state(DeviceState** out, int* dev_out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  DeviceState& st = g_dev[dev];
+  if (!st.init) {
+    e = cudaDeviceGetAttribute(&st.num_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+    e = pa::device_error_word(&st.err_word);
+    if (e != cudaSuccess) return cuda_fail(e, "device error word");
+    st.init = true;
+  }
+  *out = &st;
+  if (dev_out) *dev_out = dev;
+  return PA_OK;
+}
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+size_t workspace_bytes(int64_t B, int Hkv, int G, int D, int64_t workers) {
+  const size_t ctrl = round_up(static_cast<size_t>(B + 3) * sizeof(int32_t), 256);
+  const size_t slots = static_cast<size_t>(B * Hkv + workers);
+  return ctrl + slots * static_cast<size_t>(G) * (D + 2) * sizeof(float);
+}
+
+// ------------------------------------------------------------ TMA descriptors
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 2-D view of a cache [NB * Hkv * bs rows, D]: box of 16 rows x 128 bytes,
+// 128-byte swizzle.
+pa_status make_cache_map(CUtensorMap* map, const void* base, int64_t rows, int D, int elt) {
+  auto fn = encode_fn();
+  if (!fn) return fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(D) * elt};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / elt), static_cast<cuuint32_t>(pa::kTile)};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, elt == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_UINT16,
+                  2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  return PA_OK;
+}
+
+// ------------------------------------------------------------ dispatch glue
+
+cudaError_t variant_of(int ct, int qt, int D, int nt, pa::DecodeVariant* v) {
+  if (ct == pa::kE4M3) return pa::decode_variant_fp8(qt, D, nt, v);
+  if (ct == pa::kBF16) return pa::decode_variant_bf16(D, nt, v);
+  return pa::decode_variant_f16(D, nt, v);
+}
+
+cudaError_t prepare_of(int ct, int qt, int D, int nt, int smem, int* ctas) {
+  if (ct == pa::kE4M3) return pa::decode_prepare_fp8(qt, D, nt, smem, ctas);
+  if (ct == pa::kBF16) return pa::decode_prepare_bf16(D, nt, smem, ctas);
+  return pa::decode_prepare_f16(D, nt, smem, ctas);
+}
+
+cudaError_t launch_of(int ct, int qt, int D, int nt, const CUtensorMap& tk, const CUtensorMap& tv,
+                      const pa::DecodeArgs& a, int grid, int smem, cudaStream_t s, bool pdl) {
+  if (ct == pa::kE4M3) return pa::decode_launch_fp8(qt, D, nt, tk, tv, a, grid, smem, s, pdl);
+  if (ct == pa::kBF16) return pa::decode_launch_bf16(D, nt, tk, tv, a, grid, smem, s, pdl);
+  return pa::decode_launch_f16(D, nt, tk, tv, a, grid, smem, s, pdl);
+}
+
+struct DecodePlan {
+  int ct, qt, nt, G;
+  int smem, grid, workers, min_tiles;
+  pa::DecodeVariant var;
+};
+
+// Shape validation shared by pa_decode and the workspace query.
+pa_status check_heads(int64_t Hq, int64_t Hkv, int64_t D) {
+  if (Hkv <= 0 || Hq <= 0) return fail(PA_ERR_INVALID_ARG, "head counts must be positive");
+  if (Hq % Hkv) return fail(PA_ERR_INVALID_ARG, "num_q_heads %% num_kv_heads != 0");
+  if (Hq / Hkv > 16) return fail(PA_ERR_UNSUPPORTED, "GQA group %lld > 16", (long long)(Hq / Hkv));
+  if (D != 64 && D != 128 && D != 256) return fail(PA_ERR_UNSUPPORTED, "head_dim %lld", (long long)D);
+  return PA_OK;
+}
+
+pa_status plan_decode(DeviceState* st, int dev, int ct, int qt, int64_t B, int Hq, int Hkv,
+                      int D, DecodePlan* p) {
+  p->ct = ct;
+  p->qt = qt;
+  p->G = Hq / Hkv;
+  p->nt = p->G > 8 ? 2 : 1;
+  cudaError_t e = variant_of(ct, qt, D, p->nt, &p->var);
+  if (e != cudaSuccess) return fail(PA_ERR_UNSUPPORTED, "no decode kernel for this dtype/head_dim");
+  const size_t smem = 1024 + p->var.ring_bytes + p->var.warps * p->var.stages * 8 +
+                      static_cast<size_t>(2 * B + 1) * sizeof(int32_t);
+  p->smem = static_cast<int>(round_up(smem, 1024));
+  auto key = std::make_tuple(ct, qt, D, p->nt, p->smem);
+  auto it = st->occupancy.find(key);
+  int ctas = 0;
+  if (it == st->occupancy.end()) {
+    e = prepare_of(ct, qt, D, p->nt, p->smem, &ctas);
+    if (e != cudaSuccess) return cuda_fail(e, "decode kernel setup");
+    st->occupancy[key] = ctas;
+  } else {
+    ctas = it->second;
+  }
+  (void)dev;
+  if (ctas < 1) return fail(PA_ERR_UNSUPPORTED, "decode kernel does not fit on an SM (smem %d)", p->smem);
+  if (ctas > kMaxCtasPerSm) ctas = kMaxCtasPerSm;
+  p->grid = st->num_sms * ctas;
+  const int cap = g_tune_max_ctas.load();
+  if (cap > 0 && p->grid > cap) p->grid = cap;
+  p->workers = p->grid * p->var.warps;
+  const int mt = g_tune_min_tiles.load();
+  p->min_tiles = mt > 0 ? mt : kDefaultMinTiles;
+  return PA_OK;
+}
+
+pa_status get_workspace(DeviceState* st, cudaStream_t stream, size_t need, void** ws) {
+  if (st->user_ws) {
+    if (st->user_ws_bytes < need)
+      return fail(PA_ERR_WORKSPACE, "workspace too small: %zu bytes set, %zu needed",
+                  st->user_ws_bytes, need);
+    *ws = st->user_ws;
+    return PA_OK;
+  }
+  auto& slot = st->lib_ws[reinterpret_cast<uintptr_t>(stream)];
+  if (slot.second >= need) {
+    *ws = slot.first;
+    return PA_OK;
+  }
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  cudaError_t e = cudaStreamIsCapturing(stream, &cap);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamIsCapturing");
+  if (cap != cudaStreamCaptureStatusNone)
+    return fail(PA_ERR_WORKSPACE,
+                "decode workspace must grow to %zu bytes during stream capture; run one step "
+                "before capturing or call pa_set_workspace",
+                need);
+  if (slot.first) {
+    e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+    cudaFree(slot.first);
+    slot = {nullptr, 0};
+  }
+  const size_t bytes = round_up(need + need / 4, 1 << 20);
+  void* p = nullptr;
+  e = cudaMalloc(&p, bytes);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(workspace)");
+  slot = {p, bytes};
+  *ws = p;
+  return PA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* pa_last_error(void) { return g_last_error.c_str(); }
+
+int32_t pa_version(void) { return 10000; }
+
+uint64_t pa_launch_count(void) { return g_launches.load(); }
+
+pa_status pa_set_decode_tuning(int32_t max_ctas, int32_t min_tiles) {
+  if (max_ctas < 0 || min_tiles < 0) return fail(PA_ERR_INVALID_ARG, "negative tuning value");
+  g_tune_max_ctas = max_ctas;
+  g_tune_min_tiles = min_tiles;
+  return ok();
+}
+
+pa_status pa_profile_events(void* ev_before, void* ev_after) {
+  if ((ev_before == nullptr) != (ev_after == nullptr))
+    return fail(PA_ERR_INVALID_ARG, "give both events or neither");
+  g_prof_before = ev_before;
+  g_prof_after = ev_after;
+  return ok();
+}
+
+pa_status pa_set_workspace(void* ptr, size_t bytes) {
+  if (ptr && (reinterpret_cast<uintptr_t>(ptr) % 256))
+    return fail(PA_ERR_LAYOUT, "workspace must be 256-byte aligned");
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceState* st;
+  pa_status s = device_state(&st, nullptr);
+  if (s) return s;
+  st->user_ws = ptr;
+  st->user_ws_bytes = ptr ? bytes : 0;
+  return ok();
+}
+
+pa_status pa_decode_workspace_size(int64_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+                                   int32_t head_dim, size_t* bytes) {
+  if (!bytes) return fail(PA_ERR_INVALID_ARG, "bytes is null");
+  if (batch < 0 || batch > kMaxBatch) return fail(PA_ERR_UNSUPPORTED, "batch %lld", (long long)batch);
+  pa_status s = check_heads(num_q_heads, num_kv_heads, head_dim);
+  if (s) return s;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceState* st;
+  s = device_state(&st, nullptr);
+  if (s) return s;
+  const int64_t workers = static_cast<int64_t>(st->num_sms) * kMaxCtasPerSm * kWarpsPerCta;
+  *bytes = workspace_bytes(batch, num_kv_heads, num_q_heads / num_kv_heads, head_dim, workers);
+  return ok();
+}
+
+pa_status pa_check_device_error(int32_t* bits, pa_stream stream) {
+  if (!bits) return fail(PA_ERR_INVALID_ARG, "bits is null");
+  DeviceState* st;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    pa_status s = device_state(&st, nullptr);
+    if (s) return s;
+  }
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  int32_t v = 0;
+  cudaError_t e = cudaMemcpyAsync(&v, st->err_word, sizeof(v), cudaMemcpyDeviceToHost, cs);
+  if (e == cudaSuccess) e = cudaMemsetAsync(st->err_word, 0, sizeof(int32_t), cs);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(cs);
+  if (e != cudaSuccess) return cuda_fail(e, "reading the device error word");
+  *bits = v;
+  return ok();
+}
+
+pa_status pa_reshape_and_cache(const pa_tensor* k, const pa_tensor* v, const pa_tensor* key_cache,
+                               const pa_tensor* value_cache, const pa_tensor* slot_mapping,
+                               int32_t kv_dtype, float k_scale, float v_scale, pa_stream stream) {
+  pa_status s;
+  if ((s = check_tensor(k, "k", 3)) || (s = check_tensor(v, "v", 3)) ||
+      (s = check_tensor(key_cache, "key_cache", 4)) ||
+      (s = check_tensor(value_cache, "value_cache", 4)) ||
+      (s = check_tensor(slot_mapping, "slot_mapping", 1)))
+    return s;
+  if (k->dtype != PA_F16 && k->dtype != PA_BF16)
+    return fail(PA_ERR_UNSUPPORTED, "k must be f16 or bf16");
+  if (v->dtype != k->dtype) return fail(PA_ERR_INVALID_ARG, "k and v dtypes differ");
+  for (int i = 0; i < 3; ++i)
+    if (k->shape[i] != v->shape[i]) return fail(PA_ERR_INVALID_ARG, "k and v shapes differ");
+  const int64_t T = k->shape[0], H = k->shape[1], D = k->shape[2];
+  if (kv_dtype != PA_KV_AUTO && kv_dtype != PA_KV_FP8_E4M3)
+    return fail(PA_ERR_INVALID_ARG, "bad kv_dtype %d", kv_dtype);
+  const bool fp8 = kv_dtype == PA_KV_FP8_E4M3;
+  const int32_t cdt = fp8 ? PA_FP8_E4M3 : k->dtype;
+  if (key_cache->dtype != cdt || value_cache->dtype != cdt)
+    return fail(PA_ERR_INVALID_ARG, "cache dtype does not match kv_dtype");
+  for (int i = 0; i < 4; ++i)
+    if (key_cache->shape[i] != value_cache->shape[i])
+      return fail(PA_ERR_INVALID_ARG, "key and value cache shapes differ");
+  if (key_cache->shape[1] != H || key_cache->shape[3] != D)
+    return fail(PA_ERR_INVALID_ARG, "cache [NB, Hkv, bs, D] does not match k [T, Hkv, D]");
+  if (slot_mapping->dtype != PA_I64 || slot_mapping->shape[0] != T)
+    return fail(PA_ERR_INVALID_ARG, "slot_mapping must be int64 [T]");
+  if (D % 8) return fail(PA_ERR_UNSUPPORTED, "head_dim must be a multiple of 8");
+  if (!is_contiguous(key_cache) || !is_contiguous(value_cache) || !is_contiguous(slot_mapping))
+    return fail(PA_ERR_LAYOUT, "caches and slot_mapping must be contiguous");
+  for (const pa_tensor* x : {k, v}) {
+    if (x->strides[2] != 1 || (H > 1 && x->strides[1] != D))
+      return fail(PA_ERR_LAYOUT, "k/v rows [Hkv, D] must be contiguous");
+    if ((reinterpret_cast<uintptr_t>(x->data) % 16) || ((x->strides[0] * 2) % 16))
+      return fail(PA_ERR_LAYOUT, "k/v rows must be 16-byte aligned");
+  }
+  if ((reinterpret_cast<uintptr_t>(key_cache->data) % 16) ||
+      (reinterpret_cast<uintptr_t>(value_cache->data) % 16))
+    return fail(PA_ERR_LAYOUT, "caches must be 16-byte aligned");
+  if (fp8 && !(std::isfinite(k_scale) && std::isfinite(v_scale) && k_scale > 0 && v_scale > 0))
+    return fail(PA_ERR_INVALID_ARG, "fp8 scales must be finite and positive");
+  if (key_cache->data == value_cache->data && numel(key_cache) > 0)
+    return fail(PA_ERR_INVALID_ARG, "key and value caches alias");
+  if (T > (int64_t(1) << 30) || H > 65535) return fail(PA_ERR_UNSUPPORTED, "too many tokens/heads");
+  if (T == 0 || H == 0) return ok();
+
+  DeviceState* st;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if ((s = device_state(&st, nullptr))) return s;
+  }
+  pa::ReshapeArgs a;
+  a.k = k->data;
+  a.v = v->data;
+  a.kc = key_cache->data;
+  a.vc = value_cache->data;
+  a.slots = static_cast<const int64_t*>(slot_mapping->data);
+  a.err = st->err_word;
+  a.k_stride_t = k->strides[0];
+  a.k_stride_h = D;
+  a.v_stride_t = v->strides[0];
+  a.v_stride_h = D;
+  a.T = static_cast<int>(T);
+  a.H = static_cast<int>(H);
+  a.D = static_cast<int>(D);
+  a.bs = static_cast<int>(key_cache->shape[2]);
+  a.NB = key_cache->shape[0];
+  a.k_scale = k_scale;
+  a.v_scale = v_scale;
+  cudaError_t e = pa::reshape_launch(k->dtype, fp8, a, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "reshape_and_cache launch");
+  g_launches += 1;
+  return ok();
+}
+
+pa_status pa_decode(const pa_tensor* out, const pa_tensor* q, const pa_tensor* key_cache,
+                    const pa_tensor* value_cache, const pa_tensor* block_tables,
+                    const pa_tensor* seq_lens, int32_t num_kv_heads, float scale,
+                    int32_t block_size, int32_t window, int32_t kv_dtype, float k_scale,
+                    float v_scale, pa_stream stream) {
+  pa_status s;
+  if ((s = check_tensor(out, "out", 3)) || (s = check_tensor(q, "q", 3)) ||
+      (s = check_tensor(key_cache, "key_cache", 4)) ||
+      (s = check_tensor(value_cache, "value_cache", 4)) ||
+      (s = check_tensor(block_tables, "block_tables", 2)) ||
+      (s = check_tensor(seq_lens, "seq_lens", 1)))
+    return s;
+  if (q->dtype != PA_F16 && q->dtype != PA_BF16) return fail(PA_ERR_UNSUPPORTED, "q must be f16 or bf16");
+  if (out->dtype != q->dtype) return fail(PA_ERR_INVALID_ARG, "out dtype must equal q dtype");
+  const int64_t B = q->shape[0], Hq = q->shape[1], D = q->shape[2];
+  for (int i = 0; i < 3; ++i)
+    if (out->shape[i] != q->shape[i]) return fail(PA_ERR_INVALID_ARG, "out shape != q shape");
+  if (kv_dtype != PA_KV_AUTO && kv_dtype != PA_KV_FP8_E4M3)
+    return fail(PA_ERR_INVALID_ARG, "bad kv_dtype %d", kv_dtype);
+  const bool fp8 = kv_dtype == PA_KV_FP8_E4M3;
+  const int32_t cdt = fp8 ? PA_FP8_E4M3 : q->dtype;
+  if (key_cache->dtype != cdt || value_cache->dtype != cdt)
+    return fail(PA_ERR_INVALID_ARG, "cache dtype does not match q dtype / kv_dtype");
+  for (int i = 0; i < 4; ++i)
+    if (key_cache->shape[i] != value_cache->shape[i])
+      return fail(PA_ERR_INVALID_ARG, "key and value cache shapes differ");
+  const int64_t NB = key_cache->shape[0], Hkv = key_cache->shape[1];
+  if (num_kv_heads != Hkv) return fail(PA_ERR_INVALID_ARG, "num_kv_heads != key_cache.shape[1]");
+  if (block_size != key_cache->shape[2]) return fail(PA_ERR_INVALID_ARG, "block_size != key_cache.shape[2]");
+  if (key_cache->shape[3] != D) return fail(PA_ERR_INVALID_ARG, "cache head_dim != q head_dim");
+  if ((s = check_heads(Hq, Hkv, D))) return s;
+  if (fp8 && D == 64) return fail(PA_ERR_UNSUPPORTED, "fp8 caches need head_dim 128 or 256");
+  if (block_size <= 0 || block_size % 16 || block_size > 1024)
+    return fail(PA_ERR_UNSUPPORTED, "block_size must be a multiple of 16 in [16, 1024]");
+  if (block_tables->dtype != PA_I32 || seq_lens->dtype != PA_I32)
+    return fail(PA_ERR_INVALID_ARG, "block_tables and seq_lens must be int32");
+  if (block_tables->shape[0] != B || seq_lens->shape[0] != B)
+    return fail(PA_ERR_INVALID_ARG, "block_tables / seq_lens batch != q batch");
+  const int64_t MB = block_tables->shape[1];
+  if (B > kMaxBatch) return fail(PA_ERR_UNSUPPORTED, "batch %lld > %lld", (long long)B, (long long)kMaxBatch);
+  if (!is_contiguous(out) || !is_contiguous(q) || !is_contiguous(key_cache) ||
+      !is_contiguous(value_cache) || !is_contiguous(block_tables) || !is_contiguous(seq_lens))
+    return fail(PA_ERR_LAYOUT, "pa_decode needs contiguous tensors");
+  for (const pa_tensor* x : {key_cache, value_cache, q, out})
+    if (reinterpret_cast<uintptr_t>(x->data) % 16)
+      return fail(PA_ERR_LAYOUT, "q, out and caches must be 16-byte aligned");
+  if (!std::isfinite(scale)) return fail(PA_ERR_INVALID_ARG, "scale must be finite");
+  if (fp8 && !(std::isfinite(k_scale) && std::isfinite(v_scale) && k_scale > 0 && v_scale > 0))
+    return fail(PA_ERR_INVALID_ARG, "fp8 scales must be finite and positive");
+  // 32-bit index limits inside the kernels
+  if (NB * Hkv * block_size >= (int64_t(1) << 31) || MB * block_size >= (int64_t(1) << 31) ||
+      B * Hkv * (MB * block_size / 16 + 1) >= (int64_t(1) << 31) || B * MB >= (int64_t(1) << 31))
+    return fail(PA_ERR_UNSUPPORTED, "pool or tables exceed 32-bit indexing");
+  for (const pa_tensor* x : {q, key_cache, value_cache, block_tables, seq_lens})
+    if (overlaps(out, x)) return fail(PA_ERR_INVALID_ARG, "out overlaps an input");
+  if (B == 0) return ok();
+  if (MB == 0) return fail(PA_ERR_INVALID_ARG, "block_tables has no columns");
+  if (NB == 0) return fail(PA_ERR_INVALID_ARG, "empty block pool");
+
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  DeviceState* st;
+  int dev;
+  DecodePlan plan;
+  void* ws = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if ((s = device_state(&st, &dev))) return s;
+    const int ct = fp8 ? pa::kE4M3 : (q->dtype == PA_BF16 ? pa::kBF16 : pa::kF16);
+    if ((s = plan_decode(st, dev, ct, q->dtype, B, static_cast<int>(Hq), static_cast<int>(Hkv),
+                         static_cast<int>(D), &plan)))
+      return s;
+    const size_t need = workspace_bytes(B, static_cast<int>(Hkv), plan.G, static_cast<int>(D),
+                                        plan.workers);
+    if ((s = get_workspace(st, cs, need, &ws))) return s;
+  }
+  const int elt = fp8 ? 1 : 2;
+  CUtensorMap tk, tv;
+  if ((s = make_cache_map(&tk, key_cache->data, NB * Hkv * block_size, static_cast<int>(D), elt)) ||
+      (s = make_cache_map(&tv, value_cache->data, NB * Hkv * block_size, static_cast<int>(D), elt)))
+    return s;
+
+  const double log2e = 1.4426950408889634;
+  pa::DecodeArgs a;
+  a.q = q->data;
+  a.block_tables = static_cast<const int32_t*>(block_tables->data);
+  a.seq_lens = static_cast<const int32_t*>(seq_lens->data);
+  a.ctrl = static_cast<int32_t*>(ws);
+  a.part = reinterpret_cast<float*>(static_cast<char*>(ws) +
+                                    round_up(static_cast<size_t>(B + 3) * sizeof(int32_t), 256));
+  a.err = st->err_word;
+  a.B = static_cast<int>(B);
+  a.Hq = static_cast<int>(Hq);
+  a.Hkv = static_cast<int>(Hkv);
+  a.G = plan.G;
+  a.D = static_cast<int>(D);
+  a.bs = block_size;
+  a.MB = static_cast<int>(MB);
+  a.NB = static_cast<int>(NB);
+  a.window = window > 0 ? window : 0;
+  a.score_scale = static_cast<float>(static_cast<double>(scale) * log2e *
+                                     (fp8 ? static_cast<double>(k_scale) : 1.0));
+  a.v_scale = fp8 ? v_scale : 1.f;
+  a.min_tiles = plan.min_tiles;
+
+  const bool prof = g_prof_before && g_prof_after;
+  cudaError_t e;
+  if (prof && (e = cudaEventRecord(static_cast<cudaEvent_t>(g_prof_before), cs)) != cudaSuccess)
+    return cuda_fail(e, "profile event");
+  e = launch_of(plan.ct, plan.qt, static_cast<int>(D), plan.nt, tk, tv, a, plan.grid, plan.smem,
+                cs, !prof);
+  if (e != cudaSuccess) return cuda_fail(e, "decode kernel launch");
+  if (prof && (e = cudaEventRecord(static_cast<cudaEvent_t>(g_prof_after), cs)) != cudaSuccess)
+    return cuda_fail(e, "profile event");
+  pa::MergeArgs m;
+  m.out = out->data;
+  m.part = a.part;
+  m.ctrl = a.ctrl;
+  m.B = a.B;
+  m.Hq = a.Hq;
+  m.Hkv = a.Hkv;
+  m.G = a.G;
+  m.D = a.D;
+  e = pa::merge_launch(q->dtype, m, cs, !prof);
+  if (e != cudaSuccess) return cuda_fail(e, "merge kernel launch");
+  g_launches += 2;
+  return ok();
+}
+
+}  // extern "C"

@@ -1,0 +1,78 @@
+// Internal declarations shared by the C-ABI layer and the kernel translation
+// units. Host-only types; no kernel code here.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace pa {
+
+// Element type codes used inside the library (same values as the ABI enums).
+enum ElemType { kF16 = 0, kBF16 = 1, kE4M3 = 2 };
+
+constexpr int kTile = 16;  // tokens per pipeline tile (one mma m-tile)
+
+// Arguments of the persistent decode kernel (see decode.cuh).
+struct DecodeArgs {
+  const void* q;             // [B, Hq, D]
+  const int32_t* block_tables;  // [B, MB]
+  const int32_t* seq_lens;   // [B]
+  float* part;               // partial slots: [(B*Hkv + workers)][G][D + 2] fp32
+  int32_t* ctrl;             // [0] tiles per worker, [1] total tiles, [2..B+2] tile prefix
+  int32_t* err;              // device error word
+  int B, Hq, Hkv, G, D, bs, MB, NB, window;
+  float score_scale;         // scale * log2(e) (* k_scale for FP8)
+  float v_scale;             // FP8: applied to the partial outputs
+  int min_tiles;             // least tiles per worker warp
+};
+
+struct MergeArgs {
+  void* out;                 // [B, Hq, D], dtype of q
+  const float* part;
+  const int32_t* ctrl;
+  int B, Hq, Hkv, G, D;
+};
+
+struct ReshapeArgs {
+  const void* k;
+  const void* v;
+  void* kc;
+  void* vc;
+  const int64_t* slots;
+  int32_t* err;
+  int64_t k_stride_t, k_stride_h, v_stride_t, v_stride_h;  // elements
+  int T, H, D, bs;
+  int64_t NB;
+  float k_scale, v_scale;
+};
+
+// Kernel configuration chosen for a (cache type, q type, D, n-tiles) variant.
+struct DecodeVariant {
+  int warps;          // worker warps per CTA
+  int stages;         // pipeline stages per warp
+  int ring_bytes;     // shared memory for the K/V rings of one CTA
+};
+
+// Per-variant entry points, implemented in decode_<type>.cu.
+// Returns cudaErrorInvalidValue for an unsupported (D, NT) combination.
+cudaError_t decode_variant_f16(int D, int nt, DecodeVariant* v);
+cudaError_t decode_variant_bf16(int D, int nt, DecodeVariant* v);
+cudaError_t decode_variant_fp8(int qt, int D, int nt, DecodeVariant* v);
+cudaError_t decode_prepare_f16(int D, int nt, int smem_bytes, int* ctas_per_sm);
+cudaError_t decode_prepare_bf16(int D, int nt, int smem_bytes, int* ctas_per_sm);
+cudaError_t decode_prepare_fp8(int qt, int D, int nt, int smem_bytes, int* ctas_per_sm);
+cudaError_t decode_launch_f16(int D, int nt, const CUtensorMap& tk, const CUtensorMap& tv,
+                              const DecodeArgs& a, int grid, int smem, cudaStream_t s, bool pdl);
+cudaError_t decode_launch_bf16(int D, int nt, const CUtensorMap& tk, const CUtensorMap& tv,
+                               const DecodeArgs& a, int grid, int smem, cudaStream_t s, bool pdl);
+cudaError_t decode_launch_fp8(int qt, int D, int nt, const CUtensorMap& tk,
+                              const CUtensorMap& tv, const DecodeArgs& a, int grid, int smem,
+                              cudaStream_t s, bool pdl);
+
+// merge_reshape.cu
+cudaError_t merge_launch(int out_type, const MergeArgs& a, cudaStream_t s, bool pdl);
+cudaError_t reshape_launch(int src_type, bool fp8, const ReshapeArgs& a, cudaStream_t s);
+cudaError_t device_error_word(int32_t** ptr);  // address of this device's error word
+
+}  // namespace pa

@@ -1,0 +1,101 @@
+"""Shared helpers for the GPU parity tests.
+
+The product side runs the library's kernels; the oracle side runs the fp64 C
+oracle on host copies of the generator's inputs, taken before the product
+writes anything, so no oracle input ever comes from the CUDA path.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import numpy as np
+import torch
+
+import oracle
+import paged_kv_cache_267_gb300 as pa
+from workloads import generate
+from workloads.gen import E4M3_NAN
+
+MAX_ABS_TOL = 1e-2   # attention output tolerances (bf16/fp16 outputs vs fp64)
+MEAN_ABS_TOL = 1e-3
+
+
+@dataclass
+class Sides:
+    w: object
+    out: torch.Tensor          # product output (device)
+    kc: torch.Tensor           # product caches after the write path (device)
+    vc: torch.Tensor
+    ref: np.ndarray | None     # oracle output fp64
+    kc_ref: np.ndarray         # oracle caches after the write path (host)
+    vc_ref: np.ndarray
+
+
+def host_copy(t: torch.Tensor) -> np.ndarray:
+    t = t.detach().cpu().contiguous()
+    if t.dtype in (torch.float16, torch.bfloat16):
+        return t.view(torch.int16).numpy().view(np.uint16).copy()
+    return t.numpy().copy()
+
+
+def run_both(spec, device="cuda", pairs=None, run_oracle_decode=True, threads=None) -> Sides:
+    w = generate(spec, device=device)
+    s = w.spec
+    fp8 = s.kv_fp8
+    kv = "fp8" if fp8 else "auto"
+    # ---- oracle inputs first (host copies of generator output)
+    if fp8:
+        shape = (w.num_blocks, s.num_kv_heads, s.block_size, s.head_dim)
+        kc_ref = np.full(shape, E4M3_NAN, np.uint8)
+        vc_ref = np.full(shape, E4M3_NAN, np.uint8)
+        oracle.reshape_and_cache(w.k_hist.cpu(), w.v_hist.cpu(), kc_ref, vc_ref,
+                                 w.slot_hist.cpu().numpy(), s.dtype, "fp8", w.k_scale,
+                                 w.v_scale, threads=threads)
+    else:
+        kc_ref, vc_ref = host_copy(w.key_cache), host_copy(w.value_cache)
+    oracle.reshape_and_cache(w.k_new.cpu(), w.v_new.cpu(), kc_ref, vc_ref,
+                             w.slot_new.cpu().numpy(), s.dtype, "fp8" if fp8 else s.dtype,
+                             w.k_scale, w.v_scale, threads=threads)
+    # ---- product path
+    if fp8:
+        kc, vc = w.empty_fp8_cache()
+        pa.reshape_and_cache(w.k_hist, w.v_hist, kc, vc, w.slot_hist, kv, w.k_scale, w.v_scale)
+    else:
+        kc, vc = w.key_cache, w.value_cache
+    pa.reshape_and_cache(w.k_new, w.v_new, kc, vc, w.slot_new, kv, w.k_scale, w.v_scale)
+    bt = torch.from_numpy(w.block_tables).to(device)
+    sl = torch.from_numpy(w.seq_lens).to(device)
+    out = pa.decode(w.q, kc, vc, bt, sl, num_kv_heads=s.num_kv_heads, scale=s.softmax_scale,
+                    block_size=s.block_size, window=s.window, kv_dtype=kv, k_scale=w.k_scale,
+                    v_scale=w.v_scale)
+    torch.cuda.synchronize()
+    ref = None
+    if run_oracle_decode:
+        ref = oracle.decode(w.q.cpu(), kc_ref, vc_ref, w.block_tables, w.seq_lens,
+                            num_kv_heads=s.num_kv_heads, scale=s.softmax_scale,
+                            block_size=s.block_size, window=s.window, q_dtype=s.dtype,
+                            cache_dtype="fp8" if fp8 else s.dtype, k_scale=w.k_scale,
+                            v_scale=w.v_scale, pairs=pairs, threads=threads)
+    return Sides(w, out, kc, vc, ref, kc_ref, vc_ref)
+
+
+def out_f64(out: torch.Tensor) -> np.ndarray:
+    return out.detach().float().cpu().double().numpy()
+
+
+def assert_close(got: np.ndarray, ref: np.ndarray, pairs=None, what=""):
+    if pairs is not None:
+        idx = tuple(np.asarray(pairs).T)
+        got, ref = got[idx], ref[idx]
+    assert np.isfinite(got).all(), f"{what}: non-finite outputs"
+    err = np.abs(got - ref)
+    assert err.max() <= MAX_ABS_TOL, f"{what}: max abs err {err.max():.3e}"
+    assert err.mean() <= MEAN_ABS_TOL, f"{what}: mean abs err {err.mean():.3e}"
+    return float(err.max()), float(err.mean())
+
+
+def assert_caches_equal(sides: Sides, what=""):
+    kc = host_copy(sides.kc)
+    vc = host_copy(sides.vc)
+    assert np.array_equal(kc, sides.kc_ref), f"{what}: key cache differs from the oracle"
+    assert np.array_equal(vc, sides.vc_ref), f"{what}: value cache differs from the oracle"

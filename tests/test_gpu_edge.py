@@ -1,0 +1,217 @@
+"""GPU edge cases of pa_decode / pa_reshape_and_cache against the oracle.
+
+Ragged lengths around tile and block boundaries, empty sequences, every
+supported head_dim, block sizes 16/32/64, GQA groups 1..16, windows that cut
+inside a tile, FP8 caches with f16 and bf16 queries, forced worker layouts
+(one CTA for everything; one tile per worker), device-side error flags,
+caller-owned workspace, CUDA graph capture, and allocator-built layouts.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from conftest import have_gpu
+from pa_testutil import (assert_caches_equal, assert_close, host_copy, out_f64, run_both)
+from workloads import generate
+from workloads.configs import Spec
+
+pytestmark = [pytest.mark.gpu, pytest.mark.skipif(not have_gpu(), reason="needs a GPU")]
+
+RAGGED = (0, 1, 15, 16, 17, 31, 32, 33, 63, 64, 65, 100, 257, 300)
+
+
+def spec(**kw):
+    base = dict(name="edge", batch=len(RAGGED), num_q_heads=8, num_kv_heads=2, head_dim=128,
+                block_size=16, dtype="bf16", seq_lens=RAGGED, pool_factor=1.5, seed=4242)
+    base.update(kw)
+    if "seq_lens" in kw:
+        base["batch"] = len(kw["seq_lens"])
+    return Spec(**base)
+
+
+CASES = [
+    dict(dtype="f16", head_dim=64),
+    dict(dtype="bf16", head_dim=64, block_size=32),
+    dict(dtype="bf16", head_dim=128),
+    dict(dtype="f16", head_dim=128, block_size=64),
+    dict(dtype="bf16", head_dim=256),
+    dict(dtype="f16", head_dim=256, block_size=32),
+    dict(num_q_heads=2, num_kv_heads=2),                 # G = 1
+    dict(num_q_heads=4, num_kv_heads=2),                 # G = 2
+    dict(num_q_heads=6, num_kv_heads=2),                 # G = 3
+    dict(num_q_heads=16, num_kv_heads=2),                # G = 8
+    dict(num_q_heads=24, num_kv_heads=2),                # G = 12
+    dict(num_q_heads=32, num_kv_heads=2, head_dim=64),   # G = 16
+    dict(num_q_heads=16, num_kv_heads=1, head_dim=256),  # G = 16, D = 256
+    dict(window=1),
+    dict(window=16),
+    dict(window=40),
+    dict(window=100, block_size=32),
+    dict(window=1000),
+    dict(kv_fp8=True),
+    dict(kv_fp8=True, dtype="f16"),
+    dict(kv_fp8=True, head_dim=256, block_size=32, window=50),
+    dict(kv_fp8=True, num_q_heads=32, num_kv_heads=2, window=33),
+    dict(shared_prefix=32, seq_lens=(33, 40, 64, 100, 257), window=60),
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=lambda c: ",".join(f"{k}={v}" for k, v in c.items()))
+def test_edge_shapes(case, pa_lib):
+    s = spec(**case)
+    sides = run_both(s)
+    assert_caches_equal(sides, str(case))
+    assert_close(out_f64(sides.out), sides.ref, what=str(case))
+    # empty sequences give exact zeros
+    for b, L in enumerate(sides.w.seq_lens):
+        if L == 0:
+            assert (sides.out[b] == 0).all()
+    assert pa_lib.check_device_error() == 0
+
+
+@pytest.mark.parametrize("tuning", [(1, 0), (0, 1), (3, 2), (7, 5)])
+@pytest.mark.parametrize("case", [dict(), dict(kv_fp8=True, window=45),
+                                  dict(num_q_heads=24, num_kv_heads=2, block_size=32)])
+def test_forced_worker_layouts(tuning, case, pa_lib):
+    pa_lib.set_decode_tuning(*tuning)
+    try:
+        sides = run_both(spec(**case))
+    finally:
+        pa_lib.set_decode_tuning(0, 0)
+    assert_close(out_f64(sides.out), sides.ref, what=f"{tuning} {case}")
+
+
+def test_skewed_batch_with_many_partials(pa_lib):
+    s = spec(seq_lens=(20000, 3, 0, 700, 16, 4096, 1), num_q_heads=32, num_kv_heads=4,
+             window=5000)
+    pa_lib.set_decode_tuning(0, 1)
+    try:
+        sides = run_both(s)
+    finally:
+        pa_lib.set_decode_tuning(0, 0)
+    assert_close(out_f64(sides.out), sides.ref, what="skew")
+
+
+def test_bad_block_id_and_long_seq_are_flagged_not_faulted(pa_lib):
+    w = generate(spec(seq_lens=(40, 50)), device="cuda")
+    bt = torch.from_numpy(w.block_tables).cuda()
+    sl = torch.from_numpy(w.seq_lens).cuda()
+    s = w.spec
+    assert pa_lib.check_device_error() == 0
+    bt_bad = bt.clone()
+    bt_bad[0, 1] = w.num_blocks + 5
+    pa_lib.decode(w.q, w.key_cache, w.value_cache, bt_bad, sl, num_kv_heads=2,
+                  scale=s.softmax_scale, block_size=16)
+    assert pa_lib.check_device_error() & pa_lib.DEVERR_BLOCK_ID
+    assert pa_lib.check_device_error() == 0  # cleared by the read
+    bt_bad[0, 1] = -3
+    pa_lib.decode(w.q, w.key_cache, w.value_cache, bt_bad, sl, num_kv_heads=2,
+                  scale=s.softmax_scale, block_size=16)
+    assert pa_lib.check_device_error() & pa_lib.DEVERR_BLOCK_ID
+    sl_bad = sl.clone()
+    sl_bad[1] = w.max_blocks * 16 + 7
+    pa_lib.decode(w.q, w.key_cache, w.value_cache, bt, sl_bad, num_kv_heads=2,
+                  scale=s.softmax_scale, block_size=16)
+    assert pa_lib.check_device_error() & pa_lib.DEVERR_SEQ_LEN
+
+
+def test_validation_errors_on_device_tensors(pa_lib):
+    w = generate(spec(seq_lens=(10, 20)), device="cuda")
+    bt = torch.from_numpy(w.block_tables).cuda()
+    sl = torch.from_numpy(w.seq_lens).cuda()
+    kw = dict(num_kv_heads=2, scale=0.1, block_size=16)
+    with pytest.raises(pa_lib.PAError) as e:
+        pa_lib.decode(w.q, w.key_cache, w.value_cache, bt, sl, num_kv_heads=3, scale=0.1,
+                      block_size=16)
+    assert e.value.status == -1
+    with pytest.raises(pa_lib.PAError) as e:
+        pa_lib.decode(w.q, w.key_cache, w.value_cache, bt.long(), sl, **kw)
+    assert e.value.status == -1
+    with pytest.raises(pa_lib.PAError) as e:
+        pa_lib.decode(w.q, w.key_cache, w.value_cache, bt, sl, out=w.q, **kw)
+    assert e.value.status == -1  # out aliases q
+    qnc = w.q.transpose(0, 1).contiguous().transpose(0, 1)
+    with pytest.raises(pa_lib.PAError) as e:
+        pa_lib.decode(qnc, w.key_cache, w.value_cache, bt, sl, **kw)
+    assert e.value.status == -3
+    with pytest.raises(pa_lib.PAError) as e:
+        pa_lib.decode(w.q[:, :, :96].contiguous(), w.key_cache[..., :96].contiguous(),
+                      w.value_cache[..., :96].contiguous(), bt, sl, **kw)
+    assert e.value.status == -2
+
+
+def test_caller_owned_workspace(pa_lib):
+    s = spec(seq_lens=(500, 1, 77, 1000))
+    w = generate(s, device="cuda")
+    bt = torch.from_numpy(w.block_tables).cuda()
+    sl = torch.from_numpy(w.seq_lens).cuda()
+    kw = dict(num_kv_heads=2, scale=s.softmax_scale, block_size=16)
+    ref = pa_lib.decode(w.q, w.key_cache, w.value_cache, bt, sl, **kw)
+    n = pa_lib.workspace_size(4, 8, 2, 128)
+    buf = torch.empty(n, dtype=torch.uint8, device="cuda")
+    pa_lib.set_workspace(buf)
+    try:
+        got = pa_lib.decode(w.q, w.key_cache, w.value_cache, bt, sl, **kw)
+        torch.cuda.synchronize()
+        assert torch.equal(got.view(torch.int16), ref.view(torch.int16))
+        pa_lib.set_workspace(buf[:1024])
+        with pytest.raises(pa_lib.PAError) as e:
+            pa_lib.decode(w.q, w.key_cache, w.value_cache, bt, sl, **kw)
+        assert e.value.status == -6
+    finally:
+        pa_lib.set_workspace(None)
+
+
+def test_cuda_graph_replay_matches_eager(pa_lib):
+    s = spec(seq_lens=(300, 17, 1, 2000))
+    w = generate(s, device="cuda")
+    bt = torch.from_numpy(w.block_tables).cuda()
+    sl = torch.from_numpy(w.seq_lens).cuda()
+    kw = dict(num_kv_heads=2, scale=s.softmax_scale, block_size=16)
+    stream = torch.cuda.Stream()
+    out = torch.empty_like(w.q)
+    with torch.cuda.stream(stream):
+        pa_lib.reshape_and_cache(w.k_new, w.v_new, w.key_cache, w.value_cache, w.slot_new)
+        pa_lib.decode(w.q, w.key_cache, w.value_cache, bt, sl, out=out, **kw)
+    stream.synchronize()
+    eager = out.clone()
+    out.zero_()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        pa_lib.reshape_and_cache(w.k_new, w.v_new, w.key_cache, w.value_cache, w.slot_new)
+        pa_lib.decode(w.q, w.key_cache, w.value_cache, bt, sl, out=out, **kw)
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), eager.view(torch.int16))
+
+
+def test_allocator_built_layout_with_sharing_and_cow(pa_lib):
+    """Tables from the library's allocator: a shared prefix (fork), a
+    copy-on-write append on a shared partial block, then decode vs oracle."""
+    bs, Hkv, Hq, D = 16, 2, 8, 128
+    alloc = pa_lib.BlockAllocator(256, bs, seed=9)
+    root = alloc.add(40)                 # 3 blocks, last partial
+    seqs = [alloc.fork(root) for _ in range(4)]
+    cows = []
+    for i, sq in enumerate(seqs):
+        src, dst = alloc.append(sq, 10 * (i + 1))
+        cows.append((src, dst))
+    assert all(c[0] == alloc.table(root)[-1] for c in cows[:3])
+    tables, lens = alloc.fill_tables(seqs, max_blocks=8)
+    NB = 256
+    g = torch.Generator(device="cuda").manual_seed(5)
+    kc = torch.randn((NB, Hkv, bs, D), generator=g, device="cuda").to(torch.bfloat16)
+    vc = torch.randn((NB, Hkv, bs, D), generator=g, device="cuda").to(torch.bfloat16)
+    # the caller performs the copy-on-write copies the allocator reported
+    for src, dst in cows:
+        if src >= 0:
+            kc[dst].copy_(kc[src])
+            vc[dst].copy_(vc[src])
+    q = torch.randn((len(seqs), Hq, D), generator=g, device="cuda").to(torch.bfloat16)
+    out = pa_lib.decode(q, kc, vc, torch.from_numpy(tables).cuda(), torch.from_numpy(lens).cuda(),
+                        num_kv_heads=Hkv, scale=D ** -0.5, block_size=bs)
+    ref = oracle.decode(q.cpu(), host_copy(kc), host_copy(vc), tables, lens, num_kv_heads=Hkv,
+                        scale=D ** -0.5, block_size=bs, q_dtype="bf16", cache_dtype="bf16")
+    assert_close(out_f64(out), ref, what="allocator layout")
+    assert (lens == np.array([50, 60, 70, 80])).all()

@@ -1,0 +1,172 @@
+"""CPU checks of libpa: it builds, loads, exports every symbol include/pa.h
+declares, rejects bad arguments on the host before touching a device, and its
+host block allocator agrees exactly with the allocator model."""
+import ctypes
+import os
+import random
+import re
+
+import numpy as np
+import pytest
+
+from conftest import ROOT
+from oracle.alloc_model import BlockAllocatorModel, OutOfBlocks
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "pa.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(pa_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_every_declared_function_is_exported(pa_lib):
+    names = declared_functions()
+    assert len(names) >= 20
+    L = ctypes.CDLL(pa_lib.build.LIB_PATH)
+    missing = [n for n in names if not hasattr(L, n)]
+    assert not missing, missing
+
+
+def test_version_and_launch_count(pa_lib):
+    assert pa_lib.version() == 10000
+    assert pa_lib.launch_count() >= 0
+
+
+def _desc(pa, dtype, shape, data=0x1000):
+    d = pa.PaTensor()
+    d.data = data
+    d.dtype = dtype
+    d.ndim = len(shape)
+    st = 1
+    for i in reversed(range(len(shape))):
+        d.shape[i] = shape[i]
+        d.strides[i] = st
+        st *= shape[i]
+    return d
+
+
+def test_host_validation_rejects_bad_arguments_without_a_device(pa_lib):
+    pa = pa_lib
+    L = pa.lib()
+    B, Hq, Hkv, D, NB, bs, MB = 2, 8, 2, 128, 10, 16, 4
+    base = 0x10000000
+
+    def call(q=None, out=None, kc=None, vc=None, bt=None, sl=None, hkv=Hkv, bsz=bs, kv=0,
+             ks=1.0, vs=1.0):
+        q = q or _desc(pa, pa.PA_BF16, (B, Hq, D), base)
+        out = out or _desc(pa, pa.PA_BF16, (B, Hq, D), base + 0x100000)
+        kc = kc or _desc(pa, pa.PA_BF16, (NB, Hkv, bs, D), base + 0x200000)
+        vc = vc or _desc(pa, pa.PA_BF16, (NB, Hkv, bs, D), base + 0x400000)
+        bt = bt or _desc(pa, pa.PA_I32, (B, MB), base + 0x600000)
+        sl = sl or _desc(pa, pa.PA_I32, (B,), base + 0x700000)
+        args = [ctypes.byref(x) for x in (out, q, kc, vc, bt, sl)]
+        return L.pa_decode(*args, hkv, 0.1, bsz, 0, kv, ks, vs, None)
+
+    assert call(hkv=3) == -1                                      # num_kv_heads mismatch
+    assert call(bsz=32) == -1                                     # block_size mismatch
+    assert call(q=_desc(pa, pa.PA_BF16, (B, 12, D), base),
+                out=_desc(pa, pa.PA_BF16, (B, 12, D), base + 0x100000),
+                kc=_desc(pa, pa.PA_BF16, (NB, 5, bs, D), base + 0x200000),
+                vc=_desc(pa, pa.PA_BF16, (NB, 5, bs, D), base + 0x400000), hkv=5) == -1
+    assert call(q=_desc(pa, pa.PA_BF16, (B, 40, D), base),
+                out=_desc(pa, pa.PA_BF16, (B, 40, D), base + 0x100000)) == -2   # G = 20
+    assert call(q=_desc(pa, pa.PA_BF16, (B, Hq, 96), base),
+                out=_desc(pa, pa.PA_BF16, (B, Hq, 96), base + 0x100000),
+                kc=_desc(pa, pa.PA_BF16, (NB, Hkv, bs, 96), base + 0x200000),
+                vc=_desc(pa, pa.PA_BF16, (NB, Hkv, bs, 96), base + 0x400000)) == -2
+    assert call(out=_desc(pa, pa.PA_BF16, (B, Hq, D), base)) == -1    # out aliases q
+    assert call(kv=2) == -1                                        # cache not e4m3
+    assert call(kc=_desc(pa, pa.PA_FP8_E4M3, (NB, Hkv, bs, D), base + 0x200000),
+                vc=_desc(pa, pa.PA_FP8_E4M3, (NB, Hkv, bs, D), base + 0x400000), kv=2,
+                ks=0.0) == -1                                      # bad scale
+    assert call(kc=_desc(pa, pa.PA_BF16, (NB, Hkv, bs, D), base + 0x200002)) == -3  # misaligned
+    bad_bs = _desc(pa, pa.PA_BF16, (NB, Hkv, 24, D), base + 0x200000)
+    assert call(kc=bad_bs, vc=_desc(pa, pa.PA_BF16, (NB, Hkv, 24, D), base + 0x400000),
+                bsz=24) == -2
+    assert call(bt=_desc(pa, pa.PA_I64, (B, MB), base + 0x600000)) == -1
+    assert L.pa_decode(None, None, None, None, None, None, 2, 0.1, 16, 0, 0, 1.0, 1.0, None) == -1
+    assert "null" in pa.last_error()
+    # write path
+    k = _desc(pa, pa.PA_F16, (4, Hkv, D), base)
+    v = _desc(pa, pa.PA_F16, (4, Hkv, D), base + 0x10000)
+    kc = _desc(pa, pa.PA_F16, (NB, Hkv, bs, D), base + 0x200000)
+    vc = _desc(pa, pa.PA_F16, (NB, Hkv, bs, D), base + 0x400000)
+    sm = _desc(pa, pa.PA_I32, (4,), base + 0x600000)
+    assert L.pa_reshape_and_cache(*[ctypes.byref(x) for x in (k, v, kc, vc, sm)], 0, 1.0, 1.0,
+                                  None) == -1                      # slot_mapping must be int64
+    sm64 = _desc(pa, pa.PA_I64, (4,), base + 0x600000)
+    assert L.pa_reshape_and_cache(*[ctypes.byref(x) for x in (k, v, kc, vc, sm64)], 2, 1.0, 1.0,
+                                  None) == -1                      # fp8 requested, f16 cache
+    assert pa.lib().pa_set_decode_tuning(-1, 0) == -1
+    assert pa.lib().pa_profile_events(ctypes.c_void_p(1), None) == -1
+
+
+def _model_vs_lib(pa, seed):
+    rnd = random.Random(seed)
+    bs = rnd.choice([1, 8, 16, 32])
+    nb = rnd.randint(0, 150)
+    m = BlockAllocatorModel(nb, bs, seed=seed * 7 + 1)
+    a = pa.BlockAllocator(nb, bs, seed=seed * 7 + 1)
+    for _ in range(500):
+        op = rnd.random()
+        sids = sorted(m.seqs)
+        if op < 0.3 or not sids:
+            n = rnd.randint(0, 4 * bs)
+            try:
+                sm = m.add(n)
+            except OutOfBlocks:
+                with pytest.raises(pa.OutOfBlocks):
+                    a.add(n)
+                continue
+            assert a.add(n) == sm
+        elif op < 0.45:
+            src = rnd.choice(sids)
+            assert a.fork(src) == m.fork(src)
+        elif op < 0.75:
+            sid, n = rnd.choice(sids), rnd.randint(0, 3 * bs)
+            try:
+                pm = m.append(sid, n)
+            except OutOfBlocks:
+                with pytest.raises(pa.OutOfBlocks):
+                    a.append(sid, n)
+                continue
+            assert a.append(sid, n) == pm
+        elif op < 0.95:
+            sid = rnd.choice(sids)
+            m.free_seq(sid)
+            a.free(sid)
+        else:
+            assert a.reclaim() == m.reclaim()
+        for sid in m.seqs:
+            assert a.table(sid) == m.table(sid)
+            assert a.seq_len(sid) == m.seq_len(sid)
+        assert [a.refcount(b) for b in range(nb)] == m.ref
+        assert a.num_free() == m.num_free() and a.num_pending() == m.num_pending()
+    if m.seqs:
+        ids = sorted(m.seqs)
+        mb = max(len(m.table(s)) for s in ids) + 2
+        tables, lens = a.fill_tables(ids, mb)
+        for i, s in enumerate(ids):
+            t = m.table(s)
+            assert list(tables[i, :len(t)]) == t and (tables[i, len(t):] == -1).all()
+            assert lens[i] == m.seq_len(s)
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_allocator_matches_model_exactly(seed, pa_lib):
+    _model_vs_lib(pa_lib, seed)
+
+
+def test_allocator_errors(pa_lib):
+    a = pa_lib.BlockAllocator(4, 16, seed=0)
+    with pytest.raises(pa_lib.PAError) as e:
+        a.free(99)
+    assert e.value.status == -7
+    assert a.refcount(-1) == -1 and a.refcount(4) == -1
+    s = a.add(64)
+    with pytest.raises(pa_lib.OutOfBlocks):
+        a.add(1)
+    with pytest.raises(pa_lib.PAError):
+        a.fill_tables([s], 2)        # table wider than the matrix
+    t, lens = a.fill_tables([s], 4)
+    assert sorted(t[0]) == [0, 1, 2, 3] and lens[0] == 64
