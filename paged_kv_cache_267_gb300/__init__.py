@@ -57,7 +57,7 @@ def lib() -> ctypes.CDLL:
             "pa_decode": (st, [P, P, P, P, P, P, i32, f32, i32, i32, i32, f32, f32, vp]),
             "pa_decode_workspace_size": (st, [i64, i32, i32, i32, ctypes.POINTER(ctypes.c_size_t)]),
             "pa_set_workspace": (st, [vp, ctypes.c_size_t]),
-            "pa_set_decode_tuning": (st, [i32, i32]),
+            "pa_set_decode_tuning": (st, [i32, i32, i32, i32]),
             "pa_profile_events": (st, [vp, vp]),
             "pa_check_device_error": (st, [ctypes.POINTER(i32), vp]),
             "pa_launch_count": (ctypes.c_uint64, []),
@@ -170,12 +170,17 @@ def set_workspace(buf: torch.Tensor | None) -> None:
         _check(lib().pa_set_workspace(buf.data_ptr(), buf.numel() * buf.element_size()))
 
 
-def set_decode_tuning(max_ctas: int = 0, min_tiles: int = 0) -> None:
-    _check(lib().pa_set_decode_tuning(max_ctas, min_tiles))
+def set_decode_tuning(max_ctas: int = 0, min_tiles: int = 0, claim_tiles: int = 0,
+                      steal_slots: int = 0) -> None:
+    """0 keeps a default; steal_slots < 0 turns work stealing off."""
+    _check(lib().pa_set_decode_tuning(max_ctas, min_tiles, claim_tiles, steal_slots))
 
 
 def profile_events(before=None, after=None) -> None:
     """Record torch.cuda.Event `before`/`after` around the main decode kernel."""
+    for ev in (before, after):
+        if ev is not None and not ev.cuda_event:
+            ev.record()  # torch creates the CUDA event on its first record
     b = before.cuda_event if before is not None else None
     a = after.cuda_event if after is not None else None
     _check(lib().pa_profile_events(b, a))

@@ -1,24 +1,29 @@
 // Persistent paged-decode kernel for sm_103a.
 //
-// Work decomposition (balanced split-KV). Every (sequence b, KV head) pair owns
-// the 16-token tiles that cover its attended positions [start, L) — tiles never
-// straddle a physical block because block_size is a multiple of 16. All tiles
-// of all pairs form one flat index space (pair-major). Each worker warp takes
-// a contiguous range of `wt` tiles of it, so every warp moves the same number
-// of K/V bytes however skewed the sequence lengths are. A worker's range cut
-// at pair boundaries gives "segments"; each segment produces one partial
-// result (running max m, running sum l, unnormalised output) in partial slot
-// (pair index + worker index), which is unique because the walk through the
-// (pair, worker) grid is a monotone staircase. A small merge kernel combines
-// the partials of each pair by their log-sum-exp weights.
+// Work decomposition (balanced split-KV with work stealing). Every (sequence
+// b, KV head) pair owns the 16-token tiles that cover its attended positions
+// [start, L); tiles never straddle a physical block because block_size is a
+// multiple of 16. All tiles of all pairs form one flat index space
+// (pair-major). Each worker warp owns an equal contiguous range of it and
+// consumes the range front to back in small claimed windows, through an
+// atomic (head << 32 | tail) word. A warp that runs out steals the back half
+// (at most one claim window) of another warp's unclaimed tail, so warps on
+// SMs that get less bandwidth do not stretch the step. A contiguous run of
+// tiles cut at pair boundaries is a segment; each segment writes one partial
+// (running max m, running sum l, unnormalised output): an owner segment of
+// pair s by warp w into slot s + w (unique: the walk through the (pair,
+// warp) grid is a monotone staircase), a stolen segment into the thief's
+// own slots, linked into a per-pair list. Every slot is tagged with the
+// call's epoch, so stale workspace contents are never merged. A merge kernel
+// combines each pair's partials by their log-sum-exp weights.
 //
 // Data movement. Each warp owns a ring of STAGES shared-memory stages; one
 // stage holds the K tile and the V tile [16 rows x D] of one (block, KV head),
 // loaded by TMA boxes of [16 rows x 128 bytes] with the 128-byte swizzle, and
-// signalled on an mbarrier. Block ids are read 32 at a time per warp and
-// broadcast with shuffles. Each K/V byte of the step is loaded once and used
-// by all G query heads of its group. Blocks wholly outside the window are
-// never loaded ("vLLM 0.7.2深度解析" §2.3).
+// signalled on an mbarrier. Block ids are read 32 at a time per warp, the next
+// window prefetched, and broadcast with shuffles. Each K/V byte of the step
+// is loaded once and used by all G query heads of its group. Blocks wholly
+// outside the window are never loaded ("vLLM 0.7.2深度解析" §2.3).
 //
 // Math (per tile, per warp), on the tensor cores with fp32 accumulation:
 //   S^T[16 tok x 8 heads] = K[16 x D] . Q^T[D x 8]     (mma m16n8k16, M = tokens)
@@ -133,6 +138,10 @@ __device__ __forceinline__ int acc_dim(int mt, int g, int hi) {
   }
 }
 
+constexpr unsigned kFlagStart = 1, kFlagEnd = 2, kFlagStolen = 4;
+constexpr uint32_t kNoSlot = 0xffffffffu;
+constexpr int kStealRounds = 8;
+
 template <int CT, int QT, int D, int NT, int WARPS, int STAGES>
 __global__ void __launch_bounds__(WARPS * 32)
     paged_decode_kernel(const __grid_constant__ CUtensorMap tmK,
@@ -148,7 +157,8 @@ __global__ void __launch_bounds__(WARPS * 32)
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* gbase = smem_raw + (base - raw);
   const uint32_t bars = base + WARPS * Gm::RING_BYTES;
-  int* s_len = reinterpret_cast<int*>(gbase + WARPS * Gm::RING_BYTES + WARPS * STAGES * 8);
+  int* s_meta = reinterpret_cast<int*>(gbase + WARPS * Gm::RING_BYTES + WARPS * STAGES * 8);
+  int* s_len = s_meta + 2 * WARPS * STAGES;
   int* s_pref = s_len + a.B;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -195,38 +205,182 @@ __global__ void __launch_bounds__(WARPS * 32)
 
   const int total = a.Hkv * s_pref[a.B];
   const int nw = gridDim.x * WARPS;
-  int wt = (total + nw - 1) / nw;
-  if (wt < a.min_tiles) wt = a.min_tiles;
+  int ws = (total + nw - 1) / nw;
+  if (ws < a.min_tiles) ws = a.min_tiles;
   if (blockIdx.x == 0) {
     if (tid == 0) {
-      a.ctrl[0] = wt;
+      a.ctrl[0] = ws;
       a.ctrl[1] = total;
+      a.ctrl[2] = a.claim;
+      a.ctrl[3] = a.steal_slots;
     }
-    for (int b = tid; b <= a.B; b += blockDim.x) a.ctrl[2 + b] = s_pref[b];
+    for (int b = tid; b <= a.B; b += blockDim.x) a.ctrl[4 + b] = s_pref[b];
   }
   const int w = blockIdx.x * WARPS + warp;
-  const long long f0ll = static_cast<long long>(w) * wt;
-  if (f0ll >= total) return;
-  const int f0 = static_cast<int>(f0ll);
-  const int f1 = min(f0 + wt, total);
+  const int f0 = static_cast<int>(min(static_cast<long long>(w) * ws, static_cast<long long>(total)));
+  const int f1 = min(f0 + ws, total);
+  // publish this warp's range word, then its epoch (thieves check the epoch first)
+  if (lane == 0) {
+    a.words[w] = (static_cast<unsigned long long>(f0) << 32) | static_cast<unsigned>(f1);
+    __threadfence();
+    *reinterpret_cast<volatile uint32_t*>(a.wepoch + w) = a.epoch;
+  }
 
   const uint32_t ring = base + warp * Gm::RING_BYTES;
   const uint32_t wbars = bars + warp * STAGES * 8;
+  int* meta_f = s_meta + warp * 2 * STAGES;
+  int* meta_fl = meta_f + STAGES;
+  const int npairs = a.B * a.Hkv;
 
   // ---------------------------------------------------------------- producer
-  Cursor pc, cc;
-  cursor_locate(pc, f0, s_pref, a.B, a.Hkv);
-  cc = pc;
-  int id_b = -1, id_lb0 = 0, id_val = 0;
-  auto produce = [&](int slot) {
+  // Runs: the owner run (claimed window by window from this warp's word) and
+  // stolen runs. np = next flat tile to load, run_end = end of the current
+  // window (owner) or run (stolen).
+  Cursor pc;
+  pc.b = pc.kvh = pc.t = pc.nt = 0;
+  int phase = 0;  // 0 owner, 1 stealing, 2 done
+  int np = 0, run_end = 0;
+  bool run_first = false, owner_any = false;
+  unsigned long long pending = 0;  // lane 0: prefetched owner claim
+  int stolen_used = 0;             // stolen partial slots used (consumer side)
+  int steals = 0;                  // stolen runs taken (producer side)
+
+  auto owner_claim = [&]() -> unsigned long long {
+    unsigned long long r = 0;
+    if (lane == 0)
+      r = atomicAdd(a.words + w, static_cast<unsigned long long>(a.claim) << 32);
+    return r;
+  };
+  // first owner window
+  {
+    unsigned long long c = owner_claim();
+    c = __shfl_sync(FULL, c, 0);
+    const int h = static_cast<int>(c >> 32), t = static_cast<int>(c & 0xffffffffu);
+    if (h < t) {
+      np = h;
+      run_end = min(h + a.claim, t);
+      run_first = true;
+      pending = owner_claim();
+    } else {
+      phase = 1;
+    }
+  }
+
+  // steal: sets [np, run_end) to a stolen run and returns true, or false
+  auto steal = [&]() -> bool {
+    // Slots: a stolen run of at most `claim` tiles spans at most `claim` pairs.
+    if (steals >= a.steal_slots / a.claim) return false;
+    uint32_t seed = static_cast<uint32_t>(w) * 2654435761u;
+    for (int round = 0; round < kStealRounds; ++round) {
+      const int v = static_cast<int>((seed + static_cast<uint32_t>(round * 32 + lane) * 40503u) %
+                                     static_cast<uint32_t>(nw));
+      const uint32_t ep = *reinterpret_cast<volatile const uint32_t*>(a.wepoch + v);
+      __threadfence();
+      const unsigned long long wd = *reinterpret_cast<volatile const unsigned long long*>(a.words + v);
+      int rem = 0;
+      if (ep == a.epoch && v != w)
+        rem = static_cast<int>(wd & 0xffffffffu) - static_cast<int>(wd >> 32);
+      // best victim in this group of 32
+      int best = rem, bl = lane;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const int ob = __shfl_xor_sync(FULL, best, o), ol = __shfl_xor_sync(FULL, bl, o);
+        if (ob > best || (ob == best && ol < bl)) {
+          best = ob;
+          bl = ol;
+        }
+      }
+      if (best < 2) continue;
+      int lo = 0, hi = 0;
+      if (lane == bl) {
+        unsigned long long cur = wd;
+        for (int tries = 0; tries < 4; ++tries) {
+          const int h = static_cast<int>(cur >> 32), t = static_cast<int>(cur & 0xffffffffu);
+          if (t - h < 2) break;
+          const int take = min(a.claim, (t - h) >> 1);
+          const unsigned long long nv =
+              (static_cast<unsigned long long>(h) << 32) | static_cast<unsigned>(t - take);
+          const unsigned long long prev = atomicCAS(a.words + v, cur, nv);
+          if (prev == cur) {
+            lo = t - take;
+            hi = t;
+            break;
+          }
+          cur = prev;
+        }
+      }
+      lo = __shfl_sync(FULL, lo, bl);
+      hi = __shfl_sync(FULL, hi, bl);
+      if (hi > lo) {
+        np = lo;
+        run_end = hi;
+        run_first = true;
+        ++steals;
+        return true;
+      }
+    }
+    return false;
+  };
+
+  int id_b = -1, id_lb0 = 0, id_val = 0;      // current block-id window
+  int pf_b = -1, pf_lb0 = 0, pf_val = 0;      // prefetched next window
+  int produced = 0, consumed = 0;
+
+  // Produces the next tile into stage `slot`; false when no work is left.
+  auto produce = [&](int slot) -> bool {
+    unsigned flags = 0;
+    while (true) {
+      if (phase == 2) return false;
+      if (np < run_end) break;
+      if (phase == 0) {
+        const unsigned long long c = __shfl_sync(FULL, pending, 0);
+        const int h = static_cast<int>(c >> 32), t = static_cast<int>(c & 0xffffffffu);
+        if (h < t) {  // next owner window, contiguous with the previous one
+          np = h;
+          run_end = min(h + a.claim, t);
+          pending = owner_claim();
+          continue;
+        }
+        // the owner run ends with the last tile produced (not yet consumed)
+        if (owner_any && produced > consumed) meta_fl[(produced - 1) % STAGES] |= kFlagEnd;
+        phase = 1;
+      }
+      if (phase == 1 && !steal()) phase = 2;
+    }
+    const int f = np++;
+    const bool stolen = phase == 1;
+    if (run_first) {
+      flags |= kFlagStart;
+      cursor_locate(pc, f, s_pref, a.B, a.Hkv);
+      run_first = false;
+    } else {
+      cursor_next(pc, s_pref, a.B, a.Hkv);
+    }
+    if (stolen) {
+      flags |= kFlagStolen;
+      if (np == run_end) flags |= kFlagEnd;
+    } else {
+      owner_any = true;
+    }
     const int L = s_len[pc.b];
     const int pt = win_start(L, a.window) / kTile + pc.t;  // tile index in position space
     const int lb = (pt * kTile) / a.bs;
     if (pc.b != id_b || lb < id_lb0 || lb >= id_lb0 + 32) {
-      id_b = pc.b;
-      id_lb0 = lb;
-      const int e = lb + lane;
-      id_val = (e < a.MB) ? __ldg(a.block_tables + static_cast<size_t>(pc.b) * a.MB + e) : 0;
+      if (pc.b == pf_b && lb >= pf_lb0 && lb < pf_lb0 + 32) {
+        id_b = pf_b;
+        id_lb0 = pf_lb0;
+        id_val = pf_val;
+      } else {
+        id_b = pc.b;
+        id_lb0 = lb;
+        const int e = lb + lane;
+        id_val = (e < a.MB) ? __ldg(a.block_tables + static_cast<size_t>(pc.b) * a.MB + e) : 0;
+      }
+      // prefetch the following window of this sequence's table
+      pf_b = id_b;
+      pf_lb0 = id_lb0 + 32;
+      const int e2 = pf_lb0 + lane;
+      pf_val = (e2 < a.MB) ? __ldg(a.block_tables + static_cast<size_t>(pf_b) * a.MB + e2) : 0;
     }
     int phys = __shfl_sync(FULL, id_val, lb - id_lb0);
     if (static_cast<unsigned>(phys) >= static_cast<unsigned>(a.NB)) {
@@ -235,6 +389,8 @@ __global__ void __launch_bounds__(WARPS * 32)
     }
     const int row = (phys * a.Hkv + pc.kvh) * a.bs + (pt * kTile) % a.bs;
     if (lane == 0) {
+      meta_f[slot] = f;
+      meta_fl[slot] = static_cast<int>(flags);
       const uint32_t bar = wbars + 8 * slot;
       const uint32_t kd = ring + slot * Gm::STAGE_BYTES;
       mbar_arrive_expect_tx(bar, Gm::STAGE_BYTES);
@@ -244,12 +400,12 @@ __global__ void __launch_bounds__(WARPS * 32)
         tma_load_2d(kd + Gm::TILE_BYTES + j * 2048, &tmV, j * Gm::BOX_ELEMS, row, bar);
       }
     }
-    cursor_next(pc, s_pref, a.B, a.Hkv);
+    __syncwarp();
+    return true;
   };
 
-  int produced = 0, consumed = 0;
-  for (int f = f0; f < f1 && produced < STAGES; ++f) {
-    produce(produced % STAGES);
+  for (int i = 0; i < STAGES; ++i) {
+    if (!produce(produced % STAGES)) break;
     ++produced;
   }
 
@@ -259,11 +415,17 @@ __global__ void __launch_bounds__(WARPS * 32)
   float acc[MT][NT][4];
   float sc = a.score_scale;
   bool ok = true;
+  Cursor cc;
+  cc.b = cc.kvh = cc.t = cc.nt = 0;
 
-  for (int f = f0; f < f1; ++f) {
+  while (consumed < produced) {
     const int slot = consumed % STAGES;
     const uint32_t parity = (consumed / STAGES) & 1;
-    const bool seg_start = (f == f0) || (cc.t == 0);
+    const int f = meta_f[slot];
+    const unsigned flags = static_cast<unsigned>(meta_fl[slot]);
+    if (flags & kFlagStart) cursor_locate(cc, f, s_pref, a.B, a.Hkv);
+    else cursor_next(cc, s_pref, a.B, a.Hkv);
+    const bool seg_start = (flags & kFlagStart) || (cc.t == 0);
     if (seg_start) {
       // query fragments of this pair's G heads (B operand, k = head dim)
       const uint16_t* qg = reinterpret_cast<const uint16_t*>(a.q) +
@@ -463,16 +625,24 @@ __global__ void __launch_bounds__(WARPS * 32)
     }
     __syncwarp();
     ++consumed;
-    if (produced < f1 - f0) {  // refill the stage just consumed
-      produce(produced % STAGES);
-      ++produced;
-    }
+    // refill the stage just consumed (may also set the end flag of an earlier stage)
+    if (produce(produced % STAGES)) ++produced;
 
-    // ---- segment end: write the partial (m, l, unnormalised output)
-    const bool seg_end = (f == f1 - 1) || (cc.t == cc.nt - 1);
+    // ---- segment end: write the partial (m, l, unnormalised output). The
+    // flags were read before the refill; a late end mark always lands on a
+    // stage that has not been consumed yet.
+    const unsigned fl = flags;
+    const bool seg_end = (fl & kFlagEnd) || (cc.t == cc.nt - 1);
     if (seg_end) {
       const int pair = cc.b * a.Hkv + cc.kvh;
-      float* P = a.part + static_cast<size_t>(pair + w) * (a.G * (D + 2));
+      uint32_t pslot;
+      if (fl & kFlagStolen) {
+        pslot = static_cast<uint32_t>(npairs + nw + w * a.steal_slots + stolen_used);
+        ++stolen_used;
+      } else {
+        pslot = static_cast<uint32_t>(pair + w);
+      }
+      float* P = a.part + static_cast<size_t>(pslot) * (a.G * (D + 2));
       const float vs = kFp8 ? a.v_scale : 1.f;
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
@@ -497,8 +667,17 @@ __global__ void __launch_bounds__(WARPS * 32)
           }
         }
       }
+      if (lane == 0) {
+        a.tags[pslot] = a.epoch;
+        if (fl & kFlagStolen) {
+          const unsigned long long node = (static_cast<unsigned long long>(a.epoch) << 32) | pslot;
+          const unsigned long long old = atomicExch(a.heads + pair, node);
+          a.next[pslot] = (static_cast<uint32_t>(old >> 32) == a.epoch)
+                              ? static_cast<uint32_t>(old & 0xffffffffu)
+                              : kNoSlot;
+        }
+      }
     }
-    cursor_next(cc, s_pref, a.B, a.Hkv);
   }
 
   if (!ok) {

@@ -19,42 +19,118 @@ cudaError_t device_error_word(int32_t** ptr) {
 // ------------------------------------------------------------------ merge
 //
 // One CTA per (pair, q head of the group); each thread owns two head dims.
-// The workers that covered pair s are those whose tile range meets the pair's
-// range [F, F + nt) of the flat tile space; worker w wrote slot s + w. With
-// partial maxima m_w (log2 domain), sums l_w and unnormalised outputs o_w:
-//   out = sum_w 2^(m_w - M) o_w / sum_w 2^(m_w - M) l_w,  M = max_w m_w.
-// A pair with no tiles (seq_len 0) gets zeros.
+// The partials of pair s are the owner slots s + w of every warp w whose
+// static range meets the pair's tiles [F, F + nt) and that was written in this
+// call (tag == epoch), plus the pair's list of stolen slots. With partial
+// maxima m_p (log2 domain), sums l_p and unnormalised outputs o_p:
+//   out = sum_p 2^(m_p - M) o_p / sum_p 2^(m_p - M) l_p,  M = max_p m_p,
+// evaluated chunk by chunk with a running maximum so any number of partials
+// fits in shared memory. A pair with no tiles (seq_len 0) gets zeros.
+constexpr int kMergeChunk = 256;
+constexpr uint32_t kNoSlot = 0xffffffffu;
+
 template <int OT>
 __global__ void __launch_bounds__(128) merge_kernel(const MergeArgs a) {
+  __shared__ uint32_t s_slot[kMergeChunk];
+  __shared__ float s_fac[kMergeChunk];
+  __shared__ int s_n;
+  __shared__ float s_M, s_den, s_scale;
+  __shared__ uint32_t s_list;
   griddep_wait();
   const int s = blockIdx.x, h = blockIdx.y;
   const int b = s / a.Hkv, kvh = s - b * a.Hkv;
-  const int d = 2 * threadIdx.x;
-  if (d >= a.D) return;
+  const int tid = threadIdx.x;
+  const int d = 2 * tid;
   const size_t orow = (static_cast<size_t>(b) * a.Hq + kvh * a.G + h) * a.D + d;
-  const int wt = a.ctrl[0];
-  const int pb = a.ctrl[2 + b], nt = a.ctrl[3 + b] - pb;
+  const int ws = a.ctrl[0];
+  const int pb = a.ctrl[4 + b], nt = a.ctrl[5 + b] - pb;
+  float n0 = 0.f, n1 = 0.f;
   float r0 = 0.f, r1 = 0.f;
   if (nt > 0) {
     const int F = a.Hkv * pb + kvh * nt;
-    const int w0 = F / wt, w1 = (F + nt - 1) / wt;
+    const int w0 = F / ws, w1 = min((F + nt - 1) / ws, a.NW - 1);
     const size_t stride = static_cast<size_t>(a.G) * (a.D + 2);
-    const float* base = a.part + static_cast<size_t>(s) * stride;
     const int mo = a.G * a.D + h, lo = a.G * a.D + a.G + h;
-    float M = -INFINITY;
-    for (int w = w0; w <= w1; ++w) M = fmaxf(M, base[w * stride + mo]);
-    float n0 = 0.f, n1 = 0.f, den = 0.f;
-    for (int w = w0; w <= w1; ++w) {
-      const float* P = base + w * stride;
-      const float f = exp2f(P[mo] - M);
-      den += f * P[lo];
-      const float2 o = *reinterpret_cast<const float2*>(P + h * a.D + d);
-      n0 += f * o.x;
-      n1 += f * o.y;
+    if (tid == 0) {
+      s_M = -INFINITY;
+      s_den = 0.f;
+      const unsigned long long hd = a.heads[s];
+      s_list = (static_cast<uint32_t>(hd >> 32) == a.epoch) ? static_cast<uint32_t>(hd) : kNoSlot;
     }
+    int wcur = w0;
+    while (true) {
+      if (tid == 0) s_n = 0;
+      __syncthreads();
+      // owner slots of the next group of warps
+      const int na = min(w1 - wcur + 1, kMergeChunk);
+      for (int i = tid; i < na; i += blockDim.x) {
+        const uint32_t slot = static_cast<uint32_t>(s + wcur + i);
+        if (a.tags[slot] == a.epoch) s_slot[atomicAdd(&s_n, 1)] = slot;
+      }
+      wcur += max(na, 0);
+      __syncthreads();
+      // stolen slots from the pair's list
+      if (tid == 0) {
+        int n = s_n;
+        uint32_t cur = s_list;
+        while (cur != kNoSlot && n < kMergeChunk) {
+          s_slot[n++] = cur;
+          cur = a.next[cur];
+        }
+        s_list = cur;
+        s_n = n;
+      }
+      __syncthreads();
+      const int n = s_n;
+      const bool more = (wcur <= w1) || (s_list != kNoSlot);
+      if (n == 0) {
+        if (!more) break;
+        __syncthreads();
+        continue;
+      }
+      // chunk maximum, new running maximum and rescale of what came before
+      if (tid < 32) {
+        float mx = -INFINITY;
+        for (int i = tid; i < n; i += 32) mx = fmaxf(mx, a.part[s_slot[i] * stride + mo]);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        const float Mn = fmaxf(s_M, mx);
+        float den = 0.f;
+        for (int i = tid; i < n; i += 32) {
+          const float* P = a.part + s_slot[i] * stride;
+          const float fct = exp2f(P[mo] - Mn);
+          s_fac[i] = fct;
+          den += fct * P[lo];
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+        if (tid == 0) {
+          const float sc = exp2f(s_M - Mn);  // 0 on the first chunk
+          s_scale = sc;
+          s_den = s_den * sc + den;
+          s_M = Mn;
+        }
+      }
+      __syncthreads();
+      if (d < a.D) {
+        const float sc = s_scale;
+        n0 *= sc;
+        n1 *= sc;
+        for (int i = 0; i < n; ++i) {
+          const float2 o = *reinterpret_cast<const float2*>(a.part + s_slot[i] * stride +
+                                                            h * a.D + d);
+          n0 += s_fac[i] * o.x;
+          n1 += s_fac[i] * o.y;
+        }
+      }
+      __syncthreads();
+      if (!more) break;
+    }
+    const float den = s_den;
     r0 = n0 / den;
     r1 = n1 / den;
   }
+  if (d >= a.D) return;
   if constexpr (OT == kBF16) {
     *reinterpret_cast<__nv_bfloat162*>(reinterpret_cast<__nv_bfloat16*>(a.out) + orow) =
         __floats2bfloat162_rn(r0, r1);

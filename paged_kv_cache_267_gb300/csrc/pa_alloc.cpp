@@ -7,7 +7,7 @@
 #include <unordered_map>
 #include <vector>
 
-#include "../../include/pa.h"
+#include "pa.h"
 
 struct pa_alloc {
   int32_t num_blocks = 0;

@@ -16,7 +16,7 @@
 #include <string>
 #include <tuple>
 
-#include "../../include/pa.h"
+#include "pa.h"
 #include "pa_internal.h"
 
 namespace {
@@ -25,10 +25,14 @@ thread_local std::string g_last_error;
 std::atomic<uint64_t> g_launches{0};
 std::atomic<int32_t> g_tune_max_ctas{0};
 std::atomic<int32_t> g_tune_min_tiles{0};
+std::atomic<int32_t> g_tune_claim{0};
+std::atomic<int32_t> g_tune_steal_slots{0};
 thread_local void* g_prof_before = nullptr;
 thread_local void* g_prof_after = nullptr;
 
 constexpr int kDefaultMinTiles = 4;
+constexpr int kDefaultClaim = 4;        // tiles per owner claim / largest steal
+constexpr int kDefaultStealSlots = 16;  // partial slots per warp for stolen work
 constexpr int kMaxCtasPerSm = 2;
 constexpr int kWarpsPerCta = 4;
 constexpr int64_t kMaxBatch = 4096;
@@ -108,13 +112,18 @@ pa_status check_tensor(const pa_tensor* t, const char* name, int ndim) {
 
 // ------------------------------------------------------------ device state
 
+struct Workspace {
+  void* ptr = nullptr;
+  size_t bytes = 0;
+  uint32_t epoch = 0;  // last epoch used with this buffer (0: freshly zeroed)
+};
+
 struct DeviceState {
   bool init = false;
   int num_sms = 0;
   int32_t* err_word = nullptr;
-  void* user_ws = nullptr;
-  size_t user_ws_bytes = 0;
-  std::map<uintptr_t, std::pair<void*, size_t>> lib_ws;  // per stream
+  Workspace user_ws;                        // caller-owned (pa_set_workspace)
+  std::map<uintptr_t, Workspace> lib_ws;    // library-owned, one per stream
   std::map<std::tuple<int, int, int, int, int>, int> occupancy;
 };
 
@@ -140,10 +149,35 @@ pa_status device_state(DeviceState** out, int* dev_out) {
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-size_t workspace_bytes(int64_t B, int Hkv, int G, int D, int64_t workers) {
-  const size_t ctrl = round_up(static_cast<size_t>(B + 3) * sizeof(int32_t), 256);
-  const size_t slots = static_cast<size_t>(B * Hkv + workers);
-  return ctrl + slots * static_cast<size_t>(G) * (D + 2) * sizeof(float);
+// Section offsets of the decode workspace (layout described in pa_internal.h).
+struct WsLayout {
+  size_t ctrl, words, wepoch, heads, tags, next, part, total;
+};
+
+WsLayout ws_layout(int64_t B, int Hkv, int G, int D, int64_t workers, int steal_slots) {
+  const size_t S = static_cast<size_t>(B) * Hkv;
+  const size_t nslot = S + workers + static_cast<size_t>(workers) * steal_slots;
+  WsLayout L;
+  size_t o = 0;
+  L.ctrl = o;   o += round_up(static_cast<size_t>(B + 5) * sizeof(int32_t), 256);
+  L.words = o;  o += round_up(workers * sizeof(unsigned long long), 256);
+  L.wepoch = o; o += round_up(workers * sizeof(uint32_t), 256);
+  L.heads = o;  o += round_up(S * sizeof(unsigned long long), 256);
+  L.tags = o;   o += round_up(nslot * sizeof(uint32_t), 256);
+  L.next = o;   o += round_up(nslot * sizeof(uint32_t), 256);
+  L.part = o;   o += nslot * static_cast<size_t>(G) * (D + 2) * sizeof(float);
+  L.total = o;
+  return L;
+}
+
+int tuned_steal_slots() {
+  const int v = g_tune_steal_slots.load();
+  return v == 0 ? kDefaultStealSlots : (v < 0 ? 0 : v);
+}
+
+int tuned_claim() {
+  const int v = g_tune_claim.load();
+  return v > 0 ? v : kDefaultClaim;
 }
 
 // ------------------------------------------------------------ TMA descriptors
@@ -202,7 +236,7 @@ cudaError_t launch_of(int ct, int qt, int D, int nt, const CUtensorMap& tk, cons
 
 struct DecodePlan {
   int ct, qt, nt, G;
-  int smem, grid, workers, min_tiles;
+  int smem, grid, workers, min_tiles, claim, steal_slots;
   pa::DecodeVariant var;
 };
 
@@ -223,7 +257,7 @@ pa_status plan_decode(DeviceState* st, int dev, int ct, int qt, int64_t B, int H
   p->nt = p->G > 8 ? 2 : 1;
   cudaError_t e = variant_of(ct, qt, D, p->nt, &p->var);
   if (e != cudaSuccess) return fail(PA_ERR_UNSUPPORTED, "no decode kernel for this dtype/head_dim");
-  const size_t smem = 1024 + p->var.ring_bytes + p->var.warps * p->var.stages * 8 +
+  const size_t smem = 1024 + p->var.ring_bytes + p->var.warps * p->var.stages * (8 + 8) +
                       static_cast<size_t>(2 * B + 1) * sizeof(int32_t);
   p->smem = static_cast<int>(round_up(smem, 1024));
   auto key = std::make_tuple(ct, qt, D, p->nt, p->smem);
@@ -245,42 +279,55 @@ pa_status plan_decode(DeviceState* st, int dev, int ct, int qt, int64_t B, int H
   p->workers = p->grid * p->var.warps;
   const int mt = g_tune_min_tiles.load();
   p->min_tiles = mt > 0 ? mt : kDefaultMinTiles;
+  p->claim = tuned_claim();
+  p->steal_slots = tuned_steal_slots();
   return PA_OK;
 }
 
-pa_status get_workspace(DeviceState* st, cudaStream_t stream, size_t need, void** ws) {
-  if (st->user_ws) {
-    if (st->user_ws_bytes < need)
+// Picks the workspace for this call and the epoch that tags its writes.
+pa_status get_workspace(DeviceState* st, cudaStream_t stream, size_t need, void** ws,
+                        uint32_t* epoch) {
+  Workspace* w;
+  if (st->user_ws.ptr) {
+    if (st->user_ws.bytes < need)
       return fail(PA_ERR_WORKSPACE, "workspace too small: %zu bytes set, %zu needed",
-                  st->user_ws_bytes, need);
-    *ws = st->user_ws;
-    return PA_OK;
+                  st->user_ws.bytes, need);
+    w = &st->user_ws;
+  } else {
+    w = &st->lib_ws[reinterpret_cast<uintptr_t>(stream)];
+    if (w->bytes < need) {
+      cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+      cudaError_t e = cudaStreamIsCapturing(stream, &cap);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaStreamIsCapturing");
+      if (cap != cudaStreamCaptureStatusNone)
+        return fail(PA_ERR_WORKSPACE,
+                    "decode workspace must grow to %zu bytes during stream capture; run one "
+                    "step before capturing or call pa_set_workspace",
+                    need);
+      if (w->ptr) {
+        e = cudaStreamSynchronize(stream);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+        cudaFree(w->ptr);
+        *w = Workspace{};
+      }
+      const size_t bytes = round_up(need + need / 4, 1 << 20);
+      void* p = nullptr;
+      e = cudaMalloc(&p, bytes);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(workspace)");
+      e = cudaMemsetAsync(p, 0, bytes, stream);
+      if (e != cudaSuccess) {
+        cudaFree(p);
+        return cuda_fail(e, "cudaMemsetAsync(workspace)");
+      }
+      w->ptr = p;
+      w->bytes = bytes;
+      w->epoch = 0;
+    }
   }
-  auto& slot = st->lib_ws[reinterpret_cast<uintptr_t>(stream)];
-  if (slot.second >= need) {
-    *ws = slot.first;
-    return PA_OK;
-  }
-  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
-  cudaError_t e = cudaStreamIsCapturing(stream, &cap);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamIsCapturing");
-  if (cap != cudaStreamCaptureStatusNone)
-    return fail(PA_ERR_WORKSPACE,
-                "decode workspace must grow to %zu bytes during stream capture; run one step "
-                "before capturing or call pa_set_workspace",
-                need);
-  if (slot.first) {
-    e = cudaStreamSynchronize(stream);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
-    cudaFree(slot.first);
-    slot = {nullptr, 0};
-  }
-  const size_t bytes = round_up(need + need / 4, 1 << 20);
-  void* p = nullptr;
-  e = cudaMalloc(&p, bytes);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(workspace)");
-  slot = {p, bytes};
-  *ws = p;
+  // Epoch 0 marks never-written slots of a zeroed buffer; skip it on wrap.
+  if (++w->epoch == 0) w->epoch = 1;
+  *ws = w->ptr;
+  *epoch = w->epoch;
   return PA_OK;
 }
 
@@ -294,10 +341,16 @@ int32_t pa_version(void) { return 10000; }
 
 uint64_t pa_launch_count(void) { return g_launches.load(); }
 
-pa_status pa_set_decode_tuning(int32_t max_ctas, int32_t min_tiles) {
-  if (max_ctas < 0 || min_tiles < 0) return fail(PA_ERR_INVALID_ARG, "negative tuning value");
+pa_status pa_set_decode_tuning(int32_t max_ctas, int32_t min_tiles, int32_t claim_tiles,
+                               int32_t steal_slots) {
+  if (max_ctas < 0 || min_tiles < 0 || claim_tiles < 0)
+    return fail(PA_ERR_INVALID_ARG, "negative tuning value");
+  if (claim_tiles > 1024 || steal_slots > 1024 || min_tiles > (1 << 20))
+    return fail(PA_ERR_INVALID_ARG, "tuning value out of range");
   g_tune_max_ctas = max_ctas;
   g_tune_min_tiles = min_tiles;
+  g_tune_claim = claim_tiles;
+  g_tune_steal_slots = steal_slots;
   return ok();
 }
 
@@ -316,8 +369,18 @@ pa_status pa_set_workspace(void* ptr, size_t bytes) {
   DeviceState* st;
   pa_status s = device_state(&st, nullptr);
   if (s) return s;
-  st->user_ws = ptr;
-  st->user_ws_bytes = ptr ? bytes : 0;
+  if (ptr && bytes) {
+    // Slots are tagged with per-call epochs starting at 1; a zeroed buffer
+    // holds no slot that a call could mistake for its own.
+    cudaError_t e = cudaMemset(ptr, 0, bytes);
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(e, "zeroing the workspace");
+  }
+  st->user_ws = Workspace{};
+  if (ptr) {
+    st->user_ws.ptr = ptr;
+    st->user_ws.bytes = bytes;
+  }
   return ok();
 }
 
@@ -331,8 +394,11 @@ pa_status pa_decode_workspace_size(int64_t batch, int32_t num_q_heads, int32_t n
   DeviceState* st;
   s = device_state(&st, nullptr);
   if (s) return s;
-  const int64_t workers = static_cast<int64_t>(st->num_sms) * kMaxCtasPerSm * kWarpsPerCta;
-  *bytes = workspace_bytes(batch, num_kv_heads, num_q_heads / num_kv_heads, head_dim, workers);
+  int64_t workers = static_cast<int64_t>(st->num_sms) * kMaxCtasPerSm * kWarpsPerCta;
+  const int cap = g_tune_max_ctas.load();
+  if (cap > 0 && cap * kWarpsPerCta < workers) workers = static_cast<int64_t>(cap) * kWarpsPerCta;
+  *bytes = ws_layout(batch, num_kv_heads, num_q_heads / num_kv_heads, head_dim, workers,
+                     tuned_steal_slots()).total;
   return ok();
 }
 
@@ -493,7 +559,9 @@ pa_status pa_decode(const pa_tensor* out, const pa_tensor* q, const pa_tensor* k
   DeviceState* st;
   int dev;
   DecodePlan plan;
+  WsLayout layout;
   void* ws = nullptr;
+  uint32_t epoch = 0;
   {
     std::lock_guard<std::mutex> lk(g_mu);
     if ((s = device_state(&st, &dev))) return s;
@@ -501,9 +569,9 @@ pa_status pa_decode(const pa_tensor* out, const pa_tensor* q, const pa_tensor* k
     if ((s = plan_decode(st, dev, ct, q->dtype, B, static_cast<int>(Hq), static_cast<int>(Hkv),
                          static_cast<int>(D), &plan)))
       return s;
-    const size_t need = workspace_bytes(B, static_cast<int>(Hkv), plan.G, static_cast<int>(D),
-                                        plan.workers);
-    if ((s = get_workspace(st, cs, need, &ws))) return s;
+    layout = ws_layout(B, static_cast<int>(Hkv), plan.G, static_cast<int>(D), plan.workers,
+                       plan.steal_slots);
+    if ((s = get_workspace(st, cs, layout.total, &ws, &epoch))) return s;
   }
   const int elt = fp8 ? 1 : 2;
   CUtensorMap tk, tv;
@@ -516,10 +584,16 @@ pa_status pa_decode(const pa_tensor* out, const pa_tensor* q, const pa_tensor* k
   a.q = q->data;
   a.block_tables = static_cast<const int32_t*>(block_tables->data);
   a.seq_lens = static_cast<const int32_t*>(seq_lens->data);
-  a.ctrl = static_cast<int32_t*>(ws);
-  a.part = reinterpret_cast<float*>(static_cast<char*>(ws) +
-                                    round_up(static_cast<size_t>(B + 3) * sizeof(int32_t), 256));
+  char* wsb = static_cast<char*>(ws);
+  a.ctrl = reinterpret_cast<int32_t*>(wsb + layout.ctrl);
+  a.words = reinterpret_cast<unsigned long long*>(wsb + layout.words);
+  a.wepoch = reinterpret_cast<uint32_t*>(wsb + layout.wepoch);
+  a.heads = reinterpret_cast<unsigned long long*>(wsb + layout.heads);
+  a.tags = reinterpret_cast<uint32_t*>(wsb + layout.tags);
+  a.next = reinterpret_cast<uint32_t*>(wsb + layout.next);
+  a.part = reinterpret_cast<float*>(wsb + layout.part);
   a.err = st->err_word;
+  a.epoch = epoch;
   a.B = static_cast<int>(B);
   a.Hq = static_cast<int>(Hq);
   a.Hkv = static_cast<int>(Hkv);
@@ -533,6 +607,8 @@ pa_status pa_decode(const pa_tensor* out, const pa_tensor* q, const pa_tensor* k
                                      (fp8 ? static_cast<double>(k_scale) : 1.0));
   a.v_scale = fp8 ? v_scale : 1.f;
   a.min_tiles = plan.min_tiles;
+  a.claim = plan.claim;
+  a.steal_slots = plan.steal_slots;
 
   const bool prof = g_prof_before && g_prof_after;
   cudaError_t e;
@@ -547,6 +623,11 @@ pa_status pa_decode(const pa_tensor* out, const pa_tensor* q, const pa_tensor* k
   m.out = out->data;
   m.part = a.part;
   m.ctrl = a.ctrl;
+  m.heads = a.heads;
+  m.tags = a.tags;
+  m.next = a.next;
+  m.epoch = epoch;
+  m.NW = plan.workers;
   m.B = a.B;
   m.Hq = a.Hq;
   m.Hkv = a.Hkv;

@@ -13,25 +13,48 @@ enum ElemType { kF16 = 0, kBF16 = 1, kE4M3 = 2 };
 
 constexpr int kTile = 16;  // tokens per pipeline tile (one mma m-tile)
 
-// Arguments of the persistent decode kernel (see decode.cuh).
+// Decode workspace layout (device memory, all sections 256-byte aligned):
+//   ctrl   int32 [4 + B + 1]: [0] static tiles per warp, [1] total tiles,
+//          [2] claim size, [3] steal slots per warp, [4..] tile prefix
+//   words  u64 [NW]   per-warp range word (head << 32 | tail)
+//   wepoch u32 [NW]   epoch in which the warp's word was initialised
+//   heads  u64 [S]    per-pair list of stolen partials (epoch << 32 | slot)
+//   tags   u32 [NSLOT] epoch of the last write of each partial slot
+//   next   u32 [NSLOT] list link of stolen partial slots
+//   part   f32 [NSLOT][G][D + 2]: acc[G][D], m[G], l[G]
+// with S = B * Hkv pairs, NW worker warps, NSLOT = S + NW + NW * K.
+// Slots [0, S + NW) hold owner segments (pair s of warp w at s + w); slots
+// [S + NW + w * K, S + NW + (w + 1) * K) hold the segments warp w stole.
 struct DecodeArgs {
-  const void* q;             // [B, Hq, D]
-  const int32_t* block_tables;  // [B, MB]
-  const int32_t* seq_lens;   // [B]
-  float* part;               // partial slots: [(B*Hkv + workers)][G][D + 2] fp32
-  int32_t* ctrl;             // [0] tiles per worker, [1] total tiles, [2..B+2] tile prefix
-  int32_t* err;              // device error word
+  const void* q;                 // [B, Hq, D]
+  const int32_t* block_tables;   // [B, MB]
+  const int32_t* seq_lens;       // [B]
+  int32_t* ctrl;
+  unsigned long long* words;
+  uint32_t* wepoch;
+  unsigned long long* heads;
+  uint32_t* tags;
+  uint32_t* next;
+  float* part;
+  int32_t* err;                  // device error word
+  uint32_t epoch;                // differs on every call that shares this workspace
   int B, Hq, Hkv, G, D, bs, MB, NB, window;
-  float score_scale;         // scale * log2(e) (* k_scale for FP8)
-  float v_scale;             // FP8: applied to the partial outputs
-  int min_tiles;             // least tiles per worker warp
+  float score_scale;             // scale * log2(e) (* k_scale for FP8)
+  float v_scale;                 // FP8: applied to the partial outputs
+  int min_tiles;                 // least tiles per warp in the static split
+  int claim;                     // tiles per owner claim and largest steal
+  int steal_slots;               // K: partial slots per warp for stolen work
 };
 
 struct MergeArgs {
-  void* out;                 // [B, Hq, D], dtype of q
+  void* out;                     // [B, Hq, D], dtype of q
   const float* part;
   const int32_t* ctrl;
-  int B, Hq, Hkv, G, D;
+  const unsigned long long* heads;
+  const uint32_t* tags;
+  const uint32_t* next;
+  uint32_t epoch;
+  int B, Hq, Hkv, G, D, NW;
 };
 
 struct ReshapeArgs {
