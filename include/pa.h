@@ -132,14 +132,14 @@ pa_status pa_reshape_and_cache(const pa_tensor* k, const pa_tensor* v,
  *   window        <= 0: no window.
  * Supported D: 64, 128, 256 for 16-bit caches; 128, 256 for FP8. B <= 4096.
  *
- * Work is split evenly over the worker warps of a persistent grid; warps that
- * finish early steal unclaimed tiles of others, so with stealing on (the
- * default) the summation order, and with it the last bits of the output, can
- * differ from run to run (pa_set_decode_tuning turns stealing off).
+ * Most tiles are split evenly over the worker warps of a persistent grid; the
+ * rest are handed out in small pieces to whichever warps finish first, so the
+ * summation order, and with it the last bits of the output, can differ from
+ * run to run (pa_set_decode_tuning can turn the dynamic share off).
  *
  * Workspace: the step writes per-segment partial results (running max, sum
- * and unnormalised output), per-warp range words and a small control block to
- * a device workspace of pa_decode_workspace_size() bytes. It is the buffer
+ * and unnormalised output), a piece counter and a small control block to a
+ * device workspace of pa_decode_workspace_size() bytes. It is the buffer
  * given to pa_set_workspace() for the current device, or else a buffer the
  * library allocates (and zeroes) once per (device, stream) outside stream
  * capture and keeps. Calls that overlap on the GPU must not share a
@@ -158,22 +158,22 @@ pa_status pa_decode_workspace_size(int64_t batch, int32_t num_q_heads, int32_t n
 
 /* Use caller-owned device memory [ptr, ptr + bytes) as the decode workspace on
  * the current device (ptr 256-byte aligned). The call zeroes the buffer and
- * synchronises the device. ptr == NULL returns to the library-managed
+ * synchronises the device; each step leaves its piece counter at zero. ptr == NULL returns to the library-managed
  * workspace. The caller keeps the memory alive while decode steps that use it
  * are in flight, and does not write to it between calls. */
 pa_status pa_set_workspace(void* ptr, size_t bytes);
 
 /* Test and tuning knobs, process-wide for later pa_decode calls; 0 keeps the
  * default of each:
- *   max_ctas     caps the persistent decode grid (default: 2 CTAs per SM);
- *   min_tiles    least number of 16-token tiles per worker warp (default 4);
- *   claim_tiles  tiles a warp claims from its own range at a time, and the
- *                largest piece it steals from another warp (default 4);
- *   steal_slots  partial-result slots per warp for stolen work (default 16);
- *                negative turns stealing off, which makes results
- *                bit-reproducible from run to run. */
-pa_status pa_set_decode_tuning(int32_t max_ctas, int32_t min_tiles, int32_t claim_tiles,
-                               int32_t steal_slots);
+ *   max_ctas       caps the persistent decode grid (default: 2 CTAs per SM);
+ *   min_tiles      least number of 16-token tiles per warp's static range
+ *                  (default 4);
+ *   pool_permille  share of the tiles handed out dynamically in small pieces
+ *                  after the static ranges (default 200); negative turns the
+ *                  pool off, which makes results bit-reproducible run to run;
+ *   piece_tiles    least tiles per pool piece (default 4). */
+pa_status pa_set_decode_tuning(int32_t max_ctas, int32_t min_tiles, int32_t pool_permille,
+                               int32_t piece_tiles);
 
 /* Profiling hook: when both are non-NULL, the next pa_decode calls on this
  * thread record the CUDA events (cudaEvent_t) immediately before and after the

@@ -170,10 +170,10 @@ def set_workspace(buf: torch.Tensor | None) -> None:
         _check(lib().pa_set_workspace(buf.data_ptr(), buf.numel() * buf.element_size()))
 
 
-def set_decode_tuning(max_ctas: int = 0, min_tiles: int = 0, claim_tiles: int = 0,
-                      steal_slots: int = 0) -> None:
-    """0 keeps a default; steal_slots < 0 turns work stealing off."""
-    _check(lib().pa_set_decode_tuning(max_ctas, min_tiles, claim_tiles, steal_slots))
+def set_decode_tuning(max_ctas: int = 0, min_tiles: int = 0, pool_permille: int = 0,
+                      piece_tiles: int = 0) -> None:
+    """0 keeps a default; pool_permille < 0 turns the dynamic pool off."""
+    _check(lib().pa_set_decode_tuning(max_ctas, min_tiles, pool_permille, piece_tiles))
 
 
 def profile_events(before=None, after=None) -> None:

@@ -1,21 +1,21 @@
 // Persistent paged-decode kernel for sm_103a.
 //
-// Work decomposition (balanced split-KV with work stealing). Every (sequence
-// b, KV head) pair owns the 16-token tiles that cover its attended positions
-// [start, L); tiles never straddle a physical block because block_size is a
-// multiple of 16. All tiles of all pairs form one flat index space
-// (pair-major). Each worker warp owns an equal contiguous range of it and
-// consumes the range front to back in small claimed windows, through an
-// atomic (head << 32 | tail) word. A warp that runs out steals the back half
-// (at most one claim window) of another warp's unclaimed tail, so warps on
-// SMs that get less bandwidth do not stretch the step. A contiguous run of
-// tiles cut at pair boundaries is a segment; each segment writes one partial
-// (running max m, running sum l, unnormalised output): an owner segment of
-// pair s by warp w into slot s + w (unique: the walk through the (pair,
-// warp) grid is a monotone staircase), a stolen segment into the thief's
-// own slots, linked into a per-pair list. Every slot is tagged with the
-// call's epoch, so stale workspace contents are never merged. A merge kernel
-// combines each pair's partials by their log-sum-exp weights.
+// Work decomposition (balanced split-KV). Every (sequence b, KV head) pair
+// owns the 16-token tiles that cover its attended positions [start, L); tiles
+// never straddle a physical block because block_size is a multiple of 16.
+// All tiles of all pairs form one flat index space (pair-major). The first
+// part of it (about 80%) is split into equal contiguous static ranges, one per
+// worker warp; the rest is a pool of small pieces that warps claim with one
+// atomicAdd each once their static range is done (the claim for the next
+// piece is issued a piece ahead, so the copy pipeline never drains). Warps on
+// SMs that get less bandwidth thus take fewer pieces and all warps finish
+// together. A run of one warp's tiles inside one pair is a segment; each
+// segment writes one partial (running max m, running sum l, unnormalised
+// output) to a slot fixed by arithmetic: pair + warp for static segments,
+// pair + piece (in a second region) for pool segments -- unique because the
+// walk through the (pair, warp) and (pair, piece) grids is a monotone
+// staircase. A merge kernel combines each pair's partials by their
+// log-sum-exp weights.
 //
 // Data movement. Each warp owns a ring of STAGES shared-memory stages; one
 // stage holds the K tile and the V tile [16 rows x D] of one (block, KV head),
@@ -138,9 +138,7 @@ __device__ __forceinline__ int acc_dim(int mt, int g, int hi) {
   }
 }
 
-constexpr unsigned kFlagStart = 1, kFlagEnd = 2, kFlagStolen = 4;
-constexpr uint32_t kNoSlot = 0xffffffffu;
-constexpr int kStealRounds = 8;
+constexpr unsigned kFlagStart = 1, kFlagEnd = 2, kFlagPool = 4;
 
 template <int CT, int QT, int D, int NT, int WARPS, int STAGES>
 __global__ void __launch_bounds__(WARPS * 32)
@@ -203,28 +201,28 @@ __global__ void __launch_bounds__(WARPS * 32)
   }
   __syncthreads();
 
+  // static ranges for about (1 - pool share) of the tiles, then the pool
   const int total = a.Hkv * s_pref[a.B];
   const int nw = gridDim.x * WARPS;
-  int ws = (total + nw - 1) / nw;
+  const long long pool_want = static_cast<long long>(total) * a.pool_permille / 1000;
+  int ws = static_cast<int>((total - pool_want) / nw);
   if (ws < a.min_tiles) ws = a.min_tiles;
+  const int ts = static_cast<int>(min(static_cast<long long>(ws) * nw, static_cast<long long>(total)));
+  const int pool_tiles = total - ts;
+  int piece = (pool_tiles + a.np_max - 1) / a.np_max;
+  if (piece < a.piece_min) piece = a.piece_min;
   if (blockIdx.x == 0) {
     if (tid == 0) {
       a.ctrl[0] = ws;
       a.ctrl[1] = total;
-      a.ctrl[2] = a.claim;
-      a.ctrl[3] = a.steal_slots;
+      a.ctrl[2] = ts;
+      a.ctrl[3] = piece;
     }
     for (int b = tid; b <= a.B; b += blockDim.x) a.ctrl[4 + b] = s_pref[b];
   }
   const int w = blockIdx.x * WARPS + warp;
-  const int f0 = static_cast<int>(min(static_cast<long long>(w) * ws, static_cast<long long>(total)));
-  const int f1 = min(f0 + ws, total);
-  // publish this warp's range word, then its epoch (thieves check the epoch first)
-  if (lane == 0) {
-    a.words[w] = (static_cast<unsigned long long>(f0) << 32) | static_cast<unsigned>(f1);
-    __threadfence();
-    *reinterpret_cast<volatile uint32_t*>(a.wepoch + w) = a.epoch;
-  }
+  const int f0 = static_cast<int>(min(static_cast<long long>(w) * ws, static_cast<long long>(ts)));
+  const int f1 = min(f0 + ws, ts);
 
   const uint32_t ring = base + warp * Gm::RING_BYTES;
   const uint32_t wbars = bars + warp * STAGES * 8;
@@ -233,122 +231,50 @@ __global__ void __launch_bounds__(WARPS * 32)
   const int npairs = a.B * a.Hkv;
 
   // ---------------------------------------------------------------- producer
-  // Runs: the owner run (claimed window by window from this warp's word) and
-  // stolen runs. np = next flat tile to load, run_end = end of the current
-  // window (owner) or run (stolen).
+  // Runs: the static range [f0, f1), then pool pieces. np = next flat tile to
+  // load, run_end = end of the current run, run_id = piece index (pool runs).
   Cursor pc;
   pc.b = pc.kvh = pc.t = pc.nt = 0;
-  int phase = 0;  // 0 owner, 1 stealing, 2 done
-  int np = 0, run_end = 0;
-  bool run_first = false, owner_any = false;
-  unsigned long long pending = 0;  // lane 0: prefetched owner claim
-  int stolen_used = 0;             // stolen partial slots used (consumer side)
-  int steals = 0;                  // stolen runs taken (producer side)
+  int phase = 0;  // 0 static, 1 pool, 2 done
+  int np = f0, run_end = f1, run_id = -1;
+  bool run_first = true;
+  bool claim_issued = false;
+  uint32_t pending = 0;  // lane 0: prefetched pool claim
 
-  auto owner_claim = [&]() -> unsigned long long {
-    unsigned long long r = 0;
-    if (lane == 0)
-      r = atomicAdd(a.words + w, static_cast<unsigned long long>(a.claim) << 32);
-    return r;
-  };
-  // first owner window
-  {
-    unsigned long long c = owner_claim();
-    c = __shfl_sync(FULL, c, 0);
-    const int h = static_cast<int>(c >> 32), t = static_cast<int>(c & 0xffffffffu);
-    if (h < t) {
-      np = h;
-      run_end = min(h + a.claim, t);
-      run_first = true;
-      pending = owner_claim();
-    } else {
-      phase = 1;
-    }
-  }
-
-  // steal: sets [np, run_end) to a stolen run and returns true, or false
-  auto steal = [&]() -> bool {
-    // Slots: a stolen run of at most `claim` tiles spans at most `claim` pairs.
-    if (steals >= a.steal_slots / a.claim) return false;
-    uint32_t seed = static_cast<uint32_t>(w) * 2654435761u;
-    for (int round = 0; round < kStealRounds; ++round) {
-      const int v = static_cast<int>((seed + static_cast<uint32_t>(round * 32 + lane) * 40503u) %
-                                     static_cast<uint32_t>(nw));
-      const uint32_t ep = *reinterpret_cast<volatile const uint32_t*>(a.wepoch + v);
-      __threadfence();
-      const unsigned long long wd = *reinterpret_cast<volatile const unsigned long long*>(a.words + v);
-      int rem = 0;
-      if (ep == a.epoch && v != w)
-        rem = static_cast<int>(wd & 0xffffffffu) - static_cast<int>(wd >> 32);
-      // best victim in this group of 32
-      int best = rem, bl = lane;
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const int ob = __shfl_xor_sync(FULL, best, o), ol = __shfl_xor_sync(FULL, bl, o);
-        if (ob > best || (ob == best && ol < bl)) {
-          best = ob;
-          bl = ol;
-        }
-      }
-      if (best < 2) continue;
-      int lo = 0, hi = 0;
-      if (lane == bl) {
-        unsigned long long cur = wd;
-        for (int tries = 0; tries < 4; ++tries) {
-          const int h = static_cast<int>(cur >> 32), t = static_cast<int>(cur & 0xffffffffu);
-          if (t - h < 2) break;
-          const int take = min(a.claim, (t - h) >> 1);
-          const unsigned long long nv =
-              (static_cast<unsigned long long>(h) << 32) | static_cast<unsigned>(t - take);
-          const unsigned long long prev = atomicCAS(a.words + v, cur, nv);
-          if (prev == cur) {
-            lo = t - take;
-            hi = t;
-            break;
-          }
-          cur = prev;
-        }
-      }
-      lo = __shfl_sync(FULL, lo, bl);
-      hi = __shfl_sync(FULL, hi, bl);
-      if (hi > lo) {
-        np = lo;
-        run_end = hi;
-        run_first = true;
-        ++steals;
-        return true;
-      }
-    }
-    return false;
+  auto issue_claim = [&]() {
+    if (lane == 0) pending = atomicAdd(a.pool, 1u);
+    claim_issued = true;
   };
 
-  int id_b = -1, id_lb0 = 0, id_val = 0;      // current block-id window
-  int pf_b = -1, pf_lb0 = 0, pf_val = 0;      // prefetched next window
+  int id_b = -1, id_lb0 = 0, id_val = 0;  // current block-id window
+  int pf_b = -1, pf_lb0 = 0, pf_val = 0;  // prefetched next window
   int produced = 0, consumed = 0;
 
   // Produces the next tile into stage `slot`; false when no work is left.
   auto produce = [&](int slot) -> bool {
-    unsigned flags = 0;
-    while (true) {
+    while (np >= run_end) {
       if (phase == 2) return false;
-      if (np < run_end) break;
-      if (phase == 0) {
-        const unsigned long long c = __shfl_sync(FULL, pending, 0);
-        const int h = static_cast<int>(c >> 32), t = static_cast<int>(c & 0xffffffffu);
-        if (h < t) {  // next owner window, contiguous with the previous one
-          np = h;
-          run_end = min(h + a.claim, t);
-          pending = owner_claim();
-          continue;
-        }
-        // the owner run ends with the last tile produced (not yet consumed)
-        if (owner_any && produced > consumed) meta_fl[(produced - 1) % STAGES] |= kFlagEnd;
-        phase = 1;
+      if (pool_tiles == 0) {
+        phase = 2;
+        return false;
       }
-      if (phase == 1 && !steal()) phase = 2;
+      if (!claim_issued) issue_claim();
+      const int i = static_cast<int>(__shfl_sync(FULL, pending, 0));
+      claim_issued = false;
+      const long long p0 = static_cast<long long>(ts) + static_cast<long long>(i) * piece;
+      if (p0 >= total) {
+        phase = 2;
+        return false;
+      }
+      phase = 1;
+      np = static_cast<int>(p0);
+      run_end = min(np + piece, total);
+      run_id = i;
+      run_first = true;
+      issue_claim();  // the next piece, one piece ahead
     }
     const int f = np++;
-    const bool stolen = phase == 1;
+    unsigned flags = (phase == 1) ? kFlagPool : 0u;
     if (run_first) {
       flags |= kFlagStart;
       cursor_locate(pc, f, s_pref, a.B, a.Hkv);
@@ -356,11 +282,10 @@ __global__ void __launch_bounds__(WARPS * 32)
     } else {
       cursor_next(pc, s_pref, a.B, a.Hkv);
     }
-    if (stolen) {
-      flags |= kFlagStolen;
-      if (np == run_end) flags |= kFlagEnd;
-    } else {
-      owner_any = true;
+    if (np == run_end) {
+      flags |= kFlagEnd;
+      // static range about to end: claim the first pool piece now
+      if (phase == 0 && pool_tiles > 0 && !claim_issued) issue_claim();
     }
     const int L = s_len[pc.b];
     const int pt = win_start(L, a.window) / kTile + pc.t;  // tile index in position space
@@ -390,7 +315,7 @@ __global__ void __launch_bounds__(WARPS * 32)
     const int row = (phys * a.Hkv + pc.kvh) * a.bs + (pt * kTile) % a.bs;
     if (lane == 0) {
       meta_f[slot] = f;
-      meta_fl[slot] = static_cast<int>(flags);
+      meta_fl[slot] = static_cast<int>(flags) | ((phase == 1 ? run_id : 0) << 3);
       const uint32_t bar = wbars + 8 * slot;
       const uint32_t kd = ring + slot * Gm::STAGE_BYTES;
       mbar_arrive_expect_tx(bar, Gm::STAGE_BYTES);
@@ -422,7 +347,9 @@ __global__ void __launch_bounds__(WARPS * 32)
     const int slot = consumed % STAGES;
     const uint32_t parity = (consumed / STAGES) & 1;
     const int f = meta_f[slot];
-    const unsigned flags = static_cast<unsigned>(meta_fl[slot]);
+    const int mf = meta_fl[slot];
+    const unsigned flags = static_cast<unsigned>(mf) & 7u;
+    const int piece_id = mf >> 3;
     if (flags & kFlagStart) cursor_locate(cc, f, s_pref, a.B, a.Hkv);
     else cursor_next(cc, s_pref, a.B, a.Hkv);
     const bool seg_start = (flags & kFlagStart) || (cc.t == 0);
@@ -625,24 +552,17 @@ __global__ void __launch_bounds__(WARPS * 32)
     }
     __syncwarp();
     ++consumed;
-    // refill the stage just consumed (may also set the end flag of an earlier stage)
+    // refill the stage just consumed
     if (produce(produced % STAGES)) ++produced;
 
-    // ---- segment end: write the partial (m, l, unnormalised output). The
-    // flags were read before the refill; a late end mark always lands on a
-    // stage that has not been consumed yet.
-    const unsigned fl = flags;
-    const bool seg_end = (fl & kFlagEnd) || (cc.t == cc.nt - 1);
+    // ---- segment end: write the partial (m, l, unnormalised output)
+    const bool seg_end = (flags & kFlagEnd) || (cc.t == cc.nt - 1);
     if (seg_end) {
       const int pair = cc.b * a.Hkv + cc.kvh;
-      uint32_t pslot;
-      if (fl & kFlagStolen) {
-        pslot = static_cast<uint32_t>(npairs + nw + w * a.steal_slots + stolen_used);
-        ++stolen_used;
-      } else {
-        pslot = static_cast<uint32_t>(pair + w);
-      }
-      float* P = a.part + static_cast<size_t>(pslot) * (a.G * (D + 2));
+      const size_t pslot = (flags & kFlagPool)
+                               ? static_cast<size_t>(npairs) + nw + pair + piece_id
+                               : static_cast<size_t>(pair) + w;
+      float* P = a.part + pslot * (a.G * (D + 2));
       const float vs = kFp8 ? a.v_scale : 1.f;
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
@@ -665,16 +585,6 @@ __global__ void __launch_bounds__(WARPS * 32)
               P[a.G * D + a.G + h] = l;
             }
           }
-        }
-      }
-      if (lane == 0) {
-        a.tags[pslot] = a.epoch;
-        if (fl & kFlagStolen) {
-          const unsigned long long node = (static_cast<unsigned long long>(a.epoch) << 32) | pslot;
-          const unsigned long long old = atomicExch(a.heads + pair, node);
-          a.next[pslot] = (static_cast<uint32_t>(old >> 32) == a.epoch)
-                              ? static_cast<uint32_t>(old & 0xffffffffu)
-                              : kNoSlot;
         }
       }
     }

@@ -19,76 +19,60 @@ cudaError_t device_error_word(int32_t** ptr) {
 // ------------------------------------------------------------------ merge
 //
 // One CTA per (pair, q head of the group); each thread owns two head dims.
-// The partials of pair s are the owner slots s + w of every warp w whose
-// static range meets the pair's tiles [F, F + nt) and that was written in this
-// call (tag == epoch), plus the pair's list of stolen slots. With partial
-// maxima m_p (log2 domain), sums l_p and unnormalised outputs o_p:
+// The partials of pair s (tiles [F, F + nt) of the flat space) are the static
+// slots s + w of the warps w whose static range meets [F, min(F + nt, Ts)),
+// and the pool slots S + NW + s + i of the pieces i that meet [max(F, Ts),
+// F + nt). With partial maxima m_p (log2 domain), sums l_p and unnormalised
+// outputs o_p:
 //   out = sum_p 2^(m_p - M) o_p / sum_p 2^(m_p - M) l_p,  M = max_p m_p,
-// evaluated chunk by chunk with a running maximum so any number of partials
-// fits in shared memory. A pair with no tiles (seq_len 0) gets zeros.
+// evaluated in chunks with a running maximum, so any number of partials
+// works. A pair with no tiles (seq_len 0) gets zeros. Block (0, 0) also
+// resets the pool counter for the next step.
 constexpr int kMergeChunk = 256;
-constexpr uint32_t kNoSlot = 0xffffffffu;
 
 template <int OT>
 __global__ void __launch_bounds__(128) merge_kernel(const MergeArgs a) {
   __shared__ uint32_t s_slot[kMergeChunk];
   __shared__ float s_fac[kMergeChunk];
-  __shared__ int s_n;
   __shared__ float s_M, s_den, s_scale;
-  __shared__ uint32_t s_list;
   griddep_wait();
   const int s = blockIdx.x, h = blockIdx.y;
   const int b = s / a.Hkv, kvh = s - b * a.Hkv;
   const int tid = threadIdx.x;
   const int d = 2 * tid;
+  if (s == 0 && h == 0 && tid == 0) *a.pool = 0u;
   const size_t orow = (static_cast<size_t>(b) * a.Hq + kvh * a.G + h) * a.D + d;
-  const int ws = a.ctrl[0];
+  const int ws = a.ctrl[0], ts = a.ctrl[2], piece = a.ctrl[3];
   const int pb = a.ctrl[4 + b], nt = a.ctrl[5 + b] - pb;
-  float n0 = 0.f, n1 = 0.f;
-  float r0 = 0.f, r1 = 0.f;
+  const int S = a.B * a.Hkv;
+  float n0 = 0.f, n1 = 0.f, r0 = 0.f, r1 = 0.f;
   if (nt > 0) {
     const int F = a.Hkv * pb + kvh * nt;
-    const int w0 = F / ws, w1 = min((F + nt - 1) / ws, a.NW - 1);
+    // candidate slots: static warps [w0, w1], then pool pieces [i0, i1]
+    int w0 = 0, w1 = -1, i0 = 0, i1 = -1;
+    if (F < ts) {
+      w0 = F / ws;
+      w1 = (min(F + nt, ts) - 1) / ws;
+    }
+    if (F + nt > ts) {
+      i0 = (max(F, ts) - ts) / piece;
+      i1 = (F + nt - 1 - ts) / piece;
+    }
+    const int na = w1 - w0 + 1, np = i1 - i0 + 1, ntot = na + np;
     const size_t stride = static_cast<size_t>(a.G) * (a.D + 2);
     const int mo = a.G * a.D + h, lo = a.G * a.D + a.G + h;
     if (tid == 0) {
       s_M = -INFINITY;
       s_den = 0.f;
-      const unsigned long long hd = a.heads[s];
-      s_list = (static_cast<uint32_t>(hd >> 32) == a.epoch) ? static_cast<uint32_t>(hd) : kNoSlot;
     }
-    int wcur = w0;
-    while (true) {
-      if (tid == 0) s_n = 0;
-      __syncthreads();
-      // owner slots of the next group of warps
-      const int na = min(w1 - wcur + 1, kMergeChunk);
-      for (int i = tid; i < na; i += blockDim.x) {
-        const uint32_t slot = static_cast<uint32_t>(s + wcur + i);
-        if (a.tags[slot] == a.epoch) s_slot[atomicAdd(&s_n, 1)] = slot;
-      }
-      wcur += max(na, 0);
-      __syncthreads();
-      // stolen slots from the pair's list
-      if (tid == 0) {
-        int n = s_n;
-        uint32_t cur = s_list;
-        while (cur != kNoSlot && n < kMergeChunk) {
-          s_slot[n++] = cur;
-          cur = a.next[cur];
-        }
-        s_list = cur;
-        s_n = n;
+    for (int c0 = 0; c0 < ntot; c0 += kMergeChunk) {
+      const int n = min(kMergeChunk, ntot - c0);
+      for (int i = tid; i < n; i += blockDim.x) {
+        const int k = c0 + i;
+        s_slot[i] = (k < na) ? static_cast<uint32_t>(s + w0 + k)
+                             : static_cast<uint32_t>(S + a.NW + s + i0 + (k - na));
       }
       __syncthreads();
-      const int n = s_n;
-      const bool more = (wcur <= w1) || (s_list != kNoSlot);
-      if (n == 0) {
-        if (!more) break;
-        __syncthreads();
-        continue;
-      }
-      // chunk maximum, new running maximum and rescale of what came before
       if (tid < 32) {
         float mx = -INFINITY;
         for (int i = tid; i < n; i += 32) mx = fmaxf(mx, a.part[s_slot[i] * stride + mo]);
@@ -117,14 +101,13 @@ __global__ void __launch_bounds__(128) merge_kernel(const MergeArgs a) {
         n0 *= sc;
         n1 *= sc;
         for (int i = 0; i < n; ++i) {
-          const float2 o = *reinterpret_cast<const float2*>(a.part + s_slot[i] * stride +
-                                                            h * a.D + d);
+          const float2 o =
+              *reinterpret_cast<const float2*>(a.part + s_slot[i] * stride + h * a.D + d);
           n0 += s_fac[i] * o.x;
           n1 += s_fac[i] * o.y;
         }
       }
       __syncthreads();
-      if (!more) break;
     }
     const float den = s_den;
     r0 = n0 / den;

@@ -25,14 +25,15 @@ thread_local std::string g_last_error;
 std::atomic<uint64_t> g_launches{0};
 std::atomic<int32_t> g_tune_max_ctas{0};
 std::atomic<int32_t> g_tune_min_tiles{0};
-std::atomic<int32_t> g_tune_claim{0};
-std::atomic<int32_t> g_tune_steal_slots{0};
+std::atomic<int32_t> g_tune_pool{0};
+std::atomic<int32_t> g_tune_piece{0};
 thread_local void* g_prof_before = nullptr;
 thread_local void* g_prof_after = nullptr;
 
 constexpr int kDefaultMinTiles = 4;
-constexpr int kDefaultClaim = 4;        // tiles per owner claim / largest steal
-constexpr int kDefaultStealSlots = 16;  // partial slots per warp for stolen work
+constexpr int kDefaultPoolPermille = 200;  // share of tiles handed out dynamically
+constexpr int kDefaultPiece = 4;           // least tiles per pool piece
+constexpr int kPiecesPerWorker = 4;        // pool pieces per worker warp, at most
 constexpr int kMaxCtasPerSm = 2;
 constexpr int kWarpsPerCta = 4;
 constexpr int64_t kMaxBatch = 4096;
@@ -115,7 +116,7 @@ pa_status check_tensor(const pa_tensor* t, const char* name, int ndim) {
 struct Workspace {
   void* ptr = nullptr;
   size_t bytes = 0;
-  uint32_t epoch = 0;  // last epoch used with this buffer (0: freshly zeroed)
+  bool dirty = false;  // the pool counter may be nonzero (a merge launch failed)
 };
 
 struct DeviceState {
@@ -151,33 +152,29 @@ size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // Section offsets of the decode workspace (layout described in pa_internal.h).
 struct WsLayout {
-  size_t ctrl, words, wepoch, heads, tags, next, part, total;
+  size_t ctrl, pool, part, total;
 };
 
-WsLayout ws_layout(int64_t B, int Hkv, int G, int D, int64_t workers, int steal_slots) {
+WsLayout ws_layout(int64_t B, int Hkv, int G, int D, int64_t workers) {
   const size_t S = static_cast<size_t>(B) * Hkv;
-  const size_t nslot = S + workers + static_cast<size_t>(workers) * steal_slots;
+  const size_t nslot = 2 * S + workers + static_cast<size_t>(workers) * kPiecesPerWorker;
   WsLayout L;
   size_t o = 0;
-  L.ctrl = o;   o += round_up(static_cast<size_t>(B + 5) * sizeof(int32_t), 256);
-  L.words = o;  o += round_up(workers * sizeof(unsigned long long), 256);
-  L.wepoch = o; o += round_up(workers * sizeof(uint32_t), 256);
-  L.heads = o;  o += round_up(S * sizeof(unsigned long long), 256);
-  L.tags = o;   o += round_up(nslot * sizeof(uint32_t), 256);
-  L.next = o;   o += round_up(nslot * sizeof(uint32_t), 256);
-  L.part = o;   o += nslot * static_cast<size_t>(G) * (D + 2) * sizeof(float);
+  L.ctrl = o;  o += round_up(static_cast<size_t>(B + 5) * sizeof(int32_t), 256);
+  L.pool = o;  o += 256;
+  L.part = o;  o += nslot * static_cast<size_t>(G) * (D + 2) * sizeof(float);
   L.total = o;
   return L;
 }
 
-int tuned_steal_slots() {
-  const int v = g_tune_steal_slots.load();
-  return v == 0 ? kDefaultStealSlots : (v < 0 ? 0 : v);
+int tuned_pool_permille() {
+  const int v = g_tune_pool.load();
+  return v == 0 ? kDefaultPoolPermille : (v < 0 ? 0 : v);
 }
 
-int tuned_claim() {
-  const int v = g_tune_claim.load();
-  return v > 0 ? v : kDefaultClaim;
+int tuned_piece() {
+  const int v = g_tune_piece.load();
+  return v > 0 ? v : kDefaultPiece;
 }
 
 // ------------------------------------------------------------ TMA descriptors
@@ -236,7 +233,7 @@ cudaError_t launch_of(int ct, int qt, int D, int nt, const CUtensorMap& tk, cons
 
 struct DecodePlan {
   int ct, qt, nt, G;
-  int smem, grid, workers, min_tiles, claim, steal_slots;
+  int smem, grid, workers, min_tiles, pool_permille, piece;
   pa::DecodeVariant var;
 };
 
@@ -279,15 +276,17 @@ pa_status plan_decode(DeviceState* st, int dev, int ct, int qt, int64_t B, int H
   p->workers = p->grid * p->var.warps;
   const int mt = g_tune_min_tiles.load();
   p->min_tiles = mt > 0 ? mt : kDefaultMinTiles;
-  p->claim = tuned_claim();
-  p->steal_slots = tuned_steal_slots();
+  p->pool_permille = tuned_pool_permille();
+  p->piece = tuned_piece();
   return PA_OK;
 }
 
-// Picks the workspace for this call and the epoch that tags its writes.
-pa_status get_workspace(DeviceState* st, cudaStream_t stream, size_t need, void** ws,
-                        uint32_t* epoch) {
+// Picks the workspace for this call (zeroed on allocation: the pool counter
+// starts at zero, and each step's merge kernel leaves it at zero).
+pa_status get_workspace(DeviceState* st, cudaStream_t stream, const WsLayout& lay, void** ws,
+                        Workspace** wsp) {
   Workspace* w;
+  const size_t need = lay.total;
   if (st->user_ws.ptr) {
     if (st->user_ws.bytes < need)
       return fail(PA_ERR_WORKSPACE, "workspace too small: %zu bytes set, %zu needed",
@@ -321,13 +320,15 @@ pa_status get_workspace(DeviceState* st, cudaStream_t stream, size_t need, void*
       }
       w->ptr = p;
       w->bytes = bytes;
-      w->epoch = 0;
     }
   }
-  // Epoch 0 marks never-written slots of a zeroed buffer; skip it on wrap.
-  if (++w->epoch == 0) w->epoch = 1;
+  if (w->dirty) {
+    cudaError_t e = cudaMemsetAsync(static_cast<char*>(w->ptr) + lay.pool, 0, 256, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(pool counter)");
+    w->dirty = false;
+  }
   *ws = w->ptr;
-  *epoch = w->epoch;
+  *wsp = w;
   return PA_OK;
 }
 
@@ -341,16 +342,16 @@ int32_t pa_version(void) { return 10000; }
 
 uint64_t pa_launch_count(void) { return g_launches.load(); }
 
-pa_status pa_set_decode_tuning(int32_t max_ctas, int32_t min_tiles, int32_t claim_tiles,
-                               int32_t steal_slots) {
-  if (max_ctas < 0 || min_tiles < 0 || claim_tiles < 0)
+pa_status pa_set_decode_tuning(int32_t max_ctas, int32_t min_tiles, int32_t pool_permille,
+                               int32_t piece_tiles) {
+  if (max_ctas < 0 || min_tiles < 0 || piece_tiles < 0)
     return fail(PA_ERR_INVALID_ARG, "negative tuning value");
-  if (claim_tiles > 1024 || steal_slots > 1024 || min_tiles > (1 << 20))
+  if (pool_permille > 1000 || piece_tiles > (1 << 20) || min_tiles > (1 << 20))
     return fail(PA_ERR_INVALID_ARG, "tuning value out of range");
   g_tune_max_ctas = max_ctas;
   g_tune_min_tiles = min_tiles;
-  g_tune_claim = claim_tiles;
-  g_tune_steal_slots = steal_slots;
+  g_tune_pool = pool_permille;
+  g_tune_piece = piece_tiles;
   return ok();
 }
 
@@ -370,8 +371,7 @@ pa_status pa_set_workspace(void* ptr, size_t bytes) {
   pa_status s = device_state(&st, nullptr);
   if (s) return s;
   if (ptr && bytes) {
-    // Slots are tagged with per-call epochs starting at 1; a zeroed buffer
-    // holds no slot that a call could mistake for its own.
+    // The pool counter must start at zero; zero the whole buffer.
     cudaError_t e = cudaMemset(ptr, 0, bytes);
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
     if (e != cudaSuccess) return cuda_fail(e, "zeroing the workspace");
@@ -397,8 +397,7 @@ pa_status pa_decode_workspace_size(int64_t batch, int32_t num_q_heads, int32_t n
   int64_t workers = static_cast<int64_t>(st->num_sms) * kMaxCtasPerSm * kWarpsPerCta;
   const int cap = g_tune_max_ctas.load();
   if (cap > 0 && cap * kWarpsPerCta < workers) workers = static_cast<int64_t>(cap) * kWarpsPerCta;
-  *bytes = ws_layout(batch, num_kv_heads, num_q_heads / num_kv_heads, head_dim, workers,
-                     tuned_steal_slots()).total;
+  *bytes = ws_layout(batch, num_kv_heads, num_q_heads / num_kv_heads, head_dim, workers).total;
   return ok();
 }
 
@@ -561,7 +560,7 @@ pa_status pa_decode(const pa_tensor* out, const pa_tensor* q, const pa_tensor* k
   DecodePlan plan;
   WsLayout layout;
   void* ws = nullptr;
-  uint32_t epoch = 0;
+  Workspace* wsp = nullptr;
   {
     std::lock_guard<std::mutex> lk(g_mu);
     if ((s = device_state(&st, &dev))) return s;
@@ -569,9 +568,8 @@ pa_status pa_decode(const pa_tensor* out, const pa_tensor* q, const pa_tensor* k
     if ((s = plan_decode(st, dev, ct, q->dtype, B, static_cast<int>(Hq), static_cast<int>(Hkv),
                          static_cast<int>(D), &plan)))
       return s;
-    layout = ws_layout(B, static_cast<int>(Hkv), plan.G, static_cast<int>(D), plan.workers,
-                       plan.steal_slots);
-    if ((s = get_workspace(st, cs, layout.total, &ws, &epoch))) return s;
+    layout = ws_layout(B, static_cast<int>(Hkv), plan.G, static_cast<int>(D), plan.workers);
+    if ((s = get_workspace(st, cs, layout, &ws, &wsp))) return s;
   }
   const int elt = fp8 ? 1 : 2;
   CUtensorMap tk, tv;
@@ -586,14 +584,9 @@ pa_status pa_decode(const pa_tensor* out, const pa_tensor* q, const pa_tensor* k
   a.seq_lens = static_cast<const int32_t*>(seq_lens->data);
   char* wsb = static_cast<char*>(ws);
   a.ctrl = reinterpret_cast<int32_t*>(wsb + layout.ctrl);
-  a.words = reinterpret_cast<unsigned long long*>(wsb + layout.words);
-  a.wepoch = reinterpret_cast<uint32_t*>(wsb + layout.wepoch);
-  a.heads = reinterpret_cast<unsigned long long*>(wsb + layout.heads);
-  a.tags = reinterpret_cast<uint32_t*>(wsb + layout.tags);
-  a.next = reinterpret_cast<uint32_t*>(wsb + layout.next);
+  a.pool = reinterpret_cast<uint32_t*>(wsb + layout.pool);
   a.part = reinterpret_cast<float*>(wsb + layout.part);
   a.err = st->err_word;
-  a.epoch = epoch;
   a.B = static_cast<int>(B);
   a.Hq = static_cast<int>(Hq);
   a.Hkv = static_cast<int>(Hkv);
@@ -607,8 +600,9 @@ pa_status pa_decode(const pa_tensor* out, const pa_tensor* q, const pa_tensor* k
                                      (fp8 ? static_cast<double>(k_scale) : 1.0));
   a.v_scale = fp8 ? v_scale : 1.f;
   a.min_tiles = plan.min_tiles;
-  a.claim = plan.claim;
-  a.steal_slots = plan.steal_slots;
+  a.pool_permille = plan.pool_permille;
+  a.piece_min = plan.piece;
+  a.np_max = plan.workers * kPiecesPerWorker;
 
   const bool prof = g_prof_before && g_prof_after;
   cudaError_t e;
@@ -623,10 +617,7 @@ pa_status pa_decode(const pa_tensor* out, const pa_tensor* q, const pa_tensor* k
   m.out = out->data;
   m.part = a.part;
   m.ctrl = a.ctrl;
-  m.heads = a.heads;
-  m.tags = a.tags;
-  m.next = a.next;
-  m.epoch = epoch;
+  m.pool = a.pool;
   m.NW = plan.workers;
   m.B = a.B;
   m.Hq = a.Hq;
@@ -634,7 +625,11 @@ pa_status pa_decode(const pa_tensor* out, const pa_tensor* q, const pa_tensor* k
   m.G = a.G;
   m.D = a.D;
   e = pa::merge_launch(q->dtype, m, cs, !prof);
-  if (e != cudaSuccess) return cuda_fail(e, "merge kernel launch");
+  if (e != cudaSuccess) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    wsp->dirty = true;  // the decode kernel ran; its pool counter was not reset
+    return cuda_fail(e, "merge kernel launch");
+  }
   g_launches += 2;
   return ok();
 }

@@ -14,46 +14,39 @@ enum ElemType { kF16 = 0, kBF16 = 1, kE4M3 = 2 };
 constexpr int kTile = 16;  // tokens per pipeline tile (one mma m-tile)
 
 // Decode workspace layout (device memory, all sections 256-byte aligned):
-//   ctrl   int32 [4 + B + 1]: [0] static tiles per warp, [1] total tiles,
-//          [2] claim size, [3] steal slots per warp, [4..] tile prefix
-//   words  u64 [NW]   per-warp range word (head << 32 | tail)
-//   wepoch u32 [NW]   epoch in which the warp's word was initialised
-//   heads  u64 [S]    per-pair list of stolen partials (epoch << 32 | slot)
-//   tags   u32 [NSLOT] epoch of the last write of each partial slot
-//   next   u32 [NSLOT] list link of stolen partial slots
-//   part   f32 [NSLOT][G][D + 2]: acc[G][D], m[G], l[G]
-// with S = B * Hkv pairs, NW worker warps, NSLOT = S + NW + NW * K.
-// Slots [0, S + NW) hold owner segments (pair s of warp w at s + w); slots
-// [S + NW + w * K, S + NW + (w + 1) * K) hold the segments warp w stole.
+//   ctrl  int32 [4 + B + 1]: [0] static tiles per warp (ws), [1] total tiles,
+//         [2] end of the static region (Ts), [3] pool piece size (P),
+//         [4..] tile prefix over the sequences
+//   pool  u32: pool piece counter; zero between calls (the merge kernel
+//         resets it after each step)
+//   part  f32 [NSLOT][G][D + 2]: acc[G][D], m[G], l[G]
+// with S = B * Hkv pairs, NW worker warps, NSLOT = 2 S + NW + NPMAX.
+// A segment is a run of one warp's tiles inside one pair. Static segments of
+// pair s by warp w use slot s + w; segments of pool piece i use slot
+// S + NW + s + i. Both are unique because the walk through the (pair, warp)
+// and (pair, piece) grids is a monotone staircase.
 struct DecodeArgs {
   const void* q;                 // [B, Hq, D]
   const int32_t* block_tables;   // [B, MB]
   const int32_t* seq_lens;       // [B]
   int32_t* ctrl;
-  unsigned long long* words;
-  uint32_t* wepoch;
-  unsigned long long* heads;
-  uint32_t* tags;
-  uint32_t* next;
+  uint32_t* pool;
   float* part;
   int32_t* err;                  // device error word
-  uint32_t epoch;                // differs on every call that shares this workspace
   int B, Hq, Hkv, G, D, bs, MB, NB, window;
   float score_scale;             // scale * log2(e) (* k_scale for FP8)
   float v_scale;                 // FP8: applied to the partial outputs
   int min_tiles;                 // least tiles per warp in the static split
-  int claim;                     // tiles per owner claim and largest steal
-  int steal_slots;               // K: partial slots per warp for stolen work
+  int pool_permille;             // share of tiles handed out dynamically
+  int piece_min;                 // least tiles per pool piece
+  int np_max;                    // most pool pieces (bounds the slots)
 };
 
 struct MergeArgs {
   void* out;                     // [B, Hq, D], dtype of q
   const float* part;
   const int32_t* ctrl;
-  const unsigned long long* heads;
-  const uint32_t* tags;
-  const uint32_t* next;
-  uint32_t epoch;
+  uint32_t* pool;                // reset to zero for the next step
   int B, Hq, Hkv, G, D, NW;
 };
 

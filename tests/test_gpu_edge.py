@@ -70,8 +70,8 @@ def test_edge_shapes(case, pa_lib):
     assert pa_lib.check_device_error() == 0
 
 
-@pytest.mark.parametrize("tuning", [(1, 0), (0, 1), (3, 2), (7, 5), (0, 0, 1, 64),
-                                    (5, 1, 1, 256), (0, 0, 0, -1), (2, 3, 2, -1)])
+@pytest.mark.parametrize("tuning", [(1, 0), (0, 1), (3, 2), (7, 5), (0, 0, 900, 1),
+                                    (5, 1, 500, 1), (0, 0, -1, 0), (2, 3, -1, 0), (1, 1, 1000, 2)])
 @pytest.mark.parametrize("case", [dict(), dict(kv_fp8=True, window=45),
                                   dict(num_q_heads=24, num_kv_heads=2, block_size=32)])
 def test_forced_worker_layouts(tuning, case, pa_lib):
@@ -83,25 +83,25 @@ def test_forced_worker_layouts(tuning, case, pa_lib):
     assert_close(out_f64(sides.out), sides.ref, what=f"{tuning} {case}")
 
 
-def test_stealing_stress_matches_oracle_and_deterministic_mode_is_reproducible(pa_lib):
-    """One-tile claims with many steal slots (every warp steals constantly),
-    then stealing off: both match the oracle, and the off mode repeats bit for
-    bit."""
+def test_pool_stress_matches_oracle_and_static_mode_is_reproducible(pa_lib):
+    """90% of the tiles in one-tile pool pieces (every warp claims constantly),
+    then the pool off: both match the oracle, and the static mode repeats bit
+    for bit."""
     s = spec(seq_lens=(5000, 3, 0, 700, 16, 2048, 1, 900), num_q_heads=16, num_kv_heads=4)
-    pa_lib.set_decode_tuning(0, 1, 1, 512)
+    pa_lib.set_decode_tuning(0, 1, 900, 1)
     try:
         sides = run_both(s)
-        assert_close(out_f64(sides.out), sides.ref, what="steal stress")
+        assert_close(out_f64(sides.out), sides.ref, what="pool stress")
         w = sides.w
         bt = torch.from_numpy(w.block_tables).cuda()
         sl = torch.from_numpy(w.seq_lens).cuda()
         kw = dict(num_kv_heads=4, scale=s.softmax_scale, block_size=16)
-        pa_lib.set_decode_tuning(0, 0, 0, -1)
+        pa_lib.set_decode_tuning(0, 0, -1, 0)
         o1 = pa_lib.decode(w.q, sides.kc, sides.vc, bt, sl, **kw)
         o2 = pa_lib.decode(w.q, sides.kc, sides.vc, bt, sl, **kw)
         torch.cuda.synchronize()
         assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))
-        assert_close(out_f64(o1), sides.ref, what="no stealing")
+        assert_close(out_f64(o1), sides.ref, what="static only")
     finally:
         pa_lib.set_decode_tuning(0, 0, 0, 0)
 
@@ -187,13 +187,13 @@ def test_caller_owned_workspace(pa_lib):
         pa_lib.set_workspace(None)
 
 
-@pytest.mark.parametrize("steal", [False, True])
-def test_cuda_graph_replay_matches_eager(steal, pa_lib):
-    """Replay equals eager bit for bit with stealing off; with stealing on the
+@pytest.mark.parametrize("pool", [False, True])
+def test_cuda_graph_replay_matches_eager(pool, pa_lib):
+    """Replay equals eager bit for bit with the dynamic pool off; with it on the
     segment boundaries (and so the rounding) may differ between runs."""
-    pa_lib.set_decode_tuning(0, 0, 0, 0 if steal else -1)
+    pa_lib.set_decode_tuning(0, 0, 0 if pool else -1, 0)
     try:
-        _graph_vs_eager(pa_lib, exact=not steal)
+        _graph_vs_eager(pa_lib, exact=not pool)
     finally:
         pa_lib.set_decode_tuning(0, 0, 0, 0)
 

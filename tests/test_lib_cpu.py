@@ -98,7 +98,8 @@ def test_host_validation_rejects_bad_arguments_without_a_device(pa_lib):
     assert L.pa_reshape_and_cache(*[ctypes.byref(x) for x in (k, v, kc, vc, sm64)], 2, 1.0, 1.0,
                                   None) == -1                      # fp8 requested, f16 cache
     assert pa.lib().pa_set_decode_tuning(-1, 0, 0, 0) == -1
-    assert pa.lib().pa_set_decode_tuning(0, 0, -2, 0) == -1
+    assert pa.lib().pa_set_decode_tuning(0, 0, 0, -2) == -1
+    assert pa.lib().pa_set_decode_tuning(0, 0, 1001, 0) == -1
     assert pa.lib().pa_profile_events(ctypes.c_void_p(1), None) == -1
 
 
