@@ -160,8 +160,10 @@ WsLayout ws_layout(int64_t B, int Hkv, int G, int D, int64_t workers) {
   const size_t nslot = 2 * S + workers + static_cast<size_t>(workers) * kPiecesPerWorker;
   WsLayout L;
   size_t o = 0;
-  L.ctrl = o;  o += round_up(static_cast<size_t>(B + 5) * sizeof(int32_t), 256);
+  // The pool counter sits at a fixed offset: it must stay zero between calls
+  // whatever their shapes, and each step's merge only resets its own copy.
   L.pool = o;  o += 256;
+  L.ctrl = o;  o += round_up(static_cast<size_t>(B + 5) * sizeof(int32_t), 256);
   L.part = o;  o += nslot * static_cast<size_t>(G) * (D + 2) * sizeof(float);
   L.total = o;
   return L;

@@ -14,11 +14,11 @@ enum ElemType { kF16 = 0, kBF16 = 1, kE4M3 = 2 };
 constexpr int kTile = 16;  // tokens per pipeline tile (one mma m-tile)
 
 // Decode workspace layout (device memory, all sections 256-byte aligned):
+//   pool  u32 at offset 0: pool piece counter; zero between calls (the merge
+//         kernel resets it after each step), at the same place for any shape
 //   ctrl  int32 [4 + B + 1]: [0] static tiles per warp (ws), [1] total tiles,
 //         [2] end of the static region (Ts), [3] pool piece size (P),
 //         [4..] tile prefix over the sequences
-//   pool  u32: pool piece counter; zero between calls (the merge kernel
-//         resets it after each step)
 //   part  f32 [NSLOT][G][D + 2]: acc[G][D], m[G], l[G]
 // with S = B * Hkv pairs, NW worker warps, NSLOT = 2 S + NW + NPMAX.
 // A segment is a run of one warp's tiles inside one pair. Static segments of

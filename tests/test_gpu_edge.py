@@ -254,3 +254,19 @@ def test_allocator_built_layout_with_sharing_and_cow(pa_lib):
                         scale=D ** -0.5, block_size=bs, q_dtype="bf16", cache_dtype="bf16")
     assert_close(out_f64(out), ref, what="allocator layout")
     assert (lens == np.array([50, 60, 70, 80])).all()
+
+
+def test_calls_with_different_batches_share_one_workspace(pa_lib):
+    """Consecutive steps of different shapes on one stream reuse the
+    library's workspace; the dynamic pool must start from zero each time."""
+    specs = [spec(seq_lens=(3000, 17, 900)), spec(seq_lens=RAGGED),
+             spec(seq_lens=(5000,) * 9, num_q_heads=16, num_kv_heads=4),
+             spec(seq_lens=(1200, 1, 2000, 33))]
+    pa_lib.set_decode_tuning(0, 1, 300, 1)
+    try:
+        for _ in range(2):
+            for sp in specs:
+                sides = run_both(sp)
+                assert_close(out_f64(sides.out), sides.ref, what=f"B={sp.batch}")
+    finally:
+        pa_lib.set_decode_tuning(0, 0, 0, 0)
