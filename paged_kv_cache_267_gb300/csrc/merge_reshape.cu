@@ -18,115 +18,192 @@ cudaError_t device_error_word(int32_t** ptr) {
 
 // ------------------------------------------------------------------ merge
 //
-// One CTA per (pair, q head of the group); each thread owns two head dims.
-// The partials of pair s (tiles [F, F + nt) of the flat space) are the static
-// slots s + w of the warps w whose static range meets [F, min(F + nt, Ts)),
-// and the pool slots S + NW + s + i of the pieces i that meet [max(F, Ts),
-// F + nt). With partial maxima m_p (log2 domain), sums l_p and unnormalised
-// outputs o_p:
-//   out = sum_p 2^(m_p - M) o_p / sum_p 2^(m_p - M) l_p,  M = max_p m_p,
-// evaluated in chunks with a running maximum, so any number of partials
-// works. A pair with no tiles (seq_len 0) gets zeros. Block (0, 0) also
-// resets the pool counter for the next step.
-constexpr int kMergeChunk = 256;
+// Partials of pair s (tiles [F, F + nt) of the flat space) are its candidates:
+// the static slots s + w of the warps w whose static range meets
+// [F, min(F + nt, Ts)), then the pool slots S + NW + s + i of the pieces i
+// that meet [max(F, Ts), F + nt). With partial maxima m_p (log2 domain), sums
+// l_p and unnormalised outputs o_p the result is
+//   out = sum_p 2^(m_p - M) o_p / sum_p 2^(m_p - M) l_p,  M = max_p m_p.
+// Work units are (group g of candidates, pair s, chunk c of 512 (head, dim)
+// elements), spread over a persistent grid. A unit combines its group with all
+// eight warps (each warp a strided subset, online in registers, then across
+// warps in shared memory). A pair whose candidates fit one group is written
+// out directly. Otherwise each unit stores its group result, which has the
+// same form as a partial, in place in the slot of the group's first
+// candidate; the unit that completes the (pair, chunk) counter combines the
+// group results and resets the counter. Pairs without tiles get zeros.
+constexpr int kMergeThreads = 256;
+constexpr int kMergeWarps = kMergeThreads / 32;
+
+struct MergeSmem {
+  float M[kMergeWarps][kMergeChunk / 4];
+  float den[kMergeWarps][kMergeChunk / 4];
+  float acc[kMergeWarps][kMergeChunk];
+  int last;
+};
+
+// Combines candidates k0, k0 + step, ... (< k1) of one pair for chunk c; on
+// return every thread holds the combined (M, den, acc) of its two elements
+// el = 2 * tid, 2 * tid + 1 of the chunk (M, den per element's head).
+template <typename SlotFn>
+__device__ __forceinline__ void merge_combine(const MergeArgs& a, MergeSmem& sm, SlotFn slot_of,
+                                              int k0, int k1, int step, int c, float (&rM)[2],
+                                              float (&rden)[2], float (&racc)[2]) {
+  const int tid = threadIdx.x, wp = tid >> 5, lane = tid & 31;
+  const int GD = a.G * a.D;
+  const size_t stride = static_cast<size_t>(a.G) * (a.D + 2);
+  float M[4], den[4];
+  float4 acc[4];
+  int eq[4], hq[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    M[q] = -INFINITY;
+    den[q] = 0.f;
+    acc[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+    eq[q] = c * kMergeChunk + q * 128 + lane * 4;
+    hq[q] = eq[q] / a.D;
+  }
+  for (int k = k0 + wp * step; k < k1; k += kMergeWarps * step) {
+    const float* P = a.part + static_cast<size_t>(slot_of(k)) * stride;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      if (eq[q] >= GD || eq[q] >= (c + 1) * kMergeChunk) continue;
+      const float mm = P[GD + hq[q]], ll = P[GD + a.G + hq[q]];
+      const float4 o = *reinterpret_cast<const float4*>(P + eq[q]);
+      const float Mn = fmaxf(M[q], mm);
+      const float sc = exp2f(M[q] - Mn), f = exp2f(mm - Mn);
+      den[q] = den[q] * sc + f * ll;
+      acc[q].x = acc[q].x * sc + f * o.x;
+      acc[q].y = acc[q].y * sc + f * o.y;
+      acc[q].z = acc[q].z * sc + f * o.z;
+      acc[q].w = acc[q].w * sc + f * o.w;
+      M[q] = Mn;
+    }
+  }
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    sm.M[wp][q * 32 + lane] = M[q];
+    sm.den[wp][q * 32 + lane] = den[q];
+    *reinterpret_cast<float4*>(&sm.acc[wp][q * 128 + lane * 4]) = acc[q];
+  }
+  __syncthreads();
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    const int el = 2 * tid + j, gi = el >> 2;
+    float Ms = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kMergeWarps; ++w) Ms = fmaxf(Ms, sm.M[w][gi]);
+    float d = 0.f, x = 0.f;
+#pragma unroll
+    for (int w = 0; w < kMergeWarps; ++w) {
+      const float f = exp2f(sm.M[w][gi] - Ms);  // 0 for warps without candidates
+      d += f * sm.den[w][gi];
+      x += f * sm.acc[w][el];
+    }
+    rM[j] = Ms;
+    rden[j] = d;
+    racc[j] = x;
+  }
+  __syncthreads();
+}
 
 template <int OT>
-__global__ void __launch_bounds__(128) merge_kernel(const MergeArgs a) {
-  __shared__ uint32_t s_slot[kMergeChunk];
-  __shared__ float s_fac[kMergeChunk];
-  __shared__ float s_M, s_den, s_scale;
-  griddep_wait();
-  const int s = blockIdx.x, h = blockIdx.y;
-  const int b = s / a.Hkv, kvh = s - b * a.Hkv;
-  const int tid = threadIdx.x;
-  const int d = 2 * tid;
-  if (s == 0 && h == 0 && tid == 0) *a.pool = 0u;
-  const size_t orow = (static_cast<size_t>(b) * a.Hq + kvh * a.G + h) * a.D + d;
-  const int ws = a.ctrl[0], ts = a.ctrl[2], piece = a.ctrl[3];
-  const int pb = a.ctrl[4 + b], nt = a.ctrl[5 + b] - pb;
-  const int S = a.B * a.Hkv;
-  float n0 = 0.f, n1 = 0.f, r0 = 0.f, r1 = 0.f;
-  if (nt > 0) {
-    const int F = a.Hkv * pb + kvh * nt;
-    // candidate slots: static warps [w0, w1], then pool pieces [i0, i1]
-    int w0 = 0, w1 = -1, i0 = 0, i1 = -1;
-    if (F < ts) {
-      w0 = F / ws;
-      w1 = (min(F + nt, ts) - 1) / ws;
-    }
-    if (F + nt > ts) {
-      i0 = (max(F, ts) - ts) / piece;
-      i1 = (F + nt - 1 - ts) / piece;
-    }
-    const int na = w1 - w0 + 1, np = i1 - i0 + 1, ntot = na + np;
-    const size_t stride = static_cast<size_t>(a.G) * (a.D + 2);
-    const int mo = a.G * a.D + h, lo = a.G * a.D + a.G + h;
-    if (tid == 0) {
-      s_M = -INFINITY;
-      s_den = 0.f;
-    }
-    for (int c0 = 0; c0 < ntot; c0 += kMergeChunk) {
-      const int n = min(kMergeChunk, ntot - c0);
-      for (int i = tid; i < n; i += blockDim.x) {
-        const int k = c0 + i;
-        s_slot[i] = (k < na) ? static_cast<uint32_t>(s + w0 + k)
-                             : static_cast<uint32_t>(S + a.NW + s + i0 + (k - na));
-      }
-      __syncthreads();
-      if (tid < 32) {
-        float mx = -INFINITY;
-        for (int i = tid; i < n; i += 32) mx = fmaxf(mx, a.part[s_slot[i] * stride + mo]);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-        const float Mn = fmaxf(s_M, mx);
-        float den = 0.f;
-        for (int i = tid; i < n; i += 32) {
-          const float* P = a.part + s_slot[i] * stride;
-          const float fct = exp2f(P[mo] - Mn);
-          s_fac[i] = fct;
-          den += fct * P[lo];
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
-        if (tid == 0) {
-          const float sc = exp2f(s_M - Mn);  // 0 on the first chunk
-          s_scale = sc;
-          s_den = s_den * sc + den;
-          s_M = Mn;
-        }
-      }
-      __syncthreads();
-      if (d < a.D) {
-        const float sc = s_scale;
-        n0 *= sc;
-        n1 *= sc;
-        for (int i = 0; i < n; ++i) {
-          const float2 o =
-              *reinterpret_cast<const float2*>(a.part + s_slot[i] * stride + h * a.D + d);
-          n0 += s_fac[i] * o.x;
-          n1 += s_fac[i] * o.y;
-        }
-      }
-      __syncthreads();
-    }
-    const float den = s_den;
-    r0 = n0 / den;
-    r1 = n1 / den;
-  }
-  if (d >= a.D) return;
+__device__ __forceinline__ void store_out2(void* out, size_t idx, float x0, float x1) {
   if constexpr (OT == kBF16) {
-    *reinterpret_cast<__nv_bfloat162*>(reinterpret_cast<__nv_bfloat16*>(a.out) + orow) =
-        __floats2bfloat162_rn(r0, r1);
+    *reinterpret_cast<__nv_bfloat162*>(reinterpret_cast<__nv_bfloat16*>(out) + idx) =
+        __floats2bfloat162_rn(x0, x1);
   } else {
-    *reinterpret_cast<__half2*>(reinterpret_cast<__half*>(a.out) + orow) =
-        __floats2half2_rn(r0, r1);
+    *reinterpret_cast<__half2*>(reinterpret_cast<__half*>(out) + idx) = __floats2half2_rn(x0, x1);
   }
 }
 
-cudaError_t merge_launch(int out_type, const MergeArgs& a, cudaStream_t s, bool pdl) {
+template <int OT>
+__global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeArgs a) {
+  extern __shared__ int s_pref[];  // B + 1
+  __shared__ MergeSmem sm;
+  griddep_wait();
+  const int tid = threadIdx.x;
+  if (blockIdx.x == 0 && tid == 0) *a.pool = 0u;
+  const int ws = a.ctrl[0], ts = a.ctrl[2], piece = a.ctrl[3];
+  for (int i = tid; i <= a.B; i += blockDim.x) s_pref[i] = a.ctrl[4 + i];
+  __syncthreads();
+  const int S = a.B * a.Hkv, GD = a.G * a.D;
+  const int nchunk = (GD + kMergeChunk - 1) / kMergeChunk;
+  const long long units = static_cast<long long>(kMergeGroupsMax) * S * nchunk;
+  for (long long u = blockIdx.x; u < units; u += gridDim.x) {
+    const int g = static_cast<int>(u / (static_cast<long long>(S) * nchunk));
+    const int r = static_cast<int>(u % (static_cast<long long>(S) * nchunk));
+    const int s = r / nchunk, c = r - (r / nchunk) * nchunk;
+    const int b = s / a.Hkv, kvh = s - b * a.Hkv;
+    const int nt = s_pref[b + 1] - s_pref[b];
+    const int F = a.Hkv * s_pref[b] + kvh * nt;
+    int w0 = 0, na = 0, i0 = 0, np = 0;
+    if (nt > 0 && F < ts) {
+      w0 = F / ws;
+      na = (min(F + nt, ts) - 1) / ws - w0 + 1;
+    }
+    if (nt > 0 && F + nt > ts) {
+      i0 = (max(F, ts) - ts) / piece;
+      np = (F + nt - 1 - ts) / piece - i0 + 1;
+    }
+    const int ncand = na + np;
+    int gsz = (ncand + kMergeGroupsMax - 1) / kMergeGroupsMax;
+    if (gsz < kMergeGroupMin) gsz = kMergeGroupMin;
+    const int ngroups = ncand > 0 ? (ncand + gsz - 1) / gsz : 1;
+    if (g >= ngroups) continue;
+    const size_t obase = (static_cast<size_t>(b) * a.Hq + kvh * a.G) * a.D;
+    const int e0 = c * kMergeChunk + 2 * tid;
+    if (ncand == 0) {
+      if (e0 < GD) store_out2<OT>(a.out, obase + e0, 0.f, 0.f);
+      continue;
+    }
+    auto slot_of = [&](int k) -> int {
+      return k < na ? s + w0 + k : S + a.NW + s + i0 + (k - na);
+    };
+    float rM[2], rden[2], racc[2];
+    const int k0 = g * gsz, k1 = min(k0 + gsz, ncand);
+    merge_combine(a, sm, slot_of, k0, k1, 1, c, rM, rden, racc);
+    if (ngroups == 1) {
+      if (e0 < GD) store_out2<OT>(a.out, obase + e0, racc[0] / rden[0], racc[1] / rden[1]);
+      continue;
+    }
+    // group result, in place in the slot of the group's first candidate
+    {
+      const size_t stride = static_cast<size_t>(a.G) * (a.D + 2);
+      float* P = a.part + static_cast<size_t>(slot_of(k0)) * stride;
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int e = e0 + j;
+        if (e < GD) {
+          P[e] = racc[j];
+          if (e % a.D == 0) {
+            P[GD + e / a.D] = rM[j];
+            P[GD + a.G + e / a.D] = rden[j];
+          }
+        }
+      }
+    }
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) {
+      const uint32_t done = atomicAdd(a.counters + static_cast<size_t>(s) * nchunk + c, 1u) + 1;
+      sm.last = (done == static_cast<uint32_t>(ngroups));
+      if (sm.last) a.counters[static_cast<size_t>(s) * nchunk + c] = 0u;
+    }
+    __syncthreads();
+    if (!sm.last) continue;
+    __threadfence();
+    // combine the group results (first candidate of each group)
+    merge_combine(a, sm, slot_of, 0, ngroups * gsz, gsz, c, rM, rden, racc);
+    if (e0 < GD) store_out2<OT>(a.out, obase + e0, racc[0] / rden[0], racc[1] / rden[1]);
+  }
+}
+
+cudaError_t merge_launch(int out_type, const MergeArgs& a, int grid, cudaStream_t s, bool pdl) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(a.B * a.Hkv, a.G);
-  cfg.blockDim = dim3((a.D / 2 + 31) / 32 * 32);
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kMergeThreads);
+  cfg.dynamicSmemBytes = static_cast<size_t>(a.B + 1) * sizeof(int);
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

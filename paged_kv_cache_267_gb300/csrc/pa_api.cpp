@@ -152,7 +152,7 @@ size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // Section offsets of the decode workspace (layout described in pa_internal.h).
 struct WsLayout {
-  size_t ctrl, pool, part, total;
+  size_t pool, counters, ctrl, part, total;
 };
 
 WsLayout ws_layout(int64_t B, int Hkv, int G, int D, int64_t workers) {
@@ -162,7 +162,8 @@ WsLayout ws_layout(int64_t B, int Hkv, int G, int D, int64_t workers) {
   size_t o = 0;
   // The pool counter sits at a fixed offset: it must stay zero between calls
   // whatever their shapes, and each step's merge only resets its own copy.
-  L.pool = o;  o += 256;
+  L.pool = o;      o += 256;
+  L.counters = o;  o += static_cast<size_t>(pa::kMaxMergeCounters) * sizeof(uint32_t);
   L.ctrl = o;  o += round_up(static_cast<size_t>(B + 5) * sizeof(int32_t), 256);
   L.part = o;  o += nslot * static_cast<size_t>(G) * (D + 2) * sizeof(float);
   L.total = o;
@@ -325,7 +326,8 @@ pa_status get_workspace(DeviceState* st, cudaStream_t stream, const WsLayout& la
     }
   }
   if (w->dirty) {
-    cudaError_t e = cudaMemsetAsync(static_cast<char*>(w->ptr) + lay.pool, 0, 256, stream);
+    cudaError_t e = cudaMemsetAsync(static_cast<char*>(w->ptr) + lay.pool, 0,
+                                    lay.ctrl - lay.pool, stream);
     if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(pool counter)");
     w->dirty = false;
   }
@@ -552,6 +554,8 @@ pa_status pa_decode(const pa_tensor* out, const pa_tensor* q, const pa_tensor* k
     return fail(PA_ERR_UNSUPPORTED, "pool or tables exceed 32-bit indexing");
   for (const pa_tensor* x : {q, key_cache, value_cache, block_tables, seq_lens})
     if (overlaps(out, x)) return fail(PA_ERR_INVALID_ARG, "out overlaps an input");
+  if (B * Hkv * ((Hq / Hkv * D + pa::kMergeChunk - 1) / pa::kMergeChunk) > pa::kMaxMergeCounters)
+    return fail(PA_ERR_UNSUPPORTED, "batch * num_kv_heads too large");
   if (B == 0) return ok();
   if (MB == 0) return fail(PA_ERR_INVALID_ARG, "block_tables has no columns");
   if (NB == 0) return fail(PA_ERR_INVALID_ARG, "empty block pool");
@@ -620,13 +624,14 @@ pa_status pa_decode(const pa_tensor* out, const pa_tensor* q, const pa_tensor* k
   m.part = a.part;
   m.ctrl = a.ctrl;
   m.pool = a.pool;
+  m.counters = reinterpret_cast<uint32_t*>(wsb + layout.counters);
   m.NW = plan.workers;
   m.B = a.B;
   m.Hq = a.Hq;
   m.Hkv = a.Hkv;
   m.G = a.G;
   m.D = a.D;
-  e = pa::merge_launch(q->dtype, m, cs, !prof);
+  e = pa::merge_launch(q->dtype, m, st->num_sms * 2, cs, !prof);
   if (e != cudaSuccess) {
     std::lock_guard<std::mutex> lk(g_mu);
     wsp->dirty = true;  // the decode kernel ran; its pool counter was not reset

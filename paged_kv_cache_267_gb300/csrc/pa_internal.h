@@ -16,6 +16,8 @@ constexpr int kTile = 16;  // tokens per pipeline tile (one mma m-tile)
 // Decode workspace layout (device memory, all sections 256-byte aligned):
 //   pool  u32 at offset 0: pool piece counter; zero between calls (the merge
 //         kernel resets it after each step), at the same place for any shape
+//   cnt   u32 [kMaxMergeCounters] at offset 256: merge group counters, zero
+//         between calls (each is reset by the unit that finds it complete)
 //   ctrl  int32 [4 + B + 1]: [0] static tiles per warp (ws), [1] total tiles,
 //         [2] end of the static region (Ts), [3] pool piece size (P),
 //         [4..] tile prefix over the sequences
@@ -44,11 +46,17 @@ struct DecodeArgs {
 
 struct MergeArgs {
   void* out;                     // [B, Hq, D], dtype of q
-  const float* part;
+  float* part;                   // group results are written in place
   const int32_t* ctrl;
   uint32_t* pool;                // reset to zero for the next step
+  uint32_t* counters;            // [S * chunks] groups done per (pair, chunk); left at zero
   int B, Hq, Hkv, G, D, NW;
 };
+
+constexpr int kMergeChunk = 512;      // (head, dim) elements per merge unit
+constexpr int kMergeGroupsMax = 16;   // groups of partials per (pair, chunk), at most
+constexpr int kMergeGroupMin = 16;    // partials per group, at least
+constexpr int kMaxMergeCounters = 1 << 19;
 
 struct ReshapeArgs {
   const void* k;
@@ -87,7 +95,7 @@ cudaError_t decode_launch_fp8(int qt, int D, int nt, const CUtensorMap& tk,
                               cudaStream_t s, bool pdl);
 
 // merge_reshape.cu
-cudaError_t merge_launch(int out_type, const MergeArgs& a, cudaStream_t s, bool pdl);
+cudaError_t merge_launch(int out_type, const MergeArgs& a, int grid, cudaStream_t s, bool pdl);
 cudaError_t reshape_launch(int src_type, bool fp8, const ReshapeArgs& a, cudaStream_t s);
 cudaError_t device_error_word(int32_t** ptr);  // address of this device's error word
 
