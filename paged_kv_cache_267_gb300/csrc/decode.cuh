@@ -562,7 +562,7 @@ __global__ void __launch_bounds__(WARPS * 32)
       const size_t pslot = (flags & kFlagPool)
                                ? static_cast<size_t>(npairs) + nw + pair + piece_id
                                : static_cast<size_t>(pair) + w;
-      float* P = a.part + pslot * (a.G * (D + 2));
+      float* P = a.part + pslot * part_stride(a.G, D);
       const float vs = kFp8 ? a.v_scale : 1.f;
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {

@@ -35,7 +35,7 @@ cudaError_t device_error_word(int32_t** ptr) {
 constexpr int kMergeThreads = 256;
 constexpr int kMergeWarps = kMergeThreads / 32;
 
-struct MergeSmem {
+struct __align__(16) MergeSmem {
   float M[kMergeWarps][kMergeChunk / 4];
   float den[kMergeWarps][kMergeChunk / 4];
   float acc[kMergeWarps][kMergeChunk];
@@ -51,7 +51,7 @@ __device__ __forceinline__ void merge_combine(const MergeArgs& a, MergeSmem& sm,
                                               float (&rden)[2], float (&racc)[2]) {
   const int tid = threadIdx.x, wp = tid >> 5, lane = tid & 31;
   const int GD = a.G * a.D;
-  const size_t stride = static_cast<size_t>(a.G) * (a.D + 2);
+  const size_t stride = static_cast<size_t>(part_stride(a.G, a.D));
   float M[4], den[4];
   float4 acc[4];
   int eq[4], hq[4];
@@ -169,7 +169,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeArgs a)
     }
     // group result, in place in the slot of the group's first candidate
     {
-      const size_t stride = static_cast<size_t>(a.G) * (a.D + 2);
+      const size_t stride = static_cast<size_t>(part_stride(a.G, a.D));
       float* P = a.part + static_cast<size_t>(slot_of(k0)) * stride;
 #pragma unroll
       for (int j = 0; j < 2; ++j) {

@@ -13,6 +13,12 @@ enum ElemType { kF16 = 0, kBF16 = 1, kE4M3 = 2 };
 
 constexpr int kTile = 16;  // tokens per pipeline tile (one mma m-tile)
 
+// Floats per decode partial slot: acc[G][D], m[G], l[G], rounded up to a
+// multiple of 4 so that slots can be read with 16-byte vector loads.
+__host__ __device__ constexpr inline int part_stride(int G, int D) {
+  return G * D + ((2 * G + 3) & ~3);
+}
+
 // Decode workspace layout (device memory, all sections 256-byte aligned):
 //   pool  u32 at offset 0: pool piece counter; zero between calls (the merge
 //         kernel resets it after each step), at the same place for any shape
@@ -21,7 +27,8 @@ constexpr int kTile = 16;  // tokens per pipeline tile (one mma m-tile)
 //   ctrl  int32 [4 + B + 1]: [0] static tiles per warp (ws), [1] total tiles,
 //         [2] end of the static region (Ts), [3] pool piece size (P),
 //         [4..] tile prefix over the sequences
-//   part  f32 [NSLOT][G][D + 2]: acc[G][D], m[G], l[G]
+//   part  f32 [NSLOT][part_stride(G, D)]: acc[G][D], m[G], l[G], padding to a
+//         multiple of 4 floats so every slot starts 16-byte aligned
 // with S = B * Hkv pairs, NW worker warps, NSLOT = 2 S + NW + NPMAX.
 // A segment is a run of one warp's tiles inside one pair. Static segments of
 // pair s by warp w use slot s + w; segments of pool piece i use slot
