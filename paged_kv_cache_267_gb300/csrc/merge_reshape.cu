@@ -22,118 +22,114 @@ cudaError_t device_error_word(int32_t** ptr) {
 // the static slots s + w of the warps w whose static range meets
 // [F, min(F + nt, Ts)), then the pool slots S + NW + s + i of the pieces i
 // that meet [max(F, Ts), F + nt). With partial maxima m_p (log2 domain), sums
-// l_p and unnormalised outputs o_p the result is
+// l_p and unnormalised outputs o_p the result for a q head is
 //   out = sum_p 2^(m_p - M) o_p / sum_p 2^(m_p - M) l_p,  M = max_p m_p.
-// Work units are (group g of candidates, pair s, chunk c of 512 (head, dim)
-// elements), spread over a persistent grid. A unit combines its group with all
-// eight warps (each warp a strided subset, online in registers, then across
-// warps in shared memory). A pair whose candidates fit one group is written
-// out directly. Otherwise each unit stores its group result, which has the
-// same form as a partial, in place in the slot of the group's first
-// candidate; the unit that completes the (pair, chunk) counter combines the
+// Work units are (group g of candidates, q head of pair s), one warp each,
+// spread over a persistent grid of many warps per SM so that the L2 latency
+// of one unit hides behind the others. A unit folds its candidates in online
+// (four loads in flight per lane). A head whose candidates fit one group is
+// written out directly; otherwise each unit stores its group result, which
+// has the same form as a partial, in place in the slot of the group's first
+// candidate, and the unit that completes the head's counter combines the
 // group results and resets the counter. Pairs without tiles get zeros.
 constexpr int kMergeThreads = 256;
 constexpr int kMergeWarps = kMergeThreads / 32;
 
-struct __align__(16) MergeSmem {
-  float M[kMergeWarps][kMergeChunk / 4];
-  float den[kMergeWarps][kMergeChunk / 4];
-  float acc[kMergeWarps][kMergeChunk];
-  int last;
+struct HeadAcc {
+  float M, den;
+  float4 acc[2];  // head dims v * 128 + 4 * lane .. + 3, v = 0, 1
 };
 
-// Combines candidates k0, k0 + step, ... (< k1) of one pair for chunk c; on
-// return every thread holds the combined (M, den, acc) of its two elements
-// el = 2 * tid, 2 * tid + 1 of the chunk (M, den per element's head).
+// Folds candidates k0, k0 + step, ... (< k1) of head h into `r`.
 template <typename SlotFn>
-__device__ __forceinline__ void merge_combine(const MergeArgs& a, MergeSmem& sm, SlotFn slot_of,
-                                              int k0, int k1, int step, int c, float (&rM)[2],
-                                              float (&rden)[2], float (&racc)[2]) {
-  const int tid = threadIdx.x, wp = tid >> 5, lane = tid & 31;
+__device__ __forceinline__ void merge_fold(const MergeArgs& a, SlotFn slot_of, int k0, int k1,
+                                           int step, int h, HeadAcc& r) {
+  const int lane = threadIdx.x & 31;
   const int GD = a.G * a.D;
   const size_t stride = static_cast<size_t>(part_stride(a.G, a.D));
-  float M[4], den[4];
-  float4 acc[4];
-  int eq[4], hq[4];
+  r.M = -INFINITY;
+  r.den = 0.f;
+  r.acc[0] = r.acc[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+  const bool v0 = 4 * lane < a.D, v1 = 128 + 4 * lane < a.D;
+  for (int k = k0; k < k1; k += 4 * step) {
+    float mm[4], ll[4];
+    float4 o0[4], o1[4];
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    M[q] = -INFINITY;
-    den[q] = 0.f;
-    acc[q] = make_float4(0.f, 0.f, 0.f, 0.f);
-    eq[q] = c * kMergeChunk + q * 128 + lane * 4;
-    hq[q] = eq[q] / a.D;
-  }
-  for (int k = k0 + wp * step; k < k1; k += kMergeWarps * step) {
-    const float* P = a.part + static_cast<size_t>(slot_of(k)) * stride;
+    for (int j = 0; j < 4; ++j) {
+      const int kk = k + j * step;
+      mm[j] = -INFINITY;
+      ll[j] = 0.f;
+      o0[j] = o1[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (kk < k1) {
+        const float* P = a.part + static_cast<size_t>(slot_of(kk)) * stride;
+        mm[j] = P[GD + h];
+        ll[j] = P[GD + a.G + h];
+        if (v0) o0[j] = *reinterpret_cast<const float4*>(P + h * a.D + 4 * lane);
+        if (v1) o1[j] = *reinterpret_cast<const float4*>(P + h * a.D + 128 + 4 * lane);
+      }
+    }
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      if (eq[q] >= GD || eq[q] >= (c + 1) * kMergeChunk) continue;
-      const float mm = P[GD + hq[q]], ll = P[GD + a.G + hq[q]];
-      const float4 o = *reinterpret_cast<const float4*>(P + eq[q]);
-      const float Mn = fmaxf(M[q], mm);
-      const float sc = exp2f(M[q] - Mn), f = exp2f(mm - Mn);
-      den[q] = den[q] * sc + f * ll;
-      acc[q].x = acc[q].x * sc + f * o.x;
-      acc[q].y = acc[q].y * sc + f * o.y;
-      acc[q].z = acc[q].z * sc + f * o.z;
-      acc[q].w = acc[q].w * sc + f * o.w;
-      M[q] = Mn;
+    for (int j = 0; j < 4; ++j) {
+      if (k + j * step >= k1) break;
+      const float Mn = fmaxf(r.M, mm[j]);
+      const float sc = exp2f(r.M - Mn), f = exp2f(mm[j] - Mn);
+      r.den = r.den * sc + f * ll[j];
+      r.acc[0].x = r.acc[0].x * sc + f * o0[j].x;
+      r.acc[0].y = r.acc[0].y * sc + f * o0[j].y;
+      r.acc[0].z = r.acc[0].z * sc + f * o0[j].z;
+      r.acc[0].w = r.acc[0].w * sc + f * o0[j].w;
+      r.acc[1].x = r.acc[1].x * sc + f * o1[j].x;
+      r.acc[1].y = r.acc[1].y * sc + f * o1[j].y;
+      r.acc[1].z = r.acc[1].z * sc + f * o1[j].z;
+      r.acc[1].w = r.acc[1].w * sc + f * o1[j].w;
+      r.M = Mn;
     }
   }
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    sm.M[wp][q * 32 + lane] = M[q];
-    sm.den[wp][q * 32 + lane] = den[q];
-    *reinterpret_cast<float4*>(&sm.acc[wp][q * 128 + lane * 4]) = acc[q];
-  }
-  __syncthreads();
-#pragma unroll
-  for (int j = 0; j < 2; ++j) {
-    const int el = 2 * tid + j, gi = el >> 2;
-    float Ms = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < kMergeWarps; ++w) Ms = fmaxf(Ms, sm.M[w][gi]);
-    float d = 0.f, x = 0.f;
-#pragma unroll
-    for (int w = 0; w < kMergeWarps; ++w) {
-      const float f = exp2f(sm.M[w][gi] - Ms);  // 0 for warps without candidates
-      d += f * sm.den[w][gi];
-      x += f * sm.acc[w][el];
-    }
-    rM[j] = Ms;
-    rden[j] = d;
-    racc[j] = x;
-  }
-  __syncthreads();
 }
 
 template <int OT>
-__device__ __forceinline__ void store_out2(void* out, size_t idx, float x0, float x1) {
+__device__ __forceinline__ void store_out4(void* out, size_t idx, float4 x, float inv) {
   if constexpr (OT == kBF16) {
-    *reinterpret_cast<__nv_bfloat162*>(reinterpret_cast<__nv_bfloat16*>(out) + idx) =
-        __floats2bfloat162_rn(x0, x1);
+    __nv_bfloat162 p0 = __floats2bfloat162_rn(x.x * inv, x.y * inv);
+    __nv_bfloat162 p1 = __floats2bfloat162_rn(x.z * inv, x.w * inv);
+    uint2 u = make_uint2(*reinterpret_cast<uint32_t*>(&p0), *reinterpret_cast<uint32_t*>(&p1));
+    *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(out) + idx) = u;
   } else {
-    *reinterpret_cast<__half2*>(reinterpret_cast<__half*>(out) + idx) = __floats2half2_rn(x0, x1);
+    __half2 p0 = __floats2half2_rn(x.x * inv, x.y * inv);
+    __half2 p1 = __floats2half2_rn(x.z * inv, x.w * inv);
+    uint2 u = make_uint2(*reinterpret_cast<uint32_t*>(&p0), *reinterpret_cast<uint32_t*>(&p1));
+    *reinterpret_cast<uint2*>(reinterpret_cast<__half*>(out) + idx) = u;
   }
+}
+
+template <int OT>
+__device__ __forceinline__ void store_head(const MergeArgs& a, size_t orow, const HeadAcc& r,
+                                           bool zero) {
+  const int lane = threadIdx.x & 31;
+  const float inv = zero ? 0.f : 1.f / r.den;
+  const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (4 * lane < a.D) store_out4<OT>(a.out, orow + 4 * lane, zero ? z : r.acc[0], inv);
+  if (128 + 4 * lane < a.D) store_out4<OT>(a.out, orow + 128 + 4 * lane, zero ? z : r.acc[1], inv);
 }
 
 template <int OT>
 __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeArgs a) {
   extern __shared__ int s_pref[];  // B + 1
-  __shared__ MergeSmem sm;
   griddep_wait();
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31;
   if (blockIdx.x == 0 && tid == 0) *a.pool = 0u;
   const int ws = a.ctrl[0], ts = a.ctrl[2], piece = a.ctrl[3];
   for (int i = tid; i <= a.B; i += blockDim.x) s_pref[i] = a.ctrl[4 + i];
   __syncthreads();
   const int S = a.B * a.Hkv, GD = a.G * a.D;
-  const int nchunk = (GD + kMergeChunk - 1) / kMergeChunk;
-  const long long units = static_cast<long long>(kMergeGroupsMax) * S * nchunk;
-  for (long long u = blockIdx.x; u < units; u += gridDim.x) {
-    const int g = static_cast<int>(u / (static_cast<long long>(S) * nchunk));
-    const int r = static_cast<int>(u % (static_cast<long long>(S) * nchunk));
-    const int s = r / nchunk, c = r - (r / nchunk) * nchunk;
+  const long long heads = static_cast<long long>(S) * a.G;
+  const long long units = static_cast<long long>(kMergeGroupsMax) * heads;
+  const long long wid = static_cast<long long>(blockIdx.x) * kMergeWarps + (tid >> 5);
+  const long long nwarps = static_cast<long long>(gridDim.x) * kMergeWarps;
+  for (long long u = wid; u < units; u += nwarps) {
+    const int g = static_cast<int>(u / heads);
+    const long long hr = u - static_cast<long long>(g) * heads;  // q-head row b * Hq + hq
+    const int s = static_cast<int>(hr / a.G), h = static_cast<int>(hr - static_cast<long long>(s) * a.G);
     const int b = s / a.Hkv, kvh = s - b * a.Hkv;
     const int nt = s_pref[b + 1] - s_pref[b];
     const int F = a.Hkv * s_pref[b] + kvh * nt;
@@ -151,51 +147,48 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeArgs a)
     if (gsz < kMergeGroupMin) gsz = kMergeGroupMin;
     const int ngroups = ncand > 0 ? (ncand + gsz - 1) / gsz : 1;
     if (g >= ngroups) continue;
-    const size_t obase = (static_cast<size_t>(b) * a.Hq + kvh * a.G) * a.D;
-    const int e0 = c * kMergeChunk + 2 * tid;
+    const size_t orow = static_cast<size_t>(hr) * a.D;
+    HeadAcc r;
+    r.M = -INFINITY;
+    r.den = 1.f;
+    r.acc[0] = r.acc[1] = make_float4(0.f, 0.f, 0.f, 0.f);
     if (ncand == 0) {
-      if (e0 < GD) store_out2<OT>(a.out, obase + e0, 0.f, 0.f);
+      store_head<OT>(a, orow, r, true);
       continue;
     }
     auto slot_of = [&](int k) -> int {
       return k < na ? s + w0 + k : S + a.NW + s + i0 + (k - na);
     };
-    float rM[2], rden[2], racc[2];
     const int k0 = g * gsz, k1 = min(k0 + gsz, ncand);
-    merge_combine(a, sm, slot_of, k0, k1, 1, c, rM, rden, racc);
+    merge_fold(a, slot_of, k0, k1, 1, h, r);
     if (ngroups == 1) {
-      if (e0 < GD) store_out2<OT>(a.out, obase + e0, racc[0] / rden[0], racc[1] / rden[1]);
+      store_head<OT>(a, orow, r, false);
       continue;
     }
     // group result, in place in the slot of the group's first candidate
     {
-      const size_t stride = static_cast<size_t>(part_stride(a.G, a.D));
-      float* P = a.part + static_cast<size_t>(slot_of(k0)) * stride;
-#pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        const int e = e0 + j;
-        if (e < GD) {
-          P[e] = racc[j];
-          if (e % a.D == 0) {
-            P[GD + e / a.D] = rM[j];
-            P[GD + a.G + e / a.D] = rden[j];
-          }
-        }
+      float* P = a.part + static_cast<size_t>(slot_of(k0)) * part_stride(a.G, a.D);
+      if (4 * lane < a.D) *reinterpret_cast<float4*>(P + h * a.D + 4 * lane) = r.acc[0];
+      if (128 + 4 * lane < a.D) *reinterpret_cast<float4*>(P + h * a.D + 128 + 4 * lane) = r.acc[1];
+      if (lane == 0) {
+        P[GD + h] = r.M;
+        P[GD + a.G + h] = r.den;
       }
     }
     __threadfence();
-    __syncthreads();
-    if (tid == 0) {
-      const uint32_t done = atomicAdd(a.counters + static_cast<size_t>(s) * nchunk + c, 1u) + 1;
-      sm.last = (done == static_cast<uint32_t>(ngroups));
-      if (sm.last) a.counters[static_cast<size_t>(s) * nchunk + c] = 0u;
+    __syncwarp();
+    int last = 0;
+    if (lane == 0) {
+      const uint32_t done = atomicAdd(a.counters + hr, 1u) + 1;
+      last = (done == static_cast<uint32_t>(ngroups));
+      if (last) a.counters[hr] = 0u;
     }
-    __syncthreads();
-    if (!sm.last) continue;
+    last = __shfl_sync(0xffffffffu, last, 0);
+    if (!last) continue;
     __threadfence();
-    // combine the group results (first candidate of each group)
-    merge_combine(a, sm, slot_of, 0, ngroups * gsz, gsz, c, rM, rden, racc);
-    if (e0 < GD) store_out2<OT>(a.out, obase + e0, racc[0] / rden[0], racc[1] / rden[1]);
+    // combine the group results (the first candidate of each group)
+    merge_fold(a, slot_of, 0, ngroups * gsz, gsz, h, r);
+    store_head<OT>(a, orow, r, false);
   }
 }
 

@@ -554,8 +554,8 @@ pa_status pa_decode(const pa_tensor* out, const pa_tensor* q, const pa_tensor* k
     return fail(PA_ERR_UNSUPPORTED, "pool or tables exceed 32-bit indexing");
   for (const pa_tensor* x : {q, key_cache, value_cache, block_tables, seq_lens})
     if (overlaps(out, x)) return fail(PA_ERR_INVALID_ARG, "out overlaps an input");
-  if (B * Hkv * ((Hq / Hkv * D + pa::kMergeChunk - 1) / pa::kMergeChunk) > pa::kMaxMergeCounters)
-    return fail(PA_ERR_UNSUPPORTED, "batch * num_kv_heads too large");
+  if (B * Hq > pa::kMaxMergeCounters)
+    return fail(PA_ERR_UNSUPPORTED, "batch * num_q_heads too large");
   if (B == 0) return ok();
   if (MB == 0) return fail(PA_ERR_INVALID_ARG, "block_tables has no columns");
   if (NB == 0) return fail(PA_ERR_INVALID_ARG, "empty block pool");
@@ -631,7 +631,7 @@ pa_status pa_decode(const pa_tensor* out, const pa_tensor* q, const pa_tensor* k
   m.Hkv = a.Hkv;
   m.G = a.G;
   m.D = a.D;
-  e = pa::merge_launch(q->dtype, m, st->num_sms * 2, cs, !prof);
+  e = pa::merge_launch(q->dtype, m, st->num_sms * 4, cs, !prof);
   if (e != cudaSuccess) {
     std::lock_guard<std::mutex> lk(g_mu);
     wsp->dirty = true;  // the decode kernel ran; its pool counter was not reset

@@ -22,7 +22,8 @@ __host__ __device__ constexpr inline int part_stride(int G, int D) {
 // Decode workspace layout (device memory, all sections 256-byte aligned):
 //   pool  u32 at offset 0: pool piece counter; zero between calls (the merge
 //         kernel resets it after each step), at the same place for any shape
-//   cnt   u32 [kMaxMergeCounters] at offset 256: merge group counters, zero
+//   cnt   u32 [kMaxMergeCounters] at offset 256: merge group counters (one
+//         per q head), zero
 //         between calls (each is reset by the unit that finds it complete)
 //   ctrl  int32 [4 + B + 1]: [0] static tiles per warp (ws), [1] total tiles,
 //         [2] end of the static region (Ts), [3] pool piece size (P),
@@ -56,12 +57,11 @@ struct MergeArgs {
   float* part;                   // group results are written in place
   const int32_t* ctrl;
   uint32_t* pool;                // reset to zero for the next step
-  uint32_t* counters;            // [S * chunks] groups done per (pair, chunk); left at zero
+  uint32_t* counters;            // [B * Hq] groups done per q head; left at zero
   int B, Hq, Hkv, G, D, NW;
 };
 
-constexpr int kMergeChunk = 512;      // (head, dim) elements per merge unit
-constexpr int kMergeGroupsMax = 16;   // groups of partials per (pair, chunk), at most
+constexpr int kMergeGroupsMax = 16;   // groups of partials per q head, at most
 constexpr int kMergeGroupMin = 16;    // partials per group, at least
 constexpr int kMaxMergeCounters = 1 << 19;
 
