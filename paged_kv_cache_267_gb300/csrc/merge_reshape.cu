@@ -35,53 +35,62 @@ cudaError_t device_error_word(int32_t** ptr) {
 constexpr int kMergeThreads = 256;
 constexpr int kMergeWarps = kMergeThreads / 32;
 
+// Per-lane state of one q head: head dims v * 128 + 4 * lane .. + 3 for
+// v < VPL (VPL = 1 for D <= 128, 2 for D = 256).
+template <int VPL>
 struct HeadAcc {
   float M, den;
-  float4 acc[2];  // head dims v * 128 + 4 * lane .. + 3, v = 0, 1
+  float4 acc[VPL];
 };
 
-// Folds candidates k0, k0 + step, ... (< k1) of head h into `r`.
-template <typename SlotFn>
+// Folds candidates k0, k0 + step, ... (< k1) of head h into `r`, with
+// 8 / (2 VPL) candidates' loads in flight per lane.
+template <int VPL, typename SlotFn>
 __device__ __forceinline__ void merge_fold(const MergeArgs& a, SlotFn slot_of, int k0, int k1,
-                                           int step, int h, HeadAcc& r) {
+                                           int step, int h, HeadAcc<VPL>& r) {
+  constexpr int U = 4 / VPL;
   const int lane = threadIdx.x & 31;
   const int GD = a.G * a.D;
   const size_t stride = static_cast<size_t>(part_stride(a.G, a.D));
   r.M = -INFINITY;
   r.den = 0.f;
-  r.acc[0] = r.acc[1] = make_float4(0.f, 0.f, 0.f, 0.f);
-  const bool v0 = 4 * lane < a.D, v1 = 128 + 4 * lane < a.D;
-  for (int k = k0; k < k1; k += 4 * step) {
-    float mm[4], ll[4];
-    float4 o0[4], o1[4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
+  for (int v = 0; v < VPL; ++v) r.acc[v] = make_float4(0.f, 0.f, 0.f, 0.f);
+  const bool on = 4 * lane < a.D;  // D = 64 uses half the lanes
+  for (int k = k0; k < k1; k += U * step) {
+    float mm[U], ll[U];
+    float4 o[U][VPL];
+#pragma unroll
+    for (int j = 0; j < U; ++j) {
       const int kk = k + j * step;
       mm[j] = -INFINITY;
       ll[j] = 0.f;
-      o0[j] = o1[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int v = 0; v < VPL; ++v) o[j][v] = make_float4(0.f, 0.f, 0.f, 0.f);
       if (kk < k1) {
         const float* P = a.part + static_cast<size_t>(slot_of(kk)) * stride;
         mm[j] = P[GD + h];
         ll[j] = P[GD + a.G + h];
-        if (v0) o0[j] = *reinterpret_cast<const float4*>(P + h * a.D + 4 * lane);
-        if (v1) o1[j] = *reinterpret_cast<const float4*>(P + h * a.D + 128 + 4 * lane);
+        if (on) {
+#pragma unroll
+          for (int v = 0; v < VPL; ++v)
+            o[j][v] = *reinterpret_cast<const float4*>(P + h * a.D + v * 128 + 4 * lane);
+        }
       }
     }
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
+    for (int j = 0; j < U; ++j) {
       if (k + j * step >= k1) break;
       const float Mn = fmaxf(r.M, mm[j]);
-      const float sc = exp2f(r.M - Mn), f = exp2f(mm[j] - Mn);
+      const float sc = fast_exp2(r.M - Mn), f = fast_exp2(mm[j] - Mn);
       r.den = r.den * sc + f * ll[j];
-      r.acc[0].x = r.acc[0].x * sc + f * o0[j].x;
-      r.acc[0].y = r.acc[0].y * sc + f * o0[j].y;
-      r.acc[0].z = r.acc[0].z * sc + f * o0[j].z;
-      r.acc[0].w = r.acc[0].w * sc + f * o0[j].w;
-      r.acc[1].x = r.acc[1].x * sc + f * o1[j].x;
-      r.acc[1].y = r.acc[1].y * sc + f * o1[j].y;
-      r.acc[1].z = r.acc[1].z * sc + f * o1[j].z;
-      r.acc[1].w = r.acc[1].w * sc + f * o1[j].w;
+#pragma unroll
+      for (int v = 0; v < VPL; ++v) {
+        r.acc[v].x = r.acc[v].x * sc + f * o[j][v].x;
+        r.acc[v].y = r.acc[v].y * sc + f * o[j][v].y;
+        r.acc[v].z = r.acc[v].z * sc + f * o[j][v].z;
+        r.acc[v].w = r.acc[v].w * sc + f * o[j][v].w;
+      }
       r.M = Mn;
     }
   }
@@ -102,74 +111,141 @@ __device__ __forceinline__ void store_out4(void* out, size_t idx, float4 x, floa
   }
 }
 
-template <int OT>
-__device__ __forceinline__ void store_head(const MergeArgs& a, size_t orow, const HeadAcc& r,
+template <int OT, int VPL>
+__device__ __forceinline__ void store_head(const MergeArgs& a, size_t orow, const HeadAcc<VPL>& r,
                                            bool zero) {
   const int lane = threadIdx.x & 31;
+  if (4 * lane >= a.D) return;
   const float inv = zero ? 0.f : 1.f / r.den;
   const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (4 * lane < a.D) store_out4<OT>(a.out, orow + 4 * lane, zero ? z : r.acc[0], inv);
-  if (128 + 4 * lane < a.D) store_out4<OT>(a.out, orow + 128 + 4 * lane, zero ? z : r.acc[1], inv);
+#pragma unroll
+  for (int v = 0; v < VPL; ++v)
+    store_out4<OT>(a.out, orow + v * 128 + 4 * lane, zero ? z : r.acc[v], inv);
 }
 
-template <int OT>
-__global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeArgs a) {
-  extern __shared__ int s_pref[];  // B + 1
+// Candidate range of pair (b, kvh): static warps [w0, w0 + na), pool pieces
+// [i0, i0 + np).
+struct Cands {
+  int w0, na, i0, np;
+};
+
+__device__ __forceinline__ Cands pair_cands(int F, int nt, int ws, int ts, int piece) {
+  Cands c = {0, 0, 0, 0};
+  if (nt > 0 && F < ts) {
+    c.w0 = F / ws;
+    c.na = (min(F + nt, ts) - 1) / ws - c.w0 + 1;
+  }
+  if (nt > 0 && F + nt > ts) {
+    c.i0 = (max(F, ts) - ts) / piece;
+    c.np = (F + nt - 1 - ts) / piece - c.i0 + 1;
+  }
+  return c;
+}
+
+__device__ __forceinline__ int group_size(int ncand) {
+  const int gsz = (ncand + kMergeGroupsMax - 1) / kMergeGroupsMax;
+  return gsz < kMergeGroupMin ? kMergeGroupMin : gsz;
+}
+
+// Units: first group 0 of every q head (B * Hq of them), then groups 1.. of the
+// heads of sequences whose candidate bound needs more than one group; the
+// latter are enumerated through a per-CTA prefix over sequences (s_extra),
+// and a unit whose group turns out empty is skipped.
+template <int OT, int VPL>
+__global__ void __launch_bounds__(kMergeThreads, 4) merge_kernel(const MergeArgs a) {
+  extern __shared__ int s_dyn[];
+  int* s_pref = s_dyn;             // B + 1 tile prefix
+  int* s_extra = s_dyn + a.B + 1;  // B + 1 prefix of extra units per sequence
   griddep_wait();
   const int tid = threadIdx.x, lane = tid & 31;
   if (blockIdx.x == 0 && tid == 0) *a.pool = 0u;
   const int ws = a.ctrl[0], ts = a.ctrl[2], piece = a.ctrl[3];
   for (int i = tid; i <= a.B; i += blockDim.x) s_pref[i] = a.ctrl[4 + i];
   __syncthreads();
+  // extra group units per sequence, from an upper bound of its pairs' candidates
+  if (tid < 32) {
+    int run = 0;
+    for (int b0 = 0; b0 < a.B; b0 += 32) {
+      const int b = b0 + lane;
+      int x = 0;
+      if (b < a.B) {
+        const int nt = s_pref[b + 1] - s_pref[b];
+        if (nt > 0) {
+          const int ub = nt / ws + 2 + nt / piece + 2;
+          const int gmax = (ub + group_size(ub) - 1) / group_size(ub);
+          x = (gmax - 1) * a.Hq;
+        }
+      }
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+      }
+      if (b < a.B) s_extra[b + 1] = run + x;
+      run += __shfl_sync(0xffffffffu, x, 31);
+    }
+    if (lane == 0) s_extra[0] = 0;
+  }
+  __syncthreads();
   const int S = a.B * a.Hkv, GD = a.G * a.D;
-  const long long heads = static_cast<long long>(S) * a.G;
-  const long long units = static_cast<long long>(kMergeGroupsMax) * heads;
-  const long long wid = static_cast<long long>(blockIdx.x) * kMergeWarps + (tid >> 5);
-  const long long nwarps = static_cast<long long>(gridDim.x) * kMergeWarps;
-  for (long long u = wid; u < units; u += nwarps) {
-    const int g = static_cast<int>(u / heads);
-    const long long hr = u - static_cast<long long>(g) * heads;  // q-head row b * Hq + hq
-    const int s = static_cast<int>(hr / a.G), h = static_cast<int>(hr - static_cast<long long>(s) * a.G);
-    const int b = s / a.Hkv, kvh = s - b * a.Hkv;
+  const int heads = a.B * a.Hq;
+  const int units = heads + s_extra[a.B];
+  const int nwarps = gridDim.x * kMergeWarps;
+  for (int u = blockIdx.x * kMergeWarps + (tid >> 5); u < units; u += nwarps) {
+    int b, hq, g;
+    if (u < heads) {
+      b = u / a.Hq;
+      hq = u - b * a.Hq;
+      g = 0;
+    } else {
+      const int e = u - heads;
+      int lo = 0, hi = a.B;  // largest b with s_extra[b] <= e
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (s_extra[mid] <= e) lo = mid; else hi = mid;
+      }
+      b = lo;
+      const int rem = e - s_extra[b];
+      g = 1 + rem / a.Hq;
+      hq = rem - (g - 1) * a.Hq;
+    }
+    const int kvh = hq / a.G, h = hq - kvh * a.G;
+    const int s = b * a.Hkv + kvh;
+    const int hr = b * a.Hq + hq;
     const int nt = s_pref[b + 1] - s_pref[b];
     const int F = a.Hkv * s_pref[b] + kvh * nt;
-    int w0 = 0, na = 0, i0 = 0, np = 0;
-    if (nt > 0 && F < ts) {
-      w0 = F / ws;
-      na = (min(F + nt, ts) - 1) / ws - w0 + 1;
-    }
-    if (nt > 0 && F + nt > ts) {
-      i0 = (max(F, ts) - ts) / piece;
-      np = (F + nt - 1 - ts) / piece - i0 + 1;
-    }
-    const int ncand = na + np;
-    int gsz = (ncand + kMergeGroupsMax - 1) / kMergeGroupsMax;
-    if (gsz < kMergeGroupMin) gsz = kMergeGroupMin;
+    const Cands cd = pair_cands(F, nt, ws, ts, piece);
+    const int ncand = cd.na + cd.np;
+    const int gsz = group_size(ncand);
     const int ngroups = ncand > 0 ? (ncand + gsz - 1) / gsz : 1;
     if (g >= ngroups) continue;
     const size_t orow = static_cast<size_t>(hr) * a.D;
-    HeadAcc r;
+    HeadAcc<VPL> r;
     r.M = -INFINITY;
     r.den = 1.f;
-    r.acc[0] = r.acc[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int v = 0; v < VPL; ++v) r.acc[v] = make_float4(0.f, 0.f, 0.f, 0.f);
     if (ncand == 0) {
-      store_head<OT>(a, orow, r, true);
+      store_head<OT, VPL>(a, orow, r, true);
       continue;
     }
     auto slot_of = [&](int k) -> int {
-      return k < na ? s + w0 + k : S + a.NW + s + i0 + (k - na);
+      return k < cd.na ? s + cd.w0 + k : S + a.NW + s + cd.i0 + (k - cd.na);
     };
     const int k0 = g * gsz, k1 = min(k0 + gsz, ncand);
     merge_fold(a, slot_of, k0, k1, 1, h, r);
     if (ngroups == 1) {
-      store_head<OT>(a, orow, r, false);
+      store_head<OT, VPL>(a, orow, r, false);
       continue;
     }
     // group result, in place in the slot of the group's first candidate
     {
       float* P = a.part + static_cast<size_t>(slot_of(k0)) * part_stride(a.G, a.D);
-      if (4 * lane < a.D) *reinterpret_cast<float4*>(P + h * a.D + 4 * lane) = r.acc[0];
-      if (128 + 4 * lane < a.D) *reinterpret_cast<float4*>(P + h * a.D + 128 + 4 * lane) = r.acc[1];
+      if (4 * lane < a.D) {
+#pragma unroll
+        for (int v = 0; v < VPL; ++v)
+          *reinterpret_cast<float4*>(P + h * a.D + v * 128 + 4 * lane) = r.acc[v];
+      }
       if (lane == 0) {
         P[GD + h] = r.M;
         P[GD + a.G + h] = r.den;
@@ -188,7 +264,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeArgs a)
     __threadfence();
     // combine the group results (the first candidate of each group)
     merge_fold(a, slot_of, 0, ngroups * gsz, gsz, h, r);
-    store_head<OT>(a, orow, r, false);
+    store_head<OT, VPL>(a, orow, r, false);
   }
 }
 
@@ -196,15 +272,19 @@ cudaError_t merge_launch(int out_type, const MergeArgs& a, int grid, cudaStream_
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kMergeThreads);
-  cfg.dynamicSmemBytes = static_cast<size_t>(a.B + 1) * sizeof(int);
+  cfg.dynamicSmemBytes = static_cast<size_t>(2 * (a.B + 1)) * sizeof(int);
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (out_type == kBF16) return cudaLaunchKernelEx(&cfg, merge_kernel<kBF16>, a);
-  return cudaLaunchKernelEx(&cfg, merge_kernel<kF16>, a);
+  if (a.D > 128) {
+    if (out_type == kBF16) return cudaLaunchKernelEx(&cfg, merge_kernel<kBF16, 2>, a);
+    return cudaLaunchKernelEx(&cfg, merge_kernel<kF16, 2>, a);
+  }
+  if (out_type == kBF16) return cudaLaunchKernelEx(&cfg, merge_kernel<kBF16, 1>, a);
+  return cudaLaunchKernelEx(&cfg, merge_kernel<kF16, 1>, a);
 }
 
 // ------------------------------------------------------------- write path
