@@ -183,12 +183,15 @@ __global__ void __launch_bounds__(WARPS * 32)
     s_len[b] = L;
   }
   __syncthreads();
-  // exclusive prefix of tiles per pair over the sequences (one warp)
+  // exclusive prefix of tiles per pair over the sequences (one warp), and the
+  // longest sequence's tile count
+  __shared__ int s_maxnt;
   if (warp == 0) {
-    int run = 0;
+    int run = 0, mx = 0;
     for (int b0 = 0; b0 < a.B; b0 += 32) {
       const int b = b0 + lane;
       int x = (b < a.B) ? tiles_of(s_len[b], a.window) : 0;
+      mx = max(mx, x);
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const int y = __shfl_up_sync(FULL, x, o);
@@ -197,14 +200,24 @@ __global__ void __launch_bounds__(WARPS * 32)
       if (b < a.B) s_pref[b + 1] = run + x;
       run += __shfl_sync(FULL, x, 31);
     }
-    if (lane == 0) s_pref[0] = 0;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(FULL, mx, o));
+    if (lane == 0) {
+      s_pref[0] = 0;
+      s_maxnt = mx;
+    }
   }
   __syncthreads();
 
-  // static ranges for about (1 - pool share) of the tiles, then the pool
+  // Static ranges for about (1 - pool share) of the tiles, then the pool. The
+  // pool covers the end of the flat space; when one sequence is much longer
+  // than the mean, that end can lie inside it and the pool would cut it into
+  // thousands of small partials, so skewed batches are split statically only.
   const int total = a.Hkv * s_pref[a.B];
   const int nw = gridDim.x * WARPS;
-  const long long pool_want = static_cast<long long>(total) * a.pool_permille / 1000;
+  const bool skewed = static_cast<long long>(s_maxnt) * a.B > 4ll * s_pref[a.B];
+  const long long pool_want =
+      skewed ? 0 : static_cast<long long>(total) * a.pool_permille / 1000;
   int ws = static_cast<int>((total - pool_want) / nw);
   if (ws < a.min_tiles) ws = a.min_tiles;
   const int ts = static_cast<int>(min(static_cast<long long>(ws) * nw, static_cast<long long>(total)));

@@ -31,7 +31,7 @@ thread_local void* g_prof_before = nullptr;
 thread_local void* g_prof_after = nullptr;
 
 constexpr int kDefaultMinTiles = 4;
-constexpr int kDefaultPoolPermille = 200;  // share of tiles handed out dynamically
+constexpr int kDefaultPoolPermille = 100;  // share of tiles handed out dynamically
 constexpr int kDefaultPiece = 4;           // least tiles per pool piece
 constexpr int kPiecesPerWorker = 4;        // pool pieces per worker warp, at most
 constexpr int kMaxCtasPerSm = 2;
