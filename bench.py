@@ -337,14 +337,17 @@ def run_ours(args, world, rank, local):
     rbytes = reshape_bytes(w)
     step_bytes = dbytes["total"] + rbytes
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    flush_w = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
-    flush_r = torch.ones(max(2 * l2, 256 << 20) // 8, dtype=torch.int64, device=dev)
+    nflush = max(4 * l2, 512 << 20)
+    flush_w = torch.empty(nflush, dtype=torch.uint8, device=dev)
+    flush_r = torch.ones(nflush // 8, dtype=torch.int64, device=dev)
     flush_sink = torch.empty((), dtype=torch.int64, device=dev)
 
     class _Flush:
-        """Write a buffer larger than L2 (evicts every line), then read another
-        one, so the timed step starts with a cold L2 that holds no dirty lines
-        whose write-back would land inside the timed region."""
+        """Write a buffer four times the L2 size (evicts every line), then read
+        another one as large, so the timed step starts with a cold L2 that
+        holds no dirty lines whose write-back would land inside the timed
+        region (with only twice the L2 size some dirty lines survived and
+        slowed the next step measurably)."""
 
         @staticmethod
         def zero_():
@@ -457,7 +460,7 @@ def run_ours(args, world, rank, local):
                    "step": "pa_reshape_and_cache (1 new token per sequence) + pa_decode",
                    "attended_tokens_per_rank": dbytes["tokens"],
                    "bytes_per_step_per_rank": step_bytes,
-                   "l2": "flushed between timed steps, outside the events: write 2x L2, then read 2x L2"},
+                   "l2": "flushed between timed steps, outside the events: write 4x L2, then read 4x L2"},
         "pct_of_peak": 100.0 * value / world / peak,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,

@@ -232,6 +232,25 @@ __global__ void __launch_bounds__(WARPS * 32)
       a.ctrl[3] = piece;
     }
     for (int b = tid; b <= a.B; b += blockDim.x) a.ctrl[4 + b] = s_pref[b];
+    // prefix of the merge kernel's extra group units per sequence
+    if (warp == 0) {
+      int run = 0;
+      for (int b0 = 0; b0 < a.B; b0 += 32) {
+        const int b = b0 + lane;
+        int x = 0;
+        if (b < a.B)
+          x = merge_extra_units(s_pref[b + 1] - s_pref[b], a.Hkv * s_pref[b],
+                                a.Hkv * s_pref[b + 1], ws, ts, piece, a.Hq);
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(FULL, x, o);
+          if (lane >= o) x += y;
+        }
+        if (b < a.B) a.ctrl[6 + a.B + b] = run + x;
+        run += __shfl_sync(FULL, x, 31);
+      }
+      if (lane == 0) a.ctrl[5 + a.B] = 0;
+    }
   }
   const int w = blockIdx.x * WARPS + warp;
   const int f0 = static_cast<int>(min(static_cast<long long>(w) * ws, static_cast<long long>(ts)));

@@ -142,15 +142,10 @@ __device__ __forceinline__ Cands pair_cands(int F, int nt, int ws, int ts, int p
   return c;
 }
 
-__device__ __forceinline__ int group_size(int ncand) {
-  const int gsz = (ncand + kMergeGroupsMax - 1) / kMergeGroupsMax;
-  return gsz < kMergeGroupMin ? kMergeGroupMin : gsz;
-}
-
 // Units: first group 0 of every q head (B * Hq of them), then groups 1.. of the
 // heads of sequences whose candidate bound needs more than one group; the
-// latter are enumerated through a per-CTA prefix over sequences (s_extra),
-// and a unit whose group turns out empty is skipped.
+// latter are enumerated through a prefix over sequences (written by the
+// decode kernel), and a unit whose group turns out empty is skipped.
 template <int OT, int VPL>
 __global__ void __launch_bounds__(kMergeThreads, 4) merge_kernel(const MergeArgs a) {
   extern __shared__ int s_dyn[];
@@ -160,31 +155,9 @@ __global__ void __launch_bounds__(kMergeThreads, 4) merge_kernel(const MergeArgs
   const int tid = threadIdx.x, lane = tid & 31;
   if (blockIdx.x == 0 && tid == 0) *a.pool = 0u;
   const int ws = a.ctrl[0], ts = a.ctrl[2], piece = a.ctrl[3];
-  for (int i = tid; i <= a.B; i += blockDim.x) s_pref[i] = a.ctrl[4 + i];
-  __syncthreads();
-  // extra group units per sequence, from an upper bound of its pairs' candidates
-  if (tid < 32) {
-    int run = 0;
-    for (int b0 = 0; b0 < a.B; b0 += 32) {
-      const int b = b0 + lane;
-      int x = 0;
-      if (b < a.B) {
-        const int nt = s_pref[b + 1] - s_pref[b];
-        if (nt > 0) {
-          const int ub = nt / ws + 2 + nt / piece + 2;
-          const int gmax = (ub + group_size(ub) - 1) / group_size(ub);
-          x = (gmax - 1) * a.Hq;
-        }
-      }
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, x, o);
-        if (lane >= o) x += y;
-      }
-      if (b < a.B) s_extra[b + 1] = run + x;
-      run += __shfl_sync(0xffffffffu, x, 31);
-    }
-    if (lane == 0) s_extra[0] = 0;
+  for (int i = tid; i <= a.B; i += blockDim.x) {
+    s_pref[i] = a.ctrl[4 + i];
+    s_extra[i] = a.ctrl[5 + a.B + i];
   }
   __syncthreads();
   const int S = a.B * a.Hkv, GD = a.G * a.D;
@@ -216,7 +189,7 @@ __global__ void __launch_bounds__(kMergeThreads, 4) merge_kernel(const MergeArgs
     const int F = a.Hkv * s_pref[b] + kvh * nt;
     const Cands cd = pair_cands(F, nt, ws, ts, piece);
     const int ncand = cd.na + cd.np;
-    const int gsz = group_size(ncand);
+    const int gsz = merge_group_size(ncand);
     const int ngroups = ncand > 0 ? (ncand + gsz - 1) / gsz : 1;
     if (g >= ngroups) continue;
     const size_t orow = static_cast<size_t>(hr) * a.D;

@@ -164,7 +164,7 @@ WsLayout ws_layout(int64_t B, int Hkv, int G, int D, int64_t workers) {
   // whatever their shapes, and each step's merge only resets its own copy.
   L.pool = o;      o += 256;
   L.counters = o;  o += static_cast<size_t>(pa::kMaxMergeCounters) * sizeof(uint32_t);
-  L.ctrl = o;  o += round_up(static_cast<size_t>(B + 5) * sizeof(int32_t), 256);
+  L.ctrl = o;  o += round_up(static_cast<size_t>(2 * B + 6) * sizeof(int32_t), 256);
   L.part = o;  o += nslot * static_cast<size_t>(pa::part_stride(G, D)) * sizeof(float);
   L.total = o;
   return L;

@@ -25,9 +25,10 @@ __host__ __device__ constexpr inline int part_stride(int G, int D) {
 //   cnt   u32 [kMaxMergeCounters] at offset 256: merge group counters (one
 //         per q head), zero
 //         between calls (each is reset by the unit that finds it complete)
-//   ctrl  int32 [4 + B + 1]: [0] static tiles per warp (ws), [1] total tiles,
+//   ctrl  int32 [2 B + 6]: [0] static tiles per warp (ws), [1] total tiles,
 //         [2] end of the static region (Ts), [3] pool piece size (P),
-//         [4..] tile prefix over the sequences
+//         [4 .. 4 + B] tile prefix over the sequences, [5 + B .. 5 + 2 B]
+//         prefix of the merge's extra group units over the sequences
 //   part  f32 [NSLOT][part_stride(G, D)]: acc[G][D], m[G], l[G], padding to a
 //         multiple of 4 floats so every slot starts 16-byte aligned
 // with S = B * Hkv pairs, NW worker warps, NSLOT = 2 S + NW + NPMAX.
@@ -64,6 +65,26 @@ struct MergeArgs {
 constexpr int kMergeGroupsMax = 16;   // groups of partials per q head, at most
 constexpr int kMergeGroupMin = 16;    // partials per group, at least
 constexpr int kMaxMergeCounters = 1 << 19;
+
+// Partials per merge group for a head with n candidate partials.
+__host__ __device__ inline int merge_group_size(int n) {
+  const int g = (n + kMergeGroupsMax - 1) / kMergeGroupsMax;
+  return g < kMergeGroupMin ? kMergeGroupMin : g;
+}
+
+// Merge units beyond group 0 for the Hq heads of one sequence whose pairs
+// span flat tiles [lo, hi), nt tiles each: from an upper bound of a pair's
+// candidates (static warps met, plus pool pieces met inside [ts, hi)).
+__host__ __device__ inline int merge_extra_units(int nt, int lo, int hi, int ws, int ts,
+                                                 int piece, int Hq) {
+  if (nt <= 0) return 0;
+  const int start = lo > ts ? lo : ts;
+  const int in_pool = hi > start ? hi - start : 0;
+  const int pool_part = in_pool > 0 ? (nt < in_pool ? nt : in_pool) / piece + 2 : 0;
+  const int ub = nt / ws + 2 + pool_part;
+  const int gsz = merge_group_size(ub);
+  return ((ub + gsz - 1) / gsz - 1) * Hq;
+}
 
 struct ReshapeArgs {
   const void* k;
