@@ -151,6 +151,38 @@ pa_status pa_decode(const pa_tensor* out, const pa_tensor* q, const pa_tensor* k
                     int32_t block_size, int32_t window, int32_t kv_dtype, float k_scale,
                     float v_scale, pa_stream stream);
 
+/*
+ * pa_decode_noalloc — pa_decode for callers that cannot allocate device
+ * memory when they decode: code that runs inside a memory pool or arena
+ * owning all of the GPU's memory, runtimes whose allocator must not be
+ * re-entered from this call, and services that forbid cudaMalloc after
+ * start-up so that their memory use stays fixed. (The paged-attention pages
+ * describe no such variant; it is a property of this library.)
+ *
+ * Arguments, results and errors are those of pa_decode. Instead of a
+ * workspace, the call keeps its scratch in one 32 MiB array compiled into the
+ * library; every GPU that loads the library holds that array until the
+ * process exits. The call allocates and frees nothing (no cudaMalloc or
+ * cudaFree, directly or through another library). A step whose scratch would
+ * exceed 32 MiB (roughly: batch * num_kv_heads * G * head_dim beyond what fits
+ * next to the per-warp partials; for example G = 16 with head_dim 256) is
+ * rejected with PA_ERR_WORKSPACE and a message giving the bytes needed.
+ *
+ * The first call on a device looks up that device's address of the array
+ * (cudaGetSymbolAddress, with that device current); make that first call
+ * before any stream capture. All calls share the one array and find the last
+ * call's contents in it; each call clears, on its stream, the counters that
+ * must start at zero. Calls that overlap on the GPU (on different streams, or
+ * different host threads, of one device) race on the array and must not be
+ * issued.
+ */
+pa_status pa_decode_noalloc(const pa_tensor* out, const pa_tensor* q,
+                            const pa_tensor* key_cache, const pa_tensor* value_cache,
+                            const pa_tensor* block_tables, const pa_tensor* seq_lens,
+                            int32_t num_kv_heads, float scale, int32_t block_size,
+                            int32_t window, int32_t kv_dtype, float k_scale, float v_scale,
+                            pa_stream stream);
+
 /* Workspace bytes pa_decode needs on the current device for a batch of
  * `batch` sequences with these head counts and head_dim. */
 pa_status pa_decode_workspace_size(int64_t batch, int32_t num_q_heads, int32_t num_kv_heads,

@@ -55,6 +55,7 @@ def lib() -> ctypes.CDLL:
         sig = {
             "pa_reshape_and_cache": (st, [P, P, P, P, P, i32, f32, f32, vp]),
             "pa_decode": (st, [P, P, P, P, P, P, i32, f32, i32, i32, i32, f32, f32, vp]),
+            "pa_decode_noalloc": (st, [P, P, P, P, P, P, i32, f32, i32, i32, i32, f32, f32, vp]),
             "pa_decode_workspace_size": (st, [i64, i32, i32, i32, ctypes.POINTER(ctypes.c_size_t)]),
             "pa_set_workspace": (st, [vp, ctypes.c_size_t]),
             "pa_set_decode_tuning": (st, [i32, i32, i32, i32]),
@@ -153,6 +154,19 @@ def decode(q, key_cache, value_cache, block_tables, seq_lens, *, num_kv_heads: i
     _check(lib().pa_decode(*[ctypes.byref(d) for d in descs], int(num_kv_heads), float(scale),
                            int(block_size), int(window), _kv(kv_dtype), float(k_scale),
                            float(v_scale), _stream(stream)))
+    return out
+
+
+def decode_noalloc(q, key_cache, value_cache, block_tables, seq_lens, *, num_kv_heads: int,
+                   scale: float, block_size: int, out, window: int = 0, kv_dtype="auto",
+                   k_scale: float = 1.0, v_scale: float = 1.0, stream=None):
+    """pa_decode_noalloc: the decode step with the library's built-in scratch
+    array instead of a workspace, for callers that cannot allocate device
+    memory at decode time. `out` must be given (nothing is allocated)."""
+    descs = [tensor_desc(x) for x in (out, q, key_cache, value_cache, block_tables, seq_lens)]
+    _check(lib().pa_decode_noalloc(*[ctypes.byref(d) for d in descs], int(num_kv_heads),
+                                   float(scale), int(block_size), int(window), _kv(kv_dtype),
+                                   float(k_scale), float(v_scale), _stream(stream)))
     return out
 
 

@@ -642,3 +642,159 @@ pa_status pa_decode(const pa_tensor* out, const pa_tensor* q, const pa_tensor* k
 }
 
 }  // extern "C"
+
+
+// pa_decode's validation and launches, with the scratch in a caller-given
+// device buffer of `capacity` bytes instead of a library workspace; used by
+// the allocation-free entry point (decode_noalloc.cu). Allocates nothing.
+namespace pa {
+pa_status decode_in_buffer(const pa_tensor* out, const pa_tensor* q, const pa_tensor* key_cache,
+                           const pa_tensor* value_cache, const pa_tensor* block_tables,
+                           const pa_tensor* seq_lens, int32_t num_kv_heads, float scale,
+                           int32_t block_size, int32_t window, int32_t kv_dtype, float k_scale,
+                           float v_scale, pa_stream stream, void* buffer, size_t capacity) {
+  pa_status s;
+  if ((s = check_tensor(out, "out", 3)) || (s = check_tensor(q, "q", 3)) ||
+      (s = check_tensor(key_cache, "key_cache", 4)) ||
+      (s = check_tensor(value_cache, "value_cache", 4)) ||
+      (s = check_tensor(block_tables, "block_tables", 2)) ||
+      (s = check_tensor(seq_lens, "seq_lens", 1)))
+    return s;
+  if (q->dtype != PA_F16 && q->dtype != PA_BF16) return fail(PA_ERR_UNSUPPORTED, "q must be f16 or bf16");
+  if (out->dtype != q->dtype) return fail(PA_ERR_INVALID_ARG, "out dtype must equal q dtype");
+  const int64_t B = q->shape[0], Hq = q->shape[1], D = q->shape[2];
+  for (int i = 0; i < 3; ++i)
+    if (out->shape[i] != q->shape[i]) return fail(PA_ERR_INVALID_ARG, "out shape != q shape");
+  if (kv_dtype != PA_KV_AUTO && kv_dtype != PA_KV_FP8_E4M3)
+    return fail(PA_ERR_INVALID_ARG, "bad kv_dtype %d", kv_dtype);
+  const bool fp8 = kv_dtype == PA_KV_FP8_E4M3;
+  const int32_t cdt = fp8 ? PA_FP8_E4M3 : q->dtype;
+  if (key_cache->dtype != cdt || value_cache->dtype != cdt)
+    return fail(PA_ERR_INVALID_ARG, "cache dtype does not match q dtype / kv_dtype");
+  for (int i = 0; i < 4; ++i)
+    if (key_cache->shape[i] != value_cache->shape[i])
+      return fail(PA_ERR_INVALID_ARG, "key and value cache shapes differ");
+  const int64_t NB = key_cache->shape[0], Hkv = key_cache->shape[1];
+  if (num_kv_heads != Hkv) return fail(PA_ERR_INVALID_ARG, "num_kv_heads != key_cache.shape[1]");
+  if (block_size != key_cache->shape[2]) return fail(PA_ERR_INVALID_ARG, "block_size != key_cache.shape[2]");
+  if (key_cache->shape[3] != D) return fail(PA_ERR_INVALID_ARG, "cache head_dim != q head_dim");
+  if ((s = check_heads(Hq, Hkv, D))) return s;
+  if (fp8 && D == 64) return fail(PA_ERR_UNSUPPORTED, "fp8 caches need head_dim 128 or 256");
+  if (block_size <= 0 || block_size % 16 || block_size > 1024)
+    return fail(PA_ERR_UNSUPPORTED, "block_size must be a multiple of 16 in [16, 1024]");
+  if (block_tables->dtype != PA_I32 || seq_lens->dtype != PA_I32)
+    return fail(PA_ERR_INVALID_ARG, "block_tables and seq_lens must be int32");
+  if (block_tables->shape[0] != B || seq_lens->shape[0] != B)
+    return fail(PA_ERR_INVALID_ARG, "block_tables / seq_lens batch != q batch");
+  const int64_t MB = block_tables->shape[1];
+  if (B > kMaxBatch) return fail(PA_ERR_UNSUPPORTED, "batch %lld > %lld", (long long)B, (long long)kMaxBatch);
+  if (!is_contiguous(out) || !is_contiguous(q) || !is_contiguous(key_cache) ||
+      !is_contiguous(value_cache) || !is_contiguous(block_tables) || !is_contiguous(seq_lens))
+    return fail(PA_ERR_LAYOUT, "pa_decode needs contiguous tensors");
+  for (const pa_tensor* x : {key_cache, value_cache, q, out})
+    if (reinterpret_cast<uintptr_t>(x->data) % 16)
+      return fail(PA_ERR_LAYOUT, "q, out and caches must be 16-byte aligned");
+  if (!std::isfinite(scale)) return fail(PA_ERR_INVALID_ARG, "scale must be finite");
+  if (fp8 && !(std::isfinite(k_scale) && std::isfinite(v_scale) && k_scale > 0 && v_scale > 0))
+    return fail(PA_ERR_INVALID_ARG, "fp8 scales must be finite and positive");
+  // 32-bit index limits inside the kernels
+  if (NB * Hkv * block_size >= (int64_t(1) << 31) || MB * block_size >= (int64_t(1) << 31) ||
+      B * Hkv * (MB * block_size / 16 + 1) >= (int64_t(1) << 31) || B * MB >= (int64_t(1) << 31))
+    return fail(PA_ERR_UNSUPPORTED, "pool or tables exceed 32-bit indexing");
+  for (const pa_tensor* x : {q, key_cache, value_cache, block_tables, seq_lens})
+    if (overlaps(out, x)) return fail(PA_ERR_INVALID_ARG, "out overlaps an input");
+  if (B * Hq > pa::kMaxMergeCounters)
+    return fail(PA_ERR_UNSUPPORTED, "batch * num_q_heads too large");
+  if (B == 0) return ok();
+  if (MB == 0) return fail(PA_ERR_INVALID_ARG, "block_tables has no columns");
+  if (NB == 0) return fail(PA_ERR_INVALID_ARG, "empty block pool");
+
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  DeviceState* st;
+  int dev;
+  DecodePlan plan;
+  WsLayout layout;
+  void* ws = buffer;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if ((s = device_state(&st, &dev))) return s;
+    const int ct = fp8 ? pa::kE4M3 : (q->dtype == PA_BF16 ? pa::kBF16 : pa::kF16);
+    if ((s = plan_decode(st, dev, ct, q->dtype, B, static_cast<int>(Hq), static_cast<int>(Hkv),
+                         static_cast<int>(D), &plan)))
+      return s;
+    layout = ws_layout(B, static_cast<int>(Hkv), plan.G, static_cast<int>(D), plan.workers);
+  }
+  if (layout.total > capacity)
+    return fail(PA_ERR_WORKSPACE,
+                "this step needs %zu bytes of scratch; the built-in buffer holds %zu (use "
+                "pa_decode with its own workspace for larger batches or head counts)",
+                layout.total, capacity);
+  // The piece counter and this step's merge counters must start at zero; the
+  // buffer keeps whatever the previous call left there.
+  {
+    cudaError_t e0 = cudaMemsetAsync(static_cast<char*>(ws) + layout.pool, 0,
+                                     layout.counters - layout.pool +
+                                         static_cast<size_t>(B * Hq) * sizeof(uint32_t),
+                                     cs);
+    if (e0 != cudaSuccess) return cuda_fail(e0, "clearing the scratch counters");
+  }
+  const int elt = fp8 ? 1 : 2;
+  CUtensorMap tk, tv;
+  if ((s = make_cache_map(&tk, key_cache->data, NB * Hkv * block_size, static_cast<int>(D), elt)) ||
+      (s = make_cache_map(&tv, value_cache->data, NB * Hkv * block_size, static_cast<int>(D), elt)))
+    return s;
+
+  const double log2e = 1.4426950408889634;
+  pa::DecodeArgs a;
+  a.q = q->data;
+  a.block_tables = static_cast<const int32_t*>(block_tables->data);
+  a.seq_lens = static_cast<const int32_t*>(seq_lens->data);
+  char* wsb = static_cast<char*>(ws);
+  a.ctrl = reinterpret_cast<int32_t*>(wsb + layout.ctrl);
+  a.pool = reinterpret_cast<uint32_t*>(wsb + layout.pool);
+  a.part = reinterpret_cast<float*>(wsb + layout.part);
+  a.err = st->err_word;
+  a.B = static_cast<int>(B);
+  a.Hq = static_cast<int>(Hq);
+  a.Hkv = static_cast<int>(Hkv);
+  a.G = plan.G;
+  a.D = static_cast<int>(D);
+  a.bs = block_size;
+  a.MB = static_cast<int>(MB);
+  a.NB = static_cast<int>(NB);
+  a.window = window > 0 ? window : 0;
+  a.score_scale = static_cast<float>(static_cast<double>(scale) * log2e *
+                                     (fp8 ? static_cast<double>(k_scale) : 1.0));
+  a.v_scale = fp8 ? v_scale : 1.f;
+  a.min_tiles = plan.min_tiles;
+  a.pool_permille = plan.pool_permille;
+  a.piece_min = plan.piece;
+  a.np_max = plan.workers * kPiecesPerWorker;
+
+  const bool prof = g_prof_before && g_prof_after;
+  cudaError_t e;
+  if (prof && (e = cudaEventRecord(static_cast<cudaEvent_t>(g_prof_before), cs)) != cudaSuccess)
+    return cuda_fail(e, "profile event");
+  e = launch_of(plan.ct, plan.qt, static_cast<int>(D), plan.nt, tk, tv, a, plan.grid, plan.smem,
+                cs, !prof);
+  if (e != cudaSuccess) return cuda_fail(e, "decode kernel launch");
+  if (prof && (e = cudaEventRecord(static_cast<cudaEvent_t>(g_prof_after), cs)) != cudaSuccess)
+    return cuda_fail(e, "profile event");
+  pa::MergeArgs m;
+  m.out = out->data;
+  m.part = a.part;
+  m.ctrl = a.ctrl;
+  m.pool = a.pool;
+  m.counters = reinterpret_cast<uint32_t*>(wsb + layout.counters);
+  m.NW = plan.workers;
+  m.B = a.B;
+  m.Hq = a.Hq;
+  m.Hkv = a.Hkv;
+  m.G = a.G;
+  m.D = a.D;
+  e = pa::merge_launch(q->dtype, m, st->num_sms * 4, cs, !prof);
+  if (e != cudaSuccess) return cuda_fail(e, "merge kernel launch");
+  g_launches += 2;
+  return ok();
+}
+}  // namespace pa

@@ -128,3 +128,16 @@ cudaError_t reshape_launch(int src_type, bool fp8, const ReshapeArgs& a, cudaStr
 cudaError_t device_error_word(int32_t** ptr);  // address of this device's error word
 
 }  // namespace pa
+
+#include "pa.h"
+
+namespace pa {
+
+// pa_decode with the scratch in a given device buffer (pa_api.cpp).
+pa_status decode_in_buffer(const pa_tensor* out, const pa_tensor* q, const pa_tensor* key_cache,
+                           const pa_tensor* value_cache, const pa_tensor* block_tables,
+                           const pa_tensor* seq_lens, int32_t num_kv_heads, float scale,
+                           int32_t block_size, int32_t window, int32_t kv_dtype, float k_scale,
+                           float v_scale, pa_stream stream, void* buffer, size_t capacity);
+
+}  // namespace pa
