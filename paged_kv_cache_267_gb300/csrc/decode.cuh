@@ -141,7 +141,7 @@ __device__ __forceinline__ int acc_dim(int mt, int g, int hi) {
 constexpr unsigned kFlagStart = 1, kFlagEnd = 2, kFlagPool = 4;
 
 template <int CT, int QT, int D, int NT, int WARPS, int STAGES>
-__global__ void __launch_bounds__(WARPS * 32)
+__global__ void __launch_bounds__(WARPS * 32, 2)
     paged_decode_kernel(const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV, const DecodeArgs a) {
   using Gm = Geometry<CT, D, STAGES>;
@@ -662,38 +662,52 @@ struct DecodeKernel {
   }
 };
 
-// Stage count per variant: about 24 KB of ring per warp (two stages at least).
-template <int CT, int D>
-constexpr int stages_for() {
-  constexpr int pair = 2 * kTile * D * ((CT == kE4M3) ? 1 : 2);
-  constexpr int s = (24 * 1024) / pair;
-  return s < 2 ? 2 : s;
+// Worker warps per CTA and pipeline stages per warp. Two CTAs share an SM.
+// The e4m3 path with one n-tile at D = 128 spends about three times the
+// instructions per byte of the 16-bit path, so it runs 8 warps of 3 stages
+// (12 KB of ring each); every other variant runs 4 warps with about 24 KB of
+// ring each (two stages at least).
+template <int CT, int D, int NT>
+constexpr int warps_for() {
+  return (CT == kE4M3 && D == 128 && NT == 1) ? 8 : 4;
 }
 
-constexpr int kWarps = 4;
+template <int CT, int D, int NT>
+constexpr int stages_for() {
+  constexpr int pair = 2 * kTile * D * ((CT == kE4M3) ? 1 : 2);
+  constexpr int ring = (warps_for<CT, D, NT>() == 8) ? 12 * 1024 : 24 * 1024;
+  constexpr int s = ring / pair;
+  return s < 2 ? 2 : s;
+}
 
 // Expands `BODY` with the kernel type K for a runtime (D, NT) pair.
 #define PA_DECODE_DISPATCH(CT, QT, D_, NT_, BODY)                                \
   do {                                                                            \
     if ((D_) == 64 && (NT_) == 1 && (CT) != kE4M3) {                              \
-      using K = DecodeKernel<CT, QT, ((CT) != kE4M3 ? 64 : 128), 1, kWarps,       \
-                             stages_for<CT, ((CT) != kE4M3 ? 64 : 128)>()>;       \
+      constexpr int D0 = (CT) != kE4M3 ? 64 : 128;                                \
+      using K = DecodeKernel<CT, QT, D0, 1, warps_for<CT, D0, 1>(),               \
+                             stages_for<CT, D0, 1>()>;                            \
       BODY;                                                                       \
     } else if ((D_) == 64 && (NT_) == 2 && (CT) != kE4M3) {                       \
-      using K = DecodeKernel<CT, QT, ((CT) != kE4M3 ? 64 : 128), 2, kWarps,       \
-                             stages_for<CT, ((CT) != kE4M3 ? 64 : 128)>()>;       \
+      constexpr int D0 = (CT) != kE4M3 ? 64 : 128;                                \
+      using K = DecodeKernel<CT, QT, D0, 2, warps_for<CT, D0, 2>(),               \
+                             stages_for<CT, D0, 2>()>;                            \
       BODY;                                                                       \
     } else if ((D_) == 128 && (NT_) == 1) {                                       \
-      using K = DecodeKernel<CT, QT, 128, 1, kWarps, stages_for<CT, 128>()>;      \
+      using K = DecodeKernel<CT, QT, 128, 1, warps_for<CT, 128, 1>(),            \
+                             stages_for<CT, 128, 1>()>;                          \
       BODY;                                                                       \
     } else if ((D_) == 128 && (NT_) == 2) {                                       \
-      using K = DecodeKernel<CT, QT, 128, 2, kWarps, stages_for<CT, 128>()>;      \
+      using K = DecodeKernel<CT, QT, 128, 2, warps_for<CT, 128, 2>(),            \
+                             stages_for<CT, 128, 2>()>;                          \
       BODY;                                                                       \
     } else if ((D_) == 256 && (NT_) == 1) {                                       \
-      using K = DecodeKernel<CT, QT, 256, 1, kWarps, stages_for<CT, 256>()>;      \
+      using K = DecodeKernel<CT, QT, 256, 1, warps_for<CT, 256, 1>(),            \
+                             stages_for<CT, 256, 1>()>;                          \
       BODY;                                                                       \
     } else if ((D_) == 256 && (NT_) == 2) {                                       \
-      using K = DecodeKernel<CT, QT, 256, 2, kWarps, stages_for<CT, 256>()>;      \
+      using K = DecodeKernel<CT, QT, 256, 2, warps_for<CT, 256, 2>(),            \
+                             stages_for<CT, 256, 2>()>;                          \
       BODY;                                                                       \
     } else {                                                                      \
       return cudaErrorInvalidValue;                                               \

@@ -35,7 +35,7 @@ constexpr int kDefaultPoolPermille = 100;  // share of tiles handed out dynamica
 constexpr int kDefaultPiece = 4;           // least tiles per pool piece
 constexpr int kPiecesPerWorker = 4;        // pool pieces per worker warp, at most
 constexpr int kMaxCtasPerSm = 2;
-constexpr int kWarpsPerCta = 4;
+constexpr int kWarpsPerCta = 8;  // most worker warps of any decode variant
 constexpr int64_t kMaxBatch = 4096;
 
 pa_status fail(pa_status code, const char* fmt, ...) {
