@@ -201,9 +201,10 @@ pa_status pa_set_workspace(void* ptr, size_t bytes);
  *   min_tiles      least number of 16-token tiles per warp's static range
  *                  (default 4);
  *   pool_permille  share of the tiles handed out dynamically in small pieces
- *                  after the static ranges (default 100; batches where one
- *                  sequence is over 4x the mean length use no pool); negative
- *                  turns the pool off, which makes results bit-reproducible;
+ *                  after the static ranges (default 100; the pool only
+ *                  covers the trailing run of sequences no longer than 4x the
+ *                  mean length); negative turns the pool off, which makes
+ *                  results bit-reproducible;
  *   piece_tiles    least tiles per pool piece (default 4). */
 pa_status pa_set_decode_tuning(int32_t max_ctas, int32_t min_tiles, int32_t pool_permille,
                                int32_t piece_tiles);

@@ -183,15 +183,12 @@ __global__ void __launch_bounds__(WARPS * 32, 2)
     s_len[b] = L;
   }
   __syncthreads();
-  // exclusive prefix of tiles per pair over the sequences (one warp), and the
-  // longest sequence's tile count
-  __shared__ int s_maxnt;
+  // exclusive prefix of tiles per pair over the sequences (one warp)
   if (warp == 0) {
-    int run = 0, mx = 0;
+    int run = 0;
     for (int b0 = 0; b0 < a.B; b0 += 32) {
       const int b = b0 + lane;
       int x = (b < a.B) ? tiles_of(s_len[b], a.window) : 0;
-      mx = max(mx, x);
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const int y = __shfl_up_sync(FULL, x, o);
@@ -200,24 +197,30 @@ __global__ void __launch_bounds__(WARPS * 32, 2)
       if (b < a.B) s_pref[b + 1] = run + x;
       run += __shfl_sync(FULL, x, 31);
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(FULL, mx, o));
-    if (lane == 0) {
-      s_pref[0] = 0;
-      s_maxnt = mx;
-    }
+    if (lane == 0) s_pref[0] = 0;
   }
   __syncthreads();
 
-  // Static ranges for about (1 - pool share) of the tiles, then the pool. The
-  // pool covers the end of the flat space; when one sequence is much longer
-  // than the mean, that end can lie inside it and the pool would cut it into
-  // thousands of small partials, so skewed batches are split statically only.
+  // Static ranges for about (1 - pool share) of the tiles, then the pool at
+  // the end of the flat space. Small pool pieces inside a sequence far longer
+  // than the mean would cut it into thousands of partials, so the pool only
+  // covers the trailing run of sequences at most four times the mean length.
+  __shared__ int s_last_long;
+  if (warp == 0) {
+    const long long thr = 4ll * s_pref[a.B];  // nt_b * B > thr  <=>  nt_b > 4 * mean
+    int last = -1;
+    for (int b = lane; b < a.B; b += 32)
+      if (static_cast<long long>(s_pref[b + 1] - s_pref[b]) * a.B > thr) last = b;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) last = max(last, __shfl_xor_sync(FULL, last, o));
+    if (lane == 0) s_last_long = last;
+  }
+  __syncthreads();
   const int total = a.Hkv * s_pref[a.B];
   const int nw = gridDim.x * WARPS;
-  const bool skewed = static_cast<long long>(s_maxnt) * a.B > 4ll * s_pref[a.B];
-  const long long pool_want =
-      skewed ? 0 : static_cast<long long>(total) * a.pool_permille / 1000;
+  const long long short_tail = total - static_cast<long long>(a.Hkv) * s_pref[s_last_long + 1];
+  long long pool_want = static_cast<long long>(total) * a.pool_permille / 1000;
+  if (pool_want > short_tail) pool_want = short_tail;
   int ws = static_cast<int>((total - pool_want) / nw);
   if (ws < a.min_tiles) ws = a.min_tiles;
   const int ts = static_cast<int>(min(static_cast<long long>(ws) * nw, static_cast<long long>(total)));
