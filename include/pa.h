@@ -244,6 +244,7 @@ int32_t pa_version(void);
  *     reclamation: call it once the GPU work reading them has finished).
  *   - Every call is all-or-nothing: PA_ERR_OUT_OF_BLOCKS leaves the pool as it
  *     was (a hard cap: requests beyond it are rejected, not queued).
+ *   - trim_window() releases blocks a sliding window has left behind.
  * Handles are not thread-safe; use one per thread or lock around calls.
  */
 typedef struct pa_alloc pa_alloc;
@@ -255,6 +256,14 @@ pa_status pa_alloc_fork(pa_alloc* a, int32_t src_seq, int32_t* seq_out);
 pa_status pa_alloc_append(pa_alloc* a, int32_t seq, int64_t n_tokens, int32_t* cow_src,
                           int32_t* cow_dst);
 pa_status pa_alloc_free(pa_alloc* a, int32_t seq);
+/* Releases the blocks of `seq` that lie wholly before its sliding window
+ * [max(0, len - window), len) ("vLLM 0.7.2深度解析" §2.3: blocks known to be
+ * outside the window need not stay allocated). Each drops one reference
+ * (reaching zero, it waits for reclaim()) and its table entry becomes -1,
+ * which a decode with that window never reads. fork() copies -1 entries and
+ * free() skips them. window <= 0 releases nothing. *n_released (may be NULL)
+ * receives the count. */
+pa_status pa_alloc_trim_window(pa_alloc* a, int32_t seq, int32_t window, int32_t* n_released);
 /* Returns the number of blocks moved from pending to free. */
 int32_t pa_alloc_reclaim(pa_alloc* a);
 /* Copies the sequence's block ids (logical order) into out[0 .. capacity);

@@ -24,6 +24,12 @@ Behaviour fixed by this model (the pages leave it open):
     can copy the cached rows.
   * Every operation is all-or-nothing: if the free list cannot cover it,
     ``OutOfBlocks`` is raised and the state is unchanged.
+  * ``trim_window`` ("vLLM 0.7.2深度解析" §2.3: blocks known to lie outside a
+    sliding window are skipped for allocation and loading) releases the
+    blocks of a sequence that lie wholly before its window start
+    ``max(0, len - window)``: each drops one reference and its table entry
+    becomes -1 (never read by a windowed decode). Released entries stay -1;
+    fork copies them as -1, free skips them.
 """
 from __future__ import annotations
 
@@ -87,7 +93,8 @@ class BlockAllocatorModel:
     def fork(self, src: int) -> int:
         s = self.seqs[src]
         for b in s["blocks"]:
-            self.ref[b] += 1
+            if b >= 0:
+                self.ref[b] += 1
         sid = self.next_id
         self.next_id += 1
         self.seqs[sid] = {"blocks": list(s["blocks"]), "len": s["len"]}
@@ -120,9 +127,29 @@ class BlockAllocatorModel:
     def free_seq(self, sid: int) -> None:
         s = self.seqs.pop(sid)
         for b in s["blocks"]:
+            if b < 0:
+                continue
             self.ref[b] -= 1
             if self.ref[b] == 0:
                 self.pending.append(b)
+
+    def trim_window(self, sid: int, window: int) -> int:
+        """Releases the blocks wholly before the window; returns how many."""
+        if window <= 0:
+            return 0
+        s = self.seqs[sid]
+        first_live = max(0, s["len"] - window) // self.block_size
+        n = 0
+        for i in range(min(first_live, len(s["blocks"]))):
+            b = s["blocks"][i]
+            if b < 0:
+                continue
+            s["blocks"][i] = -1
+            self.ref[b] -= 1
+            if self.ref[b] == 0:
+                self.pending.append(b)
+            n += 1
+        return n
 
     def reclaim(self) -> int:
         n = len(self.pending)

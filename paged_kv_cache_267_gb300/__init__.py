@@ -70,6 +70,7 @@ def lib() -> ctypes.CDLL:
             "pa_alloc_fork": (st, [vp, i32, ctypes.POINTER(i32)]),
             "pa_alloc_append": (st, [vp, i32, i64, ctypes.POINTER(i32), ctypes.POINTER(i32)]),
             "pa_alloc_free": (st, [vp, i32]),
+            "pa_alloc_trim_window": (st, [vp, i32, i32, ctypes.POINTER(i32)]),
             "pa_alloc_reclaim": (i32, [vp]),
             "pa_alloc_block_table": (st, [vp, i32, vp, i32, ctypes.POINTER(i32)]),
             "pa_alloc_seq_len": (st, [vp, i32, ctypes.POINTER(i64)]),
@@ -249,6 +250,12 @@ class BlockAllocator:
 
     def free(self, seq: int) -> None:
         _check(lib().pa_alloc_free(self._h, seq))
+
+    def trim_window(self, seq: int, window: int) -> int:
+        """Releases the blocks before the sliding window; returns how many."""
+        n = ctypes.c_int32()
+        _check(lib().pa_alloc_trim_window(self._h, seq, window, ctypes.byref(n)))
+        return n.value
 
     def reclaim(self) -> int:
         return lib().pa_alloc_reclaim(self._h)

@@ -1,7 +1,9 @@
 // Host block allocator of libpa: a fixed pool of physical KV blocks with a
 // seeded shuffled free list, reference-counted sharing (fork), copy-on-write
-// of a shared partial last block on append, deferred reclamation, and a hard
-// capacity ("vLLM 0.5 深度解析" §2.1; "vLLM 0.7.2深度解析" §2.1 and §5.3).
+// of a shared partial last block on append, deferred reclamation, a hard
+// capacity ("vLLM 0.5 深度解析" §2.1; "vLLM 0.7.2深度解析" §2.1 and §5.3), and
+// release of blocks that a sliding window has left behind ("vLLM 0.7.2深度解析"
+// §2.3). A released table entry is -1.
 #include <cstdint>
 #include <new>
 #include <unordered_map>
@@ -90,7 +92,8 @@ pa_status pa_alloc_fork(pa_alloc* a, int32_t src, int32_t* seq_out) {
   auto it = a->seqs.find(src);
   if (it == a->seqs.end()) return PA_ERR_NOT_FOUND;
   pa_alloc::Seq s = it->second;
-  for (int32_t b : s.blocks) a->ref[b] += 1;
+  for (int32_t b : s.blocks)
+    if (b >= 0) a->ref[b] += 1;
   const int32_t id = a->next_id++;
   a->seqs.emplace(id, std::move(s));
   *seq_out = id;
@@ -130,9 +133,30 @@ pa_status pa_alloc_free(pa_alloc* a, int32_t seq) {
   auto it = a->seqs.find(seq);
   if (it == a->seqs.end()) return PA_ERR_NOT_FOUND;
   for (int32_t b : it->second.blocks) {
-    if (--a->ref[b] == 0) a->pending.push_back(b);
+    if (b >= 0 && --a->ref[b] == 0) a->pending.push_back(b);
   }
   a->seqs.erase(it);
+  return PA_OK;
+}
+
+pa_status pa_alloc_trim_window(pa_alloc* a, int32_t seq, int32_t window, int32_t* n_released) {
+  if (!a) return PA_ERR_INVALID_ARG;
+  auto it = a->seqs.find(seq);
+  if (it == a->seqs.end()) return PA_ERR_NOT_FOUND;
+  int32_t n = 0;
+  if (window > 0) {
+    pa_alloc::Seq& s = it->second;
+    const int64_t start = s.len > window ? s.len - window : 0;
+    const int64_t first_live = start / a->block_size;
+    for (int64_t i = 0; i < first_live && i < static_cast<int64_t>(s.blocks.size()); ++i) {
+      const int32_t b = s.blocks[i];
+      if (b < 0) continue;
+      s.blocks[i] = -1;
+      if (--a->ref[b] == 0) a->pending.push_back(b);
+      ++n;
+    }
+  }
+  if (n_released) *n_released = n;
   return PA_OK;
 }
 

@@ -35,7 +35,8 @@ def check_invariants(m: BlockAllocatorModel):
     for s in m.seqs.values():
         assert len(s["blocks"]) == -(-s["len"] // m.block_size)
         for blk in s["blocks"]:
-            counts[blk] += 1
+            if blk >= 0:
+                counts[blk] += 1
     # every reference held by a live sequence is counted exactly once
     assert counts == m.ref
     live = {i for i in range(m.num_blocks) if m.ref[i] > 0}
@@ -74,14 +75,24 @@ def test_random_operation_sequences_keep_invariants():
                     n = rnd.randint(0, 3 * bs)
                     src, dst = m.append(sid, n)
                     new_tab = m.table(sid)
-                    if n > 0 and old_len % bs != 0 and shared_last:
+                    if n > 0 and old_len % bs != 0 and shared_last and old_tab[-1] >= 0:
                         assert src == old_tab[-1] and dst == new_tab[len(old_tab) - 1]
                         assert new_tab[:len(old_tab) - 1] == old_tab[:-1]
                     else:
                         assert (src, dst) == (-1, -1)
                         assert new_tab[:len(old_tab)] == old_tab
-                elif op < 0.95:
+                elif op < 0.85:
                     m.free_seq(rnd.choice(sids))
+                elif op < 0.95:
+                    sid = rnd.choice(sids)
+                    W = rnd.randint(1, 4 * bs)
+                    before = m.table(sid)
+                    n = m.trim_window(sid, W)
+                    after = m.table(sid)
+                    first_live = max(0, m.seq_len(sid) - W) // bs
+                    assert all(b == -1 for b in after[:first_live])
+                    assert after[first_live:] == before[first_live:]
+                    assert n == sum(1 for b in before[:first_live] if b >= 0)
                 else:
                     m.reclaim()
                     assert m.num_pending() == 0
@@ -120,3 +131,21 @@ def test_shared_prefix_fork_and_copy_on_write():
     f = m.fork(q)
     assert m.append(f, 5) == (-1, -1)
     assert m.table(f)[:2] == m.table(q)
+
+
+def test_trim_window_releases_only_blocks_before_the_window():
+    m = BlockAllocatorModel(32, 16, seed=5)
+    p = m.add(64)                       # 4 full blocks, shared below
+    f = m.fork(p)
+    m.append(f, 40)                     # f: 104 tokens, 7 blocks
+    before = m.table(f)
+    assert m.trim_window(f, 50) == 3    # window [54, 104) starts in block 3
+    assert m.table(f)[:3] == [-1, -1, -1] and m.table(f)[3:] == before[3:]
+    assert all(m.refcount(b) == 1 for b in before[:3])   # still held by p
+    assert m.num_pending() == 0
+    m.free_seq(p)
+    assert m.num_pending() == 3         # blocks 0..2; block 3 is still held by f
+    assert m.refcount(before[3]) == 1
+    assert m.trim_window(f, 50) == 0    # idempotent
+    g = m.fork(f)
+    assert m.table(g)[:3] == [-1, -1, -1]

@@ -270,3 +270,33 @@ def test_calls_with_different_batches_share_one_workspace(pa_lib):
                 assert_close(out_f64(sides.out), sides.ref, what=f"B={sp.batch}")
     finally:
         pa_lib.set_decode_tuning(0, 0, 0, 0)
+
+
+def test_decode_on_window_trimmed_tables(pa_lib):
+    """Blocks a sliding window left behind are released by the allocator (table
+    entries -1); decode with that window never reads them, and the released
+    blocks are reused after reclaim."""
+    bs, Hkv, Hq, D, W = 16, 2, 8, 128, 100
+    alloc = pa_lib.BlockAllocator(128, bs, seed=21)
+    root = alloc.add(96)                      # a shared prefix of 6 full blocks
+    seqs = [alloc.fork(root) for _ in range(3)]
+    for i, sq in enumerate(seqs):
+        alloc.append(sq, 150 + 37 * i)
+    alloc.free(root)
+    released = [alloc.trim_window(sq, W) for sq in seqs]
+    assert all(r > 0 for r in released)
+    tables, lens = alloc.fill_tables(seqs, max_blocks=32)
+    assert (tables[:, 0] == -1).all()
+    g = torch.Generator(device="cuda").manual_seed(8)
+    kc = torch.randn((128, Hkv, bs, D), generator=g, device="cuda").to(torch.bfloat16)
+    vc = torch.randn((128, Hkv, bs, D), generator=g, device="cuda").to(torch.bfloat16)
+    q = torch.randn((3, Hq, D), generator=g, device="cuda").to(torch.bfloat16)
+    out = pa_lib.decode(q, kc, vc, torch.from_numpy(tables).cuda(), torch.from_numpy(lens).cuda(),
+                        num_kv_heads=Hkv, scale=D ** -0.5, block_size=bs, window=W)
+    ref = oracle.decode(q.cpu(), host_copy(kc), host_copy(vc), tables, lens, num_kv_heads=Hkv,
+                        scale=D ** -0.5, block_size=bs, window=W, q_dtype="bf16",
+                        cache_dtype="bf16")
+    assert_close(out_f64(out), ref, what="window-trimmed tables")
+    assert pa_lib.check_device_error() == 0
+    free_before = alloc.num_free()
+    assert alloc.reclaim() > 0 and alloc.num_free() > free_before

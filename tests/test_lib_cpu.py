@@ -133,10 +133,13 @@ def _model_vs_lib(pa, seed):
                     a.append(sid, n)
                 continue
             assert a.append(sid, n) == pm
-        elif op < 0.95:
+        elif op < 0.85:
             sid = rnd.choice(sids)
             m.free_seq(sid)
             a.free(sid)
+        elif op < 0.95:
+            sid, W = rnd.choice(sids), rnd.randint(-1, 4 * bs)
+            assert a.trim_window(sid, W) == m.trim_window(sid, W)
         else:
             assert a.reclaim() == m.reclaim()
         for sid in m.seqs:
