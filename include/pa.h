@@ -253,6 +253,18 @@ pa_status pa_alloc_create(int32_t num_blocks, int32_t block_size, uint64_t seed,
 void pa_alloc_destroy(pa_alloc* a);
 pa_status pa_alloc_add(pa_alloc* a, int64_t n_tokens, int32_t* seq_out);
 pa_status pa_alloc_fork(pa_alloc* a, int32_t src_seq, int32_t* seq_out);
+/* Prefix caching ("vLLM 0.7.2深度解析" §2.1 and §5.2; "vLLM 0.5 深度解析"
+ * §4.4): a new sequence for n_tokens token ids that reuses cached full blocks
+ * for its longest cached prefix. Full block i is keyed by
+ * FNV-1a-64(key_{i-1} as 8 little-endian bytes || its token ids as 4
+ * little-endian bytes each), key_{-1} = 0, and a hit also needs equal token
+ * ids. Reused blocks gain a reference (one waiting for reclaim() is taken back);
+ * the rest are allocated as by add(), and new full blocks are registered.
+ * *n_cached (may be NULL) receives the number of tokens covered by reused
+ * blocks: their K/V are already cached and need not be written again.
+ * reclaim() drops the cache entries of the blocks it frees. */
+pa_status pa_alloc_add_cached(pa_alloc* a, const int32_t* tokens, int64_t n_tokens,
+                              int32_t* seq_out, int64_t* n_cached);
 pa_status pa_alloc_append(pa_alloc* a, int32_t seq, int64_t n_tokens, int32_t* cow_src,
                           int32_t* cow_dst);
 pa_status pa_alloc_free(pa_alloc* a, int32_t seq);

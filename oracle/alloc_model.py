@@ -24,6 +24,15 @@ Behaviour fixed by this model (the pages leave it open):
     can copy the cached rows.
   * Every operation is all-or-nothing: if the free list cannot cover it,
     ``OutOfBlocks`` is raised and the state is unchanged.
+  * ``add_cached`` (prefix caching: "vLLM 0.7.2深度解析" §2.1 and §5.2,
+    "vLLM 0.5 深度解析" §4.4) allocates a sequence for a list of token ids and
+    reuses cached full blocks for its longest cached prefix. Full block i is
+    keyed by h_i = FNV-1a-64(le64(h_{i-1}) || le32 tokens of block i), with
+    h_{-1} = 0; a hit also needs the stored token ids to be equal. Cached
+    blocks are live or waiting in the pending list (a hit there takes the
+    block back out of it); ``reclaim`` drops the cache entries of the blocks it
+    returns to the free list. New full blocks are registered if their key is
+    not yet cached; partial blocks never are.
   * ``trim_window`` ("vLLM 0.7.2深度解析" §2.3: blocks known to lie outside a
     sliding window are skipped for allocation and loading) releases the
     blocks of a sequence that lie wholly before its window start
@@ -54,6 +63,24 @@ class SplitMix64:
         return z ^ (z >> 31)
 
 
+FNV64_OFFSET = 0xCBF29CE484222325
+FNV64_PRIME = 0x100000001B3
+
+
+def fnv1a64(data: bytes, h: int = FNV64_OFFSET) -> int:
+    """FNV-1a, 64-bit (Fowler, Noll, Vo): per byte, xor then multiply."""
+    for byte in data:
+        h ^= byte
+        h = (h * FNV64_PRIME) & MASK64
+    return h
+
+
+def block_key(prev: int, tokens) -> int:
+    data = prev.to_bytes(8, "little") + b"".join(
+        (int(t) & 0xFFFFFFFF).to_bytes(4, "little") for t in tokens)
+    return fnv1a64(data)
+
+
 class BlockAllocatorModel:
     def __init__(self, num_blocks: int, block_size: int, seed: int):
         if num_blocks < 0 or block_size <= 0:
@@ -70,6 +97,8 @@ class BlockAllocatorModel:
         self.ref = [0] * num_blocks
         self.seqs: dict[int, dict] = {}
         self.next_id = 0
+        self.cache: dict[int, int] = {}              # key -> block
+        self.cached: dict[int, tuple] = {}           # block -> (key, token ids)
 
     def _blocks_for(self, n_tokens: int) -> int:
         return (n_tokens + self.block_size - 1) // self.block_size
@@ -151,8 +180,50 @@ class BlockAllocatorModel:
             n += 1
         return n
 
+    def add_cached(self, tokens) -> tuple[int, int]:
+        """New sequence for `tokens`; returns (sequence id, cached tokens)."""
+        tokens = [int(t) for t in tokens]
+        n = len(tokens)
+        bs = self.block_size
+        nblk = -(-n // bs)
+        nfull = n // bs
+        keys, reuse, prev, matching = [], [], 0, True
+        for i in range(nfull):
+            blk_tokens = tuple(tokens[i * bs:(i + 1) * bs])
+            key = block_key(prev, blk_tokens)
+            keys.append(key)
+            prev = key
+            if matching:
+                b = self.cache.get(key)
+                if b is not None and self.cached[b][1] == blk_tokens:
+                    reuse.append(b)
+                else:
+                    matching = False
+        if nblk - len(reuse) > len(self.free):
+            raise OutOfBlocks()
+        blocks = []
+        for b in reuse:
+            if self.ref[b] == 0:
+                self.pending.remove(b)
+            self.ref[b] += 1
+            blocks.append(b)
+        for i in range(len(reuse), nblk):
+            b = self._pop()
+            blocks.append(b)
+            if i < nfull and keys[i] not in self.cache:
+                self.cache[keys[i]] = b
+                self.cached[b] = (keys[i], tuple(tokens[i * bs:(i + 1) * bs]))
+        sid = self.next_id
+        self.next_id += 1
+        self.seqs[sid] = {"blocks": blocks, "len": n}
+        return sid, len(reuse) * bs
+
     def reclaim(self) -> int:
         n = len(self.pending)
+        for b in self.pending:
+            entry = self.cached.pop(b, None)
+            if entry is not None:
+                del self.cache[entry[0]]
         self.free.extend(self.pending)
         self.pending = []
         return n

@@ -68,6 +68,7 @@ def lib() -> ctypes.CDLL:
             "pa_alloc_destroy": (None, [vp]),
             "pa_alloc_add": (st, [vp, i64, ctypes.POINTER(i32)]),
             "pa_alloc_fork": (st, [vp, i32, ctypes.POINTER(i32)]),
+            "pa_alloc_add_cached": (st, [vp, vp, i64, ctypes.POINTER(i32), ctypes.POINTER(i64)]),
             "pa_alloc_append": (st, [vp, i32, i64, ctypes.POINTER(i32), ctypes.POINTER(i32)]),
             "pa_alloc_free": (st, [vp, i32]),
             "pa_alloc_trim_window": (st, [vp, i32, i32, ctypes.POINTER(i32)]),
@@ -237,6 +238,16 @@ class BlockAllocator:
         s = ctypes.c_int32()
         _check(lib().pa_alloc_add(self._h, n_tokens, ctypes.byref(s)))
         return s.value
+
+    def add_cached(self, tokens) -> tuple[int, int]:
+        """New sequence for token ids, reusing cached full blocks of its longest
+        cached prefix; returns (sequence id, number of cached tokens)."""
+        import numpy as np
+        t = np.ascontiguousarray(np.asarray(tokens, dtype=np.int32))
+        s, c = ctypes.c_int32(), ctypes.c_int64()
+        _check(lib().pa_alloc_add_cached(self._h, t.ctypes.data if t.size else None, t.size,
+                                         ctypes.byref(s), ctypes.byref(c)))
+        return s.value, c.value
 
     def fork(self, src: int) -> int:
         s = ctypes.c_int32()

@@ -4,9 +4,11 @@
 // capacity ("vLLM 0.5 深度解析" §2.1; "vLLM 0.7.2深度解析" §2.1 and §5.3), and
 // release of blocks that a sliding window has left behind ("vLLM 0.7.2深度解析"
 // §2.3). A released table entry is -1.
+#include <algorithm>
 #include <cstdint>
 #include <new>
 #include <unordered_map>
+#include <utility>
 #include <vector>
 
 #include "pa.h"
@@ -23,6 +25,9 @@ struct pa_alloc {
   };
   std::unordered_map<int32_t, Seq> seqs;
   int32_t next_id = 0;
+  // prefix cache: key -> block, and block -> (key, token ids of the block)
+  std::unordered_map<uint64_t, int32_t> cache;
+  std::unordered_map<int32_t, std::pair<uint64_t, std::vector<int32_t>>> cached;
 };
 
 namespace {
@@ -40,6 +45,31 @@ struct SplitMix64 {
 };
 
 int64_t blocks_for(int64_t n, int32_t bs) { return (n + bs - 1) / bs; }
+
+// FNV-1a, 64-bit (Fowler, Noll, Vo): per byte, xor then multiply.
+uint64_t fnv1a64_bytes(const unsigned char* p, size_t n, uint64_t h) {
+  for (size_t i = 0; i < n; ++i) {
+    h ^= p[i];
+    h *= 0x100000001B3ull;
+  }
+  return h;
+}
+
+// Key of a full block: FNV-1a-64 over the previous key (8 bytes, little
+// endian) followed by the block's token ids (4 bytes each, little endian).
+uint64_t block_key(uint64_t prev, const int32_t* tok, int32_t bs) {
+  unsigned char buf[8];
+  for (int i = 0; i < 8; ++i) buf[i] = static_cast<unsigned char>(prev >> (8 * i));
+  uint64_t h = fnv1a64_bytes(buf, 8, 0xCBF29CE484222325ull);
+  for (int32_t j = 0; j < bs; ++j) {
+    const uint32_t t = static_cast<uint32_t>(tok[j]);
+    unsigned char b4[4] = {static_cast<unsigned char>(t), static_cast<unsigned char>(t >> 8),
+                           static_cast<unsigned char>(t >> 16),
+                           static_cast<unsigned char>(t >> 24)};
+    h = fnv1a64_bytes(b4, 4, h);
+  }
+  return h;
+}
 
 int32_t pop_block(pa_alloc* a) {
   int32_t b = a->free_list.back();
@@ -160,8 +190,64 @@ pa_status pa_alloc_trim_window(pa_alloc* a, int32_t seq, int32_t window, int32_t
   return PA_OK;
 }
 
+pa_status pa_alloc_add_cached(pa_alloc* a, const int32_t* tokens, int64_t n_tokens,
+                              int32_t* seq_out, int64_t* n_cached) {
+  if (!a || !seq_out || n_tokens < 0 || (n_tokens > 0 && !tokens)) return PA_ERR_INVALID_ARG;
+  const int32_t bs = a->block_size;
+  const int64_t nblk = blocks_for(n_tokens, bs), nfull = n_tokens / bs;
+  std::vector<uint64_t> keys(static_cast<size_t>(nfull));
+  std::vector<int32_t> reuse;
+  uint64_t prev = 0;
+  bool matching = true;
+  for (int64_t i = 0; i < nfull; ++i) {
+    const int32_t* tok = tokens + i * bs;
+    keys[i] = block_key(prev, tok, bs);
+    prev = keys[i];
+    if (!matching) continue;
+    auto it = a->cache.find(keys[i]);
+    if (it != a->cache.end()) {
+      const auto& stored = a->cached[it->second].second;
+      if (std::equal(stored.begin(), stored.end(), tok)) {
+        reuse.push_back(it->second);
+        continue;
+      }
+    }
+    matching = false;
+  }
+  if (nblk - static_cast<int64_t>(reuse.size()) > static_cast<int64_t>(a->free_list.size()))
+    return PA_ERR_OUT_OF_BLOCKS;
+  pa_alloc::Seq s;
+  s.len = n_tokens;
+  s.blocks.reserve(static_cast<size_t>(nblk));
+  for (int32_t b : reuse) {
+    if (a->ref[b] == 0) a->pending.erase(std::find(a->pending.begin(), a->pending.end(), b));
+    a->ref[b] += 1;
+    s.blocks.push_back(b);
+  }
+  for (int64_t i = static_cast<int64_t>(reuse.size()); i < nblk; ++i) {
+    const int32_t b = pop_block(a);
+    s.blocks.push_back(b);
+    if (i < nfull && a->cache.find(keys[i]) == a->cache.end()) {
+      a->cache.emplace(keys[i], b);
+      a->cached[b] = {keys[i], std::vector<int32_t>(tokens + i * bs, tokens + (i + 1) * bs)};
+    }
+  }
+  const int32_t id = a->next_id++;
+  a->seqs.emplace(id, std::move(s));
+  *seq_out = id;
+  if (n_cached) *n_cached = static_cast<int64_t>(reuse.size()) * bs;
+  return PA_OK;
+}
+
 int32_t pa_alloc_reclaim(pa_alloc* a) {
   if (!a) return 0;
+  for (int32_t b : a->pending) {
+    auto it = a->cached.find(b);
+    if (it != a->cached.end()) {
+      a->cache.erase(it->second.first);
+      a->cached.erase(it);
+    }
+  }
   const int32_t n = static_cast<int32_t>(a->pending.size());
   a->free_list.insert(a->free_list.end(), a->pending.begin(), a->pending.end());
   a->pending.clear();

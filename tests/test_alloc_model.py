@@ -8,7 +8,7 @@ import random
 
 import pytest
 
-from oracle.alloc_model import BlockAllocatorModel, OutOfBlocks, SplitMix64
+from oracle.alloc_model import BlockAllocatorModel, OutOfBlocks, SplitMix64, block_key, fnv1a64
 
 
 def test_splitmix64_reference_outputs():
@@ -149,3 +149,68 @@ def test_trim_window_releases_only_blocks_before_the_window():
     assert m.trim_window(f, 50) == 0    # idempotent
     g = m.fork(f)
     assert m.table(g)[:3] == [-1, -1, -1]
+
+
+def test_fnv1a64_reference_values():
+    # published FNV-1a 64-bit test vectors
+    assert fnv1a64(b"") == 0xCBF29CE484222325
+    assert fnv1a64(b"a") == 0xAF63DC4C8601EC8C
+    assert fnv1a64(b"foobar") == 0x85944171F73967E8
+
+
+def test_prefix_cache_reuses_full_blocks_of_the_longest_cached_prefix():
+    bs = 16
+    m = BlockAllocatorModel(64, bs, seed=9)
+    prompt = list(range(100, 140))                # 40 tokens: 2 full blocks + 8
+    a, ca = m.add_cached(prompt)
+    assert ca == 0
+    b, cb = m.add_cached(prompt + [7, 8, 9])
+    assert cb == 32 and m.table(b)[:2] == m.table(a)[:2]
+    assert m.table(b)[2] != m.table(a)[2]           # partial blocks are never shared
+    assert all(m.refcount(x) == 2 for x in m.table(a)[:2])
+    c, cc = m.add_cached(prompt[:16] + [0] * 24)    # differs in block 1
+    assert cc == 16 and m.table(c)[0] == m.table(a)[0] and m.table(c)[1] != m.table(a)[1]
+    # keys chain: block 1 of a different first block is a different key
+    assert block_key(block_key(0, prompt[:16]), prompt[16:32]) != \
+        block_key(block_key(0, [0] * 16), prompt[16:32])
+    check_invariants(m)
+    # a cached block waiting for reclaim is taken back out of the pending list
+    for sid in (a, b, c):
+        m.free_seq(sid)
+    assert m.num_pending() > 0
+    d, cd = m.add_cached(prompt)
+    assert cd == 32 and all(m.refcount(x) == 1 for x in m.table(d)[:2])
+    check_invariants(m)
+    # reclaim drops the cache entries of the blocks it frees
+    m.free_seq(d)
+    m.reclaim()
+    e, ce = m.add_cached(prompt)
+    assert ce == 0 and not set(m.cache.values()) - set(m.table(e))
+    check_invariants(m)
+
+
+def test_prefix_cache_random_sequences_keep_invariants():
+    rnd = random.Random(7)
+    bs = 4
+    m = BlockAllocatorModel(200, bs, seed=3)
+    prompts = [[rnd.randrange(5) for _ in range(rnd.randint(0, 40))] for _ in range(6)]
+    for step in range(500):
+        op = rnd.random()
+        sids = sorted(m.seqs)
+        try:
+            if op < 0.5 or not sids:
+                p = list(rnd.choice(prompts))
+                p += [rnd.randrange(5) for _ in range(rnd.randint(0, 10))]
+                sid, c = m.add_cached(p)
+                assert c % bs == 0 and c <= len(p)
+            elif op < 0.8:
+                m.free_seq(rnd.choice(sids))
+            elif op < 0.9:
+                m.append(rnd.choice(sids), rnd.randint(1, 9))
+            else:
+                m.reclaim()
+        except OutOfBlocks:
+            pass
+        check_invariants(m)
+        for key, b in m.cache.items():
+            assert m.cached[b][0] == key and (m.ref[b] > 0 or b in m.pending)

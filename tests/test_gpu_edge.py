@@ -300,3 +300,44 @@ def test_decode_on_window_trimmed_tables(pa_lib):
     assert pa_lib.check_device_error() == 0
     free_before = alloc.num_free()
     assert alloc.reclaim() > 0 and alloc.num_free() > free_before
+
+
+def test_prefix_cached_requests_write_only_uncached_rows(pa_lib):
+    """Request B repeats request A's 40-token prompt and adds 8 tokens: B
+    reuses A's two cached full blocks, writes K/V only for its other 16
+    positions, and both decode to the oracle's result."""
+    bs, Hkv, Hq, D, NB = 16, 2, 8, 64, 64
+    alloc = pa_lib.BlockAllocator(NB, bs, seed=4)
+    rng = np.random.default_rng(12)
+    prompt = list(rng.integers(0, 1000, 40))
+    toks_b = prompt + list(rng.integers(0, 1000, 8))
+
+    def row(tokens, p):  # K/V of position p depends on the prefix tokens[:p + 1] only
+        g = torch.Generator().manual_seed(hash(tuple(int(t) for t in tokens[:p + 1])) % (1 << 62))
+        return torch.randn((2, Hkv, D), generator=g).to(torch.bfloat16)
+
+    kc = torch.full((NB, Hkv, bs, D), float("nan"), dtype=torch.bfloat16, device="cuda")
+    vc = kc.clone()
+
+    def write(seq, tokens, first):
+        tab = alloc.table(seq)
+        pos = list(range(first, len(tokens)))
+        rows = torch.stack([row(tokens, p) for p in pos]).cuda()
+        slots = torch.tensor([tab[p // bs] * bs + p % bs for p in pos], dtype=torch.int64,
+                             device="cuda")
+        pa_lib.reshape_and_cache(rows[:, 0].contiguous(), rows[:, 1].contiguous(), kc, vc, slots)
+
+    a, ca = alloc.add_cached(prompt)
+    assert ca == 0
+    write(a, prompt, 0)
+    b, cb = alloc.add_cached(toks_b)
+    assert cb == 32 and alloc.table(b)[:2] == alloc.table(a)[:2]
+    write(b, toks_b, cb)
+    tables, lens = alloc.fill_tables([a, b], max_blocks=4)
+    q = torch.randn((2, Hq, D), generator=torch.Generator(device="cuda").manual_seed(3),
+                    device="cuda").to(torch.bfloat16)
+    out = pa_lib.decode(q, kc, vc, torch.from_numpy(tables).cuda(), torch.from_numpy(lens).cuda(),
+                        num_kv_heads=Hkv, scale=D ** -0.5, block_size=bs)
+    ref = oracle.decode(q.cpu(), host_copy(kc), host_copy(vc), tables, lens, num_kv_heads=Hkv,
+                        scale=D ** -0.5, block_size=bs, q_dtype="bf16", cache_dtype="bf16")
+    assert_close(out_f64(out), ref, what="prefix-cached requests")

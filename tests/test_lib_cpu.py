@@ -175,3 +175,47 @@ def test_allocator_errors(pa_lib):
         a.fill_tables([s], 2)        # table wider than the matrix
     t, lens = a.fill_tables([s], 4)
     assert sorted(t[0]) == [0, 1, 2, 3] and lens[0] == 64
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_allocator_prefix_cache_matches_model_exactly(seed, pa_lib):
+    rnd = random.Random(100 + seed)
+    bs = rnd.choice([1, 4, 16])
+    nb = rnd.randint(20, 200)
+    m = BlockAllocatorModel(nb, bs, seed=seed)
+    a = pa_lib.BlockAllocator(nb, bs, seed=seed)
+    prompts = [[rnd.randrange(4) for _ in range(rnd.randint(0, 6 * bs))] for _ in range(5)]
+    for _ in range(400):
+        op = rnd.random()
+        sids = sorted(m.seqs)
+        if op < 0.45 or not sids:
+            p = list(rnd.choice(prompts)) + [rnd.randrange(4) for _ in range(rnd.randint(0, 2 * bs))]
+            try:
+                want = m.add_cached(p)
+            except OutOfBlocks:
+                with pytest.raises(pa_lib.OutOfBlocks):
+                    a.add_cached(p)
+                continue
+            assert a.add_cached(p) == want
+        elif op < 0.7:
+            sid = rnd.choice(sids)
+            m.free_seq(sid)
+            a.free(sid)
+        elif op < 0.8:
+            sid, n = rnd.choice(sids), rnd.randint(1, 2 * bs)
+            try:
+                want = m.append(sid, n)
+            except OutOfBlocks:
+                with pytest.raises(pa_lib.OutOfBlocks):
+                    a.append(sid, n)
+                continue
+            assert a.append(sid, n) == want
+        elif op < 0.9:
+            sid, W = rnd.choice(sids), rnd.randint(1, 3 * bs)
+            assert a.trim_window(sid, W) == m.trim_window(sid, W)
+        else:
+            assert a.reclaim() == m.reclaim()
+        for sid in m.seqs:
+            assert a.table(sid) == m.table(sid)
+        assert [a.refcount(b) for b in range(nb)] == m.ref
+        assert a.num_free() == m.num_free() and a.num_pending() == m.num_pending()
