@@ -53,6 +53,10 @@ def lib() -> ctypes.CDLL:
         L.orc_decode.argtypes = [vp, vp, c_int, vp, vp, c_int, vp, vp, c_i64, c_i64, c_i64,
                                  c_i64, c_i64, c_i64, c_i64, c_dbl, c_i64, c_dbl, c_dbl, vp,
                                  c_i64, c_int]
+        L.orc_decode_multi.restype = c_int
+        L.orc_decode_multi.argtypes = [vp, vp, c_int, vp, vp, c_int, vp, vp, c_i64, c_i64, c_i64,
+                                       c_i64, c_i64, c_i64, c_i64, c_i64, c_dbl, c_i64, c_dbl,
+                                       c_dbl, vp, c_i64, c_int]
         _lib = L
     return _lib
 
@@ -173,4 +177,37 @@ def decode(q, key_cache, value_cache, block_tables, seq_lens, *, num_kv_heads: i
                           float(v_scale), pp, npairs, threads or default_threads())
     if rc != 0:
         raise ValueError(f"oracle decode failed: {rc}")
+    return out
+
+
+def decode_multi(q, key_cache, value_cache, block_tables, seq_lens, *, num_kv_heads: int,
+                 scale: float, block_size: int, window: int = 0, q_dtype: str,
+                 cache_dtype: str, k_scale: float = 1.0, v_scale: float = 1.0,
+                 triples=None, threads: int | None = None) -> np.ndarray:
+    """fp64 output [B, T, Hq, D] of T causal queries per sequence at its last T
+    positions; rows not listed in ``triples`` (b, t, h) stay zero."""
+    qb = _bits16(q)
+    B, T, Hq, D = qb.shape
+    if _DT[cache_dtype] == E4M3:
+        kc, vc = _bytes8(key_cache), _bytes8(value_cache)
+    else:
+        kc, vc = _bits16(key_cache), _bits16(value_cache)
+    NB, Hkv, bs, D2 = kc.shape
+    assert Hkv == num_kv_heads and bs == block_size and D2 == D
+    bt = np.ascontiguousarray(np.asarray(block_tables, dtype=np.int32))
+    lens = np.ascontiguousarray(np.asarray(seq_lens, dtype=np.int32))
+    MB = bt.shape[1]
+    out = np.zeros((B, T, Hq, D), np.float64)
+    if triples is not None:
+        tr = np.ascontiguousarray(np.asarray(triples, dtype=np.int32).reshape(-1, 3))
+        tp, ntr = _ptr(tr), tr.shape[0]
+    else:
+        tr, tp, ntr = None, None, 0
+    rc = lib().orc_decode_multi(_ptr(out), _ptr(qb), _DT[q_dtype], _ptr(kc), _ptr(vc),
+                                _DT[cache_dtype], _ptr(bt) if bt.size else None, _ptr(lens), B,
+                                T, Hq, Hkv, D, NB, bs, MB, float(scale), int(window),
+                                float(k_scale), float(v_scale), tp, ntr,
+                                threads or default_threads())
+    if rc != 0:
+        raise ValueError(f"oracle decode_multi failed: {rc}")
     return out

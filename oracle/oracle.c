@@ -330,3 +330,117 @@ int orc_decode(double* out, const uint16_t* q, int q_dtype, const void* key_cach
   orc_parallel(orc_decode_range, &c, n, threads);
   return c.err;
 }
+
+/* ------------------------------------------------- multi-token (causal) */
+
+typedef struct {
+  double* out;
+  const uint16_t* q;
+  int q_dtype;
+  const void *kc, *vc;
+  int cache_dtype;
+  const int32_t *bt, *lens;
+  int64_t B, T, Hq, Hkv, D, nb, bs, mb, window;
+  double scale, k_scale, v_scale;
+  const int32_t* triples;
+  volatile int err;
+} orc_multi_ctx;
+
+/* Query t of sequence b, head h: softmax over [start_t, p_t] of the causal
+ * prefix ending at its own position. */
+static void orc_multi_one(orc_multi_ctx* c, int64_t b, int64_t t, int64_t h, double* s) {
+  const int64_t D = c->D;
+  double* o = c->out + ((b * c->T + t) * c->Hq + h) * D;
+  for (int64_t d = 0; d < D; ++d) o[d] = 0.0;
+  const int64_t L = c->lens[b];
+  if (L > c->mb * c->bs) {
+    c->err = ORC_ERANGE;
+    return;
+  }
+  const int64_t p = L - c->T + t; /* this query's position */
+  if (p < 0) return;
+  const int64_t start = (c->window > 0 && p + 1 > c->window) ? p + 1 - c->window : 0;
+  const int64_t kvh = h / (c->Hq / c->Hkv);
+  const uint16_t* qh = c->q + ((b * c->T + t) * c->Hq + h) * D;
+  orc_decode_ctx view = {0};
+  view.kc = c->kc;
+  view.vc = c->vc;
+  view.cache_dtype = c->cache_dtype;
+  view.D = D;
+  double m = -INFINITY;
+  for (int64_t j = start; j <= p; ++j) {
+    int64_t blk = c->bt[b * c->mb + j / c->bs];
+    if (blk < 0 || blk >= c->nb) {
+      c->err = ORC_ERANGE;
+      return;
+    }
+    int64_t row = (blk * c->Hkv + kvh) * c->bs + j % c->bs;
+    double dot = 0.0;
+    for (int64_t d = 0; d < D; ++d)
+      dot += decode16(qh[d], c->q_dtype) * cache_elem(&view, c->kc, row, d, c->k_scale);
+    s[j - start] = c->scale * dot;
+    if (s[j - start] > m) m = s[j - start];
+  }
+  double den = 0.0;
+  for (int64_t j = start; j <= p; ++j) {
+    double w = exp(s[j - start] - m);
+    den += w;
+    int64_t blk = c->bt[b * c->mb + j / c->bs];
+    int64_t row = (blk * c->Hkv + kvh) * c->bs + j % c->bs;
+    for (int64_t d = 0; d < D; ++d) o[d] += w * cache_elem(&view, c->vc, row, d, c->v_scale);
+  }
+  for (int64_t d = 0; d < D; ++d) o[d] /= den;
+}
+
+static void orc_multi_range(void* p, int64_t lo, int64_t hi) {
+  orc_multi_ctx* c = (orc_multi_ctx*)p;
+  int64_t maxlen = c->mb * c->bs;
+  double* s = (double*)malloc(sizeof(double) * (size_t)(maxlen > 0 ? maxlen : 1));
+  if (!s) {
+    c->err = ORC_ENOMEM;
+    return;
+  }
+  for (int64_t i = lo; i < hi; ++i) {
+    int64_t b, t, h;
+    if (c->triples) {
+      b = c->triples[3 * i];
+      t = c->triples[3 * i + 1];
+      h = c->triples[3 * i + 2];
+    } else {
+      b = i / (c->T * c->Hq);
+      t = (i / c->Hq) % c->T;
+      h = i % c->Hq;
+    }
+    orc_multi_one(c, b, t, h, s);
+  }
+  free(s);
+}
+
+int orc_decode_multi(double* out, const uint16_t* q, int q_dtype, const void* key_cache,
+                     const void* value_cache, int cache_dtype, const int32_t* block_tables,
+                     const int32_t* seq_lens, int64_t batch, int64_t num_queries,
+                     int64_t num_q_heads, int64_t num_kv_heads, int64_t head_dim,
+                     int64_t num_blocks, int64_t block_size, int64_t max_blocks, double scale,
+                     int64_t window, double k_scale, double v_scale, const int32_t* triples,
+                     int64_t n_triples, int threads) {
+  if (batch < 0 || num_queries <= 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0)
+    return ORC_EINVAL;
+  if (num_q_heads % num_kv_heads != 0 || block_size <= 0 || max_blocks < 0) return ORC_EINVAL;
+  if (q_dtype != ORC_F16 && q_dtype != ORC_BF16) return ORC_EINVAL;
+  if (cache_dtype != ORC_F16 && cache_dtype != ORC_BF16 && cache_dtype != ORC_E4M3)
+    return ORC_EINVAL;
+  int64_t n = triples ? n_triples : batch * num_queries * num_q_heads;
+  if (triples) {
+    for (int64_t i = 0; i < n; ++i)
+      if (triples[3 * i] < 0 || triples[3 * i] >= batch || triples[3 * i + 1] < 0 ||
+          triples[3 * i + 1] >= num_queries || triples[3 * i + 2] < 0 ||
+          triples[3 * i + 2] >= num_q_heads)
+        return ORC_EINVAL;
+  }
+  orc_multi_ctx c = {out, q, q_dtype, key_cache, value_cache, cache_dtype, block_tables,
+                     seq_lens, batch, num_queries, num_q_heads, num_kv_heads, head_dim,
+                     num_blocks, block_size, max_blocks, window, scale, k_scale, v_scale,
+                     triples, 0};
+  orc_parallel(orc_multi_range, &c, n, threads);
+  return c.err;
+}

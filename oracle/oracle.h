@@ -78,6 +78,22 @@ int orc_decode(double* out, const uint16_t* q, int q_dtype, const void* key_cach
                double k_scale, double v_scale, const int32_t* pairs, int64_t n_pairs,
                int threads);
 
+/*
+ * Multi-token decode (chunked queries with a causal mask): q and out are
+ * [B, T, Hq, D]; the T queries of sequence b sit at positions
+ * p_t = seq_lens[b] - T + t (the last T positions of the sequence), and query
+ * t attends to [start_t, p_t], start_t = max(0, p_t + 1 - window) when
+ * window > 0, else 0. A query with p_t < 0 gives zeros. With T = 1 this is
+ * orc_decode. pairs lists (b, t, h) triples, or is NULL for all of them.
+ */
+int orc_decode_multi(double* out, const uint16_t* q, int q_dtype, const void* key_cache,
+                     const void* value_cache, int cache_dtype, const int32_t* block_tables,
+                     const int32_t* seq_lens, int64_t batch, int64_t num_queries,
+                     int64_t num_q_heads, int64_t num_kv_heads, int64_t head_dim,
+                     int64_t num_blocks, int64_t block_size, int64_t max_blocks, double scale,
+                     int64_t window, double k_scale, double v_scale, const int32_t* triples,
+                     int64_t n_triples, int threads);
+
 #ifdef __cplusplus
 }
 #endif

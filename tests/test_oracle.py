@@ -384,3 +384,55 @@ def test_reshape_fp8_matches_torch_cast_of_fp32_quotient():
     for t, s in enumerate(slots):
         assert np.array_equal(kc[s // bs, :, s % bs, :], kq[t].numpy())
         assert np.array_equal(vc[s // bs, :, s % bs, :], vq[t].numpy())
+
+
+# ------------------------------------------------- multi-token (causal)
+
+def _odecode_multi(q, kc, vc, tables, lens, Hkv, bs, scale, window=0, dt="f16", **kw):
+    return oracle.decode_multi(q.view(np.uint16), kc.view(np.uint16), vc.view(np.uint16), tables,
+                               np.asarray(lens, np.int32), num_kv_heads=Hkv, scale=scale,
+                               block_size=bs, window=window, q_dtype=dt, cache_dtype=dt, **kw)
+
+
+@pytest.mark.parametrize("T,W", [(1, 0), (3, 0), (4, 0), (2, 0), (3, 20), (5, 7)])
+def test_decode_multi_matches_dense_causal_sdpa(T, W):
+    rng = np.random.default_rng(200 + T + W)
+    Hkv, G, D, bs = 2, 2, 32, 16
+    lens = [T, T + 1, 40, 17, 90]
+    tables, kc, vc, K, V = _build_paged(rng, lens, Hkv, D, bs)
+    q = rng.normal(size=(len(lens), T, Hkv * G, D)).astype(np.float16)
+    out = _odecode_multi(q, kc, vc, tables, lens, Hkv, bs, 0.3, window=W)
+    for b, L in enumerate(lens):
+        # dense: queries at positions L-T..L-1, boolean causal (+ window) mask
+        pos_q = np.arange(L - T, L)[:, None]
+        pos_k = np.arange(L)[None, :]
+        allowed = pos_k <= pos_q
+        if W > 0:
+            allowed &= pos_k > pos_q - W
+        qd = torch.from_numpy(q[b].astype(np.float64)).permute(1, 0, 2)       # Hq,T,D
+        Kd = torch.from_numpy(K[b].astype(np.float64)).permute(1, 0, 2).repeat_interleave(G, 0)
+        Vd = torch.from_numpy(V[b].astype(np.float64)).permute(1, 0, 2).repeat_interleave(G, 0)
+        ref = F.scaled_dot_product_attention(qd, Kd, Vd, attn_mask=torch.from_numpy(allowed),
+                                             scale=0.3).permute(1, 0, 2).numpy()
+        assert np.abs(out[b] - ref).max() < 1e-13
+
+
+def test_decode_multi_rows_equal_single_query_decode_of_their_prefix():
+    rng = np.random.default_rng(301)
+    Hkv, G, D, bs, T = 2, 4, 16, 16, 3
+    lens = [30, 3, 65]
+    tables, kc, vc, K, V = _build_paged(rng, lens, Hkv, D, bs)
+    q = rng.normal(size=(3, T, Hkv * G, D)).astype(np.float16)
+    multi = _odecode_multi(q, kc, vc, tables, lens, Hkv, bs, 0.25, window=9)
+    for t in range(T):
+        single = _odecode(np.ascontiguousarray(q[:, t]), kc, vc, tables,
+                          [L - T + t + 1 for L in lens], Hkv, bs, 0.25, window=9)
+        assert np.array_equal(multi[:, t], single)
+
+
+def test_decode_multi_queries_before_the_sequence_give_zeros():
+    rng = np.random.default_rng(302)
+    tables, kc, vc, K, V = _build_paged(rng, [2], 1, 8, 16)
+    q = rng.normal(size=(1, 4, 1, 8)).astype(np.float16)
+    out = _odecode_multi(q, kc, vc, tables, [2], 1, 16, 1.0)
+    assert (out[0, :2] == 0).all() and (out[0, 2:] != 0).any()
