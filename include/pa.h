@@ -188,6 +188,40 @@ pa_status pa_decode_noalloc(const pa_tensor* out, const pa_tensor* q,
 pa_status pa_decode_workspace_size(int64_t batch, int32_t num_q_heads, int32_t num_kv_heads,
                                    int32_t head_dim, size_t* bytes);
 
+/*
+ * pa_prefill_chunk — attention of a chunk of T new query tokens per sequence
+ * over the paged cache, causal within the chunk: the chunked-prefill step
+ * that "vLLM 0.5 深度解析" §5.2 switches on in its batching configuration
+ * (the pages give only the switch; the computation below is the plain
+ * reading), and equally the verification step of T drafted tokens.
+ * The chunk's own K/V rows are written to the cache first (pa_reshape_and_cache
+ * with B * T rows); seq_lens[b] counts them. Query t of sequence b sits at
+ * position p = seq_lens[b] - T + t and, with
+ * start = (window > 0 && p + 1 > window) ? p + 1 - window : 0,
+ *   out[b, t, h, :] = sum_{j in [start, p]} softmax_j(scale * q[b,t,h,:] . K_j) V_j
+ * with K_j, V_j as in pa_decode. A query with p < 0 (seq_lens[b] < T) gives a
+ * row of zeros. With T = 1 the result equals pa_decode's.
+ *
+ *   out, q        [B, T, Hq, D] contiguous (q f16 or bf16, out the same),
+ *                 1 <= T <= 4096; every other argument as for pa_decode.
+ * The (query, head) pairs of one KV head are processed 16 at a time, so the
+ * step reads each attended K/V byte ceil(T * G / 16) times (from L2 where
+ * they are close together); for T * G <= 16 it reads it once. Workspace:
+ * pa_prefill_chunk_workspace_size() bytes, from the same source as
+ * pa_decode's. Errors as for pa_decode, plus PA_ERR_UNSUPPORTED for T out of
+ * range or B * Hkv * ceil(T * G / 16) * 16 > 2^19.
+ */
+pa_status pa_prefill_chunk(const pa_tensor* out, const pa_tensor* q, const pa_tensor* key_cache,
+                           const pa_tensor* value_cache, const pa_tensor* block_tables,
+                           const pa_tensor* seq_lens, int32_t num_kv_heads, float scale,
+                           int32_t block_size, int32_t window, int32_t kv_dtype, float k_scale,
+                           float v_scale, pa_stream stream);
+
+/* Workspace bytes pa_prefill_chunk needs on the current device. */
+pa_status pa_prefill_chunk_workspace_size(int64_t batch, int32_t num_queries,
+                                          int32_t num_q_heads, int32_t num_kv_heads,
+                                          int32_t head_dim, size_t* bytes);
+
 /* Use caller-owned device memory [ptr, ptr + bytes) as the decode workspace on
  * the current device (ptr 256-byte aligned). The call zeroes the buffer and
  * synchronises the device; each step leaves its piece counter at zero. ptr == NULL returns to the library-managed

@@ -79,7 +79,9 @@ int orc_decode(double* out, const uint16_t* q, int q_dtype, const void* key_cach
                int threads);
 
 /*
- * Multi-token decode (chunked queries with a causal mask): q and out are
+ * Multi-token decode (chunked queries with a causal mask), the attention of
+ * the chunked prefill that "vLLM 0.5 深度解析" §5.2 switches on; the pages
+ * name only the switch, so this is the plain causal reading: q and out are
  * [B, T, Hq, D]; the T queries of sequence b sit at positions
  * p_t = seq_lens[b] - T + t (the last T positions of the sequence), and query
  * t attends to [start_t, p_t], start_t = max(0, p_t + 1 - window) when

@@ -57,6 +57,9 @@ def lib() -> ctypes.CDLL:
             "pa_decode": (st, [P, P, P, P, P, P, i32, f32, i32, i32, i32, f32, f32, vp]),
             "pa_decode_noalloc": (st, [P, P, P, P, P, P, i32, f32, i32, i32, i32, f32, f32, vp]),
             "pa_decode_workspace_size": (st, [i64, i32, i32, i32, ctypes.POINTER(ctypes.c_size_t)]),
+            "pa_prefill_chunk": (st, [P, P, P, P, P, P, i32, f32, i32, i32, i32, f32, f32, vp]),
+            "pa_prefill_chunk_workspace_size": (st, [i64, i32, i32, i32, i32,
+                                                     ctypes.POINTER(ctypes.c_size_t)]),
             "pa_set_workspace": (st, [vp, ctypes.c_size_t]),
             "pa_set_decode_tuning": (st, [i32, i32, i32, i32]),
             "pa_profile_events": (st, [vp, vp]),
@@ -159,6 +162,21 @@ def decode(q, key_cache, value_cache, block_tables, seq_lens, *, num_kv_heads: i
     return out
 
 
+def prefill_chunk(q, key_cache, value_cache, block_tables, seq_lens, *, num_kv_heads: int,
+                  scale: float, block_size: int, window: int = 0, kv_dtype="auto",
+                  k_scale: float = 1.0, v_scale: float = 1.0, out=None, stream=None):
+    """Causal attention of T query tokens per sequence (q [B, T, Hq, D], at
+    the last T positions of each sequence) over the paged cache; returns out
+    [B, T, Hq, D] (allocated if not given)."""
+    if out is None:
+        out = torch.empty_like(q)
+    descs = [tensor_desc(x) for x in (out, q, key_cache, value_cache, block_tables, seq_lens)]
+    _check(lib().pa_prefill_chunk(*[ctypes.byref(d) for d in descs], int(num_kv_heads),
+                                  float(scale), int(block_size), int(window), _kv(kv_dtype),
+                                  float(k_scale), float(v_scale), _stream(stream)))
+    return out
+
+
 def decode_noalloc(q, key_cache, value_cache, block_tables, seq_lens, *, num_kv_heads: int,
                    scale: float, block_size: int, out, window: int = 0, kv_dtype="auto",
                    k_scale: float = 1.0, v_scale: float = 1.0, stream=None):
@@ -176,6 +194,14 @@ def workspace_size(batch: int, num_q_heads: int, num_kv_heads: int, head_dim: in
     n = ctypes.c_size_t(0)
     _check(lib().pa_decode_workspace_size(batch, num_q_heads, num_kv_heads, head_dim,
                                           ctypes.byref(n)))
+    return n.value
+
+
+def prefill_chunk_workspace_size(batch: int, num_queries: int, num_q_heads: int,
+                                 num_kv_heads: int, head_dim: int) -> int:
+    n = ctypes.c_size_t(0)
+    _check(lib().pa_prefill_chunk_workspace_size(batch, num_queries, num_q_heads, num_kv_heads,
+                                                 head_dim, ctypes.byref(n)))
     return n.value
 
 

@@ -34,6 +34,17 @@
 // the first and last tile of a pair get score -inf and their V rows are
 // zeroed in the fragment, so poisoned slots never reach the result.
 //
+// Chunked queries (MQ = true). A sequence may bring T query tokens at its
+// last T positions, each attending causally to its own prefix (clipped by
+// the window), as in the chunked prefill of "vLLM 0.7.2深度解析". The mma
+// n-columns of a pair are then (query, head) columns c = t * G + h, at most
+// 16 per pair; with more, the columns are cut into NCG groups of 16 and each
+// group is a pair of its own (a "virtual" KV head vh = kvh * NCG + group), so
+// the same K/V tile is read once per group. A pair's tiles cover the union of
+// its queries' ranges; scores outside a column's own range get -inf, and the
+// running maxima start at a finite floor so that a column with no position in
+// a segment yields m = floor, l = 0 and a zero output.
+//
 // FP8 e4m3 caches: codes are converted to f16 in registers (exact), Q is
 // converted once per segment to f16 after a power-of-two rescale so its
 // largest magnitude lies in [2^14, 2^15), and k_scale, v_scale and the rescale
@@ -140,7 +151,9 @@ __device__ __forceinline__ int acc_dim(int mt, int g, int hi) {
 
 constexpr unsigned kFlagStart = 1, kFlagEnd = 2, kFlagPool = 4;
 
-template <int CT, int QT, int D, int NT, int WARPS, int STAGES>
+constexpr float kMaskedFloor = -1e30f;  // running-max start of chunked columns
+
+template <int CT, int QT, int D, int NT, int WARPS, int STAGES, bool MQ>
 __global__ void __launch_bounds__(WARPS * 32, 2)
     paged_decode_kernel(const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV, const DecodeArgs a) {
@@ -188,7 +201,7 @@ __global__ void __launch_bounds__(WARPS * 32, 2)
     int run = 0;
     for (int b0 = 0; b0 < a.B; b0 += 32) {
       const int b = b0 + lane;
-      int x = (b < a.B) ? tiles_of(s_len[b], a.window) : 0;
+      int x = (b < a.B) ? tiles_of(s_len[b], a.span) : 0;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const int y = __shfl_up_sync(FULL, x, o);
@@ -216,9 +229,9 @@ __global__ void __launch_bounds__(WARPS * 32, 2)
     if (lane == 0) s_last_long = last;
   }
   __syncthreads();
-  const int total = a.Hkv * s_pref[a.B];
+  const int total = a.Hv * s_pref[a.B];
   const int nw = gridDim.x * WARPS;
-  const long long short_tail = total - static_cast<long long>(a.Hkv) * s_pref[s_last_long + 1];
+  const long long short_tail = total - static_cast<long long>(a.Hv) * s_pref[s_last_long + 1];
   long long pool_want = static_cast<long long>(total) * a.pool_permille / 1000;
   if (pool_want > short_tail) pool_want = short_tail;
   int ws = static_cast<int>((total - pool_want) / nw);
@@ -242,8 +255,8 @@ __global__ void __launch_bounds__(WARPS * 32, 2)
         const int b = b0 + lane;
         int x = 0;
         if (b < a.B)
-          x = merge_extra_units(s_pref[b + 1] - s_pref[b], a.Hkv * s_pref[b],
-                                a.Hkv * s_pref[b + 1], ws, ts, piece, a.Hq);
+          x = merge_extra_units(s_pref[b + 1] - s_pref[b], a.Hv * s_pref[b],
+                                a.Hv * s_pref[b + 1], ws, ts, piece, a.Hv * a.CG);
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
           const int y = __shfl_up_sync(FULL, x, o);
@@ -263,7 +276,7 @@ __global__ void __launch_bounds__(WARPS * 32, 2)
   const uint32_t wbars = bars + warp * STAGES * 8;
   int* meta_f = s_meta + warp * 2 * STAGES;
   int* meta_fl = meta_f + STAGES;
-  const int npairs = a.B * a.Hkv;
+  const int npairs = a.B * a.Hv;
 
   // ---------------------------------------------------------------- producer
   // Runs: the static range [f0, f1), then pool pieces. np = next flat tile to
@@ -312,10 +325,10 @@ __global__ void __launch_bounds__(WARPS * 32, 2)
     unsigned flags = (phase == 1) ? kFlagPool : 0u;
     if (run_first) {
       flags |= kFlagStart;
-      cursor_locate(pc, f, s_pref, a.B, a.Hkv);
+      cursor_locate(pc, f, s_pref, a.B, a.Hv);
       run_first = false;
     } else {
-      cursor_next(pc, s_pref, a.B, a.Hkv);
+      cursor_next(pc, s_pref, a.B, a.Hv);
     }
     if (np == run_end) {
       flags |= kFlagEnd;
@@ -323,7 +336,7 @@ __global__ void __launch_bounds__(WARPS * 32, 2)
       if (phase == 0 && pool_tiles > 0 && !claim_issued) issue_claim();
     }
     const int L = s_len[pc.b];
-    const int pt = win_start(L, a.window) / kTile + pc.t;  // tile index in position space
+    const int pt = win_start(L, a.span) / kTile + pc.t;  // tile index in position space
     const int lb = (pt * kTile) / a.bs;
     if (pc.b != id_b || lb < id_lb0 || lb >= id_lb0 + 32) {
       if (pc.b == pf_b && lb >= pf_lb0 && lb < pf_lb0 + 32) {
@@ -347,7 +360,8 @@ __global__ void __launch_bounds__(WARPS * 32, 2)
       if (lane == 0) atomicOr(a.err, kErrBlockId);
       phys = 0;
     }
-    const int row = (phys * a.Hkv + pc.kvh) * a.bs + (pt * kTile) % a.bs;
+    const int kvh = MQ ? pc.kvh / a.NCG : pc.kvh;
+    const int row = (phys * a.Hkv + kvh) * a.bs + (pt * kTile) % a.bs;
     if (lane == 0) {
       meta_f[slot] = f;
       meta_fl[slot] = static_cast<int>(flags) | ((phase == 1 ? run_id : 0) << 3);
@@ -372,6 +386,8 @@ __global__ void __launch_bounds__(WARPS * 32, 2)
   // ---------------------------------------------------------------- consumer
   uint32_t qf[MT][NT][2];
   float m_run[NT][2], l_run[NT][2];
+  int qlo[NT][2], qhi[NT][2];  // chunked: attended positions [lo, hi] per score column
+  int lo_max = 0, hi_min = 0;  // chunked: tiles inside [lo_max, hi_min] need no column mask
   float acc[MT][NT][4];
   float sc = a.score_scale;
   bool ok = true;
@@ -385,23 +401,56 @@ __global__ void __launch_bounds__(WARPS * 32, 2)
     const int mf = meta_fl[slot];
     const unsigned flags = static_cast<unsigned>(mf) & 7u;
     const int piece_id = mf >> 3;
-    if (flags & kFlagStart) cursor_locate(cc, f, s_pref, a.B, a.Hkv);
-    else cursor_next(cc, s_pref, a.B, a.Hkv);
+    if (flags & kFlagStart) cursor_locate(cc, f, s_pref, a.B, a.Hv);
+    else cursor_next(cc, s_pref, a.B, a.Hv);
     const bool seg_start = (flags & kFlagStart) || (cc.t == 0);
     if (seg_start) {
-      // query fragments of this pair's G heads (B operand, k = head dim)
-      const uint16_t* qg = reinterpret_cast<const uint16_t*>(a.q) +
-                           (static_cast<size_t>(cc.b) * a.Hq + cc.kvh * a.G) * D;
+      // Query fragments of this pair's columns (B operand, k = head dim).
+      // Column c is q head kvh * G + c (T = 1), or, chunked, column
+      // gc = group * CG + c of the kv head's T * G (query, head) columns.
+      const uint16_t* q0 = reinterpret_cast<const uint16_t*>(a.q);
+      const int kvh = MQ ? cc.kvh / a.NCG : cc.kvh;
+      const int grp = MQ ? cc.kvh - kvh * a.NCG : 0;
+      auto qrow = [&](int c) -> const uint16_t* {
+        if (c >= a.CG) return nullptr;
+        if constexpr (!MQ) {
+          return q0 + (static_cast<size_t>(cc.b) * a.Hq + kvh * a.G + c) * D;
+        } else {
+          const int gc = grp * a.CG + c;
+          if (gc >= a.T * a.G) return nullptr;
+          const int t = gc / a.G;
+          return q0 + ((static_cast<size_t>(cc.b) * a.T + t) * a.Hq + kvh * a.G + (gc - t * a.G)) * D;
+        }
+      };
+      if constexpr (MQ) {
+        const int L = s_len[cc.b];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int c = 8 * nt + 2 * t4 + e;
+            const int gc = grp * a.CG + c;
+            if (c < a.CG && gc < a.T * a.G) {
+              const int p = L - a.T + gc / a.G;  // this query's position
+              qhi[nt][e] = p;
+              qlo[nt][e] = (a.window > 0 && p + 1 > a.window) ? p + 1 - a.window : 0;
+            } else {
+              qhi[nt][e] = -1;
+              qlo[nt][e] = 0x7fffffff;  // padding column: every score masked
+            }
+          }
+        lo_max = win_start(L, a.window);  // range start of the last query
+        hi_min = L - a.T;                 // position of the first query
+      }
       sc = a.score_scale;
       if constexpr (!kFp8) {
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
-          const int h = 8 * nt + g;
-          const uint32_t* qh = reinterpret_cast<const uint32_t*>(qg + h * D);
+          const uint32_t* qh = reinterpret_cast<const uint32_t*>(qrow(8 * nt + g));
 #pragma unroll
           for (int ks = 0; ks < MT; ++ks) {
-            qf[ks][nt][0] = (h < a.G) ? qh[(16 * ks + 2 * t4) >> 1] : 0u;
-            qf[ks][nt][1] = (h < a.G) ? qh[(16 * ks + 8 + 2 * t4) >> 1] : 0u;
+            qf[ks][nt][0] = qh ? qh[(16 * ks + 2 * t4) >> 1] : 0u;
+            qf[ks][nt][1] = qh ? qh[(16 * ks + 8 + 2 * t4) >> 1] : 0u;
           }
         }
       } else {
@@ -410,12 +459,12 @@ __global__ void __launch_bounds__(WARPS * 32, 2)
         float amax = 0.f;
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
-          const int h = 8 * nt + g;
+          const uint16_t* qh = qrow(8 * nt + g);
 #pragma unroll
           for (int ks = 0; ks < MT; ++ks) {
             const int d = 64 * (ks >> 2) + 16 * t4 + 4 * (ks & 3);
             uint2 raw2 = make_uint2(0u, 0u);
-            if (h < a.G) raw2 = *reinterpret_cast<const uint2*>(qg + h * D + d);
+            if (qh) raw2 = *reinterpret_cast<const uint2*>(qh + d);
             qv[ks][nt][0] = to_float<QT>(static_cast<uint16_t>(raw2.x & 0xffffu));
             qv[ks][nt][1] = to_float<QT>(static_cast<uint16_t>(raw2.x >> 16));
             qv[ks][nt][2] = to_float<QT>(static_cast<uint16_t>(raw2.y & 0xffffu));
@@ -443,7 +492,7 @@ __global__ void __launch_bounds__(WARPS * 32, 2)
       }
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
-        m_run[nt][0] = m_run[nt][1] = -INFINITY;
+        m_run[nt][0] = m_run[nt][1] = MQ ? kMaskedFloor : -INFINITY;
         l_run[nt][0] = l_run[nt][1] = 0.f;
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt)
@@ -462,9 +511,9 @@ __global__ void __launch_bounds__(WARPS * 32, 2)
 
     // tile position and edge masks
     const int L = s_len[cc.b];
-    const int st = win_start(L, a.window);
+    const int st = win_start(L, a.span);
     const int p0 = (st / kTile + cc.t) * kTile;
-    const bool edge = (p0 < st) || (p0 + kTile > L);
+    const bool edge = (p0 < st) || (p0 + kTile > L);  // outside the pair's union range
     auto valid = [&](int r) { return !edge || (p0 + r >= st && p0 + r < L); };
 
     // ---- S^T = K . Q^T
@@ -505,13 +554,24 @@ __global__ void __launch_bounds__(WARPS * 32, 2)
 
     // ---- online softmax (log2 domain), P^T fragments
     const bool vlo = valid(g), vhi = valid(g + 8);
+    // chunked: does some column's own range cut this tile?
+    const bool cedge = MQ && (p0 < lo_max || p0 + kTile - 1 > hi_min);
     uint32_t pb[NT][2];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-      const float s0 = vlo ? sacc[nt][0] * sc : -INFINITY;
-      const float s1 = vlo ? sacc[nt][1] * sc : -INFINITY;
-      const float s2 = vhi ? sacc[nt][2] * sc : -INFINITY;
-      const float s3 = vhi ? sacc[nt][3] * sc : -INFINITY;
+      float s0, s1, s2, s3;
+      if (MQ && cedge) {
+        const int r0 = p0 + g, r1 = p0 + g + 8;
+        s0 = (r0 >= qlo[nt][0] && r0 <= qhi[nt][0]) ? sacc[nt][0] * sc : -INFINITY;
+        s1 = (r0 >= qlo[nt][1] && r0 <= qhi[nt][1]) ? sacc[nt][1] * sc : -INFINITY;
+        s2 = (r1 >= qlo[nt][0] && r1 <= qhi[nt][0]) ? sacc[nt][2] * sc : -INFINITY;
+        s3 = (r1 >= qlo[nt][1] && r1 <= qhi[nt][1]) ? sacc[nt][3] * sc : -INFINITY;
+      } else {
+        s0 = vlo ? sacc[nt][0] * sc : -INFINITY;
+        s1 = vlo ? sacc[nt][1] * sc : -INFINITY;
+        s2 = vhi ? sacc[nt][2] * sc : -INFINITY;
+        s3 = vhi ? sacc[nt][3] * sc : -INFINITY;
+      }
       float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
 #pragma unroll
       for (int o = 4; o < 32; o <<= 1) {
@@ -593,11 +653,11 @@ __global__ void __launch_bounds__(WARPS * 32, 2)
     // ---- segment end: write the partial (m, l, unnormalised output)
     const bool seg_end = (flags & kFlagEnd) || (cc.t == cc.nt - 1);
     if (seg_end) {
-      const int pair = cc.b * a.Hkv + cc.kvh;
+      const int pair = cc.b * a.Hv + cc.kvh;
       const size_t pslot = (flags & kFlagPool)
                                ? static_cast<size_t>(npairs) + nw + pair + piece_id
                                : static_cast<size_t>(pair) + w;
-      float* P = a.part + pslot * part_stride(a.G, D);
+      float* P = a.part + pslot * part_stride(a.CG, D);
       const float vs = kFp8 ? a.v_scale : 1.f;
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
@@ -608,7 +668,7 @@ __global__ void __launch_bounds__(WARPS * 32, 2)
           l += __shfl_xor_sync(FULL, l, 8);
           l += __shfl_xor_sync(FULL, l, 16);
           const int h = 8 * nt + 2 * t4 + e;
-          if (h < a.G) {
+          if (h < a.CG) {
             float* Ph = P + h * D;
 #pragma unroll
             for (int mt = 0; mt < MT; ++mt) {
@@ -616,8 +676,8 @@ __global__ void __launch_bounds__(WARPS * 32, 2)
               Ph[acc_dim<kFp8>(mt, g, 1)] = acc[mt][nt][2 + e] * vs;
             }
             if (g == 0) {
-              P[a.G * D + h] = m_run[nt][e];
-              P[a.G * D + a.G + h] = l;
+              P[a.CG * D + h] = m_run[nt][e];
+              P[a.CG * D + a.CG + h] = l;
             }
           }
         }
@@ -636,11 +696,11 @@ __global__ void __launch_bounds__(WARPS * 32, 2)
 
 // ---------------------------------------------------------------- host side
 
-template <int CT, int QT, int D, int NT, int WARPS, int STAGES>
+template <int CT, int QT, int D, int NT, int WARPS, int STAGES, bool MQ>
 struct DecodeKernel {
   using Gm = Geometry<CT, D, STAGES>;
   static void* fn() {
-    return reinterpret_cast<void*>(&paged_decode_kernel<CT, QT, D, NT, WARPS, STAGES>);
+    return reinterpret_cast<void*>(&paged_decode_kernel<CT, QT, D, NT, WARPS, STAGES, MQ>);
   }
   static DecodeVariant variant() { return DecodeVariant{WARPS, STAGES, WARPS * Gm::RING_BYTES}; }
   static cudaError_t prepare(int smem, int* ctas_per_sm) {
@@ -661,7 +721,8 @@ struct DecodeKernel {
     attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, paged_decode_kernel<CT, QT, D, NT, WARPS, STAGES>, tk, tv, a);
+    return cudaLaunchKernelEx(&cfg, paged_decode_kernel<CT, QT, D, NT, WARPS, STAGES, MQ>, tk,
+                              tv, a);
   }
 };
 
@@ -684,37 +745,56 @@ constexpr int stages_for() {
 }
 
 // Expands `BODY` with the kernel type K for a runtime (D, NT) pair.
-#define PA_DECODE_DISPATCH(CT, QT, D_, NT_, BODY)                                \
+#define PA_DECODE_DISPATCH(CT, QT, MQ, D_, NT_, BODY)                             \
   do {                                                                            \
     if ((D_) == 64 && (NT_) == 1 && (CT) != kE4M3) {                              \
       constexpr int D0 = (CT) != kE4M3 ? 64 : 128;                                \
       using K = DecodeKernel<CT, QT, D0, 1, warps_for<CT, D0, 1>(),               \
-                             stages_for<CT, D0, 1>()>;                            \
+                             stages_for<CT, D0, 1>(), MQ>;                        \
       BODY;                                                                       \
     } else if ((D_) == 64 && (NT_) == 2 && (CT) != kE4M3) {                       \
       constexpr int D0 = (CT) != kE4M3 ? 64 : 128;                                \
       using K = DecodeKernel<CT, QT, D0, 2, warps_for<CT, D0, 2>(),               \
-                             stages_for<CT, D0, 2>()>;                            \
+                             stages_for<CT, D0, 2>(), MQ>;                        \
       BODY;                                                                       \
     } else if ((D_) == 128 && (NT_) == 1) {                                       \
       using K = DecodeKernel<CT, QT, 128, 1, warps_for<CT, 128, 1>(),            \
-                             stages_for<CT, 128, 1>()>;                          \
+                             stages_for<CT, 128, 1>(), MQ>;                      \
       BODY;                                                                       \
     } else if ((D_) == 128 && (NT_) == 2) {                                       \
       using K = DecodeKernel<CT, QT, 128, 2, warps_for<CT, 128, 2>(),            \
-                             stages_for<CT, 128, 2>()>;                          \
+                             stages_for<CT, 128, 2>(), MQ>;                      \
       BODY;                                                                       \
     } else if ((D_) == 256 && (NT_) == 1) {                                       \
       using K = DecodeKernel<CT, QT, 256, 1, warps_for<CT, 256, 1>(),            \
-                             stages_for<CT, 256, 1>()>;                          \
+                             stages_for<CT, 256, 1>(), MQ>;                      \
       BODY;                                                                       \
     } else if ((D_) == 256 && (NT_) == 2) {                                       \
       using K = DecodeKernel<CT, QT, 256, 2, warps_for<CT, 256, 2>(),            \
-                             stages_for<CT, 256, 2>()>;                          \
+                             stages_for<CT, 256, 2>(), MQ>;                      \
       BODY;                                                                       \
     } else {                                                                      \
       return cudaErrorInvalidValue;                                               \
     }                                                                             \
   } while (0)
+
+// The three entry points of one (cache type, q type, chunked) family; each
+// translation unit defines one or two families so that they build in parallel.
+#define PA_DECODE_FAMILY(NAME, CT, QT, MQ)                                             \
+  cudaError_t decode_variant_##NAME(int D, int nt, DecodeVariant* v) {                  \
+    PA_DECODE_DISPATCH(CT, QT, MQ, D, nt, {                                            \
+      *v = K::variant();                                                               \
+      return cudaSuccess;                                                              \
+    });                                                                                \
+  }                                                                                    \
+  cudaError_t decode_prepare_##NAME(int D, int nt, int smem, int* ctas_per_sm) {        \
+    PA_DECODE_DISPATCH(CT, QT, MQ, D, nt, { return K::prepare(smem, ctas_per_sm); });  \
+  }                                                                                    \
+  cudaError_t decode_launch_##NAME(int D, int nt, const CUtensorMap& tk,                \
+                                   const CUtensorMap& tv, const DecodeArgs& a, int grid, \
+                                   int smem, cudaStream_t s, bool pdl) {               \
+    PA_DECODE_DISPATCH(CT, QT, MQ, D, nt,                                              \
+                       { return K::launch(tk, tv, a, grid, smem, s, pdl); });          \
+  }
 
 }  // namespace pa

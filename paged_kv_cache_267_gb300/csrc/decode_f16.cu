@@ -3,18 +3,6 @@
 
 namespace pa {
 
-cudaError_t decode_variant_f16(int D, int nt, DecodeVariant* v) {
-  PA_DECODE_DISPATCH(kF16, kF16, D, nt, { *v = K::variant(); return cudaSuccess; });
-}
-
-cudaError_t decode_prepare_f16(int D, int nt, int smem, int* ctas_per_sm) {
-  PA_DECODE_DISPATCH(kF16, kF16, D, nt, { return K::prepare(smem, ctas_per_sm); });
-}
-
-cudaError_t decode_launch_f16(int D, int nt, const CUtensorMap& tk, const CUtensorMap& tv,
-                              const DecodeArgs& a, int grid, int smem, cudaStream_t s,
-                              bool pdl) {
-  PA_DECODE_DISPATCH(kF16, kF16, D, nt, { return K::launch(tk, tv, a, grid, smem, s, pdl); });
-}
+PA_DECODE_FAMILY(f16, kF16, kF16, false)
 
 }  // namespace pa

@@ -22,9 +22,13 @@ cudaError_t device_error_word(int32_t** ptr) {
 // the static slots s + w of the warps w whose static range meets
 // [F, min(F + nt, Ts)), then the pool slots S + NW + s + i of the pieces i
 // that meet [max(F, Ts), F + nt). With partial maxima m_p (log2 domain), sums
-// l_p and unnormalised outputs o_p the result for a q head is
-//   out = sum_p 2^(m_p - M) o_p / sum_p 2^(m_p - M) l_p,  M = max_p m_p.
-// Work units are (group g of candidates, q head of pair s), one warp each,
+// l_p and unnormalised outputs o_p the result for an output column is
+//   out = sum_p 2^(m_p - M) o_p / sum_p 2^(m_p - M) l_p,  M = max_p m_p,
+// and zero when the denominator is zero (a chunked query placed before the
+// start of its sequence attends to nothing). A column is a q head of the pair
+// (single-query decode) or a (query, q head) of a chunk; columns that pad the
+// last group of a chunk have no output row and are skipped.
+// Work units are (group g of candidates, column of pair s), one warp each,
 // spread over a persistent grid of many warps per SM so that the L2 latency
 // of one unit hides behind the others. A unit folds its candidates in online
 // (four loads in flight per lane). A head whose candidates fit one group is
@@ -50,8 +54,8 @@ __device__ __forceinline__ void merge_fold(const MergeArgs& a, SlotFn slot_of, i
                                            int step, int h, HeadAcc<VPL>& r) {
   constexpr int U = 4 / VPL;
   const int lane = threadIdx.x & 31;
-  const int GD = a.G * a.D;
-  const size_t stride = static_cast<size_t>(part_stride(a.G, a.D));
+  const int GD = a.CG * a.D;
+  const size_t stride = static_cast<size_t>(part_stride(a.CG, a.D));
   r.M = -INFINITY;
   r.den = 0.f;
 #pragma unroll
@@ -70,7 +74,7 @@ __device__ __forceinline__ void merge_fold(const MergeArgs& a, SlotFn slot_of, i
       if (kk < k1) {
         const float* P = a.part + static_cast<size_t>(slot_of(kk)) * stride;
         mm[j] = P[GD + h];
-        ll[j] = P[GD + a.G + h];
+        ll[j] = P[GD + a.CG + h];
         if (on) {
 #pragma unroll
           for (int v = 0; v < VPL; ++v)
@@ -116,7 +120,7 @@ __device__ __forceinline__ void store_head(const MergeArgs& a, size_t orow, cons
                                            bool zero) {
   const int lane = threadIdx.x & 31;
   if (4 * lane >= a.D) return;
-  const float inv = zero ? 0.f : 1.f / r.den;
+  const float inv = (zero || !(r.den > 0.f)) ? 0.f : 1.f / r.den;
   const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
   for (int v = 0; v < VPL; ++v)
@@ -142,8 +146,8 @@ __device__ __forceinline__ Cands pair_cands(int F, int nt, int ws, int ts, int p
   return c;
 }
 
-// Units: first group 0 of every q head (B * Hq of them), then groups 1.. of the
-// heads of sequences whose candidate bound needs more than one group; the
+// Units: first group 0 of every column (B * Hv * CG of them), then groups 1..
+// of the columns of sequences whose candidate bound needs more than one group; the
 // latter are enumerated through a prefix over sequences (written by the
 // decode kernel), and a unit whose group turns out empty is skipped.
 template <int OT, int VPL>
@@ -160,15 +164,16 @@ __global__ void __launch_bounds__(kMergeThreads, 4) merge_kernel(const MergeArgs
     s_extra[i] = a.ctrl[5 + a.B + i];
   }
   __syncthreads();
-  const int S = a.B * a.Hkv, GD = a.G * a.D;
-  const int heads = a.B * a.Hq;
+  const int S = a.B * a.Hv, GD = a.CG * a.D;
+  const int HC = a.Hv * a.CG;  // columns per sequence
+  const int heads = a.B * HC;
   const int units = heads + s_extra[a.B];
   const int nwarps = gridDim.x * kMergeWarps;
   for (int u = blockIdx.x * kMergeWarps + (tid >> 5); u < units; u += nwarps) {
-    int b, hq, g;
+    int b, col, g;
     if (u < heads) {
-      b = u / a.Hq;
-      hq = u - b * a.Hq;
+      b = u / HC;
+      col = u - b * HC;
       g = 0;
     } else {
       const int e = u - heads;
@@ -179,20 +184,25 @@ __global__ void __launch_bounds__(kMergeThreads, 4) merge_kernel(const MergeArgs
       }
       b = lo;
       const int rem = e - s_extra[b];
-      g = 1 + rem / a.Hq;
-      hq = rem - (g - 1) * a.Hq;
+      g = 1 + rem / HC;
+      col = rem - (g - 1) * HC;
     }
-    const int kvh = hq / a.G, h = hq - kvh * a.G;
-    const int s = b * a.Hkv + kvh;
-    const int hr = b * a.Hq + hq;
+    const int vh = col / a.CG, h = col - vh * a.CG;  // pair and column within it
+    const int kvh = vh / a.NCG;
+    const int gc = (vh - kvh * a.NCG) * a.CG + h;    // column among the kv head's T * G
+    if (gc >= a.T * a.G) continue;                    // padding column
+    const int tq = gc / a.G;
+    const int s = b * a.Hv + vh;
+    const int hr = b * HC + col;
     const int nt = s_pref[b + 1] - s_pref[b];
-    const int F = a.Hkv * s_pref[b] + kvh * nt;
+    const int F = a.Hv * s_pref[b] + vh * nt;
     const Cands cd = pair_cands(F, nt, ws, ts, piece);
     const int ncand = cd.na + cd.np;
     const int gsz = merge_group_size(ncand);
     const int ngroups = ncand > 0 ? (ncand + gsz - 1) / gsz : 1;
     if (g >= ngroups) continue;
-    const size_t orow = static_cast<size_t>(hr) * a.D;
+    const size_t orow =
+        ((static_cast<size_t>(b) * a.T + tq) * a.Hq + kvh * a.G + (gc - tq * a.G)) * a.D;
     HeadAcc<VPL> r;
     r.M = -INFINITY;
     r.den = 1.f;
@@ -213,7 +223,7 @@ __global__ void __launch_bounds__(kMergeThreads, 4) merge_kernel(const MergeArgs
     }
     // group result, in place in the slot of the group's first candidate
     {
-      float* P = a.part + static_cast<size_t>(slot_of(k0)) * part_stride(a.G, a.D);
+      float* P = a.part + static_cast<size_t>(slot_of(k0)) * part_stride(a.CG, a.D);
       if (4 * lane < a.D) {
 #pragma unroll
         for (int v = 0; v < VPL; ++v)
@@ -221,7 +231,7 @@ __global__ void __launch_bounds__(kMergeThreads, 4) merge_kernel(const MergeArgs
       }
       if (lane == 0) {
         P[GD + h] = r.M;
-        P[GD + a.G + h] = r.den;
+        P[GD + a.CG + h] = r.den;
       }
     }
     __threadfence();

@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstdarg>
@@ -37,6 +38,7 @@ constexpr int kPiecesPerWorker = 4;        // pool pieces per worker warp, at mo
 constexpr int kMaxCtasPerSm = 2;
 constexpr int kWarpsPerCta = 8;  // most worker warps of any decode variant
 constexpr int64_t kMaxBatch = 4096;
+constexpr int64_t kMaxChunk = 4096;        // query tokens per sequence in a chunk call
 
 pa_status fail(pa_status code, const char* fmt, ...) {
   char buf[512];
@@ -125,7 +127,7 @@ struct DeviceState {
   int32_t* err_word = nullptr;
   Workspace user_ws;                        // caller-owned (pa_set_workspace)
   std::map<uintptr_t, Workspace> lib_ws;    // library-owned, one per stream
-  std::map<std::tuple<int, int, int, int, int>, int> occupancy;
+  std::map<std::tuple<int, int, int, int, int, bool>, int> occupancy;
 };
 
 std::mutex g_mu;
@@ -155,8 +157,9 @@ struct WsLayout {
   size_t pool, counters, ctrl, part, total;
 };
 
-WsLayout ws_layout(int64_t B, int Hkv, int G, int D, int64_t workers) {
-  const size_t S = static_cast<size_t>(B) * Hkv;
+// Hv pairs per sequence with CG columns each (Hkv and G for single-query decode).
+WsLayout ws_layout(int64_t B, int Hv, int CG, int D, int64_t workers) {
+  const size_t S = static_cast<size_t>(B) * Hv;
   const size_t nslot = 2 * S + workers + static_cast<size_t>(workers) * kPiecesPerWorker;
   WsLayout L;
   size_t o = 0;
@@ -165,7 +168,7 @@ WsLayout ws_layout(int64_t B, int Hkv, int G, int D, int64_t workers) {
   L.pool = o;      o += 256;
   L.counters = o;  o += static_cast<size_t>(pa::kMaxMergeCounters) * sizeof(uint32_t);
   L.ctrl = o;  o += round_up(static_cast<size_t>(2 * B + 6) * sizeof(int32_t), 256);
-  L.part = o;  o += nslot * static_cast<size_t>(pa::part_stride(G, D)) * sizeof(float);
+  L.part = o;  o += nslot * static_cast<size_t>(pa::part_stride(CG, D)) * sizeof(float);
   L.total = o;
   return L;
 }
@@ -215,27 +218,30 @@ pa_status make_cache_map(CUtensorMap* map, const void* base, int64_t rows, int D
 
 // ------------------------------------------------------------ dispatch glue
 
-cudaError_t variant_of(int ct, int qt, int D, int nt, pa::DecodeVariant* v) {
-  if (ct == pa::kE4M3) return pa::decode_variant_fp8(qt, D, nt, v);
-  if (ct == pa::kBF16) return pa::decode_variant_bf16(D, nt, v);
-  return pa::decode_variant_f16(D, nt, v);
-}
+// The kernel family of a (cache type, q type, chunked) combination.
+struct Family {
+  cudaError_t (*variant)(int D, int nt, pa::DecodeVariant* v);
+  cudaError_t (*prepare)(int D, int nt, int smem, int* ctas_per_sm);
+  cudaError_t (*launch)(int D, int nt, const CUtensorMap& tk, const CUtensorMap& tv,
+                        const pa::DecodeArgs& a, int grid, int smem, cudaStream_t s, bool pdl);
+};
 
-cudaError_t prepare_of(int ct, int qt, int D, int nt, int smem, int* ctas) {
-  if (ct == pa::kE4M3) return pa::decode_prepare_fp8(qt, D, nt, smem, ctas);
-  if (ct == pa::kBF16) return pa::decode_prepare_bf16(D, nt, smem, ctas);
-  return pa::decode_prepare_f16(D, nt, smem, ctas);
-}
+#define PA_FAMILY(NAME) \
+  Family { pa::decode_variant_##NAME, pa::decode_prepare_##NAME, pa::decode_launch_##NAME }
 
-cudaError_t launch_of(int ct, int qt, int D, int nt, const CUtensorMap& tk, const CUtensorMap& tv,
-                      const pa::DecodeArgs& a, int grid, int smem, cudaStream_t s, bool pdl) {
-  if (ct == pa::kE4M3) return pa::decode_launch_fp8(qt, D, nt, tk, tv, a, grid, smem, s, pdl);
-  if (ct == pa::kBF16) return pa::decode_launch_bf16(D, nt, tk, tv, a, grid, smem, s, pdl);
-  return pa::decode_launch_f16(D, nt, tk, tv, a, grid, smem, s, pdl);
+Family family_of(int ct, int qt, bool mq) {
+  if (ct == pa::kE4M3) {
+    if (qt == pa::kBF16) return mq ? PA_FAMILY(mq_fp8_bf16) : PA_FAMILY(fp8_bf16);
+    return mq ? PA_FAMILY(mq_fp8_f16) : PA_FAMILY(fp8_f16);
+  }
+  if (ct == pa::kBF16) return mq ? PA_FAMILY(mq_bf16) : PA_FAMILY(bf16);
+  return mq ? PA_FAMILY(mq_f16) : PA_FAMILY(f16);
 }
+#undef PA_FAMILY
 
 struct DecodePlan {
-  int ct, qt, nt, G;
+  Family fam;
+  int nt;
   int smem, grid, workers, min_tiles, pool_permille, piece;
   pa::DecodeVariant var;
 };
@@ -249,28 +255,32 @@ pa_status check_heads(int64_t Hq, int64_t Hkv, int64_t D) {
   return PA_OK;
 }
 
-pa_status plan_decode(DeviceState* st, int dev, int ct, int qt, int64_t B, int Hq, int Hkv,
-                      int D, DecodePlan* p) {
-  p->ct = ct;
-  p->qt = qt;
-  p->G = Hq / Hkv;
-  p->nt = p->G > 8 ? 2 : 1;
-  cudaError_t e = variant_of(ct, qt, D, p->nt, &p->var);
+// Columns per pair and column groups for T queries of a G-head group.
+void chunk_columns(int64_t T, int G, int* CG, int* NCG) {
+  const int64_t cols = T * G;
+  *NCG = static_cast<int>((cols + 15) / 16);
+  *CG = *NCG == 1 ? static_cast<int>(cols) : 16;
+}
+
+pa_status plan_decode(DeviceState* st, int ct, int qt, bool mq, int64_t B, int CG, int D,
+                      DecodePlan* p) {
+  p->fam = family_of(ct, qt, mq);
+  p->nt = CG > 8 ? 2 : 1;
+  cudaError_t e = p->fam.variant(D, p->nt, &p->var);
   if (e != cudaSuccess) return fail(PA_ERR_UNSUPPORTED, "no decode kernel for this dtype/head_dim");
   const size_t smem = 1024 + p->var.ring_bytes + p->var.warps * p->var.stages * (8 + 8) +
                       static_cast<size_t>(2 * B + 1) * sizeof(int32_t);
   p->smem = static_cast<int>(round_up(smem, 1024));
-  auto key = std::make_tuple(ct, qt, D, p->nt, p->smem);
+  auto key = std::make_tuple(ct, qt, D, p->nt, p->smem, mq);
   auto it = st->occupancy.find(key);
   int ctas = 0;
   if (it == st->occupancy.end()) {
-    e = prepare_of(ct, qt, D, p->nt, p->smem, &ctas);
+    e = p->fam.prepare(D, p->nt, p->smem, &ctas);
     if (e != cudaSuccess) return cuda_fail(e, "decode kernel setup");
     st->occupancy[key] = ctas;
   } else {
     ctas = it->second;
   }
-  (void)dev;
   if (ctas < 1) return fail(PA_ERR_UNSUPPORTED, "decode kernel does not fit on an SM (smem %d)", p->smem);
   if (ctas > kMaxCtasPerSm) ctas = kMaxCtasPerSm;
   p->grid = st->num_sms * ctas;
@@ -388,9 +398,15 @@ pa_status pa_set_workspace(void* ptr, size_t bytes) {
   return ok();
 }
 
-pa_status pa_decode_workspace_size(int64_t batch, int32_t num_q_heads, int32_t num_kv_heads,
-                                   int32_t head_dim, size_t* bytes) {
+}  // extern "C"
+
+namespace {
+
+pa_status workspace_size(int64_t batch, int64_t num_queries, int32_t num_q_heads,
+                         int32_t num_kv_heads, int32_t head_dim, size_t* bytes) {
   if (!bytes) return fail(PA_ERR_INVALID_ARG, "bytes is null");
+  if (num_queries < 1 || num_queries > kMaxChunk)
+    return fail(PA_ERR_UNSUPPORTED, "num_queries %lld", (long long)num_queries);
   if (batch < 0 || batch > kMaxBatch) return fail(PA_ERR_UNSUPPORTED, "batch %lld", (long long)batch);
   pa_status s = check_heads(num_q_heads, num_kv_heads, head_dim);
   if (s) return s;
@@ -401,8 +417,24 @@ pa_status pa_decode_workspace_size(int64_t batch, int32_t num_q_heads, int32_t n
   int64_t workers = static_cast<int64_t>(st->num_sms) * kMaxCtasPerSm * kWarpsPerCta;
   const int cap = g_tune_max_ctas.load();
   if (cap > 0 && cap * kWarpsPerCta < workers) workers = static_cast<int64_t>(cap) * kWarpsPerCta;
-  *bytes = ws_layout(batch, num_kv_heads, num_q_heads / num_kv_heads, head_dim, workers).total;
+  int CG, NCG;
+  chunk_columns(num_queries, num_q_heads / num_kv_heads, &CG, &NCG);
+  *bytes = ws_layout(batch, num_kv_heads * NCG, CG, head_dim, workers).total;
   return ok();
+}
+
+}  // namespace
+
+extern "C" {
+
+pa_status pa_decode_workspace_size(int64_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+                                   int32_t head_dim, size_t* bytes) {
+  return workspace_size(batch, 1, num_q_heads, num_kv_heads, head_dim, bytes);
+}
+
+pa_status pa_prefill_chunk_workspace_size(int64_t batch, int32_t num_queries, int32_t num_q_heads,
+                                          int32_t num_kv_heads, int32_t head_dim, size_t* bytes) {
+  return workspace_size(batch, num_queries, num_q_heads, num_kv_heads, head_dim, bytes);
 }
 
 pa_status pa_check_device_error(int32_t* bits, pa_stream stream) {
@@ -499,13 +531,31 @@ pa_status pa_reshape_and_cache(const pa_tensor* k, const pa_tensor* v, const pa_
   return ok();
 }
 
-pa_status pa_decode(const pa_tensor* out, const pa_tensor* q, const pa_tensor* key_cache,
-                    const pa_tensor* value_cache, const pa_tensor* block_tables,
-                    const pa_tensor* seq_lens, int32_t num_kv_heads, float scale,
-                    int32_t block_size, int32_t window, int32_t kv_dtype, float k_scale,
-                    float v_scale, pa_stream stream) {
+}  // extern "C"
+
+namespace {
+
+// A validated decode or chunk call.
+struct DecodeCall {
+  const pa_tensor *out, *q, *kc, *vc, *bt, *sl;
+  int64_t B, T, Hq, Hkv, D, NB, MB;
+  int G, CG, NCG, Hv;
+  int32_t bs, window;
+  bool fp8;
+  int ct, qt;
+  float scale, k_scale, v_scale;
+};
+
+// Host validation shared by the decode entry points: q and out are
+// [B, Hq, D] (chunked = false) or [B, T, Hq, D] (chunked = true).
+pa_status check_decode(const pa_tensor* out, const pa_tensor* q, const pa_tensor* key_cache,
+                       const pa_tensor* value_cache, const pa_tensor* block_tables,
+                       const pa_tensor* seq_lens, int32_t num_kv_heads, float scale,
+                       int32_t block_size, int32_t window, int32_t kv_dtype, float k_scale,
+                       float v_scale, bool chunked, DecodeCall* c) {
   pa_status s;
-  if ((s = check_tensor(out, "out", 3)) || (s = check_tensor(q, "q", 3)) ||
+  const int qd = chunked ? 4 : 3;
+  if ((s = check_tensor(out, "out", qd)) || (s = check_tensor(q, "q", qd)) ||
       (s = check_tensor(key_cache, "key_cache", 4)) ||
       (s = check_tensor(value_cache, "value_cache", 4)) ||
       (s = check_tensor(block_tables, "block_tables", 2)) ||
@@ -513,9 +563,13 @@ pa_status pa_decode(const pa_tensor* out, const pa_tensor* q, const pa_tensor* k
     return s;
   if (q->dtype != PA_F16 && q->dtype != PA_BF16) return fail(PA_ERR_UNSUPPORTED, "q must be f16 or bf16");
   if (out->dtype != q->dtype) return fail(PA_ERR_INVALID_ARG, "out dtype must equal q dtype");
-  const int64_t B = q->shape[0], Hq = q->shape[1], D = q->shape[2];
-  for (int i = 0; i < 3; ++i)
+  for (int i = 0; i < qd; ++i)
     if (out->shape[i] != q->shape[i]) return fail(PA_ERR_INVALID_ARG, "out shape != q shape");
+  const int64_t B = q->shape[0], T = chunked ? q->shape[1] : 1;
+  const int64_t Hq = q->shape[qd - 2], D = q->shape[qd - 1];
+  if (chunked && (T < 1 || T > kMaxChunk))
+    return fail(PA_ERR_UNSUPPORTED, "num_queries %lld not in [1, %lld]", (long long)T,
+                (long long)kMaxChunk);
   if (kv_dtype != PA_KV_AUTO && kv_dtype != PA_KV_FP8_E4M3)
     return fail(PA_ERR_INVALID_ARG, "bad kv_dtype %d", kv_dtype);
   const bool fp8 = kv_dtype == PA_KV_FP8_E4M3;
@@ -541,70 +595,86 @@ pa_status pa_decode(const pa_tensor* out, const pa_tensor* q, const pa_tensor* k
   if (B > kMaxBatch) return fail(PA_ERR_UNSUPPORTED, "batch %lld > %lld", (long long)B, (long long)kMaxBatch);
   if (!is_contiguous(out) || !is_contiguous(q) || !is_contiguous(key_cache) ||
       !is_contiguous(value_cache) || !is_contiguous(block_tables) || !is_contiguous(seq_lens))
-    return fail(PA_ERR_LAYOUT, "pa_decode needs contiguous tensors");
+    return fail(PA_ERR_LAYOUT, "decode needs contiguous tensors");
   for (const pa_tensor* x : {key_cache, value_cache, q, out})
     if (reinterpret_cast<uintptr_t>(x->data) % 16)
       return fail(PA_ERR_LAYOUT, "q, out and caches must be 16-byte aligned");
   if (!std::isfinite(scale)) return fail(PA_ERR_INVALID_ARG, "scale must be finite");
   if (fp8 && !(std::isfinite(k_scale) && std::isfinite(v_scale) && k_scale > 0 && v_scale > 0))
     return fail(PA_ERR_INVALID_ARG, "fp8 scales must be finite and positive");
+  const int G = static_cast<int>(Hq / Hkv);
+  int CG, NCG;
+  chunk_columns(T, G, &CG, &NCG);
+  const int64_t Hv = Hkv * NCG;
   // 32-bit index limits inside the kernels
   if (NB * Hkv * block_size >= (int64_t(1) << 31) || MB * block_size >= (int64_t(1) << 31) ||
-      B * Hkv * (MB * block_size / 16 + 1) >= (int64_t(1) << 31) || B * MB >= (int64_t(1) << 31))
+      B * Hv * (MB * block_size / 16 + 1) >= (int64_t(1) << 31) || B * MB >= (int64_t(1) << 31) ||
+      B * T * Hq * D >= (int64_t(1) << 40))
     return fail(PA_ERR_UNSUPPORTED, "pool or tables exceed 32-bit indexing");
   for (const pa_tensor* x : {q, key_cache, value_cache, block_tables, seq_lens})
     if (overlaps(out, x)) return fail(PA_ERR_INVALID_ARG, "out overlaps an input");
-  if (B * Hq > pa::kMaxMergeCounters)
-    return fail(PA_ERR_UNSUPPORTED, "batch * num_q_heads too large");
-  if (B == 0) return ok();
-  if (MB == 0) return fail(PA_ERR_INVALID_ARG, "block_tables has no columns");
-  if (NB == 0) return fail(PA_ERR_INVALID_ARG, "empty block pool");
+  if (B * Hv * CG > pa::kMaxMergeCounters)
+    return fail(PA_ERR_UNSUPPORTED, "batch * num_q_heads * num_queries too large");
+  if (B > 0 && MB == 0) return fail(PA_ERR_INVALID_ARG, "block_tables has no columns");
+  if (B > 0 && NB == 0) return fail(PA_ERR_INVALID_ARG, "empty block pool");
+  *c = DecodeCall{out, q, key_cache, value_cache, block_tables, seq_lens, B, T, Hq, Hkv, D, NB,
+                  MB, G, CG, NCG, static_cast<int>(Hv), block_size, window > 0 ? window : 0,
+                  fp8, fp8 ? pa::kE4M3 : (q->dtype == PA_BF16 ? pa::kBF16 : pa::kF16),
+                  q->dtype, scale, k_scale, v_scale};
+  return PA_OK;
+}
 
-  cudaStream_t cs = static_cast<cudaStream_t>(stream);
-  DeviceState* st;
-  int dev;
-  DecodePlan plan;
-  WsLayout layout;
-  void* ws = nullptr;
-  Workspace* wsp = nullptr;
-  {
-    std::lock_guard<std::mutex> lk(g_mu);
-    if ((s = device_state(&st, &dev))) return s;
-    const int ct = fp8 ? pa::kE4M3 : (q->dtype == PA_BF16 ? pa::kBF16 : pa::kF16);
-    if ((s = plan_decode(st, dev, ct, q->dtype, B, static_cast<int>(Hq), static_cast<int>(Hkv),
-                         static_cast<int>(D), &plan)))
-      return s;
-    layout = ws_layout(B, static_cast<int>(Hkv), plan.G, static_cast<int>(D), plan.workers);
-    if ((s = get_workspace(st, cs, layout, &ws, &wsp))) return s;
-  }
-  const int elt = fp8 ? 1 : 2;
+pa_status plan_call(DeviceState* st, const DecodeCall& c, DecodePlan* plan, WsLayout* layout) {
+  pa_status s = plan_decode(st, c.ct, c.qt, c.T > 1, c.B, c.CG, static_cast<int>(c.D), plan);
+  if (s) return s;
+  *layout = ws_layout(c.B, c.Hv, c.CG, static_cast<int>(c.D), plan->workers);
+  return PA_OK;
+}
+
+// Encodes the cache maps and launches the decode and merge kernels with the
+// scratch at `ws`. `wsp` (if given) is marked dirty when the merge launch
+// fails after the decode kernel ran, so that its pool counter is cleared
+// before the next use.
+pa_status run_decode(const DecodeCall& c, DeviceState* st, const DecodePlan& plan,
+                     const WsLayout& layout, void* ws, Workspace* wsp, cudaStream_t cs) {
+  pa_status s;
+  const int elt = c.fp8 ? 1 : 2;
+  const int D = static_cast<int>(c.D);
   CUtensorMap tk, tv;
-  if ((s = make_cache_map(&tk, key_cache->data, NB * Hkv * block_size, static_cast<int>(D), elt)) ||
-      (s = make_cache_map(&tv, value_cache->data, NB * Hkv * block_size, static_cast<int>(D), elt)))
+  if ((s = make_cache_map(&tk, c.kc->data, c.NB * c.Hkv * c.bs, D, elt)) ||
+      (s = make_cache_map(&tv, c.vc->data, c.NB * c.Hkv * c.bs, D, elt)))
     return s;
 
   const double log2e = 1.4426950408889634;
   pa::DecodeArgs a;
-  a.q = q->data;
-  a.block_tables = static_cast<const int32_t*>(block_tables->data);
-  a.seq_lens = static_cast<const int32_t*>(seq_lens->data);
+  a.q = c.q->data;
+  a.block_tables = static_cast<const int32_t*>(c.bt->data);
+  a.seq_lens = static_cast<const int32_t*>(c.sl->data);
   char* wsb = static_cast<char*>(ws);
   a.ctrl = reinterpret_cast<int32_t*>(wsb + layout.ctrl);
   a.pool = reinterpret_cast<uint32_t*>(wsb + layout.pool);
   a.part = reinterpret_cast<float*>(wsb + layout.part);
   a.err = st->err_word;
-  a.B = static_cast<int>(B);
-  a.Hq = static_cast<int>(Hq);
-  a.Hkv = static_cast<int>(Hkv);
-  a.G = plan.G;
-  a.D = static_cast<int>(D);
-  a.bs = block_size;
-  a.MB = static_cast<int>(MB);
-  a.NB = static_cast<int>(NB);
-  a.window = window > 0 ? window : 0;
-  a.score_scale = static_cast<float>(static_cast<double>(scale) * log2e *
-                                     (fp8 ? static_cast<double>(k_scale) : 1.0));
-  a.v_scale = fp8 ? v_scale : 1.f;
+  a.B = static_cast<int>(c.B);
+  a.Hq = static_cast<int>(c.Hq);
+  a.Hkv = static_cast<int>(c.Hkv);
+  a.G = c.G;
+  a.D = D;
+  a.bs = c.bs;
+  a.MB = static_cast<int>(c.MB);
+  a.NB = static_cast<int>(c.NB);
+  a.window = c.window;
+  a.T = static_cast<int>(c.T);
+  a.NCG = c.NCG;
+  a.CG = c.CG;
+  a.Hv = c.Hv;
+  // a window at least as long as the table covers acts as no window
+  a.span = c.window > 0
+               ? static_cast<int>(std::min<int64_t>(int64_t(c.window) + c.T - 1, c.MB * c.bs))
+               : 0;
+  a.score_scale = static_cast<float>(static_cast<double>(c.scale) * log2e *
+                                     (c.fp8 ? static_cast<double>(c.k_scale) : 1.0));
+  a.v_scale = c.fp8 ? c.v_scale : 1.f;
   a.min_tiles = plan.min_tiles;
   a.pool_permille = plan.pool_permille;
   a.piece_min = plan.piece;
@@ -614,13 +684,12 @@ pa_status pa_decode(const pa_tensor* out, const pa_tensor* q, const pa_tensor* k
   cudaError_t e;
   if (prof && (e = cudaEventRecord(static_cast<cudaEvent_t>(g_prof_before), cs)) != cudaSuccess)
     return cuda_fail(e, "profile event");
-  e = launch_of(plan.ct, plan.qt, static_cast<int>(D), plan.nt, tk, tv, a, plan.grid, plan.smem,
-                cs, !prof);
+  e = plan.fam.launch(D, plan.nt, tk, tv, a, plan.grid, plan.smem, cs, !prof);
   if (e != cudaSuccess) return cuda_fail(e, "decode kernel launch");
   if (prof && (e = cudaEventRecord(static_cast<cudaEvent_t>(g_prof_after), cs)) != cudaSuccess)
     return cuda_fail(e, "profile event");
   pa::MergeArgs m;
-  m.out = out->data;
+  m.out = c.out->data;
   m.part = a.part;
   m.ctrl = a.ctrl;
   m.pool = a.pool;
@@ -631,98 +700,96 @@ pa_status pa_decode(const pa_tensor* out, const pa_tensor* q, const pa_tensor* k
   m.Hkv = a.Hkv;
   m.G = a.G;
   m.D = a.D;
-  e = pa::merge_launch(q->dtype, m, st->num_sms * 4, cs, !prof);
+  m.T = a.T;
+  m.NCG = a.NCG;
+  m.CG = a.CG;
+  m.Hv = a.Hv;
+  e = pa::merge_launch(c.qt, m, st->num_sms * 4, cs, !prof);
   if (e != cudaSuccess) {
-    std::lock_guard<std::mutex> lk(g_mu);
-    wsp->dirty = true;  // the decode kernel ran; its pool counter was not reset
+    if (wsp) {
+      std::lock_guard<std::mutex> lk(g_mu);
+      wsp->dirty = true;  // the decode kernel ran; its pool counter was not reset
+    }
     return cuda_fail(e, "merge kernel launch");
   }
   g_launches += 2;
   return ok();
 }
 
+// Validation, planning and launch with the library's (or the caller's set)
+// workspace.
+pa_status decode_entry(const pa_tensor* out, const pa_tensor* q, const pa_tensor* key_cache,
+                       const pa_tensor* value_cache, const pa_tensor* block_tables,
+                       const pa_tensor* seq_lens, int32_t num_kv_heads, float scale,
+                       int32_t block_size, int32_t window, int32_t kv_dtype, float k_scale,
+                       float v_scale, pa_stream stream, bool chunked) {
+  DecodeCall c;
+  pa_status s = check_decode(out, q, key_cache, value_cache, block_tables, seq_lens,
+                             num_kv_heads, scale, block_size, window, kv_dtype, k_scale, v_scale,
+                             chunked, &c);
+  if (s) return s;
+  if (c.B == 0) return ok();
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  DeviceState* st;
+  DecodePlan plan;
+  WsLayout layout;
+  void* ws = nullptr;
+  Workspace* wsp = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if ((s = device_state(&st, nullptr)) || (s = plan_call(st, c, &plan, &layout)) ||
+        (s = get_workspace(st, cs, layout, &ws, &wsp)))
+      return s;
+  }
+  return run_decode(c, st, plan, layout, ws, wsp, cs);
+}
+
+}  // namespace
+
+extern "C" {
+
+pa_status pa_decode(const pa_tensor* out, const pa_tensor* q, const pa_tensor* key_cache,
+                    const pa_tensor* value_cache, const pa_tensor* block_tables,
+                    const pa_tensor* seq_lens, int32_t num_kv_heads, float scale,
+                    int32_t block_size, int32_t window, int32_t kv_dtype, float k_scale,
+                    float v_scale, pa_stream stream) {
+  return decode_entry(out, q, key_cache, value_cache, block_tables, seq_lens, num_kv_heads, scale,
+                      block_size, window, kv_dtype, k_scale, v_scale, stream, false);
+}
+
+pa_status pa_prefill_chunk(const pa_tensor* out, const pa_tensor* q, const pa_tensor* key_cache,
+                           const pa_tensor* value_cache, const pa_tensor* block_tables,
+                           const pa_tensor* seq_lens, int32_t num_kv_heads, float scale,
+                           int32_t block_size, int32_t window, int32_t kv_dtype, float k_scale,
+                           float v_scale, pa_stream stream) {
+  return decode_entry(out, q, key_cache, value_cache, block_tables, seq_lens, num_kv_heads, scale,
+                      block_size, window, kv_dtype, k_scale, v_scale, stream, true);
+}
+
 }  // extern "C"
 
-
-// pa_decode's validation and launches, with the scratch in a caller-given
-// device buffer of `capacity` bytes instead of a library workspace; used by
-// the allocation-free entry point (decode_noalloc.cu). Allocates nothing.
+// pa_decode with the scratch in a caller-given device buffer of `capacity`
+// bytes instead of a library workspace; used by the allocation-free entry
+// point (decode_noalloc.cu). Allocates nothing.
 namespace pa {
 pa_status decode_in_buffer(const pa_tensor* out, const pa_tensor* q, const pa_tensor* key_cache,
                            const pa_tensor* value_cache, const pa_tensor* block_tables,
                            const pa_tensor* seq_lens, int32_t num_kv_heads, float scale,
                            int32_t block_size, int32_t window, int32_t kv_dtype, float k_scale,
                            float v_scale, pa_stream stream, void* buffer, size_t capacity) {
-  pa_status s;
-  if ((s = check_tensor(out, "out", 3)) || (s = check_tensor(q, "q", 3)) ||
-      (s = check_tensor(key_cache, "key_cache", 4)) ||
-      (s = check_tensor(value_cache, "value_cache", 4)) ||
-      (s = check_tensor(block_tables, "block_tables", 2)) ||
-      (s = check_tensor(seq_lens, "seq_lens", 1)))
-    return s;
-  if (q->dtype != PA_F16 && q->dtype != PA_BF16) return fail(PA_ERR_UNSUPPORTED, "q must be f16 or bf16");
-  if (out->dtype != q->dtype) return fail(PA_ERR_INVALID_ARG, "out dtype must equal q dtype");
-  const int64_t B = q->shape[0], Hq = q->shape[1], D = q->shape[2];
-  for (int i = 0; i < 3; ++i)
-    if (out->shape[i] != q->shape[i]) return fail(PA_ERR_INVALID_ARG, "out shape != q shape");
-  if (kv_dtype != PA_KV_AUTO && kv_dtype != PA_KV_FP8_E4M3)
-    return fail(PA_ERR_INVALID_ARG, "bad kv_dtype %d", kv_dtype);
-  const bool fp8 = kv_dtype == PA_KV_FP8_E4M3;
-  const int32_t cdt = fp8 ? PA_FP8_E4M3 : q->dtype;
-  if (key_cache->dtype != cdt || value_cache->dtype != cdt)
-    return fail(PA_ERR_INVALID_ARG, "cache dtype does not match q dtype / kv_dtype");
-  for (int i = 0; i < 4; ++i)
-    if (key_cache->shape[i] != value_cache->shape[i])
-      return fail(PA_ERR_INVALID_ARG, "key and value cache shapes differ");
-  const int64_t NB = key_cache->shape[0], Hkv = key_cache->shape[1];
-  if (num_kv_heads != Hkv) return fail(PA_ERR_INVALID_ARG, "num_kv_heads != key_cache.shape[1]");
-  if (block_size != key_cache->shape[2]) return fail(PA_ERR_INVALID_ARG, "block_size != key_cache.shape[2]");
-  if (key_cache->shape[3] != D) return fail(PA_ERR_INVALID_ARG, "cache head_dim != q head_dim");
-  if ((s = check_heads(Hq, Hkv, D))) return s;
-  if (fp8 && D == 64) return fail(PA_ERR_UNSUPPORTED, "fp8 caches need head_dim 128 or 256");
-  if (block_size <= 0 || block_size % 16 || block_size > 1024)
-    return fail(PA_ERR_UNSUPPORTED, "block_size must be a multiple of 16 in [16, 1024]");
-  if (block_tables->dtype != PA_I32 || seq_lens->dtype != PA_I32)
-    return fail(PA_ERR_INVALID_ARG, "block_tables and seq_lens must be int32");
-  if (block_tables->shape[0] != B || seq_lens->shape[0] != B)
-    return fail(PA_ERR_INVALID_ARG, "block_tables / seq_lens batch != q batch");
-  const int64_t MB = block_tables->shape[1];
-  if (B > kMaxBatch) return fail(PA_ERR_UNSUPPORTED, "batch %lld > %lld", (long long)B, (long long)kMaxBatch);
-  if (!is_contiguous(out) || !is_contiguous(q) || !is_contiguous(key_cache) ||
-      !is_contiguous(value_cache) || !is_contiguous(block_tables) || !is_contiguous(seq_lens))
-    return fail(PA_ERR_LAYOUT, "pa_decode needs contiguous tensors");
-  for (const pa_tensor* x : {key_cache, value_cache, q, out})
-    if (reinterpret_cast<uintptr_t>(x->data) % 16)
-      return fail(PA_ERR_LAYOUT, "q, out and caches must be 16-byte aligned");
-  if (!std::isfinite(scale)) return fail(PA_ERR_INVALID_ARG, "scale must be finite");
-  if (fp8 && !(std::isfinite(k_scale) && std::isfinite(v_scale) && k_scale > 0 && v_scale > 0))
-    return fail(PA_ERR_INVALID_ARG, "fp8 scales must be finite and positive");
-  // 32-bit index limits inside the kernels
-  if (NB * Hkv * block_size >= (int64_t(1) << 31) || MB * block_size >= (int64_t(1) << 31) ||
-      B * Hkv * (MB * block_size / 16 + 1) >= (int64_t(1) << 31) || B * MB >= (int64_t(1) << 31))
-    return fail(PA_ERR_UNSUPPORTED, "pool or tables exceed 32-bit indexing");
-  for (const pa_tensor* x : {q, key_cache, value_cache, block_tables, seq_lens})
-    if (overlaps(out, x)) return fail(PA_ERR_INVALID_ARG, "out overlaps an input");
-  if (B * Hq > pa::kMaxMergeCounters)
-    return fail(PA_ERR_UNSUPPORTED, "batch * num_q_heads too large");
-  if (B == 0) return ok();
-  if (MB == 0) return fail(PA_ERR_INVALID_ARG, "block_tables has no columns");
-  if (NB == 0) return fail(PA_ERR_INVALID_ARG, "empty block pool");
-
+  DecodeCall c;
+  pa_status s = check_decode(out, q, key_cache, value_cache, block_tables, seq_lens,
+                             num_kv_heads, scale, block_size, window, kv_dtype, k_scale, v_scale,
+                             false, &c);
+  if (s) return s;
+  if (c.B == 0) return ok();
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
   DeviceState* st;
-  int dev;
   DecodePlan plan;
   WsLayout layout;
-  void* ws = buffer;
   {
     std::lock_guard<std::mutex> lk(g_mu);
-    if ((s = device_state(&st, &dev))) return s;
-    const int ct = fp8 ? pa::kE4M3 : (q->dtype == PA_BF16 ? pa::kBF16 : pa::kF16);
-    if ((s = plan_decode(st, dev, ct, q->dtype, B, static_cast<int>(Hq), static_cast<int>(Hkv),
-                         static_cast<int>(D), &plan)))
-      return s;
-    layout = ws_layout(B, static_cast<int>(Hkv), plan.G, static_cast<int>(D), plan.workers);
+    if ((s = device_state(&st, nullptr)) || (s = plan_call(st, c, &plan, &layout))) return s;
   }
   if (layout.total > capacity)
     return fail(PA_ERR_WORKSPACE,
@@ -731,70 +798,11 @@ pa_status decode_in_buffer(const pa_tensor* out, const pa_tensor* q, const pa_te
                 layout.total, capacity);
   // The piece counter and this step's merge counters must start at zero; the
   // buffer keeps whatever the previous call left there.
-  {
-    cudaError_t e0 = cudaMemsetAsync(static_cast<char*>(ws) + layout.pool, 0,
-                                     layout.counters - layout.pool +
-                                         static_cast<size_t>(B * Hq) * sizeof(uint32_t),
-                                     cs);
-    if (e0 != cudaSuccess) return cuda_fail(e0, "clearing the scratch counters");
-  }
-  const int elt = fp8 ? 1 : 2;
-  CUtensorMap tk, tv;
-  if ((s = make_cache_map(&tk, key_cache->data, NB * Hkv * block_size, static_cast<int>(D), elt)) ||
-      (s = make_cache_map(&tv, value_cache->data, NB * Hkv * block_size, static_cast<int>(D), elt)))
-    return s;
-
-  const double log2e = 1.4426950408889634;
-  pa::DecodeArgs a;
-  a.q = q->data;
-  a.block_tables = static_cast<const int32_t*>(block_tables->data);
-  a.seq_lens = static_cast<const int32_t*>(seq_lens->data);
-  char* wsb = static_cast<char*>(ws);
-  a.ctrl = reinterpret_cast<int32_t*>(wsb + layout.ctrl);
-  a.pool = reinterpret_cast<uint32_t*>(wsb + layout.pool);
-  a.part = reinterpret_cast<float*>(wsb + layout.part);
-  a.err = st->err_word;
-  a.B = static_cast<int>(B);
-  a.Hq = static_cast<int>(Hq);
-  a.Hkv = static_cast<int>(Hkv);
-  a.G = plan.G;
-  a.D = static_cast<int>(D);
-  a.bs = block_size;
-  a.MB = static_cast<int>(MB);
-  a.NB = static_cast<int>(NB);
-  a.window = window > 0 ? window : 0;
-  a.score_scale = static_cast<float>(static_cast<double>(scale) * log2e *
-                                     (fp8 ? static_cast<double>(k_scale) : 1.0));
-  a.v_scale = fp8 ? v_scale : 1.f;
-  a.min_tiles = plan.min_tiles;
-  a.pool_permille = plan.pool_permille;
-  a.piece_min = plan.piece;
-  a.np_max = plan.workers * kPiecesPerWorker;
-
-  const bool prof = g_prof_before && g_prof_after;
-  cudaError_t e;
-  if (prof && (e = cudaEventRecord(static_cast<cudaEvent_t>(g_prof_before), cs)) != cudaSuccess)
-    return cuda_fail(e, "profile event");
-  e = launch_of(plan.ct, plan.qt, static_cast<int>(D), plan.nt, tk, tv, a, plan.grid, plan.smem,
-                cs, !prof);
-  if (e != cudaSuccess) return cuda_fail(e, "decode kernel launch");
-  if (prof && (e = cudaEventRecord(static_cast<cudaEvent_t>(g_prof_after), cs)) != cudaSuccess)
-    return cuda_fail(e, "profile event");
-  pa::MergeArgs m;
-  m.out = out->data;
-  m.part = a.part;
-  m.ctrl = a.ctrl;
-  m.pool = a.pool;
-  m.counters = reinterpret_cast<uint32_t*>(wsb + layout.counters);
-  m.NW = plan.workers;
-  m.B = a.B;
-  m.Hq = a.Hq;
-  m.Hkv = a.Hkv;
-  m.G = a.G;
-  m.D = a.D;
-  e = pa::merge_launch(q->dtype, m, st->num_sms * 4, cs, !prof);
-  if (e != cudaSuccess) return cuda_fail(e, "merge kernel launch");
-  g_launches += 2;
-  return ok();
+  cudaError_t e = cudaMemsetAsync(static_cast<char*>(buffer) + layout.pool, 0,
+                                  layout.counters - layout.pool +
+                                      static_cast<size_t>(c.B * c.Hv * c.CG) * sizeof(uint32_t),
+                                  cs);
+  if (e != cudaSuccess) return cuda_fail(e, "clearing the scratch counters");
+  return run_decode(c, st, plan, layout, buffer, nullptr, cs);
 }
 }  // namespace pa

@@ -23,21 +23,22 @@ __host__ __device__ constexpr inline int part_stride(int G, int D) {
 //   pool  u32 at offset 0: pool piece counter; zero between calls (the merge
 //         kernel resets it after each step), at the same place for any shape
 //   cnt   u32 [kMaxMergeCounters] at offset 256: merge group counters (one
-//         per q head), zero
-//         between calls (each is reset by the unit that finds it complete)
+//         per output column), zero between calls (each is reset by the unit
+//         that finds it complete)
 //   ctrl  int32 [2 B + 6]: [0] static tiles per warp (ws), [1] total tiles,
 //         [2] end of the static region (Ts), [3] pool piece size (P),
 //         [4 .. 4 + B] tile prefix over the sequences, [5 + B .. 5 + 2 B]
 //         prefix of the merge's extra group units over the sequences
-//   part  f32 [NSLOT][part_stride(G, D)]: acc[G][D], m[G], l[G], padding to a
-//         multiple of 4 floats so every slot starts 16-byte aligned
-// with S = B * Hkv pairs, NW worker warps, NSLOT = 2 S + NW + NPMAX.
+//   part  f32 [NSLOT][part_stride(CG, D)]: acc[CG][D], m[CG], l[CG], padding
+//         to a multiple of 4 floats so every slot starts 16-byte aligned
+// with S = B * Hv pairs, NW worker warps, NSLOT = 2 S + NW + NPMAX. For
+// single-query decode Hv = Hkv and CG = G (columns are the group's q heads).
 // A segment is a run of one warp's tiles inside one pair. Static segments of
 // pair s by warp w use slot s + w; segments of pool piece i use slot
 // S + NW + s + i. Both are unique because the walk through the (pair, warp)
 // and (pair, piece) grids is a monotone staircase.
 struct DecodeArgs {
-  const void* q;                 // [B, Hq, D]
+  const void* q;                 // [B, T, Hq, D] ([B, Hq, D] when T = 1)
   const int32_t* block_tables;   // [B, MB]
   const int32_t* seq_lens;       // [B]
   int32_t* ctrl;
@@ -45,6 +46,11 @@ struct DecodeArgs {
   float* part;
   int32_t* err;                  // device error word
   int B, Hq, Hkv, G, D, bs, MB, NB, window;
+  int T;                         // queries per sequence, at its last T positions
+  int NCG;                       // column groups per kv head (1 when T * G <= 16)
+  int CG;                        // (query, head) columns per pair: T * G, or 16
+  int Hv;                        // pairs per sequence: Hkv * NCG
+  int span;                      // window of the pairs' tile ranges: W + T - 1, 0 if W = 0
   float score_scale;             // scale * log2(e) (* k_scale for FP8)
   float v_scale;                 // FP8: applied to the partial outputs
   int min_tiles;                 // least tiles per warp in the static split
@@ -54,12 +60,13 @@ struct DecodeArgs {
 };
 
 struct MergeArgs {
-  void* out;                     // [B, Hq, D], dtype of q
+  void* out;                     // [B, T, Hq, D], dtype of q
   float* part;                   // group results are written in place
   const int32_t* ctrl;
   uint32_t* pool;                // reset to zero for the next step
-  uint32_t* counters;            // [B * Hq] groups done per q head; left at zero
+  uint32_t* counters;            // [B * Hv * CG] groups done per column; left at zero
   int B, Hq, Hkv, G, D, NW;
+  int T, NCG, CG, Hv;            // as in DecodeArgs
 };
 
 constexpr int kMergeGroupsMax = 16;   // groups of partials per q head, at most
@@ -72,18 +79,18 @@ __host__ __device__ inline int merge_group_size(int n) {
   return g < kMergeGroupMin ? kMergeGroupMin : g;
 }
 
-// Merge units beyond group 0 for the Hq heads of one sequence whose pairs
-// span flat tiles [lo, hi), nt tiles each: from an upper bound of a pair's
-// candidates (static warps met, plus pool pieces met inside [ts, hi)).
+// Merge units beyond group 0 for the `cols` output columns of one sequence
+// whose pairs span flat tiles [lo, hi), nt tiles each: from an upper bound of
+// a pair's candidates (static warps met, plus pool pieces met inside [ts, hi)).
 __host__ __device__ inline int merge_extra_units(int nt, int lo, int hi, int ws, int ts,
-                                                 int piece, int Hq) {
+                                                 int piece, int cols) {
   if (nt <= 0) return 0;
   const int start = lo > ts ? lo : ts;
   const int in_pool = hi > start ? hi - start : 0;
   const int pool_part = in_pool > 0 ? (nt < in_pool ? nt : in_pool) / piece + 2 : 0;
   const int ub = nt / ws + 2 + pool_part;
   const int gsz = merge_group_size(ub);
-  return ((ub + gsz - 1) / gsz - 1) * Hq;
+  return ((ub + gsz - 1) / gsz - 1) * cols;
 }
 
 struct ReshapeArgs {
@@ -106,21 +113,24 @@ struct DecodeVariant {
   int ring_bytes;     // shared memory for the K/V rings of one CTA
 };
 
-// Per-variant entry points, implemented in decode_<type>.cu.
-// Returns cudaErrorInvalidValue for an unsupported (D, NT) combination.
-cudaError_t decode_variant_f16(int D, int nt, DecodeVariant* v);
-cudaError_t decode_variant_bf16(int D, int nt, DecodeVariant* v);
-cudaError_t decode_variant_fp8(int qt, int D, int nt, DecodeVariant* v);
-cudaError_t decode_prepare_f16(int D, int nt, int smem_bytes, int* ctas_per_sm);
-cudaError_t decode_prepare_bf16(int D, int nt, int smem_bytes, int* ctas_per_sm);
-cudaError_t decode_prepare_fp8(int qt, int D, int nt, int smem_bytes, int* ctas_per_sm);
-cudaError_t decode_launch_f16(int D, int nt, const CUtensorMap& tk, const CUtensorMap& tv,
-                              const DecodeArgs& a, int grid, int smem, cudaStream_t s, bool pdl);
-cudaError_t decode_launch_bf16(int D, int nt, const CUtensorMap& tk, const CUtensorMap& tv,
-                               const DecodeArgs& a, int grid, int smem, cudaStream_t s, bool pdl);
-cudaError_t decode_launch_fp8(int qt, int D, int nt, const CUtensorMap& tk,
-                              const CUtensorMap& tv, const DecodeArgs& a, int grid, int smem,
-                              cudaStream_t s, bool pdl);
+// Per-variant entry points of one (cache type, q type, chunked) family,
+// implemented in decode_[mq_]<type>.cu. Each returns cudaErrorInvalidValue for
+// an unsupported (D, NT) combination.
+#define PA_DECLARE_DECODE_FAMILY(NAME)                                                   \
+  cudaError_t decode_variant_##NAME(int D, int nt, DecodeVariant* v);                    \
+  cudaError_t decode_prepare_##NAME(int D, int nt, int smem_bytes, int* ctas_per_sm);    \
+  cudaError_t decode_launch_##NAME(int D, int nt, const CUtensorMap& tk,                 \
+                                   const CUtensorMap& tv, const DecodeArgs& a, int grid, \
+                                   int smem, cudaStream_t s, bool pdl);
+PA_DECLARE_DECODE_FAMILY(f16)
+PA_DECLARE_DECODE_FAMILY(bf16)
+PA_DECLARE_DECODE_FAMILY(fp8_f16)
+PA_DECLARE_DECODE_FAMILY(fp8_bf16)
+PA_DECLARE_DECODE_FAMILY(mq_f16)
+PA_DECLARE_DECODE_FAMILY(mq_bf16)
+PA_DECLARE_DECODE_FAMILY(mq_fp8_f16)
+PA_DECLARE_DECODE_FAMILY(mq_fp8_bf16)
+#undef PA_DECLARE_DECODE_FAMILY
 
 // merge_reshape.cu
 cudaError_t merge_launch(int out_type, const MergeArgs& a, int grid, cudaStream_t s, bool pdl);

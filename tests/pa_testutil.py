@@ -99,3 +99,47 @@ def assert_caches_equal(sides: Sides, what=""):
     vc = host_copy(sides.vc)
     assert np.array_equal(kc, sides.kc_ref), f"{what}: key cache differs from the oracle"
     assert np.array_equal(vc, sides.vc_ref), f"{what}: value cache differs from the oracle"
+
+
+def run_chunk(spec, device="cuda", triples=None, threads=None, use_chunk_entry=True) -> Sides:
+    """The chunked step: the write path stores the B * T new K/V rows, then
+    pa_prefill_chunk attends each sequence's T queries causally; the oracle
+    runs its reshape and causal multi-query decode on host copies."""
+    w = generate(spec, device=device)
+    s = w.spec
+    fp8 = s.kv_fp8
+    kv = "fp8" if fp8 else "auto"
+    if fp8:
+        shape = (w.num_blocks, s.num_kv_heads, s.block_size, s.head_dim)
+        kc_ref = np.full(shape, E4M3_NAN, np.uint8)
+        vc_ref = np.full(shape, E4M3_NAN, np.uint8)
+        oracle.reshape_and_cache(w.k_hist.cpu(), w.v_hist.cpu(), kc_ref, vc_ref,
+                                 w.slot_hist.cpu().numpy(), s.dtype, "fp8", w.k_scale,
+                                 w.v_scale, threads=threads)
+    else:
+        kc_ref, vc_ref = host_copy(w.key_cache), host_copy(w.value_cache)
+    oracle.reshape_and_cache(w.k_new.cpu(), w.v_new.cpu(), kc_ref, vc_ref,
+                             w.slot_new.cpu().numpy(), s.dtype, "fp8" if fp8 else s.dtype,
+                             w.k_scale, w.v_scale, threads=threads)
+    q4 = w.q if w.q.dim() == 4 else w.q.unsqueeze(1)
+    if fp8:
+        kc, vc = w.empty_fp8_cache()
+        pa.reshape_and_cache(w.k_hist, w.v_hist, kc, vc, w.slot_hist, kv, w.k_scale, w.v_scale)
+    else:
+        kc, vc = w.key_cache, w.value_cache
+    pa.reshape_and_cache(w.k_new, w.v_new, kc, vc, w.slot_new, kv, w.k_scale, w.v_scale)
+    bt = torch.from_numpy(w.block_tables).to(device)
+    sl = torch.from_numpy(w.seq_lens).to(device)
+    kw = dict(num_kv_heads=s.num_kv_heads, scale=s.softmax_scale, block_size=s.block_size,
+              window=s.window, kv_dtype=kv, k_scale=w.k_scale, v_scale=w.v_scale)
+    if use_chunk_entry:
+        out = pa.prefill_chunk(q4, kc, vc, bt, sl, **kw)
+    else:
+        out = pa.decode(w.q, kc, vc, bt, sl, **kw)
+    torch.cuda.synchronize()
+    ref = oracle.decode_multi(q4.cpu(), kc_ref, vc_ref, w.block_tables, w.seq_lens,
+                              num_kv_heads=s.num_kv_heads, scale=s.softmax_scale,
+                              block_size=s.block_size, window=s.window, q_dtype=s.dtype,
+                              cache_dtype="fp8" if fp8 else s.dtype, k_scale=w.k_scale,
+                              v_scale=w.v_scale, triples=triples, threads=threads)
+    return Sides(w, out, kc, vc, ref, kc_ref, vc_ref)

@@ -1,0 +1,105 @@
+"""GPU parity of the chunked-query path (pa_prefill_chunk) against the fp64
+oracle's causal multi-query decode, through the C ABI.
+
+Each case writes the chunk's B * T new K/V rows with the write path, then
+attends every sequence's T queries causally over the paged cache; the write
+must match the oracle bit for bit and the outputs within max-abs 1e-2 and
+mean-abs 1e-3. The cases cover one and several column groups (T * G above
+16, with padding columns), GQA groups 1 to 16, head dims 64 to 256, block
+sizes 16 and 32, sliding windows, FP8 caches, sequences shorter than the
+chunk (rows of zeros for queries before the sequence) and empty sequences.
+"""
+import numpy as np
+import pytest
+import torch
+
+from conftest import have_gpu
+from workloads.configs import Spec
+from pa_testutil import assert_caches_equal, assert_close, out_f64, run_chunk
+
+pytestmark = [pytest.mark.gpu, pytest.mark.skipif(not have_gpu(), reason="needs a GPU")]
+
+SMALL_LENS = (0, 1, 2, 3, 7, 16, 17, 31, 33, 64, 100, 129, 250, 300, 5, 48)
+
+CASES = [
+    # T, Hq, Hkv, D, bs, W, dtype, fp8
+    (2, 8, 2, 128, 16, 0, "bf16", False),     # 8 columns: one n-tile
+    (4, 8, 2, 128, 16, 0, "bf16", False),     # 16 columns: two n-tiles
+    (5, 8, 2, 128, 16, 0, "f16", False),      # 20 columns: two groups, padding
+    (3, 16, 2, 64, 32, 40, "f16", False),     # 24 columns, window, bs 32
+    (16, 16, 2, 128, 16, 100, "bf16", False), # 128 columns: eight groups
+    (7, 2, 2, 256, 16, 0, "bf16", False),     # G = 1: 7 columns, D = 256
+    (3, 32, 2, 128, 16, 0, "bf16", False),    # G = 16: three groups
+    (4, 8, 2, 128, 16, 0, "bf16", True),      # FP8 cache, bf16 q
+    (6, 4, 2, 256, 32, 50, "f16", True),      # FP8 cache, f16 q, window
+]
+
+
+def _spec(T, Hq, Hkv, D, bs, W, dt, fp8, lens=SMALL_LENS, seed=2671, **kw):
+    return Spec(f"chunk_T{T}", batch=len(lens), num_q_heads=Hq, num_kv_heads=Hkv, head_dim=D,
+                block_size=bs, dtype=dt, kv_fp8=fp8, window=W, seq_lens=tuple(lens),
+                max_len=max(lens) + 2 * bs, num_queries=T, pool_factor=1.3, seed=seed, **kw)
+
+
+@pytest.mark.parametrize("case", CASES, ids=[f"T{c[0]}_G{c[1] // c[2]}_D{c[3]}_bs{c[4]}_W{c[5]}_{c[6]}"
+                                              f"{'_fp8' if c[7] else ''}" for c in CASES])
+def test_chunk_parity(case, pa_lib):
+    sides = run_chunk(_spec(*case))
+    assert_caches_equal(sides, "chunk write path")
+    got = out_f64(sides.out)
+    assert_close(got, sides.ref, what=str(case))
+    T = case[0]
+    for b, L in enumerate(sides.w.seq_lens):
+        for t in range(T):
+            if L - T + t < 0:            # query before the sequence: zeros
+                assert (got[b, t] == 0).all()
+    assert pa_lib.check_device_error() == 0
+
+
+def test_single_query_chunk_equals_decode_bit_for_bit(pa_lib):
+    spec = _spec(1, 32, 8, 128, 16, 0, "bf16", False, lens=tuple(range(1, 400, 13)))
+    pa_lib.set_decode_tuning(pool_permille=-1)     # fixed summation order
+    try:
+        a = run_chunk(spec).out
+        b = run_chunk(spec, use_chunk_entry=False).out
+    finally:
+        pa_lib.set_decode_tuning()
+    assert torch.equal(a.squeeze(1), b)
+
+
+@pytest.mark.parametrize("tuning", [(8, 1, 500, 1), (0, 1, 1000, 1), (3, 2, -1, 0)])
+def test_chunk_under_tuning_layouts(tuning, pa_lib):
+    """Few CTAs, one-tile pieces and all-pool splits: many partials per pair,
+    several merge groups per column."""
+    pa_lib.set_decode_tuning(*tuning)
+    try:
+        sides = run_chunk(_spec(5, 8, 2, 128, 16, 30, "bf16", False,
+                                lens=(900, 3, 0, 2000, 64, 17, 1500, 5), seed=2672))
+    finally:
+        pa_lib.set_decode_tuning()
+    assert_close(out_f64(sides.out), sides.ref, what=f"tuning {tuning}")
+    assert pa_lib.check_device_error() == 0
+
+
+def _sample_triples(rng, B, T, Hq, n):
+    return np.stack([rng.integers(0, B, n), rng.integers(0, T, n), rng.integers(0, Hq, n)], 1)
+
+
+@pytest.mark.parametrize("name,T,lens,W", [
+    ("verify_llama8b", 4, ("uniform", 512, 4096), 0),     # 4 drafted tokens per sequence
+    ("prefill_chunk512", 512, ("uniform", 512, 8192), 0), # chunked prefill
+    ("prefill_chunk256_window", 256, ("uniform", 256, 12000), 4096),
+])
+def test_chunk_workloads_sampled(name, T, lens, W, pa_lib):
+    B = 64 if T <= 4 else 8
+    spec = Spec(name, batch=B, num_q_heads=32, num_kv_heads=8, head_dim=128, block_size=16,
+                dtype="bf16", window=W, len_dist=lens, num_queries=T, pool_factor=1.2,
+                seed=2673 + T)
+    rng = np.random.default_rng(5)
+    tr = _sample_triples(rng, B, T, 32, 512)
+    sides = run_chunk(spec, triples=tr)
+    assert_caches_equal(sides, name)
+    got = out_f64(sides.out)
+    assert np.isfinite(got).all()
+    assert_close(got[tuple(tr.T)], sides.ref[tuple(tr.T)], what=name)
+    assert pa_lib.check_device_error() == 0

@@ -219,3 +219,31 @@ def test_allocator_prefix_cache_matches_model_exactly(seed, pa_lib):
             assert a.table(sid) == m.table(sid)
         assert [a.refcount(b) for b in range(nb)] == m.ref
         assert a.num_free() == m.num_free() and a.num_pending() == m.num_pending()
+
+
+def test_prefill_chunk_host_validation(pa_lib):
+    pa = pa_lib
+    L = pa.lib()
+    B, T, Hq, Hkv, D, NB, bs, MB = 2, 3, 8, 2, 128, 10, 16, 4
+    base = 0x10000000
+
+    def call(q_shape=(B, T, Hq, D), out_shape=None, sl=None):
+        far = 1 << 40                                         # disjoint fake address ranges
+        q = _desc(pa, pa.PA_BF16, q_shape, base)
+        out = _desc(pa, pa.PA_BF16, out_shape or q_shape, base + far)
+        kc = _desc(pa, pa.PA_BF16, (NB, Hkv, bs, D), base + 2 * far)
+        vc = _desc(pa, pa.PA_BF16, (NB, Hkv, bs, D), base + 3 * far)
+        bt = _desc(pa, pa.PA_I32, (q_shape[0], MB), base + 4 * far)
+        sl = sl or _desc(pa, pa.PA_I32, (q_shape[0],), base + 5 * far)
+        args = [ctypes.byref(x) for x in (out, q, kc, vc, bt, sl)]
+        return L.pa_prefill_chunk(*args, Hkv, 0.1, bs, 0, 0, 1.0, 1.0, None)
+
+    assert call(q_shape=(B, Hq, D)) == -1                      # q must be [B, T, Hq, D]
+    assert call(out_shape=(B, T + 1, Hq, D)) == -1             # out shape != q shape
+    assert call(q_shape=(B, 0, Hq, D)) == -2                   # T = 0
+    assert call(q_shape=(B, 4097, Hq, D)) == -2                # T beyond the chunk limit
+    assert call(q_shape=(B, T, 9, D)) == -1                    # Hq not a multiple of Hkv
+    assert call(q_shape=(4096, 128, Hq, D)) == -2              # merge counters exceeded
+    assert "too large" in pa.last_error()
+    n = ctypes.c_size_t(0)
+    assert L.pa_prefill_chunk_workspace_size(4, 0, Hq, Hkv, D, ctypes.byref(n)) == -2

@@ -96,3 +96,30 @@ def test_fp8_workload_scales_and_history():
     assert w.k_scale == float(allk.abs().amax() / 448.0)
     kc, vc = w.empty_fp8_cache()
     assert kc.dtype == torch.uint8 and (kc == 0x7F).all()
+
+
+def test_chunk_workload_new_rows_and_union_range():
+    T, W = 5, 24
+    s = _small_prefix_window_spec(num_queries=T, window=W, shared_prefix=0,
+                                  seq_lens=(3, 40, 17, 0, 64, 5), seed=78)
+    w = generate(s)
+    assert tuple(w.q.shape) == (6, T, 4, 16)
+    assert tuple(w.k_new.shape) == (6 * T, 2, 16) and w.slot_new.shape == (6 * T,)
+    slots = w.slot_new.numpy()
+    for b, L in enumerate(w.seq_lens):
+        L = int(L)
+        for t in range(T):
+            p = L - T + t
+            want = -1 if p < 0 else int(w.block_tables[b, p // 16]) * 16 + p % 16
+            assert slots[b * T + t] == want
+        # the union of the queries' windows starts at the first query's start
+        assert w.starts[b] == max(0, L - T + 1 - W)
+    # every new slot is poisoned until the write path fills it
+    kc = w.key_cache.permute(0, 2, 1, 3).reshape(-1, 2, 16)
+    live = slots >= 0
+    assert torch.isnan(kc[torch.from_numpy(slots[live])].float()).all()
+    # positions read by some query but before the chunk hold history values
+    b, L = 4, 64
+    p = L - T - 1
+    slot = int(w.block_tables[b, p // 16]) * 16 + p % 16
+    assert not torch.isnan(kc[slot].float()).any()

@@ -29,7 +29,8 @@ class Spec:
     max_len: int | None = None     # sizes max_blocks_per_seq; default: the distribution's max
     pool_blocks: int | None = None # explicit pool size; default ceil(pool_factor * need)
     pool_factor: float = 1.2
-    new_tokens: bool = True        # the last position of each sequence is written by reshape
+    new_tokens: bool = True        # the last position(s) of each sequence are written by reshape
+    num_queries: int = 1           # query tokens per sequence (a chunk at its last positions)
     seed: int = 0
     scale: float | None = None     # default head_dim ** -0.5
     extra: dict = field(default_factory=dict, compare=False)

@@ -8,10 +8,12 @@ Recipe, in order:
   3. one K row and one V row of N(0, 1) values per unique token (shared prefix
      tokens are one row for all sequences), drawn by torch's generator seeded
      with ``spec.seed`` on the target device and rounded to the 16-bit dtype;
-  4. q ~ N(0, 1) of shape [B, Hq, D];
-  5. the last position of each sequence is the new token (``k_new``, ``v_new``
-     and its slot); every other position that some sequence reads is a history
-     row (``k_hist``, ``v_hist``, ``slot_hist``);
+  4. q ~ N(0, 1) of shape [B, Hq, D], or [B, T, Hq, D] for a chunk of
+     T = ``num_queries`` query tokens per sequence;
+  5. the last T positions of each sequence are the new tokens (``k_new``,
+     ``v_new`` and their slots, row b * T + t for position L - T + t, slot -1
+     where that position is negative); every other position that some
+     sequence reads is a history row (``k_hist``, ``v_hist``, ``slot_hist``);
   6. for 16-bit caches, history rows are placed in their slots and every other
      slot of the pool holds NaN, so a read of an unused slot, a tail slot past
      the sequence end, a slot before the window, or a new-token slot that was
@@ -19,7 +21,9 @@ Recipe, in order:
      (0x7F) and are filled by the write path from the history rows.
 
 The window is read as "a sequence of length L attends to its last min(L, W)
-positions" (W <= 0: all positions).
+positions" (W <= 0: all positions); query t of a chunk, at position
+p = L - T + t, attends to [max(0, p + 1 - W), p], so a chunk reads the
+union [max(0, L - T + 1 - W), L).
 """
 from __future__ import annotations
 
@@ -39,19 +43,19 @@ E4M3_NAN = 0x7F
 class Workload:
     spec: Spec
     seq_lens: np.ndarray          # int32 [B]
-    starts: np.ndarray            # int64 [B], first attended position
+    starts: np.ndarray            # int64 [B], first position read (by the first query)
     block_tables: np.ndarray      # int32 [B, MB], -1 past the used blocks
     num_blocks: int
     max_blocks: int
-    q: torch.Tensor               # [B, Hq, D]
+    q: torch.Tensor               # [B, Hq, D], or [B, T, Hq, D] for a chunk
     key_cache: torch.Tensor | None    # 16-bit [NB, Hkv, bs, D]; None for FP8
     value_cache: torch.Tensor | None
     k_hist: torch.Tensor | None   # [Nh, Hkv, D]
     v_hist: torch.Tensor | None
     slot_hist: torch.Tensor | None  # int64 [Nh]
-    k_new: torch.Tensor           # [B, Hkv, D] (row b is sequence b's last position)
+    k_new: torch.Tensor           # [B * T, Hkv, D] (row b * T + t: position L_b - T + t)
     v_new: torch.Tensor
-    slot_new: torch.Tensor        # int64 [B]; -1 for an empty sequence
+    slot_new: torch.Tensor        # int64 [B * T]; -1 where the position is negative
     k_scale: float
     v_scale: float
 
@@ -127,8 +131,10 @@ def generate(spec: Spec, device="cpu", keep_hist: bool | None = None) -> Workloa
         tables[b, shared_blocks:shared_blocks + n_priv] = perm[cursor:cursor + n_priv]
         cursor += n_priv
 
-    # attended range per sequence
-    W = s.window
+    # range read per sequence: the union of its queries' ranges
+    T = s.num_queries
+    assert T >= 1
+    W = s.window + T - 1 if s.window > 0 else 0
     starts = np.where((W > 0) & (lens > W), lens - W, 0).astype(np.int64)
 
     # unique token rows: shared prefix first, then each sequence's private tokens
@@ -143,24 +149,24 @@ def generate(spec: Spec, device="cpu", keep_hist: bool | None = None) -> Workloa
     pos = pos.astype(np.int64)
     row = np.where(pos < P, pos, P + priv_off[b_idx] + (pos - P))
     slot = tables[b_idx, pos // bs].astype(np.int64) * bs + pos % bs
-    is_new = pos == (lens[b_idx] - 1)
+    is_new = pos >= (lens[b_idx] - T)
     # rows read by several sequences (shared prefix) appear once
     hist_rows, first = np.unique(row[~is_new], return_index=True)
     hist_slots = slot[~is_new][first]
 
-    new_rows = np.where(lens > 0, P + priv_off + priv - 1, 0)
-    new_rows = np.where((lens > 0) & (lens <= P), lens - 1, new_rows)
-    new_slots = np.where(lens > 0,
-                         tables[np.arange(B), np.maximum(lens - 1, 0) // bs].astype(np.int64) * bs
-                         + np.maximum(lens - 1, 0) % bs, -1)
+    # new tokens: position L - T + t of sequence b is row b * T + t
+    nb_ = np.repeat(np.arange(B), T)
+    npos = np.repeat(lens, T) - T + np.tile(np.arange(T), B)
+    live = npos >= 0
+    pc = np.maximum(npos, 0)
+    new_rows = np.where(pc < P, pc, P + priv_off[nb_] + (pc - P))
+    new_rows = np.where(live, new_rows, 0)
+    new_slots = np.where(live, tables[nb_, pc // bs].astype(np.int64) * bs + pc % bs, -1)
     if not s.new_tokens:
-        new_slots = np.full(B, -1, np.int64)
         # without a write step, the last positions are history rows too
-        extra = lens > 0
-        hist_rows = np.concatenate([hist_rows, new_rows[extra]])
-        hist_slots = np.concatenate([hist_slots, tables[np.arange(B)[extra],
-                                                        (lens[extra] - 1) // bs].astype(np.int64)
-                                     * bs + (lens[extra] - 1) % bs])
+        hist_rows = np.concatenate([hist_rows, new_rows[live]])
+        hist_slots = np.concatenate([hist_slots, new_slots[live]])
+        new_slots = np.full(B * T, -1, np.int64)
 
     # values
     tdt = TORCH_DTYPES[s.dtype]
@@ -168,7 +174,8 @@ def generate(spec: Spec, device="cpu", keep_hist: bool | None = None) -> Workloa
     g.manual_seed(s.seed)
     Kl = torch.randn((max(R, 1), Hkv, D), generator=g, device=dev, dtype=torch.float32).to(tdt)
     Vl = torch.randn((max(R, 1), Hkv, D), generator=g, device=dev, dtype=torch.float32).to(tdt)
-    q = torch.randn((B, s.num_q_heads, D), generator=g, device=dev, dtype=torch.float32).to(tdt)
+    qshape = (B, s.num_q_heads, D) if T == 1 else (B, T, s.num_q_heads, D)
+    q = torch.randn(qshape, generator=g, device=dev, dtype=torch.float32).to(tdt)
 
     hr = torch.as_tensor(hist_rows, dtype=torch.int64, device=dev)
     k_hist, v_hist = Kl[hr], Vl[hr]
