@@ -13,6 +13,10 @@ e2e    : the same metric through the public API with host buffers: per step
 roofline: the decode kernel alone (CUDA events around it on its stream).
 cpu_baseline: the fp64 C oracle on this host's cores.
 
+--config picks another named workload; the chunk workloads (num_queries > 1)
+time pa_reshape_and_cache of the B * T new tokens + pa_prefill_chunk, with the
+same byte model (each K/V row of a sequence's read range counted once).
+
 --impl reference times the oracle (the CPU reference of this build) on a
 bounded sample of the same workload with the same metric.
 """
@@ -43,8 +47,9 @@ UNIT = "GB/s"
 # ----------------------------------------------------------- byte models
 
 def decode_bytes(w) -> dict:
-    """Algorithmic bytes of one pa_decode: every attended K/V row once, q,
-    out, the block-table entries of the touched blocks and seq_lens."""
+    """Algorithmic bytes of one pa_decode (or pa_prefill_chunk): every K/V row
+    of each sequence's read range once, q, out, the block-table entries of
+    the touched blocks and seq_lens."""
     s = w.spec
     L = w.seq_lens.astype(np.int64)
     st = w.starts.astype(np.int64)
@@ -52,7 +57,7 @@ def decode_bytes(w) -> dict:
     elt = 1 if s.kv_fp8 else 2
     kv = int(n.sum()) * s.num_kv_heads * 2 * s.head_dim * elt
     blocks = np.where(L > 0, -(-L // s.block_size) - st // s.block_size, 0)
-    q = s.batch * s.num_q_heads * s.head_dim * 2
+    q = s.batch * s.num_queries * s.num_q_heads * s.head_dim * 2
     tables = 4 * int(blocks.sum()) + 4 * s.batch
     return {"kv": kv, "q": q, "out": q, "tables": tables,
             "kernel": kv + q + tables, "total": kv + 2 * q + tables,
@@ -207,22 +212,29 @@ def oracle_baseline(w, kc_host, vc_host, budget_s: float, seq_subset=None) -> di
     s = w.spec
     B = s.batch
     seqs = list(range(B)) if seq_subset is None else list(seq_subset)
+    T = s.num_queries
     pairs = np.array([(b, h) for b in seqs for h in range(s.num_q_heads)], np.int32)
+    triples = np.array([(b, t, h) for b in seqs for t in range(T)
+                        for h in range(s.num_q_heads)], np.int32)
     sel = np.zeros(B, bool)
     sel[seqs] = True
     L = w.seq_lens.astype(np.int64)
     n = (L - w.starts)[sel]
     elt = 1 if s.kv_fp8 else 2
-    bytes_ = int(n.sum()) * s.num_kv_heads * 2 * s.head_dim * elt + 2 * len(pairs) * s.head_dim * 2
+    bytes_ = (int(n.sum()) * s.num_kv_heads * 2 * s.head_dim * elt
+              + 2 * len(triples) * s.head_dim * 2)
     threads = oracle.default_threads()
     qh = w.q.cpu()
     reps, t0 = 0, time.perf_counter()
+    kw = dict(num_kv_heads=s.num_kv_heads, scale=s.softmax_scale, block_size=s.block_size,
+              window=s.window, q_dtype=s.dtype, cache_dtype="fp8" if s.kv_fp8 else s.dtype,
+              k_scale=w.k_scale, v_scale=w.v_scale, threads=threads)
     while True:
-        oracle.decode(qh, kc_host, vc_host, w.block_tables, w.seq_lens,
-                      num_kv_heads=s.num_kv_heads, scale=s.softmax_scale,
-                      block_size=s.block_size, window=s.window, q_dtype=s.dtype,
-                      cache_dtype="fp8" if s.kv_fp8 else s.dtype, k_scale=w.k_scale,
-                      v_scale=w.v_scale, pairs=pairs, threads=threads)
+        if T == 1:
+            oracle.decode(qh, kc_host, vc_host, w.block_tables, w.seq_lens, pairs=pairs, **kw)
+        else:
+            oracle.decode_multi(qh, kc_host, vc_host, w.block_tables, w.seq_lens,
+                                triples=triples, **kw)
         reps += 1
         el = time.perf_counter() - t0
         if el >= budget_s:
@@ -231,7 +243,8 @@ def oracle_baseline(w, kc_host, vc_host, budget_s: float, seq_subset=None) -> di
     return {"value": bytes_ / per / 1e9, "unit": UNIT, "cores": threads, "kind": "oracle",
             "seconds_per_sample": per,
             "sample": f"fp64 C oracle decode of {len(seqs)} of {B} sequences x "
-                      f"{s.num_q_heads} heads ({int(n.sum())} attended tokens), {reps} run(s)"}
+                      f"{T} queries x {s.num_q_heads} heads ({int(n.sum())} tokens in the "
+                      f"read ranges), {reps} run(s)"}
 
 
 def host_caches(w, kc, vc):
@@ -302,6 +315,8 @@ def workload_desc(s) -> str:
         d += f", window {s.window}"
     if s.shared_prefix:
         d += f", shared prefix {s.shared_prefix}"
+    if s.num_queries > 1:
+        d += f", {s.num_queries} causal queries per sequence"
     return d
 
 
@@ -329,9 +344,11 @@ def run_ours(args, world, rank, local):
     kw = dict(num_kv_heads=s.num_kv_heads, scale=s.softmax_scale, block_size=s.block_size,
               window=s.window, kv_dtype=kv, k_scale=w.k_scale, v_scale=w.v_scale, out=out)
 
+    attend = pa.decode if s.num_queries == 1 else pa.prefill_chunk
+
     def step():
         pa.reshape_and_cache(w.k_new, w.v_new, kc, vc, w.slot_new, kv, w.k_scale, w.v_scale)
-        pa.decode(w.q, kc, vc, bt, sl, **kw)
+        attend(w.q, kc, vc, bt, sl, **kw)
 
     dbytes = decode_bytes(w)
     rbytes = reshape_bytes(w)
@@ -399,7 +416,7 @@ def run_ours(args, world, rank, local):
     for i in range(args.steps):
         flush.zero_()
         pa.profile_events(ev_a[i], ev_b[i])
-        pa.decode(w.q, kc, vc, bt, sl, **kw)
+        attend(w.q, kc, vc, bt, sl, **kw)
     pa.profile_events(None, None)
     torch.cuda.synchronize()
     k_ms = statistics.mean(a.elapsed_time(b) for a, b in zip(ev_a, ev_b))
@@ -433,7 +450,7 @@ def run_ours(args, world, rank, local):
         dev_stage.copy_(host_stage, non_blocking=True)
         pa.reshape_and_cache(dev_in["k"], dev_in["v"], kc, vc, dev_in["slot"], kv, w.k_scale,
                              w.v_scale)
-        pa.decode(dev_in["q"], kc, vc, dev_in["bt"], dev_in["sl"], **kw)
+        attend(dev_in["q"], kc, vc, dev_in["bt"], dev_in["sl"], **kw)
         host_out.copy_(out, non_blocking=True)
 
     for _ in range(3):
@@ -469,7 +486,10 @@ def run_ours(args, world, rank, local):
         "data": "synthetic",
         "config": {"workload": f"{args.config}: {workload_desc(s)}",
                    "global_batch": s.batch * world, "parallelism": f"replicas{world}",
-                   "step": "pa_reshape_and_cache (1 new token per sequence) + pa_decode",
+                   "step": ("pa_reshape_and_cache (1 new token per sequence) + pa_decode"
+                            if s.num_queries == 1 else
+                            f"pa_reshape_and_cache ({s.num_queries} new tokens per sequence) + "
+                            "pa_prefill_chunk"),
                    "attended_tokens_per_rank": dbytes["tokens"],
                    "bytes_per_step_per_rank": step_bytes,
                    "l2": "flushed between timed steps, outside the events: write 4x L2, then read 4x L2"},

@@ -1,4 +1,4 @@
-"""The five named decode workloads and the spec type for custom ones.
+"""The named decode and chunk workloads and the spec type for custom ones.
 
 Shapes follow the decode configurations the paged-attention pages motivate:
 GQA head groups ("vLLM 0.7.2深度解析" §2.2), block sizes 16 and 32 (§2.1 of the
@@ -68,6 +68,16 @@ CONFIGS: dict[str, Spec] = {
     "fp8": Spec("fp8", batch=256, num_q_heads=32, num_kv_heads=8, head_dim=128, block_size=16,
                 dtype="bf16", kv_fp8=True, len_dist=("loguniform", 1024, 8192),
                 pool_factor=1.2, seed=_seed(5)),
+    # chunked queries (pa_prefill_chunk): T query tokens per sequence at its
+    # last T positions, causal within the chunk
+    "verify4_llama8b": Spec("verify4_llama8b", batch=64, num_q_heads=32, num_kv_heads=8,
+                            head_dim=128, block_size=16, dtype="bf16",
+                            len_dist=("uniform", 512, 4096), num_queries=4, pool_factor=1.2,
+                            seed=_seed(6)),
+    "prefill_chunk512": Spec("prefill_chunk512", batch=8, num_q_heads=32, num_kv_heads=8,
+                             head_dim=128, block_size=16, dtype="bf16",
+                             len_dist=("uniform", 512, 8192), num_queries=512, pool_factor=1.2,
+                             seed=_seed(7)),
 }
 
 
