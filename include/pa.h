@@ -137,6 +137,13 @@ pa_status pa_reshape_and_cache(const pa_tensor* k, const pa_tensor* v,
  * summation order, and with it the last bits of the output, can differ from
  * run to run (pa_set_decode_tuning can turn the dynamic share off).
  *
+ * Ordering: the kernels use programmatic dependent launch. The decode kernel
+ * reads q, block_tables and seq_lens (and plans the step) before it waits for
+ * the previous kernel of the stream, and reads the caches only after. A
+ * predecessor that lets its dependents start early (as pa_reshape_and_cache
+ * does) must therefore have written q, block_tables and seq_lens before doing
+ * so; ordinary kernels and copies are waited for in full.
+ *
  * Workspace: the step writes per-segment partial results (running max, sum
  * and unnormalised output), a piece counter and a small control block to a
  * device workspace of pa_decode_workspace_size() bytes. It is the buffer

@@ -175,7 +175,12 @@ __global__ void __launch_bounds__(WARPS * 32, 2)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, t4 = lane & 3;
 
-  griddep_wait();
+  // Programmatic launch: the work before griddep_wait() below (planning from
+  // seq_lens, the control block) overlaps the previous kernel of the stream.
+  // A kernel of this library that lets dependents start early (the write
+  // path) does so only once its own predecessors have finished, and it
+  // writes none of q, seq_lens, block_tables or this workspace, only the
+  // caches, which are first read after the wait.
   griddep_launch_dependents();
 
   if (tid == 0) {
@@ -234,7 +239,8 @@ __global__ void __launch_bounds__(WARPS * 32, 2)
   const long long short_tail = total - static_cast<long long>(a.Hv) * s_pref[s_last_long + 1];
   long long pool_want = static_cast<long long>(total) * a.pool_permille / 1000;
   if (pool_want > short_tail) pool_want = short_tail;
-  int ws = static_cast<int>((total - pool_want) / nw);
+  // rounded up, so that the static ranges never reach into the pool's share
+  int ws = static_cast<int>((total - pool_want + nw - 1) / nw);
   if (ws < a.min_tiles) ws = a.min_tiles;
   const int ts = static_cast<int>(min(static_cast<long long>(ws) * nw, static_cast<long long>(total)));
   const int pool_tiles = total - ts;
@@ -378,6 +384,7 @@ __global__ void __launch_bounds__(WARPS * 32, 2)
     return true;
   };
 
+  griddep_wait();  // the caches may have been written by the previous kernel
   for (int i = 0; i < STAGES; ++i) {
     if (!produce(produced % STAGES)) break;
     ++produced;

@@ -283,6 +283,11 @@ __device__ __forceinline__ uint16_t e4m3x2_from_f32(float lo, float hi) {
 
 template <int ST, bool FP8>
 __global__ void __launch_bounds__(128) reshape_kernel(const ReshapeArgs a) {
+  // k/v may come from the previous kernel, and the cache may still be read
+  // by it: touch nothing before it completes; then let the next kernel (the
+  // decode) start its launch
+  griddep_wait();
+  griddep_launch_dependents();
   const int chunks = a.D >> 3;
   const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   const long long n = static_cast<long long>(a.T) * a.H * chunks;
@@ -340,15 +345,20 @@ __global__ void __launch_bounds__(128) reshape_kernel(const ReshapeArgs a) {
 cudaError_t reshape_launch(int src_type, bool fp8, const ReshapeArgs& a, cudaStream_t s) {
   const long long n = static_cast<long long>(a.T) * a.H * (a.D / 8);
   if (n == 0) return cudaSuccess;
-  const dim3 grid(static_cast<unsigned>((n + 127) / 128), 2);
-  if (src_type == kBF16) {
-    if (fp8) reshape_kernel<kBF16, true><<<grid, 128, 0, s>>>(a);
-    else reshape_kernel<kBF16, false><<<grid, 128, 0, s>>>(a);
-  } else {
-    if (fp8) reshape_kernel<kF16, true><<<grid, 128, 0, s>>>(a);
-    else reshape_kernel<kF16, false><<<grid, 128, 0, s>>>(a);
-  }
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>((n + 127) / 128), 2);
+  cfg.blockDim = dim3(128);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (src_type == kBF16)
+    return fp8 ? cudaLaunchKernelEx(&cfg, reshape_kernel<kBF16, true>, a)
+               : cudaLaunchKernelEx(&cfg, reshape_kernel<kBF16, false>, a);
+  return fp8 ? cudaLaunchKernelEx(&cfg, reshape_kernel<kF16, true>, a)
+             : cudaLaunchKernelEx(&cfg, reshape_kernel<kF16, false>, a);
 }
 
 }  // namespace pa
