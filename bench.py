@@ -467,6 +467,31 @@ def run_ours(args, world, rank, local):
     e2e_ms = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in zip(e_s, e_e)), world)
     e2e_value = total_bytes / (e2e_ms * 1e-3) / 1e9
 
+    # ---- the same step captured once in a CUDA graph and replayed (the L2
+    # flush stays outside the graph, events around each replay)
+    gstream = torch.cuda.Stream(device=dev)
+    gstream.wait_stream(stream)
+    with torch.cuda.stream(gstream):
+        for _ in range(3):
+            step()  # the library's workspace for this stream exists before capture
+    gstream.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=gstream):
+        step()
+    g_s = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    g_e = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        flush.zero_()
+        g_s[i].record(stream)
+        graph.replay()
+        g_e[i].record(stream)
+    torch.cuda.synchronize()
+    graph_ms = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in zip(g_s, g_e)), world)
+    del graph
+
     bad = pa.check_device_error()
     if bad:
         raise RuntimeError(f"device error flag {bad} during the benchmark")
@@ -500,6 +525,9 @@ def run_ours(args, world, rank, local):
                      "bytes_per_launch": dbytes["kernel"], "peak_kind": peak_kind},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "graph": {"value": total_bytes / (graph_ms * 1e-3) / 1e9, "unit": UNIT,
+                  "us_per_step": graph_ms * 1e3,
+                  "what": "the step captured in one CUDA graph, replayed per step"},
         "gpu_launches": launches,
         "clocks": clk,
         "wall_s_timed": wall,
