@@ -167,7 +167,10 @@ def decode(q, key_cache, value_cache, block_tables, seq_lens, *, num_kv_heads: i
     MB = bt.shape[1]
     out = np.zeros((B, Hq, D), np.float64)
     if pairs is not None:
-        pr = np.ascontiguousarray(np.asarray(pairs, dtype=np.int32).reshape(-1, 2))
+        # distinct rows only: the C oracle runs listed rows on parallel threads,
+        # and two threads must not write one output row
+        pr = np.ascontiguousarray(np.unique(np.asarray(pairs, dtype=np.int32).reshape(-1, 2),
+                                            axis=0))
         pp, npairs = _ptr(pr), pr.shape[0]
     else:
         pr, pp, npairs = None, None, 0
@@ -199,7 +202,8 @@ def decode_multi(q, key_cache, value_cache, block_tables, seq_lens, *, num_kv_he
     MB = bt.shape[1]
     out = np.zeros((B, T, Hq, D), np.float64)
     if triples is not None:
-        tr = np.ascontiguousarray(np.asarray(triples, dtype=np.int32).reshape(-1, 3))
+        tr = np.ascontiguousarray(np.unique(np.asarray(triples, dtype=np.int32).reshape(-1, 3),
+                                            axis=0))  # distinct rows, as for pairs
         tp, ntr = _ptr(tr), tr.shape[0]
     else:
         tr, tp, ntr = None, None, 0

@@ -62,7 +62,8 @@ int orc_reshape_and_cache(const uint16_t* k, const uint16_t* v, int64_t num_toke
 
 /*
  * Decode: out[b, h, :] (fp64) for each requested (b, h); pairs holds n_pairs
- * (b, h) couples, or is NULL for all B * Hq of them. q is [B, Hq, D] 16-bit,
+ * distinct (b, h) couples (computed on parallel threads), or is NULL for all
+ * B * Hq of them. q is [B, Hq, D] 16-bit,
  * block_tables is [B, max_blocks] int32, seq_lens [B] int32. q head h reads KV
  * head h / (Hq / Hkv). The attended positions are [start, L) with
  * start = max(0, L - window) when window > 0, else 0. For ORC_E4M3 caches the
@@ -86,7 +87,8 @@ int orc_decode(double* out, const uint16_t* q, int q_dtype, const void* key_cach
  * p_t = seq_lens[b] - T + t (the last T positions of the sequence), and query
  * t attends to [start_t, p_t], start_t = max(0, p_t + 1 - window) when
  * window > 0, else 0. A query with p_t < 0 gives zeros. With T = 1 this is
- * orc_decode. pairs lists (b, t, h) triples, or is NULL for all of them.
+ * orc_decode. triples lists distinct (b, t, h) rows (they are computed on
+ * parallel threads), or is NULL for all of them.
  */
 int orc_decode_multi(double* out, const uint16_t* q, int q_dtype, const void* key_cache,
                      const void* value_cache, int cache_dtype, const int32_t* block_tables,

@@ -436,3 +436,24 @@ def test_decode_multi_queries_before_the_sequence_give_zeros():
     q = rng.normal(size=(1, 4, 1, 8)).astype(np.float16)
     out = _odecode_multi(q, kc, vc, tables, [2], 1, 16, 1.0)
     assert (out[0, :2] == 0).all() and (out[0, 2:] != 0).any()
+
+
+def test_repeated_rows_in_a_request_are_computed_once_and_correctly():
+    """Requests that list a row twice (random samples do) give the same
+    values as requests that list it once: the rows are computed on parallel
+    threads, which must never share an output row."""
+    rng = np.random.default_rng(303)
+    Hkv, G, D, bs, T = 2, 2, 16, 16, 3
+    lens = [70, 33]
+    tables, kc, vc, K, V = _build_paged(rng, lens, Hkv, D, bs)
+    q3 = rng.normal(size=(2, Hkv * G, D)).astype(np.float16)
+    pairs = [(1, 3)] * 64 + [(0, 0)] * 64
+    once = _odecode(q3, kc, vc, tables, lens, Hkv, bs, 0.2, pairs=[(1, 3), (0, 0)])
+    many = _odecode(q3, kc, vc, tables, lens, Hkv, bs, 0.2, pairs=pairs)
+    assert np.array_equal(once, many)
+    q4 = rng.normal(size=(2, T, Hkv * G, D)).astype(np.float16)
+    tr = [(1, 2, 3)] * 64 + [(0, 1, 0)] * 64
+    once = _odecode_multi(q4, kc, vc, tables, lens, Hkv, bs, 0.2,
+                          triples=[(1, 2, 3), (0, 1, 0)])
+    many = _odecode_multi(q4, kc, vc, tables, lens, Hkv, bs, 0.2, triples=tr)
+    assert np.array_equal(once, many)
