@@ -224,7 +224,18 @@ pa_status pa_prefill_chunk(const pa_tensor* out, const pa_tensor* q, const pa_te
                            int32_t block_size, int32_t window, int32_t kv_dtype, float k_scale,
                            float v_scale, pa_stream stream);
 
-/* Workspace bytes pa_prefill_chunk needs on the current device. */
+/* Kernel choice for pa_prefill_chunk, process-wide: 0 (default) picks per
+ * call; 1 always uses the persistent split-KV kernel (16 (query, head)
+ * columns per pass over K/V, any head dim, FP8 caches); 2 uses the
+ * tensor-memory kernel wherever it applies (16-bit caches, head_dim 128),
+ * which tiles 128 (query, head) rows against 64-token K/V tiles on the
+ * tcgen05 tensor cores and reads each K/V tile once per 128 rows. The
+ * default takes the tensor-memory kernel for chunks of more than 32 (query,
+ * head) columns per KV head. */
+pa_status pa_set_prefill_path(int32_t path);
+
+/* Workspace bytes pa_prefill_chunk needs on the current device (the
+ * tensor-memory kernel needs none). */
 pa_status pa_prefill_chunk_workspace_size(int64_t batch, int32_t num_queries,
                                           int32_t num_q_heads, int32_t num_kv_heads,
                                           int32_t head_dim, size_t* bytes);

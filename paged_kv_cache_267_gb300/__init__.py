@@ -62,6 +62,7 @@ def lib() -> ctypes.CDLL:
                                                      ctypes.POINTER(ctypes.c_size_t)]),
             "pa_set_workspace": (st, [vp, ctypes.c_size_t]),
             "pa_set_decode_tuning": (st, [i32, i32, i32, i32]),
+            "pa_set_prefill_path": (st, [i32]),
             "pa_profile_events": (st, [vp, vp]),
             "pa_check_device_error": (st, [ctypes.POINTER(i32), vp]),
             "pa_launch_count": (ctypes.c_uint64, []),
@@ -210,6 +211,12 @@ def set_workspace(buf: torch.Tensor | None) -> None:
         _check(lib().pa_set_workspace(None, 0))
     else:
         _check(lib().pa_set_workspace(buf.data_ptr(), buf.numel() * buf.element_size()))
+
+
+def set_prefill_path(path: int = 0) -> None:
+    """pa_prefill_chunk's kernel: 0 auto, 1 persistent split-KV kernel,
+    2 tensor-memory kernel wherever it applies."""
+    _check(lib().pa_set_prefill_path(path))
 
 
 def set_decode_tuning(max_ctas: int = 0, min_tiles: int = 0, pool_permille: int = 0,

@@ -28,6 +28,7 @@ std::atomic<int32_t> g_tune_max_ctas{0};
 std::atomic<int32_t> g_tune_min_tiles{0};
 std::atomic<int32_t> g_tune_pool{0};
 std::atomic<int32_t> g_tune_piece{0};
+std::atomic<int32_t> g_chunk_path{0};  // 0 auto, 1 persistent kernel, 2 tensor-memory kernel
 thread_local void* g_prof_before = nullptr;
 thread_local void* g_prof_after = nullptr;
 
@@ -39,6 +40,10 @@ constexpr int kMaxCtasPerSm = 2;
 constexpr int kWarpsPerCta = 8;  // most worker warps of any decode variant
 constexpr int64_t kMaxBatch = 4096;
 constexpr int64_t kMaxChunk = 4096;        // query tokens per sequence in a chunk call
+// Chunks with more (query, head) columns per KV head than this go to the
+// tensor-memory kernel (16-bit caches, head dim 128): the persistent kernel
+// reads each K/V tile once per 16 columns.
+constexpr int64_t kTcMinColumns = 32;
 
 pa_status fail(pa_status code, const char* fmt, ...) {
   char buf[512];
@@ -125,6 +130,7 @@ struct DeviceState {
   bool init = false;
   int num_sms = 0;
   int32_t* err_word = nullptr;
+  bool chunk_tc_ready = false;              // tensor-memory kernel configured
   Workspace user_ws;                        // caller-owned (pa_set_workspace)
   std::map<uintptr_t, Workspace> lib_ws;    // library-owned, one per stream
   std::map<std::tuple<int, int, int, int, int, bool>, int> occupancy;
@@ -366,6 +372,12 @@ pa_status pa_set_decode_tuning(int32_t max_ctas, int32_t min_tiles, int32_t pool
   g_tune_min_tiles = min_tiles;
   g_tune_pool = pool_permille;
   g_tune_piece = piece_tiles;
+  return ok();
+}
+
+pa_status pa_set_prefill_path(int32_t path) {
+  if (path < 0 || path > 2) return fail(PA_ERR_INVALID_ARG, "path must be 0, 1 or 2");
+  g_chunk_path = path;
   return ok();
 }
 
@@ -716,6 +728,59 @@ pa_status run_decode(const DecodeCall& c, DeviceState* st, const DecodePlan& pla
   return ok();
 }
 
+bool use_chunk_tc(const DecodeCall& c) {
+  const int path = g_chunk_path.load();
+  if (path == 1 || c.fp8 || c.D != 128) return false;
+  return path == 2 || c.T * c.G > kTcMinColumns;
+}
+
+// A chunk on the tensor-memory kernel: no workspace, one launch.
+pa_status run_chunk_tc(const DecodeCall& c, cudaStream_t cs) {
+  pa_status s;
+  DeviceState* st;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if ((s = device_state(&st, nullptr))) return s;
+    if (!st->chunk_tc_ready) {
+      cudaError_t e = pa::chunk_tc_prepare();
+      if (e != cudaSuccess) return cuda_fail(e, "chunk kernel setup");
+      st->chunk_tc_ready = true;
+    }
+  }
+  const int D = static_cast<int>(c.D);
+  CUtensorMap tk, tv;
+  if ((s = make_cache_map(&tk, c.kc->data, c.NB * c.Hkv * c.bs, D, 2)) ||
+      (s = make_cache_map(&tv, c.vc->data, c.NB * c.Hkv * c.bs, D, 2)))
+    return s;
+  pa::ChunkArgs a;
+  a.q = c.q->data;
+  a.out = c.out->data;
+  a.block_tables = static_cast<const int32_t*>(c.bt->data);
+  a.seq_lens = static_cast<const int32_t*>(c.sl->data);
+  a.err = st->err_word;
+  a.B = static_cast<int>(c.B);
+  a.T = static_cast<int>(c.T);
+  a.Hq = static_cast<int>(c.Hq);
+  a.Hkv = static_cast<int>(c.Hkv);
+  a.G = c.G;
+  a.bs = c.bs;
+  a.MB = static_cast<int>(c.MB);
+  a.NB = static_cast<int>(c.NB);
+  a.window = c.window;
+  a.QT = static_cast<int>((c.T * c.G + 127) / 128);
+  a.score_scale = static_cast<float>(static_cast<double>(c.scale) * 1.4426950408889634);
+  const bool prof = g_prof_before && g_prof_after;
+  cudaError_t e;
+  if (prof && (e = cudaEventRecord(static_cast<cudaEvent_t>(g_prof_before), cs)) != cudaSuccess)
+    return cuda_fail(e, "profile event");
+  e = pa::chunk_tc_launch(c.qt, tk, tv, a, cs, !prof);
+  if (e != cudaSuccess) return cuda_fail(e, "chunk kernel launch");
+  if (prof && (e = cudaEventRecord(static_cast<cudaEvent_t>(g_prof_after), cs)) != cudaSuccess)
+    return cuda_fail(e, "profile event");
+  g_launches += 1;
+  return ok();
+}
+
 // Validation, planning and launch with the library's (or the caller's set)
 // workspace.
 pa_status decode_entry(const pa_tensor* out, const pa_tensor* q, const pa_tensor* key_cache,
@@ -730,6 +795,7 @@ pa_status decode_entry(const pa_tensor* out, const pa_tensor* q, const pa_tensor
   if (s) return s;
   if (c.B == 0) return ok();
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  if (chunked && use_chunk_tc(c)) return run_chunk_tc(c, cs);
   DeviceState* st;
   DecodePlan plan;
   WsLayout layout;

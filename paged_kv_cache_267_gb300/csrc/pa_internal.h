@@ -106,6 +106,23 @@ struct ReshapeArgs {
   float k_scale, v_scale;
 };
 
+// Chunked queries on the tensor-memory kernel (chunk_tc.cu): one CTA per
+// (sequence, KV head, tile of 128 (query, head) rows); head dim 128, 16-bit
+// caches.
+struct ChunkArgs {
+  const void* q;                 // [B, T, Hq, D]
+  void* out;                     // [B, T, Hq, D]
+  const int32_t* block_tables;   // [B, MB]
+  const int32_t* seq_lens;       // [B]
+  int32_t* err;                  // device error word
+  int B, T, Hq, Hkv, G, bs, MB, NB, window;
+  int QT;                        // row tiles per (sequence, KV head): ceil(T * G / 128)
+  float score_scale;             // scale * log2(e)
+};
+cudaError_t chunk_tc_prepare();  // once per device: the kernel's shared-memory size
+cudaError_t chunk_tc_launch(int qt, const CUtensorMap& tk, const CUtensorMap& tv,
+                            const ChunkArgs& a, cudaStream_t s, bool pdl);
+
 // Kernel configuration chosen for a (cache type, q type, D, n-tiles) variant.
 struct DecodeVariant {
   int warps;          // worker warps per CTA

@@ -83,13 +83,21 @@ def out_f64(out: torch.Tensor) -> np.ndarray:
     return out.detach().float().cpu().double().numpy()
 
 
-def assert_close(got: np.ndarray, ref: np.ndarray, pairs=None, what=""):
+# Chunked queries: rows that attend to a handful of positions have outputs of
+# magnitude up to ~4 (nearly one V row), where rounding the output to bf16
+# alone costs up to 2^-9 |out| and rounding P to bf16 up to 2^-9 max|v|; the
+# bound grows by 2^-8 |ref| on top of the decode tolerance.
+CHUNK_REL_TOL = 2.0 ** -8
+
+
+def assert_close(got: np.ndarray, ref: np.ndarray, pairs=None, what="", rel=0.0):
     if pairs is not None:
         idx = tuple(np.asarray(pairs).T)
         got, ref = got[idx], ref[idx]
     assert np.isfinite(got).all(), f"{what}: non-finite outputs"
     err = np.abs(got - ref)
-    assert err.max() <= MAX_ABS_TOL, f"{what}: max abs err {err.max():.3e}"
+    excess = err - (MAX_ABS_TOL + rel * np.abs(ref))
+    assert excess.max() <= 0, f"{what}: max abs err {err.max():.3e} (bound exceeded by {excess.max():.3e})"
     assert err.mean() <= MEAN_ABS_TOL, f"{what}: mean abs err {err.mean():.3e}"
     return float(err.max()), float(err.mean())
 
