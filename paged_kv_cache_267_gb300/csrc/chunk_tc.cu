@@ -3,28 +3,31 @@
 // is the block-wise scaled dot product with a running max/sum of §2.3 of
 // the same page), on the 5th-generation tensor cores of sm_103a.
 //
-// Work unit: one (sequence b, KV head, tile of 128 (query, head) rows), the
-// rows being r = t * G + h over the chunk's T queries and the group's G
-// heads: one CTA each. The unit's read range is the union of its rows'
-// ranges, [lo, hi] with lo the first row's window start and hi the last
-// row's position; it is walked in K/V tiles of 64 tokens (four 16-token
-// slices, each inside one physical block, fetched by TMA through the block
-// table).
+// Work unit: one (sequence b, KV head, 256 (query, head) rows), the rows
+// being r = t * G + h over the chunk's T queries and the group's G heads: one
+// CTA each, holding two 128-row tiles A and B. The unit's read range is the
+// union of its rows' ranges, [lo, hi] with lo the first row's window start
+// and hi the last row's position; it is walked in K/V tiles of 64 tokens
+// (four 16-token slices, each inside one physical block, fetched by TMA
+// through the block table), each shared by both row tiles.
 //
-// Per K/V tile n, with one control warp and four softmax warps (one row per
-// thread):
-//   control : S = Q . K_n^T           tcgen05.mma M128 N64  K128 -> TMEM
-//   softmax : S from TMEM; per-row causal/window mask; online softmax in the
-//             log2 domain; P (16-bit) -> shared memory, 128-byte swizzle
-//   control : O_n = P . V_n           tcgen05.mma M128 N128 K64  -> TMEM
-//             (V MN-major: its rows are tokens, head dims contiguous)
-//   softmax : O = alpha O + O_n in registers
-// Q (128 rows x 128 dims) stays in shared memory for the whole unit; K/V
-// tiles stream through a three-stage ring; the control warp issues S_{n+1}
-// while the softmax warps fold O_n. V rows of an edge tile that lie outside
-// [lo, hi] (not loaded, or NaN-poisoned slots past the sequence or before
-// the window) are zeroed in shared memory before the P . V product, so only
-// attended rows reach the tensor core. Head dim 128, f16 or bf16 caches.
+// Roles: a control warp streams K/V tiles through a three-stage ring and
+// issues every MMA; two groups of four softmax warps (one row per thread)
+// serve tiles A and B, so the tensor core works for one group while the
+// other runs its softmax. Per K/V tile n and row tile X:
+//   S_X  = Q_X . K_n^T        tcgen05.mma M128 N64  K128 -> TMEM
+//   softmax X: S_X from TMEM; per-row causal/window mask; online softmax in
+//          the log2 domain against the row's reference max m; P_X (16-bit)
+//          -> shared memory, 128-byte swizzle
+//   O_X += P_X . V_n          tcgen05.mma M128 N128 K64 -> TMEM (V MN-major)
+// The output accumulates in tensor memory. A row's reference max moves only
+// when its running max exceeds it by more than 8 (log2 units); the warp then
+// rescales those rows of O_X in tensor memory (load, scale, store) before the
+// next product, so P stays below 2^8 and most tiles never touch O. V rows of
+// an edge tile that lie outside [lo, hi] (not loaded, or NaN-poisoned slots
+// past the sequence or before the window) are zeroed in shared memory before
+// the products, so only attended rows reach the tensor core. Head dim 128,
+// f16 or bf16 caches.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -35,28 +38,31 @@
 namespace pa {
 namespace {
 
-constexpr int kRows = 128;      // (query, head) rows per unit: the MMA M
+constexpr int kRows = 128;      // rows per row tile: the MMA M
+constexpr int kUnitRows = 2 * kRows;
 constexpr int kKv = 64;         // tokens per K/V tile
 constexpr int kHd = 128;        // head dim
 constexpr int kStages = 3;      // K/V ring depth
-constexpr int kSoftWarps = 4;
-constexpr int kThreads = (kSoftWarps + 1) * 32;
-constexpr uint32_t kQBytes = kRows * kHd * 2;   // [2 boxes][128 rows][128 B]
+constexpr int kGroupWarps = 4;  // softmax warps per row tile
+constexpr int kCtrlWarp = 2 * kGroupWarps;
+constexpr int kThreads = (kCtrlWarp + 1) * 32;
+constexpr uint32_t kQBytes = kRows * kHd * 2;   // per row tile: [2 boxes][128 rows][128 B]
 constexpr uint32_t kKvBytes = kKv * kHd * 2;    // [2 boxes][64 rows][128 B]
-constexpr uint32_t kPBytes = kRows * kKv * 2;   // [128 rows][128 B]
-constexpr uint32_t kOffQ = 0;
-constexpr uint32_t kOffK = kOffQ + kQBytes;
+constexpr uint32_t kPBytes = kRows * kKv * 2;   // per row tile: [128 rows][128 B]
+constexpr uint32_t kOffQ = 0;                   // Q_A, Q_B
+constexpr uint32_t kOffK = kOffQ + 2 * kQBytes;
 constexpr uint32_t kOffV = kOffK + kStages * kKvBytes;
-constexpr uint32_t kOffP = kOffV + kStages * kKvBytes;
-constexpr uint32_t kOffBar = kOffP + kPBytes;
-constexpr int kBarFull = 0, kBarEmpty = kStages, kBarS = 2 * kStages, kBarP = kBarS + 1,
-              kBarO = kBarS + 2, kBarQ = kBarS + 3, kNumBars = kBarS + 4;
+constexpr uint32_t kOffP = kOffV + kStages * kKvBytes;  // P_A, P_B
+constexpr uint32_t kOffBar = kOffP + 2 * kPBytes;
+constexpr int kBarFull = 0, kBarEmpty = kStages, kBarS = 2 * kStages,  // S_A, S_B
+    kBarP = kBarS + 2, kBarO = kBarS + 4, kBarQ = kBarS + 6, kNumBars = kBarS + 7;
 constexpr uint32_t kOffSlot = kOffBar + 8 * kNumBars;
 constexpr uint32_t kSmemBytes = kOffSlot + 16 + 1024;  // + room to align the base to 1 KB
-constexpr uint32_t kTmemCols = 256;                    // S: columns [0, 64); O_n: [128, 256)
+constexpr uint32_t kTmemCols = 512;  // S_A [0,64) S_B [64,128) O_A [128,256) O_B [256,384)
 constexpr uint32_t kColS = 0, kColO = 128;
-constexpr uint64_t kWaitNs = 2000000000ull;            // bound of every wait (2 s)
-constexpr float kFloor = -1e30f;                       // running-max start
+constexpr uint64_t kWaitNs = 2000000000ull;  // bound of every wait (2 s)
+constexpr float kFloor = -1e30f;             // reference-max start
+constexpr float kRescaleAbove = 8.f;         // log2 units
 constexpr unsigned kFull = 0xffffffffu;
 
 __device__ __forceinline__ void sts_v4(uint32_t addr, uint4 v) {
@@ -82,6 +88,9 @@ __device__ __forceinline__ float ex2(float x) {
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
+__device__ __forceinline__ bool wait_all(uint32_t bar, uint32_t parity) {
+  return __all_sync(kFull, mbar_wait_bounded(bar, parity, kWaitNs));
+}
 
 template <int QT>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -96,7 +105,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t* tslot = reinterpret_cast<const uint32_t*>(smem_raw + (base - raw) + kOffSlot);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int qt = blockIdx.x % a.QT;
+  const int ut = blockIdx.x % a.QT;  // unit (256 rows) within the (sequence, KV head)
   const int kvh = (blockIdx.x / a.QT) % a.Hkv;
   const int b = blockIdx.x / (a.QT * a.Hkv);
 
@@ -107,10 +116,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(kBarFull + i), 1);
       mbar_init(bar(kBarEmpty + i), 1);
     }
-    mbar_init(bar(kBarS), 1);
-    mbar_init(bar(kBarP), kSoftWarps * 32);
-    mbar_init(bar(kBarO), 1);
-    mbar_init(bar(kBarQ), kSoftWarps * 32);
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(bar(kBarS + x), 1);
+      mbar_init(bar(kBarP + x), kGroupWarps * 32);
+      mbar_init(bar(kBarO + x), 1);
+    }
+    mbar_init(bar(kBarQ), 2 * kGroupWarps * 32);
     fence_mbar_init();
   }
   if (warp == 0) tc::tmem_alloc(base + kOffSlot, kTmemCols);
@@ -128,15 +139,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (tid == 0) atomicOr(a.err, PA_DEVERR_SEQ_LEN);
     L = L < 0 ? 0 : cap;
   }
-  const int r0 = qt * kRows;
-  const int r1 = min(r0 + kRows, a.T * a.G);  // valid rows [r0, r1)
+  const int nrows = a.T * a.G;
+  const int r0 = ut * kUnitRows;
+  const int r1 = min(r0 + kUnitRows, nrows);  // valid rows [r0, r1)
+  const bool hasB = r0 + kRows < r1;
   const int p_first = L - a.T + r0 / a.G;
-  const int hi = L - a.T + (r1 - 1) / a.G;    // last position read
+  const int hi = L - a.T + (r1 - 1) / a.G;  // last position read
   const int lo = (a.window > 0 && p_first + 1 > a.window) ? p_first + 1 - a.window : 0;
   const int lo16 = lo & ~15;
   const int ntiles = hi >= lo ? (hi + 1 - lo16 + kKv - 1) / kKv : 0;
 
-  if (warp == kSoftWarps) {
+  if (warp == kCtrlWarp) {
     // ------------------------------------------------------------ control
     // Loads K/V tile n into `stage`: lanes 0..3 each look up one 16-token
     // slice in the block table and copy it (two 64-dim boxes of K and of V).
@@ -167,161 +180,198 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     constexpr uint32_t idS = tc::idesc_f16(kRows, kKv, kBf16, false);
     constexpr uint32_t idO = tc::idesc_f16(kRows, kHd, kBf16, true);
-    // S = Q . K_n^T over the 128 head dims (8 steps of 16)
-    auto issue_s = [&](int n) {
+    // S_X = Q_X . K_n^T over the 128 head dims (8 steps of 16)
+    auto issue_s = [&](int x, int n) {
       const int st = n % kStages;
       if (lane == 0) {
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
           const uint32_t box = ks >> 2, kk = (ks & 3) * 32;
-          const uint64_t ad = tc::sdesc_sw128(sQ + box * 16384 + kk, 16, 1024);
+          const uint64_t ad = tc::sdesc_sw128(sQ + x * kQBytes + box * 16384 + kk, 16, 1024);
           const uint64_t bd = tc::sdesc_sw128(sK + st * kKvBytes + box * 8192 + kk, 16, 1024);
-          tc::mma_f16(tmem + kColS, ad, bd, idS, ks > 0);
+          tc::mma_f16(tmem + kColS + 64 * x, ad, bd, idS, ks > 0);
         }
-        tc::commit(bar(kBarS));
+        tc::commit(bar(kBarS + x));
+      }
+      __syncwarp();
+    };
+    // O_X (+)= P_X . V_n over 64 tokens (4 steps of 16)
+    auto issue_o = [&](int x, int n) {
+      const int st = n % kStages;
+      if (lane == 0) {
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) {
+          const uint64_t ad = tc::sdesc_sw128(sP + x * kPBytes + ks * 32, 16, 1024);
+          const uint64_t bd = tc::sdesc_sw128(sV + st * kKvBytes + ks * 2048, 8192, 1024);
+          tc::mma_f16(tmem + kColO + 128 * x, ad, bd, idO, (n > 0 || ks > 0) ? 1u : 0u);
+        }
+        tc::commit(bar(kBarO + x));
       }
       __syncwarp();
     };
     bool ok = true;
     for (int i = 0; i < kStages && i < ntiles; ++i) load_tile(i, i);
     if (ntiles > 0) {
-      ok = __all_sync(kFull, mbar_wait_bounded(bar(kBarQ), 0, kWaitNs)) &&
-           __all_sync(kFull, mbar_wait_bounded(bar(kBarFull), 0, kWaitNs));
+      ok = wait_all(bar(kBarQ), 0) && wait_all(bar(kBarFull), 0);
       if (ok) {
         tc::fence_after_sync();
-        issue_s(0);
+        issue_s(0, 0);
+        if (hasB) issue_s(1, 0);
       }
     }
     for (int n = 0; ok && n < ntiles; ++n) {
       const int st = n % kStages;
-      // P_n written (and V_n cleaned) by the softmax warps
-      ok = __all_sync(kFull, mbar_wait_bounded(bar(kBarP), n & 1, kWaitNs));
-      if (!ok) break;
+      const bool more = n + 1 < ntiles;
+      if (!(ok = wait_all(bar(kBarP), n & 1))) break;  // P_A(n) written, V_n cleaned
       tc::fence_after_sync();
-      if (lane == 0) {
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks) {  // O_n = P . V_n over 64 tokens (4 steps of 16)
-          const uint64_t ad = tc::sdesc_sw128(sP + ks * 32, 16, 1024);
-          const uint64_t bd = tc::sdesc_sw128(sV + st * kKvBytes + ks * 2048, 8192, 1024);
-          tc::mma_f16(tmem + kColO, ad, bd, idO, ks > 0);
-        }
-        tc::commit(bar(kBarO));
-        tc::commit(bar(kBarEmpty + st));
-      }
-      __syncwarp();
-      if (n + 1 < ntiles) {
-        ok = __all_sync(kFull, mbar_wait_bounded(bar(kBarFull + (n + 1) % kStages),
-                                                 ((n + 1) / kStages) & 1, kWaitNs));
-        if (!ok) break;
+      issue_o(0, n);
+      if (more) {
+        if (!(ok = wait_all(bar(kBarFull + (n + 1) % kStages), ((n + 1) / kStages) & 1))) break;
         tc::fence_after_sync();
-        issue_s(n + 1);
+        issue_s(0, n + 1);
       }
+      if (hasB) {
+        if (!(ok = wait_all(bar(kBarP + 1), n & 1))) break;
+        tc::fence_after_sync();
+        issue_o(1, n);
+      }
+      if (lane == 0) tc::commit(bar(kBarEmpty + st));  // both products of tile n issued
+      __syncwarp();
+      if (hasB && more) issue_s(1, n + 1);
       if (n + kStages < ntiles) {
-        ok = __all_sync(kFull, mbar_wait_bounded(bar(kBarEmpty + st), (n / kStages) & 1, kWaitNs));
-        if (!ok) break;
+        if (!(ok = wait_all(bar(kBarEmpty + st), (n / kStages) & 1))) break;
         load_tile(n + kStages, st);
       }
     }
     if (!ok && lane == 0) atomicOr(a.err, PA_DEVERR_TIMEOUT);
   } else {
     // ------------------------------------------------------------ softmax
-    const int r = tid;  // row of the unit = tensor-memory lane
-    const int gr = r0 + r;
+    const int x = warp / kGroupWarps;  // row tile: 0 = A, 1 = B
+    const int r = tid - x * kRows;     // row within the tile = tensor-memory lane
+    const int gr = r0 + x * kRows + r;
     const bool valid = gr < r1;
+    const bool active = x == 0 || hasB;
     const int tq = valid ? gr / a.G : 0;
     const int hq = gr - tq * a.G;
     const int hi_r = valid ? L - a.T + tq : -1;  // this row's query position
     const int lo_r = (a.window > 0 && hi_r + 1 > a.window) ? hi_r + 1 - a.window : 0;
     const size_t orow =
         ((static_cast<size_t>(b) * a.T + tq) * a.Hq + static_cast<size_t>(kvh) * a.G + hq) * kHd;
+    const uint32_t q_tile = sQ + x * kQBytes, p_tile = sP + x * kPBytes;
     {  // Q row -> shared memory (K-major, 128-byte swizzle)
-      const uint4* src = reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(a.q) + orow);
+      const uint4* src =
+          reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(a.q) + orow);
 #pragma unroll
       for (int c = 0; c < 16; ++c) {
-        const uint4 x = valid ? src[c] : make_uint4(0u, 0u, 0u, 0u);
-        sts_v4(sQ + (c >> 3) * 16384 + r * 128 + (((c & 7) ^ (r & 7)) << 4), x);
+        const uint4 v = valid ? src[c] : make_uint4(0u, 0u, 0u, 0u);
+        sts_v4(q_tile + (c >> 3) * 16384 + r * 128 + (((c & 7) ^ (r & 7)) << 4), v);
       }
       fence_proxy_async();
       mbar_arrive(bar(kBarQ));
     }
-    const uint32_t trow = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-    float m = kFloor, l = 0.f;
-    float o[kHd];
-#pragma unroll
-    for (int i = 0; i < kHd; ++i) o[i] = 0.f;
+    const uint32_t trow = tmem + (static_cast<uint32_t>((warp % 4) * 32) << 16);
+    const uint32_t tS = trow + kColS + 64 * x, tO = trow + kColO + 128 * x;
+    float m = kFloor, l = 0.f;  // reference max and running sum of the row
     bool ok = true;
-    for (int n = 0; n < ntiles; ++n) {
+    for (int n = 0; active && n < ntiles; ++n) {
       const int st = n % kStages;
       const int t0 = lo16 + n * kKv;  // position of the tile's first token
-      ok = __all_sync(kFull, mbar_wait_bounded(bar(kBarS), n & 1, kWaitNs));
-      if (!ok) break;
+      if (!(ok = wait_all(bar(kBarS + x), n & 1))) break;
       tc::fence_after_sync();
+      uint32_t sr[2][32];
+      tc::ld32_async(tS, sr[0]);
+      tc::ld32_async(tS + 32, sr[1]);
+      tc::wait_ld();
       float s[kKv];
-      tc::ld32(trow + kColS, s);
-      tc::ld32(trow + kColS + 32, s + 32);
       const bool inside = t0 >= lo_r && t0 + kKv - 1 <= hi_r;
       float mx = kFloor;
 #pragma unroll
       for (int j = 0; j < kKv; ++j) {
         const bool keep = inside || (t0 + j >= lo_r && t0 + j <= hi_r);
-        s[j] = keep ? s[j] * a.score_scale : -INFINITY;
+        s[j] = keep ? __uint_as_float(sr[j >> 5][j & 31]) * a.score_scale : -INFINITY;
         mx = fmaxf(mx, s[j]);
       }
-      const float m_new = fmaxf(m, mx);
-      const float alpha = ex2(m - m_new);
+      // the previous product of this tile X is done: P_X and O_X are free
+      if (n > 0 && !(ok = wait_all(bar(kBarO + x), (n - 1) & 1))) break;
+      tc::fence_after_sync();
+      const bool grow = mx > m + kRescaleAbove;
+      if (n == 0) {
+        m = mx;  // nothing accumulated yet
+      } else if (__any_sync(kFull, grow)) {
+        const float alpha = grow ? ex2(m - mx) : 1.f;
+#pragma unroll
+        for (int c0 = 0; c0 < kHd; c0 += 32) {
+          uint32_t ov[32];
+          tc::ld32_async(tO + c0, ov);
+          tc::wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+          tc::st32(tO + c0, ov);
+        }
+        tc::wait_st();
+        l *= alpha;
+        if (grow) m = mx;
+      }
       float sum = 0.f;
       uint32_t pk[kKv / 2];
 #pragma unroll
       for (int j = 0; j < kKv / 2; ++j) {
-        const float p0 = ex2(s[2 * j] - m_new), p1 = ex2(s[2 * j + 1] - m_new);
+        const float p0 = ex2(s[2 * j] - m), p1 = ex2(s[2 * j + 1] - m);
         sum += p0 + p1;
         pk[j] = pack16x2<kBf16>(p0, p1);
       }
-      l = l * alpha + sum;
-      m = m_new;
-      if (t0 < lo || t0 + kKv - 1 > hi) {
+      l += sum;
+      if (x == 0 && (t0 < lo || t0 + kKv - 1 > hi)) {
         // edge tile: once it has landed, zero the V rows outside [lo, hi]
-        ok = __all_sync(kFull, mbar_wait_bounded(bar(kBarFull + st), (n / kStages) & 1, kWaitNs));
-        if (!ok) break;
-        for (int i = r; i < kKv * 16; i += kSoftWarps * 32) {
+        if (!(ok = wait_all(bar(kBarFull + st), (n / kStages) & 1))) break;
+        for (int i = r; i < kKv * 16; i += kRows) {
           const int row = i >> 4, box = (i >> 3) & 1, ch = i & 7;
           const int pos = t0 + row;
           if (pos < lo || pos > hi)
-            sts_v4(sV + st * kKvBytes + box * 8192 + row * 128 + ch * 16, make_uint4(0u, 0u, 0u, 0u));
+            sts_v4(sV + st * kKvBytes + box * 8192 + row * 128 + ch * 16,
+                   make_uint4(0u, 0u, 0u, 0u));
         }
       }
 #pragma unroll
       for (int c = 0; c < 8; ++c)
-        sts_v4(sP + r * 128 + ((c ^ (r & 7)) << 4),
+        sts_v4(p_tile + r * 128 + ((c ^ (r & 7)) << 4),
                make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]));
       fence_proxy_async();  // P and the cleaned V rows, visible to the tensor core
       tc::fence_before_sync();
-      mbar_arrive(bar(kBarP));
-      ok = __all_sync(kFull, mbar_wait_bounded(bar(kBarO), n & 1, kWaitNs));
-      if (!ok) break;
-      tc::fence_after_sync();
-#pragma unroll
-      for (int c0 = 0; c0 < kHd; c0 += 32) {
-        float ot[32];
-        tc::ld32(trow + kColO + c0, ot);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) o[c0 + i] = o[c0 + i] * alpha + ot[i];
-      }
+      mbar_arrive(bar(kBarP + x));
     }
     if (!ok && lane == 0) atomicOr(a.err, PA_DEVERR_TIMEOUT);
-    if (valid) {
-      const float inv = l > 0.f ? 1.f / l : 0.f;
+    if (active) {
+      // the last product, then the output row
+      if (ok && ntiles > 0) ok = wait_all(bar(kBarO + x), (ntiles - 1) & 1);
+      tc::fence_after_sync();
+      const float inv = (ok && ntiles > 0 && l > 0.f) ? 1.f / l : 0.f;
       uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(a.out) + orow);
 #pragma unroll
-      for (int c = 0; c < 16; ++c)
-        dst[c] = make_uint4(pack16x2<kBf16>(o[8 * c] * inv, o[8 * c + 1] * inv),
-                            pack16x2<kBf16>(o[8 * c + 2] * inv, o[8 * c + 3] * inv),
-                            pack16x2<kBf16>(o[8 * c + 4] * inv, o[8 * c + 5] * inv),
-                            pack16x2<kBf16>(o[8 * c + 6] * inv, o[8 * c + 7] * inv));
+      for (int c0 = 0; c0 < kHd; c0 += 32) {
+        uint32_t ov[32];
+        if (ntiles > 0) {
+          tc::ld32_async(tO + c0, ov);
+          tc::wait_ld();
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) ov[i] = 0u;
+        }
+        if (valid) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const float* f = reinterpret_cast<const float*>(ov) + 8 * c;
+            dst[c0 / 8 + c] = make_uint4(pack16x2<kBf16>(f[0] * inv, f[1] * inv),
+                                         pack16x2<kBf16>(f[2] * inv, f[3] * inv),
+                                         pack16x2<kBf16>(f[4] * inv, f[5] * inv),
+                                         pack16x2<kBf16>(f[6] * inv, f[7] * inv));
+          }
+        }
+      }
     }
   }
 
-  // every MMA has completed (the softmax warps waited for the last one)
+  // every MMA has completed (each active group waited for its last product)
   tc::fence_before_sync();
   __syncthreads();
   if (warp == 0) {
@@ -347,6 +397,8 @@ cudaError_t launch_typed(const CUtensorMap& tk, const CUtensorMap& tv, const Chu
 }
 
 }  // namespace
+
+int chunk_tc_unit_rows() { return kUnitRows; }
 
 cudaError_t chunk_tc_prepare() {
   cudaError_t e = cudaFuncSetAttribute(chunk_attn_tc_kernel<kBF16>,

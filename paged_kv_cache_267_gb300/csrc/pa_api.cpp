@@ -767,7 +767,8 @@ pa_status run_chunk_tc(const DecodeCall& c, cudaStream_t cs) {
   a.MB = static_cast<int>(c.MB);
   a.NB = static_cast<int>(c.NB);
   a.window = c.window;
-  a.QT = static_cast<int>((c.T * c.G + 127) / 128);
+  const int unit = pa::chunk_tc_unit_rows();
+  a.QT = static_cast<int>((c.T * c.G + unit - 1) / unit);
   a.score_scale = static_cast<float>(static_cast<double>(c.scale) * 1.4426950408889634);
   const bool prof = g_prof_before && g_prof_after;
   cudaError_t e;

@@ -107,8 +107,8 @@ struct ReshapeArgs {
 };
 
 // Chunked queries on the tensor-memory kernel (chunk_tc.cu): one CTA per
-// (sequence, KV head, tile of 128 (query, head) rows); head dim 128, 16-bit
-// caches.
+// (sequence, KV head, unit of chunk_tc_unit_rows() (query, head) rows); head
+// dim 128, 16-bit caches.
 struct ChunkArgs {
   const void* q;                 // [B, T, Hq, D]
   void* out;                     // [B, T, Hq, D]
@@ -116,9 +116,10 @@ struct ChunkArgs {
   const int32_t* seq_lens;       // [B]
   int32_t* err;                  // device error word
   int B, T, Hq, Hkv, G, bs, MB, NB, window;
-  int QT;                        // row tiles per (sequence, KV head): ceil(T * G / 128)
+  int QT;                        // units per (sequence, KV head): ceil(T * G / unit rows)
   float score_scale;             // scale * log2(e)
 };
+int chunk_tc_unit_rows();
 cudaError_t chunk_tc_prepare();  // once per device: the kernel's shared-memory size
 cudaError_t chunk_tc_launch(int qt, const CUtensorMap& tk, const CUtensorMap& tv,
                             const ChunkArgs& a, cudaStream_t s, bool pdl);
