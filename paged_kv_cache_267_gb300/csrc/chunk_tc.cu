@@ -11,8 +11,9 @@
 // (four 16-token slices, each inside one physical block, fetched by TMA
 // through the block table), each shared by both row tiles.
 //
-// Roles: a control warp streams K/V tiles through a three-stage ring and
-// issues every MMA; two groups of four softmax warps (one row per thread)
+// Roles: a producer warp streams K/V tiles through a three-stage ring (block
+// table lookups and TMA), an MMA warp issues every product, and two groups
+// of four softmax warps (one row per thread)
 // serve tiles A and B, so the tensor core works for one group while the
 // other runs its softmax. Per K/V tile n and row tile X:
 //   S_X  = Q_X . K_n^T        tcgen05.mma M128 N64  K128 -> TMEM
@@ -44,8 +45,9 @@ constexpr int kKv = 64;         // tokens per K/V tile
 constexpr int kHd = 128;        // head dim
 constexpr int kStages = 3;      // K/V ring depth
 constexpr int kGroupWarps = 4;  // softmax warps per row tile
-constexpr int kCtrlWarp = 2 * kGroupWarps;
-constexpr int kThreads = (kCtrlWarp + 1) * 32;
+constexpr int kCtrlWarp = 2 * kGroupWarps;  // issues the MMAs
+constexpr int kLoadWarp = kCtrlWarp + 1;     // streams K/V tiles
+constexpr int kThreads = (kLoadWarp + 1) * 32;
 constexpr uint32_t kQBytes = kRows * kHd * 2;   // per row tile: [2 boxes][128 rows][128 B]
 constexpr uint32_t kKvBytes = kKv * kHd * 2;    // [2 boxes][64 rows][128 B]
 constexpr uint32_t kPBytes = kRows * kKv * 2;   // per row tile: [128 rows][128 B]
@@ -149,8 +151,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lo16 = lo & ~15;
   const int ntiles = hi >= lo ? (hi + 1 - lo16 + kKv - 1) / kKv : 0;
 
-  if (warp == kCtrlWarp) {
-    // ------------------------------------------------------------ control
+  if (warp == kLoadWarp) {
+    // ------------------------------------------------------------ producer
     // Loads K/V tile n into `stage`: lanes 0..3 each look up one 16-token
     // slice in the block table and copy it (two 64-dim boxes of K and of V).
     auto load_tile = [&](int n, int stage) {
@@ -178,6 +180,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       __syncwarp();
     };
+    bool ok = true;
+    for (int n = 0; n < ntiles; ++n) {
+      const int st = n % kStages;
+      if (n >= kStages && !(ok = wait_all(bar(kBarEmpty + st), ((n - kStages) / kStages) & 1)))
+        break;
+      load_tile(n, st);
+    }
+    if (!ok && lane == 0) atomicOr(a.err, PA_DEVERR_TIMEOUT);
+  } else if (warp == kCtrlWarp) {
+    // ------------------------------------------------------------ MMA issue
     constexpr uint32_t idS = tc::idesc_f16(kRows, kKv, kBf16, false);
     constexpr uint32_t idO = tc::idesc_f16(kRows, kHd, kBf16, true);
     // S_X = Q_X . K_n^T over the 128 head dims (8 steps of 16)
@@ -210,7 +222,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
     };
     bool ok = true;
-    for (int i = 0; i < kStages && i < ntiles; ++i) load_tile(i, i);
     if (ntiles > 0) {
       ok = wait_all(bar(kBarQ), 0) && wait_all(bar(kBarFull), 0);
       if (ok) {
@@ -238,10 +249,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) tc::commit(bar(kBarEmpty + st));  // both products of tile n issued
       __syncwarp();
       if (hasB && more) issue_s(1, n + 1);
-      if (n + kStages < ntiles) {
-        if (!(ok = wait_all(bar(kBarEmpty + st), (n / kStages) & 1))) break;
-        load_tile(n + kStages, st);
-      }
     }
     if (!ok && lane == 0) atomicOr(a.err, PA_DEVERR_TIMEOUT);
   } else {
