@@ -291,13 +291,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::wait_ld();
       float s[kKv];
       const bool inside = t0 >= lo_r && t0 + kKv - 1 <= hi_r;
-      float mx = kFloor;
+      float mxp[8];  // eight independent partial maxima: short dependency chains
 #pragma unroll
-      for (int j = 0; j < kKv; ++j) {
-        const bool keep = inside || (t0 + j >= lo_r && t0 + j <= hi_r);
-        s[j] = keep ? __uint_as_float(sr[j >> 5][j & 31]) * a.score_scale : -INFINITY;
-        mx = fmaxf(mx, s[j]);
+      for (int i = 0; i < 8; ++i) mxp[i] = kFloor;
+      if (inside) {
+#pragma unroll
+        for (int j = 0; j < kKv; ++j) {
+          s[j] = __uint_as_float(sr[j >> 5][j & 31]) * a.score_scale;
+          mxp[j & 7] = fmaxf(mxp[j & 7], s[j]);
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < kKv; ++j) {
+          const bool keep = t0 + j >= lo_r && t0 + j <= hi_r;
+          s[j] = keep ? __uint_as_float(sr[j >> 5][j & 31]) * a.score_scale : -INFINITY;
+          mxp[j & 7] = fmaxf(mxp[j & 7], s[j]);
+        }
       }
+      const float mx = fmaxf(fmaxf(fmaxf(mxp[0], mxp[1]), fmaxf(mxp[2], mxp[3])),
+                             fmaxf(fmaxf(mxp[4], mxp[5]), fmaxf(mxp[6], mxp[7])));
       // the previous product of this tile X is done: P_X and O_X are free
       if (n > 0 && !(ok = wait_all(bar(kBarO + x), (n - 1) & 1))) break;
       tc::fence_after_sync();
@@ -319,15 +331,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         l *= alpha;
         if (grow) m = mx;
       }
-      float sum = 0.f;
+      float sp[8];  // eight independent partial sums
+#pragma unroll
+      for (int i = 0; i < 8; ++i) sp[i] = 0.f;
       uint32_t pk[kKv / 2];
 #pragma unroll
       for (int j = 0; j < kKv / 2; ++j) {
         const float p0 = ex2(s[2 * j] - m), p1 = ex2(s[2 * j + 1] - m);
-        sum += p0 + p1;
+        sp[j & 7] += p0 + p1;
         pk[j] = pack16x2<kBf16>(p0, p1);
       }
-      l += sum;
+      l += ((sp[0] + sp[1]) + (sp[2] + sp[3])) + ((sp[4] + sp[5]) + (sp[6] + sp[7]));
       if (x == 0 && (t0 < lo || t0 + kKv - 1 > hi)) {
         // edge tile: once it has landed, zero the V rows outside [lo, hi]
         if (!(ok = wait_all(bar(kBarFull + st), (n / kStages) & 1))) break;
