@@ -22,9 +22,15 @@
  *     thread is available from pa_last_error(). No C++ exception crosses the
  *     ABI. Host-detectable errors are reported before anything is launched.
  *   - Tensors are described by pa_tensor: data pointer, dtype, rank, shape and
- *     strides in elements. Device tensors must live in memory of the current
- *     CUDA device. The caller owns every tensor; the library keeps no pointer
- *     to them after the call returns.
+ *     strides in elements. A tensor lives in memory of the current CUDA device,
+ *     or in pinned host memory mapped into the device's address space at the
+ *     same address (cudaHostAlloc / cudaHostRegister with mapping, as every
+ *     pinned allocation is under unified addressing); the kernels then read or
+ *     write it in place over the CPU-GPU link, which on GB300 saves the copy
+ *     engine's per-copy latency for a step's small inputs and outputs. Any
+ *     other pointer (pageable host memory, another device) is rejected with
+ *     PA_ERR_INVALID_ARG before launch. The caller owns every tensor; the
+ *     library keeps no pointer to them after the call returns.
  *   - Launches are asynchronous on the given stream (a cudaStream_t; NULL is
  *     the legacy default stream). No entry point synchronises the stream
  *     except pa_check_device_error().

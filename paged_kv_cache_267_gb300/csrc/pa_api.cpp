@@ -118,6 +118,27 @@ pa_status check_tensor(const pa_tensor* t, const char* name, int ndim) {
   return PA_OK;
 }
 
+// The kernels may only touch memory of the current device, or pinned host
+// memory mapped into its address space at the same address (on GB300 the
+// kernels then read and write it over the CPU-GPU link). Anything else
+// (pageable host memory, another device's memory) is rejected before launch.
+pa_status check_accessible(const pa_tensor* t, const char* name) {
+  if (!t || numel(t) == 0 || !t->data) return PA_OK;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  cudaPointerAttributes at;
+  e = cudaPointerGetAttributes(&at, t->data);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaPointerGetAttributes");
+  if ((at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged) && at.device == dev)
+    return PA_OK;
+  if (at.type == cudaMemoryTypeHost && at.devicePointer == t->data) return PA_OK;
+  return fail(PA_ERR_INVALID_ARG,
+              "%s: memory not accessible from the current device (use device memory or pinned, "
+              "mapped host memory)",
+              name);
+}
+
 // ------------------------------------------------------------ device state
 
 struct Workspace {
@@ -513,6 +534,11 @@ pa_status pa_reshape_and_cache(const pa_tensor* k, const pa_tensor* v, const pa_
     return fail(PA_ERR_INVALID_ARG, "key and value caches alias");
   if (T > (int64_t(1) << 30) || H > 65535) return fail(PA_ERR_UNSUPPORTED, "too many tokens/heads");
   if (T == 0 || H == 0) return ok();
+  if ((s = check_accessible(k, "k")) || (s = check_accessible(v, "v")) ||
+      (s = check_accessible(key_cache, "key_cache")) ||
+      (s = check_accessible(value_cache, "value_cache")) ||
+      (s = check_accessible(slot_mapping, "slot_mapping")))
+    return s;
 
   DeviceState* st;
   {
@@ -629,6 +655,12 @@ pa_status check_decode(const pa_tensor* out, const pa_tensor* q, const pa_tensor
     return fail(PA_ERR_UNSUPPORTED, "batch * num_q_heads * num_queries too large");
   if (B > 0 && MB == 0) return fail(PA_ERR_INVALID_ARG, "block_tables has no columns");
   if (B > 0 && NB == 0) return fail(PA_ERR_INVALID_ARG, "empty block pool");
+  if (B > 0 && ((s = check_accessible(out, "out")) || (s = check_accessible(q, "q")) ||
+                (s = check_accessible(key_cache, "key_cache")) ||
+                (s = check_accessible(value_cache, "value_cache")) ||
+                (s = check_accessible(block_tables, "block_tables")) ||
+                (s = check_accessible(seq_lens, "seq_lens"))))
+    return s;
   *c = DecodeCall{out, q, key_cache, value_cache, block_tables, seq_lens, B, T, Hq, Hkv, D, NB,
                   MB, G, CG, NCG, static_cast<int>(Hv), block_size, window > 0 ? window : 0,
                   fp8, fp8 ? pa::kE4M3 : (q->dtype == PA_BF16 ? pa::kBF16 : pa::kF16),

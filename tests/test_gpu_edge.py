@@ -341,3 +341,37 @@ def test_prefix_cached_requests_write_only_uncached_rows(pa_lib):
     ref = oracle.decode(q.cpu(), host_copy(kc), host_copy(vc), tables, lens, num_kv_heads=Hkv,
                         scale=D ** -0.5, block_size=bs, q_dtype="bf16", cache_dtype="bf16")
     assert_close(out_f64(out), ref, what="prefix-cached requests")
+
+
+def test_pinned_host_tensors_are_read_and_written_in_place(pa_lib):
+    """The step's small inputs (new k/v, slots, q, tables, lengths) and the
+    output in pinned host memory: the kernels use them in place, with results
+    identical to the device-memory call; pageable host memory is refused
+    before anything is launched."""
+    s = spec(seq_lens=(300, 17, 1, 2000, 0, 64))
+    kw = dict(num_kv_heads=2, scale=s.softmax_scale, block_size=16)
+    pa_lib.set_decode_tuning(pool_permille=-1)
+    try:
+        outs = []
+        for pinned in (False, True):
+            w = generate(s, device="cuda")
+            bt = torch.from_numpy(w.block_tables).cuda()
+            sl = torch.from_numpy(w.seq_lens).cuda()
+            args = [w.k_new, w.v_new, w.slot_new, w.q, bt, sl]
+            if pinned:
+                args = [t.cpu().pin_memory() for t in args]
+                out = torch.empty(w.q.shape, dtype=w.q.dtype, pin_memory=True)
+            else:
+                out = torch.empty_like(w.q)
+            k, v, slot, q, btx, slx = args
+            pa_lib.reshape_and_cache(k, v, w.key_cache, w.value_cache, slot)
+            pa_lib.decode(q, w.key_cache, w.value_cache, btx, slx, out=out, **kw)
+            torch.cuda.synchronize()
+            outs.append(out.cpu())
+        assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
+        with pytest.raises(pa_lib.PAError) as e:
+            pa_lib.decode(w.q.cpu(), w.key_cache, w.value_cache, bt, sl, **kw)
+        assert e.value.status == -1 and "not accessible" in str(e.value)
+    finally:
+        pa_lib.set_decode_tuning()
+    assert pa_lib.check_device_error() == 0
