@@ -235,7 +235,7 @@ pa_status pa_prefill_chunk(const pa_tensor* out, const pa_tensor* q, const pa_te
  * columns per pass over K/V, any head dim, FP8 caches); 2 uses the
  * tensor-memory kernel wherever it applies (16-bit caches, head_dim 128),
  * which tiles 128 (query, head) rows against 64-token K/V tiles on the
- * tcgen05 tensor cores and reads each K/V tile once per 128 rows. The
+ * tcgen05 tensor cores and reads each K/V tile once per 256 rows. The
  * default takes the tensor-memory kernel for chunks of more than 32 (query,
  * head) columns per KV head. */
 pa_status pa_set_prefill_path(int32_t path);
