@@ -51,6 +51,8 @@
 // are folded into the score scale and the partial outputs.
 #pragma once
 
+#include <type_traits>
+
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -604,54 +606,72 @@ __global__ void __launch_bounds__(WARPS * 32, 2)
       pb[nt][1] = movmatrix_trans(pack2<kBf16Mma>(p2v, p3v));
     }
 
-    // ---- O^T += V^T . P^T
-    uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;
-    if (edge) {
-      mlo = (valid(2 * t4) ? 0x0000ffffu : 0u) | (valid(2 * t4 + 1) ? 0xffff0000u : 0u);
-      mhi = (valid(2 * t4 + 8) ? 0x0000ffffu : 0u) | (valid(2 * t4 + 9) ? 0xffff0000u : 0u);
-    }
-    if constexpr (!kFp8) {
-#pragma unroll
-      for (int mt = 0; mt < MT; ++mt) {
-        uint32_t a0, a1, a2, a3;
-        ldsm_x4_trans(vt + tile_off((lane & 7) + ((lane >> 4) << 3), 2 * mt + ((lane >> 3) & 1)),
-                      a0, a1, a2, a3);
-        a0 &= mlo;
-        a1 &= mlo;
-        a2 &= mhi;
-        a3 &= mhi;
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-          mma_16816<kBf16Mma>(acc[mt][nt], a0, a1, a2, a3, pb[nt][0], pb[nt][1]);
+    // ---- O^T += V^T . P^T (the V rows of positions outside [start, L) are
+    // zeroed in edge tiles only; interior tiles skip the masking work)
+    auto pv = [&](auto masked) {
+      constexpr bool kMask = decltype(masked)::value;
+      uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;
+      if constexpr (kMask) {
+        mlo = (valid(2 * t4) ? 0x0000ffffu : 0u) | (valid(2 * t4 + 1) ? 0xffff0000u : 0u);
+        mhi = (valid(2 * t4 + 8) ? 0x0000ffffu : 0u) | (valid(2 * t4 + 9) ? 0xffff0000u : 0u);
       }
-    } else {
+      if constexpr (!kFp8) {
 #pragma unroll
-      for (int u = 0; u < D / 32; ++u) {
-        const int dby = 32 * u + 4 * g;  // byte (= element) offset in the row
-        const uint32_t co = (dby & 15);
-        const int c = dby >> 4;
-        const uint32_t w0 = lds_b32(vt + tile_off(2 * t4, c) + co);
-        const uint32_t w1 = lds_b32(vt + tile_off(2 * t4 + 1, c) + co);
-        const uint32_t w8 = lds_b32(vt + tile_off(2 * t4 + 8, c) + co);
-        const uint32_t w9 = lds_b32(vt + tile_off(2 * t4 + 9, c) + co);
-        const uint32_t x01a = __byte_perm(w0, w1, 0x5140), x01b = __byte_perm(w0, w1, 0x7362);
-        const uint32_t x89a = __byte_perm(w8, w9, 0x5140), x89b = __byte_perm(w8, w9, 0x7362);
-        // m-tile 2u: rows g, g+8 hold dims dby, dby+1; m-tile 2u+1: dby+2, dby+3
-        const uint32_t e0 = e4m3x2_to_f16x2(static_cast<uint16_t>(x01a & 0xffffu)) & mlo;
-        const uint32_t e1 = e4m3x2_to_f16x2(static_cast<uint16_t>(x01a >> 16)) & mlo;
-        const uint32_t e2 = e4m3x2_to_f16x2(static_cast<uint16_t>(x89a & 0xffffu)) & mhi;
-        const uint32_t e3 = e4m3x2_to_f16x2(static_cast<uint16_t>(x89a >> 16)) & mhi;
-        const uint32_t f0v = e4m3x2_to_f16x2(static_cast<uint16_t>(x01b & 0xffffu)) & mlo;
-        const uint32_t f1v = e4m3x2_to_f16x2(static_cast<uint16_t>(x01b >> 16)) & mlo;
-        const uint32_t f2v = e4m3x2_to_f16x2(static_cast<uint16_t>(x89b & 0xffffu)) & mhi;
-        const uint32_t f3v = e4m3x2_to_f16x2(static_cast<uint16_t>(x89b >> 16)) & mhi;
+        for (int mt = 0; mt < MT; ++mt) {
+          uint32_t a0, a1, a2, a3;
+          ldsm_x4_trans(vt + tile_off((lane & 7) + ((lane >> 4) << 3), 2 * mt + ((lane >> 3) & 1)),
+                        a0, a1, a2, a3);
+          if constexpr (kMask) {
+            a0 &= mlo;
+            a1 &= mlo;
+            a2 &= mhi;
+            a3 &= mhi;
+          }
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          mma_16816<false>(acc[2 * u][nt], e0, e1, e2, e3, pb[nt][0], pb[nt][1]);
-          mma_16816<false>(acc[2 * u + 1][nt], f0v, f1v, f2v, f3v, pb[nt][0], pb[nt][1]);
+          for (int nt = 0; nt < NT; ++nt)
+            mma_16816<kBf16Mma>(acc[mt][nt], a0, a1, a2, a3, pb[nt][0], pb[nt][1]);
+        }
+      } else {
+#pragma unroll
+        for (int u = 0; u < D / 32; ++u) {
+          const int dby = 32 * u + 4 * g;  // byte (= element) offset in the row
+          const uint32_t co = (dby & 15);
+          const int c = dby >> 4;
+          const uint32_t w0 = lds_b32(vt + tile_off(2 * t4, c) + co);
+          const uint32_t w1 = lds_b32(vt + tile_off(2 * t4 + 1, c) + co);
+          const uint32_t w8 = lds_b32(vt + tile_off(2 * t4 + 8, c) + co);
+          const uint32_t w9 = lds_b32(vt + tile_off(2 * t4 + 9, c) + co);
+          const uint32_t x01a = __byte_perm(w0, w1, 0x5140), x01b = __byte_perm(w0, w1, 0x7362);
+          const uint32_t x89a = __byte_perm(w8, w9, 0x5140), x89b = __byte_perm(w8, w9, 0x7362);
+          // m-tile 2u: rows g, g+8 hold dims dby, dby+1; m-tile 2u+1: dby+2, dby+3
+          uint32_t e0 = e4m3x2_to_f16x2(static_cast<uint16_t>(x01a & 0xffffu));
+          uint32_t e1 = e4m3x2_to_f16x2(static_cast<uint16_t>(x01a >> 16));
+          uint32_t e2 = e4m3x2_to_f16x2(static_cast<uint16_t>(x89a & 0xffffu));
+          uint32_t e3 = e4m3x2_to_f16x2(static_cast<uint16_t>(x89a >> 16));
+          uint32_t f0v = e4m3x2_to_f16x2(static_cast<uint16_t>(x01b & 0xffffu));
+          uint32_t f1v = e4m3x2_to_f16x2(static_cast<uint16_t>(x01b >> 16));
+          uint32_t f2v = e4m3x2_to_f16x2(static_cast<uint16_t>(x89b & 0xffffu));
+          uint32_t f3v = e4m3x2_to_f16x2(static_cast<uint16_t>(x89b >> 16));
+          if constexpr (kMask) {
+            e0 &= mlo;
+            e1 &= mlo;
+            e2 &= mhi;
+            e3 &= mhi;
+            f0v &= mlo;
+            f1v &= mlo;
+            f2v &= mhi;
+            f3v &= mhi;
+          }
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            mma_16816<false>(acc[2 * u][nt], e0, e1, e2, e3, pb[nt][0], pb[nt][1]);
+            mma_16816<false>(acc[2 * u + 1][nt], f0v, f1v, f2v, f3v, pb[nt][0], pb[nt][1]);
+          }
         }
       }
-    }
+    };
+    if (edge) pv(std::true_type{});
+    else pv(std::false_type{});
     __syncwarp();
     ++consumed;
     // refill the stage just consumed
