@@ -150,3 +150,71 @@ def test_chunk_kernels_forced(case, path, pa_lib):
             if L - T + t < 0:
                 assert (got[b, t] == 0).all()
     assert pa_lib.check_device_error() == 0
+
+
+@pytest.mark.parametrize("path", [1, 2], ids=["persistent", "tensor_memory"])
+def test_chunk_bad_block_id_and_long_seq_are_flagged_not_faulted(path, pa_lib):
+    """Device-side data errors in a chunk call: a block id outside the pool and
+    a length beyond the table set their error bits; the kernels substitute a
+    safe block / clamp the length instead of reading out of bounds."""
+    import paged_kv_cache_267_gb300 as pa
+    from workloads import generate
+    w = generate(_spec(40, 8, 2, 128, 16, 0, "bf16", False, lens=(120, 300, 77)), device="cuda")
+    s = w.spec
+    bt = torch.from_numpy(w.block_tables).cuda()
+    sl = torch.from_numpy(w.seq_lens).cuda()
+    kw = dict(num_kv_heads=2, scale=s.softmax_scale, block_size=16)
+    assert pa_lib.check_device_error() == 0
+    pa_lib.set_prefill_path(path)
+    try:
+        for bad in (w.num_blocks + 5, -3):
+            bt_bad = bt.clone()
+            bt_bad[1, 2] = bad
+            pa.prefill_chunk(w.q, w.key_cache, w.value_cache, bt_bad, sl, **kw)
+            assert pa_lib.check_device_error() & pa_lib.DEVERR_BLOCK_ID
+            assert pa_lib.check_device_error() == 0
+        sl_bad = sl.clone()
+        sl_bad[0] = w.max_blocks * 16 + 9
+        pa.prefill_chunk(w.q, w.key_cache, w.value_cache, bt, sl_bad, **kw)
+        assert pa_lib.check_device_error() & pa_lib.DEVERR_SEQ_LEN
+    finally:
+        pa_lib.set_prefill_path(0)
+
+
+@pytest.mark.parametrize("path", [1, 2], ids=["persistent", "tensor_memory"])
+def test_chunk_step_replays_from_a_cuda_graph(path, pa_lib):
+    """The chunk step (write path + pa_prefill_chunk) captured in one CUDA
+    graph and replayed gives the eager result (the persistent kernel with the
+    dynamic pool off, the tensor-memory kernel as it is: both repeat bit for
+    bit)."""
+    import paged_kv_cache_267_gb300 as pa
+    from workloads import generate
+    w = generate(_spec(48, 8, 2, 128, 16, 0, "bf16", False, lens=(300, 60, 1000)), device="cuda")
+    s = w.spec
+    bt = torch.from_numpy(w.block_tables).cuda()
+    sl = torch.from_numpy(w.seq_lens).cuda()
+    kw = dict(num_kv_heads=2, scale=s.softmax_scale, block_size=16)
+    out = torch.empty_like(w.q)
+    stream = torch.cuda.Stream()
+    pa_lib.set_prefill_path(path)
+    pa_lib.set_decode_tuning(pool_permille=-1)
+    try:
+        def step():
+            pa.reshape_and_cache(w.k_new, w.v_new, w.key_cache, w.value_cache, w.slot_new)
+            pa.prefill_chunk(w.q, w.key_cache, w.value_cache, bt, sl, out=out, **kw)
+        with torch.cuda.stream(stream):
+            step()
+        stream.synchronize()
+        eager = out.clone()
+        out.zero_()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            step()
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out.view(torch.int16), eager.view(torch.int16))
+    finally:
+        pa_lib.set_prefill_path(0)
+        pa_lib.set_decode_tuning()
+    assert pa_lib.check_device_error() == 0
