@@ -566,6 +566,10 @@ __global__ void __launch_bounds__(WARPS * 32, 2)
     // chunked: does some column's own range cut this tile?
     const bool cedge = MQ && (p0 < lo_max || p0 + kTile - 1 > hi_min);
     uint32_t pb[NT][2];
+    // bf16 caches: P is split into a bf16 high part and a bf16 remainder, and
+    // P.V runs on both, so P enters the product with ~16 bits instead of 8
+    // (f16 P, used with f16 and FP8 caches, already has 11)
+    uint32_t pr[NT][2];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       float s0, s1, s2, s3;
@@ -602,6 +606,13 @@ __global__ void __launch_bounds__(WARPS * 32, 2)
         acc[mt][nt][2] *= al0;
         acc[mt][nt][3] *= al1;
       }
+      if constexpr (kBf16Mma) {
+        const uint32_t h01 = pack2<true>(p0v, p1v), h23 = pack2<true>(p2v, p3v);
+        pr[nt][0] = movmatrix_trans(pack2<true>(p0v - __uint_as_float(h01 << 16),
+                                                p1v - __uint_as_float(h01 & 0xffff0000u)));
+        pr[nt][1] = movmatrix_trans(pack2<true>(p2v - __uint_as_float(h23 << 16),
+                                                p3v - __uint_as_float(h23 & 0xffff0000u)));
+      }
       pb[nt][0] = movmatrix_trans(pack2<kBf16Mma>(p0v, p1v));
       pb[nt][1] = movmatrix_trans(pack2<kBf16Mma>(p2v, p3v));
     }
@@ -629,7 +640,11 @@ __global__ void __launch_bounds__(WARPS * 32, 2)
           }
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt)
+          {
             mma_16816<kBf16Mma>(acc[mt][nt], a0, a1, a2, a3, pb[nt][0], pb[nt][1]);
+            if constexpr (kBf16Mma)
+              mma_16816<true>(acc[mt][nt], a0, a1, a2, a3, pr[nt][0], pr[nt][1]);
+          }
         }
       } else {
 #pragma unroll

@@ -218,3 +218,23 @@ def test_chunk_step_replays_from_a_cuda_graph(path, pa_lib):
         pa_lib.set_prefill_path(0)
         pa_lib.set_decode_tuning()
     assert pa_lib.check_device_error() == 0
+
+
+@pytest.mark.parametrize("path", [1, 2], ids=["persistent", "tensor_memory"])
+def test_maximum_chunk(path, pa_lib):
+    """T = 4096 queries (the library's limit) on one sequence of 4200
+    positions: 16384 (query, head) rows per KV head; sampled rows against the
+    oracle."""
+    spec = _spec(4096, 8, 2, 128, 16, 0, "bf16", False, lens=(4200,), seed=2701)
+    rng = np.random.default_rng(9)
+    tr = np.stack([np.zeros(256, np.int64), rng.integers(0, 4096, 256), rng.integers(0, 8, 256)], 1)
+    pa_lib.set_prefill_path(path)
+    try:
+        sides = run_chunk(spec, triples=tr)
+    finally:
+        pa_lib.set_prefill_path(0)
+    assert pa_lib.check_device_error() == 0
+    idx = tuple(tr.T)
+    got = out_f64(sides.out)
+    assert np.isfinite(got).all()
+    assert_close(got[idx], sides.ref[idx], what=f"T=4096 path {path}", rel=CHUNK_REL_TOL)

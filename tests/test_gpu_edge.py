@@ -375,3 +375,30 @@ def test_pinned_host_tensors_are_read_and_written_in_place(pa_lib):
     finally:
         pa_lib.set_decode_tuning()
     assert pa_lib.check_device_error() == 0
+
+
+def test_maximum_batch(pa_lib):
+    """B = 4096, the library's limit: the planning prologue holds per-sequence
+    prefixes of 4097 entries in shared memory (fewer CTAs fit per SM) and the
+    merge one unit per q head; B = 4097 is refused on the host."""
+    rng = np.random.default_rng(77)
+    lens = tuple(int(x) for x in rng.integers(0, 49, 4096))
+    s = spec(seq_lens=lens, seed=4343)
+    sides = run_both(s)
+    assert_caches_equal(sides, "max batch")
+    # Thousands of 1..48-token spans give some outputs of magnitude 4 or more
+    # (nearly single V rows); bf16 spaces such values 2^-5 apart, so rounding
+    # the output alone can cost 1.56e-2. Below 4 the plain bar holds; above,
+    # the bar plus the output's own half-spacing.
+    got = out_f64(sides.out)
+    small = np.abs(sides.ref) < 4.0
+    assert_close(got[small], sides.ref[small], what="max batch, |out| < 4")
+    assert_close(got, sides.ref, what="max batch", rel=2.0 ** -8)
+    assert pa_lib.check_device_error() == 0
+    w = sides.w
+    q = torch.zeros((4097,) + tuple(w.q.shape[1:]), dtype=w.q.dtype, device="cuda")
+    bt = torch.zeros((4097, w.block_tables.shape[1]), dtype=torch.int32, device="cuda")
+    sl = torch.zeros(4097, dtype=torch.int32, device="cuda")
+    with pytest.raises(pa_lib.PAError) as e:
+        pa_lib.decode(q, sides.kc, sides.vc, bt, sl, num_kv_heads=2, scale=0.1, block_size=16)
+    assert e.value.status == -2
