@@ -4,12 +4,13 @@
 // owns the 16-token tiles that cover its attended positions [start, L); tiles
 // never straddle a physical block because block_size is a multiple of 16.
 // All tiles of all pairs form one flat index space (pair-major). The first
-// part of it (about 80%) is split into equal contiguous static ranges, one per
+// part of it (about 90%) is split into equal contiguous static ranges, one per
 // worker warp; the rest is a pool of small pieces that warps claim with one
 // atomicAdd each once their static range is done (the claim for the next
 // piece is issued a piece ahead, so the copy pipeline never drains). Warps on
 // SMs that get less bandwidth thus take fewer pieces and all warps finish
-// together. A run of one warp's tiles inside one pair is a segment; each
+// together. The pool only covers the trailing run of sequences no longer than
+// four times the mean, so a long sequence is never cut into small pieces. A run of one warp's tiles inside one pair is a segment; each
 // segment writes one partial (running max m, running sum l, unnormalised
 // output) to a slot fixed by arithmetic: pair + warp for static segments,
 // pair + piece (in a second region) for pool segments -- unique because the
@@ -30,13 +31,15 @@
 //   online softmax on S in the log2 domain (scale * log2 e folded in)
 //   O^T[D x 8 heads] += V^T[D x 16 tok] . P^T[16 x 8]  (P^T via movmatrix)
 // i.e. the block-wise scaled dot product, max/sum state and V-weighted sum of
-// "vLLM 0.5 深度解析" §2.3, done in one pass. Positions outside [start, L) in
-// the first and last tile of a pair get score -inf and their V rows are
-// zeroed in the fragment, so poisoned slots never reach the result.
+// "vLLM 0.5 深度解析" §2.3, done in one pass. With bf16 caches P enters P.V
+// as a bf16 high part plus a bf16 remainder (two mma), about 16 bits. Positions
+// outside [start, L) in the first and last tile of a pair get score -inf and
+// their V rows are zeroed in the fragment, so poisoned slots never reach the
+// result.
 //
 // Chunked queries (MQ = true). A sequence may bring T query tokens at its
 // last T positions, each attending causally to its own prefix (clipped by
-// the window), as in the chunked prefill of "vLLM 0.7.2深度解析". The mma
+// the window), as in the chunked prefill of "vLLM 0.5 深度解析" §5.2. The mma
 // n-columns of a pair are then (query, head) columns c = t * G + h, at most
 // 16 per pair; with more, the columns are cut into NCG groups of 16 and each
 // group is a pair of its own (a "virtual" KV head vh = kvh * NCG + group), so
