@@ -27,8 +27,15 @@
 // next product, so P stays below 2^8 and most tiles never touch O. V rows of
 // an edge tile that lie outside [lo, hi] (not loaded, or NaN-poisoned slots
 // past the sequence or before the window) are zeroed in shared memory before
-// the products, so only attended rows reach the tensor core. Head dim 128,
-// f16 or bf16 caches.
+// the products, so only attended rows reach the tensor core. Head dim 128.
+//
+// FP8 e4m3 caches (FP8 = true): the ring holds the raw e4m3 tiles (8 KB of K
+// and of V per tile), and two converter warps turn each into f16 tiles of the
+// same swizzled layouts (exact), in a double buffer the products read; they
+// write zeros for the V rows outside [lo, hi]. Q is converted per row to f16
+// after a power-of-two rescale that brings its largest magnitude into
+// [2^14, 2^15); the rescale and k_scale fold into the row's score scale, and
+// v_scale is applied to the output.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -47,19 +54,33 @@ constexpr int kStages = 3;      // K/V ring depth
 constexpr int kGroupWarps = 4;  // softmax warps per row tile
 constexpr int kCtrlWarp = 2 * kGroupWarps;  // issues the MMAs
 constexpr int kLoadWarp = kCtrlWarp + 1;     // streams K/V tiles
-constexpr int kThreads = (kLoadWarp + 1) * 32;
+constexpr int kConvWarp0 = kLoadWarp + 1;    // FP8: e4m3 -> f16 converters
+constexpr int kConvWarps = 2;
 constexpr uint32_t kQBytes = kRows * kHd * 2;   // per row tile: [2 boxes][128 rows][128 B]
-constexpr uint32_t kKvBytes = kKv * kHd * 2;    // [2 boxes][64 rows][128 B]
+constexpr uint32_t kKvBytes = kKv * kHd * 2;    // 16-bit tile: [2 boxes][64 rows][128 B]
+constexpr uint32_t kRawBytes = kKv * kHd;       // e4m3 tile: [64 rows][128 B]
 constexpr uint32_t kPBytes = kRows * kKv * 2;   // per row tile: [128 rows][128 B]
-constexpr uint32_t kOffQ = 0;                   // Q_A, Q_B
-constexpr uint32_t kOffK = kOffQ + 2 * kQBytes;
-constexpr uint32_t kOffV = kOffK + kStages * kKvBytes;
-constexpr uint32_t kOffP = kOffV + kStages * kKvBytes;  // P_A, P_B
-constexpr uint32_t kOffBar = kOffP + 2 * kPBytes;
 constexpr int kBarFull = 0, kBarEmpty = kStages, kBarS = 2 * kStages,  // S_A, S_B
-    kBarP = kBarS + 2, kBarO = kBarS + 4, kBarQ = kBarS + 6, kNumBars = kBarS + 7;
-constexpr uint32_t kOffSlot = kOffBar + 8 * kNumBars;
-constexpr uint32_t kSmemBytes = kOffSlot + 16 + 1024;  // + room to align the base to 1 KB
+    kBarP = kBarS + 2, kBarO = kBarS + 4, kBarQ = kBarS + 6,
+    kBarCFull = kBarS + 7, kBarCEmpty = kBarS + 9,  // FP8: converted buffers 0, 1
+    kNumBars = kBarS + 11;
+
+// Shared-memory layout: Q_A, Q_B, the ring, (FP8: the converted double
+// buffer of K and V), P_A, P_B, barriers, the tensor-memory address.
+template <bool FP8>
+struct Smem {
+  static constexpr uint32_t kThreads = (kConvWarp0 + (FP8 ? kConvWarps : 0)) * 32;
+  static constexpr uint32_t kTileK = FP8 ? kRawBytes : kKvBytes;  // one ring tile of K (or V)
+  static constexpr uint32_t kQ = 0;
+  static constexpr uint32_t kK = kQ + 2 * kQBytes;               // ring: K tiles
+  static constexpr uint32_t kV = kK + kStages * kTileK;          // ring: V tiles
+  static constexpr uint32_t kKc = kV + kStages * kTileK;         // FP8: f16 K tiles [2]
+  static constexpr uint32_t kVc = kKc + (FP8 ? 2 * kKvBytes : 0);
+  static constexpr uint32_t kP = kVc + (FP8 ? 2 * kKvBytes : 0);
+  static constexpr uint32_t kBar = kP + 2 * kPBytes;
+  static constexpr uint32_t kSlot = kBar + 8 * kNumBars;
+  static constexpr uint32_t kBytes = kSlot + 16 + 1024;  // + room to align the base to 1 KB
+};
 constexpr uint32_t kTmemCols = 512;  // S_A [0,64) S_B [64,128) O_A [128,256) O_B [256,384)
 constexpr uint32_t kColS = 0, kColO = 128;
 constexpr uint64_t kWaitNs = 2000000000ull;  // bound of every wait (2 s)
@@ -94,17 +115,30 @@ __device__ __forceinline__ bool wait_all(uint32_t bar, uint32_t parity) {
   return __all_sync(kFull, mbar_wait_bounded(bar, parity, kWaitNs));
 }
 
-template <int QT>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int QT, bool FP8>
+__global__ void __launch_bounds__(Smem<FP8>::kThreads, 1)
     chunk_attn_tc_kernel(const __grid_constant__ CUtensorMap tmK,
                          const __grid_constant__ CUtensorMap tmV, const ChunkArgs a) {
-  constexpr bool kBf16 = QT == kBF16;
+  using SL = Smem<FP8>;
+  // operand type of the products: the q type, or f16 for FP8 caches
+  constexpr bool kBf16 = !FP8 && QT == kBF16;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
-  const uint32_t sQ = base + kOffQ, sK = base + kOffK, sV = base + kOffV, sP = base + kOffP;
-  auto bar = [&](int i) -> uint32_t { return base + kOffBar + 8u * i; };
-  const uint32_t* tslot = reinterpret_cast<const uint32_t*>(smem_raw + (base - raw) + kOffSlot);
+  const uint32_t sQ = base + SL::kQ, sK = base + SL::kK, sV = base + SL::kV, sP = base + SL::kP;
+  const uint32_t sKc = base + SL::kKc, sVc = base + SL::kVc;
+  auto bar = [&](int i) -> uint32_t { return base + SL::kBar + 8u * i; };
+  const uint32_t* tslot = reinterpret_cast<const uint32_t*>(smem_raw + (base - raw) + SL::kSlot);
+  // the f16/bf16 K and V tiles the products read for K/V tile n
+  auto tile_k = [&](int n) -> uint32_t {
+    return FP8 ? sKc + (n & 1) * kKvBytes : sK + (n % kStages) * kKvBytes;
+  };
+  auto tile_v = [&](int n) -> uint32_t {
+    return FP8 ? sVc + (n & 1) * kKvBytes : sV + (n % kStages) * kKvBytes;
+  };
+  // barrier (and parity) that says tile n is ready for the products
+  auto ready_bar = [&](int n) -> uint32_t { return FP8 ? bar(kBarCFull + (n & 1)) : bar(kBarFull + n % kStages); };
+  auto ready_par = [&](int n) -> uint32_t { return FP8 ? (n >> 1) & 1 : (n / kStages) & 1; };
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int ut = blockIdx.x % a.QT;  // unit (256 rows) within the (sequence, KV head)
@@ -116,7 +150,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tmV);
     for (int i = 0; i < kStages; ++i) {
       mbar_init(bar(kBarFull + i), 1);
-      mbar_init(bar(kBarEmpty + i), 1);
+      // freed by the products' commit, or (FP8) by the converters
+      mbar_init(bar(kBarEmpty + i), FP8 ? kConvWarps * 32 : 1);
     }
     for (int x = 0; x < 2; ++x) {
       mbar_init(bar(kBarS + x), 1);
@@ -124,9 +159,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(kBarO + x), 1);
     }
     mbar_init(bar(kBarQ), 2 * kGroupWarps * 32);
+    if constexpr (FP8) {
+      for (int j = 0; j < 2; ++j) {
+        mbar_init(bar(kBarCFull + j), kConvWarps * 32);
+        mbar_init(bar(kBarCEmpty + j), 1);
+      }
+    }
     fence_mbar_init();
   }
-  if (warp == 0) tc::tmem_alloc(base + kOffSlot, kTmemCols);
+  if (warp == 0) tc::tmem_alloc(base + SL::kSlot, kTmemCols);
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
@@ -154,7 +195,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kLoadWarp) {
     // ------------------------------------------------------------ producer
     // Loads K/V tile n into `stage`: lanes 0..3 each look up one 16-token
-    // slice in the block table and copy it (two 64-dim boxes of K and of V).
+    // slice in the block table and copy it (16-bit: two 64-dim boxes of K and
+    // of V; e4m3: one 128-dim box each).
     auto load_tile = [&](int n, int stage) {
       const int pos0 = lo16 + n * kKv + 16 * lane;
       int row = -1;
@@ -167,15 +209,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         row = (blk * a.Hkv + kvh) * a.bs + pos0 % a.bs;
       }
       const int nslices = __popc(__ballot_sync(kFull, row >= 0));
-      if (lane == 0) mbar_arrive_expect_tx(bar(kBarFull + stage), nslices * 4 * 2048);
+      if (lane == 0)
+        mbar_arrive_expect_tx(bar(kBarFull + stage), nslices * (FP8 ? 2 : 4) * 2048);
       __syncwarp();
       if (row >= 0) {
-        const uint32_t kd = sK + stage * kKvBytes + lane * 2048;
-        const uint32_t vd = sV + stage * kKvBytes + lane * 2048;
+        const uint32_t kd = sK + stage * SL::kTileK + lane * 2048;
+        const uint32_t vd = sV + stage * SL::kTileK + lane * 2048;
+        if constexpr (FP8) {
+          tma_load_2d(kd, &tmK, 0, row, bar(kBarFull + stage));
+          tma_load_2d(vd, &tmV, 0, row, bar(kBarFull + stage));
+        } else {
 #pragma unroll
-        for (int box = 0; box < 2; ++box) {
-          tma_load_2d(kd + box * 8192, &tmK, box * 64, row, bar(kBarFull + stage));
-          tma_load_2d(vd + box * 8192, &tmV, box * 64, row, bar(kBarFull + stage));
+          for (int box = 0; box < 2; ++box) {
+            tma_load_2d(kd + box * 8192, &tmK, box * 64, row, bar(kBarFull + stage));
+            tma_load_2d(vd + box * 8192, &tmV, box * 64, row, bar(kBarFull + stage));
+          }
         }
       }
       __syncwarp();
@@ -194,13 +242,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr uint32_t idO = tc::idesc_f16(kRows, kHd, kBf16, true);
     // S_X = Q_X . K_n^T over the 128 head dims (8 steps of 16)
     auto issue_s = [&](int x, int n) {
-      const int st = n % kStages;
       if (lane == 0) {
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
           const uint32_t box = ks >> 2, kk = (ks & 3) * 32;
           const uint64_t ad = tc::sdesc_sw128(sQ + x * kQBytes + box * 16384 + kk, 16, 1024);
-          const uint64_t bd = tc::sdesc_sw128(sK + st * kKvBytes + box * 8192 + kk, 16, 1024);
+          const uint64_t bd = tc::sdesc_sw128(tile_k(n) + box * 8192 + kk, 16, 1024);
           tc::mma_f16(tmem + kColS + 64 * x, ad, bd, idS, ks > 0);
         }
         tc::commit(bar(kBarS + x));
@@ -209,12 +256,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     // O_X (+)= P_X . V_n over 64 tokens (4 steps of 16)
     auto issue_o = [&](int x, int n) {
-      const int st = n % kStages;
       if (lane == 0) {
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks) {
           const uint64_t ad = tc::sdesc_sw128(sP + x * kPBytes + ks * 32, 16, 1024);
-          const uint64_t bd = tc::sdesc_sw128(sV + st * kKvBytes + ks * 2048, 8192, 1024);
+          const uint64_t bd = tc::sdesc_sw128(tile_v(n) + ks * 2048, 8192, 1024);
           tc::mma_f16(tmem + kColO + 128 * x, ad, bd, idO, (n > 0 || ks > 0) ? 1u : 0u);
         }
         tc::commit(bar(kBarO + x));
@@ -223,7 +269,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     bool ok = true;
     if (ntiles > 0) {
-      ok = wait_all(bar(kBarQ), 0) && wait_all(bar(kBarFull), 0);
+      ok = wait_all(bar(kBarQ), 0) && wait_all(ready_bar(0), ready_par(0));
       if (ok) {
         tc::fence_after_sync();
         issue_s(0, 0);
@@ -237,7 +283,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::fence_after_sync();
       issue_o(0, n);
       if (more) {
-        if (!(ok = wait_all(bar(kBarFull + (n + 1) % kStages), ((n + 1) / kStages) & 1))) break;
+        if (!(ok = wait_all(ready_bar(n + 1), ready_par(n + 1)))) break;
         tc::fence_after_sync();
         issue_s(0, n + 1);
       }
@@ -246,11 +292,56 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::fence_after_sync();
         issue_o(1, n);
       }
-      if (lane == 0) tc::commit(bar(kBarEmpty + st));  // both products of tile n issued
+      // both products of tile n issued: its ring stage (FP8: converted buffer)
+      // is free once they complete
+      if (lane == 0) tc::commit(FP8 ? bar(kBarCEmpty + (n & 1)) : bar(kBarEmpty + st));
       __syncwarp();
       if (hasB && more) issue_s(1, n + 1);
     }
     if (!ok && lane == 0) atomicOr(a.err, PA_DEVERR_TIMEOUT);
+  } else if (warp >= kConvWarp0) {
+    // ------------------------------------------------------------ FP8 converters
+    // e4m3 tile n (ring stage n % kStages) -> f16 tiles in converted buffer
+    // n & 1: each 16-byte chunk of 16 e4m3 codes becomes two 16-byte chunks
+    // of f16 in the 64-dim box that holds them; V rows outside [lo, hi] are
+    // written as zeros.
+    if constexpr (FP8) {
+      const int ct = tid - kConvWarp0 * 32;
+      bool ok = true;
+      for (int n = 0; n < ntiles; ++n) {
+        const int st = n % kStages, cb = n & 1;
+        const int t0 = lo16 + n * kKv;
+        if (!(ok = wait_all(bar(kBarFull + st), (n / kStages) & 1))) break;
+        if (n >= 2 && !(ok = wait_all(bar(kBarCEmpty + cb), ((n - 2) >> 1) & 1))) break;
+        for (int i = ct; i < 2 * kKv * 8; i += kConvWarps * 32) {
+          const bool is_v = i >= kKv * 8;
+          const int j = i & (kKv * 8 - 1), row = j >> 3, c = j & 7;
+          const uint32_t src = (is_v ? sV : sK) + st * kRawBytes + row * 128 + ((c ^ (row & 7)) << 4);
+          uint4 lo4 = make_uint4(0u, 0u, 0u, 0u), hi4 = lo4;
+          const int pos = t0 + row;
+          if (!is_v || (pos >= lo && pos <= hi)) {
+            uint32_t w0, w1, w2, w3;
+            lds_v4(src, w0, w1, w2, w3);
+            lo4 = make_uint4(e4m3x2_to_f16x2(static_cast<uint16_t>(w0 & 0xffffu)),
+                             e4m3x2_to_f16x2(static_cast<uint16_t>(w0 >> 16)),
+                             e4m3x2_to_f16x2(static_cast<uint16_t>(w1 & 0xffffu)),
+                             e4m3x2_to_f16x2(static_cast<uint16_t>(w1 >> 16)));
+            hi4 = make_uint4(e4m3x2_to_f16x2(static_cast<uint16_t>(w2 & 0xffffu)),
+                             e4m3x2_to_f16x2(static_cast<uint16_t>(w2 >> 16)),
+                             e4m3x2_to_f16x2(static_cast<uint16_t>(w3 & 0xffffu)),
+                             e4m3x2_to_f16x2(static_cast<uint16_t>(w3 >> 16)));
+          }
+          const uint32_t dst = (is_v ? sVc : sKc) + cb * kKvBytes + (c >> 2) * 8192 + row * 128;
+          const int c0 = 2 * (c & 3);
+          sts_v4(dst + ((c0 ^ (row & 7)) << 4), lo4);
+          sts_v4(dst + (((c0 + 1) ^ (row & 7)) << 4), hi4);
+        }
+        fence_proxy_async();  // the f16 tiles, visible to the tensor core
+        mbar_arrive(bar(kBarCFull + cb));
+        mbar_arrive(bar(kBarEmpty + st));  // the e4m3 stage may be reloaded
+      }
+      if (!ok && lane == 0) atomicOr(a.err, PA_DEVERR_TIMEOUT);
+    }
   } else {
     // ------------------------------------------------------------ softmax
     const int x = warp / kGroupWarps;  // row tile: 0 = A, 1 = B
@@ -265,14 +356,47 @@ __global__ void __launch_bounds__(kThreads, 1)
     const size_t orow =
         ((static_cast<size_t>(b) * a.T + tq) * a.Hq + static_cast<size_t>(kvh) * a.G + hq) * kHd;
     const uint32_t q_tile = sQ + x * kQBytes, p_tile = sP + x * kPBytes;
+    float sc = a.score_scale;  // this row's score scale (log2 domain)
     {  // Q row -> shared memory (K-major, 128-byte swizzle)
       const uint4* src =
           reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(a.q) + orow);
+      uint4 qv[16];
 #pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        const uint4 v = valid ? src[c] : make_uint4(0u, 0u, 0u, 0u);
-        sts_v4(q_tile + (c >> 3) * 16384 + r * 128 + (((c & 7) ^ (r & 7)) << 4), v);
+      for (int c = 0; c < 16; ++c) qv[c] = valid ? src[c] : make_uint4(0u, 0u, 0u, 0u);
+      if constexpr (FP8) {
+        // f16 after a power-of-two rescale: largest magnitude in [2^14, 2^15)
+        auto f = [&](uint32_t w, int hi) -> float {
+          const uint16_t h = static_cast<uint16_t>(hi ? w >> 16 : w & 0xffffu);
+          return QT == kBF16 ? __uint_as_float(static_cast<uint32_t>(h) << 16)
+                             : __half2float(__ushort_as_half(h));
+        };
+        float amax = 0.f;
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          const uint32_t w4[4] = {qv[c].x, qv[c].y, qv[c].z, qv[c].w};
+#pragma unroll
+          for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f(w4[i >> 1], i & 1)));
+        }
+        int sh = 0;
+        if (amax > 0.f && amax < INFINITY) {
+          int e;
+          frexpf(amax, &e);
+          sh = e - 15;
+        }
+        sc = ldexpf(a.score_scale, sh);
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          const uint32_t w4[4] = {qv[c].x, qv[c].y, qv[c].z, qv[c].w};
+          uint32_t o4[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            o4[i] = pack16x2<false>(ldexpf(f(w4[i], 0), -sh), ldexpf(f(w4[i], 1), -sh));
+          qv[c] = make_uint4(o4[0], o4[1], o4[2], o4[3]);
+        }
       }
+#pragma unroll
+      for (int c = 0; c < 16; ++c)
+        sts_v4(q_tile + (c >> 3) * 16384 + r * 128 + (((c & 7) ^ (r & 7)) << 4), qv[c]);
       fence_proxy_async();
       mbar_arrive(bar(kBarQ));
     }
@@ -297,14 +421,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (inside) {
 #pragma unroll
         for (int j = 0; j < kKv; ++j) {
-          s[j] = __uint_as_float(sr[j >> 5][j & 31]) * a.score_scale;
+          s[j] = __uint_as_float(sr[j >> 5][j & 31]) * sc;
           mxp[j & 7] = fmaxf(mxp[j & 7], s[j]);
         }
       } else {
 #pragma unroll
         for (int j = 0; j < kKv; ++j) {
           const bool keep = t0 + j >= lo_r && t0 + j <= hi_r;
-          s[j] = keep ? __uint_as_float(sr[j >> 5][j & 31]) * a.score_scale : -INFINITY;
+          s[j] = keep ? __uint_as_float(sr[j >> 5][j & 31]) * sc : -INFINITY;
           mxp[j & 7] = fmaxf(mxp[j & 7], s[j]);
         }
       }
@@ -342,8 +466,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         pk[j] = pack16x2<kBf16>(p0, p1);
       }
       l += ((sp[0] + sp[1]) + (sp[2] + sp[3])) + ((sp[4] + sp[5]) + (sp[6] + sp[7]));
-      if (x == 0 && (t0 < lo || t0 + kKv - 1 > hi)) {
+      if (!FP8 && x == 0 && (t0 < lo || t0 + kKv - 1 > hi)) {
         // edge tile: once it has landed, zero the V rows outside [lo, hi]
+        // (with FP8 caches the converters write those rows as zeros)
         if (!(ok = wait_all(bar(kBarFull + st), (n / kStages) & 1))) break;
         for (int i = r; i < kKv * 16; i += kRows) {
           const int row = i >> 4, box = (i >> 3) & 1, ch = i & 7;
@@ -366,7 +491,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // the last product, then the output row
       if (ok && ntiles > 0) ok = wait_all(bar(kBarO + x), (ntiles - 1) & 1);
       tc::fence_after_sync();
-      const float inv = (ok && ntiles > 0 && l > 0.f) ? 1.f / l : 0.f;
+      const float inv = (ok && ntiles > 0 && l > 0.f) ? (FP8 ? a.v_scale : 1.f) / l : 0.f;
       uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(a.out) + orow);
 #pragma unroll
       for (int c0 = 0; c0 < kHd; c0 += 32) {
@@ -382,10 +507,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
             const float* f = reinterpret_cast<const float*>(ov) + 8 * c;
-            dst[c0 / 8 + c] = make_uint4(pack16x2<kBf16>(f[0] * inv, f[1] * inv),
-                                         pack16x2<kBf16>(f[2] * inv, f[3] * inv),
-                                         pack16x2<kBf16>(f[4] * inv, f[5] * inv),
-                                         pack16x2<kBf16>(f[6] * inv, f[7] * inv));
+            constexpr bool kOutBf16 = QT == kBF16;
+            dst[c0 / 8 + c] = make_uint4(pack16x2<kOutBf16>(f[0] * inv, f[1] * inv),
+                                         pack16x2<kOutBf16>(f[2] * inv, f[3] * inv),
+                                         pack16x2<kOutBf16>(f[4] * inv, f[5] * inv),
+                                         pack16x2<kOutBf16>(f[6] * inv, f[7] * inv));
           }
         }
       }
@@ -401,41 +527,51 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int QT>
+template <int QT, bool FP8>
 cudaError_t launch_typed(const CUtensorMap& tk, const CUtensorMap& tv, const ChunkArgs& a,
                          int grid, cudaStream_t s, bool pdl) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.blockDim = dim3(Smem<FP8>::kThreads);
+  cfg.dynamicSmemBytes = Smem<FP8>::kBytes;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, chunk_attn_tc_kernel<QT>, tk, tv, a);
+  return cudaLaunchKernelEx(&cfg, chunk_attn_tc_kernel<QT, FP8>, tk, tv, a);
 }
 
 }  // namespace
 
 int chunk_tc_unit_rows() { return kUnitRows; }
 
-cudaError_t chunk_tc_prepare() {
-  cudaError_t e = cudaFuncSetAttribute(chunk_attn_tc_kernel<kBF16>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(chunk_attn_tc_kernel<kF16>,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+template <int QT, bool FP8>
+cudaError_t set_smem() {
+  return cudaFuncSetAttribute(chunk_attn_tc_kernel<QT, FP8>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, Smem<FP8>::kBytes);
 }
 
-cudaError_t chunk_tc_launch(int qt, const CUtensorMap& tk, const CUtensorMap& tv,
+cudaError_t chunk_tc_prepare() {
+  cudaError_t e;
+  if ((e = set_smem<kBF16, false>()) != cudaSuccess || (e = set_smem<kF16, false>()) != cudaSuccess ||
+      (e = set_smem<kBF16, true>()) != cudaSuccess || (e = set_smem<kF16, true>()) != cudaSuccess)
+    return e;
+  return cudaSuccess;
+}
+
+cudaError_t chunk_tc_launch(int qt, bool fp8, const CUtensorMap& tk, const CUtensorMap& tv,
                             const ChunkArgs& a, cudaStream_t s, bool pdl) {
   const long long grid = static_cast<long long>(a.B) * a.Hkv * a.QT;
   if (grid <= 0) return cudaSuccess;
   if (grid > 0x7fffffffLL) return cudaErrorInvalidValue;
-  return qt == kBF16 ? launch_typed<kBF16>(tk, tv, a, static_cast<int>(grid), s, pdl)
-                     : launch_typed<kF16>(tk, tv, a, static_cast<int>(grid), s, pdl);
+  const int g = static_cast<int>(grid);
+  if (fp8)
+    return qt == kBF16 ? launch_typed<kBF16, true>(tk, tv, a, g, s, pdl)
+                       : launch_typed<kF16, true>(tk, tv, a, g, s, pdl);
+  return qt == kBF16 ? launch_typed<kBF16, false>(tk, tv, a, g, s, pdl)
+                     : launch_typed<kF16, false>(tk, tv, a, g, s, pdl);
 }
 
 }  // namespace pa

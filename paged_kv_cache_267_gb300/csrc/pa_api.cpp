@@ -762,7 +762,7 @@ pa_status run_decode(const DecodeCall& c, DeviceState* st, const DecodePlan& pla
 
 bool use_chunk_tc(const DecodeCall& c) {
   const int path = g_chunk_path.load();
-  if (path == 1 || c.fp8 || c.D != 128) return false;
+  if (path == 1 || c.D != 128) return false;
   return path == 2 || c.T * c.G > kTcMinColumns;
 }
 
@@ -781,8 +781,9 @@ pa_status run_chunk_tc(const DecodeCall& c, cudaStream_t cs) {
   }
   const int D = static_cast<int>(c.D);
   CUtensorMap tk, tv;
-  if ((s = make_cache_map(&tk, c.kc->data, c.NB * c.Hkv * c.bs, D, 2)) ||
-      (s = make_cache_map(&tv, c.vc->data, c.NB * c.Hkv * c.bs, D, 2)))
+  const int elt = c.fp8 ? 1 : 2;
+  if ((s = make_cache_map(&tk, c.kc->data, c.NB * c.Hkv * c.bs, D, elt)) ||
+      (s = make_cache_map(&tv, c.vc->data, c.NB * c.Hkv * c.bs, D, elt)))
     return s;
   pa::ChunkArgs a;
   a.q = c.q->data;
@@ -801,12 +802,14 @@ pa_status run_chunk_tc(const DecodeCall& c, cudaStream_t cs) {
   a.window = c.window;
   const int unit = pa::chunk_tc_unit_rows();
   a.QT = static_cast<int>((c.T * c.G + unit - 1) / unit);
-  a.score_scale = static_cast<float>(static_cast<double>(c.scale) * 1.4426950408889634);
+  a.score_scale = static_cast<float>(static_cast<double>(c.scale) * 1.4426950408889634 *
+                                     (c.fp8 ? static_cast<double>(c.k_scale) : 1.0));
+  a.v_scale = c.fp8 ? c.v_scale : 1.f;
   const bool prof = g_prof_before && g_prof_after;
   cudaError_t e;
   if (prof && (e = cudaEventRecord(static_cast<cudaEvent_t>(g_prof_before), cs)) != cudaSuccess)
     return cuda_fail(e, "profile event");
-  e = pa::chunk_tc_launch(c.qt, tk, tv, a, cs, !prof);
+  e = pa::chunk_tc_launch(c.qt, c.fp8, tk, tv, a, cs, !prof);
   if (e != cudaSuccess) return cuda_fail(e, "chunk kernel launch");
   if (prof && (e = cudaEventRecord(static_cast<cudaEvent_t>(g_prof_after), cs)) != cudaSuccess)
     return cuda_fail(e, "profile event");

@@ -108,7 +108,7 @@ struct ReshapeArgs {
 
 // Chunked queries on the tensor-memory kernel (chunk_tc.cu): one CTA per
 // (sequence, KV head, unit of chunk_tc_unit_rows() (query, head) rows); head
-// dim 128, 16-bit caches.
+// dim 128, 16-bit or e4m3 caches.
 struct ChunkArgs {
   const void* q;                 // [B, T, Hq, D]
   void* out;                     // [B, T, Hq, D]
@@ -117,11 +117,12 @@ struct ChunkArgs {
   int32_t* err;                  // device error word
   int B, T, Hq, Hkv, G, bs, MB, NB, window;
   int QT;                        // units per (sequence, KV head): ceil(T * G / unit rows)
-  float score_scale;             // scale * log2(e)
+  float score_scale;             // scale * log2(e) (* k_scale for FP8)
+  float v_scale;                 // FP8: applied to the output
 };
 int chunk_tc_unit_rows();
 cudaError_t chunk_tc_prepare();  // once per device: the kernel's shared-memory size
-cudaError_t chunk_tc_launch(int qt, const CUtensorMap& tk, const CUtensorMap& tv,
+cudaError_t chunk_tc_launch(int qt, bool fp8, const CUtensorMap& tk, const CUtensorMap& tv,
                             const ChunkArgs& a, cudaStream_t s, bool pdl);
 
 // Kernel configuration chosen for a (cache type, q type, D, n-tiles) variant.

@@ -114,12 +114,14 @@ FORCED = [
     (64, 16, 2, 128, 32, 0, "f16", False, (0, 1, 63, 64, 65, 700, 129, 3000)),  # bs 32, L < T
     (7, 32, 2, 128, 16, 24, "f16", False, (5, 6, 7, 8, 40, 300)),  # G = 16, short window
     (128, 8, 8, 128, 16, 0, "bf16", False, (128, 127, 1000, 2047)),  # G = 1
+    (40, 32, 8, 128, 16, 100, "bf16", True, SMALL_LENS),       # e4m3 cache, window
+    (64, 16, 2, 128, 32, 0, "f16", True, (0, 1, 63, 64, 65, 700, 129, 3000)),  # e4m3, f16 q
 ]
 
 
 @pytest.mark.parametrize("path", [1, 2], ids=["persistent", "tensor_memory"])
 @pytest.mark.parametrize("case", FORCED, ids=[f"T{c[0]}_G{c[1] // c[2]}_bs{c[4]}_W{c[5]}_{c[6]}"
-                                                for c in FORCED])
+                                                f"{'_fp8' if c[7] else ''}" for c in FORCED])
 def test_chunk_kernels_forced(case, path, pa_lib):
     """Each chunk kernel, forced, against the oracle on the same inputs."""
     *shape, lens = case
@@ -140,7 +142,9 @@ def test_chunk_kernels_forced(case, path, pa_lib):
                                      torch.from_numpy(sides.w.block_tables).cuda(),
                                      torch.from_numpy(sides.w.seq_lens).cuda(),
                                      num_kv_heads=s.num_kv_heads, scale=s.softmax_scale,
-                                     block_size=s.block_size, window=s.window)
+                                     block_size=s.block_size, window=s.window,
+                                     kv_dtype="fp8" if s.kv_fp8 else "auto",
+                                     k_scale=sides.w.k_scale, v_scale=sides.w.v_scale)
         finally:
             pa_lib.set_prefill_path(0)
         assert torch.equal(again.view(torch.int16), sides.out.view(torch.int16))

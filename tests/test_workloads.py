@@ -26,7 +26,7 @@ def test_named_configs_match_their_descriptions():
     assert c["prefix_window"].window == 4096 and c["prefix_window"].shared_prefix == 2048
     assert c["fp8"].kv_fp8 and c["fp8"].batch == 256
     seeds = [s.seed for s in c.values()]
-    assert seeds == [267001, 267002, 267003, 267004, 267005, 267006, 267007]
+    assert seeds == [267001, 267002, 267003, 267004, 267005, 267006, 267007, 267008]
     assert c["verify4_llama8b"].num_queries == 4 and c["prefill_chunk512"].num_queries == 512
     assert all(c[n].num_queries == 1 for n in ("tiny", "llama8b", "long_skew", "prefix_window",
                                                "fp8"))

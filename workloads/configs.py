@@ -78,6 +78,10 @@ CONFIGS: dict[str, Spec] = {
                              head_dim=128, block_size=16, dtype="bf16",
                              len_dist=("uniform", 512, 8192), num_queries=512, pool_factor=1.2,
                              seed=_seed(7)),
+    "prefill_chunk512_fp8": Spec("prefill_chunk512_fp8", batch=8, num_q_heads=32, num_kv_heads=8,
+                                 head_dim=128, block_size=16, dtype="bf16", kv_fp8=True,
+                                 len_dist=("uniform", 512, 8192), num_queries=512,
+                                 pool_factor=1.2, seed=_seed(8)),
 }
 
 
