@@ -232,8 +232,8 @@ pa_status pa_prefill_chunk(const pa_tensor* out, const pa_tensor* q, const pa_te
 
 /* Kernel choice for pa_prefill_chunk, process-wide: 0 (default) picks per
  * call; 1 always uses the persistent split-KV kernel (16 (query, head)
- * columns per pass over K/V, any head dim, FP8 caches); 2 uses the
- * tensor-memory kernel wherever it applies (16-bit caches, head_dim 128),
+ * columns per pass over K/V, any head dim); 2 uses the tensor-memory kernel
+ * wherever it applies (head_dim 128; 16-bit or e4m3 caches),
  * which tiles 128 (query, head) rows against 64-token K/V tiles on the
  * tcgen05 tensor cores and reads each K/V tile once per 256 rows. The
  * default takes the tensor-memory kernel for chunks of more than 32 (query,
