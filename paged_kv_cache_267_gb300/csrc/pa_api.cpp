@@ -41,7 +41,7 @@ constexpr int kWarpsPerCta = 8;  // most worker warps of any decode variant
 constexpr int64_t kMaxBatch = 4096;
 constexpr int64_t kMaxChunk = 4096;        // query tokens per sequence in a chunk call
 // Chunks with more (query, head) columns per KV head than this go to the
-// tensor-memory kernel (16-bit caches, head dim 128): the persistent kernel
+// tensor-memory kernel (head dim 128, 16-bit or e4m3 caches): the persistent kernel
 // reads each K/V tile once per 16 columns.
 constexpr int64_t kTcMinColumns = 32;
 
