@@ -402,3 +402,34 @@ def test_maximum_batch(pa_lib):
     with pytest.raises(pa_lib.PAError) as e:
         pa_lib.decode(q, sides.kc, sides.vc, bt, sl, num_kv_heads=2, scale=0.1, block_size=16)
     assert e.value.status == -2
+
+
+def test_concurrent_streams_use_separate_workspaces(pa_lib):
+    """Two decode steps in flight at once on two streams (each stream gets its
+    own library workspace): both equal the same steps run alone (pool off)."""
+    specs = [spec(seq_lens=(300, 17, 1, 2000), seed=51), spec(seq_lens=(64, 900, 33), seed=52)]
+    ws = [generate(s, device="cuda") for s in specs]
+    args = []
+    for w in ws:
+        s = w.spec
+        args.append((w, torch.from_numpy(w.block_tables).cuda(),
+                     torch.from_numpy(w.seq_lens).cuda(),
+                     dict(num_kv_heads=2, scale=s.softmax_scale, block_size=16)))
+    pa_lib.set_decode_tuning(pool_permille=-1)
+    try:
+        alone = []
+        for w, bt, sl, kw in args:
+            alone.append(pa_lib.decode(w.q, w.key_cache, w.value_cache, bt, sl, **kw).clone())
+        torch.cuda.synchronize()
+        streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+        outs = [torch.empty_like(w.q) for w, *_ in args]
+        for _ in range(5):
+            for (w, bt, sl, kw), st, o in zip(args, streams, outs):
+                with torch.cuda.stream(st):
+                    pa_lib.decode(w.q, w.key_cache, w.value_cache, bt, sl, out=o, **kw)
+        torch.cuda.synchronize()
+        for a, o in zip(alone, outs):
+            assert torch.equal(a.view(torch.int16), o.view(torch.int16))
+    finally:
+        pa_lib.set_decode_tuning()
+    assert pa_lib.check_device_error() == 0
