@@ -18,9 +18,10 @@
 // other runs its softmax. Per K/V tile n and row tile X:
 //   S_X  = Q_X . K_n^T        tcgen05.mma M128 N64  K128 -> TMEM
 //   softmax X: S_X from TMEM; per-row causal/window mask; online softmax in
-//          the log2 domain against the row's reference max m; P_X (16-bit)
-//          -> shared memory, 128-byte swizzle
-//   O_X += P_X . V_n          tcgen05.mma M128 N128 K64 -> TMEM (V MN-major)
+//          the log2 domain against the row's reference max m; P_X (16-bit,
+//          packed in pairs) -> tensor memory
+//   O_X += P_X . V_n          tcgen05.mma M128 N128 K64, A = P_X from TMEM,
+//                             B = V_n (MN-major) -> TMEM
 // The output accumulates in tensor memory. A row's reference max moves only
 // when its running max exceeds it by more than 8 (log2 units); the warp then
 // rescales those rows of O_X in tensor memory (load, scale, store) before the
@@ -59,14 +60,13 @@ constexpr int kConvWarps = 2;
 constexpr uint32_t kQBytes = kRows * kHd * 2;   // per row tile: [2 boxes][128 rows][128 B]
 constexpr uint32_t kKvBytes = kKv * kHd * 2;    // 16-bit tile: [2 boxes][64 rows][128 B]
 constexpr uint32_t kRawBytes = kKv * kHd;       // e4m3 tile: [64 rows][128 B]
-constexpr uint32_t kPBytes = kRows * kKv * 2;   // per row tile: [128 rows][128 B]
 constexpr int kBarFull = 0, kBarEmpty = kStages, kBarS = 2 * kStages,  // S_A, S_B
     kBarP = kBarS + 2, kBarO = kBarS + 4, kBarQ = kBarS + 6,
     kBarCFull = kBarS + 7, kBarCEmpty = kBarS + 9,  // FP8: converted buffers 0, 1
     kNumBars = kBarS + 11;
 
 // Shared-memory layout: Q_A, Q_B, the ring, (FP8: the converted double
-// buffer of K and V), P_A, P_B, barriers, the tensor-memory address.
+// buffer of K and V), barriers, the tensor-memory address.
 template <bool FP8>
 struct Smem {
   static constexpr uint32_t kThreads = (kConvWarp0 + (FP8 ? kConvWarps : 0)) * 32;
@@ -76,13 +76,14 @@ struct Smem {
   static constexpr uint32_t kV = kK + kStages * kTileK;          // ring: V tiles
   static constexpr uint32_t kKc = kV + kStages * kTileK;         // FP8: f16 K tiles [2]
   static constexpr uint32_t kVc = kKc + (FP8 ? 2 * kKvBytes : 0);
-  static constexpr uint32_t kP = kVc + (FP8 ? 2 * kKvBytes : 0);
-  static constexpr uint32_t kBar = kP + 2 * kPBytes;
+  static constexpr uint32_t kBar = kVc + (FP8 ? 2 * kKvBytes : 0);
   static constexpr uint32_t kSlot = kBar + 8 * kNumBars;
   static constexpr uint32_t kBytes = kSlot + 16 + 1024;  // + room to align the base to 1 KB
 };
-constexpr uint32_t kTmemCols = 512;  // S_A [0,64) S_B [64,128) O_A [128,256) O_B [256,384)
-constexpr uint32_t kColS = 0, kColO = 128;
+// tensor memory: S_A [0,64) S_B [64,128) O_A [128,256) O_B [256,384)
+// P_A [384,416) P_B [416,448)
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColS = 0, kColO = 128, kColP = 384;
 constexpr uint64_t kWaitNs = 2000000000ull;  // bound of every wait (2 s)
 constexpr float kFloor = -1e30f;             // reference-max start
 constexpr float kRescaleAbove = 8.f;         // log2 units
@@ -125,7 +126,7 @@ __global__ void __launch_bounds__(Smem<FP8>::kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
-  const uint32_t sQ = base + SL::kQ, sK = base + SL::kK, sV = base + SL::kV, sP = base + SL::kP;
+  const uint32_t sQ = base + SL::kQ, sK = base + SL::kK, sV = base + SL::kV;
   const uint32_t sKc = base + SL::kKc, sVc = base + SL::kVc;
   auto bar = [&](int i) -> uint32_t { return base + SL::kBar + 8u * i; };
   const uint32_t* tslot = reinterpret_cast<const uint32_t*>(smem_raw + (base - raw) + SL::kSlot);
@@ -254,14 +255,15 @@ __global__ void __launch_bounds__(Smem<FP8>::kThreads, 1)
       }
       __syncwarp();
     };
-    // O_X (+)= P_X . V_n over 64 tokens (4 steps of 16)
+    // O_X (+)= P_X . V_n over 64 tokens (4 steps of 16); P_X in tensor
+    // memory, 8 columns (16 tokens) per step
     auto issue_o = [&](int x, int n) {
       if (lane == 0) {
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks) {
-          const uint64_t ad = tc::sdesc_sw128(sP + x * kPBytes + ks * 32, 16, 1024);
           const uint64_t bd = tc::sdesc_sw128(tile_v(n) + ks * 2048, 8192, 1024);
-          tc::mma_f16(tmem + kColO + 128 * x, ad, bd, idO, (n > 0 || ks > 0) ? 1u : 0u);
+          tc::mma_f16_ta(tmem + kColO + 128 * x, tmem + kColP + 32 * x + 8 * ks, bd, idO,
+                         (n > 0 || ks > 0) ? 1u : 0u);
         }
         tc::commit(bar(kBarO + x));
       }
@@ -355,7 +357,7 @@ __global__ void __launch_bounds__(Smem<FP8>::kThreads, 1)
     const int lo_r = (a.window > 0 && hi_r + 1 > a.window) ? hi_r + 1 - a.window : 0;
     const size_t orow =
         ((static_cast<size_t>(b) * a.T + tq) * a.Hq + static_cast<size_t>(kvh) * a.G + hq) * kHd;
-    const uint32_t q_tile = sQ + x * kQBytes, p_tile = sP + x * kPBytes;
+    const uint32_t q_tile = sQ + x * kQBytes;
     float sc = a.score_scale;  // this row's score scale (log2 domain)
     {  // Q row -> shared memory (K-major, 128-byte swizzle)
       const uint4* src =
@@ -477,12 +479,11 @@ __global__ void __launch_bounds__(Smem<FP8>::kThreads, 1)
             sts_v4(sV + st * kKvBytes + box * 8192 + row * 128 + ch * 16,
                    make_uint4(0u, 0u, 0u, 0u));
         }
+        fence_proxy_async();  // the cleaned V rows, visible to the tensor core
       }
-#pragma unroll
-      for (int c = 0; c < 8; ++c)
-        sts_v4(p_tile + r * 128 + ((c ^ (r & 7)) << 4),
-               make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]));
-      fence_proxy_async();  // P and the cleaned V rows, visible to the tensor core
+      // P_X: free, since the previous product of this tile completed above
+      tc::st32(trow + kColP + 32 * x, pk);
+      tc::wait_st();
       tc::fence_before_sync();
       mbar_arrive(bar(kBarP + x));
     }
