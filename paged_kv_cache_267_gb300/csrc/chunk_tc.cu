@@ -19,7 +19,7 @@
 //   S_X  = Q_X . K_n^T     tcgen05.mma M128 N128 K128 -> TMEM
 //   softmax X: S_X from TMEM; per-row causal/window mask; online softmax in
 //          the log2 domain against the row's reference max m; P_X (16-bit,
-//          packed in pairs) written back over the first 64 columns of S_X
+//          packed in pairs) written back over columns 0-31 and 64-95 of S_X
 //   O_X += P_X . V_n       tcgen05.mma M128 N128 K128, A = P_X from TMEM,
 //                          B = V_n (MN-major) -> TMEM
 // S_X(n+1) overwrites P_X(n), so the MMA warp issues it only once the product
@@ -31,11 +31,12 @@
 // Per-tile shapes: 128-token tiles keep every product at N = 128 or K = 128,
 // where one M128 K16 step costs about the same as at N = 64, and halve the
 // hand-offs between the softmax groups and the MMA warp per token. A thread
-// reads its 128 scores twice from tensor memory, 64 at a time (row max, then
-// exponentials), and writes the P of scores 64 h .. 64 h + 63 over columns
-// 32 h .. 32 h + 31, which it has already read: 64 scores live in registers,
-// and the loop bodies stay small enough for the instruction cache. A warp
-// takes the masked form of a half only when one of its rows needs it.
+// reads its 128 scores from tensor memory 64 at a time for the row max,
+// keeping the second half in registers; the exponentials of that half go
+// over columns 64-95 (scores it holds), then the first half is read again
+// and its P goes over columns 0-31. 64 scores live in registers, and the loop
+// bodies stay small enough for the instruction cache. A warp takes the
+// masked form of a half only when one of its rows needs it.
 //
 // The output accumulates in tensor memory. A row's reference max moves only
 // when its running max exceeds it by more than 8 (log2 units); the warp then
@@ -86,7 +87,7 @@ struct Smem {
 };
 static_assert(Smem::kBytes <= 227 * 1024, "shared memory per CTA");
 // tensor memory: S_A [0,128) S_B [128,256) O_A [256,384) O_B [384,512);
-// P_X over the first 64 columns of S_X
+// P_X over columns 0-31 (tokens 0-63) and 64-95 (tokens 64-127) of S_X
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0, kColO = 256;
 constexpr uint64_t kWaitNs = 2000000000ull;  // bound of every wait (2 s)
@@ -235,15 +236,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       __syncwarp();
     };
-    // O_X (+)= P_X . V_n over 128 tokens (8 steps of 16); P_X in the first 64
-    // columns of S_X, 8 columns (16 tokens) per step
+    // O_X (+)= P_X . V_n over 128 tokens (8 steps of 16); P_X in columns
+    // 0-31 and 64-95 of S_X, 8 columns (16 tokens) per step
     auto issue_o = [&](int x, int n) {
       if (lane == 0) {
         const uint32_t vt = sV + (n & 1) * kTileBytes;
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
           const uint64_t bd = tc::sdesc_sw128(vt + ks * 2048, kBoxBytes, 1024);
-          tc::mma_f16_ta(tmem + kColO + 128 * x, tmem + kColS + 128 * x + 8 * ks, bd, idO,
+          const uint32_t pc = ks < 4 ? 8 * ks : 32 + 8 * ks;  // P columns of tokens 16 ks ..
+          tc::mma_f16_ta(tmem + kColO + 128 * x, tmem + kColS + 128 * x + pc, bd, idO,
                          (n > 0 || ks > 0) ? 1u : 0u);
         }
         tc::commit(bar(kBarO + x));
@@ -373,15 +375,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         l *= alpha;
         if (grow) ms = mx;
       }
-      // P = 2^(s * sc - ms), packed in pairs: scores 64 h + j -> column 32 h + j / 2
+      // P = 2^(s * sc - ms), packed in pairs: scores 64 h + j -> column
+      // 64 h + j / 2; the second half first, from registers
       float sp[8];  // eight independent partial sums
 #pragma unroll
       for (int i = 0; i < 8; ++i) sp[i] = 0.f;
 #pragma unroll 1
-      for (int h = 0; h < 2; ++h) {
-        tc::ld32_async(tS + 64 * h, sv[0]);
-        tc::ld32_async(tS + 64 * h + 32, sv[1]);
-        tc::wait_ld(sv[0], sv[1]);
+      for (int h = 1; h >= 0; --h) {
+        if (h == 0) {
+          tc::ld32_async(tS, sv[0]);
+          tc::ld32_async(tS + 32, sv[1]);
+          tc::wait_ld(sv[0], sv[1]);
+        }
         uint32_t pk[32];
         if (all_in) {
 #pragma unroll
@@ -403,7 +408,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             pk[j] = pack16x2<kBf16>(p0, p1);
           }
         }
-        tc::st32(tS + 32 * h, pk);
+        tc::st32(tS + 64 * h, pk);
       }
       l += ((sp[0] + sp[1]) + (sp[2] + sp[3])) + ((sp[4] + sp[5]) + (sp[6] + sp[7]));
       if (x == 0 && (t0 < lo || t0 + kKv - 1 > hi)) {
