@@ -1,8 +1,8 @@
-// Tensor-memory kernel for chunked causal queries over a 16-bit paged cache
+// Tensor-memory kernel for chunked causal queries over the paged cache
 // (the chunked-prefill step of "vLLM 0.5 深度解析" §5.2; the attention itself
 // is the block-wise scaled dot product with a running max/sum of §2.3 of
-// the same page), on the 5th-generation tensor cores of sm_103a. FP8 e4m3
-// caches take the kernel of chunk_tc_fp8.cu.
+// the same page), on the 5th-generation tensor cores of sm_103a; 16-bit or
+// FP8 e4m3 caches.
 //
 // Work unit: one (sequence b, KV head, 256 (query, head) rows), the rows
 // being r = t * G + h over the chunk's T queries and the group's G heads: one
@@ -48,6 +48,15 @@
 // exponent through one fused multiply-add against the scaled reference max;
 // a negative softmax scale is carried by flipping the sign of Q (exact), so
 // the row max is taken on the raw scores. Head dim 128.
+//
+// FP8 e4m3 caches (FP8 = true): the rings hold the raw e4m3 tiles (16 KB of
+// K and of V per tile), and two converter warps turn each into an f16 tile
+// of the layout above (exact), in one buffer for K and one for V that the
+// products read; they write zeros for the V rows outside [lo, hi]. A
+// converted buffer is refilled once the products that read it completed.
+// Q is converted per row to f16 after a power-of-two rescale that brings its
+// largest magnitude into [2^14, 2^15); the rescale and k_scale fold into the
+// row's score scale, and v_scale is applied to the output.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -66,26 +75,36 @@ constexpr int kHd = 128;        // head dim
 constexpr int kGroupWarps = 4;  // softmax warps per row tile
 constexpr int kCtrlWarp = 2 * kGroupWarps;  // issues the MMAs
 constexpr int kLoadWarp = kCtrlWarp + 1;     // streams K/V tiles
-constexpr int kThreads = (kLoadWarp + 1) * 32;
+constexpr int kConvWarp0 = kLoadWarp + 1;    // FP8: e4m3 -> f16 converters
+constexpr int kConvWarps = 2;
 constexpr uint32_t kQBytes = kRows * kHd * 2;   // per row tile: [2 boxes][128 rows][128 B]
 constexpr uint32_t kBoxBytes = kKv * 128;       // one 64-dim box of a K or V tile
 constexpr uint32_t kTileBytes = 2 * kBoxBytes;  // K or V tile: [2 boxes][128 tokens][128 B]
+constexpr uint32_t kRawBytes = kKv * kHd;       // e4m3 tile: [128 tokens][128 B]
 // barriers: K and V rings (full, empty; two stages each); per row tile X:
-// S_X computed, P_X written, O_X product complete; Q staged
+// S_X computed, P_X written, O_X product complete; Q staged; FP8: the
+// converted K and V buffers written (full) and read by their products (free)
 constexpr int kBarKFull = 0, kBarKEmpty = 2, kBarVFull = 4, kBarVEmpty = 6, kBarS = 8,
-              kBarP = 10, kBarO = 12, kBarQ = 14, kNumBars = 15;
+              kBarP = 10, kBarO = 12, kBarQ = 14, kBarCKFull = 15, kBarCKFree = 16,
+              kBarCVFull = 17, kBarCVFree = 18, kNumBars = 19;
 
-// Shared-memory layout: Q_A, Q_B, the K ring, the V ring, barriers, the
-// tensor-memory address.
+// Shared-memory layout: Q_A, Q_B, the K ring, the V ring, (FP8: the
+// converted K and V tiles), barriers, the tensor-memory address.
+template <bool FP8>
 struct Smem {
+  static constexpr uint32_t kThreads = (kConvWarp0 + (FP8 ? kConvWarps : 0)) * 32;
+  static constexpr uint32_t kRing = FP8 ? kRawBytes : kTileBytes;  // one ring tile
   static constexpr uint32_t kQ = 0;
   static constexpr uint32_t kK = kQ + 2 * kQBytes;
-  static constexpr uint32_t kV = kK + 2 * kTileBytes;
-  static constexpr uint32_t kBar = kV + 2 * kTileBytes;
+  static constexpr uint32_t kV = kK + 2 * kRing;
+  static constexpr uint32_t kKc = kV + 2 * kRing;
+  static constexpr uint32_t kVc = kKc + (FP8 ? kTileBytes : 0);
+  static constexpr uint32_t kBar = kVc + (FP8 ? kTileBytes : 0);
   static constexpr uint32_t kSlot = kBar + 8 * kNumBars;
   static constexpr uint32_t kBytes = kSlot + 16 + 1024;  // + room to align the base to 1 KB
 };
-static_assert(Smem::kBytes <= 227 * 1024, "shared memory per CTA");
+static_assert(Smem<false>::kBytes <= 227 * 1024 && Smem<true>::kBytes <= 227 * 1024,
+              "shared memory per CTA");
 // tensor memory: S_A [0,128) S_B [128,256) O_A [256,384) O_B [384,512);
 // P_X over columns 0-31 (tokens 0-63) and 64-95 (tokens 64-127) of S_X
 constexpr uint32_t kTmemCols = 512;
@@ -122,18 +141,28 @@ __device__ __forceinline__ bool wait_all(uint32_t bar, uint32_t parity) {
   return __all_sync(kFull, mbar_wait_bounded(bar, parity, kWaitNs));
 }
 
-template <int QT>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int QT, bool FP8>
+__global__ void __launch_bounds__(Smem<FP8>::kThreads, 1)
     chunk_attn_tc128_kernel(const __grid_constant__ CUtensorMap tmK,
                             const __grid_constant__ CUtensorMap tmV, const ChunkArgs a) {
-  constexpr bool kBf16 = QT == kBF16;
+  using SL = Smem<FP8>;
+  // operand type of the products: the q type, or f16 for FP8 caches
+  constexpr bool kBf16 = !FP8 && QT == kBF16;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
-  const uint32_t sQ = base + Smem::kQ, sK = base + Smem::kK, sV = base + Smem::kV;
-  auto bar = [&](int i) -> uint32_t { return base + Smem::kBar + 8u * i; };
+  const uint32_t sQ = base + SL::kQ, sK = base + SL::kK, sV = base + SL::kV;
+  const uint32_t sKc = base + SL::kKc, sVc = base + SL::kVc;
+  auto bar = [&](int i) -> uint32_t { return base + SL::kBar + 8u * i; };
   const uint32_t* tslot =
-      reinterpret_cast<const uint32_t*>(smem_raw + (base - raw) + Smem::kSlot);
+      reinterpret_cast<const uint32_t*>(smem_raw + (base - raw) + SL::kSlot);
+  // the 16-bit K and V tiles the products read for K/V tile n, and the
+  // barrier (with parity) that says they are ready
+  auto tile_k = [&](int n) -> uint32_t { return FP8 ? sKc : sK + (n & 1) * kTileBytes; };
+  auto tile_v = [&](int n) -> uint32_t { return FP8 ? sVc : sV + (n & 1) * kTileBytes; };
+  auto k_ready = [&](int n) -> uint32_t { return FP8 ? bar(kBarCKFull) : bar(kBarKFull + (n & 1)); };
+  auto v_ready = [&](int n) -> uint32_t { return FP8 ? bar(kBarCVFull) : bar(kBarVFull + (n & 1)); };
+  auto ready_par = [&](int n) -> uint32_t { return FP8 ? n & 1 : (n >> 1) & 1; };
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int ut = blockIdx.x % a.QT;  // unit (256 rows) within the (sequence, KV head)
@@ -145,17 +174,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tmV);
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(kBarKFull + i), 1);
-      mbar_init(bar(kBarKEmpty + i), 1);
+      // a ring stage is freed by the products' commit, or (FP8) by the converters
+      mbar_init(bar(kBarKEmpty + i), FP8 ? kConvWarps * 32 : 1);
       mbar_init(bar(kBarVFull + i), 1);
-      mbar_init(bar(kBarVEmpty + i), 1);
+      mbar_init(bar(kBarVEmpty + i), FP8 ? kConvWarps * 32 : 1);
       mbar_init(bar(kBarS + i), 1);
       mbar_init(bar(kBarP + i), kGroupWarps * 32);
       mbar_init(bar(kBarO + i), 1);
     }
     mbar_init(bar(kBarQ), 2 * kGroupWarps * 32);
+    if constexpr (FP8) {
+      mbar_init(bar(kBarCKFull), kConvWarps * 32);
+      mbar_init(bar(kBarCKFree), 1);
+      mbar_init(bar(kBarCVFull), kConvWarps * 32);
+      mbar_init(bar(kBarCVFree), 1);
+    }
     fence_mbar_init();
   }
-  if (warp == 0) tc::tmem_alloc(base + Smem::kSlot, kTmemCols);
+  if (warp == 0) tc::tmem_alloc(base + SL::kSlot, kTmemCols);
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
@@ -184,7 +220,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kLoadWarp) {
     // ------------------------------------------------------------ producer
     // K (or V) tile n into ring stage n & 1: lanes 0..7 each look up one
-    // 16-token slice in the block table and copy its two 64-dim boxes.
+    // 16-token slice in the block table and copy it (16-bit: two 64-dim
+    // boxes; e4m3: one 128-dim box).
     auto load = [&](int n, bool is_v) {
       const uint32_t full = bar((is_v ? kBarVFull : kBarKFull) + (n & 1));
       const int pos0 = lo16 + n * kKv + 16 * lane;
@@ -198,13 +235,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         row = (blk * a.Hkv + kvh) * a.bs + pos0 % a.bs;
       }
       const int nslices = __popc(__ballot_sync(kFull, row >= 0));
-      if (lane == 0) mbar_arrive_expect_tx(full, nslices * 2 * 2048);
+      if (lane == 0) mbar_arrive_expect_tx(full, nslices * (FP8 ? 1 : 2) * 2048);
       __syncwarp();
       if (row >= 0) {
-        const uint32_t dst = (is_v ? sV : sK) + (n & 1) * kTileBytes + lane * 2048;
+        const uint32_t dst = (is_v ? sV : sK) + (n & 1) * SL::kRing + lane * 2048;
+        if constexpr (FP8) {
+          tma_load_2d(dst, is_v ? &tmV : &tmK, 0, row, full);
+        } else {
 #pragma unroll
-        for (int box = 0; box < 2; ++box)
-          tma_load_2d(dst + box * kBoxBytes, is_v ? &tmV : &tmK, box * 64, row, full);
+          for (int box = 0; box < 2; ++box)
+            tma_load_2d(dst + box * kBoxBytes, is_v ? &tmV : &tmK, box * 64, row, full);
+        }
       }
       __syncwarp();
     };
@@ -224,7 +265,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // S_X = Q_X . K_n^T over the 128 head dims (8 steps of 16)
     auto issue_s = [&](int x, int n) {
       if (lane == 0) {
-        const uint32_t kt = sK + (n & 1) * kTileBytes;
+        const uint32_t kt = tile_k(n);
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
           const uint32_t box = ks >> 2, kk = (ks & 3) * 32;
@@ -240,7 +281,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // 0-31 and 64-95 of S_X, 8 columns (16 tokens) per step
     auto issue_o = [&](int x, int n) {
       if (lane == 0) {
-        const uint32_t vt = sV + (n & 1) * kTileBytes;
+        const uint32_t vt = tile_v(n);
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
           const uint64_t bd = tc::sdesc_sw128(vt + ks * 2048, kBoxBytes, 1024);
@@ -252,16 +293,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       __syncwarp();
     };
+    // K_t (V_t) is released once both products of tile t that read it
+    // complete: its ring stage (16-bit), or the converted buffer (FP8). A
+    // release is committed only when something will wait for it, so no
+    // arrive outlives the CTA.
+    auto release_k = [&](int t) {
+      if (lane == 0) {
+        if (FP8 && t + 1 < ntiles) tc::commit(bar(kBarCKFree));
+        if (!FP8 && t + 2 < ntiles) tc::commit(bar(kBarKEmpty + (t & 1)));
+      }
+      __syncwarp();
+    };
+    auto release_v = [&](int t) {
+      if (lane == 0) {
+        if (FP8 && t + 1 < ntiles) tc::commit(bar(kBarCVFree));
+        if (!FP8 && t + 2 < ntiles) tc::commit(bar(kBarVEmpty + (t & 1)));
+      }
+      __syncwarp();
+    };
     bool ok = true;
     if (ntiles > 0) {
-      ok = wait_all(bar(kBarQ), 0) && wait_all(bar(kBarKFull), 0);
+      ok = wait_all(bar(kBarQ), 0) && wait_all(k_ready(0), ready_par(0));
       if (ok) {
         tc::fence_after_sync();
         for (int x = 0; x < nx; ++x) issue_s(x, 0);
-        // K_0 free once both products have read it (a stage is released only
-        // when the producer reloads it: no arrive outlives the CTA)
-        if (lane == 0 && ntiles > 2) tc::commit(bar(kBarKEmpty));
-        __syncwarp();
+        release_k(0);
       }
     }
     // per row tile in turn: O_X += P_X(n) . V_n, then (once that product has
@@ -270,27 +326,64 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int x = 0; x < nx; ++x) {
         // P_X(n) written (by group A: the V rows of an edge tile cleaned)
         if (!(ok = wait_all(bar(kBarP + x), n & 1))) break;
-        if (x == 0 && !(ok = wait_all(bar(kBarVFull + (n & 1)), (n >> 1) & 1))) break;
+        if (x == 0 && !(ok = wait_all(v_ready(n), ready_par(n)))) break;
         tc::fence_after_sync();
         issue_o(x, n);
-        if (x == nx - 1) {  // V_n free once both products of tile n complete
-          if (lane == 0 && n + 2 < ntiles) tc::commit(bar(kBarVEmpty + (n & 1)));
-          __syncwarp();
-        }
+        if (x == nx - 1) release_v(n);
         if (n + 1 < ntiles) {
-          if (x == 0 && !(ok = wait_all(bar(kBarKFull + ((n + 1) & 1)), ((n + 1) >> 1) & 1)))
-            break;
+          if (x == 0 && !(ok = wait_all(k_ready(n + 1), ready_par(n + 1)))) break;
           if (!(ok = wait_all(bar(kBarO + x), n & 1))) break;  // P_X(n) consumed
           tc::fence_after_sync();
           issue_s(x, n + 1);
-          if (x == nx - 1) {
-            if (lane == 0 && n + 3 < ntiles) tc::commit(bar(kBarKEmpty + ((n + 1) & 1)));
-            __syncwarp();
-          }
+          if (x == nx - 1) release_k(n + 1);
         }
       }
     }
     if (!ok && lane == 0) atomicOr(a.err, PA_DEVERR_TIMEOUT);
+  } else if (warp >= kConvWarp0) {
+    // ------------------------------------------------------------ FP8 converters
+    // e4m3 K (V) tile n, ring stage n & 1 -> the f16 K (V) buffer: each
+    // 16-byte chunk of 16 codes becomes two 16-byte chunks of f16 in the
+    // 64-dim box that holds them; V rows outside [lo, hi] are written as zeros.
+    if constexpr (FP8) {
+      const int ct = tid - kConvWarp0 * 32;
+      bool ok = true;
+      for (int n = 0; ok && n < ntiles; ++n) {
+        const int t0 = lo16 + n * kKv;
+        for (int is_v = 0; is_v < 2; ++is_v) {
+          if (!(ok = wait_all(bar((is_v ? kBarVFull : kBarKFull) + (n & 1)), (n >> 1) & 1))) break;
+          // the buffer's previous tile: its products have completed
+          if (n > 0 && !(ok = wait_all(bar(is_v ? kBarCVFree : kBarCKFree), (n - 1) & 1))) break;
+          const uint32_t src0 = (is_v ? sV : sK) + (n & 1) * kRawBytes;
+          const uint32_t dst0 = is_v ? sVc : sKc;
+          for (int i = ct; i < kKv * 8; i += kConvWarps * 32) {
+            const int row = i >> 3, c = i & 7;
+            uint4 lo4 = make_uint4(0u, 0u, 0u, 0u), hi4 = lo4;
+            const int pos = t0 + row;
+            if (!is_v || (pos >= lo && pos <= hi)) {
+              uint32_t w0, w1, w2, w3;
+              lds_v4(src0 + row * 128 + ((c ^ (row & 7)) << 4), w0, w1, w2, w3);
+              lo4 = make_uint4(e4m3x2_to_f16x2(static_cast<uint16_t>(w0 & 0xffffu)),
+                               e4m3x2_to_f16x2(static_cast<uint16_t>(w0 >> 16)),
+                               e4m3x2_to_f16x2(static_cast<uint16_t>(w1 & 0xffffu)),
+                               e4m3x2_to_f16x2(static_cast<uint16_t>(w1 >> 16)));
+              hi4 = make_uint4(e4m3x2_to_f16x2(static_cast<uint16_t>(w2 & 0xffffu)),
+                               e4m3x2_to_f16x2(static_cast<uint16_t>(w2 >> 16)),
+                               e4m3x2_to_f16x2(static_cast<uint16_t>(w3 & 0xffffu)),
+                               e4m3x2_to_f16x2(static_cast<uint16_t>(w3 >> 16)));
+            }
+            const uint32_t dst = dst0 + (c >> 2) * kBoxBytes + row * 128;
+            const int c0 = 2 * (c & 3);
+            sts_v4(dst + ((c0 ^ (row & 7)) << 4), lo4);
+            sts_v4(dst + (((c0 + 1) ^ (row & 7)) << 4), hi4);
+          }
+          fence_proxy_async();  // the f16 tile, visible to the tensor core
+          mbar_arrive(bar(is_v ? kBarCVFull : kBarCKFull));
+          mbar_arrive(bar((is_v ? kBarVEmpty : kBarKEmpty) + (n & 1)));  // reload the stage
+        }
+      }
+      if (!ok && lane == 0) atomicOr(a.err, PA_DEVERR_TIMEOUT);
+    }
   } else {
     // ------------------------------------------------------------ softmax
     const int x = warp / kGroupWarps;  // row tile: 0 = A, 1 = B
@@ -306,16 +399,51 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int cnt = valid ? max(hi_r - lo_r + 1, 0) : 0;
     const size_t orow =
         ((static_cast<size_t>(b) * a.T + tq) * a.Hq + static_cast<size_t>(kvh) * a.G + hq) * kHd;
-    // a negative scale flips the sign of Q instead, so sc >= 0
-    const float sc = fabsf(a.score_scale);
+    // this row's score scale (log2 domain); a negative scale flips the sign
+    // of Q instead, so sc >= 0
+    float sc = fabsf(a.score_scale);
     {  // Q row -> shared memory (K-major, 128-byte swizzle)
       const uint32_t flip = a.score_scale < 0.f ? 0x80008000u : 0u;
       const uint4* src =
           reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(a.q) + orow);
       const uint32_t q_tile = sQ + x * kQBytes;
+      uint4 qv[16];
+#pragma unroll
+      for (int c = 0; c < 16; ++c) qv[c] = valid ? src[c] : make_uint4(0u, 0u, 0u, 0u);
+      if constexpr (FP8) {
+        // f16 after a power-of-two rescale: largest magnitude in [2^14, 2^15)
+        auto f = [&](uint32_t w, int hi) -> float {
+          const uint16_t h = static_cast<uint16_t>(hi ? w >> 16 : w & 0xffffu);
+          return QT == kBF16 ? __uint_as_float(static_cast<uint32_t>(h) << 16)
+                             : __half2float(__ushort_as_half(h));
+        };
+        float amax = 0.f;
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          const uint32_t w4[4] = {qv[c].x, qv[c].y, qv[c].z, qv[c].w};
+#pragma unroll
+          for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f(w4[i >> 1], i & 1)));
+        }
+        int sh = 0;
+        if (amax > 0.f && amax < INFINITY) {
+          int e;
+          frexpf(amax, &e);
+          sh = e - 15;
+        }
+        sc = ldexpf(sc, sh);
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          const uint32_t w4[4] = {qv[c].x, qv[c].y, qv[c].z, qv[c].w};
+          uint32_t o4[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            o4[i] = pack16x2<false>(ldexpf(f(w4[i], 0), -sh), ldexpf(f(w4[i], 1), -sh));
+          qv[c] = make_uint4(o4[0], o4[1], o4[2], o4[3]);
+        }
+      }
 #pragma unroll
       for (int c = 0; c < 16; ++c) {
-        uint4 v = valid ? src[c] : make_uint4(0u, 0u, 0u, 0u);
+        uint4 v = qv[c];
         v.x ^= flip, v.y ^= flip, v.z ^= flip, v.w ^= flip;
         sts_v4(q_tile + (c >> 3) * 16384 + r * 128 + (((c & 7) ^ (r & 7)) << 4), v);
       }
@@ -411,8 +539,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::st32(tS + 64 * h, pk);
       }
       l += ((sp[0] + sp[1]) + (sp[2] + sp[3])) + ((sp[4] + sp[5]) + (sp[6] + sp[7]));
-      if (x == 0 && (t0 < lo || t0 + kKv - 1 > hi)) {
+      if (!FP8 && x == 0 && (t0 < lo || t0 + kKv - 1 > hi)) {
         // edge tile: once it has landed, zero the V rows outside [lo, hi]
+        // (with FP8 caches the converters write those rows as zeros)
         if (!(ok = wait_all(bar(kBarVFull + (n & 1)), (n >> 1) & 1))) break;
         const uint32_t vt = sV + (n & 1) * kTileBytes;
         for (int i = r; i < kKv * 16; i += kRows) {
@@ -432,7 +561,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // the last product, then the output row
       if (ok && ntiles > 0) ok = wait_all(bar(kBarO + x), (ntiles - 1) & 1);
       tc::fence_after_sync();
-      const float inv = (ok && ntiles > 0 && l > 0.f) ? 1.f / l : 0.f;
+      const float inv = (ok && ntiles > 0 && l > 0.f) ? (FP8 ? a.v_scale : 1.f) / l : 0.f;
       uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(a.out) + orow);
 #pragma unroll
       for (int c0 = 0; c0 < kHd; c0 += 32) {
@@ -445,13 +574,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int i = 0; i < 32; ++i) ov[i] = 0u;
         }
         if (valid) {
+          constexpr bool kOutBf16 = QT == kBF16;
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
             const float* f = reinterpret_cast<const float*>(ov) + 8 * c;
-            dst[c0 / 8 + c] = make_uint4(pack16x2<kBf16>(f[0] * inv, f[1] * inv),
-                                         pack16x2<kBf16>(f[2] * inv, f[3] * inv),
-                                         pack16x2<kBf16>(f[4] * inv, f[5] * inv),
-                                         pack16x2<kBf16>(f[6] * inv, f[7] * inv));
+            dst[c0 / 8 + c] = make_uint4(pack16x2<kOutBf16>(f[0] * inv, f[1] * inv),
+                                         pack16x2<kOutBf16>(f[2] * inv, f[3] * inv),
+                                         pack16x2<kOutBf16>(f[4] * inv, f[5] * inv),
+                                         pack16x2<kOutBf16>(f[6] * inv, f[7] * inv));
           }
         }
       }
@@ -467,26 +597,26 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int QT>
+template <int QT, bool FP8>
 cudaError_t launch_typed(const CUtensorMap& tk, const CUtensorMap& tv, const ChunkArgs& a,
                          int grid, cudaStream_t s, bool pdl) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = Smem::kBytes;
+  cfg.blockDim = dim3(Smem<FP8>::kThreads);
+  cfg.dynamicSmemBytes = Smem<FP8>::kBytes;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, chunk_attn_tc128_kernel<QT>, tk, tv, a);
+  return cudaLaunchKernelEx(&cfg, chunk_attn_tc128_kernel<QT, FP8>, tk, tv, a);
 }
 
-template <int QT>
+template <int QT, bool FP8>
 cudaError_t set_smem() {
-  return cudaFuncSetAttribute(chunk_attn_tc128_kernel<QT>,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize, Smem::kBytes);
+  return cudaFuncSetAttribute(chunk_attn_tc128_kernel<QT, FP8>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, Smem<FP8>::kBytes);
 }
 
 }  // namespace
@@ -495,8 +625,10 @@ int chunk_tc_unit_rows() { return kUnitRows; }
 
 cudaError_t chunk_tc_prepare() {
   cudaError_t e;
-  if ((e = set_smem<kBF16>()) != cudaSuccess || (e = set_smem<kF16>()) != cudaSuccess) return e;
-  return chunk_tc_fp8_prepare();
+  if ((e = set_smem<kBF16, false>()) != cudaSuccess || (e = set_smem<kF16, false>()) != cudaSuccess ||
+      (e = set_smem<kBF16, true>()) != cudaSuccess || (e = set_smem<kF16, true>()) != cudaSuccess)
+    return e;
+  return cudaSuccess;
 }
 
 cudaError_t chunk_tc_launch(int qt, bool fp8, const CUtensorMap& tk, const CUtensorMap& tv,
@@ -505,9 +637,11 @@ cudaError_t chunk_tc_launch(int qt, bool fp8, const CUtensorMap& tk, const CUten
   if (grid <= 0) return cudaSuccess;
   if (grid > 0x7fffffffLL) return cudaErrorInvalidValue;
   const int g = static_cast<int>(grid);
-  if (fp8) return chunk_tc_fp8_launch(qt, tk, tv, a, g, s, pdl);
-  return qt == kBF16 ? launch_typed<kBF16>(tk, tv, a, g, s, pdl)
-                     : launch_typed<kF16>(tk, tv, a, g, s, pdl);
+  if (fp8)
+    return qt == kBF16 ? launch_typed<kBF16, true>(tk, tv, a, g, s, pdl)
+                       : launch_typed<kF16, true>(tk, tv, a, g, s, pdl);
+  return qt == kBF16 ? launch_typed<kBF16, false>(tk, tv, a, g, s, pdl)
+                     : launch_typed<kF16, false>(tk, tv, a, g, s, pdl);
 }
 
 }  // namespace pa

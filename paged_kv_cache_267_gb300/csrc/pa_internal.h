@@ -106,9 +106,9 @@ struct ReshapeArgs {
   float k_scale, v_scale;
 };
 
-// Chunked queries on the tensor-memory kernels (chunk_tc.cu for 16-bit
-// caches, chunk_tc_fp8.cu for e4m3): one CTA per (sequence, KV head, unit of
-// chunk_tc_unit_rows() (query, head) rows); head dim 128.
+// Chunked queries on the tensor-memory kernel (chunk_tc.cu): one CTA per
+// (sequence, KV head, unit of chunk_tc_unit_rows() (query, head) rows); head
+// dim 128, 16-bit or e4m3 caches.
 struct ChunkArgs {
   const void* q;                 // [B, T, Hq, D]
   void* out;                     // [B, T, Hq, D]
@@ -124,10 +124,6 @@ int chunk_tc_unit_rows();
 cudaError_t chunk_tc_prepare();  // once per device: the kernel's shared-memory size
 cudaError_t chunk_tc_launch(int qt, bool fp8, const CUtensorMap& tk, const CUtensorMap& tv,
                             const ChunkArgs& a, cudaStream_t s, bool pdl);
-// The e4m3 variant (chunk_tc_fp8.cu), reached through the two calls above.
-cudaError_t chunk_tc_fp8_prepare();
-cudaError_t chunk_tc_fp8_launch(int qt, const CUtensorMap& tk, const CUtensorMap& tv,
-                                const ChunkArgs& a, int grid, cudaStream_t s, bool pdl);
 
 // Kernel configuration chosen for a (cache type, q type, D, n-tiles) variant.
 struct DecodeVariant {
