@@ -51,9 +51,10 @@
 //
 // FP8 e4m3 caches (FP8 = true): the rings hold the raw e4m3 tiles (16 KB of
 // K and of V per tile), and two converter warps turn each into an f16 tile
-// of the layout above (exact), in one buffer for K and one for V that the
+// of the layout above (exact), in one buffer for K and two for V that the
 // products read; they write zeros for the V rows outside [lo, hi]. A
-// converted buffer is refilled once the products that read it completed.
+// converted buffer is refilled once the products that read it completed
+// (V is double-buffered: its products come last in a tile's chain).
 // Q is converted per row to f16 after a power-of-two rescale that brings its
 // largest magnitude into [2^14, 2^15); the rescale and k_scale fold into the
 // row's score scale, and v_scale is applied to the output.
@@ -83,10 +84,11 @@ constexpr uint32_t kTileBytes = 2 * kBoxBytes;  // K or V tile: [2 boxes][128 to
 constexpr uint32_t kRawBytes = kKv * kHd;       // e4m3 tile: [128 tokens][128 B]
 // barriers: K and V rings (full, empty; two stages each); per row tile X:
 // S_X computed, P_X written, O_X product complete; Q staged; FP8: the
-// converted K and V buffers written (full) and read by their products (free)
+// converted K buffer and the two V buffers written (full) and read by their
+// products (free)
 constexpr int kBarKFull = 0, kBarKEmpty = 2, kBarVFull = 4, kBarVEmpty = 6, kBarS = 8,
               kBarP = 10, kBarO = 12, kBarQ = 14, kBarCKFull = 15, kBarCKFree = 16,
-              kBarCVFull = 17, kBarCVFree = 18, kNumBars = 19;
+              kBarCVFull = 17, kBarCVFree = 19, kNumBars = 21;
 
 // Shared-memory layout: Q_A, Q_B, the K ring, the V ring, (FP8: the
 // converted K and V tiles), barriers, the tensor-memory address.
@@ -99,7 +101,7 @@ struct Smem {
   static constexpr uint32_t kV = kK + 2 * kRing;
   static constexpr uint32_t kKc = kV + 2 * kRing;
   static constexpr uint32_t kVc = kKc + (FP8 ? kTileBytes : 0);
-  static constexpr uint32_t kBar = kVc + (FP8 ? kTileBytes : 0);
+  static constexpr uint32_t kBar = kVc + (FP8 ? 2 * kTileBytes : 0);
   static constexpr uint32_t kSlot = kBar + 8 * kNumBars;
   static constexpr uint32_t kBytes = kSlot + 16 + 1024;  // + room to align the base to 1 KB
 };
@@ -159,10 +161,15 @@ __global__ void __launch_bounds__(Smem<FP8>::kThreads, 1)
   // the 16-bit K and V tiles the products read for K/V tile n, and the
   // barrier (with parity) that says they are ready
   auto tile_k = [&](int n) -> uint32_t { return FP8 ? sKc : sK + (n & 1) * kTileBytes; };
-  auto tile_v = [&](int n) -> uint32_t { return FP8 ? sVc : sV + (n & 1) * kTileBytes; };
+  auto tile_v = [&](int n) -> uint32_t {
+    return (FP8 ? sVc : sV) + (n & 1) * kTileBytes;
+  };
   auto k_ready = [&](int n) -> uint32_t { return FP8 ? bar(kBarCKFull) : bar(kBarKFull + (n & 1)); };
-  auto v_ready = [&](int n) -> uint32_t { return FP8 ? bar(kBarCVFull) : bar(kBarVFull + (n & 1)); };
-  auto ready_par = [&](int n) -> uint32_t { return FP8 ? n & 1 : (n >> 1) & 1; };
+  auto v_ready = [&](int n) -> uint32_t {
+    return bar((FP8 ? kBarCVFull : kBarVFull) + (n & 1));
+  };
+  auto k_par = [&](int n) -> uint32_t { return FP8 ? n & 1 : (n >> 1) & 1; };
+  auto v_par = [&](int n) -> uint32_t { return (n >> 1) & 1; };
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int ut = blockIdx.x % a.QT;  // unit (256 rows) within the (sequence, KV head)
@@ -186,8 +193,10 @@ __global__ void __launch_bounds__(Smem<FP8>::kThreads, 1)
     if constexpr (FP8) {
       mbar_init(bar(kBarCKFull), kConvWarps * 32);
       mbar_init(bar(kBarCKFree), 1);
-      mbar_init(bar(kBarCVFull), kConvWarps * 32);
-      mbar_init(bar(kBarCVFree), 1);
+      for (int j = 0; j < 2; ++j) {
+        mbar_init(bar(kBarCVFull + j), kConvWarps * 32);
+        mbar_init(bar(kBarCVFree + j), 1);
+      }
     }
     fence_mbar_init();
   }
@@ -306,14 +315,14 @@ __global__ void __launch_bounds__(Smem<FP8>::kThreads, 1)
     };
     auto release_v = [&](int t) {
       if (lane == 0) {
-        if (FP8 && t + 1 < ntiles) tc::commit(bar(kBarCVFree));
+        if (FP8 && t + 2 < ntiles) tc::commit(bar(kBarCVFree + (t & 1)));
         if (!FP8 && t + 2 < ntiles) tc::commit(bar(kBarVEmpty + (t & 1)));
       }
       __syncwarp();
     };
     bool ok = true;
     if (ntiles > 0) {
-      ok = wait_all(bar(kBarQ), 0) && wait_all(k_ready(0), ready_par(0));
+      ok = wait_all(bar(kBarQ), 0) && wait_all(k_ready(0), k_par(0));
       if (ok) {
         tc::fence_after_sync();
         for (int x = 0; x < nx; ++x) issue_s(x, 0);
@@ -326,12 +335,12 @@ __global__ void __launch_bounds__(Smem<FP8>::kThreads, 1)
       for (int x = 0; x < nx; ++x) {
         // P_X(n) written (by group A: the V rows of an edge tile cleaned)
         if (!(ok = wait_all(bar(kBarP + x), n & 1))) break;
-        if (x == 0 && !(ok = wait_all(v_ready(n), ready_par(n)))) break;
+        if (x == 0 && !(ok = wait_all(v_ready(n), v_par(n)))) break;
         tc::fence_after_sync();
         issue_o(x, n);
         if (x == nx - 1) release_v(n);
         if (n + 1 < ntiles) {
-          if (x == 0 && !(ok = wait_all(k_ready(n + 1), ready_par(n + 1)))) break;
+          if (x == 0 && !(ok = wait_all(k_ready(n + 1), k_par(n + 1)))) break;
           if (!(ok = wait_all(bar(kBarO + x), n & 1))) break;  // P_X(n) consumed
           tc::fence_after_sync();
           issue_s(x, n + 1);
@@ -352,10 +361,12 @@ __global__ void __launch_bounds__(Smem<FP8>::kThreads, 1)
         const int t0 = lo16 + n * kKv;
         for (int is_v = 0; is_v < 2; ++is_v) {
           if (!(ok = wait_all(bar((is_v ? kBarVFull : kBarKFull) + (n & 1)), (n >> 1) & 1))) break;
-          // the buffer's previous tile: its products have completed
-          if (n > 0 && !(ok = wait_all(bar(is_v ? kBarCVFree : kBarCKFree), (n - 1) & 1))) break;
+          // the buffer's previous tile (K: n-1; V: n-2): its products completed
+          if (!is_v && n > 0 && !(ok = wait_all(bar(kBarCKFree), (n - 1) & 1))) break;
+          if (is_v && n > 1 && !(ok = wait_all(bar(kBarCVFree + (n & 1)), ((n - 2) >> 1) & 1)))
+            break;
           const uint32_t src0 = (is_v ? sV : sK) + (n & 1) * kRawBytes;
-          const uint32_t dst0 = is_v ? sVc : sKc;
+          const uint32_t dst0 = is_v ? sVc + (n & 1) * kTileBytes : sKc;
           for (int i = ct; i < kKv * 8; i += kConvWarps * 32) {
             const int row = i >> 3, c = i & 7;
             uint4 lo4 = make_uint4(0u, 0u, 0u, 0u), hi4 = lo4;
@@ -378,7 +389,7 @@ __global__ void __launch_bounds__(Smem<FP8>::kThreads, 1)
             sts_v4(dst + (((c0 + 1) ^ (row & 7)) << 4), hi4);
           }
           fence_proxy_async();  // the f16 tile, visible to the tensor core
-          mbar_arrive(bar(is_v ? kBarCVFull : kBarCKFull));
+          mbar_arrive(bar(is_v ? kBarCVFull + (n & 1) : kBarCKFull));
           mbar_arrive(bar((is_v ? kBarVEmpty : kBarKEmpty) + (n & 1)));  // reload the stage
         }
       }

@@ -156,6 +156,33 @@ def test_chunk_kernels_forced(case, path, pa_lib):
     assert pa_lib.check_device_error() == 0
 
 
+SCALES = [
+    # scale, cache: a negative scale (the tensor-memory kernel flips Q's sign
+    # to take the row max on raw scores), zero (uniform weights; masked
+    # scores must still give exactly zero), and a large one (scores spread
+    # over about +-30 log2 units: many reference-max moves and O rescales)
+    (-0.0884, "bf16"), (0.0, "bf16"), (1.0, "bf16"), (-0.0884, "fp8"), (1.0, "fp8"),
+]
+
+
+@pytest.mark.parametrize("path", [1, 2], ids=["persistent", "tensor_memory"])
+@pytest.mark.parametrize("scale,cache", SCALES, ids=[f"s{c[0]}_{c[1]}" for c in SCALES])
+def test_chunk_softmax_scale_range(scale, cache, path, pa_lib):
+    """Both chunk kernels against the oracle for softmax scales other than
+    1/sqrt(D), with a window and a tile boundary inside the chunk."""
+    fp8 = cache == "fp8"
+    spec = _spec(40, 32, 8, 128, 16, 100, "bf16", fp8, lens=(0, 39, 40, 41, 200, 300, 129, 77),
+                 seed=2700 + path, scale=scale)
+    pa_lib.set_prefill_path(path)
+    try:
+        sides = run_chunk(spec)
+    finally:
+        pa_lib.set_prefill_path(0)
+    got = out_f64(sides.out)
+    assert_close(got, sides.ref, what=f"scale {scale} {cache} path {path}", rel=CHUNK_REL_TOL)
+    assert pa_lib.check_device_error() == 0
+
+
 @pytest.mark.parametrize("path", [1, 2], ids=["persistent", "tensor_memory"])
 def test_chunk_bad_block_id_and_long_seq_are_flagged_not_faulted(path, pa_lib):
     """Device-side data errors in a chunk call: a block id outside the pool and
