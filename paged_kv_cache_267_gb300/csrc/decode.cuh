@@ -379,10 +379,14 @@ __global__ void __launch_bounds__(WARPS * 32, 2)
       const uint32_t bar = wbars + 8 * slot;
       const uint32_t kd = ring + slot * Gm::STAGE_BYTES;
       mbar_arrive_expect_tx(bar, Gm::STAGE_BYTES);
+      // K/V are read once per step: evict them first, so the stream does not
+      // push the partials (read by the merge right after) out of L2
+      const uint64_t kv_policy = l2_evict_first();
 #pragma unroll
       for (int j = 0; j < Gm::BOXES; ++j) {
-        tma_load_2d(kd + j * 2048, &tmK, j * Gm::BOX_ELEMS, row, bar);
-        tma_load_2d(kd + Gm::TILE_BYTES + j * 2048, &tmV, j * Gm::BOX_ELEMS, row, bar);
+        tma_load_2d_hint(kd + j * 2048, &tmK, j * Gm::BOX_ELEMS, row, bar, kv_policy);
+        tma_load_2d_hint(kd + Gm::TILE_BYTES + j * 2048, &tmV, j * Gm::BOX_ELEMS, row, bar,
+                         kv_policy);
       }
     }
     __syncwarp();

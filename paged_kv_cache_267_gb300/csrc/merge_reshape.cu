@@ -48,11 +48,13 @@ struct HeadAcc {
 };
 
 // Folds candidates k0, k0 + step, ... (< k1) of head h into `r`, with
-// 8 / (2 VPL) candidates' loads in flight per lane.
+// U = 8 / VPL candidates' loads in flight per lane (a group of 16 partials
+// is two round trips). Lane j < U reads candidate j's max and sum, which the
+// fold takes by shuffle.
 template <int VPL, typename SlotFn>
 __device__ __forceinline__ void merge_fold(const MergeArgs& a, SlotFn slot_of, int k0, int k1,
                                            int step, int h, HeadAcc<VPL>& r) {
-  constexpr int U = 4 / VPL;
+  constexpr int U = 8 / VPL;
   const int lane = threadIdx.x & 31;
   const int GD = a.CG * a.D;
   const size_t stride = static_cast<size_t>(part_stride(a.CG, a.D));
@@ -62,32 +64,32 @@ __device__ __forceinline__ void merge_fold(const MergeArgs& a, SlotFn slot_of, i
   for (int v = 0; v < VPL; ++v) r.acc[v] = make_float4(0.f, 0.f, 0.f, 0.f);
   const bool on = 4 * lane < a.D;  // D = 64 uses half the lanes
   for (int k = k0; k < k1; k += U * step) {
-    float mm[U], ll[U];
+    float my_m = -INFINITY, my_l = 0.f;
+    if (lane < U && k + lane * step < k1) {
+      const float* P = a.part + static_cast<size_t>(slot_of(k + lane * step)) * stride;
+      my_m = P[GD + h];
+      my_l = P[GD + a.CG + h];
+    }
     float4 o[U][VPL];
 #pragma unroll
     for (int j = 0; j < U; ++j) {
       const int kk = k + j * step;
-      mm[j] = -INFINITY;
-      ll[j] = 0.f;
 #pragma unroll
       for (int v = 0; v < VPL; ++v) o[j][v] = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (kk < k1) {
+      if (kk < k1 && on) {
         const float* P = a.part + static_cast<size_t>(slot_of(kk)) * stride;
-        mm[j] = P[GD + h];
-        ll[j] = P[GD + a.CG + h];
-        if (on) {
 #pragma unroll
-          for (int v = 0; v < VPL; ++v)
-            o[j][v] = *reinterpret_cast<const float4*>(P + h * a.D + v * 128 + 4 * lane);
-        }
+        for (int v = 0; v < VPL; ++v)
+          o[j][v] = *reinterpret_cast<const float4*>(P + h * a.D + v * 128 + 4 * lane);
       }
     }
 #pragma unroll
     for (int j = 0; j < U; ++j) {
+      const float mj = __shfl_sync(0xffffffffu, my_m, j), lj = __shfl_sync(0xffffffffu, my_l, j);
       if (k + j * step >= k1) break;
-      const float Mn = fmaxf(r.M, mm[j]);
-      const float sc = fast_exp2(r.M - Mn), f = fast_exp2(mm[j] - Mn);
-      r.den = r.den * sc + f * ll[j];
+      const float Mn = fmaxf(r.M, mj);
+      const float sc = fast_exp2(r.M - Mn), f = fast_exp2(mj - Mn);
+      r.den = r.den * sc + f * lj;
 #pragma unroll
       for (int v = 0; v < VPL; ++v) {
         r.acc[v].x = r.acc[v].x * sc + f * o[j][v].x;
@@ -151,7 +153,7 @@ __device__ __forceinline__ Cands pair_cands(int F, int nt, int ws, int ts, int p
 // latter are enumerated through a prefix over sequences (written by the
 // decode kernel), and a unit whose group turns out empty is skipped.
 template <int OT, int VPL>
-__global__ void __launch_bounds__(kMergeThreads, 4) merge_kernel(const MergeArgs a) {
+__global__ void __launch_bounds__(kMergeThreads, 3) merge_kernel(const MergeArgs a) {
   extern __shared__ int s_dyn[];
   int* s_pref = s_dyn;             // B + 1 tile prefix
   int* s_extra = s_dyn + a.B + 1;  // B + 1 prefix of extra units per sequence

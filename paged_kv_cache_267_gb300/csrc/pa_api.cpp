@@ -748,7 +748,7 @@ pa_status run_decode(const DecodeCall& c, DeviceState* st, const DecodePlan& pla
   m.NCG = a.NCG;
   m.CG = a.CG;
   m.Hv = a.Hv;
-  e = pa::merge_launch(c.qt, m, st->num_sms * 4, cs, !prof);
+  e = pa::merge_launch(c.qt, m, st->num_sms * 3, cs, !prof);
   if (e != cudaSuccess) {
     if (wsp) {
       std::lock_guard<std::mutex> lk(g_mu);
