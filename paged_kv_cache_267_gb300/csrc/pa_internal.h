@@ -69,8 +69,8 @@ struct MergeArgs {
   int T, NCG, CG, Hv;            // as in DecodeArgs
 };
 
-constexpr int kMergeGroupsMax = 16;   // groups of partials per q head, at most
-constexpr int kMergeGroupMin = 16;    // partials per group, at least
+constexpr int kMergeGroupsMax = 8;    // groups of partials per q head, at most
+constexpr int kMergeGroupMin = 8;     // partials per group, at least (one round trip of the fold)
 constexpr int kMaxMergeCounters = 1 << 19;
 
 // Partials per merge group for a head with n candidate partials.
