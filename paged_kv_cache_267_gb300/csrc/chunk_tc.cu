@@ -134,6 +134,12 @@ __device__ __forceinline__ uint32_t pack16x2(float lo, float hi) {
     return *reinterpret_cast<uint32_t*>(&v);
   }
 }
+// max of three (one instruction on sm_103a)
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
 __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -483,13 +489,18 @@ __global__ void __launch_bounds__(Smem<FP8>::kThreads, 1)
         tc::wait_ld(sv[0], sv[1]);
         if (all_in) {
 #pragma unroll
-          for (int j = 0; j < 64; ++j)
-            mxp[j & 7] = fmaxf(mxp[j & 7], __uint_as_float(sv[j >> 5][j & 31]));
+          for (int j = 0; j < 32; ++j)
+            mxp[j & 7] = fmax3(mxp[j & 7], __uint_as_float(sv[j >> 4][(2 * j) & 31]),
+                               __uint_as_float(sv[j >> 4][(2 * j + 1) & 31]));
         } else {
 #pragma unroll
-          for (int j = 0; j < 64; ++j) {
-            const bool keep = static_cast<unsigned>(d0 + 64 * h + j) < static_cast<unsigned>(cnt);
-            mxp[j & 7] = fmaxf(mxp[j & 7], keep ? __uint_as_float(sv[j >> 5][j & 31]) : -INFINITY);
+          for (int j = 0; j < 32; ++j) {
+            const int e = d0 + 64 * h + 2 * j;
+            const float v0 = __uint_as_float(sv[j >> 4][(2 * j) & 31]);
+            const float v1 = __uint_as_float(sv[j >> 4][(2 * j + 1) & 31]);
+            mxp[j & 7] = fmax3(mxp[j & 7],
+                               static_cast<unsigned>(e) < static_cast<unsigned>(cnt) ? v0 : -INFINITY,
+                               static_cast<unsigned>(e + 1) < static_cast<unsigned>(cnt) ? v1 : -INFINITY);
           }
         }
       }
