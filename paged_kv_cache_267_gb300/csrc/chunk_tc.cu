@@ -373,26 +373,33 @@ __global__ void __launch_bounds__(Smem<FP8>::kThreads, 1)
             break;
           const uint32_t src0 = (is_v ? sV : sK) + (n & 1) * kRawBytes;
           const uint32_t dst0 = is_v ? sVc + (n & 1) * kTileBytes : sKc;
-          for (int i = ct; i < kKv * 8; i += kConvWarps * 32) {
-            const int row = i >> 3, c = i & 7;
-            uint4 lo4 = make_uint4(0u, 0u, 0u, 0u), hi4 = lo4;
-            const int pos = t0 + row;
-            if (!is_v || (pos >= lo && pos <= hi)) {
-              uint32_t w0, w1, w2, w3;
-              lds_v4(src0 + row * 128 + ((c ^ (row & 7)) << 4), w0, w1, w2, w3);
-              lo4 = make_uint4(e4m3x2_to_f16x2(static_cast<uint16_t>(w0 & 0xffffu)),
-                               e4m3x2_to_f16x2(static_cast<uint16_t>(w0 >> 16)),
-                               e4m3x2_to_f16x2(static_cast<uint16_t>(w1 & 0xffffu)),
-                               e4m3x2_to_f16x2(static_cast<uint16_t>(w1 >> 16)));
-              hi4 = make_uint4(e4m3x2_to_f16x2(static_cast<uint16_t>(w2 & 0xffffu)),
-                               e4m3x2_to_f16x2(static_cast<uint16_t>(w2 >> 16)),
-                               e4m3x2_to_f16x2(static_cast<uint16_t>(w3 & 0xffffu)),
-                               e4m3x2_to_f16x2(static_cast<uint16_t>(w3 >> 16)));
+          // thread ct converts 16-byte chunk c of rows r0, r0 + 8, ..., r0 + 120:
+          // the same swizzle for all of them (row & 7 == r0), 1 KB apart
+          static_assert(kConvWarps * 32 == 64, "8 rows x 8 chunks per pass");
+          const int c = ct & 7, r0 = ct >> 3, c0 = 2 * (c & 3);
+          const uint32_t src = src0 + r0 * 128 + ((c ^ r0) << 4);
+          const uint32_t dst = dst0 + (c >> 2) * kBoxBytes + r0 * 128;
+          const uint32_t d_lo = dst + ((c0 ^ r0) << 4), d_hi = dst + (((c0 + 1) ^ r0) << 4);
+          // V rows outside [lo, hi] are written as zeros (edge tiles only)
+          const bool edge = is_v && (t0 < lo || t0 + kKv - 1 > hi);
+#pragma unroll
+          for (int k = 0; k < kKv / 8; ++k) {
+            uint32_t w0, w1, w2, w3;
+            lds_v4(src + k * 1024, w0, w1, w2, w3);
+            uint4 lo4 = make_uint4(e4m3x2_to_f16x2(static_cast<uint16_t>(w0 & 0xffffu)),
+                                   e4m3x2_to_f16x2(static_cast<uint16_t>(w0 >> 16)),
+                                   e4m3x2_to_f16x2(static_cast<uint16_t>(w1 & 0xffffu)),
+                                   e4m3x2_to_f16x2(static_cast<uint16_t>(w1 >> 16)));
+            uint4 hi4 = make_uint4(e4m3x2_to_f16x2(static_cast<uint16_t>(w2 & 0xffffu)),
+                                   e4m3x2_to_f16x2(static_cast<uint16_t>(w2 >> 16)),
+                                   e4m3x2_to_f16x2(static_cast<uint16_t>(w3 & 0xffffu)),
+                                   e4m3x2_to_f16x2(static_cast<uint16_t>(w3 >> 16)));
+            if (edge) {
+              const int pos = t0 + r0 + 8 * k;
+              if (pos < lo || pos > hi) lo4 = hi4 = make_uint4(0u, 0u, 0u, 0u);
             }
-            const uint32_t dst = dst0 + (c >> 2) * kBoxBytes + row * 128;
-            const int c0 = 2 * (c & 3);
-            sts_v4(dst + ((c0 ^ (row & 7)) << 4), lo4);
-            sts_v4(dst + (((c0 + 1) ^ (row & 7)) << 4), hi4);
+            sts_v4(d_lo + k * 1024, lo4);
+            sts_v4(d_hi + k * 1024, hi4);
           }
           fence_proxy_async();  // the f16 tile, visible to the tensor core
           mbar_arrive(bar(is_v ? kBarCVFull + (n & 1) : kBarCKFull));
