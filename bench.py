@@ -233,21 +233,28 @@ def rank_spec(config: str, rank: int):
 
 # ----------------------------------------------------------- oracle timing
 
-def oracle_baseline(w, kc_host, vc_host, budget_s: float, seq_subset=None) -> dict:
+def oracle_baseline(w, kc_host, vc_host, budget_s: float, seq_subset=None,
+                    queries=None) -> dict:
+    """Times the oracle on sequences `seq_subset` (default all) and, for a
+    chunk, query positions `queries` of each (default all), all heads. The
+    bytes are the step's algorithmic bytes for that share: each sequence's
+    K/V read range once, scaled by the share of its queries computed, plus q
+    and out of the computed rows."""
     import oracle
     s = w.spec
     B = s.batch
     seqs = list(range(B)) if seq_subset is None else list(seq_subset)
     T = s.num_queries
+    ts = list(range(T)) if queries is None else list(queries)
     pairs = np.array([(b, h) for b in seqs for h in range(s.num_q_heads)], np.int32)
-    triples = np.array([(b, t, h) for b in seqs for t in range(T)
+    triples = np.array([(b, t, h) for b in seqs for t in ts
                         for h in range(s.num_q_heads)], np.int32)
     sel = np.zeros(B, bool)
     sel[seqs] = True
     L = w.seq_lens.astype(np.int64)
     n = (L - w.starts)[sel]
     elt = 1 if s.kv_fp8 else 2
-    bytes_ = (int(n.sum()) * s.num_kv_heads * 2 * s.head_dim * elt
+    bytes_ = (int(n.sum()) * s.num_kv_heads * 2 * s.head_dim * elt * len(ts) / T
               + 2 * len(triples) * s.head_dim * 2)
     threads = oracle.default_threads()
     qh = w.q.cpu()
@@ -269,8 +276,24 @@ def oracle_baseline(w, kc_host, vc_host, budget_s: float, seq_subset=None) -> di
     return {"value": bytes_ / per / 1e9, "unit": UNIT, "cores": threads, "kind": "oracle",
             "seconds_per_sample": per,
             "sample": f"fp64 C oracle decode of {len(seqs)} of {B} sequences x "
-                      f"{T} queries x {s.num_q_heads} heads ({int(n.sum())} tokens in the "
-                      f"read ranges), {reps} run(s)"}
+                      f"{len(ts)} of {T} queries x {s.num_q_heads} heads ({int(n.sum())} "
+                      f"tokens in the read ranges), {reps} run(s)"}
+
+
+def bounded_sample(w, kc_host, vc_host, budget_s: float):
+    """(sequences, queries) whose oracle run takes about `budget_s` or less:
+    whole sequences while they fit, else evenly spaced query positions of the
+    first sequence (a chunk's queries are independent rows)."""
+    s = w.spec
+    T = s.num_queries
+    probe = oracle_baseline(w, kc_host, vc_host, 0.0, seq_subset=[0], queries=[T - 1])
+    per_query = max(probe["seconds_per_sample"], 1e-6)  # the longest row of sequence 0
+    per_seq = per_query * T
+    if per_seq <= budget_s:
+        nseq = int(max(1, min(s.batch, budget_s / per_seq)))
+        return list(range(nseq)), None
+    nq = int(max(1, min(T, budget_s / per_query)))
+    return [0], sorted({int(round(i * (T - 1) / max(1, nq - 1))) for i in range(nq)})
 
 
 def host_caches(w, kc, vc):
@@ -303,18 +326,16 @@ def run_reference(args, world, rank):
         kc, vc = host_caches(w, w.key_cache, w.value_cache)
     oracle.reshape_and_cache(w.k_new, w.v_new, kc, vc, w.slot_new.numpy(), s.dtype,
                              "fp8" if s.kv_fp8 else s.dtype, w.k_scale, w.v_scale)
-    # bounded sample per step: a few sequences, sized so the whole run stays short
+    # bounded sample per step, sized so the whole run stays short
     total_budget = 120.0
     per_step = max(0.01, total_budget / max(1, args.steps + args.warmup))
-    probe = oracle_baseline(w, kc, vc, budget_s=0.0, seq_subset=[0])
-    per_seq = probe["seconds_per_sample"]
-    nseq = int(max(1, min(s.batch, per_step / max(per_seq, 1e-6))))
-    subset = list(range(nseq))
+    subset, queries = bounded_sample(w, kc, vc, per_step)
+    nseq = len(subset)
     for _ in range(args.warmup):
-        oracle_baseline(w, kc, vc, 0.0, subset)
+        oracle_baseline(w, kc, vc, 0.0, subset, queries)
     times, vals = [], []
     for _ in range(args.steps):
-        r = oracle_baseline(w, kc, vc, 0.0, subset)
+        r = oracle_baseline(w, kc, vc, 0.0, subset, queries)
         times.append(r["seconds_per_sample"])
         vals.append(r["value"])
     ms = 1e3 * statistics.mean(times)
@@ -324,7 +345,9 @@ def run_reference(args, world, rank):
             "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": f"{args.config}: {workload_desc(s)}",
-                       "sample_per_step": f"{nseq} of {s.batch} sequences, all heads"},
+                       "sample_per_step": (f"{nseq} of {s.batch} sequences, all heads" if queries is None
+                                           else f"{len(queries)} of {s.num_queries} queries of "
+                                                f"sequence 0, all heads")},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": r["cores"],
                              "kind": "oracle", "sample": r["sample"]},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
@@ -552,7 +575,9 @@ def run_ours(args, world, rank, local):
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.quick:
         kch, vch = host_caches(w, kc, vc)
-        cpu = oracle_baseline(w, kch, vch, budget_s=args.cpu_budget)
+        subset, queries = bounded_sample(w, kch, vch, args.cpu_budget / 2)
+        cpu = oracle_baseline(w, kch, vch, budget_s=args.cpu_budget, seq_subset=subset,
+                              queries=queries)
 
     if rank != 0:
         return
