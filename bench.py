@@ -293,7 +293,9 @@ def bounded_sample(w, kc_host, vc_host, budget_s: float):
         nseq = int(max(1, min(s.batch, budget_s / per_seq)))
         return list(range(nseq)), None
     nq = int(max(1, min(T, budget_s / per_query)))
-    return [0], sorted({int(round(i * (T - 1) / max(1, nq - 1))) for i in range(nq)})
+    if nq == 1:
+        return [0], [(T - 1) // 2]  # the middle row: a chunk's rows grow with t
+    return [0], sorted({int(round(i * (T - 1) / (nq - 1))) for i in range(nq)})
 
 
 def host_caches(w, kc, vc):
