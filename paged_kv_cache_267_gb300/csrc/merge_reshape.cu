@@ -31,7 +31,8 @@ cudaError_t device_error_word(int32_t** ptr) {
 // Work units are (group g of candidates, column of pair s), one warp each,
 // spread over a persistent grid of many warps per SM so that the L2 latency
 // of one unit hides behind the others. A unit folds its candidates in online
-// (four loads in flight per lane). A head whose candidates fit one group is
+// (eight loads in flight per lane; groups of max(8, ceil(n / 8)) of a head's
+// n candidates, so at most eight groups). A head whose candidates fit one group is
 // written out directly; otherwise each unit stores its group result, which
 // has the same form as a partial, in place in the slot of the group's first
 // candidate, and the unit that completes the head's counter combines the
@@ -48,9 +49,9 @@ struct HeadAcc {
 };
 
 // Folds candidates k0, k0 + step, ... (< k1) of head h into `r`, with
-// U = 8 / VPL candidates' loads in flight per lane (a group of 16 partials
-// is two round trips). Lane j < U reads candidate j's max and sum, which the
-// fold takes by shuffle.
+// U = 8 / VPL candidates' loads in flight per lane (a group of 8 partials is
+// one round trip for D <= 128). Lane j < U reads candidate j's max and sum,
+// which the fold takes by shuffle.
 template <int VPL, typename SlotFn>
 __device__ __forceinline__ void merge_fold(const MergeArgs& a, SlotFn slot_of, int k0, int k1,
                                            int step, int h, HeadAcc<VPL>& r) {
