@@ -237,17 +237,23 @@ __global__ void __launch_bounds__(kMergeThreads, 3) merge_kernel(const MergeArgs
         P[GD + a.CG + h] = r.den;
       }
     }
-    __threadfence();
+    // the warp's stores, then lane 0's release increment; the unit that
+    // completes the count reads the group results after its acquire (the
+    // warp barriers order the other lanes' stores and loads around lane 0's)
     __syncwarp();
     int last = 0;
     if (lane == 0) {
-      const uint32_t done = atomicAdd(a.counters + hr, 1u) + 1;
-      last = (done == static_cast<uint32_t>(ngroups));
+      uint32_t prev;
+      asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;"
+                   : "=r"(prev)
+                   : "l"(a.counters + hr)
+                   : "memory");
+      last = (prev + 1 == static_cast<uint32_t>(ngroups));
       if (last) a.counters[hr] = 0u;
     }
     last = __shfl_sync(0xffffffffu, last, 0);
     if (!last) continue;
-    __threadfence();
+    __syncwarp();
     // combine the group results (the first candidate of each group)
     merge_fold(a, slot_of, 0, ngroups * gsz, gsz, h, r);
     store_head<OT, VPL>(a, orow, r, false);
