@@ -54,7 +54,9 @@
 // of the layout above (exact), in one buffer for K and two for V that the
 // products read; they write zeros for the V rows outside [lo, hi]. A
 // converted buffer is refilled once the products that read it completed
-// (V is double-buffered: its products come last in a tile's chain).
+// (V is double-buffered: its products come last in a tile's chain). K is
+// converted head dims 0-63 first: S's first four steps start on them while
+// dims 64-127 are converted.
 // Q is converted per row to f16 after a power-of-two rescale that brings its
 // largest magnitude into [2^14, 2^15); the rescale and k_scale fold into the
 // row's score scale, and v_scale is applied to the output.
@@ -87,8 +89,9 @@ constexpr uint32_t kRawBytes = kKv * kHd;       // e4m3 tile: [128 tokens][128 B
 // converted K buffer and the two V buffers written (full) and read by their
 // products (free)
 constexpr int kBarKFull = 0, kBarKEmpty = 2, kBarVFull = 4, kBarVEmpty = 6, kBarS = 8,
-              kBarP = 10, kBarO = 12, kBarQ = 14, kBarCKFull = 15, kBarCKFree = 16,
-              kBarCVFull = 17, kBarCVFree = 19, kNumBars = 21;
+              kBarP = 10, kBarO = 12, kBarQ = 14, kBarCKFull = 15 /* dims 0-63 */,
+              kBarCKFree = 16, kBarCVFull = 17, kBarCVFree = 19, kBarCKFull1 = 21 /* 64-127 */,
+              kNumBars = 22;
 
 // Shared-memory layout: Q_A, Q_B, the K ring, the V ring, (FP8: the
 // converted K and V tiles), barriers, the tensor-memory address.
@@ -198,6 +201,7 @@ __global__ void __launch_bounds__(Smem<FP8>::kThreads, 1)
     mbar_init(bar(kBarQ), 2 * kGroupWarps * 32);
     if constexpr (FP8) {
       mbar_init(bar(kBarCKFull), kConvWarps * 32);
+      mbar_init(bar(kBarCKFull1), kConvWarps * 32);
       mbar_init(bar(kBarCKFree), 1);
       for (int j = 0; j < 2; ++j) {
         mbar_init(bar(kBarCVFull + j), kConvWarps * 32);
@@ -277,21 +281,24 @@ __global__ void __launch_bounds__(Smem<FP8>::kThreads, 1)
     // ------------------------------------------------------------ MMA issue
     constexpr uint32_t idS = tc::idesc_f16(kRows, kKv, kBf16, false);
     constexpr uint32_t idO = tc::idesc_f16(kRows, kHd, kBf16, true);
-    // S_X = Q_X . K_n^T over the 128 head dims (8 steps of 16)
-    auto issue_s = [&](int x, int n) {
+    // S_X = Q_X . K_n^T over head dims [64 b0, 64 b1) (4 steps of 16 per
+    // 64-dim box); the commit once all 8 steps are issued
+    auto issue_s_part = [&](int x, int n, int b0, int b1) {
       if (lane == 0) {
         const uint32_t kt = tile_k(n);
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
+          if (ks < 4 * b0 || ks >= 4 * b1) continue;
           const uint32_t box = ks >> 2, kk = (ks & 3) * 32;
           const uint64_t ad = tc::sdesc_sw128(sQ + x * kQBytes + box * 16384 + kk, 16, 1024);
           const uint64_t bd = tc::sdesc_sw128(kt + box * kBoxBytes + kk, 16, 1024);
           tc::mma_f16(tmem + kColS + 128 * x, ad, bd, idS, ks > 0);
         }
-        tc::commit(bar(kBarS + x));
+        if (b1 == 2) tc::commit(bar(kBarS + x));
       }
       __syncwarp();
     };
+    auto issue_s = [&](int x, int n) { issue_s_part(x, n, 0, 2); };
     // O_X (+)= P_X . V_n over 128 tokens (8 steps of 16); P_X in columns
     // 0-31 and 64-95 of S_X, 8 columns (16 tokens) per step
     auto issue_o = [&](int x, int n) {
@@ -328,7 +335,8 @@ __global__ void __launch_bounds__(Smem<FP8>::kThreads, 1)
     };
     bool ok = true;
     if (ntiles > 0) {
-      ok = wait_all(bar(kBarQ), 0) && wait_all(k_ready(0), k_par(0));
+      ok = wait_all(bar(kBarQ), 0) && wait_all(k_ready(0), k_par(0)) &&
+           (!FP8 || wait_all(bar(kBarCKFull1), 0));
       if (ok) {
         tc::fence_after_sync();
         for (int x = 0; x < nx; ++x) issue_s(x, 0);
@@ -349,7 +357,15 @@ __global__ void __launch_bounds__(Smem<FP8>::kThreads, 1)
           if (x == 0 && !(ok = wait_all(k_ready(n + 1), k_par(n + 1)))) break;
           if (!(ok = wait_all(bar(kBarO + x), n & 1))) break;  // P_X(n) consumed
           tc::fence_after_sync();
-          issue_s(x, n + 1);
+          if (FP8 && x == 0) {
+            // dims 0-63 of K_{n+1} are converted; 64-127 may still be under way
+            issue_s_part(0, n + 1, 0, 1);
+            if (!(ok = wait_all(bar(kBarCKFull1), (n + 1) & 1))) break;
+            tc::fence_after_sync();
+            issue_s_part(0, n + 1, 1, 2);
+          } else {
+            issue_s(x, n + 1);
+          }
           if (x == nx - 1) release_k(n + 1);
         }
       }
@@ -373,36 +389,49 @@ __global__ void __launch_bounds__(Smem<FP8>::kThreads, 1)
             break;
           const uint32_t src0 = (is_v ? sV : sK) + (n & 1) * kRawBytes;
           const uint32_t dst0 = is_v ? sVc + (n & 1) * kTileBytes : sKc;
-          // thread ct converts 16-byte chunk c of rows r0, r0 + 8, ..., r0 + 120:
-          // the same swizzle for all of them (row & 7 == r0), 1 KB apart
-          static_assert(kConvWarps * 32 == 64, "8 rows x 8 chunks per pass");
-          const int c = ct & 7, r0 = ct >> 3, c0 = 2 * (c & 3);
-          const uint32_t src = src0 + r0 * 128 + ((c ^ r0) << 4);
-          const uint32_t dst = dst0 + (c >> 2) * kBoxBytes + r0 * 128;
-          const uint32_t d_lo = dst + ((c0 ^ r0) << 4), d_hi = dst + (((c0 + 1) ^ r0) << 4);
-          // V rows outside [lo, hi] are written as zeros (edge tiles only)
-          const bool edge = is_v && (t0 < lo || t0 + kKv - 1 > hi);
+          // a pass converts 16-byte chunks [c_lo, c_lo + nc) of every row:
+          // thread ct takes chunk c_lo + ct % nc of rows r0, r0 + per, ...
+          // (per = 64 / nc, so row & 7 == r0 & 7: one swizzle per thread)
+          static_assert(kConvWarps * 32 == 64, "64 converter threads");
+          auto convert = [&](int c_lo, int nc) {
+            const int per = 64 / nc;
+            const int c = c_lo + ct % nc, r0 = ct / nc, c0 = 2 * (c & 3);
+            const uint32_t src = src0 + r0 * 128 + ((c ^ (r0 & 7)) << 4);
+            const uint32_t dst = dst0 + (c >> 2) * kBoxBytes + r0 * 128;
+            const uint32_t d_lo = dst + ((c0 ^ (r0 & 7)) << 4);
+            const uint32_t d_hi = dst + (((c0 + 1) ^ (r0 & 7)) << 4);
+            // V rows outside [lo, hi] are written as zeros (edge tiles only)
+            const bool edge = is_v && (t0 < lo || t0 + kKv - 1 > hi);
 #pragma unroll
-          for (int k = 0; k < kKv / 8; ++k) {
-            uint32_t w0, w1, w2, w3;
-            lds_v4(src + k * 1024, w0, w1, w2, w3);
-            uint4 lo4 = make_uint4(e4m3x2_to_f16x2(static_cast<uint16_t>(w0 & 0xffffu)),
-                                   e4m3x2_to_f16x2(static_cast<uint16_t>(w0 >> 16)),
-                                   e4m3x2_to_f16x2(static_cast<uint16_t>(w1 & 0xffffu)),
-                                   e4m3x2_to_f16x2(static_cast<uint16_t>(w1 >> 16)));
-            uint4 hi4 = make_uint4(e4m3x2_to_f16x2(static_cast<uint16_t>(w2 & 0xffffu)),
-                                   e4m3x2_to_f16x2(static_cast<uint16_t>(w2 >> 16)),
-                                   e4m3x2_to_f16x2(static_cast<uint16_t>(w3 & 0xffffu)),
-                                   e4m3x2_to_f16x2(static_cast<uint16_t>(w3 >> 16)));
-            if (edge) {
-              const int pos = t0 + r0 + 8 * k;
-              if (pos < lo || pos > hi) lo4 = hi4 = make_uint4(0u, 0u, 0u, 0u);
+            for (int k = 0; k < kKv / per; ++k) {
+              uint32_t w0, w1, w2, w3;
+              lds_v4(src + per * k * 128, w0, w1, w2, w3);
+              uint4 lo4 = make_uint4(e4m3x2_to_f16x2(static_cast<uint16_t>(w0 & 0xffffu)),
+                                     e4m3x2_to_f16x2(static_cast<uint16_t>(w0 >> 16)),
+                                     e4m3x2_to_f16x2(static_cast<uint16_t>(w1 & 0xffffu)),
+                                     e4m3x2_to_f16x2(static_cast<uint16_t>(w1 >> 16)));
+              uint4 hi4 = make_uint4(e4m3x2_to_f16x2(static_cast<uint16_t>(w2 & 0xffffu)),
+                                     e4m3x2_to_f16x2(static_cast<uint16_t>(w2 >> 16)),
+                                     e4m3x2_to_f16x2(static_cast<uint16_t>(w3 & 0xffffu)),
+                                     e4m3x2_to_f16x2(static_cast<uint16_t>(w3 >> 16)));
+              if (edge) {
+                const int pos = t0 + r0 + per * k;
+                if (pos < lo || pos > hi) lo4 = hi4 = make_uint4(0u, 0u, 0u, 0u);
+              }
+              sts_v4(d_lo + per * k * 128, lo4);
+              sts_v4(d_hi + per * k * 128, hi4);
             }
-            sts_v4(d_lo + k * 1024, lo4);
-            sts_v4(d_hi + k * 1024, hi4);
+          };
+          if (is_v) {
+            convert(0, 8);
+          } else {
+            convert(0, 4);  // dims 0-63 first: S can start on them
+            fence_proxy_async();
+            mbar_arrive(bar(kBarCKFull));
+            convert(4, 4);
           }
           fence_proxy_async();  // the f16 tile, visible to the tensor core
-          mbar_arrive(bar(is_v ? kBarCVFull + (n & 1) : kBarCKFull));
+          mbar_arrive(bar(is_v ? kBarCVFull + (n & 1) : kBarCKFull1));
           mbar_arrive(bar((is_v ? kBarVEmpty : kBarKEmpty) + (n & 1)));  // reload the stage
         }
       }
