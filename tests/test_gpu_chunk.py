@@ -116,6 +116,7 @@ FORCED = [
     (128, 8, 8, 128, 16, 0, "bf16", False, (128, 127, 1000, 2047)),  # G = 1
     (48, 16, 4, 128, 64, 0, "bf16", False, (0, 47, 48, 49, 300, 1000)),  # bs 64
     (40, 16, 4, 128, 128, 70, "f16", True, (5, 40, 41, 129, 500, 2000)),  # bs 128, e4m3, window
+    (20, 8, 2, 128, 16, 30, "bf16", True, SMALL_LENS),        # e4m3, one row tile (80 rows)
     (40, 32, 8, 128, 16, 100, "bf16", True, SMALL_LENS),       # e4m3 cache, window
     (64, 16, 2, 128, 32, 0, "f16", True, (0, 1, 63, 64, 65, 700, 129, 3000)),  # e4m3, f16 q
 ]
