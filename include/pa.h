@@ -55,7 +55,8 @@ enum {
   PA_OK = 0,
   PA_ERR_INVALID_ARG = -1,   /* null pointer, bad value, aliasing, mismatched shapes */
   PA_ERR_UNSUPPORTED = -2,   /* a shape or dtype this build has no kernel for */
-  PA_ERR_LAYOUT = -3,        /* a tensor is not contiguous or not aligned as required */
+  PA_ERR_LAYOUT = -3,        /* a tensor is not contiguous or not aligned as required
+                                (a tensor with no elements counts as contiguous) */
   PA_ERR_CUDA = -4,          /* a CUDA runtime call or launch failed */
   PA_ERR_OUT_OF_BLOCKS = -5, /* allocator: the pool cannot cover the request */
   PA_ERR_WORKSPACE = -6,     /* decode workspace missing or too small */

@@ -75,7 +75,11 @@ int elem_size(int32_t dt) {
   }
 }
 
+// A tensor with no elements has no layout to get wrong (torch gives empty
+// views strides of 0), so it counts as contiguous.
 bool is_contiguous(const pa_tensor* t) {
+  for (int i = 0; i < t->ndim; ++i)
+    if (t->shape[i] == 0) return true;
   int64_t expect = 1;
   for (int i = t->ndim - 1; i >= 0; --i) {
     if (t->shape[i] != 1 && t->strides[i] != expect) return false;
@@ -520,6 +524,7 @@ pa_status pa_reshape_and_cache(const pa_tensor* k, const pa_tensor* v, const pa_
   if (!is_contiguous(key_cache) || !is_contiguous(value_cache) || !is_contiguous(slot_mapping))
     return fail(PA_ERR_LAYOUT, "caches and slot_mapping must be contiguous");
   for (const pa_tensor* x : {k, v}) {
+    if (T == 0) break;  // no rows: nothing is read
     if (x->strides[2] != 1 || (H > 1 && x->strides[1] != D))
       return fail(PA_ERR_LAYOUT, "k/v rows [Hkv, D] must be contiguous");
     if ((reinterpret_cast<uintptr_t>(x->data) % 16) || ((x->strides[0] * 2) % 16))

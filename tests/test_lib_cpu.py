@@ -103,6 +103,42 @@ def test_host_validation_rejects_bad_arguments_without_a_device(pa_lib):
     assert pa.lib().pa_profile_events(ctypes.c_void_p(1), None) == -1
 
 
+def test_empty_inputs_with_zero_strides_are_accepted(pa_lib):
+    """A write of zero rows and a decode of an empty batch are no-ops, whatever
+    strides the empty tensors carry (torch gives some empty views stride 0):
+    both return before touching a device."""
+    pa = pa_lib
+    L = pa.lib()
+    Hkv, Hq, D, NB, bs, MB = 2, 8, 128, 10, 16, 4
+    base = 0x10000000
+
+    def zero_strides(d):
+        for i in range(d.ndim):
+            d.strides[i] = 0
+        return d
+
+    k = zero_strides(_desc(pa, pa.PA_BF16, (0, Hkv, D), base))
+    v = zero_strides(_desc(pa, pa.PA_BF16, (0, Hkv, D), base + 0x10000))
+    kc = _desc(pa, pa.PA_BF16, (NB, Hkv, bs, D), base + 0x200000)
+    vc = _desc(pa, pa.PA_BF16, (NB, Hkv, bs, D), base + 0x400000)
+    sm = zero_strides(_desc(pa, pa.PA_I64, (0,), base + 0x600000))
+    assert L.pa_reshape_and_cache(*[ctypes.byref(x) for x in (k, v, kc, vc, sm)], 0, 1.0, 1.0,
+                                  None) == 0, pa.last_error()
+    q = zero_strides(_desc(pa, pa.PA_BF16, (0, Hq, D), base))
+    out = zero_strides(_desc(pa, pa.PA_BF16, (0, Hq, D), base + 0x100000))
+    bt = zero_strides(_desc(pa, pa.PA_I32, (0, MB), base + 0x600000))
+    sl = zero_strides(_desc(pa, pa.PA_I32, (0,), base + 0x700000))
+    args = [ctypes.byref(x) for x in (out, q, kc, vc, bt, sl)]
+    assert L.pa_decode(*args, Hkv, 0.1, bs, 0, 0, 1.0, 1.0, None) == 0, pa.last_error()
+    # a non-empty tensor with a wrong stride is still rejected
+    sm_bad = _desc(pa, pa.PA_I64, (3,), base + 0x600000)
+    sm_bad.strides[0] = 2
+    k3 = _desc(pa, pa.PA_BF16, (3, Hkv, D), base)
+    v3 = _desc(pa, pa.PA_BF16, (3, Hkv, D), base + 0x10000)
+    assert L.pa_reshape_and_cache(*[ctypes.byref(x) for x in (k3, v3, kc, vc, sm_bad)], 0, 1.0,
+                                  1.0, None) == -3
+
+
 def _model_vs_lib(pa, seed):
     rnd = random.Random(seed)
     bs = rnd.choice([1, 8, 16, 32])
