@@ -1,7 +1,7 @@
 """GPU edge cases of pa_decode / pa_reshape_and_cache against the oracle.
 
 Ragged lengths around tile and block boundaries, empty sequences, every
-supported head_dim, block sizes 16/32/64, GQA groups 1..16, windows that cut
+supported head_dim, block sizes 16 to 1024, GQA groups 1..16, windows that cut
 inside a tile, FP8 caches with f16 and bf16 queries, forced worker layouts
 (one CTA for everything; one tile per worker), device-side error flags,
 caller-owned workspace, CUDA graph capture, and allocator-built layouts.
@@ -12,7 +12,8 @@ import torch
 
 import oracle
 from conftest import have_gpu
-from pa_testutil import (assert_caches_equal, assert_close, host_copy, out_f64, run_both)
+from pa_testutil import (assert_caches_equal, assert_close, host_copy, out_f64, run_both,
+                         run_chunk)
 from workloads import generate
 from workloads.configs import Spec
 
@@ -37,6 +38,10 @@ CASES = [
     dict(dtype="f16", head_dim=128, block_size=64),
     dict(dtype="bf16", head_dim=256),
     dict(dtype="f16", head_dim=256, block_size=32),
+    dict(dtype="bf16", head_dim=128, block_size=128),
+    dict(dtype="f16", head_dim=64, block_size=256),
+    dict(dtype="bf16", head_dim=128, block_size=1024),
+    dict(kv_fp8=True, head_dim=256, block_size=128),
     dict(num_q_heads=2, num_kv_heads=2),                 # G = 1
     dict(num_q_heads=4, num_kv_heads=2),                 # G = 2
     dict(num_q_heads=6, num_kv_heads=2),                 # G = 3
@@ -68,6 +73,47 @@ def test_edge_shapes(case, pa_lib):
         if L == 0:
             assert (sides.out[b] == 0).all()
     assert pa_lib.check_device_error() == 0
+
+
+@pytest.mark.parametrize("path", ["decode", "chunk_persistent", "chunk_tensor_memory"])
+@pytest.mark.parametrize("dtype,fp8", [("bf16", False), ("f16", False), ("bf16", True),
+                                       ("f16", True)])
+def test_window_one_returns_the_value_row_rounded_once(dtype, fp8, path, pa_lib):
+    """With a window of one position every query attends only to itself: the
+    softmax weight is 1 and the output is that position's V row. A 16-bit
+    cache's row is representable, so the output equals it bit for bit; an
+    e4m3 row times its scale is not, so the output is it rounded once to the
+    output type (within half a unit in the last place, 2^-8 |v| for bf16,
+    2^-11 |v| for f16, 2^-25 among f16 subnormals). Such rows have magnitudes up to several units, where
+    that rounding alone exceeds the decode bar's 1e-3 mean, so this case is
+    held to the tighter rounding bound instead."""
+    T = 1 if path == "decode" else 24
+    lens = (1, 2, 17, 300, 129, 40, 0, 64)
+    s = Spec("window1", batch=len(lens), num_q_heads=16, num_kv_heads=2,
+             head_dim=256 if path == "decode" else 128, block_size=32, dtype=dtype,
+             kv_fp8=fp8, window=1, seq_lens=lens, max_len=max(lens) + 64, num_queries=T,
+             pool_factor=1.3, seed=4300 + fp8)
+    if path == "decode":
+        sides = run_both(s)
+    else:
+        pa_lib.set_prefill_path(1 if path == "chunk_persistent" else 2)
+        try:
+            sides = run_chunk(s)
+        finally:
+            pa_lib.set_prefill_path(0)
+    assert pa_lib.check_device_error() == 0
+    assert_caches_equal(sides, path)
+    got, ref = out_f64(sides.out), sides.ref
+    assert np.isfinite(got).all()
+    if not fp8:
+        assert np.array_equal(got, ref), f"max diff {np.abs(got - ref).max():.3e}"
+    else:
+        # half a unit: relative for normal outputs, 2^-25 absolute in f16's
+        # subnormal range (spacing 2^-24 below 2^-14)
+        u, floor = (2.0 ** -8, 0.0) if dtype == "bf16" else (2.0 ** -11, 2.0 ** -25)
+        excess = np.abs(got - ref) - (u * np.abs(ref) * (1 + 1e-4) + floor)
+        assert excess.max() <= 0, f"exceeds one rounding by {excess.max():.3e}"
+        assert np.abs(ref).max() > 2.0     # the rows do reach magnitudes of several units
 
 
 @pytest.mark.parametrize("tuning", [(1, 0), (0, 1), (3, 2), (7, 5), (0, 0, 900, 1),
