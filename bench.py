@@ -607,7 +607,7 @@ def run_ours(args, world, rank, local):
                      {"bound": "tensor", "achieved": flops / (k_ms * 1e-3) / 1e12,
                       "peak": tpeak, "unit": "TFLOP/s",
                       "frac": flops / (k_ms * 1e-3) / 1e12 / tpeak, "traffic": None,
-                      "kernel": "chunk_attn_tc_kernel", "kernel_us": k_ms * 1e3,
+                      "kernel": "chunk_attn_tc128_kernel", "kernel_us": k_ms * 1e3,
                       "flops_per_launch": flops, "peak_kind": tpeak_kind + " bf16 burst"}),
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d_direct,
                 "d2h_bytes_per_step": d2h_direct, "ms_per_step": e2e_ms,

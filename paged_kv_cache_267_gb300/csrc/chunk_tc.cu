@@ -143,6 +143,11 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
   return r;
 }
+// Two consecutive 32-bit tensor-memory values as an fp32 pair.
+__device__ __forceinline__ float2 score_pair(const uint32_t* v, int i) {
+  return make_float2(__uint_as_float(v[i]), __uint_as_float(v[i + 1]));
+}
+
 __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -554,18 +559,26 @@ __global__ void __launch_bounds__(Smem<FP8>::kThreads, 1)
           uint32_t ov[32];
           tc::ld32_async(tO + c0, ov);
           tc::wait_ld(ov);
+          const float2 a2 = make_float2(alpha, alpha);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+          for (int i = 0; i < 32; i += 2) {
+            const float2 o = __fmul2_rn(score_pair(ov, i), a2);
+            ov[i] = __float_as_uint(o.x);
+            ov[i + 1] = __float_as_uint(o.y);
+          }
           tc::st32(tO + c0, ov);
         }
         l *= alpha;
         if (grow) ms = mx;
       }
       // P = 2^(s * sc - ms), packed in pairs: scores 64 h + j -> column
-      // 64 h + j / 2; the second half first, from registers
-      float sp[8];  // eight independent partial sums
+      // 64 h + j / 2; the second half first, from registers. The scale FMA
+      // and the running sums work on score pairs (two-wide fp32 FMA / add,
+      // one instruction per pair).
+      const float2 sc2 = make_float2(sc, sc), nms2 = make_float2(-ms, -ms);
+      float2 sp[4];  // four independent partial sums of score pairs
 #pragma unroll
-      for (int i = 0; i < 8; ++i) sp[i] = 0.f;
+      for (int i = 0; i < 4; ++i) sp[i] = make_float2(0.f, 0.f);
 #pragma unroll 1
       for (int h = 1; h >= 0; --h) {
         if (h == 0) {
@@ -577,26 +590,28 @@ __global__ void __launch_bounds__(Smem<FP8>::kThreads, 1)
         if (all_in) {
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
-            const float p0 = ex2(fmaf(__uint_as_float(sv[j >> 4][(2 * j) & 31]), sc, -ms));
-            const float p1 = ex2(fmaf(__uint_as_float(sv[j >> 4][(2 * j + 1) & 31]), sc, -ms));
-            sp[j & 7] += p0 + p1;
+            const float2 t = __ffma2_rn(score_pair(sv[j >> 4], (2 * j) & 31), sc2, nms2);
+            const float p0 = ex2(t.x), p1 = ex2(t.y);
+            sp[j & 3] = __fadd2_rn(sp[j & 3], make_float2(p0, p1));
             pk[j] = pack16x2<kBf16>(p0, p1);
           }
         } else {  // masked scores give exactly 0 (also when sc = 0)
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
             const int e = d0 + 64 * h + 2 * j;
-            float p0 = ex2(fmaf(__uint_as_float(sv[j >> 4][(2 * j) & 31]), sc, -ms));
-            float p1 = ex2(fmaf(__uint_as_float(sv[j >> 4][(2 * j + 1) & 31]), sc, -ms));
+            const float2 t = __ffma2_rn(score_pair(sv[j >> 4], (2 * j) & 31), sc2, nms2);
+            float p0 = ex2(t.x), p1 = ex2(t.y);
             p0 = static_cast<unsigned>(e) < static_cast<unsigned>(cnt) ? p0 : 0.f;
             p1 = static_cast<unsigned>(e + 1) < static_cast<unsigned>(cnt) ? p1 : 0.f;
-            sp[j & 7] += p0 + p1;
+            sp[j & 3] = __fadd2_rn(sp[j & 3], make_float2(p0, p1));
             pk[j] = pack16x2<kBf16>(p0, p1);
           }
         }
         tc::st32(tS + 64 * h, pk);
       }
-      l += ((sp[0] + sp[1]) + (sp[2] + sp[3])) + ((sp[4] + sp[5]) + (sp[6] + sp[7]));
+      const float2 s01 = __fadd2_rn(sp[0], sp[1]), s23 = __fadd2_rn(sp[2], sp[3]);
+      const float2 st = __fadd2_rn(s01, s23);
+      l += st.x + st.y;
       if (!FP8 && x == 0 && (t0 < lo || t0 + kKv - 1 > hi)) {
         // edge tile: once it has landed, zero the V rows outside [lo, hi]
         // (with FP8 caches the converters write those rows as zeros)
