@@ -218,9 +218,11 @@ pa_status pa_decode_workspace_size(int64_t batch, int32_t num_q_heads, int32_t n
  *
  *   out, q        [B, T, Hq, D] contiguous (q f16 or bf16, out the same),
  *                 1 <= T <= 4096; every other argument as for pa_decode.
- * The (query, head) pairs of one KV head are processed 16 at a time, so the
- * step reads each attended K/V byte ceil(T * G / 16) times (from L2 where
- * they are close together); for T * G <= 16 it reads it once. Workspace:
+ * The persistent kernel processes the (query, head) pairs of one KV head 16
+ * at a time, so it reads each attended K/V byte ceil(T * G / 16) times (from
+ * L2 where they are close together); for T * G <= 16 it reads it once. The
+ * tensor-memory kernel (head_dim 128, T * G > 32 by default) reads it
+ * ceil(T * G / 256) times. Workspace:
  * pa_prefill_chunk_workspace_size() bytes, from the same source as
  * pa_decode's. Errors as for pa_decode, plus PA_ERR_UNSUPPORTED for T out of
  * range or B * Hkv * ceil(T * G / 16) * 16 > 2^19.
@@ -235,7 +237,7 @@ pa_status pa_prefill_chunk(const pa_tensor* out, const pa_tensor* q, const pa_te
  * call; 1 always uses the persistent split-KV kernel (16 (query, head)
  * columns per pass over K/V, any head dim); 2 uses the tensor-memory kernel
  * wherever it applies (head_dim 128; 16-bit or e4m3 caches),
- * which tiles 128 (query, head) rows against 64-token K/V tiles on the
+ * which tiles 128 (query, head) rows against 128-token K/V tiles on the
  * tcgen05 tensor cores and reads each K/V tile once per 256 rows. The
  * default takes the tensor-memory kernel for chunks of more than 32 (query,
  * head) columns per KV head. */
