@@ -45,8 +45,9 @@
 // edge tile that lie outside [lo, hi] (not loaded, or NaN-poisoned slots past
 // the sequence or before the window) are zeroed in shared memory before the
 // products, so only attended rows reach the tensor core. Scores enter the
-// exponent through one fused multiply-add against the scaled reference max;
-// a negative softmax scale is carried by flipping the sign of Q (exact), so
+// exponent through one fused multiply-add against the scaled reference max,
+// issued on score pairs (the two-wide fp32 FMA of sm_100+; the row sums use
+// the two-wide add); a negative softmax scale is carried by flipping the sign of Q (exact), so
 // the row max is taken on the raw scores. Head dim 128.
 //
 // FP8 e4m3 caches (FP8 = true): the rings hold the raw e4m3 tiles (16 KB of
