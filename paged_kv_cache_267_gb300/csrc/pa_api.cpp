@@ -12,6 +12,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <initializer_list>
 #include <map>
 #include <mutex>
 #include <string>
@@ -40,6 +41,7 @@ constexpr int kMaxCtasPerSm = 2;
 constexpr int kWarpsPerCta = 8;  // most worker warps of any decode variant
 constexpr int64_t kMaxBatch = 4096;
 constexpr int64_t kMaxChunk = 4096;        // query tokens per sequence in a chunk call
+constexpr double kMaxTensorBytes = 1125899906842624.0;  // 2^50: no tensor is larger
 // Chunks with more (query, head) columns per KV head than this go to the
 // tensor-memory kernel (head dim 128, 16-bit or e4m3 caches): the persistent kernel
 // reads each K/V tile once per 16 columns.
@@ -118,8 +120,27 @@ pa_status check_tensor(const pa_tensor* t, const char* name, int ndim) {
     if (t->shape[i] < 0) return fail(PA_ERR_INVALID_ARG, "%s: negative extent", name);
     if (t->strides[i] < 0) return fail(PA_ERR_LAYOUT, "%s: negative stride", name);
   }
+  // Extents and spans beyond any memory are rejected here (counted in double,
+  // which cannot overflow), so the 64-bit size arithmetic after this check
+  // stays in range for any descriptor.
+  double n = 1.0, last = 0.0;
+  for (int i = 0; i < ndim; ++i) {
+    n *= static_cast<double>(t->shape[i]);
+    if (t->shape[i] > 0)
+      last += static_cast<double>(t->shape[i] - 1) * static_cast<double>(t->strides[i]);
+  }
+  const double elt = static_cast<double>(elem_size(t->dtype));
+  if (n * elt >= kMaxTensorBytes || (n > 0 && (last + 1.0) * elt >= kMaxTensorBytes))
+    return fail(PA_ERR_UNSUPPORTED, "%s: extent or span beyond 2^50 bytes", name);
   if (!t->data && numel(t) > 0) return fail(PA_ERR_INVALID_ARG, "%s: null data", name);
   return PA_OK;
+}
+
+// Product of sizes in double, for limit checks that must not overflow.
+double dprod(std::initializer_list<double> f) {
+  double p = 1.0;
+  for (double x : f) p *= x;
+  return p;
 }
 
 // The kernels may only touch memory of the current device, or pinned host
@@ -447,6 +468,11 @@ pa_status workspace_size(int64_t batch, int64_t num_queries, int32_t num_q_heads
   if (batch < 0 || batch > kMaxBatch) return fail(PA_ERR_UNSUPPORTED, "batch %lld", (long long)batch);
   pa_status s = check_heads(num_q_heads, num_kv_heads, head_dim);
   if (s) return s;
+  int CG, NCG;
+  chunk_columns(num_queries, num_q_heads / num_kv_heads, &CG, &NCG);
+  const int64_t Hv = static_cast<int64_t>(num_kv_heads) * NCG;
+  if (dprod({double(batch), double(Hv), double(CG)}) > pa::kMaxMergeCounters)
+    return fail(PA_ERR_UNSUPPORTED, "batch * num_q_heads * num_queries too large");
   std::lock_guard<std::mutex> lk(g_mu);
   DeviceState* st;
   s = device_state(&st, nullptr);
@@ -454,9 +480,7 @@ pa_status workspace_size(int64_t batch, int64_t num_queries, int32_t num_q_heads
   int64_t workers = static_cast<int64_t>(st->num_sms) * kMaxCtasPerSm * kWarpsPerCta;
   const int cap = g_tune_max_ctas.load();
   if (cap > 0 && cap * kWarpsPerCta < workers) workers = static_cast<int64_t>(cap) * kWarpsPerCta;
-  int CG, NCG;
-  chunk_columns(num_queries, num_q_heads / num_kv_heads, &CG, &NCG);
-  *bytes = ws_layout(batch, num_kv_heads * NCG, CG, head_dim, workers).total;
+  *bytes = ws_layout(batch, static_cast<int>(Hv), CG, head_dim, workers).total;
   return ok();
 }
 
@@ -527,7 +551,7 @@ pa_status pa_reshape_and_cache(const pa_tensor* k, const pa_tensor* v, const pa_
     if (T == 0) break;  // no rows: nothing is read
     if (x->strides[2] != 1 || (H > 1 && x->strides[1] != D))
       return fail(PA_ERR_LAYOUT, "k/v rows [Hkv, D] must be contiguous");
-    if ((reinterpret_cast<uintptr_t>(x->data) % 16) || ((x->strides[0] * 2) % 16))
+    if ((reinterpret_cast<uintptr_t>(x->data) % 16) || (x->strides[0] % 8))
       return fail(PA_ERR_LAYOUT, "k/v rows must be 16-byte aligned");
   }
   if ((reinterpret_cast<uintptr_t>(key_cache->data) % 16) ||
@@ -650,13 +674,18 @@ pa_status check_decode(const pa_tensor* out, const pa_tensor* q, const pa_tensor
   chunk_columns(T, G, &CG, &NCG);
   const int64_t Hv = Hkv * NCG;
   // 32-bit index limits inside the kernels
-  if (NB * Hkv * block_size >= (int64_t(1) << 31) || MB * block_size >= (int64_t(1) << 31) ||
-      B * Hv * (MB * block_size / 16 + 1) >= (int64_t(1) << 31) || B * MB >= (int64_t(1) << 31) ||
-      B * T * Hq * D >= (int64_t(1) << 40))
+  const double k2p31 = 2147483648.0;
+  const double dNB = static_cast<double>(NB), dMB = static_cast<double>(MB);
+  const double dB = static_cast<double>(B), dHv = static_cast<double>(Hv);
+  if (dprod({dNB, double(Hkv), double(block_size)}) >= k2p31 ||
+      dprod({dMB, double(block_size)}) >= k2p31 ||
+      dprod({dB, dHv}) * (dprod({dMB, double(block_size)}) / 16 + 1) >= k2p31 ||
+      dprod({dB, dMB}) >= k2p31 ||
+      dprod({dB, double(T), double(Hq), double(D)}) >= 1099511627776.0)
     return fail(PA_ERR_UNSUPPORTED, "pool or tables exceed 32-bit indexing");
   for (const pa_tensor* x : {q, key_cache, value_cache, block_tables, seq_lens})
     if (overlaps(out, x)) return fail(PA_ERR_INVALID_ARG, "out overlaps an input");
-  if (B * Hv * CG > pa::kMaxMergeCounters)
+  if (dprod({dB, dHv, double(CG)}) > pa::kMaxMergeCounters)
     return fail(PA_ERR_UNSUPPORTED, "batch * num_q_heads * num_queries too large");
   if (B > 0 && MB == 0) return fail(PA_ERR_INVALID_ARG, "block_tables has no columns");
   if (B > 0 && NB == 0) return fail(PA_ERR_INVALID_ARG, "empty block pool");

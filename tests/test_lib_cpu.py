@@ -139,6 +139,85 @@ def test_empty_inputs_with_zero_strides_are_accepted(pa_lib):
                                   1.0, None) == -3
 
 
+EXTREMES = [0, 1, 2, 3, 7, 16, 24, 64, 128, 256, 1024, 4096, 4097, 2**31 - 1, 2**31, 2**40,
+            2**53 + 1, 2**62, 2**63 - 1]
+
+
+@pytest.mark.skipif(__import__("torch").cuda.is_available(),
+                    reason="host-only: descriptors point at made-up addresses")
+def test_validation_survives_mutated_descriptors(pa_lib):
+    """Valid-looking argument sets with one to three fields set to extreme or
+    wrong values (extents and strides up to 2^63 - 1, bad dtypes and ranks,
+    misaligned or null data, bad head counts, block sizes and scales): every
+    entry point returns a documented status without crashing, and succeeds
+    only for calls with nothing to do (no device work is possible here)."""
+    pa = pa_lib
+    L = pa.lib()
+    rnd = random.Random(2671)
+    base = 0x10000000
+    codes = {0, -1, -2, -3, -4, -6}
+
+    def fresh(entry):
+        B, T, Hq, Hkv, D, NB, bs, MB = 2, 3, 8, 2, 128, 10, 16, 4
+        if entry == "reshape":
+            return dict(k=_desc(pa, pa.PA_BF16, (5, Hkv, D), base),
+                        v=_desc(pa, pa.PA_BF16, (5, Hkv, D), base + 0x100000),
+                        kc=_desc(pa, pa.PA_BF16, (NB, Hkv, bs, D), base + 0x200000),
+                        vc=_desc(pa, pa.PA_BF16, (NB, Hkv, bs, D), base + 0x400000),
+                        sm=_desc(pa, pa.PA_I64, (5,), base + 0x600000)), \
+                dict(kv=0, ks=1.0, vs=1.0)
+        qs = (B, T, Hq, D) if entry == "chunk" else (B, Hq, D)
+        return dict(out=_desc(pa, pa.PA_BF16, qs, base + 0x100000),
+                    q=_desc(pa, pa.PA_BF16, qs, base),
+                    kc=_desc(pa, pa.PA_BF16, (NB, Hkv, bs, D), base + 0x200000),
+                    vc=_desc(pa, pa.PA_BF16, (NB, Hkv, bs, D), base + 0x400000),
+                    bt=_desc(pa, pa.PA_I32, (B, MB), base + 0x600000),
+                    sl=_desc(pa, pa.PA_I32, (B,), base + 0x700000)), \
+            dict(hkv=Hkv, scale=0.1, bs=bs, window=0, kv=0, ks=1.0, vs=1.0)
+
+    def mutate(ts, sc):
+        name = rnd.choice(sorted(ts) + ["scalar"])
+        if name == "scalar":
+            key = rnd.choice(sorted(sc))
+            if key in ("scale", "ks", "vs"):
+                sc[key] = rnd.choice([0.0, -1.0, float("nan"), float("inf"), 1e38])
+            else:
+                sc[key] = rnd.choice([-(2**31), -16, -1, 0, 1, 2, 5, 16, 17, 1024, 2048, 2**31 - 1])
+            return
+        d = ts[name]
+        what = rnd.choice(["shape", "stride", "dtype", "ndim", "data"])
+        i = rnd.randrange(min(max(d.ndim, 1), len(d.shape)))
+        if what == "shape":
+            d.shape[i] = rnd.choice(EXTREMES + [-1])
+        elif what == "stride":
+            d.strides[i] = rnd.choice(EXTREMES + [-1])
+        elif what == "dtype":
+            d.dtype = rnd.choice([pa.PA_F16, pa.PA_BF16, pa.PA_FP8_E4M3, pa.PA_I32, pa.PA_I64, 9, -1])
+        elif what == "ndim":
+            d.ndim = rnd.choice([0, 1, 2, 3, 4, 5, -1])
+        else:
+            d.data = rnd.choice([None, base + 3, base + 8, 2**64 - 16])
+
+    for it in range(4000):
+        entry = rnd.choice(["decode", "noalloc", "chunk", "reshape"])
+        ts, sc = fresh(entry)
+        for _ in range(rnd.randint(1, 3)):
+            mutate(ts, sc)
+        if entry == "reshape":
+            args = [ctypes.byref(ts[n]) for n in ("k", "v", "kc", "vc", "sm")]
+            st = L.pa_reshape_and_cache(*args, sc["kv"], sc["ks"], sc["vs"], None)
+            nothing = ts["k"].ndim == 3 and (ts["k"].shape[0] == 0 or ts["k"].shape[1] == 0)
+        else:
+            fn = {"decode": L.pa_decode, "noalloc": L.pa_decode_noalloc,
+                  "chunk": L.pa_prefill_chunk}[entry]
+            args = [ctypes.byref(ts[n]) for n in ("out", "q", "kc", "vc", "bt", "sl")]
+            st = fn(*args, sc["hkv"], sc["scale"], sc["bs"], sc["window"], sc["kv"], sc["ks"],
+                    sc["vs"], None)
+            nothing = ts["q"].ndim >= 1 and ts["q"].shape[0] == 0
+        assert st in codes, (it, entry, st, pa.last_error())
+        assert st != 0 or nothing, (it, entry, "succeeded with work to do")
+
+
 def _model_vs_lib(pa, seed):
     rnd = random.Random(seed)
     bs = rnd.choice([1, 8, 16, 32])
