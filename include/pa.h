@@ -60,7 +60,9 @@ enum {
   PA_ERR_CUDA = -4,          /* a CUDA runtime call or launch failed */
   PA_ERR_OUT_OF_BLOCKS = -5, /* allocator: the pool cannot cover the request */
   PA_ERR_WORKSPACE = -6,     /* decode workspace missing or too small */
-  PA_ERR_NOT_FOUND = -7      /* allocator: unknown sequence or block id */
+  PA_ERR_NOT_FOUND = -7,     /* allocator: unknown sequence or block id */
+  PA_ERR_HOST_MEMORY = -8    /* allocator: host memory exhausted mid-call; the
+                                allocator's state is then undefined: destroy it */
 };
 
 /* Element types. */

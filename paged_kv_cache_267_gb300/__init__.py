@@ -20,7 +20,7 @@ _MAX_DIMS = 6
 
 _STATUS = {0: "PA_OK", -1: "PA_ERR_INVALID_ARG", -2: "PA_ERR_UNSUPPORTED", -3: "PA_ERR_LAYOUT",
            -4: "PA_ERR_CUDA", -5: "PA_ERR_OUT_OF_BLOCKS", -6: "PA_ERR_WORKSPACE",
-           -7: "PA_ERR_NOT_FOUND"}
+           -7: "PA_ERR_NOT_FOUND", -8: "PA_ERR_HOST_MEMORY"}
 
 
 class PAError(RuntimeError):

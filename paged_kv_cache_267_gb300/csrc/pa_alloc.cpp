@@ -6,6 +6,7 @@
 // §2.3). A released table entry is -1.
 #include <algorithm>
 #include <cstdint>
+#include <memory>
 #include <new>
 #include <unordered_map>
 #include <utility>
@@ -44,7 +45,7 @@ struct SplitMix64 {
   }
 };
 
-int64_t blocks_for(int64_t n, int32_t bs) { return (n + bs - 1) / bs; }
+int64_t blocks_for(int64_t n, int32_t bs) { return n / bs + (n % bs != 0); }  // no overflow
 
 // FNV-1a, 64-bit (Fowler, Noll, Vo): per byte, xor then multiply.
 uint64_t fnv1a64_bytes(const unsigned char* p, size_t n, uint64_t h) {
@@ -82,10 +83,10 @@ int32_t pop_block(pa_alloc* a) {
 
 extern "C" {
 
-pa_status pa_alloc_create(int32_t num_blocks, int32_t block_size, uint64_t seed, pa_alloc** out) {
+pa_status pa_alloc_create(int32_t num_blocks, int32_t block_size, uint64_t seed,
+                          pa_alloc** out) try {
   if (!out || num_blocks < 0 || block_size <= 0) return PA_ERR_INVALID_ARG;
-  pa_alloc* a = new (std::nothrow) pa_alloc();
-  if (!a) return PA_ERR_INVALID_ARG;
+  std::unique_ptr<pa_alloc> a(new pa_alloc());
   a->num_blocks = num_blocks;
   a->block_size = block_size;
   a->ref.assign(num_blocks, 0);
@@ -97,13 +98,15 @@ pa_status pa_alloc_create(int32_t num_blocks, int32_t block_size, uint64_t seed,
     const uint64_t j = rng.next() % static_cast<uint64_t>(i + 1);
     std::swap(a->free_list[i], a->free_list[j]);
   }
-  *out = a;
+  *out = a.release();
   return PA_OK;
+} catch (const std::bad_alloc&) {
+  return PA_ERR_HOST_MEMORY;
 }
 
 void pa_alloc_destroy(pa_alloc* a) { delete a; }
 
-pa_status pa_alloc_add(pa_alloc* a, int64_t n_tokens, int32_t* seq_out) {
+pa_status pa_alloc_add(pa_alloc* a, int64_t n_tokens, int32_t* seq_out) try {
   if (!a || !seq_out || n_tokens < 0) return PA_ERR_INVALID_ARG;
   const int64_t need = blocks_for(n_tokens, a->block_size);
   if (need > static_cast<int64_t>(a->free_list.size())) return PA_ERR_OUT_OF_BLOCKS;
@@ -115,9 +118,11 @@ pa_status pa_alloc_add(pa_alloc* a, int64_t n_tokens, int32_t* seq_out) {
   a->seqs.emplace(id, std::move(s));
   *seq_out = id;
   return PA_OK;
+} catch (const std::bad_alloc&) {
+  return PA_ERR_HOST_MEMORY;
 }
 
-pa_status pa_alloc_fork(pa_alloc* a, int32_t src, int32_t* seq_out) {
+pa_status pa_alloc_fork(pa_alloc* a, int32_t src, int32_t* seq_out) try {
   if (!a || !seq_out) return PA_ERR_INVALID_ARG;
   auto it = a->seqs.find(src);
   if (it == a->seqs.end()) return PA_ERR_NOT_FOUND;
@@ -128,14 +133,17 @@ pa_status pa_alloc_fork(pa_alloc* a, int32_t src, int32_t* seq_out) {
   a->seqs.emplace(id, std::move(s));
   *seq_out = id;
   return PA_OK;
+} catch (const std::bad_alloc&) {
+  return PA_ERR_HOST_MEMORY;
 }
 
 pa_status pa_alloc_append(pa_alloc* a, int32_t seq, int64_t n_tokens, int32_t* cow_src,
-                          int32_t* cow_dst) {
+                          int32_t* cow_dst) try {
   if (!a || n_tokens < 0) return PA_ERR_INVALID_ARG;
   auto it = a->seqs.find(seq);
   if (it == a->seqs.end()) return PA_ERR_NOT_FOUND;
   pa_alloc::Seq& s = it->second;
+  if (n_tokens > INT64_MAX - s.len) return PA_ERR_INVALID_ARG;
   int32_t src = -1, dst = -1;
   if (n_tokens > 0) {
     const bool partial = s.len % a->block_size != 0;
@@ -156,9 +164,11 @@ pa_status pa_alloc_append(pa_alloc* a, int32_t seq, int64_t n_tokens, int32_t* c
   if (cow_src) *cow_src = src;
   if (cow_dst) *cow_dst = dst;
   return PA_OK;
+} catch (const std::bad_alloc&) {
+  return PA_ERR_HOST_MEMORY;
 }
 
-pa_status pa_alloc_free(pa_alloc* a, int32_t seq) {
+pa_status pa_alloc_free(pa_alloc* a, int32_t seq) try {
   if (!a) return PA_ERR_INVALID_ARG;
   auto it = a->seqs.find(seq);
   if (it == a->seqs.end()) return PA_ERR_NOT_FOUND;
@@ -167,9 +177,12 @@ pa_status pa_alloc_free(pa_alloc* a, int32_t seq) {
   }
   a->seqs.erase(it);
   return PA_OK;
+} catch (const std::bad_alloc&) {
+  return PA_ERR_HOST_MEMORY;
 }
 
-pa_status pa_alloc_trim_window(pa_alloc* a, int32_t seq, int32_t window, int32_t* n_released) {
+pa_status pa_alloc_trim_window(pa_alloc* a, int32_t seq, int32_t window,
+                               int32_t* n_released) try {
   if (!a) return PA_ERR_INVALID_ARG;
   auto it = a->seqs.find(seq);
   if (it == a->seqs.end()) return PA_ERR_NOT_FOUND;
@@ -188,10 +201,12 @@ pa_status pa_alloc_trim_window(pa_alloc* a, int32_t seq, int32_t window, int32_t
   }
   if (n_released) *n_released = n;
   return PA_OK;
+} catch (const std::bad_alloc&) {
+  return PA_ERR_HOST_MEMORY;
 }
 
 pa_status pa_alloc_add_cached(pa_alloc* a, const int32_t* tokens, int64_t n_tokens,
-                              int32_t* seq_out, int64_t* n_cached) {
+                              int32_t* seq_out, int64_t* n_cached) try {
   if (!a || !seq_out || n_tokens < 0 || (n_tokens > 0 && !tokens)) return PA_ERR_INVALID_ARG;
   const int32_t bs = a->block_size;
   const int64_t nblk = blocks_for(n_tokens, bs), nfull = n_tokens / bs;
@@ -237,6 +252,8 @@ pa_status pa_alloc_add_cached(pa_alloc* a, const int32_t* tokens, int64_t n_toke
   *seq_out = id;
   if (n_cached) *n_cached = static_cast<int64_t>(reuse.size()) * bs;
   return PA_OK;
+} catch (const std::bad_alloc&) {
+  return PA_ERR_HOST_MEMORY;
 }
 
 int32_t pa_alloc_reclaim(pa_alloc* a) {

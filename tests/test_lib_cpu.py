@@ -290,6 +290,16 @@ def test_allocator_errors(pa_lib):
         a.fill_tables([s], 2)        # table wider than the matrix
     t, lens = a.fill_tables([s], 4)
     assert sorted(t[0]) == [0, 1, 2, 3] and lens[0] == 64
+    # lengths near the int64 limit: no overflow in the block count or the
+    # appended length, and no state change
+    b = pa_lib.BlockAllocator(4, 16, seed=0)
+    with pytest.raises(pa_lib.OutOfBlocks):
+        b.add(2**63 - 1)
+    s2 = b.add(5)
+    with pytest.raises(pa_lib.PAError) as e:
+        b.append(s2, 2**63 - 3)
+    assert e.value.status == -1
+    assert b.seq_len(s2) == 5 and b.num_free() == 3
 
 
 @pytest.mark.parametrize("seed", range(6))
