@@ -218,6 +218,49 @@ def test_validation_survives_mutated_descriptors(pa_lib):
         assert st != 0 or nothing, (it, entry, "succeeded with work to do")
 
 
+@pytest.mark.skipif(__import__("torch").cuda.is_available(),
+                    reason="host-only: descriptors point at made-up addresses")
+@pytest.mark.parametrize("name", ["tiny", "llama8b", "long_skew", "prefix_window", "fp8",
+                                  "verify4_llama8b", "prefill_chunk512", "prefill_chunk512_fp8"])
+def test_named_workload_shapes_pass_host_validation(name, pa_lib):
+    """The argument sets of every named workload, with a pool of 1.2x the
+    blocks of all sequences at the longest length, pass host validation: with
+    no device here, each call stops at the device query (PA_ERR_CUDA), not at
+    a size or layout check. Guards the validation's limits against rejecting
+    the shapes the library is built for."""
+    from workloads.configs import CONFIGS
+    pa = pa_lib
+    L = pa.lib()
+    s = CONFIGS[name]
+    longest = max([s.max_len or 0, s.len_dist[2], *s.long_seqs])
+    MB = -(-longest // s.block_size) + 2
+    NB = int(1.2 * s.batch * MB) + 1
+    B, T, Hq, Hkv, D, bs = s.batch, s.num_queries, s.num_q_heads, s.num_kv_heads, s.head_dim, \
+        s.block_size
+    cdt = pa.PA_FP8_E4M3 if s.kv_fp8 else pa.PA_BF16
+    kv = 2 if s.kv_fp8 else 0
+    qs = (B, T, Hq, D) if T > 1 else (B, Hq, D)
+    at = iter(range(1, 100))
+    addr = lambda: next(at) << 40
+    ts = [_desc(pa, pa.PA_BF16, qs, addr()), _desc(pa, pa.PA_BF16, qs, addr()),
+          _desc(pa, cdt, (NB, Hkv, bs, D), addr()), _desc(pa, cdt, (NB, Hkv, bs, D), addr()),
+          _desc(pa, pa.PA_I32, (B, MB), addr()), _desc(pa, pa.PA_I32, (B,), addr())]
+    fn = L.pa_prefill_chunk if T > 1 else L.pa_decode
+    st = fn(*[ctypes.byref(t) for t in ts], Hkv, D ** -0.5, bs, s.window, kv, 0.01, 0.01, None)
+    assert st == -4, pa.last_error()
+    rows = B * T
+    k = _desc(pa, pa.PA_BF16, (rows, Hkv, D), addr())
+    v = _desc(pa, pa.PA_BF16, (rows, Hkv, D), addr())
+    sm = _desc(pa, pa.PA_I64, (rows,), addr())
+    st = L.pa_reshape_and_cache(*[ctypes.byref(x) for x in (k, v, ts[2], ts[3], sm)], kv, 0.01,
+                                0.01, None)
+    assert st == -4, pa.last_error()
+    n = ctypes.c_size_t(0)
+    st = (L.pa_prefill_chunk_workspace_size(B, T, Hq, Hkv, D, ctypes.byref(n)) if T > 1
+          else L.pa_decode_workspace_size(B, Hq, Hkv, D, ctypes.byref(n)))
+    assert st == -4, pa.last_error()
+
+
 def _model_vs_lib(pa, seed):
     rnd = random.Random(seed)
     bs = rnd.choice([1, 8, 16, 32])
