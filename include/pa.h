@@ -61,8 +61,9 @@ enum {
   PA_ERR_OUT_OF_BLOCKS = -5, /* allocator: the pool cannot cover the request */
   PA_ERR_WORKSPACE = -6,     /* decode workspace missing or too small */
   PA_ERR_NOT_FOUND = -7,     /* allocator: unknown sequence or block id */
-  PA_ERR_HOST_MEMORY = -8    /* allocator: host memory exhausted mid-call; the
-                                allocator's state is then undefined: destroy it */
+  PA_ERR_HOST_MEMORY = -8    /* host memory exhausted; no C++ exception crosses this
+                                ABI. An allocator that returns it has undefined
+                                state: destroy it */
 };
 
 /* Element types. */

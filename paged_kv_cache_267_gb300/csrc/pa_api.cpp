@@ -15,7 +15,7 @@
 #include <initializer_list>
 #include <map>
 #include <mutex>
-#include <string>
+#include <new>
 #include <tuple>
 
 #include "pa.h"
@@ -23,7 +23,7 @@
 
 namespace {
 
-thread_local std::string g_last_error;
+thread_local char g_last_error[512] = "";  // no host allocation on any error path
 std::atomic<uint64_t> g_launches{0};
 std::atomic<int32_t> g_tune_max_ctas{0};
 std::atomic<int32_t> g_tune_min_tiles{0};
@@ -48,17 +48,15 @@ constexpr double kMaxTensorBytes = 1125899906842624.0;  // 2^50: no tensor is la
 constexpr int64_t kTcMinColumns = 32;
 
 pa_status fail(pa_status code, const char* fmt, ...) {
-  char buf[512];
   va_list ap;
   va_start(ap, fmt);
-  vsnprintf(buf, sizeof(buf), fmt, ap);
+  vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
   va_end(ap);
-  g_last_error = buf;
   return code;
 }
 
 pa_status ok() {
-  g_last_error.clear();
+  g_last_error[0] = '\0';
   return PA_OK;
 }
 
@@ -189,7 +187,13 @@ pa_status device_state(DeviceState** out, int* dev_out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
-  DeviceState& st = g_dev[dev];
+  DeviceState* stp;
+  try {
+    stp = &g_dev[dev];
+  } catch (const std::bad_alloc&) {
+    return fail(PA_ERR_HOST_MEMORY, "host memory exhausted");
+  }
+  DeviceState& st = *stp;
   if (!st.init) {
     e = cudaDeviceGetAttribute(&st.num_sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
@@ -329,7 +333,11 @@ pa_status plan_decode(DeviceState* st, int ct, int qt, bool mq, int64_t B, int C
   if (it == st->occupancy.end()) {
     e = p->fam.prepare(D, p->nt, p->smem, &ctas);
     if (e != cudaSuccess) return cuda_fail(e, "decode kernel setup");
-    st->occupancy[key] = ctas;
+    try {
+      st->occupancy[key] = ctas;
+    } catch (const std::bad_alloc&) {
+      return fail(PA_ERR_HOST_MEMORY, "host memory exhausted");
+    }
   } else {
     ctas = it->second;
   }
@@ -358,7 +366,11 @@ pa_status get_workspace(DeviceState* st, cudaStream_t stream, const WsLayout& la
                   st->user_ws.bytes, need);
     w = &st->user_ws;
   } else {
-    w = &st->lib_ws[reinterpret_cast<uintptr_t>(stream)];
+    try {
+      w = &st->lib_ws[reinterpret_cast<uintptr_t>(stream)];
+    } catch (const std::bad_alloc&) {
+      return fail(PA_ERR_HOST_MEMORY, "host memory exhausted");
+    }
     if (w->bytes < need) {
       cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
       cudaError_t e = cudaStreamIsCapturing(stream, &cap);
@@ -402,7 +414,7 @@ pa_status get_workspace(DeviceState* st, cudaStream_t stream, const WsLayout& la
 
 extern "C" {
 
-const char* pa_last_error(void) { return g_last_error.c_str(); }
+const char* pa_last_error(void) { return g_last_error; }
 
 int32_t pa_version(void) { return 10000; }
 
