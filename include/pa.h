@@ -180,10 +180,16 @@ pa_status pa_decode(const pa_tensor* out, const pa_tensor* q, const pa_tensor* k
  * workspace, the call keeps its scratch in one 32 MiB array compiled into the
  * library; every GPU that loads the library holds that array until the
  * process exits. The call allocates and frees nothing (no cudaMalloc or
- * cudaFree, directly or through another library). A step whose scratch would
- * exceed 32 MiB (roughly: batch * num_kv_heads * G * head_dim beyond what fits
- * next to the per-warp partials; for example G = 16 with head_dim 256) is
- * rejected with PA_ERR_WORKSPACE and a message giving the bytes needed.
+ * cudaFree, directly or through another library). The scratch a step needs
+ * is about 2.1 MB of counters plus
+ *   4 * (G * head_dim + 2 * G rounded up to 4) * (2 * batch * num_kv_heads + 5 * W)
+ * bytes of partial results, where W is the number of worker warps of the
+ * decode kernel: 2 * (SM count) * 4, or * 8 for e4m3 caches with head_dim 128
+ * (W = 1216 or 2432 on a 152-SM GB300). The per-warp term dominates small
+ * batches: a batch of 64 with 8 KV heads, G = 4 and head_dim 128 needs about
+ * 16.9 MB; a batch of 256 of that shape with an e4m3 cache needs about
+ * 35.9 MB. A step beyond 32 MiB is rejected with PA_ERR_WORKSPACE and a
+ * message giving the bytes needed.
  *
  * The first call on a device looks up that device's address of the array
  * (cudaGetSymbolAddress, with that device current); make that first call

@@ -10,8 +10,7 @@
 // the process runs, and every call shares it.
 #include <cuda_runtime.h>
 
-#include <mutex>
-#include <unordered_map>
+#include <atomic>
 
 #include "pa.h"
 #include "pa_internal.h"
@@ -19,29 +18,37 @@
 namespace {
 
 constexpr size_t kNoallocScratchBytes = size_t(32) << 20;  // 32 MiB
+constexpr int kMaxDevices = 64;  // device ordinals this entry point serves
 
 // The scratch itself. Host code must not pass `g_noalloc_scratch` to a kernel:
 // on the host that name is only a stand-in, not a device address. The device
 // address comes from cudaGetSymbolAddress below.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
 
-std::mutex g_noalloc_mu;
-std::unordered_map<int, void*> g_noalloc_addr;  // device -> address of the array
+// Device address of the array, per device ordinal (null until first looked
+// up). A fixed table of atomics: the lookup takes no lock and allocates no
+// host memory, so nothing here can throw. Two threads that race on the first
+// call of a device both store the same address.
+std::atomic<void*> g_noalloc_addr[kMaxDevices];
 
 // Resolves the array's device address once per device, with that device
 // current (the caller's current device).
 pa_status noalloc_scratch(void** ptr) {
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return PA_ERR_CUDA;
-  std::lock_guard<std::mutex> lk(g_noalloc_mu);
-  auto it = g_noalloc_addr.find(dev);
-  if (it == g_noalloc_addr.end()) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
-      return PA_ERR_CUDA;
-    it = g_noalloc_addr.emplace(dev, p).first;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return pa::set_cuda_error(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices)
+    return pa::set_error(PA_ERR_UNSUPPORTED,
+                         "pa_decode_noalloc serves device ordinals below 64 only");
+  void* p = g_noalloc_addr[dev].load(std::memory_order_acquire);
+  if (p == nullptr) {
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return pa::set_cuda_error(e, "cudaGetSymbolAddress(scratch array)");
+    if (p == nullptr)
+      return pa::set_error(PA_ERR_CUDA, "cudaGetSymbolAddress(scratch array) gave no address");
+    g_noalloc_addr[dev].store(p, std::memory_order_release);
   }
-  *ptr = it->second;
+  *ptr = p;
   return PA_OK;
 }
 
@@ -53,10 +60,12 @@ extern "C" pa_status pa_decode_noalloc(const pa_tensor* out, const pa_tensor* q,
                                        int32_t num_kv_heads, float scale, int32_t block_size,
                                        int32_t window, int32_t kv_dtype, float k_scale,
                                        float v_scale, pa_stream stream) {
-  void* scratch = nullptr;
-  const pa_status s = noalloc_scratch(&scratch);
-  if (s != PA_OK) return s;
-  return pa::decode_in_buffer(out, q, key_cache, value_cache, block_tables, seq_lens,
-                              num_kv_heads, scale, block_size, window, kv_dtype, k_scale,
-                              v_scale, stream, scratch, kNoallocScratchBytes);
+  return pa::abi_guard([&]() -> pa_status {
+    void* scratch = nullptr;
+    const pa_status s = noalloc_scratch(&scratch);
+    if (s != PA_OK) return s;
+    return pa::decode_in_buffer(out, q, key_cache, value_cache, block_tables, seq_lens,
+                                num_kv_heads, scale, block_size, window, kv_dtype, k_scale,
+                                v_scale, stream, scratch, kNoallocScratchBytes);
+  });
 }

@@ -448,24 +448,26 @@ pa_status pa_profile_events(void* ev_before, void* ev_after) {
 }
 
 pa_status pa_set_workspace(void* ptr, size_t bytes) {
-  if (ptr && (reinterpret_cast<uintptr_t>(ptr) % 256))
-    return fail(PA_ERR_LAYOUT, "workspace must be 256-byte aligned");
-  std::lock_guard<std::mutex> lk(g_mu);
-  DeviceState* st;
-  pa_status s = device_state(&st, nullptr);
-  if (s) return s;
-  if (ptr && bytes) {
-    // The pool counter must start at zero; zero the whole buffer.
-    cudaError_t e = cudaMemset(ptr, 0, bytes);
-    if (e == cudaSuccess) e = cudaDeviceSynchronize();
-    if (e != cudaSuccess) return cuda_fail(e, "zeroing the workspace");
-  }
-  st->user_ws = Workspace{};
-  if (ptr) {
-    st->user_ws.ptr = ptr;
-    st->user_ws.bytes = bytes;
-  }
-  return ok();
+  return pa::abi_guard([&]() -> pa_status {
+    if (ptr && (reinterpret_cast<uintptr_t>(ptr) % 256))
+      return fail(PA_ERR_LAYOUT, "workspace must be 256-byte aligned");
+    std::lock_guard<std::mutex> lk(g_mu);
+    DeviceState* st;
+    pa_status s = device_state(&st, nullptr);
+    if (s) return s;
+    if (ptr && bytes) {
+      // The pool counter must start at zero; zero the whole buffer.
+      cudaError_t e = cudaMemset(ptr, 0, bytes);
+      if (e == cudaSuccess) e = cudaDeviceSynchronize();
+      if (e != cudaSuccess) return cuda_fail(e, "zeroing the workspace");
+    }
+    st->user_ws = Workspace{};
+    if (ptr) {
+      st->user_ws.ptr = ptr;
+      st->user_ws.bytes = bytes;
+    }
+    return ok();
+  });
 }
 
 }  // extern "C"
@@ -502,112 +504,120 @@ extern "C" {
 
 pa_status pa_decode_workspace_size(int64_t batch, int32_t num_q_heads, int32_t num_kv_heads,
                                    int32_t head_dim, size_t* bytes) {
-  return workspace_size(batch, 1, num_q_heads, num_kv_heads, head_dim, bytes);
+  return pa::abi_guard([&]() -> pa_status {
+    return workspace_size(batch, 1, num_q_heads, num_kv_heads, head_dim, bytes);
+  });
 }
 
 pa_status pa_prefill_chunk_workspace_size(int64_t batch, int32_t num_queries, int32_t num_q_heads,
                                           int32_t num_kv_heads, int32_t head_dim, size_t* bytes) {
-  return workspace_size(batch, num_queries, num_q_heads, num_kv_heads, head_dim, bytes);
+  return pa::abi_guard([&]() -> pa_status {
+    return workspace_size(batch, num_queries, num_q_heads, num_kv_heads, head_dim, bytes);
+  });
 }
 
 pa_status pa_check_device_error(int32_t* bits, pa_stream stream) {
-  if (!bits) return fail(PA_ERR_INVALID_ARG, "bits is null");
-  DeviceState* st;
-  {
-    std::lock_guard<std::mutex> lk(g_mu);
-    pa_status s = device_state(&st, nullptr);
-    if (s) return s;
-  }
-  cudaStream_t cs = static_cast<cudaStream_t>(stream);
-  int32_t v = 0;
-  cudaError_t e = cudaMemcpyAsync(&v, st->err_word, sizeof(v), cudaMemcpyDeviceToHost, cs);
-  if (e == cudaSuccess) e = cudaMemsetAsync(st->err_word, 0, sizeof(int32_t), cs);
-  if (e == cudaSuccess) e = cudaStreamSynchronize(cs);
-  if (e != cudaSuccess) return cuda_fail(e, "reading the device error word");
-  *bits = v;
-  return ok();
+  return pa::abi_guard([&]() -> pa_status {
+    if (!bits) return fail(PA_ERR_INVALID_ARG, "bits is null");
+    DeviceState* st;
+    {
+      std::lock_guard<std::mutex> lk(g_mu);
+      pa_status s = device_state(&st, nullptr);
+      if (s) return s;
+    }
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    int32_t v = 0;
+    cudaError_t e = cudaMemcpyAsync(&v, st->err_word, sizeof(v), cudaMemcpyDeviceToHost, cs);
+    if (e == cudaSuccess) e = cudaMemsetAsync(st->err_word, 0, sizeof(int32_t), cs);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(cs);
+    if (e != cudaSuccess) return cuda_fail(e, "reading the device error word");
+    *bits = v;
+    return ok();
+  });
 }
 
 pa_status pa_reshape_and_cache(const pa_tensor* k, const pa_tensor* v, const pa_tensor* key_cache,
                                const pa_tensor* value_cache, const pa_tensor* slot_mapping,
                                int32_t kv_dtype, float k_scale, float v_scale, pa_stream stream) {
-  pa_status s;
-  if ((s = check_tensor(k, "k", 3)) || (s = check_tensor(v, "v", 3)) ||
-      (s = check_tensor(key_cache, "key_cache", 4)) ||
-      (s = check_tensor(value_cache, "value_cache", 4)) ||
-      (s = check_tensor(slot_mapping, "slot_mapping", 1)))
-    return s;
-  if (k->dtype != PA_F16 && k->dtype != PA_BF16)
-    return fail(PA_ERR_UNSUPPORTED, "k must be f16 or bf16");
-  if (v->dtype != k->dtype) return fail(PA_ERR_INVALID_ARG, "k and v dtypes differ");
-  for (int i = 0; i < 3; ++i)
-    if (k->shape[i] != v->shape[i]) return fail(PA_ERR_INVALID_ARG, "k and v shapes differ");
-  const int64_t T = k->shape[0], H = k->shape[1], D = k->shape[2];
-  if (kv_dtype != PA_KV_AUTO && kv_dtype != PA_KV_FP8_E4M3)
-    return fail(PA_ERR_INVALID_ARG, "bad kv_dtype %d", kv_dtype);
-  const bool fp8 = kv_dtype == PA_KV_FP8_E4M3;
-  const int32_t cdt = fp8 ? PA_FP8_E4M3 : k->dtype;
-  if (key_cache->dtype != cdt || value_cache->dtype != cdt)
-    return fail(PA_ERR_INVALID_ARG, "cache dtype does not match kv_dtype");
-  for (int i = 0; i < 4; ++i)
-    if (key_cache->shape[i] != value_cache->shape[i])
-      return fail(PA_ERR_INVALID_ARG, "key and value cache shapes differ");
-  if (key_cache->shape[1] != H || key_cache->shape[3] != D)
-    return fail(PA_ERR_INVALID_ARG, "cache [NB, Hkv, bs, D] does not match k [T, Hkv, D]");
-  if (slot_mapping->dtype != PA_I64 || slot_mapping->shape[0] != T)
-    return fail(PA_ERR_INVALID_ARG, "slot_mapping must be int64 [T]");
-  if (D % 8) return fail(PA_ERR_UNSUPPORTED, "head_dim must be a multiple of 8");
-  if (!is_contiguous(key_cache) || !is_contiguous(value_cache) || !is_contiguous(slot_mapping))
-    return fail(PA_ERR_LAYOUT, "caches and slot_mapping must be contiguous");
-  for (const pa_tensor* x : {k, v}) {
-    if (T == 0) break;  // no rows: nothing is read
-    if (x->strides[2] != 1 || (H > 1 && x->strides[1] != D))
-      return fail(PA_ERR_LAYOUT, "k/v rows [Hkv, D] must be contiguous");
-    if ((reinterpret_cast<uintptr_t>(x->data) % 16) || (x->strides[0] % 8))
-      return fail(PA_ERR_LAYOUT, "k/v rows must be 16-byte aligned");
-  }
-  if ((reinterpret_cast<uintptr_t>(key_cache->data) % 16) ||
-      (reinterpret_cast<uintptr_t>(value_cache->data) % 16))
-    return fail(PA_ERR_LAYOUT, "caches must be 16-byte aligned");
-  if (fp8 && !(std::isfinite(k_scale) && std::isfinite(v_scale) && k_scale > 0 && v_scale > 0))
-    return fail(PA_ERR_INVALID_ARG, "fp8 scales must be finite and positive");
-  if (key_cache->data == value_cache->data && numel(key_cache) > 0)
-    return fail(PA_ERR_INVALID_ARG, "key and value caches alias");
-  if (T > (int64_t(1) << 30) || H > 65535) return fail(PA_ERR_UNSUPPORTED, "too many tokens/heads");
-  if (T == 0 || H == 0) return ok();
-  if ((s = check_accessible(k, "k")) || (s = check_accessible(v, "v")) ||
-      (s = check_accessible(key_cache, "key_cache")) ||
-      (s = check_accessible(value_cache, "value_cache")) ||
-      (s = check_accessible(slot_mapping, "slot_mapping")))
-    return s;
-
-  DeviceState* st;
-  {
-    std::lock_guard<std::mutex> lk(g_mu);
-    if ((s = device_state(&st, nullptr))) return s;
-  }
-  pa::ReshapeArgs a;
-  a.k = k->data;
-  a.v = v->data;
-  a.kc = key_cache->data;
-  a.vc = value_cache->data;
-  a.slots = static_cast<const int64_t*>(slot_mapping->data);
-  a.err = st->err_word;
-  a.k_stride_t = k->strides[0];
-  a.k_stride_h = D;
-  a.v_stride_t = v->strides[0];
-  a.v_stride_h = D;
-  a.T = static_cast<int>(T);
-  a.H = static_cast<int>(H);
-  a.D = static_cast<int>(D);
-  a.bs = static_cast<int>(key_cache->shape[2]);
-  a.NB = key_cache->shape[0];
-  a.k_scale = k_scale;
-  a.v_scale = v_scale;
-  cudaError_t e = pa::reshape_launch(k->dtype, fp8, a, static_cast<cudaStream_t>(stream));
-  if (e != cudaSuccess) return cuda_fail(e, "reshape_and_cache launch");
-  g_launches += 1;
-  return ok();
+  return pa::abi_guard([&]() -> pa_status {
+    pa_status s;
+    if ((s = check_tensor(k, "k", 3)) || (s = check_tensor(v, "v", 3)) ||
+        (s = check_tensor(key_cache, "key_cache", 4)) ||
+        (s = check_tensor(value_cache, "value_cache", 4)) ||
+        (s = check_tensor(slot_mapping, "slot_mapping", 1)))
+      return s;
+    if (k->dtype != PA_F16 && k->dtype != PA_BF16)
+      return fail(PA_ERR_UNSUPPORTED, "k must be f16 or bf16");
+    if (v->dtype != k->dtype) return fail(PA_ERR_INVALID_ARG, "k and v dtypes differ");
+    for (int i = 0; i < 3; ++i)
+      if (k->shape[i] != v->shape[i]) return fail(PA_ERR_INVALID_ARG, "k and v shapes differ");
+    const int64_t T = k->shape[0], H = k->shape[1], D = k->shape[2];
+    if (kv_dtype != PA_KV_AUTO && kv_dtype != PA_KV_FP8_E4M3)
+      return fail(PA_ERR_INVALID_ARG, "bad kv_dtype %d", kv_dtype);
+    const bool fp8 = kv_dtype == PA_KV_FP8_E4M3;
+    const int32_t cdt = fp8 ? PA_FP8_E4M3 : k->dtype;
+    if (key_cache->dtype != cdt || value_cache->dtype != cdt)
+      return fail(PA_ERR_INVALID_ARG, "cache dtype does not match kv_dtype");
+    for (int i = 0; i < 4; ++i)
+      if (key_cache->shape[i] != value_cache->shape[i])
+        return fail(PA_ERR_INVALID_ARG, "key and value cache shapes differ");
+    if (key_cache->shape[1] != H || key_cache->shape[3] != D)
+      return fail(PA_ERR_INVALID_ARG, "cache [NB, Hkv, bs, D] does not match k [T, Hkv, D]");
+    if (slot_mapping->dtype != PA_I64 || slot_mapping->shape[0] != T)
+      return fail(PA_ERR_INVALID_ARG, "slot_mapping must be int64 [T]");
+    if (D % 8) return fail(PA_ERR_UNSUPPORTED, "head_dim must be a multiple of 8");
+    if (!is_contiguous(key_cache) || !is_contiguous(value_cache) || !is_contiguous(slot_mapping))
+      return fail(PA_ERR_LAYOUT, "caches and slot_mapping must be contiguous");
+    for (const pa_tensor* x : {k, v}) {
+      if (T == 0) break;  // no rows: nothing is read
+      if (x->strides[2] != 1 || (H > 1 && x->strides[1] != D))
+        return fail(PA_ERR_LAYOUT, "k/v rows [Hkv, D] must be contiguous");
+      if ((reinterpret_cast<uintptr_t>(x->data) % 16) || (x->strides[0] % 8))
+        return fail(PA_ERR_LAYOUT, "k/v rows must be 16-byte aligned");
+    }
+    if ((reinterpret_cast<uintptr_t>(key_cache->data) % 16) ||
+        (reinterpret_cast<uintptr_t>(value_cache->data) % 16))
+      return fail(PA_ERR_LAYOUT, "caches must be 16-byte aligned");
+    if (fp8 && !(std::isfinite(k_scale) && std::isfinite(v_scale) && k_scale > 0 && v_scale > 0))
+      return fail(PA_ERR_INVALID_ARG, "fp8 scales must be finite and positive");
+    if (key_cache->data == value_cache->data && numel(key_cache) > 0)
+      return fail(PA_ERR_INVALID_ARG, "key and value caches alias");
+    if (T > (int64_t(1) << 30) || H > 65535) return fail(PA_ERR_UNSUPPORTED, "too many tokens/heads");
+    if (T == 0 || H == 0) return ok();
+    if ((s = check_accessible(k, "k")) || (s = check_accessible(v, "v")) ||
+        (s = check_accessible(key_cache, "key_cache")) ||
+        (s = check_accessible(value_cache, "value_cache")) ||
+        (s = check_accessible(slot_mapping, "slot_mapping")))
+      return s;
+  
+    DeviceState* st;
+    {
+      std::lock_guard<std::mutex> lk(g_mu);
+      if ((s = device_state(&st, nullptr))) return s;
+    }
+    pa::ReshapeArgs a;
+    a.k = k->data;
+    a.v = v->data;
+    a.kc = key_cache->data;
+    a.vc = value_cache->data;
+    a.slots = static_cast<const int64_t*>(slot_mapping->data);
+    a.err = st->err_word;
+    a.k_stride_t = k->strides[0];
+    a.k_stride_h = D;
+    a.v_stride_t = v->strides[0];
+    a.v_stride_h = D;
+    a.T = static_cast<int>(T);
+    a.H = static_cast<int>(H);
+    a.D = static_cast<int>(D);
+    a.bs = static_cast<int>(key_cache->shape[2]);
+    a.NB = key_cache->shape[0];
+    a.k_scale = k_scale;
+    a.v_scale = v_scale;
+    cudaError_t e = pa::reshape_launch(k->dtype, fp8, a, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "reshape_and_cache launch");
+    g_launches += 1;
+    return ok();
+  });
 }
 
 }  // extern "C"
@@ -901,8 +911,10 @@ pa_status pa_decode(const pa_tensor* out, const pa_tensor* q, const pa_tensor* k
                     const pa_tensor* seq_lens, int32_t num_kv_heads, float scale,
                     int32_t block_size, int32_t window, int32_t kv_dtype, float k_scale,
                     float v_scale, pa_stream stream) {
-  return decode_entry(out, q, key_cache, value_cache, block_tables, seq_lens, num_kv_heads, scale,
-                      block_size, window, kv_dtype, k_scale, v_scale, stream, false);
+  return pa::abi_guard([&]() -> pa_status {
+    return decode_entry(out, q, key_cache, value_cache, block_tables, seq_lens, num_kv_heads, scale,
+                        block_size, window, kv_dtype, k_scale, v_scale, stream, false);
+  });
 }
 
 pa_status pa_prefill_chunk(const pa_tensor* out, const pa_tensor* q, const pa_tensor* key_cache,
@@ -910,8 +922,10 @@ pa_status pa_prefill_chunk(const pa_tensor* out, const pa_tensor* q, const pa_te
                            const pa_tensor* seq_lens, int32_t num_kv_heads, float scale,
                            int32_t block_size, int32_t window, int32_t kv_dtype, float k_scale,
                            float v_scale, pa_stream stream) {
-  return decode_entry(out, q, key_cache, value_cache, block_tables, seq_lens, num_kv_heads, scale,
-                      block_size, window, kv_dtype, k_scale, v_scale, stream, true);
+  return pa::abi_guard([&]() -> pa_status {
+    return decode_entry(out, q, key_cache, value_cache, block_tables, seq_lens, num_kv_heads, scale,
+                        block_size, window, kv_dtype, k_scale, v_scale, stream, true);
+  });
 }
 
 }  // extern "C"
@@ -953,4 +967,9 @@ pa_status decode_in_buffer(const pa_tensor* out, const pa_tensor* q, const pa_te
   if (e != cudaSuccess) return cuda_fail(e, "clearing the scratch counters");
   return run_decode(c, st, plan, layout, buffer, nullptr, cs);
 }
+}  // namespace pa
+
+namespace pa {
+pa_status set_error(pa_status code, const char* msg) { return fail(code, "%s", msg); }
+pa_status set_cuda_error(cudaError_t e, const char* what) { return cuda_fail(e, what); }
 }  // namespace pa

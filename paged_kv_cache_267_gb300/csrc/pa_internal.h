@@ -160,7 +160,31 @@ cudaError_t device_error_word(int32_t** ptr);  // address of this device's error
 
 #include "pa.h"
 
+#include <exception>
+#include <new>
+
 namespace pa {
+
+// Records a message for pa_last_error() on the calling thread and returns
+// `code` (pa_api.cpp; never throws).
+pa_status set_error(pa_status code, const char* msg);
+pa_status set_cuda_error(cudaError_t e, const char* what);
+
+// Runs an entry point's body so that no C++ exception leaves it: host memory
+// exhaustion becomes PA_ERR_HOST_MEMORY, any other exception from the C++
+// runtime (a mutex that cannot be locked, for one) PA_ERR_CUDA.
+template <typename F>
+pa_status abi_guard(F&& body) noexcept {
+  try {
+    return body();
+  } catch (const std::bad_alloc&) {
+    return set_error(PA_ERR_HOST_MEMORY, "host memory exhausted");
+  } catch (const std::exception& ex) {
+    return set_error(PA_ERR_CUDA, ex.what());
+  } catch (...) {
+    return set_error(PA_ERR_CUDA, "unexpected host exception");
+  }
+}
 
 // pa_decode with the scratch in a given device buffer (pa_api.cpp).
 pa_status decode_in_buffer(const pa_tensor* out, const pa_tensor* q, const pa_tensor* key_cache,
