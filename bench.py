@@ -44,6 +44,8 @@ import torch  # noqa: E402
 from workloads import generate, get_config  # noqa: E402
 
 METRIC = "paged decode attention: μs/step, achieved HBM GB/s and % of GB300 peak"
+# the other seeded decode workloads, reported beside the main one
+DEFAULT_EXTRA_CONFIGS = "long_skew,fp8,prefix_window,tiny"
 UNIT = "GB/s"
 
 
@@ -186,10 +188,30 @@ def profiled_traffic(config: str, decode_launch_bytes: float):
     return d.get("dram_bytes_per_launch")
 
 
+def relaunch_under_torchrun(n_gpus: int) -> None:
+    """`--gpus N` (N > 1) started without a launcher: run this same command
+    as N processes under torch.distributed.run on this node (one per GPU),
+    and exit with its status. Never runs one rank silently."""
+    import socket
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        port = sk.getsockname()[1]
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
+           f"--nproc-per-node={n_gpus}", "--master-addr", "127.0.0.1",
+           "--master-port", str(port), os.path.abspath(__file__), *sys.argv[1:]]
+    sys.stdout.flush()
+    sys.exit(subprocess.call(cmd))
+
+
 def dist_setup(n_gpus: int):
+    """Rank layout from the launcher's environment. With no launcher and
+    `--gpus N > 1` the caller relaunches under torch.distributed.run first; a
+    launcher whose world size differs from `--gpus` is an error."""
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
+    if "WORLD_SIZE" in os.environ and world != n_gpus:
+        raise SystemExit(f"bench.py: --gpus {n_gpus} but the launcher started {world} ranks")
     if world > 1:
         import torch.distributed as dist
         backend = "nccl" if torch.cuda.is_available() else "gloo"
@@ -373,104 +395,190 @@ def workload_desc(s) -> str:
 
 # ----------------------------------------------------------- our arm
 
-def run_ours(args, world, rank, local):
-    import paged_kv_cache_267_gb300 as pa
-    from paged_kv_cache_267_gb300.build import build_library
-    build_library()
-    dev = torch.device(f"cuda:{local}")
-    torch.cuda.set_device(dev)
-    w = generate(rank_spec(args.config, rank), device=dev)
+def unique_kv_bytes(w) -> int:
+    """K/V bytes of the distinct cache rows the step reads: a physical slot
+    read by several sequences (a shared prefix block) counts once."""
     s = w.spec
-    kv = "fp8" if s.kv_fp8 else "auto"
-    if s.kv_fp8:
-        kc, vc = w.empty_fp8_cache()
-        pa.reshape_and_cache(w.k_hist, w.v_hist, kc, vc, w.slot_hist, kv, w.k_scale, w.v_scale)
-        w.k_hist = w.v_hist = w.slot_hist = None
-    else:
-        kc, vc = w.key_cache, w.value_cache
-    bt = torch.from_numpy(w.block_tables).to(dev)
-    sl = torch.from_numpy(w.seq_lens).to(dev)
-    out = torch.empty_like(w.q)
-    stream = torch.cuda.current_stream()
-    kw = dict(num_kv_heads=s.num_kv_heads, scale=s.softmax_scale, block_size=s.block_size,
-              window=s.window, kv_dtype=kv, k_scale=w.k_scale, v_scale=w.v_scale, out=out)
+    L = w.seq_lens.astype(np.int64)
+    st = w.starts.astype(np.int64)
+    slots = []
+    for b in range(s.batch):
+        if L[b] <= st[b]:
+            continue
+        pos = np.arange(st[b], L[b], dtype=np.int64)
+        slots.append(w.block_tables[b, pos // s.block_size].astype(np.int64) * s.block_size
+                     + pos % s.block_size)
+    n = int(np.unique(np.concatenate(slots)).size) if slots else 0
+    elt = 1 if s.kv_fp8 else 2
+    return n * s.num_kv_heads * 2 * s.head_dim * elt
 
-    attend = pa.decode if s.num_queries == 1 else pa.prefill_chunk
 
-    def step():
-        pa.reshape_and_cache(w.k_new, w.v_new, kc, vc, w.slot_new, kv, w.k_scale, w.v_scale)
-        attend(w.q, kc, vc, bt, sl, **kw)
+class StepCtx:
+    """One named workload on the device, ready to step: the write path of its
+    new tokens, then pa_decode (or pa_prefill_chunk for a chunk)."""
 
-    dbytes = decode_bytes(w)
-    rbytes = reshape_bytes(w)
-    step_bytes = dbytes["total"] + rbytes
-    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    nflush = max(4 * l2, 512 << 20)
-    flush_w = torch.empty(nflush, dtype=torch.uint8, device=dev)
-    flush_r = torch.ones(nflush // 8, dtype=torch.int64, device=dev)
-    flush_sink = torch.empty((), dtype=torch.int64, device=dev)
+    def __init__(self, pa, name: str, rank: int, dev):
+        self.pa = pa
+        self.name = name
+        w = generate(rank_spec(name, rank), device=dev)
+        s = w.spec
+        self.w, self.s = w, s
+        self.kv = "fp8" if s.kv_fp8 else "auto"
+        if s.kv_fp8:
+            self.kc, self.vc = w.empty_fp8_cache()
+            pa.reshape_and_cache(w.k_hist, w.v_hist, self.kc, self.vc, w.slot_hist, self.kv,
+                                 w.k_scale, w.v_scale)
+            w.k_hist = w.v_hist = w.slot_hist = None
+        else:
+            self.kc, self.vc = w.key_cache, w.value_cache
+        self.bt = torch.from_numpy(w.block_tables).to(dev)
+        self.sl = torch.from_numpy(w.seq_lens).to(dev)
+        self.out = torch.empty_like(w.q)
+        self.kw = dict(num_kv_heads=s.num_kv_heads, scale=s.softmax_scale,
+                       block_size=s.block_size, window=s.window, kv_dtype=self.kv,
+                       k_scale=w.k_scale, v_scale=w.v_scale, out=self.out)
+        self.attend = pa.decode if s.num_queries == 1 else pa.prefill_chunk
+        self.dbytes = decode_bytes(w)
+        self.rbytes = reshape_bytes(w)
+        self.step_bytes = self.dbytes["total"] + self.rbytes
 
-    class _Flush:
-        """Write a buffer four times the L2 size (evicts every line), then read
-        another one as large, so the timed step starts with a cold L2 that
-        holds no dirty lines whose write-back would land inside the timed
-        region (with only twice the L2 size some dirty lines survived and
-        slowed the next step measurably)."""
+    def step(self):
+        w = self.w
+        self.pa.reshape_and_cache(w.k_new, w.v_new, self.kc, self.vc, w.slot_new, self.kv,
+                                  w.k_scale, w.v_scale)
+        self.attend(w.q, self.kc, self.vc, self.bt, self.sl, **self.kw)
 
-        @staticmethod
-        def zero_():
-            flush_w.zero_()
-            torch.sum(flush_r, dim=0, out=flush_sink)
+    def attend_only(self):
+        self.attend(self.w.q, self.kc, self.vc, self.bt, self.sl, **self.kw)
 
-    flush = _Flush()
 
-    for _ in range(max(3, args.warmup)):
-        step()
+class L2Flush:
+    """Write a buffer four times the L2 size (evicts every line), then read
+    another one as large, so the timed step starts with a cold L2 that holds
+    no dirty lines whose write-back would land inside the timed region (with
+    only twice the L2 size some dirty lines survived and slowed the next step
+    measurably)."""
+
+    def __init__(self, dev):
+        l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+        n = max(4 * l2, 512 << 20)
+        self.w = torch.empty(n, dtype=torch.uint8, device=dev)
+        self.r = torch.ones(n // 8, dtype=torch.int64, device=dev)
+        self.sink = torch.empty((), dtype=torch.int64, device=dev)
+
+    def __call__(self):
+        self.w.zero_()
+        torch.sum(self.r, dim=0, out=self.sink)
+
+
+def timed_steps(ctx: StepCtx, flush, stream, steps: int, warmup: int, local: int,
+                world: int, quick: bool) -> dict:
+    """Device time per step (CUDA events on the launching stream, L2 flushed
+    before every step outside the events) and the clocks sampled over the
+    timed window, kept open for about a second of identical work."""
+    pa = ctx.pa
+    for _ in range(max(3, warmup)):
+        ctx.step()
     torch.cuda.synchronize()
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.15)
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     n0 = pa.launch_count()
     barrier(world)
     torch.cuda.synchronize()
     t_wall = time.perf_counter()
-    for i in range(args.steps):
-        flush.zero_()
+    for i in range(steps):
+        flush()
         starts[i].record(stream)
-        step()
+        ctx.step()
         ends[i].record(stream)
     torch.cuda.synchronize()
     barrier(world)
     wall = time.perf_counter() - t_wall
     launches = pa.launch_count() - n0
     step_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
-    # keep the clock window open for at least ~1 s of identical work
     extra = 0
-    while not args.quick and time.perf_counter() - t_wall < 1.0 and extra < 20000:
-        flush.zero_()
-        step()
+    while not quick and time.perf_counter() - t_wall < 1.0 and extra < 20000:
+        flush()
+        ctx.step()
         extra += 1
         if extra % 50 == 0:
             torch.cuda.synchronize()
     torch.cuda.synchronize()
     clk = clocks.stop()
-    ms_rank = statistics.mean(step_ms)
-    ms = max_over_ranks(ms_rank, world)
+    return {"ms": max_over_ranks(statistics.mean(step_ms), world), "clocks": clk,
+            "launches": launches, "wall": wall}
+
+
+def timed_kernel(ctx: StepCtx, flush, steps: int, world: int) -> float:
+    """Mean duration (ms) of the attention kernel alone: events recorded by
+    the library right around its launch, on its stream."""
+    pa = ctx.pa
+    ev_a = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ev_b = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    for i in range(steps):
+        flush()
+        pa.profile_events(ev_a[i], ev_b[i])
+        ctx.attend_only()
+    pa.profile_events(None, None)
+    torch.cuda.synchronize()
+    return max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in zip(ev_a, ev_b)), world)
+
+
+def extra_config(pa, name, args, world, rank, local, dev, flush, stream, peak) -> dict:
+    """The step and its attention kernel on another seeded workload, with
+    its own clock record."""
+    ctx = StepCtx(pa, name, rank, dev)
+    t = timed_steps(ctx, flush, stream, args.steps, args.warmup, local, world, args.quick)
+    k_ms = timed_kernel(ctx, flush, args.steps, world)
+    if pa.check_device_error():
+        raise RuntimeError(f"device error flag during the {name} benchmark")
+    total = sum_over_ranks(float(ctx.step_bytes), world)
+    gbs = total / (t["ms"] * 1e-3) / 1e9
+    achieved = ctx.dbytes["kernel"] / (k_ms * 1e-3) / 1e9
+    entry = {"workload": workload_desc(ctx.s), "us_per_step": t["ms"] * 1e3,
+             "value": gbs, "unit": UNIT, "pct_of_peak": 100.0 * gbs / world / peak,
+             "bytes_per_step_per_rank": ctx.step_bytes,
+             "attended_tokens_per_rank": ctx.dbytes["tokens"],
+             "roofline": {"bound": "hbm", "kernel": "paged_decode_kernel",
+                          "kernel_us": k_ms * 1e3, "bytes_per_launch": ctx.dbytes["kernel"],
+                          "achieved": achieved, "peak": peak, "unit": "GB/s",
+                          "frac": achieved / peak,
+                          "traffic": profiled_traffic(name, ctx.dbytes["kernel"])},
+             "gpu_launches": t["launches"], "clocks": t["clocks"]}
+    if ctx.s.shared_prefix:
+        # shared prefix blocks: logical bytes count them once per sequence that
+        # reads them (the metric's bytes), unique bytes once per step
+        entry["kv_bytes_logical"] = ctx.dbytes["kv"]
+        entry["kv_bytes_unique"] = unique_kv_bytes(ctx.w)
+    del ctx
+    torch.cuda.empty_cache()
+    return entry
+
+
+def run_ours(args, world, rank, local):
+    import paged_kv_cache_267_gb300 as pa
+    from paged_kv_cache_267_gb300.build import build_library
+    build_library()
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    ctx = StepCtx(pa, args.config, rank, dev)
+    w, s = ctx.w, ctx.s
+    kv, kc, vc, bt, sl, out, kw = ctx.kv, ctx.kc, ctx.vc, ctx.bt, ctx.sl, ctx.out, ctx.kw
+    attend = ctx.attend
+    stream = torch.cuda.current_stream()
+    dbytes, step_bytes = ctx.dbytes, ctx.step_bytes
+    flush = L2Flush(dev)
+
+    t = timed_steps(ctx, flush, stream, args.steps, args.warmup, local, world, args.quick)
+    ms, clk, launches, wall = t["ms"], t["clocks"], t["launches"], t["wall"]
     total_bytes = sum_over_ranks(float(step_bytes), world)
     value = total_bytes / (ms * 1e-3) / 1e9
 
     # ---- roofline: decode kernel alone, events around it on the launch stream
-    ev_a = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ev_b = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    for i in range(args.steps):
-        flush.zero_()
-        pa.profile_events(ev_a[i], ev_b[i])
-        attend(w.q, kc, vc, bt, sl, **kw)
-    pa.profile_events(None, None)
-    torch.cuda.synchronize()
-    k_ms = statistics.mean(a.elapsed_time(b) for a, b in zip(ev_a, ev_b))
+    k_ms = timed_kernel(ctx, flush, args.steps, world)
     peak, peak_kind = measured_peak()
     achieved = dbytes["kernel"] / (k_ms * 1e-3) / 1e9
     traffic = profiled_traffic(args.config, dbytes["kernel"])
@@ -482,12 +590,12 @@ def run_ours(args, world, rank, local):
     # ---- end to end through the public API with host buffers. The step's
     # host inputs (q, new k/v, slots, block tables, seq_lens) and its output
     # live in pinned host memory; the kernels use them in place.
-    host_in = {n: t.detach().cpu().contiguous().pin_memory() for n, t in
+    host_in = {n: t_.detach().cpu().contiguous().pin_memory() for n, t_ in
                (("q", w.q), ("k", w.k_new), ("v", w.v_new), ("slot", w.slot_new), ("bt", bt),
                 ("sl", sl))}
     host_res = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
     kw_host = dict(kw, out=host_res)
-    h2d_direct = sum(t.numel() * t.element_size() for t in host_in.values())
+    h2d_direct = sum(t_.numel() * t_.element_size() for t_ in host_in.values())
     d2h_direct = host_res.numel() * host_res.element_size()
 
     def e2e_direct():
@@ -498,20 +606,20 @@ def run_ours(args, world, rank, local):
     # The same with the copy engine: one packed pinned staging buffer (each
     # input at a 256-byte aligned offset) moved by one H2D copy, the library
     # on device views of it, and one D2H copy of the output.
-    parts = [(n, t.detach().contiguous()) for n, t in
+    parts = [(n, t_.detach().contiguous()) for n, t_ in
              (("q", w.q), ("k", w.k_new), ("v", w.v_new), ("slot", w.slot_new),
               ("bt", bt), ("sl", sl))]
     offs, off = {}, 0
-    for n, t in parts:
+    for n, t_ in parts:
         offs[n] = off
-        off += (t.numel() * t.element_size() + 255) // 256 * 256
+        off += (t_.numel() * t_.element_size() + 255) // 256 * 256
     host_stage = torch.empty(off, dtype=torch.uint8, pin_memory=True)
     dev_stage = torch.empty(off, dtype=torch.uint8, device=dev)
     dev_in = {}
-    for n, t in parts:
-        nb = t.numel() * t.element_size()
-        host_stage[offs[n]:offs[n] + nb].copy_(t.cpu().view(torch.uint8).reshape(-1))
-        dev_in[n] = dev_stage[offs[n]:offs[n] + nb].view(t.dtype).view(t.shape)
+    for n, t_ in parts:
+        nb = t_.numel() * t_.element_size()
+        host_stage[offs[n]:offs[n] + nb].copy_(t_.cpu().view(torch.uint8).reshape(-1))
+        dev_in[n] = dev_stage[offs[n]:offs[n] + nb].view(t_.dtype).view(t_.shape)
     host_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
     h2d = off  # bytes moved, alignment padding included
     d2h = host_out.numel() * host_out.element_size()
@@ -530,7 +638,7 @@ def run_ours(args, world, rank, local):
         e_s = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
         e_e = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
         for i in range(args.steps):
-            flush.zero_()
+            flush()
             e_s[i].record(stream)
             fn()
             e_e[i].record(stream)
@@ -551,18 +659,18 @@ def run_ours(args, world, rank, local):
     gstream.wait_stream(stream)
     with torch.cuda.stream(gstream):
         for _ in range(3):
-            step()  # the library's workspace for this stream exists before capture
+            ctx.step()  # the library's workspace for this stream exists before capture
     gstream.synchronize()
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph, stream=gstream):
-        step()
+        ctx.step()
     g_s = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     g_e = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     for _ in range(3):
         graph.replay()
     torch.cuda.synchronize()
     for i in range(args.steps):
-        flush.zero_()
+        flush()
         g_s[i].record(stream)
         graph.replay()
         g_e[i].record(stream)
@@ -580,6 +688,18 @@ def run_ours(args, world, rank, local):
         subset, queries = bounded_sample(w, kch, vch, args.cpu_budget / 2)
         cpu = oracle_baseline(w, kch, vch, budget_s=args.cpu_budget, seq_subset=subset,
                               queries=queries)
+        del kch, vch
+
+    # ---- the other seeded workloads, each with its own timed window
+    extras = {}
+    names = [n for n in (args.configs.split(",") if args.configs else []) if n and n != args.config]
+    if names:
+        del ctx, w, kc, vc, host_in, host_res, host_stage, dev_stage, dev_in, host_out, parts
+        kw = kw_host = None
+        torch.cuda.empty_cache()
+        for name in names:
+            extras[name] = extra_config(pa, name, args, world, rank, local, dev, flush, stream,
+                                        peak)
 
     if rank != 0:
         return
@@ -625,6 +745,8 @@ def run_ours(args, world, rank, local):
     }
     if cpu is not None:
         line["cpu_baseline"] = cpu
+    if extras:
+        line["configs"] = extras
     print(json.dumps(line), flush=True)
 
 
@@ -635,11 +757,18 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default="llama8b")
+    ap.add_argument("--configs", default=DEFAULT_EXTRA_CONFIGS,
+                    help="other seeded workloads timed after the main one, each reported "
+                         "under 'configs' in the JSON line (comma-separated; '' for none)")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--quick", action="store_true",
                     help="no CPU baseline and no clock-sampling extension (for profiler runs)")
     args = ap.parse_args()
+    if args.gpus < 1:
+        raise SystemExit("bench.py: --gpus must be at least 1")
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        relaunch_under_torchrun(args.gpus)
     world, rank, local = dist_setup(args.gpus)
     try:
         if args.impl == "reference":

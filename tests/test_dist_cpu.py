@@ -75,3 +75,33 @@ def test_reference_arm_runs_on_rank_zero_only(monkeypatch):
 
     bench.run_reference(Args, world=2, rank=1)   # other ranks exit without work
     assert calls == []
+
+
+def _bench_env(**extra):
+    env = {k: v for k, v in os.environ.items()
+           if k not in ("WORLD_SIZE", "RANK", "LOCAL_RANK", "MASTER_ADDR", "MASTER_PORT")}
+    env.update(CUDA_VISIBLE_DEVICES="", OMP_NUM_THREADS="1", **extra)
+    return env
+
+
+def test_gpus_flag_without_a_launcher_starts_that_many_ranks():
+    """`bench.py --gpus 2` with no launcher relaunches itself under
+    torch.distributed.run with two ranks (gloo here); the reference arm then
+    prints one line, from rank 0, for two GPUs."""
+    cmd = [sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--gpus", "2",
+           "--steps", "1", "--warmup", "0", "--config", "tiny"]
+    r = subprocess.run(cmd, env=_bench_env(), cwd=ROOT, capture_output=True, text=True,
+                       timeout=600)
+    assert r.returncode == 0, r.stderr[-3000:]
+    lines = [json.loads(ln) for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    assert lines[0]["impl"] == "reference" and lines[0]["n_gpus"] == 2
+
+
+def test_gpus_flag_must_match_the_launcher():
+    cmd = [sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--gpus", "2",
+           "--steps", "1", "--warmup", "0", "--config", "tiny"]
+    r = subprocess.run(cmd, env=_bench_env(WORLD_SIZE="1", RANK="0", LOCAL_RANK="0"), cwd=ROOT,
+                       capture_output=True, text=True, timeout=300)
+    assert r.returncode != 0
+    assert "--gpus 2 but the launcher started 1 ranks" in r.stderr

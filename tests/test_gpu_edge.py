@@ -233,42 +233,87 @@ def test_caller_owned_workspace(pa_lib):
         pa_lib.set_workspace(None)
 
 
-@pytest.mark.parametrize("pool", [False, True])
-def test_cuda_graph_replay_matches_eager(pool, pa_lib):
-    """Replay equals eager bit for bit with the dynamic pool off; with it on the
-    segment boundaries (and so the rounding) may differ between runs."""
+# Lengths of the graph-replay batches: same batch, pool and table shapes, new
+# lengths each replay (empty, one-token, tile- and block-edge, long)
+GRAPH_LENS = [(300, 17, 1, 2000, 0, 64), (5, 1999, 640, 33, 1, 16),
+              (2048, 2048, 2, 700, 15, 0), (1, 1, 1, 1, 1, 1)]
+
+
+@pytest.mark.parametrize("pool,window", [(False, 0), (True, 0), (True, 300)],
+                         ids=["static", "pool", "pool_window300"])
+def test_cuda_graph_replays_with_new_inputs_match_the_oracle(pool, window, pa_lib):
+    """The step (write path + decode) captured once in a CUDA graph, then
+    replayed once per input set after copying that set's caches, q, new
+    K/V rows, slots, block tables and lengths into the captured buffers. Each
+    replay's output must match the fp64 oracle on that set, and its caches the
+    oracle's write path bit for bit ("vLLM 0.5 深度解析" §5.1: the decode step
+    replayed as a CUDA graph)."""
     pa_lib.set_decode_tuning(0, 0, 0 if pool else -1, 0)
     try:
-        _graph_vs_eager(pa_lib, exact=not pool)
+        _graph_replays_vs_oracle(pa_lib, window)
     finally:
         pa_lib.set_decode_tuning(0, 0, 0, 0)
 
 
-def _graph_vs_eager(pa_lib, exact):
-    s = spec(seq_lens=(300, 17, 1, 2000))
-    w = generate(s, device="cuda")
-    bt = torch.from_numpy(w.block_tables).cuda()
-    sl = torch.from_numpy(w.seq_lens).cuda()
-    kw = dict(num_kv_heads=2, scale=s.softmax_scale, block_size=16)
+def _graph_replays_vs_oracle(pa_lib, window):
+    sets = []
+    for i, lens in enumerate(GRAPH_LENS):
+        s = spec(seq_lens=lens, pool_blocks=400, max_len=2048, window=window, seed=700 + i)
+        w = generate(s, device="cuda")
+        # oracle inputs: host copies of the generator's output, then the
+        # oracle's own write path
+        kc_ref, vc_ref = host_copy(w.key_cache), host_copy(w.value_cache)
+        oracle.reshape_and_cache(w.k_new.cpu(), w.v_new.cpu(), kc_ref, vc_ref,
+                                 w.slot_new.cpu().numpy(), s.dtype, s.dtype)
+        ref = oracle.decode(w.q.cpu(), kc_ref, vc_ref, w.block_tables, w.seq_lens,
+                            num_kv_heads=s.num_kv_heads, scale=s.softmax_scale,
+                            block_size=s.block_size, window=s.window, q_dtype=s.dtype,
+                            cache_dtype=s.dtype)
+        sets.append((w, kc_ref, vc_ref, ref))
+    w0 = sets[0][0]
+    s0 = w0.spec
+    # the captured buffers
+    kc, vc = w0.key_cache.clone(), w0.value_cache.clone()
+    q, k_new, v_new = w0.q.clone(), w0.k_new.clone(), w0.v_new.clone()
+    slots = w0.slot_new.clone()
+    bt = torch.from_numpy(w0.block_tables).cuda()
+    sl = torch.from_numpy(w0.seq_lens).cuda()
+    out = torch.empty_like(q)
+    kw = dict(num_kv_heads=s0.num_kv_heads, scale=s0.softmax_scale, block_size=s0.block_size,
+              window=window)
     stream = torch.cuda.Stream()
-    out = torch.empty_like(w.q)
+
+    def step():
+        pa_lib.reshape_and_cache(k_new, v_new, kc, vc, slots)
+        pa_lib.decode(q, kc, vc, bt, sl, out=out, **kw)
+
     with torch.cuda.stream(stream):
-        pa_lib.reshape_and_cache(w.k_new, w.v_new, w.key_cache, w.value_cache, w.slot_new)
-        pa_lib.decode(w.q, w.key_cache, w.value_cache, bt, sl, out=out, **kw)
+        step()  # the library's workspace for this stream exists before capture
     stream.synchronize()
-    eager = out.clone()
-    out.zero_()
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=stream):
-        pa_lib.reshape_and_cache(w.k_new, w.v_new, w.key_cache, w.value_cache, w.slot_new)
-        pa_lib.decode(w.q, w.key_cache, w.value_cache, bt, sl, out=out, **kw)
-    for _ in range(3):
-        g.replay()
-    torch.cuda.synchronize()
-    if exact:
-        assert torch.equal(out.view(torch.int16), eager.view(torch.int16))
-    else:
-        assert (out.float() - eager.float()).abs().max().item() < 1e-2
+        step()
+    for r, (w, kc_ref, vc_ref, ref) in enumerate(sets * 2):  # every set twice
+        with torch.cuda.stream(stream):
+            kc.copy_(w.key_cache)
+            vc.copy_(w.value_cache)
+            q.copy_(w.q)
+            k_new.copy_(w.k_new)
+            v_new.copy_(w.v_new)
+            slots.copy_(w.slot_new)
+            bt.copy_(torch.from_numpy(w.block_tables))
+            sl.copy_(torch.from_numpy(w.seq_lens))
+            out.fill_(float("nan"))
+            g.replay()
+        stream.synchronize()
+        what = f"replay {r} lens {tuple(int(x) for x in w.seq_lens)} window {window}"
+        assert np.array_equal(host_copy(kc), kc_ref), f"{what}: key cache"
+        assert np.array_equal(host_copy(vc), vc_ref), f"{what}: value cache"
+        assert_close(out_f64(out), ref, what=what)
+        for b, L in enumerate(w.seq_lens):
+            if L == 0:
+                assert (out[b] == 0).all()
+    assert pa_lib.check_device_error() == 0
 
 
 def test_allocator_built_layout_with_sharing_and_cow(pa_lib):

@@ -1,5 +1,6 @@
 """Structure of the seeded workloads: layouts, sharing, poisoning, determinism."""
 import numpy as np
+import pytest
 import torch
 
 from workloads import CONFIGS, generate
@@ -126,3 +127,81 @@ def test_chunk_workload_new_rows_and_union_range():
     p = L - T - 1
     slot = int(w.block_tables[b, p // 16]) * 16 + p % 16
     assert not torch.isnan(kc[slot].float()).any()
+
+
+# ---- layouts come from allocator requests
+
+def test_layout_splitmix64_published_outputs():
+    from workloads.layout import splitmix64
+    # Vigna's reference implementation seeded with 1234567 (its first outputs
+    # as listed with the public-domain source), and seed 0
+    x = splitmix64(1234567, 5)
+    assert [int(v) for v in x] == [6457827717110365317, 3203168211198807973,
+                                   9817491932198370423, 4593380528125082431,
+                                   16408922859458223821]
+    assert int(splitmix64(0, 1)[0]) == 0xE220A8397B1DCDAF
+
+
+def _model_tables(spec, lens, NB, MB):
+    """The same requests on the allocator's reference model (oracle side)."""
+    from oracle.alloc_model import BlockAllocatorModel
+    m = BlockAllocatorModel(NB, spec.block_size, spec.seed)
+    P = spec.shared_prefix
+    if P:
+        root = m.add(P)
+        seqs = []
+        for L in lens:
+            sq = m.fork(root)
+            assert m.append(sq, int(L) - P) == (-1, -1)   # block-aligned prefix: no copy
+            seqs.append(sq)
+        m.free_seq(root)
+    else:
+        seqs = [m.add(int(L)) for L in lens]
+    t = np.full((len(lens), MB), -1, np.int32)
+    for b, sq in enumerate(seqs):
+        blocks = m.table(sq)
+        t[b, :len(blocks)] = blocks
+    return t, m, seqs
+
+
+def _library_tables(spec, lens, NB, MB):
+    """The same requests on the library's C++ allocator (product side)."""
+    import paged_kv_cache_267_gb300 as pa
+    a = pa.BlockAllocator(NB, spec.block_size, seed=spec.seed)
+    P = spec.shared_prefix
+    if P:
+        root = a.add(P)
+        seqs = []
+        for L in lens:
+            sq = a.fork(root)
+            assert a.append(sq, int(L) - P) == (-1, -1)
+            seqs.append(sq)
+        a.free(root)
+    else:
+        seqs = [a.add(int(L)) for L in lens]
+    t = np.full((len(lens), MB), -1, np.int32)
+    for b, sq in enumerate(seqs):
+        blocks = a.table(sq)
+        t[b, :len(blocks)] = blocks
+    return t, a, seqs
+
+
+@pytest.mark.parametrize("name", list(CONFIGS))
+def test_named_layouts_are_the_allocators_tables(name):
+    """Every named workload's tables equal those of the allocator model and of
+    the library's allocator under the same requests (prefix configs: one
+    prefix request forked per sequence, then freed)."""
+    from workloads.gen import layout
+    s = CONFIGS[name]
+    lens, tables, NB, MB = layout(s)
+    model_t, m, seqs = _model_tables(s, lens, NB, MB)
+    assert np.array_equal(tables, model_t)
+    lib_t, a, lseqs = _library_tables(s, lens, NB, MB)
+    assert np.array_equal(tables, lib_t)
+    if s.shared_prefix:
+        # each prefix block referenced once per sequence, in both allocators
+        for blk in tables[0, :s.shared_prefix // s.block_size]:
+            assert m.refcount(int(blk)) == s.batch
+            assert a.refcount(int(blk)) == s.batch
+    used = tables[tables >= 0]
+    assert len(np.unique(used)) == len(used) or s.shared_prefix

@@ -2,9 +2,10 @@
 
 Recipe, in order:
   1. sequence lengths from numpy's PCG64 seeded with ``spec.seed``;
-  2. a pool of NB physical blocks and a seeded random permutation of their ids
-     used as the free list: the shared prefix (if any) takes the first blocks,
-     then each sequence its private ones, so physical ids are scattered;
+  2. a pool of NB physical blocks and the tables a block allocator gives
+     these requests (``layout.py``): a seeded shuffled free list; the shared
+     prefix (if any) allocated once and forked by every sequence, then each
+     sequence's private blocks, so physical ids are scattered;
   3. one K row and one V row of N(0, 1) values per unique token (shared prefix
      tokens are one row for all sequences), drawn by torch's generator seeded
      with ``spec.seed`` on the target device and rounded to the 16-bit dtype;
@@ -34,6 +35,7 @@ import numpy as np
 import torch
 
 from .configs import Spec
+from .layout import block_tables
 
 TORCH_DTYPES = {"f16": torch.float16, "bf16": torch.bfloat16}
 E4M3_NAN = 0x7F
@@ -98,16 +100,14 @@ def max_len_of(spec: Spec) -> int:
     return max([hi] + list(spec.long_seqs))
 
 
-def generate(spec: Spec, device="cpu", keep_hist: bool | None = None) -> Workload:
+def layout(spec: Spec) -> tuple[np.ndarray, np.ndarray, int, int]:
+    """Steps 1 and 2 of the recipe: (seq_lens int64 [B], block tables int32
+    [B, MB], pool blocks NB, table width MB), no values."""
     s = spec
-    dev = torch.device(device)
-    bs, Hkv, D = s.block_size, s.num_kv_heads, s.head_dim
-    assert s.num_q_heads % Hkv == 0
+    bs = s.block_size
     assert s.shared_prefix % bs == 0
     rng = np.random.default_rng(s.seed)
-
     lens = draw_seq_lens(s, rng)
-    B = s.batch
     P = s.shared_prefix
     assert (lens >= P).all() and (P == 0 or (lens > P).all())
     MB = -(-max_len_of(s) // bs)
@@ -117,19 +117,18 @@ def generate(spec: Spec, device="cpu", keep_hist: bool | None = None) -> Workloa
     need = shared_blocks + int((nblk - shared_blocks).clip(min=0).sum())
     NB = s.pool_blocks if s.pool_blocks is not None else int(math.ceil(s.pool_factor * need))
     assert NB >= need, "pool smaller than the layout needs"
+    # physical layout: the block allocator's tables for these requests
+    return lens, block_tables(lens, bs, P, NB, MB, s.seed), NB, MB
 
-    # physical layout: a seeded permutation of block ids is the free list
-    perm = rng.permutation(NB).astype(np.int64)
-    cursor = 0
-    shared_ids = perm[cursor:cursor + shared_blocks]
-    cursor += shared_blocks
-    tables = np.full((B, MB), -1, dtype=np.int32)
-    for b in range(B):
-        n_priv = int(nblk[b]) - shared_blocks if lens[b] > 0 else 0
-        if lens[b] > 0:
-            tables[b, :shared_blocks] = shared_ids
-        tables[b, shared_blocks:shared_blocks + n_priv] = perm[cursor:cursor + n_priv]
-        cursor += n_priv
+
+def generate(spec: Spec, device="cpu", keep_hist: bool | None = None) -> Workload:
+    s = spec
+    dev = torch.device(device)
+    bs, Hkv, D = s.block_size, s.num_kv_heads, s.head_dim
+    assert s.num_q_heads % Hkv == 0
+    lens, tables, NB, MB = layout(s)
+    B = s.batch
+    P = s.shared_prefix
 
     # range read per sequence: the union of its queries' ranges
     T = s.num_queries
