@@ -155,7 +155,7 @@ pa_status pa_reshape_and_cache(const pa_tensor* k, const pa_tensor* v,
  * so; ordinary kernels and copies are waited for in full.
  *
  * Workspace: the step writes per-segment partial results (running max, sum
- * and unnormalised output), a piece counter and a small control block to a
+ * and unnormalised output) and a piece counter to a
  * device workspace of pa_decode_workspace_size() bytes. It is the buffer
  * given to pa_set_workspace() for the current device, or else a buffer the
  * library allocates (and zeroes) once per (device, stream) outside stream
@@ -181,20 +181,20 @@ pa_status pa_decode(const pa_tensor* out, const pa_tensor* q, const pa_tensor* k
  * library; every GPU that loads the library holds that array until the
  * process exits. The call allocates and frees nothing (no cudaMalloc or
  * cudaFree, directly or through another library). The scratch a step needs
- * is about 2.1 MB of counters plus
+ * is 256 bytes plus
  *   4 * (G * head_dim + 2 * G rounded up to 4) * (2 * batch * num_kv_heads + 5 * W)
  * bytes of partial results, where W is the number of worker warps of the
  * decode kernel: 2 * (SM count) * 4, or * 8 for e4m3 caches with head_dim 128
  * (W = 1216 or 2432 on a 152-SM GB300). The per-warp term dominates small
  * batches: a batch of 64 with 8 KV heads, G = 4 and head_dim 128 needs about
- * 16.9 MB; a batch of 256 of that shape with an e4m3 cache needs about
- * 35.9 MB. A step beyond 32 MiB is rejected with PA_ERR_WORKSPACE and a
+ * 14.8 MB; a batch of 256 of that shape with an e4m3 cache needs about
+ * 33.8 MB. A step beyond 32 MiB is rejected with PA_ERR_WORKSPACE and a
  * message giving the bytes needed.
  *
  * The first call on a device looks up that device's address of the array
  * (cudaGetSymbolAddress, with that device current); make that first call
  * before any stream capture. All calls share the one array and find the last
- * call's contents in it; each call clears, on its stream, the counters that
+ * call's contents in it; each call clears, on its stream, the counter that
  * must start at zero. Calls that overlap on the GPU (on different streams, or
  * different host threads, of one device) race on the array and must not be
  * issued.

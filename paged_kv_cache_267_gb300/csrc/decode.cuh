@@ -60,13 +60,14 @@
 #include <cuda_fp16.h>
 
 #include "pa_internal.h"
+#include "plan.cuh"
 #include "ptx.cuh"
 
 namespace pa {
 
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // pipeline wait bound (2 s)
 constexpr uint64_t kDrainLimitNs = 200000000ull;   // bound while draining after an error
-constexpr int kErrBlockId = 1, kErrSeqLen = 2, kErrTimeout = 8;
+constexpr int kErrBlockId = PA_DEVERR_BLOCK_ID, kErrTimeout = PA_DEVERR_TIMEOUT;
 
 template <int CT, int D, int STAGES>
 struct Geometry {
@@ -87,11 +88,6 @@ struct Geometry {
 __device__ __forceinline__ uint32_t tile_off(int r, int c) {
   return (static_cast<uint32_t>(c >> 3) << 11) + (static_cast<uint32_t>(r) << 7) +
          (static_cast<uint32_t>((c & 7) ^ (r & 7)) << 4);
-}
-
-__device__ __forceinline__ int win_start(int L, int W) { return (W > 0 && L > W) ? L - W : 0; }
-__device__ __forceinline__ int tiles_of(int L, int W) {
-  return L > 0 ? (L + kTile - 1) / kTile - win_start(L, W) / kTile : 0;
 }
 
 struct Cursor {
@@ -181,7 +177,7 @@ __global__ void __launch_bounds__(WARPS * 32, 2)
   const int g = lane >> 2, t4 = lane & 3;
 
   // Programmatic launch: the work before griddep_wait() below (planning from
-  // seq_lens, the control block) overlaps the previous kernel of the stream.
+  // seq_lens) overlaps the previous kernel of the stream.
   // A kernel of this library that lets dependents start early (the write
   // path) does so only once its own predecessors have finished, and it
   // writes none of q, seq_lens, block_tables or this workspace, only the
@@ -195,90 +191,24 @@ __global__ void __launch_bounds__(WARPS * 32, 2)
     fence_mbar_init();
     fence_proxy_async();
   }
-  // sequence lengths, clamped to the block-table capacity
-  const int cap = a.MB * a.bs;
-  for (int b = tid; b < a.B; b += blockDim.x) {
-    int L = a.seq_lens[b];
-    if (L < 0 || L > cap) {
-      atomicOr(a.err, kErrSeqLen);
-      L = L < 0 ? 0 : cap;
-    }
-    s_len[b] = L;
-  }
-  __syncthreads();
-  // exclusive prefix of tiles per pair over the sequences (one warp)
-  if (warp == 0) {
-    int run = 0;
-    for (int b0 = 0; b0 < a.B; b0 += 32) {
-      const int b = b0 + lane;
-      int x = (b < a.B) ? tiles_of(s_len[b], a.span) : 0;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(FULL, x, o);
-        if (lane >= o) x += y;
-      }
-      if (b < a.B) s_pref[b + 1] = run + x;
-      run += __shfl_sync(FULL, x, 31);
-    }
-    if (lane == 0) s_pref[0] = 0;
-  }
-  __syncthreads();
-
-  // Static ranges for about (1 - pool share) of the tiles, then the pool at
-  // the end of the flat space. Small pool pieces inside a sequence far longer
-  // than the mean would cut it into thousands of partials, so the pool only
-  // covers the trailing run of sequences at most four times the mean length.
-  __shared__ int s_last_long;
-  if (warp == 0) {
-    const long long thr = 4ll * s_pref[a.B];  // nt_b * B > thr  <=>  nt_b > 4 * mean
-    int last = -1;
-    for (int b = lane; b < a.B; b += 32)
-      if (static_cast<long long>(s_pref[b + 1] - s_pref[b]) * a.B > thr) last = b;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) last = max(last, __shfl_xor_sync(FULL, last, o));
-    if (lane == 0) s_last_long = last;
-  }
-  __syncthreads();
-  const int total = a.Hv * s_pref[a.B];
-  const int nw = gridDim.x * WARPS;
-  const long long short_tail = total - static_cast<long long>(a.Hv) * s_pref[s_last_long + 1];
-  long long pool_want = static_cast<long long>(total) * a.pool_permille / 1000;
-  if (pool_want > short_tail) pool_want = short_tail;
-  // rounded up, so that the static ranges never reach into the pool's share
-  int ws = static_cast<int>((total - pool_want + nw - 1) / nw);
-  if (ws < a.min_tiles) ws = a.min_tiles;
-  const int ts = static_cast<int>(min(static_cast<long long>(ws) * nw, static_cast<long long>(total)));
+  // sequence lengths clamped to the block-table capacity, tile prefix and
+  // split (the merge kernel derives the same plan from the same inputs)
+  PlanIn pin;
+  pin.seq_lens = a.seq_lens;
+  pin.err = a.err;
+  pin.B = a.B;
+  pin.cap = a.MB * a.bs;
+  pin.span = a.span;
+  pin.Hv = a.Hv;
+  pin.nw = gridDim.x * WARPS;
+  pin.pool_permille = a.pool_permille;
+  pin.min_tiles = a.min_tiles;
+  pin.np_max = a.np_max;
+  pin.piece_min = a.piece_min;
+  const StepPlan pl = plan_step(pin, s_len, s_pref);
+  const int total = pl.total, ws = pl.ws, ts = pl.ts, piece = pl.piece;
+  const int nw = pin.nw;
   const int pool_tiles = total - ts;
-  int piece = (pool_tiles + a.np_max - 1) / a.np_max;
-  if (piece < a.piece_min) piece = a.piece_min;
-  if (blockIdx.x == 0) {
-    if (tid == 0) {
-      a.ctrl[0] = ws;
-      a.ctrl[1] = total;
-      a.ctrl[2] = ts;
-      a.ctrl[3] = piece;
-    }
-    for (int b = tid; b <= a.B; b += blockDim.x) a.ctrl[4 + b] = s_pref[b];
-    // prefix of the merge kernel's extra group units per sequence
-    if (warp == 0) {
-      int run = 0;
-      for (int b0 = 0; b0 < a.B; b0 += 32) {
-        const int b = b0 + lane;
-        int x = 0;
-        if (b < a.B)
-          x = merge_extra_units(s_pref[b + 1] - s_pref[b], a.Hv * s_pref[b],
-                                a.Hv * s_pref[b + 1], ws, ts, piece, a.Hv * a.CG);
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const int y = __shfl_up_sync(FULL, x, o);
-          if (lane >= o) x += y;
-        }
-        if (b < a.B) a.ctrl[6 + a.B + b] = run + x;
-        run += __shfl_sync(FULL, x, 31);
-      }
-      if (lane == 0) a.ctrl[5 + a.B] = 0;
-    }
-  }
   const int w = blockIdx.x * WARPS + warp;
   const int f0 = static_cast<int>(min(static_cast<long long>(w) * ws, static_cast<long long>(ts)));
   const int f1 = min(f0 + ws, ts);

@@ -4,6 +4,7 @@
 #include <cuda_fp16.h>
 
 #include "pa_internal.h"
+#include "plan.cuh"
 #include "ptx.cuh"
 
 namespace pa {
@@ -18,29 +19,29 @@ cudaError_t device_error_word(int32_t** ptr) {
 
 // ------------------------------------------------------------------ merge
 //
-// Partials of pair s (tiles [F, F + nt) of the flat space) are its candidates:
-// the static slots s + w of the warps w whose static range meets
-// [F, min(F + nt, Ts)), then the pool slots S + NW + s + i of the pieces i
-// that meet [max(F, Ts), F + nt). With partial maxima m_p (log2 domain), sums
-// l_p and unnormalised outputs o_p the result for an output column is
+// The partial results of a pair (its candidates, see pair_cands) have maxima
+// m_p (log2 domain), sums l_p and unnormalised outputs o_p; for an output
+// column the result is
 //   out = sum_p 2^(m_p - M) o_p / sum_p 2^(m_p - M) l_p,  M = max_p m_p,
 // and zero when the denominator is zero (a chunked query placed before the
 // start of its sequence attends to nothing). A column is a q head of the pair
 // (single-query decode) or a (query, q head) of a chunk; columns that pad the
 // last group of a chunk have no output row and are skipped.
-// Work units are (group g of candidates, column of pair s), one warp each,
-// spread over a persistent grid of many warps per SM so that the L2 latency
-// of one unit hides behind the others. A unit folds its candidates in online
-// (eight loads in flight per lane; groups of max(8, ceil(n / 8)) of a head's
-// n candidates, so at most eight groups). A head whose candidates fit one group is
-// written out directly; otherwise each unit stores its group result, which
-// has the same form as a partial, in place in the slot of the group's first
-// candidate, and the unit that completes the head's counter combines the
-// group results and resets the counter. Pairs without tiles get zeros.
+//
+// The kernel derives the decode kernel's plan from seq_lens before it waits
+// for the decode kernel (it is launched as its programmatic dependent), so
+// after the decode ends each column costs one round trip for its partials.
+// Columns of sequences where some pair has more than eight candidates (pairs
+// cut into pool pieces, or spanning many warps' static ranges) are "wide":
+// each goes to one whole CTA, whose eight warps fold one eighth of the
+// candidates each and combine their results through shared memory. Every
+// other column is one warp's work. A warp folds its candidates online with
+// eight loads in flight per lane (D <= 128; four for D = 256).
 constexpr int kMergeThreads = 256;
 constexpr int kMergeWarps = kMergeThreads / 32;
+constexpr int kMergeNarrow = 8;  // candidates one warp folds in one round trip
 
-// Per-lane state of one q head: head dims v * 128 + 4 * lane .. + 3 for
+// Per-lane state of one column: head dims v * 128 + 4 * lane .. + 3 for
 // v < VPL (VPL = 1 for D <= 128, 2 for D = 256).
 template <int VPL>
 struct HeadAcc {
@@ -48,13 +49,12 @@ struct HeadAcc {
   float4 acc[VPL];
 };
 
-// Folds candidates k0, k0 + step, ... (< k1) of head h into `r`, with
-// U = 8 / VPL candidates' loads in flight per lane (a group of 8 partials is
-// one round trip for D <= 128). Lane j < U reads candidate j's max and sum,
-// which the fold takes by shuffle.
+// Folds candidates k0 .. k1 - 1 of column h into `r` (which starts empty),
+// U = 8 / VPL candidates' loads in flight per lane. Lane j < U reads
+// candidate j's max and sum, which the fold takes by shuffle.
 template <int VPL, typename SlotFn>
 __device__ __forceinline__ void merge_fold(const MergeArgs& a, SlotFn slot_of, int k0, int k1,
-                                           int step, int h, HeadAcc<VPL>& r) {
+                                           int h, HeadAcc<VPL>& r) {
   constexpr int U = 8 / VPL;
   const int lane = threadIdx.x & 31;
   const int GD = a.CG * a.D;
@@ -64,17 +64,17 @@ __device__ __forceinline__ void merge_fold(const MergeArgs& a, SlotFn slot_of, i
 #pragma unroll
   for (int v = 0; v < VPL; ++v) r.acc[v] = make_float4(0.f, 0.f, 0.f, 0.f);
   const bool on = 4 * lane < a.D;  // D = 64 uses half the lanes
-  for (int k = k0; k < k1; k += U * step) {
+  for (int k = k0; k < k1; k += U) {
     float my_m = -INFINITY, my_l = 0.f;
-    if (lane < U && k + lane * step < k1) {
-      const float* P = a.part + static_cast<size_t>(slot_of(k + lane * step)) * stride;
+    if (lane < U && k + lane < k1) {
+      const float* P = a.part + static_cast<size_t>(slot_of(k + lane)) * stride;
       my_m = P[GD + h];
       my_l = P[GD + a.CG + h];
     }
     float4 o[U][VPL];
 #pragma unroll
     for (int j = 0; j < U; ++j) {
-      const int kk = k + j * step;
+      const int kk = k + j;
 #pragma unroll
       for (int v = 0; v < VPL; ++v) o[j][v] = make_float4(0.f, 0.f, 0.f, 0.f);
       if (kk < k1 && on) {
@@ -87,7 +87,7 @@ __device__ __forceinline__ void merge_fold(const MergeArgs& a, SlotFn slot_of, i
 #pragma unroll
     for (int j = 0; j < U; ++j) {
       const float mj = __shfl_sync(0xffffffffu, my_m, j), lj = __shfl_sync(0xffffffffu, my_l, j);
-      if (k + j * step >= k1) break;
+      if (k + j >= k1) break;
       const float Mn = fmaxf(r.M, mj);
       const float sc = fast_exp2(r.M - Mn), f = fast_exp2(mj - Mn);
       r.den = r.den * sc + f * lj;
@@ -130,133 +130,162 @@ __device__ __forceinline__ void store_head(const MergeArgs& a, size_t orow, cons
     store_out4<OT>(a.out, orow + v * 128 + 4 * lane, zero ? z : r.acc[v], inv);
 }
 
-// Candidate range of pair (b, kvh): static warps [w0, w0 + na), pool pieces
-// [i0, i0 + np).
-struct Cands {
-  int w0, na, i0, np;
+// Where output column `col` of sequence b lives, and its candidates.
+struct MergeCol {
+  bool pad;     // a column padding the last group of a chunk
+  int h;        // column within its pair
+  size_t orow;  // first element of its output row
+  int s;        // pair index
+  Cands cd;
+  int ncand;
 };
 
-__device__ __forceinline__ Cands pair_cands(int F, int nt, int ws, int ts, int piece) {
-  Cands c = {0, 0, 0, 0};
-  if (nt > 0 && F < ts) {
-    c.w0 = F / ws;
-    c.na = (min(F + nt, ts) - 1) / ws - c.w0 + 1;
-  }
-  if (nt > 0 && F + nt > ts) {
-    c.i0 = (max(F, ts) - ts) / piece;
-    c.np = (F + nt - 1 - ts) / piece - c.i0 + 1;
-  }
+__device__ __forceinline__ MergeCol merge_col(const MergeArgs& a, const StepPlan& pl,
+                                              const int* s_pref, int b, int col) {
+  MergeCol c;
+  const int vh = col / a.CG;
+  c.h = col - vh * a.CG;  // pair and column within it
+  const int kvh = vh / a.NCG;
+  const int gc = (vh - kvh * a.NCG) * a.CG + c.h;  // column among the kv head's T * G
+  c.pad = gc >= a.T * a.G;
+  const int tq = gc / a.G;
+  c.s = b * a.Hv + vh;
+  const int nt = s_pref[b + 1] - s_pref[b];
+  const int F = a.Hv * s_pref[b] + vh * nt;
+  c.cd = pair_cands(F, nt, pl);
+  c.ncand = c.cd.na + c.cd.np;
+  c.orow = ((static_cast<size_t>(b) * a.T + tq) * a.Hq + kvh * a.G + (gc - tq * a.G)) * a.D;
   return c;
 }
 
-// Units: first group 0 of every column (B * Hv * CG of them), then groups 1..
-// of the columns of sequences whose candidate bound needs more than one group; the
-// latter are enumerated through a prefix over sequences (written by the
-// decode kernel), and a unit whose group turns out empty is skipped.
 template <int OT, int VPL>
 __global__ void __launch_bounds__(kMergeThreads, 3) merge_kernel(const MergeArgs a) {
-  extern __shared__ int s_dyn[];
-  int* s_pref = s_dyn;             // B + 1 tile prefix
-  int* s_extra = s_dyn + a.B + 1;  // B + 1 prefix of extra units per sequence
-  griddep_wait();
-  const int tid = threadIdx.x, lane = tid & 31;
-  if (blockIdx.x == 0 && tid == 0) *a.pool = 0u;
-  const int ws = a.ctrl[0], ts = a.ctrl[2], piece = a.ctrl[3];
-  for (int i = tid; i <= a.B; i += blockDim.x) {
-    s_pref[i] = a.ctrl[4 + i];
-    s_extra[i] = a.ctrl[5 + a.B + i];
+  constexpr unsigned FULL = 0xffffffffu;
+  constexpr int ROW = VPL * 128 + 4;  // floats per group result in shared memory
+  extern __shared__ __align__(16) float s_dyn[];
+  float* s_grp = s_dyn;                                          // [8][ROW]
+  int* s_pref = reinterpret_cast<int*>(s_dyn + kMergeWarps * ROW);  // B + 1
+  int* s_wide = s_pref + a.B + 1;                                // B + 1 prefix of wide columns
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  // ---- the decode kernel's plan, before waiting for it
+  PlanIn pin;
+  pin.seq_lens = a.seq_lens;
+  pin.err = nullptr;  // the decode kernel reports bad lengths
+  pin.B = a.B;
+  pin.cap = a.cap;
+  pin.span = a.span;
+  pin.Hv = a.Hv;
+  pin.nw = a.NW;
+  pin.pool_permille = a.pool_permille;
+  pin.min_tiles = a.min_tiles;
+  pin.np_max = a.np_max;
+  pin.piece_min = a.piece_min;
+  const StepPlan pl = plan_step(pin, nullptr, s_pref);
+  const int HC = a.Hv * a.CG;  // columns per sequence
+  // wide sequences: some pair has more than kMergeNarrow candidates
+  if (warp == 0) {
+    int run = 0;
+    for (int b0 = 0; b0 < a.B; b0 += 32) {
+      const int b = b0 + lane;
+      int x = 0;
+      if (b < a.B) {
+        const int nt = s_pref[b + 1] - s_pref[b];
+        for (int vh = 0; vh < a.Hv && x == 0; ++vh) {
+          const Cands cd = pair_cands(a.Hv * s_pref[b] + vh * nt, nt, pl);
+          if (cd.na + cd.np > kMergeNarrow) x = HC;
+        }
+      }
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(FULL, x, o);
+        if (lane >= o) x += y;
+      }
+      if (b < a.B) s_wide[b + 1] = run + x;
+      run += __shfl_sync(FULL, x, 31);
+    }
+    if (lane == 0) s_wide[0] = 0;
   }
   __syncthreads();
-  const int S = a.B * a.Hv, GD = a.CG * a.D;
-  const int HC = a.Hv * a.CG;  // columns per sequence
-  const int heads = a.B * HC;
-  const int units = heads + s_extra[a.B];
-  const int nwarps = gridDim.x * kMergeWarps;
-  for (int u = blockIdx.x * kMergeWarps + (tid >> 5); u < units; u += nwarps) {
-    int b, col, g;
-    if (u < heads) {
-      b = u / HC;
-      col = u - b * HC;
-      g = 0;
-    } else {
-      const int e = u - heads;
-      int lo = 0, hi = a.B;  // largest b with s_extra[b] <= e
-      while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (s_extra[mid] <= e) lo = mid; else hi = mid;
-      }
-      b = lo;
-      const int rem = e - s_extra[b];
-      g = 1 + rem / HC;
-      col = rem - (g - 1) * HC;
+
+  griddep_wait();  // the decode kernel's partials are complete and visible
+  if (blockIdx.x == 0 && tid == 0) *a.pool = 0u;
+  const int S = a.B * a.Hv;
+
+  // ---- wide columns: one CTA each
+  const int n_wide = s_wide[a.B];
+  for (int cu = blockIdx.x; cu < n_wide; cu += gridDim.x) {
+    int lo = 0, hi = a.B;  // largest b with s_wide[b] <= cu
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (s_wide[mid] <= cu) lo = mid; else hi = mid;
     }
-    const int vh = col / a.CG, h = col - vh * a.CG;  // pair and column within it
-    const int kvh = vh / a.NCG;
-    const int gc = (vh - kvh * a.NCG) * a.CG + h;    // column among the kv head's T * G
-    if (gc >= a.T * a.G) continue;                    // padding column
-    const int tq = gc / a.G;
-    const int s = b * a.Hv + vh;
-    const int hr = b * HC + col;
-    const int nt = s_pref[b + 1] - s_pref[b];
-    const int F = a.Hv * s_pref[b] + vh * nt;
-    const Cands cd = pair_cands(F, nt, ws, ts, piece);
-    const int ncand = cd.na + cd.np;
-    const int gsz = merge_group_size(ncand);
-    const int ngroups = ncand > 0 ? (ncand + gsz - 1) / gsz : 1;
-    if (g >= ngroups) continue;
-    const size_t orow =
-        ((static_cast<size_t>(b) * a.T + tq) * a.Hq + kvh * a.G + (gc - tq * a.G)) * a.D;
-    HeadAcc<VPL> r;
-    r.M = -INFINITY;
-    r.den = 1.f;
-#pragma unroll
-    for (int v = 0; v < VPL; ++v) r.acc[v] = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (ncand == 0) {
-      store_head<OT, VPL>(a, orow, r, true);
-      continue;
-    }
-    auto slot_of = [&](int k) -> int {
-      return k < cd.na ? s + cd.w0 + k : S + a.NW + s + cd.i0 + (k - cd.na);
+    const MergeCol c = merge_col(a, pl, s_pref, lo, cu - s_wide[lo]);
+    if (c.pad) continue;  // uniform over the CTA
+    auto slot = [&](int k) -> int {
+      return k < c.cd.na ? c.s + c.cd.w0 + k : S + a.NW + c.s + c.cd.i0 + (k - c.cd.na);
     };
-    const int k0 = g * gsz, k1 = min(k0 + gsz, ncand);
-    merge_fold(a, slot_of, k0, k1, 1, h, r);
-    if (ngroups == 1) {
-      store_head<OT, VPL>(a, orow, r, false);
-      continue;
-    }
-    // group result, in place in the slot of the group's first candidate
-    {
-      float* P = a.part + static_cast<size_t>(slot_of(k0)) * part_stride(a.CG, a.D);
+    const int gsz = c.ncand > 0 ? (c.ncand + kMergeWarps - 1) / kMergeWarps : 1;
+    const int ngrp = c.ncand > 0 ? (c.ncand + gsz - 1) / gsz : 0;
+    if (warp < ngrp) {
+      HeadAcc<VPL> r;
+      merge_fold(a, slot, warp * gsz, min((warp + 1) * gsz, c.ncand), c.h, r);
+      float* g = s_grp + warp * ROW;
       if (4 * lane < a.D) {
 #pragma unroll
         for (int v = 0; v < VPL; ++v)
-          *reinterpret_cast<float4*>(P + h * a.D + v * 128 + 4 * lane) = r.acc[v];
+          *reinterpret_cast<float4*>(g + v * 128 + 4 * lane) = r.acc[v];
       }
       if (lane == 0) {
-        P[GD + h] = r.M;
-        P[GD + a.CG + h] = r.den;
+        g[VPL * 128] = r.M;
+        g[VPL * 128 + 1] = r.den;
       }
     }
-    // the warp's stores, then lane 0's release increment; the unit that
-    // completes the count reads the group results after its acquire (the
-    // warp barriers order the other lanes' stores and loads around lane 0's)
-    __syncwarp();
-    int last = 0;
-    if (lane == 0) {
-      uint32_t prev;
-      asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;"
-                   : "=r"(prev)
-                   : "l"(a.counters + hr)
-                   : "memory");
-      last = (prev + 1 == static_cast<uint32_t>(ngroups));
-      if (last) a.counters[hr] = 0u;
+    __syncthreads();
+    if (warp == 0) {
+      HeadAcc<VPL> r;
+      r.M = -INFINITY;
+      r.den = 0.f;
+#pragma unroll
+      for (int v = 0; v < VPL; ++v) r.acc[v] = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int j = 0; j < ngrp; ++j) {
+        const float* g = s_grp + j * ROW;
+        const float mj = g[VPL * 128], dj = g[VPL * 128 + 1];
+        const float Mn = fmaxf(r.M, mj);
+        const float sc = fast_exp2(r.M - Mn), f = fast_exp2(mj - Mn);
+        r.den = r.den * sc + f * dj;
+        if (4 * lane < a.D) {
+#pragma unroll
+          for (int v = 0; v < VPL; ++v) {
+            const float4 o = *reinterpret_cast<const float4*>(g + v * 128 + 4 * lane);
+            r.acc[v].x = r.acc[v].x * sc + f * o.x;
+            r.acc[v].y = r.acc[v].y * sc + f * o.y;
+            r.acc[v].z = r.acc[v].z * sc + f * o.z;
+            r.acc[v].w = r.acc[v].w * sc + f * o.w;
+          }
+        }
+        r.M = Mn;
+      }
+      store_head<OT, VPL>(a, c.orow, r, ngrp == 0);
     }
-    last = __shfl_sync(0xffffffffu, last, 0);
-    if (!last) continue;
-    __syncwarp();
-    // combine the group results (the first candidate of each group)
-    merge_fold(a, slot_of, 0, ngroups * gsz, gsz, h, r);
-    store_head<OT, VPL>(a, orow, r, false);
+    __syncthreads();  // s_grp is reused by the next wide column
+  }
+
+  // ---- narrow columns: one warp each. The CTAs that took a wide column in
+  // the last round come last in the order.
+  const int rot = (blockIdx.x + gridDim.x - (n_wide % gridDim.x)) % gridDim.x;
+  const int nwarps = gridDim.x * kMergeWarps;
+  for (int u = rot * kMergeWarps + warp; u < a.B * HC; u += nwarps) {
+    const int b = u / HC;
+    if (s_wide[b + 1] != s_wide[b]) continue;  // taken by the wide phase
+    const MergeCol c = merge_col(a, pl, s_pref, b, u - b * HC);
+    if (c.pad) continue;
+    auto slot = [&](int k) -> int {
+      return k < c.cd.na ? c.s + c.cd.w0 + k : S + a.NW + c.s + c.cd.i0 + (k - c.cd.na);
+    };
+    HeadAcc<VPL> r;
+    merge_fold(a, slot, 0, c.ncand, c.h, r);
+    store_head<OT, VPL>(a, c.orow, r, c.ncand == 0);
   }
 }
 
@@ -264,7 +293,9 @@ cudaError_t merge_launch(int out_type, const MergeArgs& a, int grid, cudaStream_
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kMergeThreads);
-  cfg.dynamicSmemBytes = static_cast<size_t>(2 * (a.B + 1)) * sizeof(int);
+  const int row = (a.D > 128 ? 2 : 1) * 128 + 4;
+  cfg.dynamicSmemBytes = static_cast<size_t>(kMergeWarps) * row * sizeof(float) +
+                         static_cast<size_t>(2 * (a.B + 1)) * sizeof(int);
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

@@ -210,7 +210,7 @@ size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // Section offsets of the decode workspace (layout described in pa_internal.h).
 struct WsLayout {
-  size_t pool, counters, ctrl, part, total;
+  size_t pool, part, total;
 };
 
 // Hv pairs per sequence with CG columns each (Hkv and G for single-query decode).
@@ -221,9 +221,7 @@ WsLayout ws_layout(int64_t B, int Hv, int CG, int D, int64_t workers) {
   size_t o = 0;
   // The pool counter sits at a fixed offset: it must stay zero between calls
   // whatever their shapes, and each step's merge only resets its own copy.
-  L.pool = o;      o += 256;
-  L.counters = o;  o += static_cast<size_t>(pa::kMaxMergeCounters) * sizeof(uint32_t);
-  L.ctrl = o;  o += round_up(static_cast<size_t>(2 * B + 6) * sizeof(int32_t), 256);
+  L.pool = o;  o += 256;
   L.part = o;  o += nslot * static_cast<size_t>(pa::part_stride(CG, D)) * sizeof(float);
   L.total = o;
   return L;
@@ -401,7 +399,7 @@ pa_status get_workspace(DeviceState* st, cudaStream_t stream, const WsLayout& la
   }
   if (w->dirty) {
     cudaError_t e = cudaMemsetAsync(static_cast<char*>(w->ptr) + lay.pool, 0,
-                                    lay.ctrl - lay.pool, stream);
+                                    lay.part - lay.pool, stream);
     if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(pool counter)");
     w->dirty = false;
   }
@@ -485,7 +483,7 @@ pa_status workspace_size(int64_t batch, int64_t num_queries, int32_t num_q_heads
   int CG, NCG;
   chunk_columns(num_queries, num_q_heads / num_kv_heads, &CG, &NCG);
   const int64_t Hv = static_cast<int64_t>(num_kv_heads) * NCG;
-  if (dprod({double(batch), double(Hv), double(CG)}) > pa::kMaxMergeCounters)
+  if (dprod({double(batch), double(Hv), double(CG)}) > pa::kMaxColumns)
     return fail(PA_ERR_UNSUPPORTED, "batch * num_q_heads * num_queries too large");
   std::lock_guard<std::mutex> lk(g_mu);
   DeviceState* st;
@@ -707,7 +705,7 @@ pa_status check_decode(const pa_tensor* out, const pa_tensor* q, const pa_tensor
     return fail(PA_ERR_UNSUPPORTED, "pool or tables exceed 32-bit indexing");
   for (const pa_tensor* x : {q, key_cache, value_cache, block_tables, seq_lens})
     if (overlaps(out, x)) return fail(PA_ERR_INVALID_ARG, "out overlaps an input");
-  if (dprod({dB, dHv, double(CG)}) > pa::kMaxMergeCounters)
+  if (dprod({dB, dHv, double(CG)}) > pa::kMaxColumns)
     return fail(PA_ERR_UNSUPPORTED, "batch * num_q_heads * num_queries too large");
   if (B > 0 && MB == 0) return fail(PA_ERR_INVALID_ARG, "block_tables has no columns");
   if (B > 0 && NB == 0) return fail(PA_ERR_INVALID_ARG, "empty block pool");
@@ -751,7 +749,6 @@ pa_status run_decode(const DecodeCall& c, DeviceState* st, const DecodePlan& pla
   a.block_tables = static_cast<const int32_t*>(c.bt->data);
   a.seq_lens = static_cast<const int32_t*>(c.sl->data);
   char* wsb = static_cast<char*>(ws);
-  a.ctrl = reinterpret_cast<int32_t*>(wsb + layout.ctrl);
   a.pool = reinterpret_cast<uint32_t*>(wsb + layout.pool);
   a.part = reinterpret_cast<float*>(wsb + layout.part);
   a.err = st->err_word;
@@ -791,9 +788,8 @@ pa_status run_decode(const DecodeCall& c, DeviceState* st, const DecodePlan& pla
   pa::MergeArgs m;
   m.out = c.out->data;
   m.part = a.part;
-  m.ctrl = a.ctrl;
+  m.seq_lens = a.seq_lens;
   m.pool = a.pool;
-  m.counters = reinterpret_cast<uint32_t*>(wsb + layout.counters);
   m.NW = plan.workers;
   m.B = a.B;
   m.Hq = a.Hq;
@@ -804,6 +800,12 @@ pa_status run_decode(const DecodeCall& c, DeviceState* st, const DecodePlan& pla
   m.NCG = a.NCG;
   m.CG = a.CG;
   m.Hv = a.Hv;
+  m.cap = a.MB * a.bs;
+  m.span = a.span;
+  m.min_tiles = a.min_tiles;
+  m.pool_permille = a.pool_permille;
+  m.piece_min = a.piece_min;
+  m.np_max = a.np_max;
   e = pa::merge_launch(c.qt, m, st->num_sms * 3, cs, !prof);
   if (e != cudaSuccess) {
     if (wsp) {
@@ -958,13 +960,11 @@ pa_status decode_in_buffer(const pa_tensor* out, const pa_tensor* q, const pa_te
                 "this step needs %zu bytes of scratch; the built-in buffer holds %zu (use "
                 "pa_decode with its own workspace for larger batches or head counts)",
                 layout.total, capacity);
-  // The piece counter and this step's merge counters must start at zero; the
-  // buffer keeps whatever the previous call left there.
+  // The piece counter must start at zero; the buffer keeps whatever the
+  // previous call left there.
   cudaError_t e = cudaMemsetAsync(static_cast<char*>(buffer) + layout.pool, 0,
-                                  layout.counters - layout.pool +
-                                      static_cast<size_t>(c.B * c.Hv * c.CG) * sizeof(uint32_t),
-                                  cs);
-  if (e != cudaSuccess) return cuda_fail(e, "clearing the scratch counters");
+                                  layout.part - layout.pool, cs);
+  if (e != cudaSuccess) return cuda_fail(e, "clearing the scratch counter");
   return run_decode(c, st, plan, layout, buffer, nullptr, cs);
 }
 }  // namespace pa

@@ -22,26 +22,21 @@ __host__ __device__ constexpr inline int part_stride(int G, int D) {
 // Decode workspace layout (device memory, all sections 256-byte aligned):
 //   pool  u32 at offset 0: pool piece counter; zero between calls (the merge
 //         kernel resets it after each step), at the same place for any shape
-//   cnt   u32 [kMaxMergeCounters] at offset 256: merge group counters (one
-//         per output column), zero between calls (each is reset by the unit
-//         that finds it complete)
-//   ctrl  int32 [2 B + 6]: [0] static tiles per warp (ws), [1] total tiles,
-//         [2] end of the static region (Ts), [3] pool piece size (P),
-//         [4 .. 4 + B] tile prefix over the sequences, [5 + B .. 5 + 2 B]
-//         prefix of the merge's extra group units over the sequences
-//   part  f32 [NSLOT][part_stride(CG, D)]: acc[CG][D], m[CG], l[CG], padding
-//         to a multiple of 4 floats so every slot starts 16-byte aligned
+//   part  f32 [NSLOT][part_stride(CG, D)] at offset 256: acc[CG][D], m[CG],
+//         l[CG], padding to a multiple of 4 floats so every slot starts
+//         16-byte aligned
 // with S = B * Hv pairs, NW worker warps, NSLOT = 2 S + NW + NPMAX. For
 // single-query decode Hv = Hkv and CG = G (columns are the group's q heads).
 // A segment is a run of one warp's tiles inside one pair. Static segments of
 // pair s by warp w use slot s + w; segments of pool piece i use slot
 // S + NW + s + i. Both are unique because the walk through the (pair, warp)
-// and (pair, piece) grids is a monotone staircase.
+// and (pair, piece) grids is a monotone staircase. The step's plan (how tiles
+// are split) is not stored: the decode and merge kernels derive it from
+// seq_lens with the same code (plan.cuh).
 struct DecodeArgs {
   const void* q;                 // [B, T, Hq, D] ([B, Hq, D] when T = 1)
   const int32_t* block_tables;   // [B, MB]
   const int32_t* seq_lens;       // [B]
-  int32_t* ctrl;
   uint32_t* pool;
   float* part;
   int32_t* err;                  // device error word
@@ -61,37 +56,17 @@ struct DecodeArgs {
 
 struct MergeArgs {
   void* out;                     // [B, T, Hq, D], dtype of q
-  float* part;                   // group results are written in place
-  const int32_t* ctrl;
+  const float* part;
+  const int32_t* seq_lens;       // [B], to derive the decode kernel's plan
   uint32_t* pool;                // reset to zero for the next step
-  uint32_t* counters;            // [B * Hv * CG] groups done per column; left at zero
   int B, Hq, Hkv, G, D, NW;
   int T, NCG, CG, Hv;            // as in DecodeArgs
+  int cap, span;                 // plan inputs, as given to the decode kernel
+  int min_tiles, pool_permille, piece_min, np_max;
 };
 
-constexpr int kMergeGroupsMax = 8;    // groups of partials per q head, at most
-constexpr int kMergeGroupMin = 8;     // partials per group, at least (one round trip of the fold)
-constexpr int kMaxMergeCounters = 1 << 19;
-
-// Partials per merge group for a head with n candidate partials.
-__host__ __device__ inline int merge_group_size(int n) {
-  const int g = (n + kMergeGroupsMax - 1) / kMergeGroupsMax;
-  return g < kMergeGroupMin ? kMergeGroupMin : g;
-}
-
-// Merge units beyond group 0 for the `cols` output columns of one sequence
-// whose pairs span flat tiles [lo, hi), nt tiles each: from an upper bound of
-// a pair's candidates (static warps met, plus pool pieces met inside [ts, hi)).
-__host__ __device__ inline int merge_extra_units(int nt, int lo, int hi, int ws, int ts,
-                                                 int piece, int cols) {
-  if (nt <= 0) return 0;
-  const int start = lo > ts ? lo : ts;
-  const int in_pool = hi > start ? hi - start : 0;
-  const int pool_part = in_pool > 0 ? (nt < in_pool ? nt : in_pool) / piece + 2 : 0;
-  const int ub = nt / ws + 2 + pool_part;
-  const int gsz = merge_group_size(ub);
-  return ((ub + gsz - 1) / gsz - 1) * cols;
-}
+// Bound on output columns (batch * q heads * queries) of one call.
+constexpr int kMaxColumns = 1 << 19;
 
 struct ReshapeArgs {
   const void* k;

@@ -1,0 +1,140 @@
+// The work plan of one decode step, computed from seq_lens alone.
+//
+// The decode kernel and the merge kernel both derive it, each in its own
+// blocks, from the same inputs with the same code, so they agree without
+// passing it through memory: the merge kernel plans while the decode kernel
+// still streams, and after the decode finishes it needs no load of a plan
+// before it reads the partial results.
+//
+// Every (sequence b, virtual KV head) pair owns the 16-token tiles covering
+// its read range [start, L); all tiles form one flat, pair-major index space.
+// Its first part is split into equal static ranges of `ws` tiles, one per
+// worker warp (ending at `ts`); the rest is a pool of pieces of `piece` tiles
+// claimed dynamically. The pool only covers the trailing run of sequences
+// whose tile count is at most four times the mean, so a long sequence is never
+// cut into many small pieces.
+#pragma once
+
+#include "pa_internal.h"
+
+namespace pa {
+
+__device__ __forceinline__ int win_start(int L, int W) { return (W > 0 && L > W) ? L - W : 0; }
+__device__ __forceinline__ int tiles_of(int L, int W) {
+  return L > 0 ? (L + kTile - 1) / kTile - win_start(L, W) / kTile : 0;
+}
+
+struct PlanIn {
+  const int32_t* seq_lens;  // [B]
+  int32_t* err;             // device error word (null: do not report)
+  int B;
+  int cap;                  // longest sequence the tables can hold: MB * bs
+  int span;                 // window of the pairs' tile ranges (0: none)
+  int Hv;                   // pairs per sequence
+  int nw;                   // worker warps of the decode kernel
+  int pool_permille, min_tiles, np_max, piece_min;
+};
+
+struct StepPlan {
+  int total;  // tiles of all pairs
+  int ws;     // static tiles per warp
+  int ts;     // end of the static region
+  int piece;  // tiles per pool piece
+};
+
+// Block-wide: every thread of the block calls it (it synchronises the
+// block). Fills s_pref[0 .. B] with the exclusive prefix of tiles per pair
+// over the sequences and, when s_len is given, s_len[0 .. B) with the lengths
+// clamped to [0, cap] (a length outside is reported through `err`).
+__device__ inline StepPlan plan_step(const PlanIn& p, int* s_len, int* s_pref) {
+  constexpr unsigned FULL = 0xffffffffu;
+  __shared__ int s_last_long;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (s_len != nullptr) {
+    for (int b = tid; b < p.B; b += blockDim.x) {
+      int L = p.seq_lens[b];
+      if (L < 0 || L > p.cap) {
+        if (p.err) atomicOr(p.err, PA_DEVERR_SEQ_LEN);
+        L = L < 0 ? 0 : p.cap;
+      }
+      s_len[b] = L;
+    }
+    __syncthreads();
+  }
+  // exclusive prefix of tiles per pair over the sequences (one warp)
+  if (warp == 0) {
+    int run = 0;
+    for (int b0 = 0; b0 < p.B; b0 += 32) {
+      const int b = b0 + lane;
+      int x = 0;
+      if (b < p.B) {
+        int L;
+        if (s_len != nullptr) {
+          L = s_len[b];
+        } else {
+          L = p.seq_lens[b];
+          L = L < 0 ? 0 : (L > p.cap ? p.cap : L);
+        }
+        x = tiles_of(L, p.span);
+      }
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(FULL, x, o);
+        if (lane >= o) x += y;
+      }
+      if (b < p.B) s_pref[b + 1] = run + x;
+      run += __shfl_sync(FULL, x, 31);
+    }
+    if (lane == 0) s_pref[0] = 0;
+  }
+  __syncthreads();
+  // the last sequence longer than four times the mean
+  if (warp == 0) {
+    const long long thr = 4ll * s_pref[p.B];  // nt_b * B > thr  <=>  nt_b > 4 * mean
+    int last = -1;
+    for (int b = lane; b < p.B; b += 32)
+      if (static_cast<long long>(s_pref[b + 1] - s_pref[b]) * p.B > thr) last = b;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) last = max(last, __shfl_xor_sync(FULL, last, o));
+    if (lane == 0) s_last_long = last;
+  }
+  __syncthreads();
+  StepPlan r;
+  r.total = p.Hv * s_pref[p.B];
+  const long long short_tail =
+      r.total - static_cast<long long>(p.Hv) * s_pref[s_last_long + 1];
+  long long pool_want = static_cast<long long>(r.total) * p.pool_permille / 1000;
+  if (pool_want > short_tail) pool_want = short_tail;
+  // rounded up, so that the static ranges never reach into the pool's share
+  r.ws = static_cast<int>((r.total - pool_want + p.nw - 1) / p.nw);
+  if (r.ws < p.min_tiles) r.ws = p.min_tiles;
+  r.ts = static_cast<int>(
+      min(static_cast<long long>(r.ws) * p.nw, static_cast<long long>(r.total)));
+  const int pool_tiles = r.total - r.ts;
+  r.piece = (pool_tiles + p.np_max - 1) / p.np_max;
+  if (r.piece < p.piece_min) r.piece = p.piece_min;
+  return r;
+}
+
+// Partial results of pair s (tiles [F, F + nt) of the flat space): the
+// static slots of the warps whose range meets [F, min(F + nt, ts)), then the
+// pool slots of the pieces that meet [max(F, ts), F + nt).
+struct Cands {
+  int w0, na;  // static warps [w0, w0 + na)
+  int i0, np;  // pool pieces [i0, i0 + np)
+};
+
+__device__ __forceinline__ Cands pair_cands(int F, int nt, const StepPlan& pl) {
+  Cands c = {0, 0, 0, 0};
+  if (nt > 0 && F < pl.ts) {
+    c.w0 = F / pl.ws;
+    c.na = (min(F + nt, pl.ts) - 1) / pl.ws - c.w0 + 1;
+  }
+  if (nt > 0 && F + nt > pl.ts) {
+    c.i0 = (max(F, pl.ts) - pl.ts) / pl.piece;
+    c.np = (F + nt - 1 - pl.ts) / pl.piece - c.i0 + 1;
+  }
+  return c;
+}
+
+}  // namespace pa
