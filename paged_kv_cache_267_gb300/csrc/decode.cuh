@@ -5,17 +5,19 @@
 // never straddle a physical block because block_size is a multiple of 16.
 // All tiles of all pairs form one flat index space (pair-major). The first
 // part of it (about 90%) is split into equal contiguous static ranges, one per
-// worker warp; the rest is a pool of small pieces that warps claim with one
+// worker warp; the rest is a pool of pieces that warps claim with one
 // atomicAdd each once their static range is done (the claim for the next
 // piece is issued a piece ahead, so the copy pipeline never drains). Warps on
 // SMs that get less bandwidth thus take fewer pieces and all warps finish
-// together. The pool only covers the trailing run of sequences no longer than
-// four times the mean, so a long sequence is never cut into small pieces. A run of one warp's tiles inside one pair is a segment; each
-// segment writes one partial (running max m, running sum l, unnormalised
-// output) to a slot fixed by arithmetic: pair + warp for static segments,
-// pair + piece (in a second region) for pool segments -- unique because the
-// walk through the (pair, warp) and (pair, piece) grids is a monotone
-// staircase. A merge kernel combines each pair's partials by their
+// together; the pool ends with one-tile pieces, so when it runs dry no warp
+// holds more than a tile or two. The pool only covers the trailing run of
+// sequences no longer than four times the mean, so a long sequence is never
+// cut into small pieces (plan.cuh). A run of one warp's tiles inside one pair
+// is a segment; each segment writes one partial (running max m, running sum
+// l, unnormalised output) to a slot fixed by arithmetic: pair + warp for
+// static segments, pair + piece (in a second region) for pool segments --
+// unique because the walk through the (pair, warp) and (pair, piece) grids is
+// a monotone staircase. A merge kernel combines each pair's partials by their
 // log-sum-exp weights.
 //
 // Data movement. Each warp owns a ring of STAGES shared-memory stages; one
@@ -206,7 +208,7 @@ __global__ void __launch_bounds__(WARPS * 32, 2)
   pin.np_max = a.np_max;
   pin.piece_min = a.piece_min;
   const StepPlan pl = plan_step(pin, s_len, s_pref);
-  const int total = pl.total, ws = pl.ws, ts = pl.ts, piece = pl.piece;
+  const int total = pl.total, ws = pl.ws, ts = pl.ts;
   const int nw = pin.nw;
   const int pool_tiles = total - ts;
   const int w = blockIdx.x * WARPS + warp;
@@ -239,6 +241,28 @@ __global__ void __launch_bounds__(WARPS * 32, 2)
   int pf_b = -1, pf_lb0 = 0, pf_val = 0;  // prefetched next window
   int produced = 0, consumed = 0;
 
+  // Makes the block-id window hold logical block lb of sequence b: 32 table
+  // entries per warp, one per lane, with the following window prefetched.
+  auto refresh_window = [&](int b, int lb) {
+    if (b != id_b || lb < id_lb0 || lb >= id_lb0 + 32) {
+      if (b == pf_b && lb >= pf_lb0 && lb < pf_lb0 + 32) {
+        id_b = pf_b;
+        id_lb0 = pf_lb0;
+        id_val = pf_val;
+      } else {
+        id_b = b;
+        id_lb0 = lb;
+        const int e = lb + lane;
+        id_val = (e < a.MB) ? __ldg(a.block_tables + static_cast<size_t>(b) * a.MB + e) : 0;
+      }
+      // prefetch the following window of this sequence's table
+      pf_b = id_b;
+      pf_lb0 = id_lb0 + 32;
+      const int e2 = pf_lb0 + lane;
+      pf_val = (e2 < a.MB) ? __ldg(a.block_tables + static_cast<size_t>(pf_b) * a.MB + e2) : 0;
+    }
+  };
+
   // Produces the next tile into stage `slot`; false when no work is left.
   auto produce = [&](int slot) -> bool {
     while (np >= run_end) {
@@ -248,17 +272,15 @@ __global__ void __launch_bounds__(WARPS * 32, 2)
         return false;
       }
       if (!claim_issued) issue_claim();
-      const int i = static_cast<int>(__shfl_sync(FULL, pending, 0));
+      const unsigned i = __shfl_sync(FULL, pending, 0);
       claim_issued = false;
-      const long long p0 = static_cast<long long>(ts) + static_cast<long long>(i) * piece;
-      if (p0 >= total) {
+      if (i >= static_cast<unsigned>(pl.n_pool)) {
         phase = 2;
         return false;
       }
       phase = 1;
-      np = static_cast<int>(p0);
-      run_end = min(np + piece, total);
-      run_id = i;
+      piece_range(static_cast<int>(i), pl, &np, &run_end);
+      run_id = static_cast<int>(i);
       run_first = true;
       issue_claim();  // the next piece, one piece ahead
     }
@@ -279,23 +301,7 @@ __global__ void __launch_bounds__(WARPS * 32, 2)
     const int L = s_len[pc.b];
     const int pt = win_start(L, a.span) / kTile + pc.t;  // tile index in position space
     const int lb = (pt * kTile) / a.bs;
-    if (pc.b != id_b || lb < id_lb0 || lb >= id_lb0 + 32) {
-      if (pc.b == pf_b && lb >= pf_lb0 && lb < pf_lb0 + 32) {
-        id_b = pf_b;
-        id_lb0 = pf_lb0;
-        id_val = pf_val;
-      } else {
-        id_b = pc.b;
-        id_lb0 = lb;
-        const int e = lb + lane;
-        id_val = (e < a.MB) ? __ldg(a.block_tables + static_cast<size_t>(pc.b) * a.MB + e) : 0;
-      }
-      // prefetch the following window of this sequence's table
-      pf_b = id_b;
-      pf_lb0 = id_lb0 + 32;
-      const int e2 = pf_lb0 + lane;
-      pf_val = (e2 < a.MB) ? __ldg(a.block_tables + static_cast<size_t>(pf_b) * a.MB + e2) : 0;
-    }
+    refresh_window(pc.b, lb);
     int phys = __shfl_sync(FULL, id_val, lb - id_lb0);
     if (static_cast<unsigned>(phys) >= static_cast<unsigned>(a.NB)) {
       if (lane == 0) atomicOr(a.err, kErrBlockId);
@@ -323,6 +329,15 @@ __global__ void __launch_bounds__(WARPS * 32, 2)
     return true;
   };
 
+  // The block tables are inputs that the write path never touches: load the
+  // window of this warp's first tile before waiting for the previous kernel,
+  // so that its first K/V copies issue right after the wait.
+  if (f0 < f1) {
+    Cursor c0;
+    cursor_locate(c0, f0, s_pref, a.B, a.Hv);
+    const int pt0 = win_start(s_len[c0.b], a.span) / kTile + c0.t;
+    refresh_window(c0.b, (pt0 * kTile) / a.bs);
+  }
   griddep_wait();  // the caches may have been written by the previous kernel
   for (int i = 0; i < STAGES; ++i) {
     if (!produce(produced % STAGES)) break;
@@ -638,6 +653,8 @@ __global__ void __launch_bounds__(WARPS * 32, 2)
                                : static_cast<size_t>(pair) + w;
       float* P = a.part + pslot * part_stride(a.CG, D);
       const float vs = kFp8 ? a.v_scale : 1.f;
+      // kept in L2 for the merge kernel, which reads them right after
+      const uint64_t keep = l2_evict_last();
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
@@ -651,12 +668,12 @@ __global__ void __launch_bounds__(WARPS * 32, 2)
             float* Ph = P + h * D;
 #pragma unroll
             for (int mt = 0; mt < MT; ++mt) {
-              Ph[acc_dim<kFp8>(mt, g, 0)] = acc[mt][nt][e] * vs;
-              Ph[acc_dim<kFp8>(mt, g, 1)] = acc[mt][nt][2 + e] * vs;
+              st_f32_hint(Ph + acc_dim<kFp8>(mt, g, 0), acc[mt][nt][e] * vs, keep);
+              st_f32_hint(Ph + acc_dim<kFp8>(mt, g, 1), acc[mt][nt][2 + e] * vs, keep);
             }
             if (g == 0) {
-              P[a.CG * D + h] = m_run[nt][e];
-              P[a.CG * D + a.CG + h] = l;
+              st_f32_hint(P + a.CG * D + h, m_run[nt][e], keep);
+              st_f32_hint(P + a.CG * D + a.CG + h, l, keep);
             }
           }
         }

@@ -64,12 +64,13 @@ __device__ __forceinline__ void merge_fold(const MergeArgs& a, SlotFn slot_of, i
 #pragma unroll
   for (int v = 0; v < VPL; ++v) r.acc[v] = make_float4(0.f, 0.f, 0.f, 0.f);
   const bool on = 4 * lane < a.D;  // D = 64 uses half the lanes
+  const uint64_t once = l2_evict_first();  // each partial is read once
   for (int k = k0; k < k1; k += U) {
     float my_m = -INFINITY, my_l = 0.f;
     if (lane < U && k + lane < k1) {
       const float* P = a.part + static_cast<size_t>(slot_of(k + lane)) * stride;
-      my_m = P[GD + h];
-      my_l = P[GD + a.CG + h];
+      my_m = ld_f32_hint(P + GD + h, once);
+      my_l = ld_f32_hint(P + GD + a.CG + h, once);
     }
     float4 o[U][VPL];
 #pragma unroll
@@ -81,7 +82,7 @@ __device__ __forceinline__ void merge_fold(const MergeArgs& a, SlotFn slot_of, i
         const float* P = a.part + static_cast<size_t>(slot_of(kk)) * stride;
 #pragma unroll
         for (int v = 0; v < VPL; ++v)
-          o[j][v] = *reinterpret_cast<const float4*>(P + h * a.D + v * 128 + 4 * lane);
+          o[j][v] = ld_f32x4_hint(P + h * a.D + v * 128 + 4 * lane, once);
       }
     }
 #pragma unroll
@@ -163,9 +164,10 @@ __global__ void __launch_bounds__(kMergeThreads, 3) merge_kernel(const MergeArgs
   constexpr unsigned FULL = 0xffffffffu;
   constexpr int ROW = VPL * 128 + 4;  // floats per group result in shared memory
   extern __shared__ __align__(16) float s_dyn[];
-  float* s_grp = s_dyn;                                          // [8][ROW]
-  int* s_pref = reinterpret_cast<int*>(s_dyn + kMergeWarps * ROW);  // B + 1
-  int* s_wide = s_pref + a.B + 1;                                // B + 1 prefix of wide columns
+  float* s_grp = s_dyn;                                             // [8][ROW]
+  int* s_len = reinterpret_cast<int*>(s_dyn + kMergeWarps * ROW);   // B
+  int* s_pref = s_len + a.B;                                        // B + 1
+  int* s_wide = s_pref + a.B + 1;                                   // B + 1 prefix of wide columns
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   // ---- the decode kernel's plan, before waiting for it
@@ -181,21 +183,24 @@ __global__ void __launch_bounds__(kMergeThreads, 3) merge_kernel(const MergeArgs
   pin.min_tiles = a.min_tiles;
   pin.np_max = a.np_max;
   pin.piece_min = a.piece_min;
-  const StepPlan pl = plan_step(pin, nullptr, s_pref);
+  const StepPlan pl = plan_step(pin, s_len, s_pref);
   const int HC = a.Hv * a.CG;  // columns per sequence
-  // wide sequences: some pair has more than kMergeNarrow candidates
+  // wide sequences: some pair has more than kMergeNarrow candidates (flags
+  // from all threads, one pair each, then a prefix of columns in warp 0)
+  for (int b = tid; b < a.B; b += blockDim.x) s_wide[b + 1] = 0;
+  __syncthreads();
+  for (int p = tid; p < a.B * a.Hv; p += blockDim.x) {
+    const int b = p / a.Hv, vh = p - b * a.Hv;
+    const int nt = s_pref[b + 1] - s_pref[b];
+    const Cands cd = pair_cands(a.Hv * s_pref[b] + vh * nt, nt, pl);
+    if (cd.na + cd.np > kMergeNarrow) s_wide[b + 1] = HC;
+  }
+  __syncthreads();
   if (warp == 0) {
     int run = 0;
     for (int b0 = 0; b0 < a.B; b0 += 32) {
       const int b = b0 + lane;
-      int x = 0;
-      if (b < a.B) {
-        const int nt = s_pref[b + 1] - s_pref[b];
-        for (int vh = 0; vh < a.Hv && x == 0; ++vh) {
-          const Cands cd = pair_cands(a.Hv * s_pref[b] + vh * nt, nt, pl);
-          if (cd.na + cd.np > kMergeNarrow) x = HC;
-        }
-      }
+      int x = (b < a.B) ? s_wide[b + 1] : 0;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const int y = __shfl_up_sync(FULL, x, o);
@@ -295,19 +300,23 @@ cudaError_t merge_launch(int out_type, const MergeArgs& a, int grid, cudaStream_
   cfg.blockDim = dim3(kMergeThreads);
   const int row = (a.D > 128 ? 2 : 1) * 128 + 4;
   cfg.dynamicSmemBytes = static_cast<size_t>(kMergeWarps) * row * sizeof(float) +
-                         static_cast<size_t>(2 * (a.B + 1)) * sizeof(int);
+                         static_cast<size_t>(3 * a.B + 2) * sizeof(int);
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (a.D > 128) {
-    if (out_type == kBF16) return cudaLaunchKernelEx(&cfg, merge_kernel<kBF16, 2>, a);
-    return cudaLaunchKernelEx(&cfg, merge_kernel<kF16, 2>, a);
+  void (*fn)(const MergeArgs);
+  if (a.D > 128) fn = out_type == kBF16 ? merge_kernel<kBF16, 2> : merge_kernel<kF16, 2>;
+  else fn = out_type == kBF16 ? merge_kernel<kBF16, 1> : merge_kernel<kF16, 1>;
+  if (cfg.dynamicSmemBytes > 48 * 1024) {  // large batches: the per-sequence prefixes
+    const cudaError_t e = cudaFuncSetAttribute(
+        reinterpret_cast<const void*>(fn), cudaFuncAttributeMaxDynamicSharedMemorySize,
+        static_cast<int>(cfg.dynamicSmemBytes));
+    if (e != cudaSuccess) return e;
   }
-  if (out_type == kBF16) return cudaLaunchKernelEx(&cfg, merge_kernel<kBF16, 1>, a);
-  return cudaLaunchKernelEx(&cfg, merge_kernel<kF16, 1>, a);
+  return cudaLaunchKernelEx(&cfg, fn, a);
 }
 
 // ------------------------------------------------------------- write path

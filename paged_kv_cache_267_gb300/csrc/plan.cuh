@@ -9,10 +9,13 @@
 // Every (sequence b, virtual KV head) pair owns the 16-token tiles covering
 // its read range [start, L); all tiles form one flat, pair-major index space.
 // Its first part is split into equal static ranges of `ws` tiles, one per
-// worker warp (ending at `ts`); the rest is a pool of pieces of `piece` tiles
-// claimed dynamically. The pool only covers the trailing run of sequences
-// whose tile count is at most four times the mean, so a long sequence is never
-// cut into many small pieces.
+// worker warp (ending at `ts`); the rest is a pool of pieces claimed
+// dynamically, in order: "head" pieces of `piece` tiles, then "tail" pieces of
+// one tile each (about one per warp). A warp streams only a few GB/s, so the
+// work a warp holds when the pool runs dry sets the kernel's tail: ending the
+// pool with one-tile pieces keeps that to a tile or two. The pool only covers
+// the trailing run of sequences whose tile count is at most four times the
+// mean, so a long sequence is never cut into many small pieces.
 #pragma once
 
 #include "pa_internal.h"
@@ -36,47 +39,56 @@ struct PlanIn {
 };
 
 struct StepPlan {
-  int total;  // tiles of all pairs
-  int ws;     // static tiles per warp
-  int ts;     // end of the static region
-  int piece;  // tiles per pool piece
+  int total;   // tiles of all pairs
+  int ws;      // static tiles per warp
+  int ts;      // end of the static region
+  int piece;   // tiles per head piece of the pool
+  int hh;      // tiles of the pool's head part (pool tiles [ts, ts + hh))
+  int n_head;  // head pieces: ceil(hh / piece)
+  int n_pool;  // all pieces: n_head + (total - ts - hh) one-tile tail pieces
 };
 
+// Pool piece holding flat tile f (ts <= f < total).
+__device__ __forceinline__ int piece_of(int f, const StepPlan& pl) {
+  const int t = f - pl.ts;
+  return t < pl.hh ? t / pl.piece : pl.n_head + (t - pl.hh);
+}
+
+// First flat tile and end of pool piece i (i < n_pool).
+__device__ __forceinline__ void piece_range(int i, const StepPlan& pl, int* f0, int* f1) {
+  if (i < pl.n_head) {
+    *f0 = pl.ts + i * pl.piece;
+    *f1 = pl.ts + min((i + 1) * pl.piece, pl.hh);
+  } else {
+    *f0 = pl.ts + pl.hh + (i - pl.n_head);
+    *f1 = *f0 + 1;
+  }
+}
+
 // Block-wide: every thread of the block calls it (it synchronises the
-// block). Fills s_pref[0 .. B] with the exclusive prefix of tiles per pair
-// over the sequences and, when s_len is given, s_len[0 .. B) with the lengths
-// clamped to [0, cap] (a length outside is reported through `err`).
+// block). Fills s_len[0 .. B) with the lengths clamped to [0, cap] (a length
+// outside is reported through `err`) and s_pref[0 .. B] with the exclusive
+// prefix of tiles per pair over the sequences. The host bounds B * Hv * tiles
+// per pair below 2^31, so the tile counts fit 32-bit integers.
 __device__ inline StepPlan plan_step(const PlanIn& p, int* s_len, int* s_pref) {
   constexpr unsigned FULL = 0xffffffffu;
   __shared__ int s_last_long;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  if (s_len != nullptr) {
-    for (int b = tid; b < p.B; b += blockDim.x) {
-      int L = p.seq_lens[b];
-      if (L < 0 || L > p.cap) {
-        if (p.err) atomicOr(p.err, PA_DEVERR_SEQ_LEN);
-        L = L < 0 ? 0 : p.cap;
-      }
-      s_len[b] = L;
+  for (int b = tid; b < p.B; b += blockDim.x) {
+    int L = p.seq_lens[b];
+    if (L < 0 || L > p.cap) {
+      if (p.err) atomicOr(p.err, PA_DEVERR_SEQ_LEN);
+      L = L < 0 ? 0 : p.cap;
     }
-    __syncthreads();
+    s_len[b] = L;
   }
+  __syncthreads();
   // exclusive prefix of tiles per pair over the sequences (one warp)
   if (warp == 0) {
     int run = 0;
     for (int b0 = 0; b0 < p.B; b0 += 32) {
       const int b = b0 + lane;
-      int x = 0;
-      if (b < p.B) {
-        int L;
-        if (s_len != nullptr) {
-          L = s_len[b];
-        } else {
-          L = p.seq_lens[b];
-          L = L < 0 ? 0 : (L > p.cap ? p.cap : L);
-        }
-        x = tiles_of(L, p.span);
-      }
+      int x = (b < p.B) ? tiles_of(s_len[b], p.span) : 0;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const int y = __shfl_up_sync(FULL, x, o);
@@ -101,18 +113,26 @@ __device__ inline StepPlan plan_step(const PlanIn& p, int* s_len, int* s_pref) {
   __syncthreads();
   StepPlan r;
   r.total = p.Hv * s_pref[p.B];
-  const long long short_tail =
-      r.total - static_cast<long long>(p.Hv) * s_pref[s_last_long + 1];
-  long long pool_want = static_cast<long long>(r.total) * p.pool_permille / 1000;
+  const int short_tail = r.total - p.Hv * s_pref[s_last_long + 1];
+  int pool_want = static_cast<int>(static_cast<long long>(r.total) * p.pool_permille / 1000);
   if (pool_want > short_tail) pool_want = short_tail;
   // rounded up, so that the static ranges never reach into the pool's share
-  r.ws = static_cast<int>((r.total - pool_want + p.nw - 1) / p.nw);
+  const unsigned nw = static_cast<unsigned>(p.nw);
+  r.ws = static_cast<int>((static_cast<unsigned>(r.total - pool_want) + nw - 1u) / nw);
   if (r.ws < p.min_tiles) r.ws = p.min_tiles;
   r.ts = static_cast<int>(
       min(static_cast<long long>(r.ws) * p.nw, static_cast<long long>(r.total)));
   const int pool_tiles = r.total - r.ts;
-  r.piece = (pool_tiles + p.np_max - 1) / p.np_max;
+  // one-tile tail pieces: about one per warp, at most half of the slots
+  int tail = min(pool_tiles, min(p.nw, p.np_max / 2));
+  r.hh = pool_tiles - tail;
+  const int head_slots = p.np_max - tail;  // >= np_max / 2 >= 1
+  r.piece = static_cast<int>((static_cast<unsigned>(r.hh) + head_slots - 1u) /
+                             static_cast<unsigned>(head_slots));
   if (r.piece < p.piece_min) r.piece = p.piece_min;
+  r.n_head = static_cast<int>((static_cast<unsigned>(r.hh) + r.piece - 1u) /
+                              static_cast<unsigned>(r.piece));
+  r.n_pool = r.n_head + tail;
   return r;
 }
 
@@ -131,8 +151,8 @@ __device__ __forceinline__ Cands pair_cands(int F, int nt, const StepPlan& pl) {
     c.na = (min(F + nt, pl.ts) - 1) / pl.ws - c.w0 + 1;
   }
   if (nt > 0 && F + nt > pl.ts) {
-    c.i0 = (max(F, pl.ts) - pl.ts) / pl.piece;
-    c.np = (F + nt - 1 - pl.ts) / pl.piece - c.i0 + 1;
+    c.i0 = piece_of(max(F, pl.ts), pl);
+    c.np = piece_of(F + nt - 1, pl) - c.i0 + 1;
   }
   return c;
 }
