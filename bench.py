@@ -167,8 +167,10 @@ def measured_peak() -> tuple[float, str]:
 
 
 def kernel_source_hash() -> str:
+    """Hash of the sources that make up the decode kernel (its code, the
+    PTX wrappers, the step plan and the argument structs)."""
     h = hashlib.sha256()
-    for f in ("decode.cuh", "ptx.cuh"):
+    for f in ("decode.cuh", "ptx.cuh", "plan.cuh", "pa_internal.h"):
         with open(os.path.join(ROOT, "paged_kv_cache_267_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]

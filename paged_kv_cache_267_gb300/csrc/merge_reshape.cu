@@ -28,18 +28,19 @@ cudaError_t device_error_word(int32_t** ptr) {
 // (single-query decode) or a (query, q head) of a chunk; columns that pad the
 // last group of a chunk have no output row and are skipped.
 //
-// The kernel derives the decode kernel's plan from seq_lens before it waits
-// for the decode kernel (it is launched as its programmatic dependent), so
-// after the decode ends each column costs one round trip for its partials.
-// Columns of sequences where some pair has more than eight candidates (pairs
-// cut into pool pieces, or spanning many warps' static ranges) are "wide":
-// each goes to one whole CTA, whose eight warps fold one eighth of the
-// candidates each and combine their results through shared memory. Every
-// other column is one warp's work. A warp folds its candidates online with
-// eight loads in flight per lane (D <= 128; four for D = 256).
+// The plan of the step (how the decode kernel split the tiles, and which
+// sequences have pairs with many partials) comes from the decode kernel's
+// first CTA through the workspace, so the merge needs one load of it after the
+// decode kernel ends (it is launched as its programmatic dependent) instead
+// of computing it again in every CTA. Columns of sequences where some pair
+// may have more than eight partials (pairs cut into pool pieces, or spanning
+// many warps' static ranges) are "wide": each goes to one whole CTA, whose
+// eight warps fold one eighth of the partials each and combine their results
+// through shared memory. Every other column is one warp's work. A warp folds
+// its partials online with eight loads in flight per lane (D <= 128; four for
+// D = 256).
 constexpr int kMergeThreads = 256;
 constexpr int kMergeWarps = kMergeThreads / 32;
-constexpr int kMergeNarrow = 8;  // candidates one warp folds in one round trip
 
 // Per-lane state of one column: head dims v * 128 + 4 * lane .. + 3 for
 // v < VPL (VPL = 1 for D <= 128, 2 for D = 256).
@@ -161,60 +162,20 @@ __device__ __forceinline__ MergeCol merge_col(const MergeArgs& a, const StepPlan
 
 template <int OT, int VPL>
 __global__ void __launch_bounds__(kMergeThreads, 3) merge_kernel(const MergeArgs a) {
-  constexpr unsigned FULL = 0xffffffffu;
   constexpr int ROW = VPL * 128 + 4;  // floats per group result in shared memory
   extern __shared__ __align__(16) float s_dyn[];
-  float* s_grp = s_dyn;                                             // [8][ROW]
-  int* s_len = reinterpret_cast<int*>(s_dyn + kMergeWarps * ROW);   // B
-  int* s_pref = s_len + a.B;                                        // B + 1
-  int* s_wide = s_pref + a.B + 1;                                   // B + 1 prefix of wide columns
+  float* s_grp = s_dyn;                                                 // [8][ROW]
+  int* s_plan = reinterpret_cast<int*>(s_dyn + kMergeWarps * ROW);      // plan_words(B)
+  int* s_pref = s_plan + kPlanScalars;                                  // B + 1
+  int* s_wide = s_pref + a.B + 1;                                       // B + 1 prefix of wide columns
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-  // ---- the decode kernel's plan, before waiting for it
-  PlanIn pin;
-  pin.seq_lens = a.seq_lens;
-  pin.err = nullptr;  // the decode kernel reports bad lengths
-  pin.B = a.B;
-  pin.cap = a.cap;
-  pin.span = a.span;
-  pin.Hv = a.Hv;
-  pin.nw = a.NW;
-  pin.pool_permille = a.pool_permille;
-  pin.min_tiles = a.min_tiles;
-  pin.np_max = a.np_max;
-  pin.piece_min = a.piece_min;
-  const StepPlan pl = plan_step(pin, s_len, s_pref);
-  const int HC = a.Hv * a.CG;  // columns per sequence
-  // wide sequences: some pair has more than kMergeNarrow candidates (flags
-  // from all threads, one pair each, then a prefix of columns in warp 0)
-  for (int b = tid; b < a.B; b += blockDim.x) s_wide[b + 1] = 0;
-  __syncthreads();
-  for (int p = tid; p < a.B * a.Hv; p += blockDim.x) {
-    const int b = p / a.Hv, vh = p - b * a.Hv;
-    const int nt = s_pref[b + 1] - s_pref[b];
-    const Cands cd = pair_cands(a.Hv * s_pref[b] + vh * nt, nt, pl);
-    if (cd.na + cd.np > kMergeNarrow) s_wide[b + 1] = HC;
-  }
-  __syncthreads();
-  if (warp == 0) {
-    int run = 0;
-    for (int b0 = 0; b0 < a.B; b0 += 32) {
-      const int b = b0 + lane;
-      int x = (b < a.B) ? s_wide[b + 1] : 0;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(FULL, x, o);
-        if (lane >= o) x += y;
-      }
-      if (b < a.B) s_wide[b + 1] = run + x;
-      run += __shfl_sync(FULL, x, 31);
-    }
-    if (lane == 0) s_wide[0] = 0;
-  }
-  __syncthreads();
-
-  griddep_wait();  // the decode kernel's partials are complete and visible
+  griddep_wait();  // the decode kernel's plan and partials are complete and visible
   if (blockIdx.x == 0 && tid == 0) *a.pool = 0u;
+  for (int i = tid; i < plan_words(a.B); i += blockDim.x) s_plan[i] = a.plan[i];
+  __syncthreads();
+  const StepPlan pl = plan_load(s_plan);
+  const int HC = a.Hv * a.CG;  // columns per sequence
   const int S = a.B * a.Hv;
 
   // ---- wide columns: one CTA each
@@ -300,7 +261,7 @@ cudaError_t merge_launch(int out_type, const MergeArgs& a, int grid, cudaStream_
   cfg.blockDim = dim3(kMergeThreads);
   const int row = (a.D > 128 ? 2 : 1) * 128 + 4;
   cfg.dynamicSmemBytes = static_cast<size_t>(kMergeWarps) * row * sizeof(float) +
-                         static_cast<size_t>(3 * a.B + 2) * sizeof(int);
+                         static_cast<size_t>(plan_words(a.B)) * sizeof(int);
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

@@ -210,7 +210,7 @@ size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // Section offsets of the decode workspace (layout described in pa_internal.h).
 struct WsLayout {
-  size_t pool, part, total;
+  size_t pool, plan, part, total;
 };
 
 // Hv pairs per sequence with CG columns each (Hkv and G for single-query decode).
@@ -222,6 +222,7 @@ WsLayout ws_layout(int64_t B, int Hv, int CG, int D, int64_t workers) {
   // The pool counter sits at a fixed offset: it must stay zero between calls
   // whatever their shapes, and each step's merge only resets its own copy.
   L.pool = o;  o += 256;
+  L.plan = o;  o += round_up(static_cast<size_t>(pa::plan_words(static_cast<int>(B))) * 4, 256);
   L.part = o;  o += nslot * static_cast<size_t>(pa::part_stride(CG, D)) * sizeof(float);
   L.total = o;
   return L;
@@ -399,7 +400,7 @@ pa_status get_workspace(DeviceState* st, cudaStream_t stream, const WsLayout& la
   }
   if (w->dirty) {
     cudaError_t e = cudaMemsetAsync(static_cast<char*>(w->ptr) + lay.pool, 0,
-                                    lay.part - lay.pool, stream);
+                                    lay.plan - lay.pool, stream);
     if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(pool counter)");
     w->dirty = false;
   }
@@ -750,6 +751,7 @@ pa_status run_decode(const DecodeCall& c, DeviceState* st, const DecodePlan& pla
   a.seq_lens = static_cast<const int32_t*>(c.sl->data);
   char* wsb = static_cast<char*>(ws);
   a.pool = reinterpret_cast<uint32_t*>(wsb + layout.pool);
+  a.plan = reinterpret_cast<int32_t*>(wsb + layout.plan);
   a.part = reinterpret_cast<float*>(wsb + layout.part);
   a.err = st->err_word;
   a.B = static_cast<int>(c.B);
@@ -788,7 +790,7 @@ pa_status run_decode(const DecodeCall& c, DeviceState* st, const DecodePlan& pla
   pa::MergeArgs m;
   m.out = c.out->data;
   m.part = a.part;
-  m.seq_lens = a.seq_lens;
+  m.plan = a.plan;
   m.pool = a.pool;
   m.NW = plan.workers;
   m.B = a.B;
@@ -800,12 +802,6 @@ pa_status run_decode(const DecodeCall& c, DeviceState* st, const DecodePlan& pla
   m.NCG = a.NCG;
   m.CG = a.CG;
   m.Hv = a.Hv;
-  m.cap = a.MB * a.bs;
-  m.span = a.span;
-  m.min_tiles = a.min_tiles;
-  m.pool_permille = a.pool_permille;
-  m.piece_min = a.piece_min;
-  m.np_max = a.np_max;
   e = pa::merge_launch(c.qt, m, st->num_sms * 3, cs, !prof);
   if (e != cudaSuccess) {
     if (wsp) {
@@ -963,7 +959,7 @@ pa_status decode_in_buffer(const pa_tensor* out, const pa_tensor* q, const pa_te
   // The piece counter must start at zero; the buffer keeps whatever the
   // previous call left there.
   cudaError_t e = cudaMemsetAsync(static_cast<char*>(buffer) + layout.pool, 0,
-                                  layout.part - layout.pool, cs);
+                                  layout.plan - layout.pool, cs);
   if (e != cudaSuccess) return cuda_fail(e, "clearing the scratch counter");
   return run_decode(c, st, plan, layout, buffer, nullptr, cs);
 }

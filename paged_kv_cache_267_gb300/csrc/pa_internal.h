@@ -22,22 +22,31 @@ __host__ __device__ constexpr inline int part_stride(int G, int D) {
 // Decode workspace layout (device memory, all sections 256-byte aligned):
 //   pool  u32 at offset 0: pool piece counter; zero between calls (the merge
 //         kernel resets it after each step), at the same place for any shape
-//   part  f32 [NSLOT][part_stride(CG, D)] at offset 256: acc[CG][D], m[CG],
-//         l[CG], padding to a multiple of 4 floats so every slot starts
-//         16-byte aligned
+//   plan  int32 [plan_words(B)] at offset 256: the step's plan, written by the
+//         decode kernel's first CTA before it streams, read by the merge
+//         kernel: kPlanScalars scalars (tiles, static tiles per warp, end of
+//         the static region, head piece size, head tiles, head pieces, all
+//         pieces), the tile prefix over the sequences (B + 1), and the prefix
+//         of "wide" columns over the sequences (B + 1): all columns of a
+//         sequence where some pair may have more than kMergeNarrow partials
+//   part  f32 [NSLOT][part_stride(CG, D)]: acc[CG][D], m[CG], l[CG], padding
+//         to a multiple of 4 floats so every slot starts 16-byte aligned
 // with S = B * Hv pairs, NW worker warps, NSLOT = 2 S + NW + NPMAX. For
 // single-query decode Hv = Hkv and CG = G (columns are the group's q heads).
 // A segment is a run of one warp's tiles inside one pair. Static segments of
 // pair s by warp w use slot s + w; segments of pool piece i use slot
 // S + NW + s + i. Both are unique because the walk through the (pair, warp)
-// and (pair, piece) grids is a monotone staircase. The step's plan (how tiles
-// are split) is not stored: the decode and merge kernels derive it from
-// seq_lens with the same code (plan.cuh).
+// and (pair, piece) grids is a monotone staircase.
+constexpr int kPlanScalars = 8;
+__host__ __device__ constexpr inline int plan_words(int B) { return kPlanScalars + 2 * (B + 1); }
+constexpr int kMergeNarrow = 8;  // partials one merge warp folds in one round trip
+
 struct DecodeArgs {
   const void* q;                 // [B, T, Hq, D] ([B, Hq, D] when T = 1)
   const int32_t* block_tables;   // [B, MB]
   const int32_t* seq_lens;       // [B]
   uint32_t* pool;
+  int32_t* plan;                 // plan region, written by the first CTA
   float* part;
   int32_t* err;                  // device error word
   int B, Hq, Hkv, G, D, bs, MB, NB, window;
@@ -57,12 +66,10 @@ struct DecodeArgs {
 struct MergeArgs {
   void* out;                     // [B, T, Hq, D], dtype of q
   const float* part;
-  const int32_t* seq_lens;       // [B], to derive the decode kernel's plan
+  const int32_t* plan;           // the decode kernel's plan region
   uint32_t* pool;                // reset to zero for the next step
   int B, Hq, Hkv, G, D, NW;
   int T, NCG, CG, Hv;            // as in DecodeArgs
-  int cap, span;                 // plan inputs, as given to the decode kernel
-  int min_tiles, pool_permille, piece_min, np_max;
 };
 
 // Bound on output columns (batch * q heads * queries) of one call.

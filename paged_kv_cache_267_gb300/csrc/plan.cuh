@@ -1,10 +1,7 @@
-// The work plan of one decode step, computed from seq_lens alone.
-//
-// The decode kernel and the merge kernel both derive it, each in its own
-// blocks, from the same inputs with the same code, so they agree without
-// passing it through memory: the merge kernel plans while the decode kernel
-// still streams, and after the decode finishes it needs no load of a plan
-// before it reads the partial results.
+// The work plan of one decode step, computed from seq_lens alone by the
+// decode kernel. Its first CTA stores it in the workspace (plan region, see
+// pa_internal.h) before streaming, and the merge kernel reads it there after
+// the decode kernel has finished.
 //
 // Every (sequence b, virtual KV head) pair owns the 16-token tiles covering
 // its read range [start, L); all tiles form one flat, pair-major index space.
@@ -136,6 +133,28 @@ __device__ inline StepPlan plan_step(const PlanIn& p, int* s_len, int* s_pref) {
   return r;
 }
 
+__device__ __forceinline__ void plan_store(int32_t* dst, const StepPlan& pl) {
+  dst[0] = pl.total;
+  dst[1] = pl.ws;
+  dst[2] = pl.ts;
+  dst[3] = pl.piece;
+  dst[4] = pl.hh;
+  dst[5] = pl.n_head;
+  dst[6] = pl.n_pool;
+  dst[7] = 0;
+}
+__device__ __forceinline__ StepPlan plan_load(const int32_t* src) {
+  StepPlan pl;
+  pl.total = src[0];
+  pl.ws = src[1];
+  pl.ts = src[2];
+  pl.piece = src[3];
+  pl.hh = src[4];
+  pl.n_head = src[5];
+  pl.n_pool = src[6];
+  return pl;
+}
+
 // Partial results of pair s (tiles [F, F + nt) of the flat space): the
 // static slots of the warps whose range meets [F, min(F + nt, ts)), then the
 // pool slots of the pieces that meet [max(F, ts), F + nt).
@@ -155,6 +174,21 @@ __device__ __forceinline__ Cands pair_cands(int F, int nt, const StepPlan& pl) {
     c.np = piece_of(F + nt - 1, pl) - c.i0 + 1;
   }
   return c;
+}
+
+// Upper bound of the partial results of any pair of a sequence whose pairs
+// have nt tiles each and span flat tiles [lo, hi): a pair meets at most
+// nt / ws + 2 static ranges, and at most as many pool pieces as the
+// sequence's range meets (and no more than its own tiles).
+__device__ __forceinline__ int seq_cand_bound(int nt, int lo, int hi, const StepPlan& pl) {
+  if (nt <= 0) return 0;
+  int ub = 0;
+  if (lo < pl.ts) ub += min(nt, nt / pl.ws + 2);
+  if (hi > pl.ts) {
+    const int first = piece_of(max(lo, pl.ts), pl), last = piece_of(hi - 1, pl);
+    ub += min(nt, last - first + 1);
+  }
+  return ub;
 }
 
 }  // namespace pa

@@ -99,6 +99,10 @@ __device__ __forceinline__ void st_f32_hint(float* ptr, float v, uint64_t policy
   asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;" ::"l"(ptr), "f"(v), "l"(policy)
                : "memory");
 }
+__device__ __forceinline__ void st_s32_hint(int32_t* ptr, int32_t v, uint64_t policy) {
+  asm volatile("st.global.L2::cache_hint.s32 [%0], %1, %2;" ::"l"(ptr), "r"(v), "l"(policy)
+               : "memory");
+}
 __device__ __forceinline__ float ld_f32_hint(const float* ptr, uint64_t policy) {
   float v;
   asm volatile("ld.global.L2::cache_hint.f32 %0, [%1], %2;" : "=f"(v) : "l"(ptr), "l"(policy));
