@@ -9,8 +9,7 @@
 // atomicAdd each once their static range is done (the claim for the next
 // piece is issued a piece ahead, so the copy pipeline never drains). Warps on
 // SMs that get less bandwidth thus take fewer pieces and all warps finish
-// together; the pool ends with one-tile pieces, so when it runs dry no warp
-// holds more than a tile or two. The pool only covers the trailing run of
+// together. The pool only covers the trailing run of
 // sequences no longer than four times the mean, so a long sequence is never
 // cut into small pieces (plan.cuh). A run of one warp's tiles inside one pair
 // is a segment; each segment writes one partial (running max m, running sum
@@ -216,8 +215,7 @@ __global__ void __launch_bounds__(WARPS * 32, 2)
     const uint64_t keep = l2_evict_last();
     int32_t* dst = a.plan;
     if (tid < kPlanScalars) {
-      const int v[kPlanScalars] = {pl.total, pl.ws, pl.ts, pl.piece, pl.hh, pl.n_head,
-                                   pl.n_pool, 0};
+      const int v[kPlanScalars] = {pl.total, pl.ws, pl.ts, pl.piece, pl.n_pool, 0, 0, 0};
       st_s32_hint(dst + tid, v[tid], keep);
     }
     for (int b = tid; b <= a.B; b += blockDim.x) st_s32_hint(dst + kPlanScalars + b, s_pref[b], keep);

@@ -25,8 +25,8 @@ __host__ __device__ constexpr inline int part_stride(int G, int D) {
 //   plan  int32 [plan_words(B)] at offset 256: the step's plan, written by the
 //         decode kernel's first CTA before it streams, read by the merge
 //         kernel: kPlanScalars scalars (tiles, static tiles per warp, end of
-//         the static region, head piece size, head tiles, head pieces, all
-//         pieces), the tile prefix over the sequences (B + 1), and the prefix
+//         the static region, piece size, pieces, unused), the tile prefix
+//         over the sequences (B + 1), and the prefix
 //         of "wide" columns over the sequences (B + 1): all columns of a
 //         sequence where some pair may have more than kMergeNarrow partials
 //   part  f32 [NSLOT][part_stride(CG, D)]: acc[CG][D], m[CG], l[CG], padding

@@ -6,13 +6,13 @@
 // Every (sequence b, virtual KV head) pair owns the 16-token tiles covering
 // its read range [start, L); all tiles form one flat, pair-major index space.
 // Its first part is split into equal static ranges of `ws` tiles, one per
-// worker warp (ending at `ts`); the rest is a pool of pieces claimed
-// dynamically, in order: "head" pieces of `piece` tiles, then "tail" pieces of
-// one tile each (about one per warp). A warp streams only a few GB/s, so the
-// work a warp holds when the pool runs dry sets the kernel's tail: ending the
-// pool with one-tile pieces keeps that to a tile or two. The pool only covers
-// the trailing run of sequences whose tile count is at most four times the
-// mean, so a long sequence is never cut into many small pieces.
+// worker warp (ending at `ts`); the rest is a pool of pieces of `piece`
+// tiles claimed dynamically. The pool only covers the trailing run of
+// sequences whose tile count is at most four times the mean, so a long
+// sequence is never cut into many small pieces. (Ending the pool with
+// one-tile pieces, so that a warp holds less work when it runs dry, gave the
+// last pairs up to 157 partials and made the step 2 us slower through the
+// merge.)
 #pragma once
 
 #include "pa_internal.h"
@@ -39,27 +39,19 @@ struct StepPlan {
   int total;   // tiles of all pairs
   int ws;      // static tiles per warp
   int ts;      // end of the static region
-  int piece;   // tiles per head piece of the pool
-  int hh;      // tiles of the pool's head part (pool tiles [ts, ts + hh))
-  int n_head;  // head pieces: ceil(hh / piece)
-  int n_pool;  // all pieces: n_head + (total - ts - hh) one-tile tail pieces
+  int piece;   // tiles per pool piece
+  int n_pool;  // pool pieces: ceil((total - ts) / piece)
 };
 
 // Pool piece holding flat tile f (ts <= f < total).
 __device__ __forceinline__ int piece_of(int f, const StepPlan& pl) {
-  const int t = f - pl.ts;
-  return t < pl.hh ? t / pl.piece : pl.n_head + (t - pl.hh);
+  return (f - pl.ts) / pl.piece;
 }
 
 // First flat tile and end of pool piece i (i < n_pool).
 __device__ __forceinline__ void piece_range(int i, const StepPlan& pl, int* f0, int* f1) {
-  if (i < pl.n_head) {
-    *f0 = pl.ts + i * pl.piece;
-    *f1 = pl.ts + min((i + 1) * pl.piece, pl.hh);
-  } else {
-    *f0 = pl.ts + pl.hh + (i - pl.n_head);
-    *f1 = *f0 + 1;
-  }
+  *f0 = pl.ts + i * pl.piece;
+  *f1 = min(*f0 + pl.piece, pl.total);
 }
 
 // Block-wide: every thread of the block calls it (it synchronises the
@@ -120,38 +112,21 @@ __device__ inline StepPlan plan_step(const PlanIn& p, int* s_len, int* s_pref) {
   r.ts = static_cast<int>(
       min(static_cast<long long>(r.ws) * p.nw, static_cast<long long>(r.total)));
   const int pool_tiles = r.total - r.ts;
-  // one-tile tail pieces: about one per warp, at most half of the slots
-  int tail = min(pool_tiles, min(p.nw, p.np_max / 2));
-  r.hh = pool_tiles - tail;
-  const int head_slots = p.np_max - tail;  // >= np_max / 2 >= 1
-  r.piece = static_cast<int>((static_cast<unsigned>(r.hh) + head_slots - 1u) /
-                             static_cast<unsigned>(head_slots));
+  r.piece = static_cast<int>((static_cast<unsigned>(pool_tiles) + p.np_max - 1u) /
+                             static_cast<unsigned>(p.np_max));
   if (r.piece < p.piece_min) r.piece = p.piece_min;
-  r.n_head = static_cast<int>((static_cast<unsigned>(r.hh) + r.piece - 1u) /
+  r.n_pool = static_cast<int>((static_cast<unsigned>(pool_tiles) + r.piece - 1u) /
                               static_cast<unsigned>(r.piece));
-  r.n_pool = r.n_head + tail;
   return r;
 }
 
-__device__ __forceinline__ void plan_store(int32_t* dst, const StepPlan& pl) {
-  dst[0] = pl.total;
-  dst[1] = pl.ws;
-  dst[2] = pl.ts;
-  dst[3] = pl.piece;
-  dst[4] = pl.hh;
-  dst[5] = pl.n_head;
-  dst[6] = pl.n_pool;
-  dst[7] = 0;
-}
 __device__ __forceinline__ StepPlan plan_load(const int32_t* src) {
   StepPlan pl;
   pl.total = src[0];
   pl.ws = src[1];
   pl.ts = src[2];
   pl.piece = src[3];
-  pl.hh = src[4];
-  pl.n_head = src[5];
-  pl.n_pool = src[6];
+  pl.n_pool = src[4];
   return pl;
 }
 
