@@ -240,6 +240,13 @@ __global__ void __launch_bounds__(WARPS * 32, 2)
       }
       if (lane == 0) st_s32_hint(wd, 0, keep);
     }
+    // publish it: merge CTAs that start before this kernel ends may then
+    // load it before their dependency wait
+    __syncthreads();
+    if (tid == 0) {
+      __threadfence();
+      st_release_gpu(reinterpret_cast<int32_t*>(a.pool) + 1, 1);
+    }
   }
   const int w = blockIdx.x * WARPS + warp;
   const int f0 = static_cast<int>(min(static_cast<long long>(w) * ws, static_cast<long long>(ts)));

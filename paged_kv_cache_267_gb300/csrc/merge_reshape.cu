@@ -30,9 +30,10 @@ cudaError_t device_error_word(int32_t** ptr) {
 //
 // The plan of the step (how the decode kernel split the tiles, and which
 // sequences have pairs with many partials) comes from the decode kernel's
-// first CTA through the workspace, so the merge needs one load of it after the
-// decode kernel ends (it is launched as its programmatic dependent) instead
-// of computing it again in every CTA. Columns of sequences where some pair
+// first CTA through the workspace (no CTA computes it again), behind a
+// release/acquire flag, so that the merge CTAs, which start before the
+// decode kernel ends (the merge is launched as its programmatic dependent),
+// know their columns when their wait returns. Columns of sequences where some pair
 // may have more than eight partials (pairs cut into pool pieces, or spanning
 // many warps' static ranges) are "wide": each goes to one whole CTA, whose
 // eight warps fold one eighth of the partials each and combine their results
@@ -40,6 +41,8 @@ cudaError_t device_error_word(int32_t** ptr) {
 // its partials online with eight loads in flight per lane (D <= 128; four for
 // D = 256).
 constexpr int kMergeThreads = 256;
+constexpr int kPlanPolls = 64;       // polls of the plan flag before the wait, at most
+constexpr int kPlanPollNs = 500;     // pause between polls
 constexpr int kMergeWarps = kMergeThreads / 32;
 
 // Per-lane state of one column: head dims v * 128 + 4 * lane .. + 3 for
@@ -170,9 +173,36 @@ __global__ void __launch_bounds__(kMergeThreads, 3) merge_kernel(const MergeArgs
   int* s_wide = s_pref + a.B + 1;                                       // B + 1 prefix of wide columns
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-  griddep_wait();  // the decode kernel's plan and partials are complete and visible
-  if (blockIdx.x == 0 && tid == 0) *a.pool = 0u;
-  for (int i = tid; i < plan_words(a.B); i += blockDim.x) s_plan[i] = a.plan[i];
+  // The decode kernel's first CTA publishes the plan a few microseconds
+  // after it starts, long before the decode kernel ends. A CTA that sees the
+  // flag set (it polls a bounded number of times) loads the plan and works
+  // out its columns and their partials' slots before the dependency wait;
+  // each thread waits right before its first load of a partial, so that
+  // after the wait only the partials are a round trip away. A CTA that gives
+  // up polling loads the plan after the wait. Each CTA counts itself in
+  // pool[2] once it has read the flag; the last one clears flag and count
+  // after the wait (the decode kernel has then set the flag, and no CTA of
+  // this grid reads it again), so a flag seen set always belongs to this
+  // step.
+  int32_t* const flag = reinterpret_cast<int32_t*>(a.pool) + 1;
+  uint32_t* const checked = a.pool + 2;
+  int early = 0;
+  bool last = false;
+  if (tid == 0) {
+    for (int i = 0; i < kPlanPolls; ++i) {
+      early = ld_acquire_gpu(flag) == 1;
+      if (early) break;
+      __nanosleep(kPlanPollNs);
+    }
+    last = atomicAdd(checked, 1u) == gridDim.x - 1;
+  }
+  early = __syncthreads_or(early);
+  if (early) {
+    for (int i = tid; i < plan_words(a.B); i += blockDim.x) s_plan[i] = ld_relaxed_gpu(a.plan + i);
+  } else {
+    griddep_wait();  // the decode kernel's plan and partials are complete and visible
+    for (int i = tid; i < plan_words(a.B); i += blockDim.x) s_plan[i] = a.plan[i];
+  }
   __syncthreads();
   const StepPlan pl = plan_load(s_plan);
   const int HC = a.Hv * a.CG;  // columns per sequence
@@ -193,6 +223,7 @@ __global__ void __launch_bounds__(kMergeThreads, 3) merge_kernel(const MergeArgs
     };
     const int gsz = c.ncand > 0 ? (c.ncand + kMergeWarps - 1) / kMergeWarps : 1;
     const int ngrp = c.ncand > 0 ? (c.ncand + gsz - 1) / gsz : 0;
+    griddep_wait();  // the partials are complete and visible
     if (warp < ngrp) {
       HeadAcc<VPL> r;
       merge_fold(a, slot, warp * gsz, min((warp + 1) * gsz, c.ncand), c.h, r);
@@ -250,8 +281,18 @@ __global__ void __launch_bounds__(kMergeThreads, 3) merge_kernel(const MergeArgs
       return k < c.cd.na ? c.s + c.cd.w0 + k : S + a.NW + c.s + c.cd.i0 + (k - c.cd.na);
     };
     HeadAcc<VPL> r;
+    griddep_wait();  // the partials are complete and visible
     merge_fold(a, slot, 0, c.ncand, c.h, r);
     store_head<OT, VPL>(a, c.orow, r, c.ncand == 0);
+  }
+  // the counters are zero between calls
+  if (tid == 0 && (blockIdx.x == 0 || last)) {
+    griddep_wait();
+    if (blockIdx.x == 0) *a.pool = 0u;
+    if (last) {
+      st_relaxed_gpu(flag, 0);
+      *checked = 0u;
+    }
   }
 }
 

@@ -20,8 +20,11 @@ __host__ __device__ constexpr inline int part_stride(int G, int D) {
 }
 
 // Decode workspace layout (device memory, all sections 256-byte aligned):
-//   pool  u32 at offset 0: pool piece counter; zero between calls (the merge
-//         kernel resets it after each step), at the same place for any shape
+//   pool  u32 [3] at offset 0, at the same place for any shape, all zero
+//         between calls (the merge kernel resets them after each step):
+//         [0] the pool piece counter; [1] the plan flag, set to 1 (release)
+//         by the decode kernel's first CTA once the plan below is stored;
+//         [2] the merge CTAs that have read the flag
 //   plan  int32 [plan_words(B)] at offset 256: the step's plan, written by the
 //         decode kernel's first CTA before it streams, read by the merge
 //         kernel: kPlanScalars scalars (tiles, static tiles per warp, end of

@@ -115,6 +115,24 @@ __device__ __forceinline__ float4 ld_f32x4_hint(const float* ptr, uint64_t polic
                : "l"(ptr), "l"(policy));
   return v;
 }
+// GPU-scope memory order for a flag between the CTAs of two kernels that
+// run at the same time (a kernel and its programmatic dependent).
+__device__ __forceinline__ void st_release_gpu(int32_t* ptr, int32_t v) {
+  asm volatile("st.release.gpu.global.s32 [%0], %1;" ::"l"(ptr), "r"(v) : "memory");
+}
+__device__ __forceinline__ void st_relaxed_gpu(int32_t* ptr, int32_t v) {
+  asm volatile("st.relaxed.gpu.global.s32 [%0], %1;" ::"l"(ptr), "r"(v) : "memory");
+}
+__device__ __forceinline__ int32_t ld_acquire_gpu(const int32_t* ptr) {
+  int32_t v;
+  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(ptr) : "memory");
+  return v;
+}
+__device__ __forceinline__ int32_t ld_relaxed_gpu(const int32_t* ptr) {
+  int32_t v;
+  asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(ptr) : "memory");
+  return v;
+}
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
