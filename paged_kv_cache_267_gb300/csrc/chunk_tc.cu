@@ -332,15 +332,19 @@ __global__ void __launch_bounds__(Smem<FP8>::kThreads, 1)
     constexpr uint32_t idO = tc::idesc_f16(kRows, kHd, kBf16, true);
     // S_X = Q_X . K_n^T over head dims [64 b0, 64 b1) (4 steps of 16 per
     // 64-dim box); the commit once all 8 steps are issued
+    // descriptors of the tiles' starts; a step's operand is the start plus a
+    // constant (in 16-byte units, within the 14-bit address field)
+    const uint64_t dQ0 = tc::sdesc_sw128(sQ, 16, 1024);
     auto issue_s_part = [&](int x, int n, int b0, int b1) {
       if (lane == 0) {
-        const uint32_t kt = tile_k(n);
+        const uint64_t dQ = dQ0 + ((x * kQBytes) >> 4);
+        const uint64_t dK = tc::sdesc_sw128(tile_k(n), 16, 1024);
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
           if (ks < 4 * b0 || ks >= 4 * b1) continue;
           const uint32_t box = ks >> 2, kk = (ks & 3) * 32;
-          const uint64_t ad = tc::sdesc_sw128(sQ + x * kQBytes + box * 16384 + kk, 16, 1024);
-          const uint64_t bd = tc::sdesc_sw128(kt + box * kBoxBytes + kk, 16, 1024);
+          const uint64_t ad = dQ + ((box * 16384 + kk) >> 4);
+          const uint64_t bd = dK + ((box * kBoxBytes + kk) >> 4);
           tc::mma_f16(tmem + kColS + 128 * x, ad, bd, idS, ks > 0);
         }
         if (b1 == 2) tc::commit(bar(kBarS + x));
@@ -352,10 +356,10 @@ __global__ void __launch_bounds__(Smem<FP8>::kThreads, 1)
     // 0-31 and 64-95 of S_X, 8 columns (16 tokens) per step
     auto issue_o = [&](int x, int n) {
       if (lane == 0) {
-        const uint32_t vt = tile_v(n);
+        const uint64_t dV = tc::sdesc_sw128(tile_v(n), kBoxBytes, 1024);
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
-          const uint64_t bd = tc::sdesc_sw128(vt + ks * 2048, kBoxBytes, 1024);
+          const uint64_t bd = dV + ((ks * 2048) >> 4);
           const uint32_t pc = ks < 4 ? 8 * ks : 32 + 8 * ks;  // P columns of tokens 16 ks ..
           tc::mma_f16_ta(tmem + kColO + 128 * x, tmem + kColS + 128 * x + pc, bd, idO,
                          (n > 0 || ks > 0) ? 1u : 0u);
