@@ -199,6 +199,65 @@ __device__ __forceinline__ void unit_of_cta(const ChunkArgs& a, int cta, int* s_
   *kvh = i % a.Hkv;
 }
 
+
+// Eight M128 K16 steps of one product group from one asm block, A and B in
+// shared memory: step k reads A at descriptor a + a_off(k) and B at
+// b + b_off(k) (offsets in 16-byte units, added to the low half: the
+// address field cannot carry), the first step overwrites D, the others
+// accumulate.
+__device__ __forceinline__ void mma8_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc) {
+  const uint32_t alo = static_cast<uint32_t>(a), ahi = static_cast<uint32_t>(a >> 32);
+  const uint32_t blo = static_cast<uint32_t>(b), bhi = static_cast<uint32_t>(b >> 32);
+  asm volatile(
+      "{\n.reg .pred p0, p1;\n.reg .b32 al, bl;\n.reg .b64 ad, bd;\n"
+      "setp.ne.b32 p0, 0, 0;\nsetp.eq.b32 p1, 0, 0;\n"
+      "mov.b64 ad, {%1, %2};\nmov.b64 bd, {%3, %4};\n"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %5, p0;\n"
+      "add.u32 al, %1, 2;\nadd.u32 bl, %3, 2;\nmov.b64 ad, {al, %2};\nmov.b64 bd, {bl, %4};\n"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %5, p1;\n"
+      "add.u32 al, %1, 4;\nadd.u32 bl, %3, 4;\nmov.b64 ad, {al, %2};\nmov.b64 bd, {bl, %4};\n"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %5, p1;\n"
+      "add.u32 al, %1, 6;\nadd.u32 bl, %3, 6;\nmov.b64 ad, {al, %2};\nmov.b64 bd, {bl, %4};\n"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %5, p1;\n"
+      "add.u32 al, %1, 1024;\nadd.u32 bl, %3, 1024;\nmov.b64 ad, {al, %2};\nmov.b64 bd, {bl, %4};\n"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %5, p1;\n"
+      "add.u32 al, %1, 1026;\nadd.u32 bl, %3, 1026;\nmov.b64 ad, {al, %2};\nmov.b64 bd, {bl, %4};\n"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %5, p1;\n"
+      "add.u32 al, %1, 1028;\nadd.u32 bl, %3, 1028;\nmov.b64 ad, {al, %2};\nmov.b64 bd, {bl, %4};\n"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %5, p1;\n"
+      "add.u32 al, %1, 1030;\nadd.u32 bl, %3, 1030;\nmov.b64 ad, {al, %2};\nmov.b64 bd, {bl, %4};\n"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %5, p1;\n}" ::"r"(d),
+      "r"(alo), "r"(ahi), "r"(blo), "r"(bhi), "r"(idesc)
+      : "memory");
+}
+// Eight M128 K16 steps with A in tensor memory: step k reads A at column
+// a + (k < 4 ? 8 k : 32 + 8 k) and B at descriptor b + 128 k; the first
+// step accumulates iff acc0 != 0, the others always.
+__device__ __forceinline__ void mma8_ts(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc,
+                                        uint32_t acc0) {
+  const uint32_t blo = static_cast<uint32_t>(b), bhi = static_cast<uint32_t>(b >> 32);
+  asm volatile(
+      "{\n.reg .pred p0, p1;\n.reg .b32 ac, bl;\n.reg .b64 bd;\n"
+      "setp.ne.b32 p0, %5, 0;\nsetp.eq.b32 p1, 0, 0;\n"
+      "mov.b64 bd, {%2, %3};\n"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], bd, %4, p0;\n"
+      "add.u32 ac, %1, 8;\nadd.u32 bl, %2, 128;\nmov.b64 bd, {bl, %3};\n"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [ac], bd, %4, p1;\n"
+      "add.u32 ac, %1, 16;\nadd.u32 bl, %2, 256;\nmov.b64 bd, {bl, %3};\n"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [ac], bd, %4, p1;\n"
+      "add.u32 ac, %1, 24;\nadd.u32 bl, %2, 384;\nmov.b64 bd, {bl, %3};\n"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [ac], bd, %4, p1;\n"
+      "add.u32 ac, %1, 64;\nadd.u32 bl, %2, 512;\nmov.b64 bd, {bl, %3};\n"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [ac], bd, %4, p1;\n"
+      "add.u32 ac, %1, 72;\nadd.u32 bl, %2, 640;\nmov.b64 bd, {bl, %3};\n"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [ac], bd, %4, p1;\n"
+      "add.u32 ac, %1, 80;\nadd.u32 bl, %2, 768;\nmov.b64 bd, {bl, %3};\n"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [ac], bd, %4, p1;\n"
+      "add.u32 ac, %1, 88;\nadd.u32 bl, %2, 896;\nmov.b64 bd, {bl, %3};\n"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [ac], bd, %4, p1;\n}" ::"r"(d),
+      "r"(a), "r"(blo), "r"(bhi), "r"(idesc), "r"(acc0)
+      : "memory");
+}
 template <int QT, bool FP8>
 __global__ void __launch_bounds__(Smem<FP8>::kThreads, 1)
     chunk_attn_tc128_kernel(const __grid_constant__ CUtensorMap tmK,
@@ -351,19 +410,25 @@ __global__ void __launch_bounds__(Smem<FP8>::kThreads, 1)
       }
       __syncwarp();
     };
-    auto issue_s = [&](int x, int n) { issue_s_part(x, n, 0, 2); };
+    auto issue_s = [&](int x, int n) {
+      if constexpr (FP8) {
+        issue_s_part(x, n, 0, 2);
+      } else {
+        if (lane == 0) {
+          mma8_ss(tmem + kColS + 128 * x, dQ0 + ((x * kQBytes) >> 4),
+                  tc::sdesc_sw128(tile_k(n), 16, 1024), idS);
+          tc::commit(bar(kBarS + x));
+        }
+        __syncwarp();
+      }
+    };
     // O_X (+)= P_X . V_n over 128 tokens (8 steps of 16); P_X in columns
     // 0-31 and 64-95 of S_X, 8 columns (16 tokens) per step
     auto issue_o = [&](int x, int n) {
       if (lane == 0) {
         const uint64_t dV = tc::sdesc_sw128(tile_v(n), kBoxBytes, 1024);
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-          const uint64_t bd = dV + ((ks * 2048) >> 4);
-          const uint32_t pc = ks < 4 ? 8 * ks : 32 + 8 * ks;  // P columns of tokens 16 ks ..
-          tc::mma_f16_ta(tmem + kColO + 128 * x, tmem + kColS + 128 * x + pc, bd, idO,
-                         (n > 0 || ks > 0) ? 1u : 0u);
-        }
+        // P columns of tokens 16 k ..: 8 k for k < 4, 32 + 8 k after
+        mma8_ts(tmem + kColO + 128 * x, tmem + kColS + 128 * x, dV, idO, n > 0 ? 1u : 0u);
         tc::commit(bar(kBarO + x));
       }
       __syncwarp();
