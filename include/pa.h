@@ -155,8 +155,9 @@ pa_status pa_reshape_and_cache(const pa_tensor* k, const pa_tensor* v,
  * so; ordinary kernels and copies are waited for in full.
  *
  * Workspace: the step writes per-segment partial results (running max, sum
- * and unnormalised output) and a piece counter to a
- * device workspace of pa_decode_workspace_size() bytes. It is the buffer
+ * and unnormalised output), its plan and three counter words (zero again
+ * when the step ends) to a device workspace of pa_decode_workspace_size()
+ * bytes. It is the buffer
  * given to pa_set_workspace() for the current device, or else a buffer the
  * library allocates (and zeroes) once per (device, stream) outside stream
  * capture and keeps. Calls that overlap on the GPU must not share a
