@@ -726,6 +726,20 @@ pa_status check_decode(const pa_tensor* out, const pa_tensor* q, const pa_tensor
 pa_status plan_call(DeviceState* st, const DecodeCall& c, DecodePlan* plan, WsLayout* layout) {
   pa_status s = plan_decode(st, c.ct, c.qt, c.T > 1, c.B, c.CG, static_cast<int>(c.D), plan);
   if (s) return s;
+  // No more worker warps than the step can fill at min_tiles each: its
+  // tiles are at most B * Hv pairs times the 16-token tiles of the longest
+  // read range the tables (or the window) allow, plus one for a window
+  // start inside a tile. Small batches then launch fewer CTAs and need
+  // less scratch; large ones keep the full grid.
+  int64_t span = c.MB * c.bs;
+  if (c.window > 0) span = std::min<int64_t>(span, int64_t(c.window) + c.T - 1);
+  const int64_t tiles = c.B * c.Hv * ((span + 15) / 16 + 1);
+  const int64_t warps = (tiles + plan->min_tiles - 1) / plan->min_tiles;
+  const int64_t ctas = (warps + plan->var.warps - 1) / plan->var.warps;
+  if (ctas < plan->grid) {
+    plan->grid = static_cast<int>(std::max<int64_t>(ctas, 1));
+    plan->workers = plan->grid * plan->var.warps;
+  }
   *layout = ws_layout(c.B, c.Hv, c.CG, static_cast<int>(c.D), plan->workers);
   return PA_OK;
 }
@@ -802,7 +816,12 @@ pa_status run_decode(const DecodeCall& c, DeviceState* st, const DecodePlan& pla
   m.NCG = a.NCG;
   m.CG = a.CG;
   m.Hv = a.Hv;
-  e = pa::merge_launch(c.qt, m, st->num_sms * 3, cs, !prof);
+  // three CTAs per SM, and no more than output columns (a wide column takes
+  // one CTA, a narrow one a warp)
+  const int64_t cols = static_cast<int64_t>(m.B) * m.Hv * m.CG;
+  const int merge_grid =
+      static_cast<int>(std::min<int64_t>(int64_t(st->num_sms) * 3, std::max<int64_t>(cols, 1)));
+  e = pa::merge_launch(c.qt, m, merge_grid, cs, !prof);
   if (e != cudaSuccess) {
     if (wsp) {
       std::lock_guard<std::mutex> lk(g_mu);

@@ -105,8 +105,10 @@ def test_noalloc_on_named_workloads(name, pa_lib):
 
 
 def test_noalloc_rejects_steps_beyond_its_scratch(pa_lib):
-    # G = 16 with head_dim 256 needs far more partial storage than 32 MiB
-    w = generate(_spec(num_q_heads=16, num_kv_heads=1, head_dim=256, seq_lens=(100, 3000)),
+    # G = 16 with head_dim 256 (16.5 KB per partial slot) on 16 sequences of
+    # 3000 tokens: enough tiles to keep the decode grid at its full size,
+    # whose worker slots alone need more than 32 MiB
+    w = generate(_spec(num_q_heads=16, num_kv_heads=1, head_dim=256, seq_lens=(3000,) * 16),
                  device="cuda")
     bt = torch.from_numpy(w.block_tables).cuda()
     sl = torch.from_numpy(w.seq_lens).cuda()
