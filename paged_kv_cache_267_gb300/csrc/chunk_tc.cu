@@ -174,8 +174,10 @@ __device__ __forceinline__ int unit_tiles(const ChunkArgs& a, int L, int cap, in
 // drops by about 7% against the plain (sequence, KV head, unit) order).
 // Sequences are ranked by the tiles of their last unit (most first, then by
 // index); within one, units from the last (the most causal work) down, each
-// for every KV head. Block-wide: every thread calls it; *s_b receives the
-// sequence.
+// for every KV head. Ranking costs every thread O(B) loads, so beyond
+// kRankMax sequences they go in index order. Block-wide: every thread calls
+// it; *s_b receives the sequence.
+constexpr int kRankMax = 64;
 __device__ __forceinline__ void unit_of_cta(const ChunkArgs& a, int cta, int* s_b, int* b,
                                             int* kvh, int* ut) {
   const int cap = a.MB * a.bs;
@@ -184,7 +186,8 @@ __device__ __forceinline__ void unit_of_cta(const ChunkArgs& a, int cta, int* s_
   const int i = cta - r * per_seq;
   const int nrows = a.T * a.G;
   const int lr0 = (a.QT - 1) * kUnitRows, lr1 = nrows;  // the last unit's rows
-  for (int c = threadIdx.x; c < a.B; c += blockDim.x) {
+  if (a.B > kRankMax && threadIdx.x == 0) *s_b = r;
+  for (int c = threadIdx.x; a.B <= kRankMax && c < a.B; c += blockDim.x) {
     const int wc = unit_tiles(a, __ldg(a.seq_lens + c), cap, lr0, lr1);
     int rank = 0;
     for (int o = 0; o < a.B; ++o) {

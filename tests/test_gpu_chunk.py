@@ -159,6 +159,29 @@ def test_chunk_kernels_forced(case, path, pa_lib):
     assert pa_lib.check_device_error() == 0
 
 
+@pytest.mark.parametrize("B", [60, 300], ids=["ranked", "index_order"])
+def test_tensor_memory_chunk_large_batch(B, pa_lib):
+    """The tensor-memory kernel hands its units out heaviest first when the
+    batch has at most 64 sequences (ranked by every CTA, equal weights
+    by index) and in sequence order beyond that: both against the oracle, on
+    batches of few distinct lengths (many equal weights), some shorter than
+    the chunk (their early queries attend to nothing)."""
+    rng = np.random.default_rng(B)
+    lens = tuple(int(x) for x in rng.choice([1, 7, 40, 100, 100, 100, 180], size=B))
+    pa_lib.set_prefill_path(2)
+    try:
+        sides = run_chunk(_spec(8, 32, 8, 128, 16, 0, "bf16", False, lens=lens, seed=2700 + B))
+    finally:
+        pa_lib.set_prefill_path(0)
+    got = out_f64(sides.out)
+    assert_close(got, sides.ref, what=f"B{B}", rel=CHUNK_REL_TOL)
+    for b, L in enumerate(sides.w.seq_lens):
+        for t in range(8):
+            if L - 8 + t < 0:
+                assert (got[b, t] == 0).all()
+    assert pa_lib.check_device_error() == 0
+
+
 SCALES = [
     # scale, cache: a negative scale (the tensor-memory kernel flips Q's sign
     # to take the row max on raw scores), zero (uniform weights; masked
