@@ -163,6 +163,39 @@ __device__ __forceinline__ MergeCol merge_col(const MergeArgs& a, const StepPlan
   return c;
 }
 
+// Combines the results of ngrp warps (shared-memory rows s_grp[w0 ..
+// w0 + ngrp)) and stores the column (zeros when ngrp == 0).
+template <int OT, int VPL>
+__device__ __forceinline__ void combine_groups(const MergeArgs& a, const float* s_grp, int w0,
+                                               int ngrp, size_t orow) {
+  constexpr int ROW = VPL * 128 + 4;
+  const int lane = threadIdx.x & 31;
+  HeadAcc<VPL> r;
+  r.M = -INFINITY;
+  r.den = 0.f;
+#pragma unroll
+  for (int v = 0; v < VPL; ++v) r.acc[v] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int j = 0; j < ngrp; ++j) {
+    const float* g = s_grp + (w0 + j) * ROW;
+    const float mj = g[VPL * 128], dj = g[VPL * 128 + 1];
+    const float Mn = fmaxf(r.M, mj);
+    const float sc = fast_exp2(r.M - Mn), f = fast_exp2(mj - Mn);
+    r.den = r.den * sc + f * dj;
+    if (4 * lane < a.D) {
+#pragma unroll
+      for (int v = 0; v < VPL; ++v) {
+        const float4 o = *reinterpret_cast<const float4*>(g + v * 128 + 4 * lane);
+        r.acc[v].x = r.acc[v].x * sc + f * o.x;
+        r.acc[v].y = r.acc[v].y * sc + f * o.y;
+        r.acc[v].z = r.acc[v].z * sc + f * o.z;
+        r.acc[v].w = r.acc[v].w * sc + f * o.w;
+      }
+    }
+    r.M = Mn;
+  }
+  store_head<OT, VPL>(a, orow, r, ngrp == 0);
+}
+
 template <int OT, int VPL>
 __global__ void __launch_bounds__(kMergeThreads, 3) merge_kernel(const MergeArgs a) {
   constexpr int ROW = VPL * 128 + 4;  // floats per group result in shared memory
@@ -170,7 +203,8 @@ __global__ void __launch_bounds__(kMergeThreads, 3) merge_kernel(const MergeArgs
   float* s_grp = s_dyn;                                                 // [8][ROW]
   int* s_plan = reinterpret_cast<int*>(s_dyn + kMergeWarps * ROW);      // plan_words(B)
   int* s_pref = s_plan + kPlanScalars;                                  // B + 1
-  int* s_wide = s_pref + a.B + 1;                                       // B + 1 prefix of wide columns
+  int* s_wide = s_pref + a.B + 1;                                       // B + 1, see below
+  __shared__ int s_red[kMergeWarps];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   // The decode kernel's first CTA publishes the plan a few microseconds
@@ -208,64 +242,97 @@ __global__ void __launch_bounds__(kMergeThreads, 3) merge_kernel(const MergeArgs
   const int HC = a.Hv * a.CG;  // columns per sequence
   const int S = a.B * a.Hv;
 
-  // ---- wide columns: one CTA each
-  const int n_wide = s_wide[a.B];
+  // Wide columns, counted in half-CTA units (this CTA's own layout; the one
+  // the decode kernel stored is not used): a column whose pairs may have
+  // more than 4 * kMergeNarrow partials takes a whole CTA (two units; its
+  // eight warps fold an eighth of the partials each), more than kMergeNarrow
+  // a half (one unit; its four warps fold a quarter each), the others one
+  // warp in the narrow phase below. Every sequence has an even number of
+  // units, so a CTA's two units belong to one sequence. s_wide[b] = (first
+  // unit of sequence b) << 2 | its class (0 narrow, 1 half, 2 whole);
+  // s_wide[B] = units << 2.
+  {
+    int carry = 0;
+    for (int b0 = 0; b0 < a.B; b0 += blockDim.x) {
+      const int b = b0 + tid;
+      int cls = 0, x = 0;
+      if (b < a.B) {
+        const int nt = s_pref[b + 1] - s_pref[b];
+        const int ub = pair_cand_bound(nt, a.Hv * s_pref[b], a.Hv * s_pref[b + 1], pl);
+        cls = ub > 4 * kMergeNarrow ? 2 : (ub > kMergeNarrow ? 1 : 0);
+        x = cls == 2 ? 2 * HC : (cls == 1 ? HC + (HC & 1) : 0);
+      }
+      int y = x;  // inclusive scan over the warp, then over the CTA
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, y, o);
+        if (lane >= o) y += t;
+      }
+      if (lane == 31) s_red[warp] = y;
+      __syncthreads();
+      int before = 0, all = 0;
+#pragma unroll
+      for (int w = 0; w < kMergeWarps; ++w) {
+        const int t = s_red[w];
+        before += w < warp ? t : 0;
+        all += t;
+      }
+      if (b < a.B) s_wide[b] = ((carry + before + y - x) << 2) | cls;
+      carry += all;
+      __syncthreads();  // s_red is reused
+    }
+    if (tid == 0) s_wide[a.B] = carry << 2;
+    __syncthreads();
+  }
+  const int n_wide = ((s_wide[a.B] >> 2) + 1) >> 1;  // CTA units
   for (int cu = blockIdx.x; cu < n_wide; cu += gridDim.x) {
-    int lo = 0, hi = a.B;  // largest b with s_wide[b] <= cu
+    int lo = 0, hi = a.B;  // the sequence of units 2 cu, 2 cu + 1
     while (hi - lo > 1) {
       const int mid = (lo + hi) >> 1;
-      if (s_wide[mid] <= cu) lo = mid; else hi = mid;
+      if ((s_wide[mid] >> 2) <= 2 * cu) lo = mid; else hi = mid;
     }
-    const MergeCol c = merge_col(a, pl, s_pref, lo, cu - s_wide[lo]);
-    if (c.pad) continue;  // uniform over the CTA
-    auto slot = [&](int k) -> int {
-      return k < c.cd.na ? c.s + c.cd.w0 + k : S + a.NW + c.s + c.cd.i0 + (k - c.cd.na);
-    };
-    const int gsz = c.ncand > 0 ? (c.ncand + kMergeWarps - 1) / kMergeWarps : 1;
-    const int ngrp = c.ncand > 0 ? (c.ncand + gsz - 1) / gsz : 0;
-    griddep_wait();  // the partials are complete and visible
-    if (warp < ngrp) {
-      HeadAcc<VPL> r;
-      merge_fold(a, slot, warp * gsz, min((warp + 1) * gsz, c.ncand), c.h, r);
-      float* g = s_grp + warp * ROW;
-      if (4 * lane < a.D) {
+    const bool whole = (s_wide[lo] & 3) == 2;
+    const int first = s_wide[lo] >> 2;
+    const int half = warp >> 2;
+    const int col = whole ? (2 * cu - first) >> 1 : 2 * cu + half - first;
+    const int w0 = whole ? 0 : 4 * half;  // the group's first warp
+    const int nwg = whole ? kMergeWarps : kMergeWarps / 2;
+    bool active = col < HC;  // an odd HC pads a half-column sequence by one unit
+    MergeCol c;
+    if (active) {
+      c = merge_col(a, pl, s_pref, lo, col);
+      active = !c.pad;
+    }
+    int ngrp = 0;
+    if (active) {
+      auto slot = [&](int k) -> int {
+        return k < c.cd.na ? c.s + c.cd.w0 + k : S + a.NW + c.s + c.cd.i0 + (k - c.cd.na);
+      };
+      const int gsz = c.ncand > 0 ? (c.ncand + nwg - 1) / nwg : 1;
+      ngrp = c.ncand > 0 ? (c.ncand + gsz - 1) / gsz : 0;
+      const int wi = warp - w0;
+      griddep_wait();  // the partials are complete and visible
+      if (wi < ngrp) {
+        HeadAcc<VPL> r;
+        merge_fold(a, slot, wi * gsz, min((wi + 1) * gsz, c.ncand), c.h, r);
+        float* g = s_grp + warp * ROW;
+        if (4 * lane < a.D) {
 #pragma unroll
-        for (int v = 0; v < VPL; ++v)
-          *reinterpret_cast<float4*>(g + v * 128 + 4 * lane) = r.acc[v];
-      }
-      if (lane == 0) {
-        g[VPL * 128] = r.M;
-        g[VPL * 128 + 1] = r.den;
+          for (int v = 0; v < VPL; ++v)
+            *reinterpret_cast<float4*>(g + v * 128 + 4 * lane) = r.acc[v];
+        }
+        if (lane == 0) {
+          g[VPL * 128] = r.M;
+          g[VPL * 128 + 1] = r.den;
+        }
       }
     }
     __syncthreads();
-    if (warp == 0) {
-      HeadAcc<VPL> r;
-      r.M = -INFINITY;
-      r.den = 0.f;
-#pragma unroll
-      for (int v = 0; v < VPL; ++v) r.acc[v] = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int j = 0; j < ngrp; ++j) {
-        const float* g = s_grp + j * ROW;
-        const float mj = g[VPL * 128], dj = g[VPL * 128 + 1];
-        const float Mn = fmaxf(r.M, mj);
-        const float sc = fast_exp2(r.M - Mn), f = fast_exp2(mj - Mn);
-        r.den = r.den * sc + f * dj;
-        if (4 * lane < a.D) {
-#pragma unroll
-          for (int v = 0; v < VPL; ++v) {
-            const float4 o = *reinterpret_cast<const float4*>(g + v * 128 + 4 * lane);
-            r.acc[v].x = r.acc[v].x * sc + f * o.x;
-            r.acc[v].y = r.acc[v].y * sc + f * o.y;
-            r.acc[v].z = r.acc[v].z * sc + f * o.z;
-            r.acc[v].w = r.acc[v].w * sc + f * o.w;
-          }
-        }
-        r.M = Mn;
-      }
-      store_head<OT, VPL>(a, c.orow, r, ngrp == 0);
+    if (active && warp == w0) {
+      griddep_wait();
+      combine_groups<OT, VPL>(a, s_grp, w0, ngrp, c.orow);
     }
-    __syncthreads();  // s_grp is reused by the next wide column
+    __syncthreads();  // s_grp is reused by the next wide unit
   }
 
   // ---- narrow columns: one warp each. The CTAs that took a wide column in
@@ -274,7 +341,7 @@ __global__ void __launch_bounds__(kMergeThreads, 3) merge_kernel(const MergeArgs
   const int nwarps = gridDim.x * kMergeWarps;
   for (int u = rot * kMergeWarps + warp; u < a.B * HC; u += nwarps) {
     const int b = u / HC;
-    if (s_wide[b + 1] != s_wide[b]) continue;  // taken by the wide phase
+    if (s_wide[b] & 3) continue;  // taken by the wide phase
     const MergeCol c = merge_col(a, pl, s_pref, b, u - b * HC);
     if (c.pad) continue;
     auto slot = [&](int k) -> int {

@@ -166,4 +166,18 @@ __device__ __forceinline__ int seq_cand_bound(int nt, int lo, int hi, const Step
   return ub;
 }
 
+// Tighter bound of the partial results of any pair of such a sequence (used
+// by the merge kernel to size its column groups): a run of nt tiles also
+// meets at most nt / piece + 2 pool pieces.
+__device__ __forceinline__ int pair_cand_bound(int nt, int lo, int hi, const StepPlan& pl) {
+  if (nt <= 0) return 0;
+  int ub = 0;
+  if (lo < pl.ts) ub += min(nt, nt / pl.ws + 2);
+  if (hi > pl.ts) {
+    const int first = piece_of(max(lo, pl.ts), pl), last = piece_of(hi - 1, pl);
+    ub += min(min(nt, nt / pl.piece + 2), last - first + 1);
+  }
+  return ub;
+}
+
 }  // namespace pa
