@@ -28,18 +28,17 @@ cudaError_t device_error_word(int32_t** ptr) {
 // (single-query decode) or a (query, q head) of a chunk; columns that pad the
 // last group of a chunk have no output row and are skipped.
 //
-// The plan of the step (how the decode kernel split the tiles, and which
-// sequences have pairs with many partials) comes from the decode kernel's
-// first CTA through the workspace (no CTA computes it again), behind a
-// release/acquire flag, so that the merge CTAs, which start before the
-// decode kernel ends (the merge is launched as its programmatic dependent),
-// know their columns when their wait returns. Columns of sequences where some pair
-// may have more than eight partials (pairs cut into pool pieces, or spanning
-// many warps' static ranges) are "wide": each goes to one whole CTA, whose
-// eight warps fold one eighth of the partials each and combine their results
-// through shared memory. Every other column is one warp's work. A warp folds
-// its partials online with eight loads in flight per lane (D <= 128; four for
-// D = 256).
+// The plan of the step (how the decode kernel split the tiles) comes from
+// the decode kernel's first CTA through the workspace, so the merge reads
+// the tile prefix rather than recomputing it from seq_lens; a CTA that sees
+// the plan flag set loads it before its dependency wait (it is launched as
+// the decode kernel's programmatic dependent). From the plan each CTA sizes
+// the work of each sequence's columns by a bound of the partials of any of
+// its pairs (pair_cand_bound): up to 8, one warp per column; up to 32, four
+// warps of a CTA (two such columns per CTA); more, all eight warps of a CTA.
+// The warps of a group fold equal shares of the column's partials and
+// combine their results through shared memory. A warp folds its partials
+// online with eight loads in flight per lane (D <= 128; four for D = 256).
 constexpr int kMergeThreads = 256;
 constexpr int kPlanPolls = 64;       // polls of the plan flag before the wait, at most
 constexpr int kPlanPollNs = 500;     // pause between polls
