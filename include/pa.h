@@ -182,7 +182,7 @@ pa_status pa_decode(const pa_tensor* out, const pa_tensor* q, const pa_tensor* k
  * library; every GPU that loads the library holds that array until the
  * process exits. The call allocates and frees nothing (no cudaMalloc or
  * cudaFree, directly or through another library). The scratch a step needs
- * is about 512 + 8 * batch bytes of counters and plan, plus
+ * is about 512 + 4 * batch bytes of counters and plan, plus
  *   4 * (G * head_dim + 2 * G rounded up to 4) * (2 * batch * num_kv_heads + 5 * W)
  * bytes of partial results, where W is the number of worker warps of the
  * decode kernel: 2 * (SM count) * 4, or * 8 for e4m3 caches with head_dim 128

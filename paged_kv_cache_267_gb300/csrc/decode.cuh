@@ -219,27 +219,6 @@ __global__ void __launch_bounds__(WARPS * 32, 2)
       st_s32_hint(dst + tid, v[tid], keep);
     }
     for (int b = tid; b <= a.B; b += blockDim.x) st_s32_hint(dst + kPlanScalars + b, s_pref[b], keep);
-    if (warp == 0) {  // prefix of wide columns over the sequences
-      int32_t* wd = dst + kPlanScalars + a.B + 1;
-      const int HC = a.Hv * a.CG;
-      int run = 0;
-      for (int b0 = 0; b0 < a.B; b0 += 32) {
-        const int b = b0 + lane;
-        int x = 0;
-        if (b < a.B) {
-          const int nt = s_pref[b + 1] - s_pref[b];
-          x = seq_cand_bound(nt, a.Hv * s_pref[b], a.Hv * s_pref[b + 1], pl) > kMergeNarrow ? HC : 0;
-        }
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const int y = __shfl_up_sync(FULL, x, o);
-          if (lane >= o) x += y;
-        }
-        if (b < a.B) st_s32_hint(wd + b + 1, run + x, keep);
-        run += __shfl_sync(FULL, x, 31);
-      }
-      if (lane == 0) st_s32_hint(wd, 0, keep);
-    }
     // publish it: merge CTAs that start before this kernel ends may then
     // load it before their dependency wait
     __syncthreads();

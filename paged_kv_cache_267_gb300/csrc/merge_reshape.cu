@@ -202,7 +202,7 @@ __global__ void __launch_bounds__(kMergeThreads, 3) merge_kernel(const MergeArgs
   float* s_grp = s_dyn;                                                 // [8][ROW]
   int* s_plan = reinterpret_cast<int*>(s_dyn + kMergeWarps * ROW);      // plan_words(B)
   int* s_pref = s_plan + kPlanScalars;                                  // B + 1
-  int* s_wide = s_pref + a.B + 1;                                       // B + 1, see below
+  int* s_wide = s_plan + plan_words(a.B);                               // B + 1, see below
   __shared__ int s_red[kMergeWarps];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
@@ -241,8 +241,7 @@ __global__ void __launch_bounds__(kMergeThreads, 3) merge_kernel(const MergeArgs
   const int HC = a.Hv * a.CG;  // columns per sequence
   const int S = a.B * a.Hv;
 
-  // Wide columns, counted in half-CTA units (this CTA's own layout; the one
-  // the decode kernel stored is not used): a column whose pairs may have
+  // Wide columns, counted in half-CTA units: a column whose pairs may have
   // more than 4 * kMergeNarrow partials takes a whole CTA (two units; its
   // eight warps fold an eighth of the partials each), more than kMergeNarrow
   // a half (one unit; its four warps fold a quarter each), the others one
@@ -368,7 +367,7 @@ cudaError_t merge_launch(int out_type, const MergeArgs& a, int grid, cudaStream_
   cfg.blockDim = dim3(kMergeThreads);
   const int row = (a.D > 128 ? 2 : 1) * 128 + 4;
   cfg.dynamicSmemBytes = static_cast<size_t>(kMergeWarps) * row * sizeof(float) +
-                         static_cast<size_t>(plan_words(a.B)) * sizeof(int);
+                         static_cast<size_t>(plan_words(a.B) + a.B + 1) * sizeof(int);
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

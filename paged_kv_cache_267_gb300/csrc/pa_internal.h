@@ -28,10 +28,8 @@ __host__ __device__ constexpr inline int part_stride(int G, int D) {
 //   plan  int32 [plan_words(B)] at offset 256: the step's plan, written by the
 //         decode kernel's first CTA before it streams, read by the merge
 //         kernel: kPlanScalars scalars (tiles, static tiles per warp, end of
-//         the static region, piece size, pieces, unused), the tile prefix
-//         over the sequences (B + 1), and the prefix
-//         of "wide" columns over the sequences (B + 1): all columns of a
-//         sequence where some pair may have more than kMergeNarrow partials
+//         the static region, piece size, pieces, unused) and the tile prefix
+//         over the sequences (B + 1)
 //   part  f32 [NSLOT][part_stride(CG, D)]: acc[CG][D], m[CG], l[CG], padding
 //         to a multiple of 4 floats so every slot starts 16-byte aligned
 // with S = B * Hv pairs, NW worker warps, NSLOT = 2 S + NW + NPMAX. For
@@ -41,7 +39,7 @@ __host__ __device__ constexpr inline int part_stride(int G, int D) {
 // S + NW + s + i. Both are unique because the walk through the (pair, warp)
 // and (pair, piece) grids is a monotone staircase.
 constexpr int kPlanScalars = 8;
-__host__ __device__ constexpr inline int plan_words(int B) { return kPlanScalars + 2 * (B + 1); }
+__host__ __device__ constexpr inline int plan_words(int B) { return kPlanScalars + B + 1; }
 constexpr int kMergeNarrow = 8;  // partials one merge warp folds in one round trip
 
 struct DecodeArgs {

@@ -152,23 +152,10 @@ __device__ __forceinline__ Cands pair_cands(int F, int nt, const StepPlan& pl) {
 }
 
 // Upper bound of the partial results of any pair of a sequence whose pairs
-// have nt tiles each and span flat tiles [lo, hi): a pair meets at most
-// nt / ws + 2 static ranges, and at most as many pool pieces as the
-// sequence's range meets (and no more than its own tiles).
-__device__ __forceinline__ int seq_cand_bound(int nt, int lo, int hi, const StepPlan& pl) {
-  if (nt <= 0) return 0;
-  int ub = 0;
-  if (lo < pl.ts) ub += min(nt, nt / pl.ws + 2);
-  if (hi > pl.ts) {
-    const int first = piece_of(max(lo, pl.ts), pl), last = piece_of(hi - 1, pl);
-    ub += min(nt, last - first + 1);
-  }
-  return ub;
-}
-
-// Tighter bound of the partial results of any pair of such a sequence (used
-// by the merge kernel to size its column groups): a run of nt tiles also
-// meets at most nt / piece + 2 pool pieces.
+// have nt tiles each and span flat tiles [lo, hi) (the merge kernel sizes
+// its column groups by it): a run of nt tiles meets at most nt / ws + 2
+// static ranges and nt / piece + 2 pool pieces (and no more than its own
+// tiles, nor more pieces than the sequence's range meets).
 __device__ __forceinline__ int pair_cand_bound(int nt, int lo, int hi, const StepPlan& pl) {
   if (nt <= 0) return 0;
   int ub = 0;
