@@ -78,7 +78,8 @@ enum {
   PA_DEVERR_BLOCK_ID = 1,  /* a block table entry outside [0, num_blocks) */
   PA_DEVERR_SEQ_LEN = 2,   /* seq_len < 0 or > max_blocks_per_seq * block_size */
   PA_DEVERR_SLOT = 4,      /* a slot_mapping entry >= num_blocks * block_size */
-  PA_DEVERR_TIMEOUT = 8    /* a pipeline wait gave up (should never happen) */
+  PA_DEVERR_TIMEOUT = 8    /* a pipeline wait gave up (should never happen, except
+                              in pa_selftest_bounded_wait) */
 };
 
 #define PA_MAX_DIMS 6
@@ -292,6 +293,23 @@ pa_status pa_profile_events(void* ev_before, void* ev_after);
 /* Reads and clears the device error word of the current device (PA_DEVERR_*
  * bits); synchronises `stream`. */
 pa_status pa_check_device_error(int32_t* bits, pa_stream stream);
+
+/* Self-test of the kernels' bounded waits. Every wait in this library's
+ * kernels (for a copy to land, for a product to complete, for another CTA's
+ * flag) gives up after a limit of device wall time, sets PA_DEVERR_TIMEOUT
+ * and lets the kernel return, so that a wait that cannot be satisfied ends
+ * with an error the host reads instead of a hung context. This call launches
+ * one CTA on `stream` whose two waits can never be satisfied, through the
+ * same bounded-wait code: an mbarrier phase that nothing completes, then a
+ * device word that nothing writes. Each gives up after `limit_us`
+ * microseconds (1 .. 1,000,000), the kernel sets PA_DEVERR_TIMEOUT and exits
+ * normally. `elapsed_ns` (NULL, or two uint64_t in memory the device can
+ * write, 8-byte aligned) receives each wait's duration in nanoseconds of the
+ * device's global timer. Asynchronous like every launch: read the bit with
+ * pa_check_device_error(), which also clears it.
+ * Errors: PA_ERR_INVALID_ARG (limit out of range, elapsed_ns unaligned or not
+ * accessible from the current device), PA_ERR_CUDA (launch failure). */
+pa_status pa_selftest_bounded_wait(uint32_t limit_us, uint64_t* elapsed_ns, pa_stream stream);
 
 /* Number of kernels this library has launched in this process. */
 uint64_t pa_launch_count(void);

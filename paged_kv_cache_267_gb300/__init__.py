@@ -65,6 +65,7 @@ def lib() -> ctypes.CDLL:
             "pa_set_prefill_path": (st, [i32]),
             "pa_profile_events": (st, [vp, vp]),
             "pa_check_device_error": (st, [ctypes.POINTER(i32), vp]),
+            "pa_selftest_bounded_wait": (st, [ctypes.c_uint32, vp, vp]),
             "pa_launch_count": (ctypes.c_uint64, []),
             "pa_last_error": (ctypes.c_char_p, []),
             "pa_version": (i32, []),
@@ -239,6 +240,19 @@ def check_device_error(stream=None) -> int:
     bits = ctypes.c_int32(0)
     _check(lib().pa_check_device_error(ctypes.byref(bits), _stream(stream)))
     return bits.value
+
+
+def selftest_bounded_wait(limit_us: int, elapsed=None, stream=None) -> None:
+    """pa_selftest_bounded_wait: one CTA whose two waits cannot be satisfied;
+    each gives up after `limit_us` and sets PA_DEVERR_TIMEOUT (read it with
+    check_device_error). `elapsed`: None, or a contiguous int64 tensor of two
+    elements on the device that receives each wait's duration in ns."""
+    ptr = None
+    if elapsed is not None:
+        if elapsed.dtype != torch.int64 or elapsed.numel() != 2 or not elapsed.is_contiguous():
+            raise ValueError("elapsed must be a contiguous int64 tensor of 2 elements")
+        ptr = elapsed.data_ptr()
+    _check(lib().pa_selftest_bounded_wait(limit_us, ptr, _stream(stream)))
 
 
 def launch_count() -> int:

@@ -21,7 +21,7 @@ LIB_PATH = os.path.join(PKG, "libpa.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CU_SOURCES = ["decode_bf16.cu", "decode_f16.cu", "decode_fp8.cu", "decode_mq_bf16.cu",
               "decode_mq_f16.cu", "decode_mq_fp8.cu", "chunk_tc.cu", "merge_reshape.cu",
-              "decode_noalloc.cu"]
+              "decode_noalloc.cu", "selftest.cu"]
 CPP_SOURCES = ["pa_api.cpp", "pa_alloc.cpp"]
 
 

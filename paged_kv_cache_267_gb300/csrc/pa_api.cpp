@@ -145,21 +145,25 @@ double dprod(std::initializer_list<double> f) {
 // memory mapped into its address space at the same address (on GB300 the
 // kernels then read and write it over the CPU-GPU link). Anything else
 // (pageable host memory, another device's memory) is rejected before launch.
-pa_status check_accessible(const pa_tensor* t, const char* name) {
-  if (!t || numel(t) == 0 || !t->data) return PA_OK;
+pa_status check_accessible_ptr(const void* p, const char* name) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
   cudaPointerAttributes at;
-  e = cudaPointerGetAttributes(&at, t->data);
+  e = cudaPointerGetAttributes(&at, p);
   if (e != cudaSuccess) return cuda_fail(e, "cudaPointerGetAttributes");
   if ((at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged) && at.device == dev)
     return PA_OK;
-  if (at.type == cudaMemoryTypeHost && at.devicePointer == t->data) return PA_OK;
+  if (at.type == cudaMemoryTypeHost && at.devicePointer == p) return PA_OK;
   return fail(PA_ERR_INVALID_ARG,
               "%s: memory not accessible from the current device (use device memory or pinned, "
               "mapped host memory)",
               name);
+}
+
+pa_status check_accessible(const pa_tensor* t, const char* name) {
+  if (!t || numel(t) == 0 || !t->data) return PA_OK;
+  return check_accessible_ptr(t->data, name);
 }
 
 // ------------------------------------------------------------ device state
@@ -531,6 +535,36 @@ pa_status pa_check_device_error(int32_t* bits, pa_stream stream) {
     if (e == cudaSuccess) e = cudaStreamSynchronize(cs);
     if (e != cudaSuccess) return cuda_fail(e, "reading the device error word");
     *bits = v;
+    return ok();
+  });
+}
+
+namespace pa {
+// (csrc/selftest.cu) One CTA whose two waits (an mbarrier phase, a device flag) can never be
+// satisfied: each gives up after limit_ns, sets PA_DEVERR_TIMEOUT in *err and
+// stores its duration in elapsed[0 .. 2) (elapsed may be null).
+cudaError_t bounded_wait_selftest(int32_t* err, uint64_t limit_ns, uint64_t* elapsed,
+                                  cudaStream_t s);
+}  // namespace pa
+
+pa_status pa_selftest_bounded_wait(uint32_t limit_us, uint64_t* elapsed_ns, pa_stream stream) {
+  return pa::abi_guard([&]() -> pa_status {
+    if (limit_us < 1 || limit_us > 1000000)
+      return fail(PA_ERR_INVALID_ARG, "limit_us must be in [1, 1000000]");
+    pa_status s;
+    if (elapsed_ns && reinterpret_cast<uintptr_t>(elapsed_ns) % alignof(uint64_t))
+      return fail(PA_ERR_INVALID_ARG, "elapsed_ns must be 8-byte aligned");
+    if (elapsed_ns && (s = check_accessible_ptr(elapsed_ns, "elapsed_ns"))) return s;
+    DeviceState* st;
+    {
+      std::lock_guard<std::mutex> lk(g_mu);
+      s = device_state(&st, nullptr);
+      if (s) return s;
+    }
+    cudaError_t e = pa::bounded_wait_selftest(st->err_word, 1000ull * limit_us, elapsed_ns,
+                                              static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "self-test launch");
+    g_launches += 1;
     return ok();
   });
 }

@@ -415,3 +415,13 @@ def test_prefill_chunk_host_validation(pa_lib):
     assert "too large" in pa.last_error()
     n = ctypes.c_size_t(0)
     assert L.pa_prefill_chunk_workspace_size(4, 0, Hq, Hkv, D, ctypes.byref(n)) == -2
+
+
+def test_bounded_wait_selftest_validates_its_arguments(pa_lib):
+    # rejected on the host, before any device call (status PA_ERR_INVALID_ARG)
+    L = pa_lib.lib()
+    for limit_us in (0, 1_000_001, 2**32 - 1):
+        assert L.pa_selftest_bounded_wait(limit_us, None, None) == -1
+        assert "limit_us" in pa_lib.last_error()
+    assert L.pa_selftest_bounded_wait(1000, 0x10000004, None) == -1  # not 8-byte aligned
+    assert "aligned" in pa_lib.last_error()
