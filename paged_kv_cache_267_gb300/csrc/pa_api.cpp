@@ -21,6 +21,15 @@
 #include "pa.h"
 #include "pa_internal.h"
 
+namespace pa {
+// Defined in selftest.cu: one CTA whose two waits (an mbarrier phase, a
+// device flag) can never be satisfied; each gives up after limit_ns, sets
+// PA_DEVERR_TIMEOUT in *err and stores its duration in elapsed[0 .. 2)
+// (elapsed may be null).
+cudaError_t bounded_wait_selftest(int32_t* err, uint64_t limit_ns, uint64_t* elapsed,
+                                  cudaStream_t s);
+}  // namespace pa
+
 namespace {
 
 thread_local char g_last_error[512] = "";  // no host allocation on any error path
@@ -538,14 +547,6 @@ pa_status pa_check_device_error(int32_t* bits, pa_stream stream) {
     return ok();
   });
 }
-
-namespace pa {
-// (csrc/selftest.cu) One CTA whose two waits (an mbarrier phase, a device flag) can never be
-// satisfied: each gives up after limit_ns, sets PA_DEVERR_TIMEOUT in *err and
-// stores its duration in elapsed[0 .. 2) (elapsed may be null).
-cudaError_t bounded_wait_selftest(int32_t* err, uint64_t limit_ns, uint64_t* elapsed,
-                                  cudaStream_t s);
-}  // namespace pa
 
 pa_status pa_selftest_bounded_wait(uint32_t limit_us, uint64_t* elapsed_ns, pa_stream stream) {
   return pa::abi_guard([&]() -> pa_status {
