@@ -188,13 +188,13 @@ pa_status pa_decode(const pa_tensor* out, const pa_tensor* q, const pa_tensor* k
  * bytes of partial results, where W is the number of worker warps of the
  * decode kernel: 2 * (SM count) * 4, or * 8 for e4m3 caches with head_dim 128
  * (W = 1216 or 2432 on a 152-SM GB300), but no more than a step can fill:
- * about batch * num_kv_heads * (block_tables' width * block_size / 16 + 1) / 4,
+ * about batch * num_kv_heads * (block_tables' width * block_size / 16 + 1),
  * rounded up to whole CTAs (the window's span instead of the tables' when it
  * is shorter). The per-warp term dominates batches of moderate size: a batch
  * of 64 with 8 KV heads, G = 4 and head_dim 128 needs about 14.8 MB; a batch
  * of 256 of that shape with an e4m3 cache needs about 33.8 MB; four
  * sequences of at most 208 positions with 2 KV heads and head_dim 64 need
- * about 0.2 MB. A step beyond 32 MiB is rejected with PA_ERR_WORKSPACE and a
+ * about 0.6 MB. A step beyond 32 MiB is rejected with PA_ERR_WORKSPACE and a
  * message giving the bytes needed.
  *
  * The first call on a device looks up that device's address of the array
@@ -274,8 +274,9 @@ pa_status pa_set_workspace(void* ptr, size_t bytes);
 /* Test and tuning knobs, process-wide for later pa_decode calls; 0 keeps the
  * default of each:
  *   max_ctas       caps the persistent decode grid (default: 2 CTAs per SM);
- *   min_tiles      least number of 16-token tiles per warp's static range
- *                  (default 4);
+ *   min_tiles      least number of 16-token tiles per warp's static range,
+ *                  which also caps the grid at the warps a step can fill
+ *                  (default 1);
  *   pool_permille  share of the tiles handed out dynamically in small pieces
  *                  after the static ranges (default 100; the pool only
  *                  covers the trailing run of sequences no longer than 4x the

@@ -42,7 +42,7 @@ std::atomic<int32_t> g_chunk_path{0};  // 0 auto, 1 persistent kernel, 2 tensor-
 thread_local void* g_prof_before = nullptr;
 thread_local void* g_prof_after = nullptr;
 
-constexpr int kDefaultMinTiles = 4;
+constexpr int kDefaultMinTiles = 1;  // small steps: as many warps as tiles (latency)
 constexpr int kDefaultPoolPermille = 100;  // share of tiles handed out dynamically
 constexpr int kDefaultPiece = 4;           // least tiles per pool piece
 constexpr int kPiecesPerWorker = 4;        // pool pieces per worker warp, at most
