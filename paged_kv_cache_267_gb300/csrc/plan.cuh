@@ -95,8 +95,7 @@ __device__ inline StepPlan plan_step(const PlanIn& p, int* s_len, int* s_pref) {
     int last = -1;
     for (int b = lane; b < p.B; b += 32)
       if (static_cast<long long>(s_pref[b + 1] - s_pref[b]) * p.B > thr) last = b;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) last = max(last, __shfl_xor_sync(FULL, last, o));
+    last = __reduce_max_sync(FULL, last);  // one redux.sync: shuffle chains are slow here
     if (lane == 0) s_last_long = last;
   }
   __syncthreads();
