@@ -450,8 +450,9 @@ __global__ void __launch_bounds__(WARPS * 32, 2)
             for (int i = 0; i < 4; ++i) amax = fmaxf(amax, fabsf(qv[ks][nt][i]));
           }
         }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(FULL, amax, o));
+        // warp max in one redux.sync: every lane's amax is a non-negative,
+        // non-NaN float (fmaxf from +0 drops NaN), whose bits order as unsigned
+        amax = __uint_as_float(__reduce_max_sync(FULL, __float_as_uint(amax)));
         int sh = 0;
         if (amax > 0.f && amax < INFINITY) {
           int e;
