@@ -154,6 +154,7 @@ __device__ __forceinline__ int acc_dim(int mt, int g, int hi) {
 constexpr unsigned kFlagStart = 1, kFlagEnd = 2, kFlagPool = 4;
 
 constexpr float kMaskedFloor = -1e30f;  // running-max start of chunked columns
+constexpr float kRefSlack = 8.f;        // log2 units a score may exceed the reference max
 
 template <int CT, int QT, int D, int NT, int WARPS, int STAGES, bool MQ>
 __global__ void __launch_bounds__(WARPS * 32, 2)
@@ -539,42 +540,64 @@ __global__ void __launch_bounds__(WARPS * 32, 2)
     // P.V runs on both, so P enters the product with ~16 bits instead of 8
     // (f16 P, used with f16 and FP8 caches, already has 11)
     uint32_t pr[NT][2];
+    // scores (log2 domain) of the lane's rows g, g + 8 in columns 2 t4, 2 t4 + 1
+    float sv[NT][4];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-      float s0, s1, s2, s3;
       if (MQ && cedge) {
         const int r0 = p0 + g, r1 = p0 + g + 8;
-        s0 = (r0 >= qlo[nt][0] && r0 <= qhi[nt][0]) ? sacc[nt][0] * sc : -INFINITY;
-        s1 = (r0 >= qlo[nt][1] && r0 <= qhi[nt][1]) ? sacc[nt][1] * sc : -INFINITY;
-        s2 = (r1 >= qlo[nt][0] && r1 <= qhi[nt][0]) ? sacc[nt][2] * sc : -INFINITY;
-        s3 = (r1 >= qlo[nt][1] && r1 <= qhi[nt][1]) ? sacc[nt][3] * sc : -INFINITY;
+        sv[nt][0] = (r0 >= qlo[nt][0] && r0 <= qhi[nt][0]) ? sacc[nt][0] * sc : -INFINITY;
+        sv[nt][1] = (r0 >= qlo[nt][1] && r0 <= qhi[nt][1]) ? sacc[nt][1] * sc : -INFINITY;
+        sv[nt][2] = (r1 >= qlo[nt][0] && r1 <= qhi[nt][0]) ? sacc[nt][2] * sc : -INFINITY;
+        sv[nt][3] = (r1 >= qlo[nt][1] && r1 <= qhi[nt][1]) ? sacc[nt][3] * sc : -INFINITY;
       } else {
-        s0 = vlo ? sacc[nt][0] * sc : -INFINITY;
-        s1 = vlo ? sacc[nt][1] * sc : -INFINITY;
-        s2 = vhi ? sacc[nt][2] * sc : -INFINITY;
-        s3 = vhi ? sacc[nt][3] * sc : -INFINITY;
+        sv[nt][0] = vlo ? sacc[nt][0] * sc : -INFINITY;
+        sv[nt][1] = vlo ? sacc[nt][1] * sc : -INFINITY;
+        sv[nt][2] = vhi ? sacc[nt][2] * sc : -INFINITY;
+        sv[nt][3] = vhi ? sacc[nt][3] * sc : -INFINITY;
       }
-      float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
+    }
+    // A column's reference max m_run moves only when one of its scores
+    // exceeds it by more than kRefSlack: the warp then takes the column maxima
+    // across its lanes and rescales l and O (always on a segment's first
+    // tile, whose reference starts at -inf or the floor). Every other tile
+    // uses the reference as it is, so P stays below 2^kRefSlack.
+    bool grow = false;
 #pragma unroll
-      for (int o = 4; o < 32; o <<= 1) {
-        mx0 = fmaxf(mx0, __shfl_xor_sync(FULL, mx0, o));
-        mx1 = fmaxf(mx1, __shfl_xor_sync(FULL, mx1, o));
-      }
-      const float mn0 = fmaxf(m_run[nt][0], mx0), mn1 = fmaxf(m_run[nt][1], mx1);
-      const float al0 = fast_exp2(m_run[nt][0] - mn0), al1 = fast_exp2(m_run[nt][1] - mn1);
-      m_run[nt][0] = mn0;
-      m_run[nt][1] = mn1;
-      const float p0v = fast_exp2(s0 - mn0), p1v = fast_exp2(s1 - mn1);
-      const float p2v = fast_exp2(s2 - mn0), p3v = fast_exp2(s3 - mn1);
-      l_run[nt][0] = l_run[nt][0] * al0 + (p0v + p2v);
-      l_run[nt][1] = l_run[nt][1] * al1 + (p1v + p3v);
+    for (int nt = 0; nt < NT; ++nt)
+      grow = grow || fmaxf(sv[nt][0], sv[nt][2]) > m_run[nt][0] + kRefSlack ||
+             fmaxf(sv[nt][1], sv[nt][3]) > m_run[nt][1] + kRefSlack;
+    if (__any_sync(FULL, grow)) {
 #pragma unroll
-      for (int mt = 0; mt < MT; ++mt) {
-        acc[mt][nt][0] *= al0;
-        acc[mt][nt][1] *= al1;
-        acc[mt][nt][2] *= al0;
-        acc[mt][nt][3] *= al1;
+      for (int nt = 0; nt < NT; ++nt) {
+        float mx0 = fmaxf(sv[nt][0], sv[nt][2]), mx1 = fmaxf(sv[nt][1], sv[nt][3]);
+#pragma unroll
+        for (int o = 4; o < 32; o <<= 1) {
+          mx0 = fmaxf(mx0, __shfl_xor_sync(FULL, mx0, o));
+          mx1 = fmaxf(mx1, __shfl_xor_sync(FULL, mx1, o));
+        }
+        const float mn0 = fmaxf(m_run[nt][0], mx0), mn1 = fmaxf(m_run[nt][1], mx1);
+        const float al0 = fast_exp2(m_run[nt][0] - mn0), al1 = fast_exp2(m_run[nt][1] - mn1);
+        m_run[nt][0] = mn0;
+        m_run[nt][1] = mn1;
+        l_run[nt][0] *= al0;
+        l_run[nt][1] *= al1;
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+          acc[mt][nt][0] *= al0;
+          acc[mt][nt][1] *= al1;
+          acc[mt][nt][2] *= al0;
+          acc[mt][nt][3] *= al1;
+        }
       }
+    }
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const float mn0 = m_run[nt][0], mn1 = m_run[nt][1];
+      const float p0v = fast_exp2(sv[nt][0] - mn0), p1v = fast_exp2(sv[nt][1] - mn1);
+      const float p2v = fast_exp2(sv[nt][2] - mn0), p3v = fast_exp2(sv[nt][3] - mn1);
+      l_run[nt][0] += p0v + p2v;
+      l_run[nt][1] += p1v + p3v;
       if constexpr (kBf16Mma) {
         const uint32_t h01 = pack2<true>(p0v, p1v), h23 = pack2<true>(p2v, p3v);
         pr[nt][0] = movmatrix_trans(pack2<true>(p0v - __uint_as_float(h01 << 16),
