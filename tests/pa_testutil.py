@@ -38,8 +38,13 @@ def host_copy(t: torch.Tensor) -> np.ndarray:
     return t.numpy().copy()
 
 
-def run_both(spec, device="cuda", pairs=None, run_oracle_decode=True, threads=None) -> Sides:
+def run_both(spec, device="cuda", pairs=None, run_oracle_decode=True, threads=None,
+             mutate=None) -> Sides:
+    """`mutate(w)`, if given, rewrites the generated inputs (test data
+    construction) before either side takes them."""
     w = generate(spec, device=device)
+    if mutate is not None:
+        mutate(w)
     s = w.spec
     fp8 = s.kv_fp8
     kv = "fp8" if fp8 else "auto"
