@@ -114,11 +114,15 @@ def assert_caches_equal(sides: Sides, what=""):
     assert np.array_equal(vc, sides.vc_ref), f"{what}: value cache differs from the oracle"
 
 
-def run_chunk(spec, device="cuda", triples=None, threads=None, use_chunk_entry=True) -> Sides:
+def run_chunk(spec, device="cuda", triples=None, threads=None, use_chunk_entry=True,
+              mutate=None) -> Sides:
     """The chunked step: the write path stores the B * T new K/V rows, then
     pa_prefill_chunk attends each sequence's T queries causally; the oracle
-    runs its reshape and causal multi-query decode on host copies."""
+    runs its reshape and causal multi-query decode on host copies. `mutate`
+    as in run_both."""
     w = generate(spec, device=device)
+    if mutate is not None:
+        mutate(w)
     s = w.spec
     fp8 = s.kv_fp8
     kv = "fp8" if fp8 else "auto"

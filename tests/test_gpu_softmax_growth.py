@@ -15,14 +15,17 @@ position p follows a pattern:
   sawtooth    0 and 7.5 in runs of 40 tokens (never moves after the first
               tile; P up to 2^7.5).
 Each runs with the grid cut to two CTAs (long segments per warp) and with
-the default grid, on 16-bit and e4m3 caches, against the fp64 oracle.
+the default grid, on 16-bit and e4m3 caches, against the fp64 oracle; and as
+chunks of 8 causal queries on both chunk kernels (the persistent one, whose
+columns start from a finite floor, and the tensor-memory one, whose rows keep
+a reference max of their own with the same rule).
 """
 import numpy as np
 import pytest
 import torch
 
 from conftest import have_gpu
-from pa_testutil import assert_close, out_f64, run_both
+from pa_testutil import CHUNK_REL_TOL, assert_close, out_f64, run_both, run_chunk
 from workloads import CONFIGS
 
 pytestmark = [pytest.mark.gpu, pytest.mark.skipif(not have_gpu(), reason="needs a GPU")]
@@ -93,4 +96,24 @@ def test_reference_max_under_crafted_score_growth(pattern, fp8, grid, pa_lib):
         pa_lib.set_decode_tuning()
     got = out_f64(sides.out)
     assert_close(got, sides.ref, what=f"{pattern} {grid} {'e4m3' if fp8 else 'bf16'}")
+    assert pa_lib.check_device_error() == 0
+
+
+@pytest.mark.parametrize("path", [1, 2], ids=["persistent", "tensor_memory"])
+@pytest.mark.parametrize("fp8", [False, True], ids=["bf16", "e4m3"])
+@pytest.mark.parametrize("pattern", list(PATTERNS))
+def test_chunk_reference_max_under_crafted_score_growth(pattern, fp8, path, pa_lib):
+    spec = CONFIGS["llama8b"].with_(name=f"chunk_growth_{pattern}", batch=3, num_queries=8,
+                                    seq_lens=(700, 2048, 333), kv_fp8=fp8,
+                                    seed=720 + list(PATTERNS).index(pattern))
+    pa_lib.set_prefill_path(path)
+    if path == 1:
+        pa_lib.set_decode_tuning(max_ctas=2)
+    try:
+        sides = run_chunk(spec, mutate=_mutator(pattern))
+    finally:
+        pa_lib.set_decode_tuning()
+        pa_lib.set_prefill_path(0)
+    assert_close(out_f64(sides.out), sides.ref, rel=CHUNK_REL_TOL,
+                 what=f"chunk {pattern} path {path} {'e4m3' if fp8 else 'bf16'}")
     assert pa_lib.check_device_error() == 0
