@@ -27,6 +27,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import re
 import json
 import os
 import statistics
@@ -168,11 +169,15 @@ def measured_peak() -> tuple[float, str]:
 
 def kernel_source_hash() -> str:
     """Hash of the sources that make up the decode kernel (its code, the
-    PTX wrappers, the step plan and the argument structs)."""
+    PTX wrappers, the step plan and the argument structs), comments and
+    whitespace left out so that a change of wording keeps the profiles."""
     h = hashlib.sha256()
     for f in ("decode.cuh", "ptx.cuh", "plan.cuh", "pa_internal.h"):
-        with open(os.path.join(ROOT, "paged_kv_cache_267_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "paged_kv_cache_267_gb300", "csrc", f), encoding="utf-8") as fh:
+            src = fh.read()
+        src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)  # block comments
+        src = re.sub(r"//[^\n]*", " ", src)                # line comments
+        h.update(" ".join(src.split()).encode())
     return h.hexdigest()[:16]
 
 

@@ -29,7 +29,9 @@
 //
 // Math (per tile, per warp), on the tensor cores with fp32 accumulation:
 //   S^T[16 tok x 8 heads] = K[16 x D] . Q^T[D x 8]     (mma m16n8k16, M = tokens)
-//   online softmax on S in the log2 domain (scale * log2 e folded in)
+//   online softmax on S in the log2 domain (scale * log2 e folded in), with a
+//     lazy reference max per column: it moves (cross-lane max, rescale of
+//     l and O) only on tiles where a score exceeds it by more than 8
 //   O^T[D x 8 heads] += V^T[D x 16 tok] . P^T[16 x 8]  (P^T via movmatrix)
 // i.e. the block-wise scaled dot product, max/sum state and V-weighted sum of
 // "vLLM 0.5 深度解析" §2.3, done in one pass. With bf16 caches P enters P.V
