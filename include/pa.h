@@ -282,7 +282,8 @@ pa_status pa_set_workspace(void* ptr, size_t bytes);
  *                  covers the trailing run of sequences no longer than 4x the
  *                  mean length); negative turns the pool off, which makes
  *                  results bit-reproducible;
- *   piece_tiles    least tiles per pool piece (default 4). */
+ *   piece_tiles    least tiles per pool piece (default 4; 8 for single-query
+ *                  decode on e4m3 caches). */
 pa_status pa_set_decode_tuning(int32_t max_ctas, int32_t min_tiles, int32_t pool_permille,
                                int32_t piece_tiles);
 

@@ -45,6 +45,9 @@ thread_local void* g_prof_after = nullptr;
 constexpr int kDefaultMinTiles = 1;  // small steps: as many warps as tiles (latency)
 constexpr int kDefaultPoolPermille = 100;  // share of tiles handed out dynamically
 constexpr int kDefaultPiece = 4;           // least tiles per pool piece
+// e4m3 caches, one query: every piece is a segment whose start (q converted
+// and rescaled to f16) costs issue slots in that issue-bound variant
+constexpr int kDefaultPieceFp8 = 8;
 constexpr int kPiecesPerWorker = 4;        // pool pieces per worker warp, at most
 constexpr int kMaxCtasPerSm = 2;
 constexpr int kWarpsPerCta = 8;  // most worker warps of any decode variant
@@ -246,9 +249,9 @@ int tuned_pool_permille() {
   return v == 0 ? kDefaultPoolPermille : (v < 0 ? 0 : v);
 }
 
-int tuned_piece() {
+int tuned_piece(bool fp8_decode) {
   const int v = g_tune_piece.load();
-  return v > 0 ? v : kDefaultPiece;
+  return v > 0 ? v : (fp8_decode ? kDefaultPieceFp8 : kDefaultPiece);
 }
 
 // ------------------------------------------------------------ TMA descriptors
@@ -362,7 +365,7 @@ pa_status plan_decode(DeviceState* st, int ct, int qt, bool mq, int64_t B, int C
   const int mt = g_tune_min_tiles.load();
   p->min_tiles = mt > 0 ? mt : kDefaultMinTiles;
   p->pool_permille = tuned_pool_permille();
-  p->piece = tuned_piece();
+  p->piece = tuned_piece(ct == pa::kE4M3 && !mq);
   return PA_OK;
 }
 
