@@ -462,13 +462,25 @@ __global__ void __launch_bounds__(WARPS * 32, 2)
           frexpf(amax, &e);  // amax = m * 2^e, m in [0.5, 1)
           sh = (e - 1) - 14;
         }
+        if (sh >= -126 && sh <= 127) {
+          // 2^-sh from its exponent bits: one exact multiply per element
+          const float r = __int_as_float((127 - sh) << 23);
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
+          for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-          for (int ks = 0; ks < MT; ++ks) {
-            qf[ks][nt][0] = pack2<false>(ldexpf(qv[ks][nt][0], -sh), ldexpf(qv[ks][nt][1], -sh));
-            qf[ks][nt][1] = pack2<false>(ldexpf(qv[ks][nt][2], -sh), ldexpf(qv[ks][nt][3], -sh));
-          }
+            for (int ks = 0; ks < MT; ++ks) {
+              qf[ks][nt][0] = pack2<false>(qv[ks][nt][0] * r, qv[ks][nt][1] * r);
+              qf[ks][nt][1] = pack2<false>(qv[ks][nt][2] * r, qv[ks][nt][3] * r);
+            }
+        } else {  // |q| below 2^-112: 2^-sh is not a normal float
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int ks = 0; ks < MT; ++ks) {
+              qf[ks][nt][0] = pack2<false>(ldexpf(qv[ks][nt][0], -sh), ldexpf(qv[ks][nt][1], -sh));
+              qf[ks][nt][1] = pack2<false>(ldexpf(qv[ks][nt][2], -sh), ldexpf(qv[ks][nt][3], -sh));
+            }
+        }
         sc = ldexpf(a.score_scale, sh);
       }
 #pragma unroll
