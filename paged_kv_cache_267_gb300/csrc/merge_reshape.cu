@@ -134,6 +134,84 @@ __device__ __forceinline__ void store_head(const MergeArgs& a, size_t orow, cons
     store_out4<OT>(a.out, orow + v * 128 + 4 * lane, zero ? z : r.acc[v], inv);
 }
 
+// Half-warp form for D <= 128, used when a step has more output columns than
+// the grid has warps: lanes 16 j .. 16 j + 15 of a warp fold one column each,
+// lane i of a half holding head dims 64 v + 4 i .. + 3 for v < D / 64, with
+// four candidates' loads in flight per lane. Both halves run the same number
+// of rounds (the larger of their two columns'), and every lane takes part in
+// the shuffles of the round's maxima and sums before any lane skips a
+// candidate, so the shuffles never diverge.
+struct HalfAcc {
+  float M, den;
+  float4 acc[2];
+};
+
+template <typename SlotFn>
+__device__ __forceinline__ void merge_fold_half(const MergeArgs& a, SlotFn slot_of, int n, int h,
+                                                HalfAcc& r) {
+  constexpr int U = 4;
+  const int lane = threadIdx.x & 31, l16 = lane & 15, hb = lane & 16;
+  const int GD = a.CG * a.D, nv = a.D >> 6;
+  const size_t stride = static_cast<size_t>(part_stride(a.CG, a.D));
+  r.M = -INFINITY;
+  r.den = 0.f;
+  r.acc[0] = r.acc[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+  const uint64_t once = l2_evict_first();  // each partial is read once
+  int rounds = (n + U - 1) / U;
+  rounds = max(rounds, __shfl_xor_sync(0xffffffffu, rounds, 16));
+  for (int k = 0; k < rounds * U; k += U) {
+    float my_m = -INFINITY, my_l = 0.f;
+    if (l16 < U && k + l16 < n) {
+      const float* P = a.part + static_cast<size_t>(slot_of(k + l16)) * stride;
+      my_m = ld_f32_hint(P + GD + h, once);
+      my_l = ld_f32_hint(P + GD + a.CG + h, once);
+    }
+    float4 o[U][2];
+#pragma unroll
+    for (int j = 0; j < U; ++j) {
+      o[j][0] = o[j][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (k + j < n) {
+        const float* P = a.part + static_cast<size_t>(slot_of(k + j)) * stride + h * a.D;
+#pragma unroll
+        for (int v = 0; v < 2; ++v)
+          if (v < nv) o[j][v] = ld_f32x4_hint(P + 64 * v + 4 * l16, once);
+      }
+    }
+    float mv[U], lv[U];
+#pragma unroll
+    for (int j = 0; j < U; ++j) {
+      mv[j] = __shfl_sync(0xffffffffu, my_m, hb + j);
+      lv[j] = __shfl_sync(0xffffffffu, my_l, hb + j);
+    }
+#pragma unroll
+    for (int j = 0; j < U; ++j) {
+      if (k + j >= n) break;
+      const float Mn = fmaxf(r.M, mv[j]);
+      const float sc = fast_exp2(r.M - Mn), f = fast_exp2(mv[j] - Mn);
+      r.den = r.den * sc + f * lv[j];
+#pragma unroll
+      for (int v = 0; v < 2; ++v) {
+        r.acc[v].x = r.acc[v].x * sc + f * o[j][v].x;
+        r.acc[v].y = r.acc[v].y * sc + f * o[j][v].y;
+        r.acc[v].z = r.acc[v].z * sc + f * o[j][v].z;
+        r.acc[v].w = r.acc[v].w * sc + f * o[j][v].w;
+      }
+      r.M = Mn;
+    }
+  }
+}
+
+template <int OT>
+__device__ __forceinline__ void store_half(const MergeArgs& a, size_t orow, const HalfAcc& r,
+                                           bool zero) {
+  const int l16 = threadIdx.x & 15, nv = a.D >> 6;
+  const float inv = (zero || !(r.den > 0.f)) ? 0.f : 1.f / r.den;
+  const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+  for (int v = 0; v < 2; ++v)
+    if (v < nv) store_out4<OT>(a.out, orow + 64 * v + 4 * l16, zero ? z : r.acc[v], inv);
+}
+
 // Where output column `col` of sequence b lives, and its candidates.
 struct MergeCol {
   bool pad;     // a column padding the last group of a chunk
@@ -337,18 +415,41 @@ __global__ void __launch_bounds__(kMergeThreads, 3) merge_kernel(const MergeArgs
   // the last round come last in the order.
   const int rot = (blockIdx.x + gridDim.x - (n_wide % gridDim.x)) % gridDim.x;
   const int nwarps = gridDim.x * kMergeWarps;
-  for (int u = rot * kMergeWarps + warp; u < a.B * HC; u += nwarps) {
-    const int b = u / HC;
-    if (s_wide[b] & 3) continue;  // taken by the wide phase
-    const MergeCol c = merge_col(a, pl, s_pref, b, u - b * HC);
-    if (c.pad) continue;
-    auto slot = [&](int k) -> int {
-      return k < c.cd.na ? c.s + c.cd.w0 + k : S + a.NW + c.s + c.cd.i0 + (k - c.cd.na);
-    };
-    HeadAcc<VPL> r;
-    griddep_wait();  // the partials are complete and visible
-    merge_fold(a, slot, 0, c.ncand, c.h, r);
-    store_head<OT, VPL>(a, c.orow, r, c.ncand == 0);
+  if (VPL == 1 && a.B * HC > nwarps) {
+    // more columns than warps: half a warp per column (warp-uniform loop;
+    // a half without a column folds nothing but joins the shuffles)
+    for (int u2 = rot * kMergeWarps + warp; 2 * u2 < a.B * HC; u2 += nwarps) {
+      const int u = 2 * u2 + (lane >> 4);
+      bool act = u < a.B * HC;
+      const int b = act ? u / HC : 0;
+      act = act && (s_wide[b] & 3) == 0;  // wide columns are taken by the wide phase
+      MergeCol c = {};
+      if (act) {
+        c = merge_col(a, pl, s_pref, b, u - b * HC);
+        act = !c.pad;
+      }
+      auto slot = [&](int k) -> int {
+        return k < c.cd.na ? c.s + c.cd.w0 + k : S + a.NW + c.s + c.cd.i0 + (k - c.cd.na);
+      };
+      HalfAcc r;
+      griddep_wait();  // the partials are complete and visible
+      merge_fold_half(a, slot, act ? c.ncand : 0, act ? c.h : 0, r);
+      if (act) store_half<OT>(a, c.orow, r, c.ncand == 0);
+    }
+  } else {
+    for (int u = rot * kMergeWarps + warp; u < a.B * HC; u += nwarps) {
+      const int b = u / HC;
+      if (s_wide[b] & 3) continue;  // taken by the wide phase
+      const MergeCol c = merge_col(a, pl, s_pref, b, u - b * HC);
+      if (c.pad) continue;
+      auto slot = [&](int k) -> int {
+        return k < c.cd.na ? c.s + c.cd.w0 + k : S + a.NW + c.s + c.cd.i0 + (k - c.cd.na);
+      };
+      HeadAcc<VPL> r;
+      griddep_wait();  // the partials are complete and visible
+      merge_fold(a, slot, 0, c.ncand, c.h, r);
+      store_head<OT, VPL>(a, c.orow, r, c.ncand == 0);
+    }
   }
   // the counters are zero between calls
   if (tid == 0 && (blockIdx.x == 0 || last)) {
