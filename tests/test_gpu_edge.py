@@ -14,7 +14,7 @@ import oracle
 from conftest import have_gpu
 from pa_testutil import (assert_caches_equal, assert_close, host_copy, out_f64, run_both,
                          run_chunk)
-from workloads import generate
+from workloads import CONFIGS, generate
 from workloads.configs import Spec
 
 pytestmark = [pytest.mark.gpu, pytest.mark.skipif(not have_gpu(), reason="needs a GPU")]
@@ -523,4 +523,17 @@ def test_concurrent_streams_use_separate_workspaces(pa_lib):
             assert torch.equal(a.view(torch.int16), o.view(torch.int16))
     finally:
         pa_lib.set_decode_tuning()
+    assert pa_lib.check_device_error() == 0
+
+
+@pytest.mark.parametrize("D,dtype", [(64, "f16"), (64, "bf16"), (128, "f16"), (128, "bf16")])
+def test_merge_half_warp_columns(D, dtype, pa_lib):
+    # 128 sequences x 32 q heads = 4096 output columns, more than the merge
+    # grid's warps: each narrow column is folded by half a warp
+    rng = np.random.default_rng(4096 + D)
+    lens = tuple(int(x) for x in rng.integers(1, 400, size=128))
+    spec = CONFIGS["llama8b"].with_(name=f"half_{D}_{dtype}", batch=128, seq_lens=lens,
+                                    head_dim=D, dtype=dtype, seed=4100 + D)
+    sides = run_both(spec)
+    assert_close(out_f64(sides.out), sides.ref, what=f"half-warp merge D={D} {dtype}")
     assert pa_lib.check_device_error() == 0
