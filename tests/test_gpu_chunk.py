@@ -295,3 +295,17 @@ def test_maximum_chunk(path, pa_lib):
     got = out_f64(sides.out)
     assert np.isfinite(got).all()
     assert_close(got[idx], sides.ref[idx], what=f"T=4096 path {path}", rel=CHUNK_REL_TOL)
+
+
+@pytest.mark.parametrize("T,fp8", [(5, False), (3, True)], ids=["T5_bf16", "T3_fp8"])
+def test_chunk_half_warp_merge_with_padded_groups(T, fp8, pa_lib):
+    # 64 sequences x 8 KV heads x two column groups of 16 (T * G = 20 or 12
+    # columns, the rest padding) = 16384 or 8192 merge columns, more than the
+    # merge grid's warps: narrow columns take half a warp each, padding
+    # columns none
+    rng = np.random.default_rng(7000 + T)
+    lens = tuple(int(x) for x in rng.integers(T, 600, size=64))
+    sides = run_chunk(_spec(T, 32, 8, 128, 16, 0, "bf16", fp8, lens=lens, seed=7100 + T))
+    got = out_f64(sides.out)
+    assert_close(got, sides.ref, what=f"half-warp merge T={T}", rel=CHUNK_REL_TOL)
+    assert pa_lib.check_device_error() == 0
